@@ -1,0 +1,453 @@
+"""Benchmark of the RLA-2 / RAPT hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one causal RLA-2 prefill (RMSNorm -> RoPE -> ReLU features, chunked causal linear
+attention with the fp32 state, Sum-denominator epilogue, final state) over one batch of the
+headline workload: B=4 sequences x L=4096 tokens, H=16 heads, d=128, bf16 in/out, per-head
+RMSNorm gains ~ U(0.8, 1.2). Inputs are seeded synthetic N(0, 1) (no dataset exists for this
+kernel). Rank 0 prints one JSON line; `value` is prefill tokens/s over all ranks (weak scaling:
+every rank runs its own independent batch, no collective on the data path).
+
+The same line carries, measured in the same run: the decode step (256 sequences x 32 heads,
+d=128, state prefilled from 512 tokens, 64 steps), the packed varlen forward (T=65536, H=32,
+d=64) and the original-RLA L2 forward (B=2, L=16384, H=16, d=128) as sub-objects; the roofline
+of the dominant prefill kernel (algorithmic bytes / CUDA-event time vs the measured HBM copy
+bandwidth); an end-to-end number through the public API with host buffers; SM clocks sampled
+during the timed region; and the fp64 oracle timed on a bounded sample on the host cores.
+
+`--impl reference` times the fp64 CPU oracle (the only reference implementation: the pages
+publish no runnable code) on the same workload, one bounded sample per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "RAPT causal prefill tokens/s + decode tokens/s on 1 GB300; % of TC/HBM roofline"
+WORKLOAD = dict(name="rla2_causal_prefill", B=4, L=4096, H=16, d=128, dtype="bf16")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20  # > 129 MB of L2
+
+
+# ----------------------------------------------------------------------------- host helpers
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Seed of a rank's independent batch (weak scaling: rank r draws its own inputs)."""
+    return int(base) + 1000 * int(rank)
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank scalar over the process group (the identity without one)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def prefill_bytes(B, L, H, d, elem=2):
+    """Algorithmic HBM bytes of one prefill: read q, k, v and write out, once each."""
+    return 4 * B * L * H * d * elem
+
+
+def prefill_flops(B, L, H, d):
+    """Algorithmic flops per token-head: state update 2d^2, readout 2d^2, z and q.z 4d."""
+    return B * L * H * (4 * d * d + 4 * d)
+
+
+def decode_bytes(N, H, d, elem=2):
+    """Per step: S read + write (fp32), z read + write, q, k, v read and out write."""
+    return N * H * (2 * d * d * 4 + 2 * d * 4 + 4 * d * elem)
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the GPU is under load."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.rows = []
+        self.proc = None
+        self.err = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", str(period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError) as e:
+            self.err = str(e)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 8:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"error": self.err or "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        mhz = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(mhz)}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def oracle_sample(budget_s: float, seed: int):
+    """Times the fp64 oracle on whole (batch row, head) pairs of the headline workload until
+    ``budget_s`` seconds of CPU work have passed. Returns (tokens/s, pairs, seconds, cores)."""
+    import oracle as O
+    from relu_linear_attention_gb300 import synthetic as syn
+
+    w = syn.prefill_bf16(seed=seed)
+    q, k, v = (syn.bf16_bits_to_f64(x) for x in (w.q, w.k, w.v))
+    pairs = [(b, h) for b in range(w.B) for h in range(w.H)]
+    done = 0
+    t0 = time.perf_counter()
+    while done < len(pairs) and (time.perf_counter() - t0) < budget_s:
+        O.rla2_prefill(q, k, v, w.gamma_q, w.gamma_k, pairs=[pairs[done]])
+        done += 1
+    dt = time.perf_counter() - t0
+    # one pair is L tokens of one of H heads: tokens/s = pairs * L / H / seconds
+    return done * w.L / w.H / dt, done, dt, os.cpu_count()
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 CPU oracle as it stands, one (batch row, head) pair of the
+    headline workload per step, rank 0 only."""
+    if rank != 0:
+        return 0
+    import oracle as O
+    from relu_linear_attention_gb300 import synthetic as syn
+
+    w = syn.prefill_bf16(seed=rank_seed(1, 0))
+    q, k, v = (syn.bf16_bits_to_f64(x) for x in (w.q, w.k, w.v))
+    pairs = [(b, h) for b in range(w.B) for h in range(w.H)]
+    for i in range(args.warmup):
+        O.rla2_prefill(q, k, v, w.gamma_q, w.gamma_k, pairs=[pairs[i % len(pairs)]])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        O.rla2_prefill(q, k, v, w.gamma_q, w.gamma_k, pairs=[pairs[(args.warmup + i) % len(pairs)]])
+    dt = time.perf_counter() - t0
+    value = args.steps * w.L / w.H / dt
+    sample = "%d (batch row, head) pairs of B=4 L=4096 H=16 d=128, all rows, fp64 quadratic form" % args.steps
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "rla2_causal_prefill B=4 L=4096 H=16 d=128 bf16 inputs",
+                   "global_batch": 4, "seq_len": 4096, "parallelism": "host oracle, rank 0 only"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def _bf(t_np, device):
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(t_np).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def _events(n):
+    import torch
+
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def time_steps(fn, steps, warmup, flush, min_warm_s=0.0, counter=None):
+    """Runs ``warmup`` untimed steps (at least ``min_warm_s`` seconds), then ``steps`` steps each
+    bracketed by CUDA events on the current stream with an L2 flush before it (outside the
+    events). Returns the list of per-step milliseconds, and with ``counter`` (a function reading
+    the library's launch counter) also the number of library launches in the timed steps."""
+    import torch
+
+    t0 = time.perf_counter()
+    i = 0
+    while i < warmup or (time.perf_counter() - t0) < min_warm_s:
+        flush.zero_()
+        fn()
+        i += 1
+        if i % 16 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    ev0, ev1 = _events(steps), _events(steps)
+    c0 = counter() if counter else 0
+    for s in range(steps):
+        flush.zero_()
+        ev0[s].record()
+        fn()
+        ev1[s].record()
+    launches = (counter() - c0) if counter else None
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    return (ms, launches) if counter else ms
+
+
+def run_gpu(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+
+    from relu_linear_attention_gb300 import _build, _lib, binding as R, synthetic as syn
+
+    _build.ensure_built()
+    lib = _lib.load()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    # ---------------- headline: dense causal prefill
+    B, L, H, d = WORKLOAD["B"], WORKLOAD["L"], WORKLOAD["H"], WORKLOAD["d"]
+    w = syn.prefill_bf16(seed=rank_seed(1, rank))
+    q, k, v = (_bf(x, device) for x in (w.q, w.k, w.v))
+    gq, gk = (torch.from_numpy(x).to(device) for x in (w.gamma_q, w.gamma_k))
+    out = torch.empty_like(q)
+    Sf = torch.empty((B, H, d, d), dtype=torch.float32, device=device)
+    zf = torch.empty((B, H, d), dtype=torch.float32, device=device)
+    step = lambda: R.rapt_prefill_fwd(q, k, v, gq, gk, out=out, S_final=Sf, z_final=zf)
+
+    clocks = ClockSampler(local)
+    barrier(device)
+    torch.cuda.synchronize()
+    ms, timed_launches = time_steps(step, args.steps, args.warmup, flush, min_warm_s=1.0,
+                                    counter=lib.rapt_launch_counter)
+    barrier(device)
+    clk = clocks.stop()
+    total_ms = max_over_ranks(sum(ms), device)
+    ms_step = total_ms / args.steps
+    value = world * B * L / (ms_step * 1e-3)
+    mean_ms = statistics.fmean(ms)
+    alg_bytes = prefill_bytes(B, L, H, d)
+    achieved = alg_bytes / (mean_ms * 1e-3) / 1e9
+
+    # ---------------- end to end through the public API with pinned host buffers
+    qh, kh, vh = (x.cpu().pin_memory() for x in (q, k, v))
+    oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        R.rapt_prefill_fwd(qd, kd, vd, gq, gk, out=out)
+        oh.copy_(out, non_blocking=True)
+
+    e2e_ms = time_steps(e2e_step, args.steps, args.warmup, flush)
+    e2e_total = max_over_ranks(sum(e2e_ms), device)
+    e2e_value = world * B * L / (e2e_total / args.steps * 1e-3)
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = out.numel() * out.element_size()
+    del qh, kh, vh, oh, qd, kd, vd
+
+    # ---------------- decode: 256 x 32 heads, d=128, state from 512 prefill tokens, 64 steps
+    Nd, Pd, Hd, dd, nsteps = 256, 512, 32, 128, 64
+    pre = syn.decode_prefix(seed=rank_seed(3, rank))
+    pq, pk, pv = (_bf(x, device) for x in (pre.q, pre.k, pre.v))
+    g1 = torch.ones(dd, dtype=torch.float32, device=device)
+    _, S_init, z_init = R.rapt_prefill_fwd(pq, pk, pv, g1, g1, final_state=True)
+    del pq, pk, pv, pre
+    toks = [syn.decode_step_tokens(seed=rank_seed(3, rank), step=t) for t in range(nsteps)]
+    tq = torch.stack([_bf(t.q, device) for t in toks])
+    tk = torch.stack([_bf(t.k, device) for t in toks])
+    tv = torch.stack([_bf(t.v, device) for t in toks])
+    tp = torch.stack([torch.from_numpy(t.positions).to(device) for t in toks])
+    del toks
+    dout = torch.empty((Nd, Hd, dd), dtype=torch.bfloat16, device=device)
+    S, z = S_init.clone(), z_init.clone()
+    for t in range(max(3, args.warmup)):  # warm-up on a scratch copy of the state
+        R.rapt_decode_step(tq[t], tk[t], tv[t], tp[t], g1, g1, S, z, out=dout)
+    S.copy_(S_init)
+    z.copy_(z_init)
+    torch.cuda.synchronize()
+    barrier(device)
+    e0, e1 = _events(1)[0], _events(1)[0]
+    e0.record()
+    for t in range(nsteps):
+        R.rapt_decode_step(tq[t], tk[t], tv[t], tp[t], g1, g1, S, z, out=dout)
+    e1.record()
+    torch.cuda.synchronize()
+    dec_ms = max_over_ranks(e0.elapsed_time(e1), device) / nsteps
+    dec_bytes = decode_bytes(Nd, Hd, dd)
+    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    decode = {"value": world * Nd / (dec_ms * 1e-3), "unit": "tokens/s", "ms_per_step": dec_ms,
+              "workload": "decode N=256 H=32 d=128 bf16, fp32 state from 512 prefill tokens, "
+                          "64 consecutive steps at positions 512..575",
+              "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"],
+                           "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
+                           "bytes_per_step": dec_bytes}}
+    del S, z, S_init, z_init, tq, tk, tv, tp, dout
+
+    # ---------------- packed varlen (T=65536, H=32, d=64)
+    wv = syn.varlen_bf16(seed=rank_seed(2, rank))
+    vq, vk, vv = (_bf(x, device) for x in (wv.q, wv.k, wv.v))
+    cu = torch.from_numpy(wv.cu_seqlens).to(device)
+    g64 = torch.ones(64, dtype=torch.float32, device=device)
+    vo = torch.empty_like(vq)
+    msl = int(wv.lengths.max())
+    v_ms = time_steps(lambda: R.rapt_varlen_fwd(vq, vk, vv, cu, g64, g64, max_seqlen=msl, out=vo),
+                      max(3, args.steps // 2), args.warmup, flush)
+    v_mean = max_over_ranks(statistics.fmean(v_ms), device)
+    v_bytes = prefill_bytes(1, wv.T, 32, 64)
+    varlen = {"value": world * wv.T / (v_mean * 1e-3), "unit": "tokens/s", "ms_per_step": v_mean,
+              "workload": "varlen T=65536 H=32 d=64 bf16, %d documents U[128,8192]" % len(wv.lengths),
+              "roofline": {"bound": "hbm", "achieved": v_bytes / (v_mean * 1e-3) / 1e9,
+                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": v_bytes / (v_mean * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
+    del vq, vk, vv, vo, wv
+
+    # ---------------- original RLA, L2 denominator (B=2, L=16384, H=16, d=128)
+    wl = syn.l2_bf16(seed=rank_seed(4, rank))
+    lq, lk, lv = (_bf(x, device) for x in (wl.q, wl.k, wl.v))
+    lo = torch.empty_like(lq)
+    ws = torch.empty(lib.rla_l2_workspace_size(2, 16384, 16, 128, 1), dtype=torch.uint8, device=device)
+    l_ms = time_steps(lambda: R.rla_l2_fwd(lq, lk, lv, eps=1e-6, out=lo, workspace=ws),
+                      max(3, args.steps // 2), args.warmup, flush)
+    l_mean = max_over_ranks(statistics.fmean(l_ms), device)
+    l_bytes = prefill_bytes(2, 16384, 16, 128)
+    l_flops = 2 * 16384 * 16 * (8 * 128 * 128 + 2 * 128)
+    rla_l2 = {"value": world * 2 * 16384 / (l_mean * 1e-3), "unit": "tokens/s", "ms_per_step": l_mean,
+              "workload": "rla_l2 B=2 L=16384 H=16 d=128 bf16, non-causal",
+              "roofline": {"bound": "hbm", "achieved": l_bytes / (l_mean * 1e-3) / 1e9,
+                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": l_bytes / (l_mean * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                           "tflops": l_flops / (l_mean * 1e-3) / 1e12}}
+    del lq, lk, lv, lo, ws
+
+    # ---------------- CPU baseline: the fp64 oracle on a bounded sample (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and world == 1:
+        tps, pairs, secs, cores = oracle_sample(args.oracle_seconds, rank_seed(1, 0))
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": "%d of 64 (batch row, head) pairs of the headline workload, all 4096 rows "
+                         "each, fp64 quadratic form, %.1f s; numpy BLAS threads = host cores"
+                         % (pairs, secs)}
+
+    traffic = read_traffic("prefill_simt_kernel")
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "rla2_causal_prefill B=4 L=4096 H=16 d=128 bf16 (fp32 state)",
+                   "model": "RLA-2/RAPT attention layer (no projections)", "global_batch": B * world,
+                   "seq_len": L, "heads": H, "d_head": d,
+                   "parallelism": "dp%d (independent batch per GPU)" % world,
+                   "l2": "256 MiB write before every timed step, outside the CUDA events"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "peak_source": "%s hbm_gbs (copy bandwidth)" % peak_src,
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "tensor_tflops_algorithmic": prefill_flops(B, L, H, d) / (mean_ms * 1e-3) / 1e12,
+                     "tensor_peak_tflops": peaks["bf16_tflops"]},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(timed_launches),
+        "clocks": clk,
+        "decode": decode, "varlen": varlen, "rla_l2": rla_l2,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def read_traffic(kernel: str):
+    """Per-launch DRAM bytes of ``kernel`` from the committed ncu summary, if it was taken on
+    the kernel source as it is now (the summary records a hash of the source file)."""
+    import hashlib
+
+    table = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(table):
+        return None
+    for line in open(table):
+        parts = [p.strip() for p in line.strip().strip("|").split("|")]
+        if len(parts) >= 4 and parts[0] == kernel:
+            src = os.path.join(ROOT, "relu_linear_attention_gb300", "csrc", parts[1])
+            if not os.path.exists(src):
+                return None
+            h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+            return float(parts[3]) if h == parts[2] else None
+    return None
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--oracle-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_gpu(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,166 @@
+/*
+ * rapt.h — C ABI of the GB300 (sm_103a) RLA-2 / RAPT causal ReLU linear attention library.
+ *
+ * The method (neuralnet.cpp page "线性注意力家族：RLA / RAPT / RLA-2 与 GPU 落地",
+ * docs/development/08-rapt-algorithm.md):
+ *   features (§1, §3, §4.2):  q' = ReLU(RoPE(RMSNorm(q))),  k' = ReLU(RoPE(RMSNorm(k))),  v untouched;
+ *                              RMSNorm per (token, head) over d, no 1/sqrt(d) scale.
+ *   state    (§3):             S_t = S_{t-1} + k'_t (x) v_t  (d x d),  z_t = z_{t-1} + k'_t,
+ *                              reset at every document boundary (§2.2, §4.1).
+ *   output   (§3):             out_t = q'_t S_t / (q'_t . z_t + eps_den),  eps_den = 1e-4.
+ *   original RLA (§2.1):       out_t = sum_i s_ti v_i / (sqrt(sum_i s_ti^2) + 1e-6), non-causal,
+ *                              s_ti = ReLU(q_t) . ReLU(k_i), no norm, no RoPE.
+ *   decode (§4.2 forward_step): features of the new token, update the state first, then read out.
+ *
+ * RMSNorm:  x_hat = x * (mean_d(x^2) + eps_norm)^(-1/2) * gamma  (gamma fp32, statistics fp32;
+ *           ruDNN README §7).  RoPE: adjacent pairs (2j, 2j+1) rotated by p * base^(-2j/d),
+ *           (x0, x1) -> (x0 cos a - x1 sin a, x0 sin a + x1 cos a); p = 0-based position of the
+ *           token inside its document (plus pos_offset for dense prefill).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers are DEVICE pointers (caller-owned; the library never frees or keeps them), except
+ *     where a parameter says "host". Tensors are dense, contiguous, row-major in the layout named,
+ *     and 16-byte aligned.
+ *   - Layouts: dense "BSND" [B, L, H, d]; packed varlen "TND" [T, H, d]; decode [N, H, d].
+ *     States are fp32 and key-major: S[..., i, j] = sum_t k'_t[i] v_t[j]  ([.., H, d, d]); z [.., H, d].
+ *   - Output dtype = input dtype (bf16 results are rounded to nearest even); all arithmetic and
+ *     all accumulation are fp32.
+ *   - d must be one of 16, 32, 64, 128 (d_v = d_k = d).
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default stream), launches only on
+ *     that stream, allocates no device memory and never synchronises.
+ *   - Host-checkable errors are returned before anything is launched and nothing is written:
+ *     RAPT_ERR_INVALID_ARG (null required pointer, size <= 0 where > 0 is required, eps not
+ *     finite or <= 0, misalignment, `out` aliasing an input), RAPT_ERR_UNSUPPORTED (d or dtype not
+ *     supported), RAPT_ERR_WORKSPACE (workspace pointer null or smaller than the size query).
+ *     RAPT_ERR_CUDA reports a failed launch (cudaGetLastError after the launch); the kernels may
+ *     then not have run.
+ *   - Optional outputs are skipped when their pointer is NULL; optional inputs count as zero.
+ *   - Initial states are read only, never written (ruDNN README §8: the initial state is not
+ *     overwritten in place). S_final / z_final may not alias S0 / z0.
+ */
+#ifndef RAPT_H
+#define RAPT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the CUDA runtime's stream handle); NULL = the legacy default stream. */
+typedef struct CUstream_st* rapt_stream_t;
+
+typedef enum rapt_status {
+  RAPT_OK = 0,
+  RAPT_ERR_INVALID_ARG = 1,
+  RAPT_ERR_UNSUPPORTED = 2,
+  RAPT_ERR_WORKSPACE = 3,
+  RAPT_ERR_CUDA = 4
+} rapt_status;
+
+typedef enum rapt_dtype { RAPT_F32 = 0, RAPT_BF16 = 1 } rapt_dtype;
+
+/* Device error word bits written by rapt_varlen_fwd when `dev_status` is given. */
+#define RAPT_DEV_BAD_CU_SEQLENS 1u /* cu_seqlens not non-decreasing from 0 to T: bad documents skipped */
+
+/* Feature / denominator settings (08-rapt-algorithm.md §1, §3). */
+typedef struct rapt_params {
+  float eps_norm;            /* RMSNorm epsilon, inside the root; finite, > 0 (1e-6)             */
+  float rope_base;           /* RoPE base; finite, > 1 (10000)                                    */
+  float eps_den;             /* Sum-denominator epsilon; finite, > 0 (1e-4)                       */
+  int32_t gamma_head_stride; /* 0: gamma_q / gamma_k are [d], shared by all heads;
+                                d: they are [H, d] (a separate gain vector per head)             */
+} rapt_params;
+
+/* Defaults of the pages: eps_norm 1e-6, rope_base 1e4, eps_den 1e-4, shared gamma. */
+rapt_params rapt_default_params(void);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* rapt_status_string(rapt_status status);
+
+/* Version of this ABI (major * 10000 + minor * 100 + patch). */
+int32_t rapt_abi_version(void);
+
+/* Number of CUDA kernel launches this library has enqueued since it was loaded (all devices,
+ * all threads; a relaxed atomic counter). Instrumentation only: lets a caller count the kernels
+ * of a timed region by differencing two reads. */
+uint64_t rapt_launch_counter(void);
+
+/*
+ * Dense causal RLA-2 prefill (08-rapt-algorithm.md §3, §4.2 forward).
+ *   q, k, v   [B, L, H, d] of `dtype`; every batch row is one document.
+ *   gamma_q, gamma_k  fp32 [d] or [H, d] (see rapt_params.gamma_head_stride).
+ *   pos_offset        RoPE position of token 0 of every batch row (>= 0); token t sits at
+ *                     pos_offset + t (for continuing a sequence whose state is in S0/z0).
+ *   S0, z0    nullable fp32 [B, H, d, d], [B, H, d]: state carried in (NULL = zeros).
+ *   out       [B, L, H, d] of `dtype`; must not alias q, k or v.
+ *   S_final, z_final  nullable fp32 [B, H, d, d], [B, H, d]: state after token L-1.
+ *   workspace / workspace_bytes: device scratch of at least rapt_prefill_workspace_size()
+ *                     bytes (may be NULL when that size is 0).
+ * Requirements: B, H >= 1, L >= 0 (L = 0 only writes S_final/z_final), B*L*H*d < 2^31.
+ */
+size_t rapt_prefill_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype);
+rapt_status rapt_prefill_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
+                             int32_t B, int32_t L, int32_t H, int32_t d,
+                             const float* gamma_q, const float* gamma_k, rapt_params params,
+                             int32_t pos_offset, const float* S0, const float* z0, void* out,
+                             float* S_final, float* z_final, void* workspace,
+                             size_t workspace_bytes, rapt_stream_t stream);
+
+/*
+ * Packed variable-length causal RLA-2 (08-rapt-algorithm.md §2.2, §4.1: the state restarts at
+ * every document; RoPE positions restart at 0 in every document).
+ *   q, k, v   [T, H, d] of `dtype`.
+ *   cu_seqlens  DEVICE int32 [N + 1]: 0 = cu[0] <= cu[1] <= ... <= cu[N] = T; document n is
+ *               tokens cu[n] .. cu[n+1]-1 (empty documents allowed).
+ *   max_seqlen  host int: an upper bound on every document length (used to size the launch);
+ *               a document longer than max_seqlen is an error reported through dev_status.
+ *   S0, z0    nullable fp32 [N, H, d, d], [N, H, d]: per-document carried-in state.
+ *   out       [T, H, d]; S_final, z_final nullable fp32 [N, H, d, d], [N, H, d] (an empty
+ *             document's final state is its initial state).
+ *   dev_status  nullable DEVICE uint32: bits RAPT_DEV_* are OR-ed in when cu_seqlens is
+ *             malformed (the offending documents are skipped, never read out of bounds). The
+ *             caller zeroes it; the library only sets bits.
+ * Requirements: T >= 0, N >= 1, H >= 1, T*H*d < 2^31.
+ */
+size_t rapt_varlen_workspace_size(int32_t T, int32_t N, int32_t H, int32_t d, rapt_dtype dtype);
+rapt_status rapt_varlen_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
+                            int32_t T, int32_t H, int32_t d, const int32_t* cu_seqlens,
+                            int32_t N, int32_t max_seqlen, const float* gamma_q,
+                            const float* gamma_k, rapt_params params, const float* S0,
+                            const float* z0, void* out, float* S_final, float* z_final,
+                            uint32_t* dev_status, void* workspace, size_t workspace_bytes,
+                            rapt_stream_t stream);
+
+/*
+ * One decode step for N sequences (08-rapt-algorithm.md §4.2 forward_step): features of the new
+ * token at positions[n]; S += k' v^T and z += k' IN PLACE; out = q' S / (q' . z + eps_den)
+ * with the updated state (the new token sees itself, like the inclusive prefill).
+ *   q, k, v    [N, H, d] of `dtype`.
+ *   positions  DEVICE int32 [N], >= 0: RoPE position of each sequence's new token.
+ *   S, z       fp32 [N, H, d, d], [N, H, d], read and updated in place.
+ *   out        [N, H, d] of `dtype`.
+ */
+rapt_status rapt_decode_step(const void* q, const void* k, const void* v, rapt_dtype dtype,
+                             int32_t N, int32_t H, int32_t d, const int32_t* positions,
+                             const float* gamma_q, const float* gamma_k, rapt_params params,
+                             float* S, float* z, void* out, rapt_stream_t stream);
+
+/*
+ * Original RLA, non-causal, L2 denominator (08-rapt-algorithm.md §2.1):
+ *   q' = ReLU(q), k' = ReLU(k) (no norm, no RoPE); M_V = K'^T V, M_K = K'^T K' over all L tokens
+ *   of each (batch row, head); out_t = q'_t M_V / (sqrt(q'_t^T M_K q'_t) + eps).
+ *   q, k, v, out  [B, L, H, d] of `dtype`; eps finite, > 0 (1e-6).
+ *   workspace     at least rla_l2_workspace_size() bytes (fp32 partial moments).
+ */
+size_t rla_l2_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype);
+rapt_status rla_l2_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
+                       int32_t B, int32_t L, int32_t H, int32_t d, float eps, void* out,
+                       void* workspace, size_t workspace_bytes, rapt_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RAPT_H */

@@ -1,0 +1,184 @@
+"""Thin PyTorch binding of the C ABI in include/rapt.h (same function names).
+
+Argument marshalling only: shapes, dtypes, devices and contiguity of torch tensors are checked,
+outputs / workspaces are allocated with torch when the caller does not pass them, and the raw
+device pointers plus the current CUDA stream go to librapt.so. Every step of the computation runs
+in the library's CUDA kernels; there is no CPU path and no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+_DT = {torch.float32: _lib.RAPT_F32, torch.bfloat16: _lib.RAPT_BF16}
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _cuda_contig(name, t, dtype=None, shape=None):
+    _need(t.is_cuda, "%s must be a CUDA tensor" % name)
+    _need(t.is_contiguous(), "%s must be contiguous" % name)
+    if dtype is not None:
+        _need(t.dtype == dtype, "%s must be %s, got %s" % (name, dtype, t.dtype))
+    if shape is not None:
+        _need(tuple(t.shape) == tuple(shape), "%s must have shape %s, got %s"
+              % (name, tuple(shape), tuple(t.shape)))
+
+
+def make_params(eps_norm=1e-6, rope_base=1e4, eps_den=1e-4, gamma_head_stride=0):
+    p = _lib.rapt_params()
+    p.eps_norm, p.rope_base, p.eps_den = float(eps_norm), float(rope_base), float(eps_den)
+    p.gamma_head_stride = int(gamma_head_stride)
+    return p
+
+
+def _gammas(gamma_q, gamma_k, H, d):
+    for name, g in (("gamma_q", gamma_q), ("gamma_k", gamma_k)):
+        _cuda_contig(name, g, torch.float32)
+        _need(tuple(g.shape) in ((d,), (H, d)), "%s must be [d] or [H, d]" % name)
+    _need(gamma_q.dim() == gamma_k.dim(), "gamma_q and gamma_k must have the same shape")
+    return 0 if gamma_q.dim() == 1 else d
+
+
+def _state(name, t, shape):
+    if t is not None:
+        _cuda_contig(name, t, torch.float32, shape)
+    return t
+
+
+def rapt_prefill_fwd(q, k, v, gamma_q, gamma_k, *, eps_norm=1e-6, rope_base=1e4, eps_den=1e-4,
+                     pos_offset=0, S0=None, z0=None, out=None, final_state=False, S_final=None,
+                     z_final=None, workspace=None, stream=None):
+    """Dense causal RLA-2 prefill; q, k, v [B, L, H, d] (fp32 or bf16). Returns
+    (out, S_final, z_final); the final state is None unless requested or passed."""
+    _need(q.dim() == 4, "q must be [B, L, H, d]")
+    B, L, H, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _cuda_contig(name, t, q.dtype, q.shape)
+    _need(q.dtype in _DT, "dtype must be float32 or bfloat16")
+    stride = _gammas(gamma_q, gamma_k, H, d)
+    _state("S0", S0, (B, H, d, d))
+    _state("z0", z0, (B, H, d))
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, q.dtype, q.shape)
+    if final_state and S_final is None:
+        S_final = torch.empty((B, H, d, d), device=q.device, dtype=torch.float32)
+    if final_state and z_final is None:
+        z_final = torch.empty((B, H, d), device=q.device, dtype=torch.float32)
+    _state("S_final", S_final, (B, H, d, d))
+    _state("z_final", z_final, (B, H, d))
+    lib = _lib.load()
+    need = lib.rapt_prefill_workspace_size(B, L, H, d, _DT[q.dtype])
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.rapt_prefill_fwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], B, L, H, d,
+                              _ptr(gamma_q), _ptr(gamma_k),
+                              make_params(eps_norm, rope_base, eps_den, stride), int(pos_offset),
+                              _ptr(S0), _ptr(z0), _ptr(out), _ptr(S_final), _ptr(z_final),
+                              _ptr(workspace), ws_bytes, _stream(stream))
+    _lib.check("rapt_prefill_fwd", st)
+    return out, S_final, z_final
+
+
+def rapt_varlen_fwd(q, k, v, cu_seqlens, gamma_q, gamma_k, *, max_seqlen, eps_norm=1e-6,
+                    rope_base=1e4, eps_den=1e-4, S0=None, z0=None, out=None, final_state=False,
+                    S_final=None, z_final=None, dev_status=None, workspace=None, stream=None):
+    """Packed varlen causal RLA-2; q, k, v [T, H, d]; cu_seqlens int32 [N + 1] on the device.
+    Returns (out, S_final, z_final)."""
+    _need(q.dim() == 3, "q must be [T, H, d]")
+    T, H, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _cuda_contig(name, t, q.dtype, q.shape)
+    _need(q.dtype in _DT, "dtype must be float32 or bfloat16")
+    _cuda_contig("cu_seqlens", cu_seqlens, torch.int32)
+    _need(cu_seqlens.dim() == 1 and cu_seqlens.numel() >= 2, "cu_seqlens must be [N + 1]")
+    N = cu_seqlens.numel() - 1
+    stride = _gammas(gamma_q, gamma_k, H, d)
+    _state("S0", S0, (N, H, d, d))
+    _state("z0", z0, (N, H, d))
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, q.dtype, q.shape)
+    if final_state and S_final is None:
+        S_final = torch.empty((N, H, d, d), device=q.device, dtype=torch.float32)
+    if final_state and z_final is None:
+        z_final = torch.empty((N, H, d), device=q.device, dtype=torch.float32)
+    _state("S_final", S_final, (N, H, d, d))
+    _state("z_final", z_final, (N, H, d))
+    if dev_status is not None:
+        _cuda_contig("dev_status", dev_status, torch.int32)
+    lib = _lib.load()
+    need = lib.rapt_varlen_workspace_size(T, N, H, d, _DT[q.dtype])
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.rapt_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], T, H, d, _ptr(cu_seqlens),
+                             N, int(max_seqlen), _ptr(gamma_q), _ptr(gamma_k),
+                             make_params(eps_norm, rope_base, eps_den, stride), _ptr(S0), _ptr(z0),
+                             _ptr(out), _ptr(S_final), _ptr(z_final), _ptr(dev_status),
+                             _ptr(workspace), ws_bytes, _stream(stream))
+    _lib.check("rapt_varlen_fwd", st)
+    return out, S_final, z_final
+
+
+def rapt_decode_step(q, k, v, positions, gamma_q, gamma_k, S, z, *, eps_norm=1e-6, rope_base=1e4,
+                     eps_den=1e-4, out=None, stream=None):
+    """One decode step; q, k, v [N, H, d]; positions int32 [N]; S [N, H, d, d] and z [N, H, d]
+    fp32 are updated in place. Returns out [N, H, d]."""
+    _need(q.dim() == 3, "q must be [N, H, d]")
+    N, H, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _cuda_contig(name, t, q.dtype, q.shape)
+    _need(q.dtype in _DT, "dtype must be float32 or bfloat16")
+    _cuda_contig("positions", positions, torch.int32, (N,))
+    stride = _gammas(gamma_q, gamma_k, H, d)
+    _cuda_contig("S", S, torch.float32, (N, H, d, d))
+    _cuda_contig("z", z, torch.float32, (N, H, d))
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, q.dtype, q.shape)
+    st = _lib.load().rapt_decode_step(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], N, H, d,
+                                      _ptr(positions), _ptr(gamma_q), _ptr(gamma_k),
+                                      make_params(eps_norm, rope_base, eps_den, stride),
+                                      _ptr(S), _ptr(z), _ptr(out), _stream(stream))
+    _lib.check("rapt_decode_step", st)
+    return out
+
+
+def rla_l2_fwd(q, k, v, *, eps=1e-6, out=None, workspace=None, stream=None):
+    """Original RLA, non-causal, L2 denominator; q, k, v [B, L, H, d]. Returns out."""
+    _need(q.dim() == 4, "q must be [B, L, H, d]")
+    B, L, H, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _cuda_contig(name, t, q.dtype, q.shape)
+    _need(q.dtype in _DT, "dtype must be float32 or bfloat16")
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, q.dtype, q.shape)
+    lib = _lib.load()
+    need = lib.rla_l2_workspace_size(B, L, H, d, _DT[q.dtype])
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.rla_l2_fwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], B, L, H, d, float(eps), _ptr(out),
+                        _ptr(workspace), ws_bytes, _stream(stream))
+    _lib.check("rla_l2_fwd", st)
+    return out

@@ -1,0 +1,223 @@
+// C ABI of the RLA-2 / RAPT library (declared in include/rapt.h): argument validation, feature
+// constants, workspace sizing and kernel dispatch. Nothing here allocates device memory or
+// synchronises; every launch goes to the caller's stream.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/rapt.h"
+#include "kernels.h"
+
+namespace {
+
+using rapt::DType;
+
+constexpr double kTwoPi = 6.283185307179586476925286766559;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool opt_aligned16(const void* p) { return p == nullptr || aligned16(p); }
+bool finite_pos(float x) { return std::isfinite(x) && x > 0.f; }
+bool supported_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool known_dtype(rapt_dtype t) { return t == RAPT_F32 || t == RAPT_BF16; }
+DType to_dt(rapt_dtype t) { return t == RAPT_F32 ? DType::F32 : DType::BF16; }
+
+// Common checks of the feature parameters and gains. Returns RAPT_OK or the error.
+rapt_status check_features(const float* gq, const float* gk, const rapt_params& p, int d) {
+  if (gq == nullptr || gk == nullptr) return RAPT_ERR_INVALID_ARG;
+  if (!aligned16(gq) || !aligned16(gk)) return RAPT_ERR_INVALID_ARG;
+  if (!finite_pos(p.eps_norm) || !finite_pos(p.eps_den) || !finite_pos(p.rope_base))
+    return RAPT_ERR_INVALID_ARG;
+  if (p.gamma_head_stride != 0 && p.gamma_head_stride != d) return RAPT_ERR_INVALID_ARG;
+  return RAPT_OK;
+}
+
+// RoPE frequencies theta_j = base^(-2j/d) in turns per position, split hi + lo (double on host).
+rapt::FeatureArgs make_features(const rapt_params& p, int d) {
+  rapt::FeatureArgs fa{};
+  fa.eps_norm = p.eps_norm;
+  fa.gamma_stride = p.gamma_head_stride;
+  for (int j = 0; j < d / 2; ++j) {
+    const double f = std::pow(static_cast<double>(p.rope_base), -2.0 * j / d) / kTwoPi;
+    const float hi = static_cast<float>(f);
+    fa.rope_hi[j] = hi;
+    fa.rope_lo[j] = static_cast<float>(f - static_cast<double>(hi));
+  }
+  return fa;
+}
+
+rapt_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RAPT_OK : RAPT_ERR_CUDA; }
+
+bool fits_i32(long long x) { return x >= 0 && x < (1LL << 31); }
+
+std::atomic<unsigned long long> g_launches{0};
+
+}  // namespace
+
+namespace rapt {
+void note_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+unsigned long long launch_count() { return g_launches.load(std::memory_order_relaxed); }
+}  // namespace rapt
+
+extern "C" {
+
+rapt_params rapt_default_params(void) {
+  rapt_params p;
+  p.eps_norm = 1e-6f;
+  p.rope_base = 10000.f;
+  p.eps_den = 1e-4f;
+  p.gamma_head_stride = 0;
+  return p;
+}
+
+const char* rapt_status_string(rapt_status s) {
+  switch (s) {
+    case RAPT_OK: return "RAPT_OK";
+    case RAPT_ERR_INVALID_ARG: return "RAPT_ERR_INVALID_ARG: invalid argument";
+    case RAPT_ERR_UNSUPPORTED: return "RAPT_ERR_UNSUPPORTED: unsupported head size or dtype";
+    case RAPT_ERR_WORKSPACE: return "RAPT_ERR_WORKSPACE: workspace missing or too small";
+    case RAPT_ERR_CUDA: return "RAPT_ERR_CUDA: CUDA launch failed";
+    default: return "RAPT: unknown status";
+  }
+}
+
+int32_t rapt_abi_version(void) { return 10000; }
+
+uint64_t rapt_launch_counter(void) { return rapt::launch_count(); }
+
+size_t rapt_prefill_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype) {
+  (void)B; (void)L; (void)H; (void)d; (void)dtype;
+  return 0;
+}
+
+rapt_status rapt_prefill_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
+                             int32_t B, int32_t L, int32_t H, int32_t d,
+                             const float* gamma_q, const float* gamma_k, rapt_params params,
+                             int32_t pos_offset, const float* S0, const float* z0, void* out,
+                             float* S_final, float* z_final, void* workspace,
+                             size_t workspace_bytes, rapt_stream_t stream) {
+  if (!known_dtype(dtype) || !supported_d(d)) return RAPT_ERR_UNSUPPORTED;
+  if (B < 1 || H < 1 || L < 0 || pos_offset < 0) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(B) * L * H * d)) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(pos_offset) + L)) return RAPT_ERR_INVALID_ARG;
+  if (L > 0 && (q == nullptr || k == nullptr || v == nullptr || out == nullptr))
+    return RAPT_ERR_INVALID_ARG;
+  if (!opt_aligned16(q) || !opt_aligned16(k) || !opt_aligned16(v) || !opt_aligned16(out) ||
+      !opt_aligned16(S0) || !opt_aligned16(z0) || !opt_aligned16(S_final) || !opt_aligned16(z_final))
+    return RAPT_ERR_INVALID_ARG;
+  if (out != nullptr && (out == q || out == k || out == v)) return RAPT_ERR_INVALID_ARG;
+  if ((S_final != nullptr && S_final == S0) || (z_final != nullptr && z_final == z0))
+    return RAPT_ERR_INVALID_ARG;
+  rapt_status st = check_features(gamma_q, gamma_k, params, d);
+  if (st != RAPT_OK) return st;
+  if (workspace_bytes < rapt_prefill_workspace_size(B, L, H, d, dtype)) return RAPT_ERR_WORKSPACE;
+  (void)workspace;
+
+  rapt::PrefillArgs a{};
+  a.q = q; a.k = k; a.v = v; a.out = out;
+  a.gamma_q = gamma_q; a.gamma_k = gamma_k;
+  a.S0 = S0; a.z0 = z0; a.S_final = S_final; a.z_final = z_final;
+  a.cu_seqlens = nullptr; a.dev_status = nullptr;
+  a.n_docs = B; a.doc_len = L; a.total_rows = B * L; a.max_seqlen = L;
+  a.H = H; a.pos_offset = pos_offset; a.eps_den = params.eps_den;
+  a.fa = make_features(params, d);
+  if (L == 0 && S_final == nullptr && z_final == nullptr) return RAPT_OK;
+  return from_cuda(rapt::launch_prefill_simt(to_dt(dtype), d, a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t rapt_varlen_workspace_size(int32_t T, int32_t N, int32_t H, int32_t d, rapt_dtype dtype) {
+  (void)T; (void)N; (void)H; (void)d; (void)dtype;
+  return 0;
+}
+
+rapt_status rapt_varlen_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
+                            int32_t T, int32_t H, int32_t d, const int32_t* cu_seqlens,
+                            int32_t N, int32_t max_seqlen, const float* gamma_q,
+                            const float* gamma_k, rapt_params params, const float* S0,
+                            const float* z0, void* out, float* S_final, float* z_final,
+                            uint32_t* dev_status, void* workspace, size_t workspace_bytes,
+                            rapt_stream_t stream) {
+  if (!known_dtype(dtype) || !supported_d(d)) return RAPT_ERR_UNSUPPORTED;
+  if (T < 0 || N < 1 || H < 1 || max_seqlen < 0) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(T) * H * d)) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(N) * H * 4)) return RAPT_ERR_INVALID_ARG;
+  if (cu_seqlens == nullptr || !aligned4(cu_seqlens)) return RAPT_ERR_INVALID_ARG;
+  if (dev_status != nullptr && !aligned4(dev_status)) return RAPT_ERR_INVALID_ARG;
+  if (T > 0 && (q == nullptr || k == nullptr || v == nullptr || out == nullptr))
+    return RAPT_ERR_INVALID_ARG;
+  if (!opt_aligned16(q) || !opt_aligned16(k) || !opt_aligned16(v) || !opt_aligned16(out) ||
+      !opt_aligned16(S0) || !opt_aligned16(z0) || !opt_aligned16(S_final) || !opt_aligned16(z_final))
+    return RAPT_ERR_INVALID_ARG;
+  if (out != nullptr && (out == q || out == k || out == v)) return RAPT_ERR_INVALID_ARG;
+  if ((S_final != nullptr && S_final == S0) || (z_final != nullptr && z_final == z0))
+    return RAPT_ERR_INVALID_ARG;
+  rapt_status st = check_features(gamma_q, gamma_k, params, d);
+  if (st != RAPT_OK) return st;
+  if (workspace_bytes < rapt_varlen_workspace_size(T, N, H, d, dtype)) return RAPT_ERR_WORKSPACE;
+  (void)workspace;
+
+  rapt::PrefillArgs a{};
+  a.q = q; a.k = k; a.v = v; a.out = out;
+  a.gamma_q = gamma_q; a.gamma_k = gamma_k;
+  a.S0 = S0; a.z0 = z0; a.S_final = S_final; a.z_final = z_final;
+  a.cu_seqlens = cu_seqlens; a.dev_status = dev_status;
+  a.n_docs = N; a.doc_len = 0; a.total_rows = T; a.max_seqlen = max_seqlen;
+  a.H = H; a.pos_offset = 0; a.eps_den = params.eps_den;
+  a.fa = make_features(params, d);
+  return from_cuda(rapt::launch_prefill_simt(to_dt(dtype), d, a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+rapt_status rapt_decode_step(const void* q, const void* k, const void* v, rapt_dtype dtype,
+                             int32_t N, int32_t H, int32_t d, const int32_t* positions,
+                             const float* gamma_q, const float* gamma_k, rapt_params params,
+                             float* S, float* z, void* out, rapt_stream_t stream) {
+  if (!known_dtype(dtype) || !supported_d(d)) return RAPT_ERR_UNSUPPORTED;
+  if (N < 1 || H < 1) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(N) * H * d * d)) return RAPT_ERR_INVALID_ARG;
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || positions == nullptr ||
+      S == nullptr || z == nullptr)
+    return RAPT_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(S) ||
+      !aligned16(z) || !aligned4(positions))
+    return RAPT_ERR_INVALID_ARG;
+  if (out == q || out == k || out == v) return RAPT_ERR_INVALID_ARG;
+  rapt_status st = check_features(gamma_q, gamma_k, params, d);
+  if (st != RAPT_OK) return st;
+
+  rapt::DecodeArgs a{};
+  a.q = q; a.k = k; a.v = v; a.out = out; a.positions = positions;
+  a.gamma_q = gamma_q; a.gamma_k = gamma_k; a.S = S; a.z = z;
+  a.N = N; a.H = H; a.eps_den = params.eps_den;
+  a.fa = make_features(params, d);
+  return from_cuda(rapt::launch_decode(to_dt(dtype), d, a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t rla_l2_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype) {
+  (void)dtype;
+  if (B < 1 || L < 0 || H < 1 || !supported_d(d)) return 0;
+  return rapt::l2_workspace_bytes(B, L, H, d);
+}
+
+rapt_status rla_l2_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
+                       int32_t B, int32_t L, int32_t H, int32_t d, float eps, void* out,
+                       void* workspace, size_t workspace_bytes, rapt_stream_t stream) {
+  if (!known_dtype(dtype) || !supported_d(d)) return RAPT_ERR_UNSUPPORTED;
+  if (B < 1 || H < 1 || L < 0) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(B) * L * H * d)) return RAPT_ERR_INVALID_ARG;
+  if (!finite_pos(eps)) return RAPT_ERR_INVALID_ARG;
+  if (L == 0) return RAPT_OK;
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return RAPT_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return RAPT_ERR_INVALID_ARG;
+  if (out == q || out == k || out == v) return RAPT_ERR_INVALID_ARG;
+  const size_t need = rla_l2_workspace_size(B, L, H, d, dtype);
+  if (workspace_bytes < need || (need > 0 && workspace == nullptr) || !aligned16(workspace))
+    return RAPT_ERR_WORKSPACE;
+
+  rapt::L2Args a{};
+  a.q = q; a.k = k; a.v = v; a.out = out;
+  a.ws = static_cast<float*>(workspace);
+  a.B = B; a.L = L; a.H = H; a.eps = eps;
+  return from_cuda(rapt::launch_rla_l2(to_dt(dtype), d, a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

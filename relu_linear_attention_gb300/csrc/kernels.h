@@ -1,0 +1,81 @@
+// Internal launch interface between the C ABI (api.cu) and the kernel translation units.
+// Host-side only; no torch types. Every launcher enqueues on `stream` and returns the
+// cudaError_t of the launch (cudaGetLastError right after it).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace rapt {
+
+enum class DType { F32 = 0, BF16 = 1 };
+
+// Counts every kernel launch the library enqueues (read by rapt_launch_counter()).
+void note_launches(unsigned n);
+unsigned long long launch_count();
+
+// One causal RLA-2 forward over a set of documents. Dense prefill is the special case of
+// `n_docs` = B documents of `doc_len` = L tokens each (cu_seqlens == nullptr); varlen reads the
+// document bounds from the device array cu_seqlens[n_docs + 1].
+struct PrefillArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  const float* gamma_q;
+  const float* gamma_k;
+  const float* S0;  // [n_docs, H, d, d] or null
+  const float* z0;  // [n_docs, H, d] or null
+  float* S_final;   // [n_docs, H, d, d] or null
+  float* z_final;   // [n_docs, H, d] or null
+  const int32_t* cu_seqlens;  // null for dense
+  uint32_t* dev_status;       // null or device error word
+  int n_docs;
+  int doc_len;     // dense: tokens per document
+  int total_rows;  // dense: B * L; varlen: T
+  int max_seqlen;  // varlen: bound on any document length (dense: L)
+  int H;
+  int pos_offset;  // dense only (0 for varlen)
+  float eps_den;
+  FeatureArgs fa;
+};
+
+cudaError_t launch_prefill_simt(DType dt, int d, const PrefillArgs& a, cudaStream_t stream);
+
+struct DecodeArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  const int32_t* positions;
+  const float* gamma_q;
+  const float* gamma_k;
+  float* S;
+  float* z;
+  int N;
+  int H;
+  float eps_den;
+  FeatureArgs fa;
+};
+
+cudaError_t launch_decode(DType dt, int d, const DecodeArgs& a, cudaStream_t stream);
+
+struct L2Args {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  float* ws;  // partial moments, then the reduced moments
+  int B;
+  int L;
+  int H;
+  float eps;
+};
+
+size_t l2_workspace_bytes(int B, int L, int H, int d);
+cudaError_t launch_rla_l2(DType dt, int d, const L2Args& a, cudaStream_t stream);
+
+}  // namespace rapt
