@@ -159,6 +159,33 @@ rapt_status rla_l2_fwd(const void* q, const void* k, const void* v, rapt_dtype d
                        int32_t B, int32_t L, int32_t H, int32_t d, float eps, void* out,
                        void* workspace, size_t workspace_bytes, rapt_stream_t stream);
 
+/*
+ * Allocation-free variant of rla_l2_fwd. The pages have no counterpart to this entry point: it
+ * exists for callers that cannot allocate device memory at all, such as a plugin inside an
+ * inference engine that owns every byte of device memory and hands the plugin only its input
+ * and output buffers, or a latency-critical loop that must not call cudaMalloc (which can
+ * synchronise the device) or grow a memory pool.
+ *
+ * Same arguments and result as rla_l2_fwd, minus the workspace: the fp32 partial moments live in
+ * a fixed device array of RAPT_L2_NOALLOC_SCRATCH_BYTES compiled into the library (every GPU that
+ * loads the library holds it until the process exits). The number of token splits is reduced
+ * until the moments fit, so results equal rla_l2_fwd's up to fp32 summation order.
+ *   - Returns RAPT_ERR_WORKSPACE, before launching anything, when even one split does not fit:
+ *     B * H * 2 * d * 2d * 4 bytes must not exceed RAPT_L2_NOALLOC_SCRATCH_BYTES (at d = 128,
+ *     B * H <= 64).
+ *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ *     with that device current); make that first call before any stream capture.
+ *   - Every call on a device uses the same array. Calls whose kernels overlap on the GPU (for
+ *     example on two streams without ordering between them) race on it and give wrong results;
+ *     serialise them. Nothing has to be cleared between calls: every element of the array that a
+ *     call reads was written earlier in the same call.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define RAPT_L2_NOALLOC_SCRATCH_BYTES (16u << 20)
+rapt_status rla_l2_fwd_noalloc(const void* q, const void* k, const void* v, rapt_dtype dtype,
+                               int32_t B, int32_t L, int32_t H, int32_t d, float eps, void* out,
+                               rapt_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

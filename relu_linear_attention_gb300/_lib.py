@@ -58,7 +58,12 @@ SIGNATURES = {
     "rla_l2_fwd": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32,
                              c_int32, c_int32, c_int32, c_int32, c_float, c_void_p,
                              c_void_p, c_size_t, c_void_p]),
+    "rla_l2_fwd_noalloc": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32,
+                                     c_int32, c_int32, c_int32, c_int32, c_float, c_void_p,
+                                     c_void_p]),
 }
+
+RAPT_L2_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _LIB = None
 

@@ -78,4 +78,11 @@ struct L2Args {
 size_t l2_workspace_bytes(int B, int L, int H, int d);
 cudaError_t launch_rla_l2(DType dt, int d, const L2Args& a, cudaStream_t stream);
 
+// Split count launch_rla_l2 would choose, and the launch with an explicit split count
+// (workspace of l2_workspace_bytes_for_splits() bytes at a.ws).
+int l2_default_splits(int B, int L, int H);
+size_t l2_workspace_bytes_for_splits(int B, int H, int d, int nsplit);
+cudaError_t launch_rla_l2_with_splits(DType dt, int d, const L2Args& a, int nsplit,
+                                      cudaStream_t stream);
+
 }  // namespace rapt

@@ -244,7 +244,63 @@ cudaError_t launch_d(int d, const L2Args& a, cudaStream_t stream) {
   }
 }
 
+// The same three launches with a caller-chosen number of token splits; the workspace at a.ws
+// holds (nsplit + 1) * B * H * d * 2d floats.
+template <typename T, int D>
+cudaError_t launch_t_splits(const L2Args& a, int nsplit, cudaStream_t stream) {
+  const int split_len = l2_split_len(a.L, nsplit);
+  const long n_bh = static_cast<long>(a.B) * a.H;
+  const int mat4 = D * 2 * D / 4;
+  if (n_bh == 0 || a.L == 0) return cudaSuccess;
+  l2_moments_kernel<T, D><<<dim3(nsplit, static_cast<unsigned>(n_bh)), kThreads, 0, stream>>>(a, nsplit, split_len);
+  note_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long red_total = n_bh * mat4;
+  long red_grid = (red_total + kThreads - 1) / kThreads;
+  if (red_grid > 152L * 16) red_grid = 152L * 16;
+  l2_reduce_kernel<<<static_cast<unsigned>(red_grid), kThreads, 0, stream>>>(a.ws, n_bh, nsplit, mat4);
+  note_launches(1);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  constexpr size_t smem = OutSmem<D>::bytes;
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(l2_out_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const long m_offset = n_bh * nsplit * static_cast<long>(D) * 2 * D;
+  const unsigned tiles = static_cast<unsigned>((a.L + kOutTile - 1) / kOutTile);
+  l2_out_kernel<T, D><<<dim3(tiles, static_cast<unsigned>(n_bh)), kThreads, smem, stream>>>(a, m_offset);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_d_splits(int d, const L2Args& a, int nsplit, cudaStream_t stream) {
+  switch (d) {
+    case 16: return launch_t_splits<T, 16>(a, nsplit, stream);
+    case 32: return launch_t_splits<T, 32>(a, nsplit, stream);
+    case 64: return launch_t_splits<T, 64>(a, nsplit, stream);
+    case 128: return launch_t_splits<T, 128>(a, nsplit, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace
+
+int l2_default_splits(int B, int L, int H) { return l2_nsplit(B, L, H); }
+
+size_t l2_workspace_bytes_for_splits(int B, int H, int d, int nsplit) {
+  return static_cast<size_t>(B) * H * (nsplit + 1) * d * 2 * d * sizeof(float);
+}
+
+cudaError_t launch_rla_l2_with_splits(DType dt, int d, const L2Args& a, int nsplit,
+                                      cudaStream_t stream) {
+  return dt == DType::F32 ? launch_d_splits<float>(d, a, nsplit, stream)
+                          : launch_d_splits<__nv_bfloat16>(d, a, nsplit, stream);
+}
 
 size_t l2_workspace_bytes(int B, int L, int H, int d) {
   const long n_bh = static_cast<long>(B) * H;
