@@ -383,7 +383,7 @@ def run_gpu(args, rank, world, local):
                          "each, fp64 quadratic form, %.1f s; numpy BLAS threads = host cores"
                          % (pairs, secs)}
 
-    traffic = read_traffic("prefill_simt_kernel")
+    traffic = read_traffic("prefill_tc_kernel")
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,

@@ -61,8 +61,9 @@ typedef enum rapt_status {
 
 typedef enum rapt_dtype { RAPT_F32 = 0, RAPT_BF16 = 1 } rapt_dtype;
 
-/* Device error word bits written by rapt_varlen_fwd when `dev_status` is given. */
+/* Device error word bits, OR-ed into a caller's `dev_status` word when one is given. */
 #define RAPT_DEV_BAD_CU_SEQLENS 1u /* cu_seqlens not non-decreasing from 0 to T: bad documents skipped */
+#define RAPT_DEV_TIMEOUT 2u        /* a tensor-core wait gave up (never expected): outputs invalid   */
 
 /* Feature / denominator settings (08-rapt-algorithm.md §1, §3). */
 typedef struct rapt_params {
@@ -96,17 +97,22 @@ uint64_t rapt_launch_counter(void);
  *   S0, z0    nullable fp32 [B, H, d, d], [B, H, d]: state carried in (NULL = zeros).
  *   out       [B, L, H, d] of `dtype`; must not alias q, k or v.
  *   S_final, z_final  nullable fp32 [B, H, d, d], [B, H, d]: state after token L-1.
+ *   dev_status  nullable DEVICE uint32: RAPT_DEV_* bits are OR-ed in on a device-side error
+ *               (the caller zeroes it; the library only sets bits).
  *   workspace / workspace_bytes: device scratch of at least rapt_prefill_workspace_size()
- *                     bytes (may be NULL when that size is 0).
+ *                     bytes, 16-byte aligned (may be NULL when that size is 0). Contents on
+ *                     entry do not matter.
  * Requirements: B, H >= 1, L >= 0 (L = 0 only writes S_final/z_final), B*L*H*d < 2^31.
+ * bf16 with d = 64 or 128 runs on the tensor cores (tcgen05); fp32, and bf16 with d = 16 or 32,
+ * run on CUDA cores.
  */
 size_t rapt_prefill_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype);
 rapt_status rapt_prefill_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
                              int32_t B, int32_t L, int32_t H, int32_t d,
                              const float* gamma_q, const float* gamma_k, rapt_params params,
                              int32_t pos_offset, const float* S0, const float* z0, void* out,
-                             float* S_final, float* z_final, void* workspace,
-                             size_t workspace_bytes, rapt_stream_t stream);
+                             float* S_final, float* z_final, uint32_t* dev_status,
+                             void* workspace, size_t workspace_bytes, rapt_stream_t stream);
 
 /*
  * Packed variable-length causal RLA-2 (08-rapt-algorithm.md §2.2, §4.1: the state restarts at
@@ -122,9 +128,11 @@ rapt_status rapt_prefill_fwd(const void* q, const void* k, const void* v, rapt_d
  *   dev_status  nullable DEVICE uint32: bits RAPT_DEV_* are OR-ed in when cu_seqlens is
  *             malformed (the offending documents are skipped, never read out of bounds). The
  *             caller zeroes it; the library only sets bits.
+ *   workspace   at least rapt_varlen_workspace_size(T, N, H, d, max_seqlen, dtype) bytes.
  * Requirements: T >= 0, N >= 1, H >= 1, T*H*d < 2^31.
  */
-size_t rapt_varlen_workspace_size(int32_t T, int32_t N, int32_t H, int32_t d, rapt_dtype dtype);
+size_t rapt_varlen_workspace_size(int32_t T, int32_t N, int32_t H, int32_t d, int32_t max_seqlen,
+                                  rapt_dtype dtype);
 rapt_status rapt_varlen_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
                             int32_t T, int32_t H, int32_t d, const int32_t* cu_seqlens,
                             int32_t N, int32_t max_seqlen, const float* gamma_q,

@@ -24,6 +24,7 @@ RAPT_ERR_CUDA = 4
 RAPT_F32 = 0
 RAPT_BF16 = 1
 RAPT_DEV_BAD_CU_SEQLENS = 1
+RAPT_DEV_TIMEOUT = 2
 
 
 class rapt_params(ctypes.Structure):
@@ -42,8 +43,8 @@ SIGNATURES = {
                                    c_int32, c_int32, c_int32, c_int32,
                                    c_void_p, c_void_p, rapt_params,
                                    c_int32, c_void_p, c_void_p, c_void_p,
-                                   c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
-    "rapt_varlen_workspace_size": (c_size_t, [c_int32] * 4 + [c_int32]),
+                                   c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "rapt_varlen_workspace_size": (c_size_t, [c_int32] * 5 + [c_int32]),
     "rapt_varlen_fwd": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32,
                                   c_int32, c_int32, c_int32, c_void_p,
                                   c_int32, c_int32, c_void_p,

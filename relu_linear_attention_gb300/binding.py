@@ -64,7 +64,7 @@ def _state(name, t, shape):
 
 def rapt_prefill_fwd(q, k, v, gamma_q, gamma_k, *, eps_norm=1e-6, rope_base=1e4, eps_den=1e-4,
                      pos_offset=0, S0=None, z0=None, out=None, final_state=False, S_final=None,
-                     z_final=None, workspace=None, stream=None):
+                     z_final=None, dev_status=None, workspace=None, stream=None):
     """Dense causal RLA-2 prefill; q, k, v [B, L, H, d] (fp32 or bf16). Returns
     (out, S_final, z_final); the final state is None unless requested or passed."""
     _need(q.dim() == 4, "q must be [B, L, H, d]")
@@ -84,6 +84,8 @@ def rapt_prefill_fwd(q, k, v, gamma_q, gamma_k, *, eps_norm=1e-6, rope_base=1e4,
         z_final = torch.empty((B, H, d), device=q.device, dtype=torch.float32)
     _state("S_final", S_final, (B, H, d, d))
     _state("z_final", z_final, (B, H, d))
+    if dev_status is not None:
+        _cuda_contig("dev_status", dev_status, torch.int32)
     lib = _lib.load()
     need = lib.rapt_prefill_workspace_size(B, L, H, d, _DT[q.dtype])
     if need > 0 and workspace is None:
@@ -93,7 +95,7 @@ def rapt_prefill_fwd(q, k, v, gamma_q, gamma_k, *, eps_norm=1e-6, rope_base=1e4,
                               _ptr(gamma_q), _ptr(gamma_k),
                               make_params(eps_norm, rope_base, eps_den, stride), int(pos_offset),
                               _ptr(S0), _ptr(z0), _ptr(out), _ptr(S_final), _ptr(z_final),
-                              _ptr(workspace), ws_bytes, _stream(stream))
+                              _ptr(dev_status), _ptr(workspace), ws_bytes, _stream(stream))
     _lib.check("rapt_prefill_fwd", st)
     return out, S_final, z_final
 
@@ -126,7 +128,7 @@ def rapt_varlen_fwd(q, k, v, cu_seqlens, gamma_q, gamma_k, *, max_seqlen, eps_no
     if dev_status is not None:
         _cuda_contig("dev_status", dev_status, torch.int32)
     lib = _lib.load()
-    need = lib.rapt_varlen_workspace_size(T, N, H, d, _DT[q.dtype])
+    need = lib.rapt_varlen_workspace_size(T, N, H, d, int(max_seqlen), _DT[q.dtype])
     if need > 0 and workspace is None:
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

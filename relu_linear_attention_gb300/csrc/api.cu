@@ -86,16 +86,17 @@ int32_t rapt_abi_version(void) { return 10000; }
 uint64_t rapt_launch_counter(void) { return rapt::launch_count(); }
 
 size_t rapt_prefill_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype) {
-  (void)B; (void)L; (void)H; (void)d; (void)dtype;
-  return 0;
+  if (!known_dtype(dtype) || !supported_d(d) || B < 1 || H < 1 || L < 0) return 0;
+  if (!rapt::tc_supported(to_dt(dtype), d)) return 0;
+  return rapt::tc_plan(B, H, L, static_cast<long>(B) * L, d).ws_bytes;
 }
 
 rapt_status rapt_prefill_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
                              int32_t B, int32_t L, int32_t H, int32_t d,
                              const float* gamma_q, const float* gamma_k, rapt_params params,
                              int32_t pos_offset, const float* S0, const float* z0, void* out,
-                             float* S_final, float* z_final, void* workspace,
-                             size_t workspace_bytes, rapt_stream_t stream) {
+                             float* S_final, float* z_final, uint32_t* dev_status,
+                             void* workspace, size_t workspace_bytes, rapt_stream_t stream) {
   if (!known_dtype(dtype) || !supported_d(d)) return RAPT_ERR_UNSUPPORTED;
   if (B < 1 || H < 1 || L < 0 || pos_offset < 0) return RAPT_ERR_INVALID_ARG;
   if (!fits_i32(static_cast<long long>(B) * L * H * d)) return RAPT_ERR_INVALID_ARG;
@@ -108,26 +109,34 @@ rapt_status rapt_prefill_fwd(const void* q, const void* k, const void* v, rapt_d
   if (out != nullptr && (out == q || out == k || out == v)) return RAPT_ERR_INVALID_ARG;
   if ((S_final != nullptr && S_final == S0) || (z_final != nullptr && z_final == z0))
     return RAPT_ERR_INVALID_ARG;
+  if (dev_status != nullptr && !aligned4(dev_status)) return RAPT_ERR_INVALID_ARG;
   rapt_status st = check_features(gamma_q, gamma_k, params, d);
   if (st != RAPT_OK) return st;
-  if (workspace_bytes < rapt_prefill_workspace_size(B, L, H, d, dtype)) return RAPT_ERR_WORKSPACE;
-  (void)workspace;
+  const size_t need = rapt_prefill_workspace_size(B, L, H, d, dtype);
+  if (workspace_bytes < need || (need > 0 && (workspace == nullptr || !aligned16(workspace))))
+    return RAPT_ERR_WORKSPACE;
 
   rapt::PrefillArgs a{};
   a.q = q; a.k = k; a.v = v; a.out = out;
   a.gamma_q = gamma_q; a.gamma_k = gamma_k;
   a.S0 = S0; a.z0 = z0; a.S_final = S_final; a.z_final = z_final;
-  a.cu_seqlens = nullptr; a.dev_status = nullptr;
+  a.cu_seqlens = nullptr; a.dev_status = dev_status;
   a.n_docs = B; a.doc_len = L; a.total_rows = B * L; a.max_seqlen = L;
   a.H = H; a.pos_offset = pos_offset; a.eps_den = params.eps_den;
   a.fa = make_features(params, d);
   if (L == 0 && S_final == nullptr && z_final == nullptr) return RAPT_OK;
-  return from_cuda(rapt::launch_prefill_simt(to_dt(dtype), d, a, reinterpret_cast<cudaStream_t>(stream)));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (rapt::tc_supported(to_dt(dtype), d))
+    return from_cuda(rapt::launch_prefill_tc(d, a, rapt::tc_plan(B, H, L, static_cast<long>(B) * L, d),
+                                             static_cast<float*>(workspace), s));
+  return from_cuda(rapt::launch_prefill_simt(to_dt(dtype), d, a, s));
 }
 
-size_t rapt_varlen_workspace_size(int32_t T, int32_t N, int32_t H, int32_t d, rapt_dtype dtype) {
-  (void)T; (void)N; (void)H; (void)d; (void)dtype;
-  return 0;
+size_t rapt_varlen_workspace_size(int32_t T, int32_t N, int32_t H, int32_t d, int32_t max_seqlen,
+                                  rapt_dtype dtype) {
+  if (!known_dtype(dtype) || !supported_d(d) || N < 1 || H < 1 || max_seqlen < 0 || T < 0) return 0;
+  if (!rapt::tc_supported(to_dt(dtype), d)) return 0;
+  return rapt::tc_plan(N, H, max_seqlen, T, d).ws_bytes;
 }
 
 rapt_status rapt_varlen_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
@@ -153,8 +162,9 @@ rapt_status rapt_varlen_fwd(const void* q, const void* k, const void* v, rapt_dt
     return RAPT_ERR_INVALID_ARG;
   rapt_status st = check_features(gamma_q, gamma_k, params, d);
   if (st != RAPT_OK) return st;
-  if (workspace_bytes < rapt_varlen_workspace_size(T, N, H, d, dtype)) return RAPT_ERR_WORKSPACE;
-  (void)workspace;
+  const size_t need = rapt_varlen_workspace_size(T, N, H, d, max_seqlen, dtype);
+  if (workspace_bytes < need || (need > 0 && (workspace == nullptr || !aligned16(workspace))))
+    return RAPT_ERR_WORKSPACE;
 
   rapt::PrefillArgs a{};
   a.q = q; a.k = k; a.v = v; a.out = out;
@@ -164,7 +174,11 @@ rapt_status rapt_varlen_fwd(const void* q, const void* k, const void* v, rapt_dt
   a.n_docs = N; a.doc_len = 0; a.total_rows = T; a.max_seqlen = max_seqlen;
   a.H = H; a.pos_offset = 0; a.eps_den = params.eps_den;
   a.fa = make_features(params, d);
-  return from_cuda(rapt::launch_prefill_simt(to_dt(dtype), d, a, reinterpret_cast<cudaStream_t>(stream)));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (rapt::tc_supported(to_dt(dtype), d))
+    return from_cuda(rapt::launch_prefill_tc(d, a, rapt::tc_plan(N, H, max_seqlen, T, d),
+                                             static_cast<float*>(workspace), s));
+  return from_cuda(rapt::launch_prefill_simt(to_dt(dtype), d, a, s));
 }
 
 rapt_status rapt_decode_step(const void* q, const void* k, const void* v, rapt_dtype dtype,

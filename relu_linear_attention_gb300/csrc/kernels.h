@@ -45,6 +45,18 @@ struct PrefillArgs {
 
 cudaError_t launch_prefill_simt(DType dt, int d, const PrefillArgs& a, cudaStream_t stream);
 
+// Tensor-core (tcgen05) chunked prefill for bf16 and d in {64, 128}. Documents are cut into
+// nseg_max segments of seg_len tokens; ws_bytes of workspace hold the segment state increments.
+struct TcPlan {
+  int nseg_max;
+  int seg_len;
+  size_t ws_bytes;
+};
+bool tc_supported(DType dt, int d);
+TcPlan tc_plan(int n_docs, int H, int max_seqlen, long total_tokens, int d);
+cudaError_t launch_prefill_tc(int d, const PrefillArgs& a, const TcPlan& plan, float* ws,
+                              cudaStream_t stream);
+
 struct DecodeArgs {
   const void* q;
   const void* k;

@@ -58,8 +58,10 @@ def test_defaults_and_strings(lib):
 
 
 def test_workspace_queries(lib):
-    assert lib.rapt_prefill_workspace_size(4, 4096, 16, 128, 1) >= 0
-    assert lib.rapt_varlen_workspace_size(65536, 16, 32, 64, 1) >= 0
+    assert lib.rapt_prefill_workspace_size(4, 4096, 16, 128, 1) > 0
+    assert lib.rapt_prefill_workspace_size(4, 4096, 16, 128, 0) == 0  # fp32: CUDA-core path
+    assert lib.rapt_varlen_workspace_size(65536, 17, 32, 64, 8192, 1) > 0
+    assert lib.rapt_varlen_workspace_size(65536, 17, 32, 16, 8192, 1) == 0
     ws = lib.rla_l2_workspace_size(2, 16384, 16, 128, 1)
     assert ws >= 2 * 16 * 128 * 256 * 4  # at least the reduced moments
     assert lib.rla_l2_workspace_size(2, 16384, 16, 48, 1) == 0
@@ -75,11 +77,11 @@ def _params(**kw):
 def _prefill(lib, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, dt=1, B=1, L=8, H=1, d=16, gq=FAKE, gk=FAKE,
              p=_params(), off=0, S0=None, z0=None, out=ctypes.c_void_p(0x7F0000002000),
-             Sf=None, zf=None, ws=None, wsb=0, s=None)
+             Sf=None, zf=None, st=None, ws=None, wsb=0, s=None)
     a.update(kw)
     return lib.rapt_prefill_fwd(a["q"], a["k"], a["v"], a["dt"], a["B"], a["L"], a["H"], a["d"],
                                 a["gq"], a["gk"], a["p"], a["off"], a["S0"], a["z0"], a["out"],
-                                a["Sf"], a["zf"], a["ws"], a["wsb"], a["s"])
+                                a["Sf"], a["zf"], a["st"], a["ws"], a["wsb"], a["s"])
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -100,6 +102,8 @@ def _prefill(lib, **kw):
     (dict(p=_params(gamma_head_stride=3)), _lib.RAPT_ERR_INVALID_ARG),
     (dict(B=1 << 20, L=1 << 20), _lib.RAPT_ERR_INVALID_ARG),
     (dict(S0=FAKE, Sf=FAKE), _lib.RAPT_ERR_INVALID_ARG),   # final state aliases initial
+    (dict(st=ctypes.c_void_p(0x7F0000001001)), _lib.RAPT_ERR_INVALID_ARG),
+    (dict(d=128, L=4096, B=4, H=16), _lib.RAPT_ERR_WORKSPACE),  # tensor-core path needs one
 ])
 def test_prefill_rejects_bad_arguments(lib, kw, code):
     assert _prefill(lib, **kw) == code
