@@ -63,7 +63,7 @@ typedef enum rapt_dtype { RAPT_F32 = 0, RAPT_BF16 = 1 } rapt_dtype;
 
 /* Device error word bits, OR-ed into a caller's `dev_status` word when one is given. */
 #define RAPT_DEV_BAD_CU_SEQLENS 1u /* cu_seqlens not non-decreasing from 0 to T: bad documents skipped */
-#define RAPT_DEV_TIMEOUT 2u        /* a tensor-core wait gave up (never expected): outputs invalid   */
+#define RAPT_DEV_INTERNAL 2u       /* a tensor-core wait gave up or smem was misaligned (never expected): outputs invalid */
 
 /* Feature / denominator settings (08-rapt-algorithm.md §1, §3). */
 typedef struct rapt_params {

@@ -24,7 +24,7 @@ RAPT_ERR_CUDA = 4
 RAPT_F32 = 0
 RAPT_BF16 = 1
 RAPT_DEV_BAD_CU_SEQLENS = 1
-RAPT_DEV_TIMEOUT = 2
+RAPT_DEV_INTERNAL = 2
 
 
 class rapt_params(ctypes.Structure):

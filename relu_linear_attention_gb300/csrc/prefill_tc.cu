@@ -2,98 +2,153 @@
 // bf16 inputs, d in {64, 128}; fp32 accumulation and fp32 state.
 //
 // The method (08-rapt-algorithm.md §3): q' = ReLU(RoPE(RMSNorm(q))), k' likewise,
-// S_t = S_{t-1} + k'_t v_t^T, z_t = z_{t-1} + k'_t, out_t = q'_t S_t / (q'_t . z_t + 1e-4),
-// with the state restarting at every document (§2.2, §4.1). It is evaluated chunk by chunk
-// (C = 128 tokens), the chunk-parallel form the page mentions (§1, §3), as four tile GEMMs per
-// chunk, all bf16 x bf16 -> fp32 on the tensor cores:
+// S_t = S_{t-1} + k'_t v_t^T, z_t = z_{t-1} + k'_t, out_t = q'_t S_t / (q'_t . z_t + 1e-4), with
+// the state restarting at every document (§2.2, §4.1). It is evaluated chunk by chunk (C = 128
+// tokens, the chunk-parallel form of §1 and §3) as four bf16 x bf16 -> fp32 tile GEMMs per chunk:
 //
-//   P  = Q'_c K'_c^T                       (128 x 128)    -> TMEM
-//   O  = Q'_c [S | z]~                     (128 x (d+16)) -> TMEM   carried-in state, bf16 copy
-//   [S | z] += K'_c^T [V_c | 1]            (d x (d+16))   -> TMEM   fp32 master state
-//   O += (P masked to tau <= t)~ [V_c | 1]                -> TMEM
-//   out = O[:, :d] / (O[:, d] + eps)
+//   O  = Q'_c S~_{c-1}        (128 x d)    -> TMEM   (inter-chunk part; ~ = bf16 copy)
+//   S += K'_c^T V_c           (d x d)      -> TMEM   (fp32 master state)
+//   P  = Q'_c K'_c^T          (128 x 128)  -> TMEM
+//   O += P~_c V_c             (P masked to tau <= t, rounded to bf16)
+//   out = O / (q'.z_{c-1} + rowsum(P~_c) + eps)
 //
-// A column of ones appended to V makes the tensor core produce z (column d of the state), the
-// inter-chunk denominator q'.z (column d of Q'[S|z]) and the intra-chunk row sums of P (column d
-// of P[V|1]) in the same MMAs, so the denominator needs no CUDA-core reduction. (~ marks the bf16
-// rounding of an MMA operand; the numerator and denominator use the same rounded weights.)
+// The denominator stays on the CUDA cores in fp32: z is a column sum of k' kept in shared memory,
+// q'.z is formed while the features are computed, and the row sums of the masked, rounded scores
+// (the same weights the numerator uses) while P is converted.
+//
+// Kernel B is warp-specialised (768 threads, six warpgroups):
+//   warps 0-15  (producers): features of chunk c+1 into one of two q' buffers while the tensor
+//                            core works on chunk c; k' (one buffer) is held in registers until the
+//                            tensor core has released the previous k'; z and q'.z. Features are
+//                            the bulk of the CUDA-core work, so they get most of the warps;
+//   warps 16-19 (consumers): one TMEM lane quarter (32 tile rows) each: S -> S~, P -> P~ and its
+//                            row sums, then the output epilogue from one of two O accumulators;
+//   warp 20     (issuer):    one thread issues the MMAs (an issue blocks while the tensor core is
+//                            busy, so it gets a warp of its own); warps 21-23 only hold registers.
+// v tiles need no transformation: the tensor-memory accelerator (TMA) copies them from HBM straight
+// into the swizzled operand layout, one chunk ahead. q and k go through registers (a short load
+// ring) because the features are computed on the way.
+// Hand-offs go through mbarriers: full[2] (producers -> issuer), vfull[2] (TMA -> issuer),
+// empty[2] (B(c) done -> buffer free), s_done / a_done / b_done (tensor core -> consumers),
+// conv_done (consumers -> issuer: S~ and P~ written, S and P read). The recurrence step of chunk c
+// (O = Q'S~, then S += K'^T V) is issued first and committed on its own (s_done), so turning S
+// into the next chunk's operand, the one serial dependency between chunks, starts early.
+// Every wait is bounded; a wait that gives up sets RAPT_DEV_INTERNAL in the caller's status word
+// and the CTA winds down.
 //
 // Sequence parallelism: a document is cut into segments of seg_len tokens. Kernel A computes the
-// state increment of every segment but the last (K'^T [V | 1] over the segment); kernel B runs one
-// CTA per (document, head, segment) that starts from S0 + the increments of the earlier segments
-// (summed in segment order: deterministic) and walks the segment's chunks. The last segment's CTA
-// writes the final state.
+// state increment (K'^T V and sum k') of every segment but the last; kernel B runs one CTA per
+// (document, head, segment) starting from S0 + the increments of the earlier segments (added in
+// segment order: deterministic). The last segment's CTA writes the final state.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
 #include "kernels.h"
 #include "tc_utils.cuh"
 
 namespace rapt {
 namespace {
 
-constexpr int kC = 128;        // chunk length = MMA M
-constexpr int kThreads = 256;  // 8 warps: two per TMEM lane quarter
-constexpr long long kWaitCycles = 2000000000LL;  // ~1 s: an MMA that has not finished by then never will
-constexpr uint32_t kDevTimeout = 2u;
+constexpr int kC = 128;          // chunk length = MMA M
+constexpr int kProd = 512;       // producer threads (16 warps)
+constexpr int kCons = 128;       // consumer threads of kernel B (4 warps)
+constexpr int kThreadsB = kProd + kCons + 128;  // + issuer warpgroup
+constexpr int kThreadsA = kProd + 128;          // kernel A: producers + issuer warpgroup
+constexpr long long kWaitCycles = 2000000000LL;  // ~1 s: a tensor-core step that is not done by then never will be
+constexpr uint32_t kDevInternal = 2u;
+constexpr uint32_t kBarProd = 1, kBarCons = 2;   // named barriers of the producer / consumer groups
+constexpr int kPad = 4;  // segment-increment rows are D + 4 floats (16-byte aligned; column D = z)
 
+// Register splits (setmaxnreg draws on the launch allocation: threads x launch registers).
+constexpr int kLaunchRegsB = 80, kRegsProdB = 88, kRegsConsB = 64, kRegsIssueB = 64;
+static_assert(kProd * kRegsProdB + kCons * kRegsConsB + 128 * kRegsIssueB <= kThreadsB * kLaunchRegsB,
+              "kernel B register split exceeds the launch allocation");
+constexpr int kLaunchRegsA = 96, kRegsProdA = 104, kRegsIssueA = 64;
+static_assert(kProd * kRegsProdA + 128 * kRegsIssueA <= kThreadsA * kLaunchRegsA,
+              "kernel A register split exceeds the launch allocation");
+
+// Producer mapping: a thread owns 8 consecutive elements (one 16-byte chunk, four RoPE pairs) of
+// one token row.
 template <int D>
-struct TcCfg {
-  static constexpr int NA = D + 16;       // [V | 1 0 ... 0] columns
-  static constexpr int KB = D / 64;       // 64-column blocks of q', k', S rows
-  static constexpr int VB = KB + 1;       // value blocks incl. the ones block
-  static constexpr int TPR = D / 16;      // prologue threads per token row (16 elements each)
-  static constexpr int RPP = kThreads / TPR;  // rows per prologue pass
-  static constexpr int NPASS = kC / RPP;
-  // shared-memory byte offsets from a 1024-byte aligned base
-  static constexpr uint32_t QS = 0;                                    // q' : KB x 16 KB
-  static constexpr uint32_t KS = QS + KB * 16384;                      // k' : KB x 16 KB (+ zero block if D = 64)
-  static constexpr uint32_t KS_END = KS + 2 * 16384;                   // M = 128 view of k'^T
-  static constexpr uint32_t PS = (D == 128) ? QS : KS_END;             // P~ : 2 x 16 KB (aliases q' at D = 128)
-  static constexpr uint32_t VS = (D == 128) ? KS_END : PS + 2 * 16384; // [V | 1] : VB x 16 KB
-  static constexpr uint32_t SS = VS + VB * 16384;                      // [S | z]~ : VB x (D rows x 128 B)
-  static constexpr uint32_t CTRL = SS + VB * D * 128;                  // barriers, TMEM base, flags
-  static constexpr uint32_t BYTES = CTRL + 64 + 1024;                  // + alignment slack
-  // TMEM columns
-  static constexpr uint32_t TP = 0, TO = 128, TS = 288;
-  static_assert(TS + NA <= 512, "TMEM budget");
+struct Prod {
+  static constexpr int TPR = D / 8;          // threads per row
+  static constexpr int RPP = kProd / TPR;    // rows per pass
+  static constexpr int NPASS = kC / RPP;     // passes per chunk
+  static constexpr int RING = 2 < NPASS ? 2 : NPASS;  // passes of q / k loads in flight
+  static constexpr int WARPS = kProd / 32;
+  static constexpr uint32_t TILE = (D / 64) * 16384;  // one 128-row bf16 tile of d columns
 };
 
-// Kernel A shared layout (k' and [V | 1] only).
+// Kernel B shared memory (byte offsets from a 1024-byte aligned base).
 template <int D>
-struct TcCfgA {
-  static constexpr int KB = D / 64, VB = KB + 1;
-  static constexpr uint32_t KS = 0;
-  static constexpr uint32_t VS = KS + 2 * 16384;
-  static constexpr uint32_t CTRL = VS + VB * 16384;
-  static constexpr uint32_t BYTES = CTRL + 64 + 1024;
+struct LayB {
+  static constexpr uint32_t TILE = Prod<D>::TILE;
+  static constexpr uint32_t Q0 = 0, Q1 = TILE;                 // q' (P~ reuses them at d = 128)
+  static constexpr uint32_t V0 = 2 * TILE, V1 = 3 * TILE;      // v
+  static constexpr uint32_t KS = 4 * TILE;                     // k' : 2 x 16 KB (d = 64: + zero block)
+  static constexpr uint32_t PS = KS + 32768;                   // P~ at d = 64
+  static constexpr uint32_t SS = PS + (D == 64 ? 32768 : 0);   // S~ : D/64 blocks of D rows x 128 B
+  static constexpr uint32_t ZP = SS + (D / 64) * D * 128;      // z partials [producer warps][D] fp32
+  static constexpr uint32_t ZS = ZP + Prod<D>::WARPS * D * 4;  // z [D] fp32
+  static constexpr uint32_t DI = ZS + D * 4;                   // q'.z [2][128] fp32
+  static constexpr uint32_t TAB = DI + 2 * kC * 4;             // feature tables (FeatTab)
+  // full0 full1 empty0 empty1 vfull0 vfull1 s_done a_done b_done conv_done
+  static constexpr uint32_t BAR = TAB + 8 * D * 4;
+  static constexpr uint32_t MISC = BAR + 10 * 8;               // TMEM base, abort, ready flags
+  static constexpr uint32_t BYTES = MISC + 16;
+  // TMEM columns: P, two O accumulators, S
+  static constexpr uint32_t TP = 0, TO0 = 128, TO1 = 128 + D, TS = 128 + 2 * D;
+  static_assert(TS + D <= 512, "TMEM budget");
+  static_assert(BYTES <= 232448, "shared memory budget");
+};
+
+// Kernel A shared memory.
+template <int D>
+struct LayA {
+  static constexpr uint32_t TILE = Prod<D>::TILE;
+  static constexpr uint32_t K0 = 0, K1 = 32768;                // k' sets, 2 x 16 KB each
+  static constexpr uint32_t V0 = 65536, V1 = V0 + TILE;
+  static constexpr uint32_t ZP = V1 + TILE;                    // z partials [producer warps][D]
+  static constexpr uint32_t TAB = ZP + Prod<D>::WARPS * D * 4; // feature tables (FeatTab)
+  static constexpr uint32_t BAR = TAB + 8 * D * 4;             // full0 full1 empty0 empty1 vfull0 vfull1
+  static constexpr uint32_t MISC = BAR + 6 * 8;
+  static constexpr uint32_t BYTES = MISC + 16;
 };
 
 struct TcArgs {
   PrefillArgs p;
-  float* ws;     // segment increments [n_docs][H][nseg_max][D][D + 1]
+  float* ws;     // segment increments [n_docs][H][nseg_max][D][D + 4] (column D = sum of k')
   int seg_len;   // tokens per segment (multiple of kC)
   int nseg_max;  // segments per document slot in the grid
 };
 
-__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const float2 g = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[m]));
-    f[2 * m] = g.x;
-    f[2 * m + 1] = g.y;
-  }
-}
-
 __device__ __forceinline__ uint4 ldg16(const void* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
-
 __device__ __forceinline__ void sts16(uint32_t addr, const uint4& v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
                : "memory");
 }
+__device__ __forceinline__ uint4 pack8(const float* f) {
+  return make_uint4(tc::pack_bf16x2(f[0], f[1]), tc::pack_bf16x2(f[2], f[3]),
+                    tc::pack_bf16x2(f[4], f[5]), tc::pack_bf16x2(f[6], f[7]));
+}
+// bar.sync over a group, returning the OR of every member's flag (so all members agree).
+__device__ __forceinline__ int group_sync_or(uint32_t id, uint32_t n, int flag) {
+  int r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.s32 p, %3, 0;\n bar.red.or.pred q, %1, %2, p;\n"
+      " selp.s32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(id), "r"(n), "r"(flag)
+      : "memory");
+  return r;
+}
 
-// Document bounds for a CTA; false if the document is malformed (reported, then skipped).
+// Document bounds; false if the document is malformed (then treated as empty).
 __device__ __forceinline__ bool doc_bounds(const PrefillArgs& a, int doc, long& row0, int& n) {
   if (a.cu_seqlens != nullptr) {
     const int s = a.cu_seqlens[doc];
@@ -115,110 +170,173 @@ __device__ __forceinline__ bool doc_bounds(const PrefillArgs& a, int doc, long& 
   return true;
 }
 
-// Features of 16 consecutive elements of one token row (this thread's part), for q and k at the
-// same position: RMSNorm over the row (shuffle across the TPR threads of the row), RoPE, ReLU,
-// rounded to bf16 and packed into 2 x 16 bytes each.
-template <int D>
-__device__ __forceinline__ void features16(const uint4 (&xq)[2], const uint4 (&xk)[2], bool valid,
-                                           int pos, const float (&gq)[16], const float (&gk)[16],
-                                           const float (&fhi)[8], const float (&flo)[8],
-                                           float eps_norm, uint4 (&oq)[2], uint4 (&ok)[2]) {
-  constexpr int TPR = TcCfg<D>::TPR;
-  float fq[16], fk[16];
-  unpack8(xq[0], fq);
-  unpack8(xq[1], fq + 8);
-  unpack8(xk[0], fk);
-  unpack8(xk[1], fk + 8);
-  float sq = 0.f, sk = 0.f;
-#pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    sq = fmaf(fq[e], fq[e], sq);
-    sk = fmaf(fk[e], fk[e], sk);
-  }
-#pragma unroll
-  for (int off = TPR / 2; off > 0; off >>= 1) {
-    sq += __shfl_xor_sync(0xffffffffu, sq, off);
-    sk += __shfl_xor_sync(0xffffffffu, sk, off);
-  }
-  const float rq = rsqrtf(sq * (1.0f / D) + eps_norm);
-  const float rk = rsqrtf(sk * (1.0f / D) + eps_norm);
-  uint32_t wq[8], wk[8];
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    float s, c;
-    rope_sincos(pos, fhi[m], flo[m], s, c);
-    const float q0 = fq[2 * m] * rq * gq[2 * m], q1 = fq[2 * m + 1] * rq * gq[2 * m + 1];
-    const float k0 = fk[2 * m] * rk * gk[2 * m], k1 = fk[2 * m + 1] * rk * gk[2 * m + 1];
-    const float qa = fmaxf(fmaf(q0, c, -q1 * s), 0.f), qb = fmaxf(fmaf(q0, s, q1 * c), 0.f);
-    const float ka = fmaxf(fmaf(k0, c, -k1 * s), 0.f), kb = fmaxf(fmaf(k0, s, k1 * c), 0.f);
-    wq[m] = valid ? tc::pack_bf16x2(qa, qb) : 0u;
-    wk[m] = valid ? tc::pack_bf16x2(ka, kb) : 0u;
-  }
-  oq[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-  oq[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
-  ok[0] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
-  ok[1] = make_uint4(wk[4], wk[5], wk[6], wk[7]);
-}
-
-// Same for k only (kernel A).
-template <int D>
-__device__ __forceinline__ void features16_k(const uint4 (&xk)[2], bool valid, int pos,
-                                             const float (&gk)[16], const float (&fhi)[8],
-                                             const float (&flo)[8], float eps_norm, uint4 (&ok)[2]) {
-  constexpr int TPR = TcCfg<D>::TPR;
-  float fk[16];
-  unpack8(xk[0], fk);
-  unpack8(xk[1], fk + 8);
-  float sk = 0.f;
-#pragma unroll
-  for (int e = 0; e < 16; ++e) sk = fmaf(fk[e], fk[e], sk);
-#pragma unroll
-  for (int off = TPR / 2; off > 0; off >>= 1) sk += __shfl_xor_sync(0xffffffffu, sk, off);
-  const float rk = rsqrtf(sk * (1.0f / D) + eps_norm);
-  uint32_t wk[8];
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    float s, c;
-    rope_sincos(pos, fhi[m], flo[m], s, c);
-    const float k0 = fk[2 * m] * rk * gk[2 * m], k1 = fk[2 * m + 1] * rk * gk[2 * m + 1];
-    const float ka = fmaxf(fmaf(k0, c, -k1 * s), 0.f), kb = fmaxf(fmaf(k0, s, k1 * c), 0.f);
-    wk[m] = valid ? tc::pack_bf16x2(ka, kb) : 0u;
-  }
-  ok[0] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
-  ok[1] = make_uint4(wk[4], wk[5], wk[6], wk[7]);
-}
-
-// Column groups (16 columns each) of the [S | z] tile handled by a thread of half `hf`:
-// half 0 takes columns [0, D/2) and the z block [D, D + 16), half 1 takes [D/2, D).
-template <int D>
-struct StateCols {
-  static constexpr int N0 = D / 32 + 1;  // groups of half 0
-  static constexpr int N1 = D / 32;      // groups of half 1
-  static __device__ __forceinline__ int count(int hf) { return hf == 0 ? N0 : N1; }
-  static __device__ __forceinline__ int col(int hf, int g) {
-    return hf == 0 ? (g < D / 32 ? 16 * g : D) : D / 2 + 16 * g;
-  }
+// ---------------------------------------------------------------------------------------------
+// Feature arithmetic on packed fp32 pairs. A thread's 8 elements are four RoPE pairs m = 0..3
+// (elements 2m, 2m+1). They are held as two "structure of arrays" groups g = 0, 1 covering pairs
+// 2g and 2g+1: x0[g] = (first element of pair 2g, first of pair 2g+1), x1[g] = the second
+// elements, so every rotation step is one packed operation over two pairs.
+struct Pairs {
+  float2 x0[2], x1[2];
 };
 
-// Writes 16 fp32 values (columns j0 .. j0+15 of state row i) as bf16 into the [S | z]~ operand.
+__device__ __forceinline__ Pairs unpack_pairs(const uint4& u) {
+  // 32-bit word m of the 16 bytes holds pair m: element 2m in the low half, 2m+1 in the high half
+  Pairs p;
+  p.x0[0] = make_float2(__uint_as_float(u.x << 16), __uint_as_float(u.y << 16));
+  p.x1[0] = make_float2(__uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y & 0xffff0000u));
+  p.x0[1] = make_float2(__uint_as_float(u.z << 16), __uint_as_float(u.w << 16));
+  p.x1[1] = make_float2(__uint_as_float(u.z & 0xffff0000u), __uint_as_float(u.w & 0xffff0000u));
+  return p;
+}
+
+__device__ __forceinline__ float sumsq(const Pairs& p) {
+  float2 acc = __fmul2_rn(p.x0[0], p.x0[0]);
+  acc = __ffma2_rn(p.x1[0], p.x1[0], acc);
+  acc = __ffma2_rn(p.x0[1], p.x0[1], acc);
+  acc = __ffma2_rn(p.x1[1], p.x1[1], acc);
+  return acc.x + acc.y;
+}
+
+template <int TPR>
+__device__ __forceinline__ float row_sum(float x) {
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+// Per-thread RoPE constants: gains and the sin/cos of the current row's angles, in pair groups.
+struct Rot {
+  float2 c[2], s[2];  // cos / sin of pairs (2g, 2g+1)
+};
+
+// ReLU(RoPE(x * gamma)) * rinv (rinv > 0 commutes with ReLU), in place: x0 <- first elements,
+// x1 <- second elements of the rotated pairs.
+__device__ __forceinline__ void rope_relu(Pairs& p, const float2 (&g0)[2], const float2 (&g1)[2],
+                                          const Rot& r, float rinv) {
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    const float2 y0 = __fmul2_rn(p.x0[g], g0[g]);
+    const float2 y1 = __fmul2_rn(p.x1[g], g1[g]);
+    const float2 ns = make_float2(-r.s[g].x, -r.s[g].y);
+    const float2 u = __ffma2_rn(y0, r.c[g], __fmul2_rn(y1, ns));   // y0 c - y1 s
+    const float2 v = __ffma2_rn(y0, r.s[g], __fmul2_rn(y1, r.c[g]));  // y0 s + y1 c
+    p.x0[g] = make_float2(fmaxf(u.x, 0.f) * rinv, fmaxf(u.y, 0.f) * rinv);
+    p.x1[g] = make_float2(fmaxf(v.x, 0.f) * rinv, fmaxf(v.y, 0.f) * rinv);
+  }
+}
+
+__device__ __forceinline__ uint4 pack_pairs(const Pairs& p) {
+  return make_uint4(tc::pack_bf16x2(p.x0[0].x, p.x1[0].x), tc::pack_bf16x2(p.x0[0].y, p.x1[0].y),
+                    tc::pack_bf16x2(p.x0[1].x, p.x1[1].x), tc::pack_bf16x2(p.x0[1].y, p.x1[1].y));
+}
+
+// Advances the angles by a fixed step (cos / sin of the step in `st`): one exact rotation.
+__device__ __forceinline__ void rot_step(Rot& r, const Rot& st) {
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    const float2 ns = make_float2(-r.s[g].x, -r.s[g].y);
+    const float2 c = __ffma2_rn(r.c[g], st.c[g], __fmul2_rn(ns, st.s[g]));
+    const float2 s = __ffma2_rn(r.s[g], st.c[g], __fmul2_rn(r.c[g], st.s[g]));
+    r.c[g] = c;
+    r.s[g] = s;
+  }
+}
+
+// Column sums of the 8 per-thread values over the rows of a warp (lanes with equal lane % TPR).
+template <int TPR>
+__device__ __forceinline__ void warp_colsum(float* z) {
+#pragma unroll
+  for (int off = TPR; off < 32; off <<= 1)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) z[e] += __shfl_xor_sync(0xffffffffu, z[e], off);
+}
+__device__ __forceinline__ void pairs_to8(const Pairs& p, float* f) {
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    f[4 * g + 0] = p.x0[g].x;
+    f[4 * g + 1] = p.x1[g].x;
+    f[4 * g + 2] = p.x0[g].y;
+    f[4 * g + 3] = p.x1[g].y;
+  }
+}
+
+// Gains of a thread's 8 elements in pair groups.
+__device__ __forceinline__ void load_gamma(const float* gp, float2 (&g0)[2], float2 (&g1)[2]) {
+  const float4 a = *reinterpret_cast<const float4*>(gp);
+  const float4 b = *reinterpret_cast<const float4*>(gp + 4);
+  g0[0] = make_float2(a.x, a.z);
+  g1[0] = make_float2(a.y, a.w);
+  g0[1] = make_float2(b.x, b.z);
+  g1[1] = make_float2(b.y, b.w);
+}
+
+// Per-CTA feature constants in shared memory (8 * D floats), so that the producers need no
+// registers for them and no lane-divergent reads of the kernel parameters: the gains of q and k,
+// and for every RoPE pair the frequency (hi, lo turns) and the cos / sin of the rotation over
+// one producer pass (RPP positions).
+struct FeatTab {
+  float* gq;   // [D]
+  float* gk;   // [D]
+  float* fhi;  // [D/2]
+  float* flo;  // [D/2]
+  float* stc;  // [D/2] cos of the per-pass rotation
+  float* sts;  // [D/2] sin
+};
 template <int D>
-__device__ __forceinline__ void store_state_bf16(uint32_t ss_base, int i, int j0, const float* v) {
-  const int jb = j0 / 64, c = (j0 % 64) / 8;
-  uint4 w0 = make_uint4(tc::pack_bf16x2(v[0], v[1]), tc::pack_bf16x2(v[2], v[3]),
-                        tc::pack_bf16x2(v[4], v[5]), tc::pack_bf16x2(v[6], v[7]));
-  uint4 w1 = make_uint4(tc::pack_bf16x2(v[8], v[9]), tc::pack_bf16x2(v[10], v[11]),
-                        tc::pack_bf16x2(v[12], v[13]), tc::pack_bf16x2(v[14], v[15]));
-  const uint32_t blk = ss_base + static_cast<uint32_t>(jb) * (D * 128);
-  sts16(blk + tc::sw128(i, c), w0);
-  sts16(blk + tc::sw128(i, c + 1), w1);
+__device__ __forceinline__ FeatTab feat_tab(uint8_t* p) {
+  float* f = reinterpret_cast<float*>(p);
+  return FeatTab{f, f + D, f + 2 * D, f + 2 * D + D / 2, f + 3 * D, f + 3 * D + D / 2};
+}
+template <int D>
+__device__ __forceinline__ void fill_tab(const FeatTab& t, const PrefillArgs& a, int h, int rpp,
+                                         int tid, int nthreads) {
+  for (int i = tid; i < D; i += nthreads) {
+    t.gq[i] = a.gamma_q[h * a.fa.gamma_stride + i];
+    t.gk[i] = a.gamma_k[h * a.fa.gamma_stride + i];
+  }
+  for (int j = tid; j < D / 2; j += nthreads) {
+    t.fhi[j] = a.fa.rope_hi[j];
+    t.flo[j] = a.fa.rope_lo[j];
+    float sn, cs;
+    rope_sincos(rpp, a.fa.rope_hi[j], a.fa.rope_lo[j], sn, cs);
+    t.stc[j] = cs;
+    t.sts[j] = sn;
+  }
+}
+// Gains / rotation step of a thread's 8 elements (pairs j0 .. j0+3) from the tables.
+__device__ __forceinline__ void tab_gamma(const float* g, int e0, float2 (&g0)[2], float2 (&g1)[2]) {
+  load_gamma(g + e0, g0, g1);
+}
+__device__ __forceinline__ void tab_step(const FeatTab& t, int j0, Rot& st) {
+  const float4 c = *reinterpret_cast<const float4*>(t.stc + j0);
+  const float4 sn = *reinterpret_cast<const float4*>(t.sts + j0);
+  st.c[0] = make_float2(c.x, c.y);
+  st.c[1] = make_float2(c.z, c.w);
+  st.s[0] = make_float2(sn.x, sn.y);
+  st.s[1] = make_float2(sn.z, sn.w);
+}
+__device__ __forceinline__ void tab_rot_at(const FeatTab& t, int pos, int j0, Rot& r) {
+  const float4 hi = *reinterpret_cast<const float4*>(t.fhi + j0);
+  const float4 lo = *reinterpret_cast<const float4*>(t.flo + j0);
+  float s0, c0, s1, c1, s2, c2, s3, c3;
+  rope_sincos(pos, hi.x, lo.x, s0, c0);
+  rope_sincos(pos, hi.y, lo.y, s1, c1);
+  rope_sincos(pos, hi.z, lo.z, s2, c2);
+  rope_sincos(pos, hi.w, lo.w, s3, c3);
+  r.c[0] = make_float2(c0, c1);
+  r.c[1] = make_float2(c2, c3);
+  r.s[0] = make_float2(s0, s1);
+  r.s[1] = make_float2(s2, s3);
 }
 
 // ------------------------------------------------------------------------------------------------
 // Kernel B: one CTA per (document, head, segment).
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs ta) {
-  using Cfg = TcCfg<D>;
-  constexpr int NA = Cfg::NA, TPR = Cfg::TPR, RPP = Cfg::RPP, NPASS = Cfg::NPASS;
+__global__ void __launch_bounds__(kThreadsB, 1)
+    prefill_tc_kernel(const TcArgs ta, const __grid_constant__ CUtensorMap tmap_v) {
+  using L = LayB<D>;
+  using PM = Prod<D>;
+  constexpr int TPR = PM::TPR, RPP = PM::RPP, NPASS = PM::NPASS, RING = PM::RING;
   const PrefillArgs& a = ta.p;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -234,308 +352,424 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const TcArgs ta
   if (seg >= nseg_doc) return;  // uniform across the CTA, before any allocation
   const int seg_start = seg * ta.seg_len;
   const int seg_n = min(ta.seg_len, n - seg_start);  // 0 only for an empty document
+  const int nchunks = (seg_n + kC - 1) / kC;
   const bool last_seg = seg == nseg_doc - 1;
+  const long bh = static_cast<long>(doc) * a.H + h;
 
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = tc::smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t bar_a = base + Cfg::CTRL, bar_b = bar_a + 8;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(gbase + Cfg::CTRL + 16);
-  int* s_abort = reinterpret_cast<int*>(gbase + Cfg::CTRL + 20);
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t base = tc::smem_u32(smem);
+  if (base & 1023u) {  // the swizzled layouts need 1024-byte alignment
+    if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, kDevInternal);
+    return;
+  }
+  float* zp = reinterpret_cast<float*>(smem + L::ZP);
+  float* zs = reinterpret_cast<float*>(smem + L::ZS);
+  float* di = reinterpret_cast<float*>(smem + L::DI);
+  const uint32_t bar_full = base + L::BAR, bar_empty = bar_full + 16, bar_vfull = bar_full + 32;
+  const uint32_t bar_s = bar_full + 48, bar_a = bar_full + 56, bar_b = bar_full + 64;
+  const uint32_t bar_conv = bar_full + 72;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::MISC);
+  int* s_abort = reinterpret_cast<int*>(smem + L::MISC + 4);
+  int* s_ready = reinterpret_cast<int*>(smem + L::MISC + 8);
 
   if (warp == 0) {
     tc::tmem_alloc(tc::smem_u32(s_tmem), 512);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
+    tc::mbar_init(bar_full, kProd);
+    tc::mbar_init(bar_full + 8, kProd);
+    tc::mbar_init(bar_empty, 1);
+    tc::mbar_init(bar_empty + 8, 1);
+    tc::mbar_init(bar_vfull, 1);
+    tc::mbar_init(bar_vfull + 8, 1);
+    tc::mbar_init(bar_s, 1);
     tc::mbar_init(bar_a, 1);
     tc::mbar_init(bar_b, 1);
+    tc::mbar_init(bar_conv, kCons);
     tc::mbar_fence_init();
     *s_abort = 0;
+    *s_ready = 0;
   }
-  // constant parts of the operands: the ones block of [V | 1] (column D of every row), and for
-  // D = 64 the zero block that pads k'^T to M = 128
-  for (int idx = tid; idx < 16384 / 16; idx += kThreads) {
-    const int r = idx / 8, c = idx % 8;
-    const uint32_t one = (c == 0) ? 0x3F80u : 0u;  // bf16 1.0 in the first element of chunk 0
-    sts16(base + Cfg::VS + Cfg::KB * 16384 + tc::sw128(r, c), make_uint4(one, 0u, 0u, 0u));
-    if (D == 64) sts16(base + Cfg::KS + 16384 + idx * 16, make_uint4(0u, 0u, 0u, 0u));
+  if (D == 64) {  // zero block that pads k'^T to M = 128 rows
+    for (int i = tid; i < 16384 / 16; i += kThreadsB) sts16(base + L::KS + 16384 + i * 16, make_uint4(0, 0, 0, 0));
   }
+  const FeatTab tab = feat_tab<D>(smem + L::TAB);
+  fill_tab<D>(tab, a, h, RPP, tid, kThreadsB);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *s_tmem;
+  const float* wsb = ta.ws + bh * ta.nseg_max * static_cast<long>(D) * (D + kPad);
 
-  const int q4 = warp & 3, hf = warp >> 2;
-  const int er = 32 * q4 + lane;  // TMEM lane / tile row owned in the epilogues
-  const uint32_t tlane = static_cast<uint32_t>(32 * q4) << 16;
-  const long bh = static_cast<long>(doc) * a.H + h;
-
-  // ---- initial state: S0 + increments of the earlier segments -> TMEM (fp32) and [S|z]~ (bf16)
-  {
-    const float* wsb = ta.ws + (bh * ta.nseg_max) * static_cast<long>(D) * (D + 1);
-    for (int g = 0; g < StateCols<D>::count(hf); ++g) {
-      const int j0 = StateCols<D>::col(hf, g);
-      float v[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int j = j0 + e;
-        float x = 0.f;
-        if (er < D && j <= D) {
-          if (j < D) {
-            if (a.S0 != nullptr) x = a.S0[(bh * D + er) * D + j];
-          } else if (a.z0 != nullptr) {
-            x = a.z0[bh * D + er];
-          }
-          for (int gs = 0; gs < seg; ++gs) x += wsb[(static_cast<long>(gs) * D + er) * (D + 1) + j];
-        }
-        v[e] = x;
-      }
-      uint32_t u[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(v[e]);
-      tc::tmem_st16(tmem + tlane + Cfg::TS + j0, u);
-      if (er < D) store_state_bf16<D>(base + Cfg::SS, er, j0, v);
+  if (warp < kProd / 32) {
+    // ============================================================ producers
+    tc::regs_inc<kRegsProdB>();
+    const int prow = tid / TPR, part = tid % TPR, e0 = 8 * part;
+    const uint32_t cblk = static_cast<uint32_t>(e0 / 64) * 16384;  // 64-column block
+    const int cidx = (e0 % 64) / 8;                                 // 16-byte chunk in the row
+    // z at the segment start: z0 + the earlier segments' sums of k'
+    for (int i = tid; i < D; i += kProd) {
+      float z = a.z0 != nullptr ? a.z0[bh * D + i] : 0.f;
+      for (int g = 0; g < seg; ++g) z += wsb[(static_cast<long>(g) * D + i) * (D + kPad) + D];
+      zs[i] = z;
     }
-    tc::tmem_wait_st();
-  }
+    tc::named_sync(kBarProd, kProd);
 
-  // ---- per-thread constants of the prologue
-  const int prow = tid / TPR, part = tid % TPR;
-  const int e0 = 16 * part;
-  float gq[16], gk[16], fhi[8], flo[8];
-  {
-    const float* gqp = a.gamma_q + h * a.fa.gamma_stride;
-    const float* gkp = a.gamma_k + h * a.fa.gamma_stride;
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      gq[e] = gqp[e0 + e];
-      gk[e] = gkp[e0 + e];
-    }
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      fhi[m] = a.fa.rope_hi[(e0 >> 1) + m];
-      flo[m] = a.fa.rope_lo[(e0 >> 1) + m];
-    }
-  }
-  const uint32_t pro_off = static_cast<uint32_t>(part / 4) * 16384;  // 64-column block
-  const int pro_c = (part % 4) * 2;                                   // first 16-byte chunk
-  const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
-  const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(a.k);
-  const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(a.v);
-  __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out);
-  const int pos_base = a.pos_offset + seg_start;
-
-  uint4 rq[NPASS][2], rk[NPASS][2], rv[NPASS][2];
-  auto prefetch = [&](int t0) {
-#pragma unroll
-    for (int p = 0; p < NPASS; ++p) {
-      const int lt = t0 + p * RPP + prow;
+    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
+    const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(a.k);
+    const int pos_base = a.pos_offset + seg_start;
+    auto load = [&](int c, int p, uint4& xq, uint4& xk) {
+      const int lt = c * kC + p * RPP + prow;
       if (lt < seg_n) {
         const long off = ((row0 + seg_start + lt) * a.H + h) * D + e0;
-        rq[p][0] = ldg16(qg + off);
-        rq[p][1] = ldg16(qg + off + 8);
-        rk[p][0] = ldg16(kg + off);
-        rk[p][1] = ldg16(kg + off + 8);
-        rv[p][0] = ldg16(vg + off);
-        rv[p][1] = ldg16(vg + off + 8);
+        xq = ldg16(qg + off);
+        xk = ldg16(kg + off);
       } else {
-        rq[p][0] = rq[p][1] = rk[p][0] = rk[p][1] = rv[p][0] = rv[p][1] = make_uint4(0, 0, 0, 0);
+        xq = xk = make_uint4(0, 0, 0, 0);
       }
-    }
-  };
-
-  constexpr uint32_t ID_P = tc::idesc_bf16(128, 128, false, false);
-  constexpr uint32_t ID_QS = tc::idesc_bf16(128, NA, false, true);
-  constexpr uint32_t ID_KV = tc::idesc_bf16(128, NA, true, true);
-  constexpr uint32_t ID_PV = tc::idesc_bf16(128, NA, false, true);
-
-  uint32_t phase_a = 0, phase_b = 0;
-  bool aborted = false;
-  uint32_t fail_bar = 0, fail_parity = 0;  // the wait that gave up, if any
-  if (seg_n > 0) prefetch(0);
-
-  for (int t0 = 0; t0 < seg_n; t0 += kC) {
-    // ---- prologue: features of the chunk into q', k'; raw v into [V | 1]
+    };
+    uint4 rq[RING], rk[RING];
+    if (nchunks > 0) {
 #pragma unroll
-    for (int p = 0; p < NPASS; ++p) {
-      const int r = p * RPP + prow;
-      const bool valid = t0 + r < seg_n;
-      uint4 oq[2], ok[2];
-      features16<D>(rq[p], rk[p], valid, pos_base + t0 + r, gq, gk, fhi, flo, a.fa.eps_norm, oq, ok);
-      sts16(base + Cfg::QS + pro_off + tc::sw128(r, pro_c), oq[0]);
-      sts16(base + Cfg::QS + pro_off + tc::sw128(r, pro_c + 1), oq[1]);
-      sts16(base + Cfg::KS + pro_off + tc::sw128(r, pro_c), ok[0]);
-      sts16(base + Cfg::KS + pro_off + tc::sw128(r, pro_c + 1), ok[1]);
-      sts16(base + Cfg::VS + pro_off + tc::sw128(r, pro_c), rv[p][0]);
-      sts16(base + Cfg::VS + pro_off + tc::sw128(r, pro_c + 1), rv[p][1]);
+      for (int p = 0; p < RING; ++p) load(0, p, rq[p], rk[p]);
     }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-
-    if (tid == 0) {
-      tc::fence_after_sync();
-      // P = Q' K'^T
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c & 1;
+      int bad = 0;
+      if (c >= 2 && !tc::mbar_wait(bar_empty + 8 * s, ((c >> 1) + 1) & 1, kWaitCycles)) bad = 1;
+      const uint32_t qb = base + (s ? L::Q1 : L::Q0), vb = base + (s ? L::V1 : L::V0);
+      if (tid == 0) {
+        // v rows of this chunk, straight into the swizzled operand (rows past the segment are
+        // either other tokens or zero fill; their k' and P columns are zero)
+        tc::mbar_arrive_expect_tx(bar_vfull + 8 * s, L::TILE);
 #pragma unroll
-      for (int s = 0; s < D / 16; ++s) {
-        const uint32_t off = (s / 4) * 16384 + (s % 4) * 32;
-        tc::mma_bf16(tmem + Cfg::TP, tc::desc_sw128(base + Cfg::QS + off, 16, 1024),
-                     tc::desc_sw128(base + Cfg::KS + off, 16, 1024), ID_P, s > 0);
+        for (int jb = 0; jb < D / 64; ++jb)
+          tc::tma_load_3d(vb + jb * 16384, &tmap_v, 64 * jb, h,
+                          static_cast<int>(row0 + seg_start + c * kC), bar_vfull + 8 * s);
       }
-      // O = Q' [S | z]~   (carried-in state)
+      float* dis = di + s * kC;
+      uint4 kreg[NPASS];
+      float2 zca[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      float2 zcb[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      Rot rot;
+      tab_rot_at(tab, pos_base + c * kC + prow, e0 / 2, rot);
 #pragma unroll
-      for (int s = 0; s < D / 16; ++s) {
-        const uint32_t off = (s / 4) * 16384 + (s % 4) * 32;
-        tc::mma_bf16(tmem + Cfg::TO, tc::desc_sw128(base + Cfg::QS + off, 16, 1024),
-                     tc::desc_sw128(base + Cfg::SS + s * 2048, D * 128, 1024), ID_QS, s > 0);
+      for (int p = 0; p < NPASS; ++p) {
+        const uint4 xq = rq[p % RING], xk = rk[p % RING];
+        if (p + RING < NPASS) load(c, p + RING, rq[p % RING], rk[p % RING]);
+        else if (c + 1 < nchunks) load(c + 1, p + RING - NPASS, rq[p % RING], rk[p % RING]);
+        const int r = p * RPP + prow;
+        const bool valid = c * kC + r < seg_n;
+        if (p > 0) {
+          Rot step;  // rotation by RPP positions (one pass further down the chunk)
+          tab_step(tab, e0 / 2, step);
+          rot_step(rot, step);
+        }
+        Pairs fq = unpack_pairs(xq), fk = unpack_pairs(xk);
+        const float rq2 = sumsq(fq), rk2 = sumsq(fk);
+        const float sq = row_sum<TPR>(rq2), sk = row_sum<TPR>(rk2);
+        const float rinvq = valid ? rsqrtf(sq * (1.0f / D) + a.fa.eps_norm) : 0.f;
+        const float rinvk = valid ? rsqrtf(sk * (1.0f / D) + a.fa.eps_norm) : 0.f;
+        {
+          float2 g0[2], g1[2];
+          tab_gamma(tab.gq, e0, g0, g1);
+          rope_relu(fq, g0, g1, rot, rinvq);
+          tab_gamma(tab.gk, e0, g0, g1);
+          rope_relu(fk, g0, g1, rot, rinvk);
+        }
+        const float4 z4a = *reinterpret_cast<const float4*>(zs + e0);
+        const float4 z4b = *reinterpret_cast<const float4*>(zs + e0 + 4);
+        const float2 zfa[2] = {make_float2(z4a.x, z4a.z), make_float2(z4b.x, z4b.z)};  // first elements
+        const float2 zfb[2] = {make_float2(z4a.y, z4a.w), make_float2(z4b.y, z4b.w)};  // second
+        float2 d2 = __fmul2_rn(fq.x0[0], zfa[0]);
+        d2 = __ffma2_rn(fq.x1[0], zfb[0], d2);
+        d2 = __ffma2_rn(fq.x0[1], zfa[1], d2);
+        d2 = __ffma2_rn(fq.x1[1], zfb[1], d2);
+        const float dq = row_sum<TPR>(d2.x + d2.y);
+        if (part == 0) dis[r] = dq;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          zca[g] = __fadd2_rn(zca[g], fk.x0[g]);
+          zcb[g] = __fadd2_rn(zcb[g], fk.x1[g]);
+        }
+        sts16(qb + cblk + tc::sw128(r, cidx), pack_pairs(fq));
+        kreg[p] = pack_pairs(fk);
       }
-      // [S | z] += K'^T [V | 1]
+      // the single k' buffer is free once the previous chunk's MMAs have completed
+      if (c >= 1 && !tc::mbar_wait(bar_a, (c - 1) & 1, kWaitCycles)) bad = 1;
 #pragma unroll
-      for (int s = 0; s < kC / 16; ++s) {
-        tc::mma_bf16(tmem + Cfg::TS, tc::desc_sw128(base + Cfg::KS + s * 2048, 16384, 1024),
-                     tc::desc_sw128(base + Cfg::VS + s * 2048, 16384, 1024), ID_KV, 1u);
+      for (int p = 0; p < NPASS; ++p) sts16(base + L::KS + cblk + tc::sw128(p * RPP + prow, cidx), kreg[p]);
+      tc::fence_async_smem();
+      tc::mbar_arrive(bar_full + 8 * s);
+      // z_c = z_{c-1} + column sums of k'_c (fixed order: deterministic)
+      float zc[8];
+      pairs_to8(Pairs{{zca[0], zca[1]}, {zcb[0], zcb[1]}}, zc);
+      warp_colsum<TPR>(zc);
+      if (lane < TPR) {
+        *reinterpret_cast<float4*>(zp + warp * D + e0) = make_float4(zc[0], zc[1], zc[2], zc[3]);
+        *reinterpret_cast<float4*>(zp + warp * D + e0 + 4) = make_float4(zc[4], zc[5], zc[6], zc[7]);
       }
-      tc::mma_commit(bar_a);
-    }
-    if (t0 + kC < seg_n) prefetch(t0 + kC);  // next chunk's loads overlap this chunk's work
-
-    if (!tc::mbar_wait(bar_a, phase_a, kWaitCycles)) *s_abort = 1;
-    __syncthreads();
-    if (*s_abort) {
-      aborted = true;
-      fail_bar = bar_a;
-      fail_parity = phase_a;
-      break;
-    }
-    phase_a ^= 1;
-    tc::fence_after_sync();
-
-    // ---- P -> masked bf16 P~ ; [S | z] (after this chunk) -> bf16 [S | z]~ for the next chunk
+      if (bad) atomicExch(s_abort, 1);
+      tc::named_sync(kBarProd, kProd);
+      if (tid < D) {
+        float z = zs[tid];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
+        for (int w = 0; w < PM::WARPS; ++w) z += zp[w * D + tid];
+        zs[tid] = z;
+      }
+      if (group_sync_or(kBarProd, kProd, *s_abort)) break;
+    }
+    if (last_seg && a.z_final != nullptr && !*s_abort) {
+      for (int i = tid; i < D; i += kProd) a.z_final[bh * D + i] = zs[i];
+    }
+  } else if (warp < (kProd + kCons) / 32) {
+    // ============================================================ consumers
+    tc::regs_dec<kRegsConsB>();
+    const int q4 = warp & 3;                 // TMEM lane quarter
+    const int er = 32 * q4 + lane;           // TMEM lane = tile row
+    const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
+
+    // initial state S0 + earlier increments -> TMEM (fp32) and S~ (bf16); zero rows >= D
+    for (int j0 = 0; j0 < D; j0 += 16) {
+      float v[16];
       uint32_t u[16];
-      tc::tmem_ld16(tmem + tlane + Cfg::TP + 64 * hf + 16 * m, u);
-      tc::tmem_wait_ld();
-      float f[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int tau = 64 * hf + 16 * m + e;
-        f[e] = tau <= er ? __uint_as_float(u[e]) : 0.f;
-      }
-      const uint32_t blk = base + Cfg::PS + hf * 16384;
-      sts16(blk + tc::sw128(er, 2 * m),
-            make_uint4(tc::pack_bf16x2(f[0], f[1]), tc::pack_bf16x2(f[2], f[3]),
-                       tc::pack_bf16x2(f[4], f[5]), tc::pack_bf16x2(f[6], f[7])));
-      sts16(blk + tc::sw128(er, 2 * m + 1),
-            make_uint4(tc::pack_bf16x2(f[8], f[9]), tc::pack_bf16x2(f[10], f[11]),
-                       tc::pack_bf16x2(f[12], f[13]), tc::pack_bf16x2(f[14], f[15])));
-    }
-    if (32 * q4 < D) {  // warp-uniform: TMEM rows >= D hold the zero padding of k'^T
-      for (int g = 0; g < StateCols<D>::count(hf); ++g) {
-        const int j0 = StateCols<D>::col(hf, g);
-        uint32_t u[16];
-        tc::tmem_ld16(tmem + tlane + Cfg::TS + j0, u);
-        tc::tmem_wait_ld();
-        float v[16];
+      for (int e = 0; e < 16; ++e) v[e] = 0.f;
+      if (er < D) {
+        if (a.S0 != nullptr) {
+          const float4* src = reinterpret_cast<const float4*>(a.S0 + (bh * D + er) * D + j0);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(u[e]);
-        store_state_bf16<D>(base + Cfg::SS, er, j0, v);
-      }
-    }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-
-    if (tid == 0) {
-      tc::fence_after_sync();
-      // O += P~ [V | 1]
+          for (int e = 0; e < 4; ++e) {
+            const float4 x = src[e];
+            v[4 * e] += x.x; v[4 * e + 1] += x.y; v[4 * e + 2] += x.z; v[4 * e + 3] += x.w;
+          }
+        }
+        for (int g = 0; g < seg; ++g) {
+          const float4* src = reinterpret_cast<const float4*>(wsb + (static_cast<long>(g) * D + er) * (D + kPad) + j0);
+          float4 x[4];
 #pragma unroll
-      for (int s = 0; s < kC / 16; ++s) {
-        const uint32_t off = (s / 4) * 16384 + (s % 4) * 32;
-        tc::mma_bf16(tmem + Cfg::TO, tc::desc_sw128(base + Cfg::PS + off, 16, 1024),
-                     tc::desc_sw128(base + Cfg::VS + s * 2048, 16384, 1024), ID_PV, 1u);
-      }
-      tc::mma_commit(bar_b);
-    }
-    if (!tc::mbar_wait(bar_b, phase_b, kWaitCycles)) *s_abort = 1;
-    __syncthreads();
-    if (*s_abort) {
-      aborted = true;
-      fail_bar = bar_b;
-      fail_parity = phase_b;
-      break;
-    }
-    phase_b ^= 1;
-    tc::fence_after_sync();
-
-    // ---- epilogue: out = O[:, :D] / (O[:, D] + eps)
-    {
-      uint32_t dz;
-      tc::tmem_ld1(tmem + tlane + Cfg::TO + D, dz);
-      tc::tmem_wait_ld();
-      const float inv = 1.0f / (__uint_as_float(dz) + a.eps_den);
-      const bool valid = t0 + er < seg_n;
-      __nv_bfloat16* orow = og + ((row0 + seg_start + t0 + er) * a.H + h) * D + hf * (D / 2);
+          for (int e = 0; e < 4; ++e) x[e] = __ldcg(src + e);
 #pragma unroll
-      for (int m = 0; m < D / 32; ++m) {
-        uint32_t u[16];
-        tc::tmem_ld16(tmem + tlane + Cfg::TO + hf * (D / 2) + 16 * m, u);
-        tc::tmem_wait_ld();
-        if (valid) {
-          float f[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(u[e]) * inv;
-          uint4* dst = reinterpret_cast<uint4*>(orow + 16 * m);
-          dst[0] = make_uint4(tc::pack_bf16x2(f[0], f[1]), tc::pack_bf16x2(f[2], f[3]),
-                              tc::pack_bf16x2(f[4], f[5]), tc::pack_bf16x2(f[6], f[7]));
-          dst[1] = make_uint4(tc::pack_bf16x2(f[8], f[9]), tc::pack_bf16x2(f[10], f[11]),
-                              tc::pack_bf16x2(f[12], f[13]), tc::pack_bf16x2(f[14], f[15]));
+          for (int e = 0; e < 4; ++e) {
+            v[4 * e] += x[e].x; v[4 * e + 1] += x[e].y; v[4 * e + 2] += x[e].z; v[4 * e + 3] += x[e].w;
+          }
         }
       }
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-  }
-
-  if (aborted) {
-    if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, kDevTimeout);
-    // give the MMAs still in flight a bounded chance to land before TMEM is released
-    tc::mbar_wait(fail_bar, fail_parity, kWaitCycles);
-  } else if (last_seg && (a.S_final != nullptr || a.z_final != nullptr) && 32 * q4 < D) {
-    // ---- final state of the document
-    tc::fence_after_sync();
-    for (int g = 0; g < StateCols<D>::count(hf); ++g) {
-      const int j0 = StateCols<D>::col(hf, g);
-      uint32_t u[16];
-      tc::tmem_ld16(tmem + tlane + Cfg::TS + j0, u);
-      tc::tmem_wait_ld();
-      if (j0 < D) {
-        if (a.S_final != nullptr) {
-          float4* dst = reinterpret_cast<float4*>(a.S_final + (bh * D + er) * D + j0);
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[e] = make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
-                                 __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3]));
-        }
-      } else if (a.z_final != nullptr) {
-        a.z_final[bh * D + er] = __uint_as_float(u[0]);
+      for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(v[e]);
+      tc::tmem_st16(tmem + tl + L::TS + j0, u);
+      if (er < D) {
+        const uint32_t blk = base + L::SS + static_cast<uint32_t>(j0 / 64) * (D * 128);
+        const int cc = (j0 % 64) / 8;
+        sts16(blk + tc::sw128(er, cc), pack8(v));
+        sts16(blk + tc::sw128(er, cc + 1), pack8(v + 8));
       }
     }
+    tc::tmem_wait_st();
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    tc::named_sync(kBarCons, kCons);
+    if (q4 == 0 && lane == 0) atomicExch(s_ready, 1);  // the issuer may start
+
+    __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out);
+    int bad = 0;
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c & 1;
+      // ---- S (this chunk's state) -> bf16 S~ for the next chunk; the serial step comes first
+      int ok = tc::mbar_wait(bar_s, c & 1, kWaitCycles);
+      if (__any_sync(0xffffffffu, !ok)) bad = 1;  // warp-uniform, so TMEM loads stay converged
+      tc::fence_after_sync();
+      if (!bad && 32 * q4 < D) {
+#pragma unroll 1
+        for (int j0 = 0; j0 < D; j0 += 32) {
+          uint32_t u[2][16];
+          tc::tmem_ld16(tmem + tl + L::TS + j0, u[0]);
+          tc::tmem_ld16(tmem + tl + L::TS + j0 + 16, u[1]);
+          tc::tmem_wait_ld();
+          const uint32_t blk = base + L::SS + static_cast<uint32_t>(j0 / 64) * (D * 128);
+          const int cc = (j0 % 64) / 8;
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            float v[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(u[m][e]);
+            sts16(blk + tc::sw128(er, cc + 2 * m), pack8(v));
+            sts16(blk + tc::sw128(er, cc + 2 * m + 1), pack8(v + 8));
+          }
+        }
+      }
+      // ---- P -> masked bf16 P~ and its row sums (of the rounded values the numerator uses)
+      ok = tc::mbar_wait(bar_a, c & 1, kWaitCycles);
+      ok &= tc::mbar_wait(bar_full + 8 * s, (c >> 1) & 1, kWaitCycles);  // the q'.z values
+      if (__any_sync(0xffffffffu, !ok)) bad = 1;
+      tc::fence_after_sync();
+      float den = 1.f;
+      if (!bad) {
+        const uint32_t pb = D == 128 ? base + (s ? L::Q1 : L::Q0) : base + L::PS;
+        float rs = 0.f;
+#pragma unroll 1
+        for (int col = 0; col < kC; col += 32) {
+          uint32_t u[2][16];
+          tc::tmem_ld16(tmem + tl + L::TP + col, u[0]);
+          tc::tmem_ld16(tmem + tl + L::TP + col + 16, u[1]);
+          tc::tmem_wait_ld();
+          const uint32_t blk = pb + (col / 64) * 16384;
+          const int cc = (col % 64) / 8;
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int tau = col + 16 * m + 2 * e;
+              const float x0 = tau <= er ? __uint_as_float(u[m][2 * e]) : 0.f;
+              const float x1 = tau + 1 <= er ? __uint_as_float(u[m][2 * e + 1]) : 0.f;
+              w[e] = tc::pack_bf16x2(x0, x1);
+              const float2 r2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+              rs += r2.x + r2.y;
+            }
+            sts16(blk + tc::sw128(er, cc + 2 * m), make_uint4(w[0], w[1], w[2], w[3]));
+            sts16(blk + tc::sw128(er, cc + 2 * m + 1), make_uint4(w[4], w[5], w[6], w[7]));
+          }
+        }
+        den = di[s * kC + er] + rs + a.eps_den;
+      }
+      tc::fence_async_smem();
+      tc::fence_before_sync();
+      tc::mbar_arrive(bar_conv);
+      // ---- out = O / den
+      const int okb = tc::mbar_wait(bar_b, c & 1, kWaitCycles);
+      if (__any_sync(0xffffffffu, !okb)) bad = 1;
+      if (!bad) {
+        tc::fence_after_sync();
+        const uint32_t to = tmem + tl + (s ? L::TO1 : L::TO0);
+        const float inv = 1.0f / den;
+        const int lt = c * kC + er;
+        __nv_bfloat16* orow = og + ((row0 + seg_start + lt) * a.H + h) * D;
+#pragma unroll 1
+        for (int j0 = 0; j0 < D; j0 += 32) {
+          uint32_t u[2][16];
+          tc::tmem_ld16(to + j0, u[0]);
+          tc::tmem_ld16(to + j0 + 16, u[1]);
+          tc::tmem_wait_ld();
+          if (lt < seg_n) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + j0);
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              float f[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(u[m][e]) * inv;
+              dst[2 * m] = pack8(f);
+              dst[2 * m + 1] = pack8(f + 8);
+            }
+          }
+        }
+      }
+      tc::fence_before_sync();
+      if (bad) atomicExch(s_abort, 1);
+      if (group_sync_or(kBarCons, kCons, *s_abort)) break;
+    }
+    if (bad) atomicExch(s_abort, 1);
+    if (last_seg && a.S_final != nullptr && !*s_abort && 32 * q4 < D) {
+      tc::fence_after_sync();
+      for (int j0 = 0; j0 < D; j0 += 16) {
+        uint32_t u[16];
+        tc::tmem_ld16(tmem + tl + L::TS + j0, u);
+        tc::tmem_wait_ld();
+        float4* dst = reinterpret_cast<float4*>(a.S_final + (bh * D + er) * D + j0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          dst[e] = make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
+                               __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3]));
+      }
+    }
+  } else {
+    // ============================================================ MMA issue (one thread)
+    tc::regs_dec<kRegsIssueB>();
+    if (warp == (kProd + kCons) / 32 && lane == 0) {
+      constexpr uint32_t ID_P = tc::idesc_bf16(128, 128, false, false);
+      constexpr uint32_t ID_QS = tc::idesc_bf16(128, D, false, true);
+      constexpr uint32_t ID_KV = tc::idesc_bf16(128, D, true, true);
+      constexpr uint32_t ID_PV = tc::idesc_bf16(128, D, false, true);
+      const volatile int* ready = s_ready;
+      const long long t0 = clock64();
+      while (*ready == 0 && clock64() - t0 < kWaitCycles) {
+      }
+      int ok = *ready != 0;
+      // descriptors: k-major operands advance 32 bytes per K=16 step inside a 64-column block and
+      // 16 KB per block; MN-major operands advance 2 KB (16 rows) per step
+      const uint64_t d_ks_k = tc::desc_sw128(base + L::KS, 16, 1024);
+      const uint64_t d_ks_mn = tc::desc_sw128(base + L::KS, 16384, 1024);
+      const uint64_t d_ss = tc::desc_sw128(base + L::SS, D * 128, 1024);
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int s = c & 1, ph = (c >> 1) & 1;
+        const uint32_t qb = base + (s ? L::Q1 : L::Q0), vb = base + (s ? L::V1 : L::V0);
+        const uint32_t to = tmem + (s ? L::TO1 : L::TO0);
+        const uint64_t d_q = tc::desc_sw128(qb, 16, 1024);
+        const uint64_t d_v = tc::desc_sw128(vb, 16384, 1024);
+        ok = tc::mbar_wait(bar_full + 8 * s, ph, kWaitCycles) &&
+             tc::mbar_wait(bar_vfull + 8 * s, ph, kWaitCycles) &&
+             (c == 0 || tc::mbar_wait(bar_conv, (c - 1) & 1, kWaitCycles));
+        if (!ok) break;
+        tc::fence_after_sync();
+        // O = Q' S~_{c-1}, then S += K'^T V: the recurrence step; once both are done (s_done) S~
+        // may be overwritten with the new state
+#pragma unroll 1
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t kofs = static_cast<uint64_t>((k / 4) * 1024 + (k % 4) * 2);
+          tc::mma_bf16(to, d_q + kofs, d_ss + static_cast<uint64_t>(k) * 128, ID_QS, k > 0);
+        }
+#pragma unroll 1
+        for (int k = 0; k < kC / 16; ++k) {
+          tc::mma_bf16(tmem + L::TS, d_ks_mn + static_cast<uint64_t>(k) * 128,
+                       d_v + static_cast<uint64_t>(k) * 128, ID_KV, 1u);
+        }
+        tc::mma_commit(bar_s);
+        // P = Q' K'^T
+#pragma unroll 1
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t kofs = static_cast<uint64_t>((k / 4) * 1024 + (k % 4) * 2);
+          tc::mma_bf16(tmem + L::TP, d_q + kofs, d_ks_k + kofs, ID_P, k > 0);
+        }
+        tc::mma_commit(bar_a);
+        // O += P~ V once the consumers have written P~ (and S~, and read P and S)
+        ok = tc::mbar_wait(bar_conv, c & 1, kWaitCycles);
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint64_t d_p = tc::desc_sw128(D == 128 ? qb : base + L::PS, 16, 1024);
+#pragma unroll 1
+        for (int k = 0; k < kC / 16; ++k) {
+          const uint64_t kofs = static_cast<uint64_t>((k / 4) * 1024 + (k % 4) * 2);
+          tc::mma_bf16(to, d_p + kofs, d_v + static_cast<uint64_t>(k) * 128, ID_PV, 1u);
+        }
+        tc::mma_commit(bar_b);
+        tc::mma_commit(bar_empty + 8 * s);
+      }
+      if (!ok) atomicExch(s_abort, 1);
+    }
   }
+
   tc::fence_before_sync();
   __syncthreads();
+  if (*s_abort) {
+    if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, kDevInternal);
+    // a bounded chance for MMAs still in flight to land before TMEM is released
+    if (tid == 0) tc::mbar_wait(bar_b, 0, kWaitCycles / 4);
+    __syncthreads();
+  }
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
 // ------------------------------------------------------------------------------------------------
-// Kernel A: state increment [S | z] of one segment (every segment but a document's last).
+// Kernel A: state increment (K'^T V and the column sums of k') of one segment (every segment of a
+// document but its last). 16 producer warps fill one of two k' buffers (v arrives by TMA) while
+// the tensor core, fed by a dedicated issuer thread, accumulates the other into TMEM.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) segment_state_kernel(const TcArgs ta) {
-  using Cfg = TcCfg<D>;
-  using CA = TcCfgA<D>;
-  constexpr int NA = Cfg::NA, TPR = Cfg::TPR, RPP = Cfg::RPP, NPASS = Cfg::NPASS;
+__global__ void __launch_bounds__(kThreadsA, 1)
+    segment_state_kernel(const TcArgs ta, const __grid_constant__ CUtensorMap tmap_v) {
+  using L = LayA<D>;
+  using PM = Prod<D>;
+  constexpr int TPR = PM::TPR, RPP = PM::RPP, NPASS = PM::NPASS, RING = PM::RING;
   const PrefillArgs& a = ta.p;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -548,131 +782,169 @@ __global__ void __launch_bounds__(kThreads, 1) segment_state_kernel(const TcArgs
   const int nseg_doc = n > 0 ? (n + ta.seg_len - 1) / ta.seg_len : 1;
   if (seg >= nseg_doc - 1) return;  // the last segment's increment is not needed
   const int seg_start = seg * ta.seg_len;
-  const int seg_n = ta.seg_len;  // a non-last segment is full
+  const int nchunks = ta.seg_len / kC;  // a non-last segment is full
 
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = tc::smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t bar = base + CA::CTRL;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(gbase + CA::CTRL + 16);
-  int* s_abort = reinterpret_cast<int*>(gbase + CA::CTRL + 20);
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t base = tc::smem_u32(smem);
+  if (base & 1023u) {
+    if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, kDevInternal);
+    return;
+  }
+  float* zp = reinterpret_cast<float*>(smem + L::ZP);
+  const uint32_t bar_full = base + L::BAR, bar_empty = bar_full + 16, bar_vfull = bar_full + 32;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::MISC);
+  int* s_abort = reinterpret_cast<int*>(smem + L::MISC + 4);
 
   if (warp == 0) {
-    tc::tmem_alloc(tc::smem_u32(s_tmem), 256);
+    tc::tmem_alloc(tc::smem_u32(s_tmem), 128);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    tc::mbar_init(bar, 1);
+    tc::mbar_init(bar_full, kProd);
+    tc::mbar_init(bar_full + 8, kProd);
+    tc::mbar_init(bar_empty, 1);
+    tc::mbar_init(bar_empty + 8, 1);
+    tc::mbar_init(bar_vfull, 1);
+    tc::mbar_init(bar_vfull + 8, 1);
     tc::mbar_fence_init();
     *s_abort = 0;
+    *reinterpret_cast<int*>(smem + L::MISC + 8) = 0;
   }
-  for (int idx = tid; idx < 16384 / 16; idx += kThreads) {
-    const int r = idx / 8, c = idx % 8;
-    const uint32_t one = (c == 0) ? 0x3F80u : 0u;
-    sts16(base + CA::VS + CA::KB * 16384 + tc::sw128(r, c), make_uint4(one, 0u, 0u, 0u));
-    if (D == 64) sts16(base + CA::KS + 16384 + idx * 16, make_uint4(0u, 0u, 0u, 0u));
+  if (D == 64) {
+    for (int i = tid; i < 16384 / 16; i += kThreadsA) {
+      sts16(base + L::K0 + 16384 + i * 16, make_uint4(0, 0, 0, 0));
+      sts16(base + L::K1 + 16384 + i * 16, make_uint4(0, 0, 0, 0));
+    }
   }
+  const FeatTab tab = feat_tab<D>(smem + L::TAB);
+  fill_tab<D>(tab, a, h, RPP, tid, kThreadsA);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *s_tmem;
+  const long bh = static_cast<long>(doc) * a.H + h;
+  float* dst = ta.ws + (bh * ta.nseg_max + seg) * static_cast<long>(D) * (D + kPad);
 
-  const int prow = tid / TPR, part = tid % TPR;
-  const int e0 = 16 * part;
-  float gk[16], fhi[8], flo[8];
-  {
-    const float* gkp = a.gamma_k + h * a.fa.gamma_stride;
+  if (warp < kProd / 32) {
+    tc::regs_inc<kRegsProdA>();
+    const int prow = tid / TPR, part = tid % TPR, e0 = 8 * part;
+    const uint32_t cblk = static_cast<uint32_t>(e0 / 64) * 16384;
+    const int cidx = (e0 % 64) / 8;
+    float2 gk0[2], gk1[2];
+    tab_gamma(tab.gk, e0, gk0, gk1);
+    Rot step;
+    tab_step(tab, e0 / 2, step);
+    const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(a.k);
+    const int pos_base = a.pos_offset + seg_start;
+    auto load = [&](int c, int p, uint4& xk) {
+      xk = ldg16(kg + ((row0 + seg_start + c * kC + p * RPP + prow) * a.H + h) * D + e0);
+    };
+    float2 zca[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float2 zcb[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    uint4 rk[RING];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) gk[e] = gkp[e0 + e];
+    for (int p = 0; p < RING; ++p) load(0, p, rk[p]);
+    int bad = 0;
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c & 1;
+      if (c >= 2 && !tc::mbar_wait(bar_empty + 8 * s, ((c >> 1) + 1) & 1, kWaitCycles)) bad = 1;
+      const uint32_t kb = base + (s ? L::K1 : L::K0), vb = base + (s ? L::V1 : L::V0);
+      if (tid == 0) {
+        tc::mbar_arrive_expect_tx(bar_vfull + 8 * s, L::TILE);
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      fhi[m] = a.fa.rope_hi[(e0 >> 1) + m];
-      flo[m] = a.fa.rope_lo[(e0 >> 1) + m];
-    }
-  }
-  const uint32_t pro_off = static_cast<uint32_t>(part / 4) * 16384;
-  const int pro_c = (part % 4) * 2;
-  const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(a.k);
-  const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(a.v);
-  const int pos_base = a.pos_offset + seg_start;
-
-  uint4 rk[NPASS][2], rv[NPASS][2];
-  auto prefetch = [&](int t0) {
-#pragma unroll
-    for (int p = 0; p < NPASS; ++p) {
-      const int lt = t0 + p * RPP + prow;
-      const long off = ((row0 + seg_start + lt) * a.H + h) * D + e0;
-      rk[p][0] = ldg16(kg + off);
-      rk[p][1] = ldg16(kg + off + 8);
-      rv[p][0] = ldg16(vg + off);
-      rv[p][1] = ldg16(vg + off + 8);
-    }
-  };
-  constexpr uint32_t ID_KV = tc::idesc_bf16(128, NA, true, true);
-  uint32_t phase = 0;
-  bool aborted = false;
-  prefetch(0);
-  for (int t0 = 0; t0 < seg_n; t0 += kC) {
-#pragma unroll
-    for (int p = 0; p < NPASS; ++p) {
-      const int r = p * RPP + prow;
-      uint4 ok[2];
-      features16_k<D>(rk[p], true, pos_base + t0 + r, gk, fhi, flo, a.fa.eps_norm, ok);
-      sts16(base + CA::KS + pro_off + tc::sw128(r, pro_c), ok[0]);
-      sts16(base + CA::KS + pro_off + tc::sw128(r, pro_c + 1), ok[1]);
-      sts16(base + CA::VS + pro_off + tc::sw128(r, pro_c), rv[p][0]);
-      sts16(base + CA::VS + pro_off + tc::sw128(r, pro_c + 1), rv[p][1]);
-    }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-      tc::fence_after_sync();
-#pragma unroll
-      for (int s = 0; s < kC / 16; ++s) {
-        tc::mma_bf16(tmem, tc::desc_sw128(base + CA::KS + s * 2048, 16384, 1024),
-                     tc::desc_sw128(base + CA::VS + s * 2048, 16384, 1024), ID_KV,
-                     (t0 > 0 || s > 0) ? 1u : 0u);
+        for (int jb = 0; jb < D / 64; ++jb)
+          tc::tma_load_3d(vb + jb * 16384, &tmap_v, 64 * jb, h,
+                          static_cast<int>(row0 + seg_start + c * kC), bar_vfull + 8 * s);
       }
-      tc::mma_commit(bar);
-    }
-    if (t0 + kC < seg_n) prefetch(t0 + kC);
-    if (!tc::mbar_wait(bar, phase, kWaitCycles)) *s_abort = 1;
-    __syncthreads();
-    if (*s_abort) {
-      aborted = true;
-      break;
-    }
-    phase ^= 1;
-  }
-
-  const int q4 = warp & 3, hf = warp >> 2;
-  const int er = 32 * q4 + lane;
-  const uint32_t tlane = static_cast<uint32_t>(32 * q4) << 16;
-  if (aborted) {
-    if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, kDevTimeout);
-    tc::mbar_wait(bar, phase, kWaitCycles);
-  } else if (32 * q4 < D) {
-    tc::fence_after_sync();
-    const long bh = static_cast<long>(doc) * a.H + h;
-    float* dst = ta.ws + ((bh * ta.nseg_max + seg) * D + er) * static_cast<long>(D + 1);
-    for (int g = 0; g < StateCols<D>::count(hf); ++g) {
-      const int j0 = StateCols<D>::col(hf, g);
-      uint32_t u[16];
-      tc::tmem_ld16(tmem + tlane + j0, u);
-      tc::tmem_wait_ld();
-      if (j0 < D) {
+      Rot rot;
+      tab_rot_at(tab, pos_base + c * kC + prow, e0 / 2, rot);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) dst[j0 + e] = __uint_as_float(u[e]);
-      } else {
-        dst[D] = __uint_as_float(u[0]);
+      for (int p = 0; p < NPASS; ++p) {
+        const uint4 xk = rk[p % RING];
+        if (p + RING < NPASS) load(c, p + RING, rk[p % RING]);
+        else if (c + 1 < nchunks) load(c + 1, p + RING - NPASS, rk[p % RING]);
+        const int r = p * RPP + prow;
+        if (p > 0) rot_step(rot, step);
+        Pairs fk = unpack_pairs(xk);
+        const float sk = row_sum<TPR>(sumsq(fk));
+        rope_relu(fk, gk0, gk1, rot, rsqrtf(sk * (1.0f / D) + a.fa.eps_norm));
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          zca[g] = __fadd2_rn(zca[g], fk.x0[g]);
+          zcb[g] = __fadd2_rn(zcb[g], fk.x1[g]);
+        }
+        sts16(kb + cblk + tc::sw128(r, cidx), pack_pairs(fk));
+      }
+      tc::fence_async_smem();
+      tc::mbar_arrive(bar_full + 8 * s);
+      if (bad) atomicExch(s_abort, 1);
+      if (group_sync_or(kBarProd, kProd, *s_abort)) break;
+    }
+    // sums of k' over the segment (fixed order: deterministic)
+    float zc[8];
+    pairs_to8(Pairs{{zca[0], zca[1]}, {zcb[0], zcb[1]}}, zc);
+    warp_colsum<TPR>(zc);
+    if (lane < TPR) {
+      *reinterpret_cast<float4*>(zp + warp * D + e0) = make_float4(zc[0], zc[1], zc[2], zc[3]);
+      *reinterpret_cast<float4*>(zp + warp * D + e0 + 4) = make_float4(zc[4], zc[5], zc[6], zc[7]);
+    }
+    tc::named_sync(kBarProd, kProd);
+    if (tid < D && !*s_abort) {
+      float z = 0.f;
+#pragma unroll
+      for (int w = 0; w < PM::WARPS; ++w) z += zp[w * D + tid];
+      dst[static_cast<long>(tid) * (D + kPad) + D] = z;
+    }
+  } else {
+    tc::regs_dec<kRegsIssueA>();
+    const int q4 = warp & 3;
+    if (warp == kProd / 32 && lane == 0) {
+      constexpr uint32_t ID_KV = tc::idesc_bf16(128, D, true, true);
+      int ok = 1;
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int s = c & 1, ph = (c >> 1) & 1;
+        const uint32_t kb = base + (s ? L::K1 : L::K0), vb = base + (s ? L::V1 : L::V0);
+        ok = tc::mbar_wait(bar_full + 8 * s, ph, kWaitCycles) &&
+             tc::mbar_wait(bar_vfull + 8 * s, ph, kWaitCycles);
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint64_t d_k = tc::desc_sw128(kb, 16384, 1024), d_v = tc::desc_sw128(vb, 16384, 1024);
+#pragma unroll 1
+        for (int k = 0; k < kC / 16; ++k)
+          tc::mma_bf16(tmem, d_k + static_cast<uint64_t>(k) * 128, d_v + static_cast<uint64_t>(k) * 128,
+                       ID_KV, (c > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit(bar_empty + 8 * s);
+      }
+      // the last accumulation
+      const int last = nchunks - 1;
+      if (ok) ok = tc::mbar_wait(bar_empty + 8 * (last & 1), (last >> 1) & 1, kWaitCycles);
+      if (!ok) atomicExch(s_abort, 1);
+      *reinterpret_cast<volatile int*>(smem + L::MISC + 8) = 1;  // accumulation complete
+    }
+    __syncwarp();
+    // the issuer warpgroup copies the increment out of TMEM (one lane quarter per warp)
+    const volatile int* done = reinterpret_cast<const volatile int*>(smem + L::MISC + 8);
+    const long long t0 = clock64();
+    while (*done == 0 && clock64() - t0 < kWaitCycles) {
+    }
+    const int go = __all_sync(0xffffffffu, *done != 0 && *s_abort == 0);
+    if (go && 32 * q4 < D) {
+      tc::fence_after_sync();
+      const int er = 32 * q4 + lane;
+      const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
+      for (int j0 = 0; j0 < D; j0 += 16) {
+        uint32_t u[16];
+        tc::tmem_ld16(tmem + tl + j0, u);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) dst[static_cast<long>(er) * (D + kPad) + j0 + e] = __uint_as_float(u[e]);
       }
     }
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+  if (*s_abort && tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, kDevInternal);
+  if (warp == 0) tc::tmem_dealloc(tmem, 128);
 }
 
 template <typename K>
@@ -686,22 +958,54 @@ cudaError_t set_smem(K kernel, uint32_t bytes, unsigned long long& configured) {
   return e;
 }
 
+// Tensor map of v ([rows, H, D] bf16, rows = B * L or T) with 64 x 1 x 128 boxes, 128-byte swizzle:
+// one box is one 64-column block of a chunk's v operand.
+cudaError_t make_v_map(CUtensorMap* map, const void* v, long rows, int H, int D) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return e != cudaSuccess ? e : cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kC)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(v), dims,
+                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int D>
 cudaError_t launch_tc_d(const TcArgs& ta, cudaStream_t stream) {
   static unsigned long long cfg_a = 0, cfg_b = 0;
-  cudaError_t e = set_smem(prefill_tc_kernel<D>, TcCfg<D>::BYTES, cfg_b);
+  cudaError_t e = set_smem(prefill_tc_kernel<D>, LayB<D>::BYTES, cfg_b);
   if (e != cudaSuccess) return e;
-  e = set_smem(segment_state_kernel<D>, TcCfgA<D>::BYTES, cfg_a);
+  e = set_smem(segment_state_kernel<D>, LayA<D>::BYTES, cfg_a);
   if (e != cudaSuccess) return e;
   const long units = static_cast<long>(ta.p.n_docs) * ta.p.H;
   if (units == 0) return cudaSuccess;
+  CUtensorMap tmap_v;
+  if (ta.p.v != nullptr && ta.p.total_rows > 0) {
+    e = make_v_map(&tmap_v, ta.p.v, ta.p.total_rows, ta.p.H, D);
+    if (e != cudaSuccess) return e;
+  } else {
+    memset(&tmap_v, 0, sizeof(tmap_v));  // no rows: the kernels issue no copy
+  }
   if (ta.nseg_max > 1) {
-    segment_state_kernel<D><<<static_cast<unsigned>(units * ta.nseg_max), kThreads, TcCfgA<D>::BYTES, stream>>>(ta);
+    segment_state_kernel<D><<<static_cast<unsigned>(units * ta.nseg_max), kThreadsA, LayA<D>::BYTES, stream>>>(ta, tmap_v);
     note_launches(1);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  prefill_tc_kernel<D><<<static_cast<unsigned>(units * ta.nseg_max), kThreads, TcCfg<D>::BYTES, stream>>>(ta);
+  prefill_tc_kernel<D><<<static_cast<unsigned>(units * ta.nseg_max), kThreadsB, LayB<D>::BYTES, stream>>>(ta, tmap_v);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -712,10 +1016,10 @@ bool tc_supported(DType dt, int d) { return dt == DType::BF16 && (d == 64 || d =
 
 TcPlan tc_plan(int n_docs, int H, int max_seqlen, long total_tokens, int d) {
   // Estimated time in units of one kernel-B chunk. Kernel B runs one CTA per SM (waves of 152
-  // CTAs, each CTA costing its chunks plus about one chunk of state set-up); a kernel-A chunk
-  // (k features + one GEMM) costs about 0.4 of a kernel-B chunk and kernel A fits two CTAs per
-  // SM. Documents are assumed to share the tokens evenly, except that the longest one bounds the
-  // segment count. The segment length with the smallest estimate wins.
+  // CTAs, each costing its chunks plus about one chunk of state set-up); a kernel-A chunk (k
+  // features and one GEMM) costs about half a kernel-B chunk, also one CTA per SM. Documents are
+  // assumed to share the tokens evenly, except that the longest one bounds the segment count.
+  // More segments cost workspace, so a longer plan must be clearly (5 %) faster to win.
   TcPlan best{1, kC, 0};
   const int chunks_max = max_seqlen > 0 ? (max_seqlen + kC - 1) / kC : 1;
   const double avg_chunks = n_docs > 0 ? static_cast<double>(total_tokens) / n_docs / kC : 0.0;
@@ -729,9 +1033,9 @@ TcPlan tc_plan(int n_docs, int H, int max_seqlen, long total_tokens, int d) {
     const double items_b = static_cast<double>(H) * n_docs * (segs_per_doc > 1 ? segs_per_doc : 1.0);
     const double items_a = items_b - static_cast<double>(H) * n_docs;
     const double waves_b = static_cast<double>(static_cast<long>((items_b + 151) / 152));
-    const double waves_a = items_a > 0 ? static_cast<double>(static_cast<long>((items_a + 303) / 304)) : 0.0;
-    const double cost = waves_b * (seg_chunks + 1.0) + 0.4 * waves_a * seg_chunks;
-    if (cost < 0.95 * best_cost) {  // more segments cost workspace: demand a clear gain
+    const double waves_a = items_a > 0 ? static_cast<double>(static_cast<long>((items_a + 151) / 152)) : 0.0;
+    const double cost = waves_b * (seg_chunks + 1.0) + 0.5 * waves_a * seg_chunks;
+    if (cost < 0.95 * best_cost) {
       best_cost = cost;
       best.nseg_max = nseg;
       best.seg_len = seg_chunks * kC;
@@ -739,7 +1043,7 @@ TcPlan tc_plan(int n_docs, int H, int max_seqlen, long total_tokens, int d) {
   }
   const long units = static_cast<long>(n_docs) * H;
   best.ws_bytes = best.nseg_max > 1
-                      ? static_cast<size_t>(units) * best.nseg_max * d * (d + 1) * sizeof(float)
+                      ? static_cast<size_t>(units) * best.nseg_max * d * (d + kPad) * sizeof(float)
                       : 0;
   return best;
 }
