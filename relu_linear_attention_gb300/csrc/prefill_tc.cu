@@ -260,20 +260,12 @@ __device__ __forceinline__ void pairs_to8(const Pairs& p, float* f) {
   }
 }
 
-// Gains of a thread's 8 elements in pair groups.
-__device__ __forceinline__ void load_gamma(const float* gp, float2 (&g0)[2], float2 (&g1)[2]) {
-  const float4 a = *reinterpret_cast<const float4*>(gp);
-  const float4 b = *reinterpret_cast<const float4*>(gp + 4);
-  g0[0] = make_float2(a.x, a.z);
-  g1[0] = make_float2(a.y, a.w);
-  g0[1] = make_float2(b.x, b.z);
-  g1[1] = make_float2(b.y, b.w);
-}
-
 // Per-CTA feature constants in shared memory (8 * D floats), so that the producers need no
 // registers for them and no lane-divergent reads of the kernel parameters: the gains of q and k,
 // and for every RoPE pair the frequency (hi, lo turns) and the cos / sin of the rotation over
-// one producer pass (RPP positions).
+// one producer pass (RPP positions). Gains are stored "split": the first 4 of a thread's 8
+// values for every thread part, then the last 4, so that a warp's 16-byte reads are contiguous
+// (no bank conflicts); split_idx maps an element index to that layout.
 struct FeatTab {
   float* gq;   // [D]
   float* gk;   // [D]
@@ -288,11 +280,15 @@ __device__ __forceinline__ FeatTab feat_tab(uint8_t* p) {
   return FeatTab{f, f + D, f + 2 * D, f + 2 * D + D / 2, f + 3 * D, f + 3 * D + D / 2};
 }
 template <int D>
+__device__ __forceinline__ int split_idx(int i) {
+  return (i & 4) * (D / 8) + (i >> 3) * 4 + (i & 3);
+}
+template <int D>
 __device__ __forceinline__ void fill_tab(const FeatTab& t, const PrefillArgs& a, int h, int rpp,
                                          int tid, int nthreads) {
   for (int i = tid; i < D; i += nthreads) {
-    t.gq[i] = a.gamma_q[h * a.fa.gamma_stride + i];
-    t.gk[i] = a.gamma_k[h * a.fa.gamma_stride + i];
+    t.gq[split_idx<D>(i)] = a.gamma_q[h * a.fa.gamma_stride + i];
+    t.gk[split_idx<D>(i)] = a.gamma_k[h * a.fa.gamma_stride + i];
   }
   for (int j = tid; j < D / 2; j += nthreads) {
     t.fhi[j] = a.fa.rope_hi[j];
@@ -303,9 +299,15 @@ __device__ __forceinline__ void fill_tab(const FeatTab& t, const PrefillArgs& a,
     t.sts[j] = sn;
   }
 }
-// Gains / rotation step of a thread's 8 elements (pairs j0 .. j0+3) from the tables.
-__device__ __forceinline__ void tab_gamma(const float* g, int e0, float2 (&g0)[2], float2 (&g1)[2]) {
-  load_gamma(g + e0, g0, g1);
+// Two float4 halves of a thread's 8 values in a split table, in pair groups.
+template <int D>
+__device__ __forceinline__ void split_load(const float* t, int part, float2 (&x0)[2], float2 (&x1)[2]) {
+  const float4 a = *reinterpret_cast<const float4*>(t + 4 * part);
+  const float4 b = *reinterpret_cast<const float4*>(t + D / 2 + 4 * part);
+  x0[0] = make_float2(a.x, a.z);
+  x1[0] = make_float2(a.y, a.w);
+  x0[1] = make_float2(b.x, b.z);
+  x1[1] = make_float2(b.y, b.w);
 }
 __device__ __forceinline__ void tab_step(const FeatTab& t, int j0, Rot& st) {
   const float4 c = *reinterpret_cast<const float4*>(t.stc + j0);
@@ -412,7 +414,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     for (int i = tid; i < D; i += kProd) {
       float z = a.z0 != nullptr ? a.z0[bh * D + i] : 0.f;
       for (int g = 0; g < seg; ++g) z += wsb[(static_cast<long>(g) * D + i) * (D + kPad) + D];
-      zs[i] = z;
+      zs[split_idx<D>(i)] = z;
     }
     tc::named_sync(kBarProd, kProd);
 
@@ -473,15 +475,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         const float rinvk = valid ? rsqrtf(sk * (1.0f / D) + a.fa.eps_norm) : 0.f;
         {
           float2 g0[2], g1[2];
-          tab_gamma(tab.gq, e0, g0, g1);
+          split_load<D>(tab.gq, part, g0, g1);
           rope_relu(fq, g0, g1, rot, rinvq);
-          tab_gamma(tab.gk, e0, g0, g1);
+          split_load<D>(tab.gk, part, g0, g1);
           rope_relu(fk, g0, g1, rot, rinvk);
         }
-        const float4 z4a = *reinterpret_cast<const float4*>(zs + e0);
-        const float4 z4b = *reinterpret_cast<const float4*>(zs + e0 + 4);
-        const float2 zfa[2] = {make_float2(z4a.x, z4a.z), make_float2(z4b.x, z4b.z)};  // first elements
-        const float2 zfb[2] = {make_float2(z4a.y, z4a.w), make_float2(z4b.y, z4b.w)};  // second
+        float2 zfa[2], zfb[2];  // z of the pairs' first / second elements
+        split_load<D>(zs, part, zfa, zfb);
         float2 d2 = __fmul2_rn(fq.x0[0], zfa[0]);
         d2 = __ffma2_rn(fq.x1[0], zfb[0], d2);
         d2 = __ffma2_rn(fq.x0[1], zfa[1], d2);
@@ -513,15 +513,15 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       if (bad) atomicExch(s_abort, 1);
       tc::named_sync(kBarProd, kProd);
       if (tid < D) {
-        float z = zs[tid];
+        float z = zs[split_idx<D>(tid)];
 #pragma unroll
         for (int w = 0; w < PM::WARPS; ++w) z += zp[w * D + tid];
-        zs[tid] = z;
+        zs[split_idx<D>(tid)] = z;
       }
       if (group_sync_or(kBarProd, kProd, *s_abort)) break;
     }
     if (last_seg && a.z_final != nullptr && !*s_abort) {
-      for (int i = tid; i < D; i += kProd) a.z_final[bh * D + i] = zs[i];
+      for (int i = tid; i < D; i += kProd) a.z_final[bh * D + i] = zs[split_idx<D>(i)];
     }
   } else if (warp < (kProd + kCons) / 32) {
     // ============================================================ consumers
@@ -608,22 +608,34 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       if (!bad) {
         const uint32_t pb = D == 128 ? base + (s ? L::Q1 : L::Q0) : base + L::PS;
         float rs = 0.f;
+        // Column groups of 32 scores: those left of this warp's rows (col < 32 q4) are fully
+        // visible, the group col == 32 q4 holds the diagonal, the rest are above it (all zero).
 #pragma unroll 1
         for (int col = 0; col < kC; col += 32) {
+          const uint32_t blk = pb + (col / 64) * 16384;
+          const int cc = (col % 64) / 8;
+          if (col > 32 * q4) {  // warp-uniform: strictly above the diagonal
+#pragma unroll
+            for (int m = 0; m < 4; ++m) sts16(blk + tc::sw128(er, cc + m), make_uint4(0, 0, 0, 0));
+            continue;
+          }
           uint32_t u[2][16];
           tc::tmem_ld16(tmem + tl + L::TP + col, u[0]);
           tc::tmem_ld16(tmem + tl + L::TP + col + 16, u[1]);
           tc::tmem_wait_ld();
-          const uint32_t blk = pb + (col / 64) * 16384;
-          const int cc = (col % 64) / 8;
+          const bool diag = col == 32 * q4;
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
             uint32_t w[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const int tau = col + 16 * m + 2 * e;
-              const float x0 = tau <= er ? __uint_as_float(u[m][2 * e]) : 0.f;
-              const float x1 = tau + 1 <= er ? __uint_as_float(u[m][2 * e + 1]) : 0.f;
+              float x0 = __uint_as_float(u[m][2 * e]);
+              float x1 = __uint_as_float(u[m][2 * e + 1]);
+              if (diag) {
+                x0 = tau <= er ? x0 : 0.f;
+                x1 = tau + 1 <= er ? x1 : 0.f;
+              }
               w[e] = tc::pack_bf16x2(x0, x1);
               const float2 r2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
               rs += r2.x + r2.y;
@@ -831,7 +843,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     const uint32_t cblk = static_cast<uint32_t>(e0 / 64) * 16384;
     const int cidx = (e0 % 64) / 8;
     float2 gk0[2], gk1[2];
-    tab_gamma(tab.gk, e0, gk0, gk1);
+    split_load<D>(tab.gk, part, gk0, gk1);
     Rot step;
     tab_step(tab, e0 / 2, step);
     const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(a.k);
