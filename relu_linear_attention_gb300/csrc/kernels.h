@@ -46,10 +46,13 @@ struct PrefillArgs {
 cudaError_t launch_prefill_simt(DType dt, int d, const PrefillArgs& a, cudaStream_t stream);
 
 // Tensor-core (tcgen05) chunked prefill for bf16 and d in {64, 128}. Documents are cut into
-// nseg_max segments of seg_len tokens; ws_bytes of workspace hold the segment state increments.
+// nseg_max segments of seg_len tokens; the state increments of every segment but a document's
+// last are computed first, in blocks of seg_len / blk_per_seg tokens, and ws_bytes of workspace
+// hold them.
 struct TcPlan {
   int nseg_max;
   int seg_len;
+  int blk_per_seg;
   size_t ws_bytes;
 };
 bool tc_supported(DType dt, int d);

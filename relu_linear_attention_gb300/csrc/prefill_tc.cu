@@ -29,7 +29,7 @@
 // into the swizzled operand layout, one chunk ahead. q and k go through registers (a short load
 // ring) because the features are computed on the way.
 // Hand-offs go through mbarriers: full[2] (producers -> issuer), vfull[2] (TMA -> issuer),
-// empty[2] (B(c) done -> buffer free), s_done / a_done / b_done (tensor core -> consumers),
+// empty[2] (output of chunk c staged and stored -> its buffers free), s_done / a_done / b_done (tensor core -> consumers),
 // conv_done (consumers -> issuer: S~ and P~ written, S and P read). The recurrence step of chunk c
 // (O = Q'S~, then S += K'^T V) is issued first and committed on its own (s_done), so turning S
 // into the next chunk's operand, the one serial dependency between chunks, starts early.
@@ -37,9 +37,13 @@
 // and the CTA winds down.
 //
 // Sequence parallelism: a document is cut into segments of seg_len tokens. Kernel A computes the
-// state increment (K'^T V and sum k') of every segment but the last; kernel B runs one CTA per
-// (document, head, segment) starting from S0 + the increments of the earlier segments (added in
-// segment order: deterministic). The last segment's CTA writes the final state.
+// state increments (K'^T V and sum k') of the parts of the document that precede its last
+// segment, in blocks of blk_len tokens (a segment holds blk_per_seg blocks, so that kernel A has
+// enough CTAs to fill the GPU); kernel B runs one CTA per (document, head, segment) starting from
+// S0 + the increments of the blocks before the segment (added in block order: deterministic). The
+// last segment's CTA writes the final state. Kernel B is launched as a programmatic dependent of
+// kernel A: its CTAs set up and compute their first features while kernel A finishes, and wait
+// for it only where they read the increments.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -59,7 +63,16 @@ constexpr int kThreadsA = kProd + 128;          // kernel A: producers + issuer 
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s: a tensor-core step that is not done by then never will be
 constexpr uint32_t kDevInternal = 2u;
 constexpr uint32_t kBarProd = 1, kBarCons = 2;   // named barriers of the producer / consumer groups
-constexpr int kPad = 4;  // segment-increment rows are D + 4 floats (16-byte aligned; column D = z)
+constexpr uint32_t kBarInit = 3;                 // consumer + issuer warpgroups after the state set-up
+
+// One increment record: K'^T V of a block as D/4 column groups of [D rows][4 columns] (the float4
+// of row r and columns 4j..4j+3 at float4 index j * D + r, so that 32 threads reading their rows'
+// same 4 columns read 512 contiguous bytes), then the block's column sums of k' (D floats).
+template <int D>
+struct Rec {
+  static constexpr long FLOATS = static_cast<long>(D) * (D + 1);
+  static constexpr long Z = static_cast<long>(D) * D;
+};
 
 // Register splits (setmaxnreg draws on the launch allocation: threads x launch registers).
 constexpr int kLaunchRegsB = 80, kRegsProdB = 88, kRegsConsB = 64, kRegsIssueB = 64;
@@ -119,9 +132,12 @@ struct LayA {
 
 struct TcArgs {
   PrefillArgs p;
-  float* ws;     // segment increments [n_docs][H][nseg_max][D][D + 4] (column D = sum of k')
-  int seg_len;   // tokens per segment (multiple of kC)
-  int nseg_max;  // segments per document slot in the grid
+  float* ws;        // increment records [n_docs][H][nblk_max] (Rec layout)
+  int seg_len;      // tokens per segment (multiple of blk_len)
+  int nseg_max;     // segments per document slot in the grid of kernel B
+  int blk_len;      // tokens per increment block (multiple of kC)
+  int blk_per_seg;  // seg_len / blk_len
+  int nblk_max;     // increment blocks per document slot: (nseg_max - 1) * blk_per_seg
 };
 
 __device__ __forceinline__ uint4 ldg16(const void* p) {
@@ -331,11 +347,71 @@ __device__ __forceinline__ void tab_rot_at(const FeatTab& t, int pos, int j0, Ro
   r.s[1] = make_float2(s2, s3);
 }
 
+// Initial state of a segment for columns [c0, c0 + D/2) of the calling thread's TMEM lane er:
+// S0 (if any) + the increments of the first nblk blocks, in block order, into the fp32 state in
+// TMEM (tmem_s: lane and column base of S) and its bf16 copy S~ in shared memory (ss); TMEM rows
+// >= D are zeroed. Two blocks are loaded at a time to keep more loads in flight.
+template <int D>
+__device__ __forceinline__ void init_state(const PrefillArgs& a, const float* wsb, int nblk, long bh,
+                                           int er, uint32_t tmem_s, uint32_t ss, int c0) {
+  for (int j0 = c0; j0 < c0 + D / 2; j0 += 16) {
+    float v[16];
+    uint32_t u[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = 0.f;
+    if (er < D) {
+      if (a.S0 != nullptr) {
+        const float4* src = reinterpret_cast<const float4*>(a.S0 + (bh * D + er) * D + j0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float4 x = src[e];
+          v[4 * e] += x.x; v[4 * e + 1] += x.y; v[4 * e + 2] += x.z; v[4 * e + 3] += x.w;
+        }
+      }
+      const float4* inc = reinterpret_cast<const float4*>(wsb) + (j0 / 4) * D + er;
+      constexpr long R4 = Rec<D>::FLOATS / 4;
+      int g = 0;
+      for (; g + 1 < nblk; g += 2) {
+        float4 x[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          x[e] = __ldcg(inc + g * R4 + e * D);
+          x[4 + e] = __ldcg(inc + (g + 1) * R4 + e * D);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int b = 4 * (e & 3);
+          v[b] += x[e].x; v[b + 1] += x[e].y; v[b + 2] += x[e].z; v[b + 3] += x[e].w;
+        }
+      }
+      if (g < nblk) {
+        float4 x[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = __ldcg(inc + g * R4 + e * D);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[4 * e] += x[e].x; v[4 * e + 1] += x[e].y; v[4 * e + 2] += x[e].z; v[4 * e + 3] += x[e].w;
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(v[e]);
+    tc::tmem_st16(tmem_s + j0, u);
+    if (er < D) {
+      const uint32_t blk = ss + static_cast<uint32_t>(j0 / 64) * (D * 128);
+      const int cc = (j0 % 64) / 8;
+      sts16(blk + tc::sw128(er, cc), pack8(v));
+      sts16(blk + tc::sw128(er, cc + 1), pack8(v + 8));
+    }
+  }
+}
+
 // ------------------------------------------------------------------------------------------------
 // Kernel B: one CTA per (document, head, segment).
 template <int D>
 __global__ void __launch_bounds__(kThreadsB, 1)
-    prefill_tc_kernel(const TcArgs ta, const __grid_constant__ CUtensorMap tmap_v) {
+    prefill_tc_kernel(const TcArgs ta, const __grid_constant__ CUtensorMap tmap_v,
+                      const __grid_constant__ CUtensorMap tmap_o) {
   using L = LayB<D>;
   using PM = Prod<D>;
   constexpr int TPR = PM::TPR, RPP = PM::RPP, NPASS = PM::NPASS, RING = PM::RING;
@@ -372,7 +448,6 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const uint32_t bar_conv = bar_full + 72;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::MISC);
   int* s_abort = reinterpret_cast<int*>(smem + L::MISC + 4);
-  int* s_ready = reinterpret_cast<int*>(smem + L::MISC + 8);
 
   if (warp == 0) {
     tc::tmem_alloc(tc::smem_u32(s_tmem), 512);
@@ -391,7 +466,6 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     tc::mbar_init(bar_conv, kCons);
     tc::mbar_fence_init();
     *s_abort = 0;
-    *s_ready = 0;
   }
   if (D == 64) {  // zero block that pads k'^T to M = 128 rows
     for (int i = tid; i < 16384 / 16; i += kThreadsB) sts16(base + L::KS + 16384 + i * 16, make_uint4(0, 0, 0, 0));
@@ -402,7 +476,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *s_tmem;
-  const float* wsb = ta.ws + bh * ta.nseg_max * static_cast<long>(D) * (D + kPad);
+  const float* wsb = ta.ws + bh * ta.nblk_max * Rec<D>::FLOATS;
+  const int nblk = seg * ta.blk_per_seg;  // increment blocks before this segment
 
   if (warp < kProd / 32) {
     // ============================================================ producers
@@ -410,10 +485,11 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const int prow = tid / TPR, part = tid % TPR, e0 = 8 * part;
     const uint32_t cblk = static_cast<uint32_t>(e0 / 64) * 16384;  // 64-column block
     const int cidx = (e0 % 64) / 8;                                 // 16-byte chunk in the row
-    // z at the segment start: z0 + the earlier segments' sums of k'
+    // z at the segment start: z0 + the earlier blocks' sums of k' (kernel A's output: wait for it)
+    if (nblk > 0) tc::grid_dep_wait();
     for (int i = tid; i < D; i += kProd) {
       float z = a.z0 != nullptr ? a.z0[bh * D + i] : 0.f;
-      for (int g = 0; g < seg; ++g) z += wsb[(static_cast<long>(g) * D + i) * (D + kPad) + D];
+      for (int g = 0; g < nblk; ++g) z += __ldcg(wsb + g * Rec<D>::FLOATS + Rec<D>::Z + i);
       zs[split_idx<D>(i)] = z;
     }
     tc::named_sync(kBarProd, kProd);
@@ -523,54 +599,22 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     if (last_seg && a.z_final != nullptr && !*s_abort) {
       for (int i = tid; i < D; i += kProd) a.z_final[bh * D + i] = zs[split_idx<D>(i)];
     }
-  } else if (warp < (kProd + kCons) / 32) {
-    // ============================================================ consumers
-    tc::regs_dec<kRegsConsB>();
+  } else {
+    // ============================================ consumers (warps 16-19), issuer warpgroup (20-23)
+    const bool cons = warp < (kProd + kCons) / 32;
+    if (cons) tc::regs_dec<kRegsConsB>();
+    else tc::regs_dec<kRegsIssueB>();
     const int q4 = warp & 3;                 // TMEM lane quarter
     const int er = 32 * q4 + lane;           // TMEM lane = tile row
     const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
-
-    // initial state S0 + earlier increments -> TMEM (fp32) and S~ (bf16); zero rows >= D
-    for (int j0 = 0; j0 < D; j0 += 16) {
-      float v[16];
-      uint32_t u[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) v[e] = 0.f;
-      if (er < D) {
-        if (a.S0 != nullptr) {
-          const float4* src = reinterpret_cast<const float4*>(a.S0 + (bh * D + er) * D + j0);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float4 x = src[e];
-            v[4 * e] += x.x; v[4 * e + 1] += x.y; v[4 * e + 2] += x.z; v[4 * e + 3] += x.w;
-          }
-        }
-        for (int g = 0; g < seg; ++g) {
-          const float4* src = reinterpret_cast<const float4*>(wsb + (static_cast<long>(g) * D + er) * (D + kPad) + j0);
-          float4 x[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) x[e] = __ldcg(src + e);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            v[4 * e] += x[e].x; v[4 * e + 1] += x[e].y; v[4 * e + 2] += x[e].z; v[4 * e + 3] += x[e].w;
-          }
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(v[e]);
-      tc::tmem_st16(tmem + tl + L::TS + j0, u);
-      if (er < D) {
-        const uint32_t blk = base + L::SS + static_cast<uint32_t>(j0 / 64) * (D * 128);
-        const int cc = (j0 % 64) / 8;
-        sts16(blk + tc::sw128(er, cc), pack8(v));
-        sts16(blk + tc::sw128(er, cc + 1), pack8(v + 8));
-      }
-    }
+    // initial state (the two warpgroups take half of the columns each)
+    if (nblk > 0) tc::grid_dep_wait();
+    init_state<D>(a, wsb, nblk, bh, er, tmem + tl + L::TS, base + L::SS, cons ? 0 : D / 2);
     tc::tmem_wait_st();
     tc::fence_async_smem();
     tc::fence_before_sync();
-    tc::named_sync(kBarCons, kCons);
-    if (q4 == 0 && lane == 0) atomicExch(s_ready, 1);  // the issuer may start
+    tc::named_sync(kBarInit, kCons + 128);
+    if (cons) {
 
     __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out);
     int bad = 0;
@@ -652,6 +696,11 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       // ---- out = O / den
       const int okb = tc::mbar_wait(bar_b, c & 1, kWaitCycles);
       if (__any_sync(0xffffffffu, !okb)) bad = 1;
+      // A whole chunk is staged in its q' buffer (free: q' and P~ were read by the finished MMAs)
+      // in the box layout of the output tensor map and written by TMA in full 128-byte lines; the
+      // ragged last chunk of a document is written row by row (its tile would reach past it).
+      const bool whole = c * kC + kC <= seg_n;
+      const uint32_t ob = base + (s ? L::Q1 : L::Q0);
       if (!bad) {
         tc::fence_after_sync();
         const uint32_t to = tmem + tl + (s ? L::TO1 : L::TO0);
@@ -664,23 +713,42 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           tc::tmem_ld16(to + j0, u[0]);
           tc::tmem_ld16(to + j0 + 16, u[1]);
           tc::tmem_wait_ld();
-          if (lt < seg_n) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + j0);
+          const uint32_t blk = ob + static_cast<uint32_t>(j0 / 64) * 16384;
+          const int cc = (j0 % 64) / 8;
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
-              float f[16];
+          for (int m = 0; m < 2; ++m) {
+            float f[16];
 #pragma unroll
-              for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(u[m][e]) * inv;
+            for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(u[m][e]) * inv;
+            if (whole) {
+              sts16(blk + tc::sw128(er, cc + 2 * m), pack8(f));
+              sts16(blk + tc::sw128(er, cc + 2 * m + 1), pack8(f + 8));
+            } else if (lt < seg_n) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + j0);
               dst[2 * m] = pack8(f);
               dst[2 * m + 1] = pack8(f + 8);
             }
           }
         }
+        if (whole) tc::fence_async_smem();
       }
       tc::fence_before_sync();
       if (bad) atomicExch(s_abort, 1);
-      if (group_sync_or(kBarCons, kCons, *s_abort)) break;
+      const int stop = group_sync_or(kBarCons, kCons, *s_abort);
+      if (q4 == 0 && lane == 0) {
+        if (!stop && whole) {
+#pragma unroll
+          for (int jb = 0; jb < D / 64; ++jb)
+            tc::tma_store_3d(&tmap_o, ob + jb * 16384, 64 * jb, h,
+                             static_cast<int>(row0 + seg_start + c * kC));
+          tc::bulk_commit();
+          tc::bulk_wait_read0();  // the buffer may be refilled once the store has read it
+        }
+        tc::mbar_arrive(bar_empty + 8 * s);  // q' and v buffers of this chunk are free
+      }
+      if (stop) break;
     }
+    if (q4 == 0 && lane == 0) tc::bulk_wait0();
     if (bad) atomicExch(s_abort, 1);
     if (last_seg && a.S_final != nullptr && !*s_abort && 32 * q4 < D) {
       tc::fence_after_sync();
@@ -695,19 +763,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                                __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3]));
       }
     }
-  } else {
-    // ============================================================ MMA issue (one thread)
-    tc::regs_dec<kRegsIssueB>();
-    if (warp == (kProd + kCons) / 32 && lane == 0) {
+    } else if (warp == (kProd + kCons) / 32 && lane == 0) {
+      // ========================================================== MMA issue (one thread)
       constexpr uint32_t ID_P = tc::idesc_bf16(128, 128, false, false);
       constexpr uint32_t ID_QS = tc::idesc_bf16(128, D, false, true);
       constexpr uint32_t ID_KV = tc::idesc_bf16(128, D, true, true);
       constexpr uint32_t ID_PV = tc::idesc_bf16(128, D, false, true);
-      const volatile int* ready = s_ready;
-      const long long t0 = clock64();
-      while (*ready == 0 && clock64() - t0 < kWaitCycles) {
-      }
-      int ok = *ready != 0;
+      tc::fence_after_sync();
+      int ok = 1;
       // descriptors: k-major operands advance 32 bytes per K=16 step inside a 64-column block and
       // 16 KB per block; MN-major operands advance 2 KB (16 rows) per step
       const uint64_t d_ks_k = tc::desc_sw128(base + L::KS, 16, 1024);
@@ -755,7 +818,6 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           tc::mma_bf16(to, d_p + kofs, d_v + static_cast<uint64_t>(k) * 128, ID_PV, 1u);
         }
         tc::mma_commit(bar_b);
-        tc::mma_commit(bar_empty + 8 * s);
       }
       if (!ok) atomicExch(s_abort, 1);
     }
@@ -773,9 +835,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 }
 
 // ------------------------------------------------------------------------------------------------
-// Kernel A: state increment (K'^T V and the column sums of k') of one segment (every segment of a
-// document but its last). 16 producer warps fill one of two k' buffers (v arrives by TMA) while
-// the tensor core, fed by a dedicated issuer thread, accumulates the other into TMEM.
+// Kernel A: state increment (K'^T V and the column sums of k') of one block of blk_len tokens (every
+// block before a document's last segment). 16 producer warps fill one of two k' buffers (v arrives
+// by TMA) while the tensor core, fed by a dedicated issuer thread, accumulates the other into TMEM.
 template <int D>
 __global__ void __launch_bounds__(kThreadsA, 1)
     segment_state_kernel(const TcArgs ta, const __grid_constant__ CUtensorMap tmap_v) {
@@ -785,16 +847,17 @@ __global__ void __launch_bounds__(kThreadsA, 1)
   const PrefillArgs& a = ta.p;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int seg = blockIdx.x % ta.nseg_max;
-  const int h = (blockIdx.x / ta.nseg_max) % a.H;
-  const int doc = blockIdx.x / (ta.nseg_max * a.H);
+  tc::grid_launch_dependents();  // kernel B may start; it waits for this grid before reading ws
+  const int blk = blockIdx.x % ta.nblk_max;
+  const int h = (blockIdx.x / ta.nblk_max) % a.H;
+  const int doc = blockIdx.x / (ta.nblk_max * a.H);
   long row0;
   int n;
   doc_bounds(a, doc, row0, n);  // a malformed document has n = 0 and is skipped
   const int nseg_doc = n > 0 ? (n + ta.seg_len - 1) / ta.seg_len : 1;
-  if (seg >= nseg_doc - 1) return;  // the last segment's increment is not needed
-  const int seg_start = seg * ta.seg_len;
-  const int nchunks = ta.seg_len / kC;  // a non-last segment is full
+  if (blk >= (nseg_doc - 1) * ta.blk_per_seg) return;  // the last segment needs no increment
+  const int seg_start = blk * ta.blk_len;
+  const int nchunks = ta.blk_len / kC;  // a block before the last segment is full
 
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t base = tc::smem_u32(smem);
@@ -835,7 +898,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *s_tmem;
   const long bh = static_cast<long>(doc) * a.H + h;
-  float* dst = ta.ws + (bh * ta.nseg_max + seg) * static_cast<long>(D) * (D + kPad);
+  float* dst = ta.ws + (bh * ta.nblk_max + blk) * Rec<D>::FLOATS;
 
   if (warp < kProd / 32) {
     tc::regs_inc<kRegsProdA>();
@@ -905,7 +968,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
       float z = 0.f;
 #pragma unroll
       for (int w = 0; w < PM::WARPS; ++w) z += zp[w * D + tid];
-      dst[static_cast<long>(tid) * (D + kPad) + D] = z;
+      dst[Rec<D>::Z + tid] = z;
     }
   } else {
     tc::regs_dec<kRegsIssueA>();
@@ -944,12 +1007,15 @@ __global__ void __launch_bounds__(kThreadsA, 1)
       tc::fence_after_sync();
       const int er = 32 * q4 + lane;
       const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
+      float4* d4 = reinterpret_cast<float4*>(dst) + er;
       for (int j0 = 0; j0 < D; j0 += 16) {
         uint32_t u[16];
         tc::tmem_ld16(tmem + tl + j0, u);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) dst[static_cast<long>(er) * (D + kPad) + j0 + e] = __uint_as_float(u[e]);
+        for (int e = 0; e < 4; ++e)
+          __stcg(d4 + (j0 / 4 + e) * D, make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
+                                                    __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3])));
       }
     }
   }
@@ -970,9 +1036,9 @@ cudaError_t set_smem(K kernel, uint32_t bytes, unsigned long long& configured) {
   return e;
 }
 
-// Tensor map of v ([rows, H, D] bf16, rows = B * L or T) with 64 x 1 x 128 boxes, 128-byte swizzle:
-// one box is one 64-column block of a chunk's v operand.
-cudaError_t make_v_map(CUtensorMap* map, const void* v, long rows, int H, int D) {
+// Tensor map of a [rows, H, D] bf16 tensor (rows = B * L or T; v or out) with 64 x 1 x 128 boxes,
+// 128-byte swizzle: one box is one 64-column block of a chunk's tile in the operand layout.
+cudaError_t make_tile_map(CUtensorMap* map, const void* v, long rows, int H, int D) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (encode == nullptr) {
     void* fn = nullptr;
@@ -1004,21 +1070,36 @@ cudaError_t launch_tc_d(const TcArgs& ta, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const long units = static_cast<long>(ta.p.n_docs) * ta.p.H;
   if (units == 0) return cudaSuccess;
-  CUtensorMap tmap_v;
+  CUtensorMap tmap_v, tmap_o;
   if (ta.p.v != nullptr && ta.p.total_rows > 0) {
-    e = make_v_map(&tmap_v, ta.p.v, ta.p.total_rows, ta.p.H, D);
+    e = make_tile_map(&tmap_v, ta.p.v, ta.p.total_rows, ta.p.H, D);
+    if (e == cudaSuccess) e = make_tile_map(&tmap_o, ta.p.out, ta.p.total_rows, ta.p.H, D);
     if (e != cudaSuccess) return e;
   } else {
     memset(&tmap_v, 0, sizeof(tmap_v));  // no rows: the kernels issue no copy
+    memset(&tmap_o, 0, sizeof(tmap_o));
   }
-  if (ta.nseg_max > 1) {
-    segment_state_kernel<D><<<static_cast<unsigned>(units * ta.nseg_max), kThreadsA, LayA<D>::BYTES, stream>>>(ta, tmap_v);
+  const bool with_a = ta.nblk_max > 0;
+  if (with_a) {
+    segment_state_kernel<D><<<static_cast<unsigned>(units * ta.nblk_max), kThreadsA, LayA<D>::BYTES, stream>>>(ta, tmap_v);
     note_launches(1);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  prefill_tc_kernel<D><<<static_cast<unsigned>(units * ta.nseg_max), kThreadsB, LayB<D>::BYTES, stream>>>(ta, tmap_v);
+  // kernel B as a programmatic dependent of kernel A (only then: it must not overlap anything else)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(units * ta.nseg_max));
+  cfg.blockDim = dim3(kThreadsB);
+  cfg.dynamicSmemBytes = LayB<D>::BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = with_a ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D>, ta, tmap_v, tmap_o);
   note_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -1031,8 +1112,8 @@ TcPlan tc_plan(int n_docs, int H, int max_seqlen, long total_tokens, int d) {
   // CTAs, each costing its chunks plus about one chunk of state set-up); a kernel-A chunk (k
   // features and one GEMM) costs about half a kernel-B chunk, also one CTA per SM. Documents are
   // assumed to share the tokens evenly, except that the longest one bounds the segment count.
-  // More segments cost workspace, so a longer plan must be clearly (5 %) faster to win.
-  TcPlan best{1, kC, 0};
+  // More segments or blocks cost workspace, so a longer plan must be clearly (5 %) faster to win.
+  TcPlan best{1, kC, 1, 0};
   const int chunks_max = max_seqlen > 0 ? (max_seqlen + kC - 1) / kC : 1;
   const double avg_chunks = n_docs > 0 ? static_cast<double>(total_tokens) / n_docs / kC : 0.0;
   double best_cost = 1e300;
@@ -1043,20 +1124,30 @@ TcPlan tc_plan(int n_docs, int H, int max_seqlen, long total_tokens, int d) {
                                                       (avg_chunks + seg_chunks - 1e-9) / seg_chunks))
                                                : 1.0;
     const double items_b = static_cast<double>(H) * n_docs * (segs_per_doc > 1 ? segs_per_doc : 1.0);
-    const double items_a = items_b - static_cast<double>(H) * n_docs;
     const double waves_b = static_cast<double>(static_cast<long>((items_b + 151) / 152));
-    const double waves_a = items_a > 0 ? static_cast<double>(static_cast<long>((items_a + 151) / 152)) : 0.0;
-    const double cost = waves_b * (seg_chunks + 1.0) + 0.5 * waves_a * seg_chunks;
-    if (cost < 0.95 * best_cost) {
-      best_cost = cost;
-      best.nseg_max = nseg;
-      best.seg_len = seg_chunks * kC;
+    for (int f = 1; f <= 8 && nseg > 1; f *= 2) {
+      if (seg_chunks % f != 0) break;
+      const double items_a = (items_b - static_cast<double>(H) * n_docs) * f;
+      const double waves_a = items_a > 0 ? static_cast<double>(static_cast<long>((items_a + 151) / 152)) : 0.0;
+      const double cost = waves_b * (seg_chunks + 1.0) + waves_a * (0.5 * seg_chunks / f + 0.5);
+      if (cost < 0.95 * best_cost) {
+        best_cost = cost;
+        best = TcPlan{nseg, seg_chunks * kC, f, 0};
+      }
+    }
+    if (nseg == 1) {
+      const double cost = waves_b * (seg_chunks + 1.0);
+      if (cost < 0.95 * best_cost) {
+        best_cost = cost;
+        best = TcPlan{1, seg_chunks * kC, 1, 0};
+      }
     }
   }
   const long units = static_cast<long>(n_docs) * H;
-  best.ws_bytes = best.nseg_max > 1
-                      ? static_cast<size_t>(units) * best.nseg_max * d * (d + kPad) * sizeof(float)
-                      : 0;
+  const long rec = static_cast<long>(d) * (d + 1);
+  best.ws_bytes = best.nseg_max > 1 ? static_cast<size_t>(units) * (best.nseg_max - 1) *
+                                          best.blk_per_seg * rec * sizeof(float)
+                                    : 0;
   return best;
 }
 
@@ -1067,6 +1158,9 @@ cudaError_t launch_prefill_tc(int d, const PrefillArgs& a, const TcPlan& plan, f
   ta.ws = ws;
   ta.seg_len = plan.seg_len;
   ta.nseg_max = plan.nseg_max;
+  ta.blk_per_seg = plan.blk_per_seg;
+  ta.blk_len = plan.seg_len / plan.blk_per_seg;
+  ta.nblk_max = (plan.nseg_max - 1) * plan.blk_per_seg;
   return d == 128 ? launch_tc_d<128>(ta, stream) : launch_tc_d<64>(ta, stream);
 }
 
