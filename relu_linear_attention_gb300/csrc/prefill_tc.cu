@@ -78,7 +78,7 @@ struct Rec {
 constexpr int kLaunchRegsB = 80, kRegsProdB = 88, kRegsConsB = 64, kRegsIssueB = 64;
 static_assert(kProd * kRegsProdB + kCons * kRegsConsB + 128 * kRegsIssueB <= kThreadsB * kLaunchRegsB,
               "kernel B register split exceeds the launch allocation");
-constexpr int kLaunchRegsA = 96, kRegsProdA = 104, kRegsIssueA = 64;
+constexpr int kLaunchRegsA = 96, kRegsProdA = 96, kRegsIssueA = 96;
 static_assert(kProd * kRegsProdA + 128 * kRegsIssueA <= kThreadsA * kLaunchRegsA,
               "kernel A register split exceeds the launch allocation");
 
@@ -350,59 +350,46 @@ __device__ __forceinline__ void tab_rot_at(const FeatTab& t, int pos, int j0, Ro
 // Initial state of a segment for columns [c0, c0 + D/2) of the calling thread's TMEM lane er:
 // S0 (if any) + the increments of the first nblk blocks, in block order, into the fp32 state in
 // TMEM (tmem_s: lane and column base of S) and its bf16 copy S~ in shared memory (ss); TMEM rows
-// >= D are zeroed. Two blocks are loaded at a time to keep more loads in flight.
+// >= D are zeroed. Eight columns at a time, with two blocks' loads in flight.
 template <int D>
 __device__ __forceinline__ void init_state(const PrefillArgs& a, const float* wsb, int nblk, long bh,
                                            int er, uint32_t tmem_s, uint32_t ss, int c0) {
-  for (int j0 = c0; j0 < c0 + D / 2; j0 += 16) {
-    float v[16];
-    uint32_t u[16];
+#pragma unroll 1
+  for (int j0 = c0; j0 < c0 + D / 2; j0 += 8) {
+    float v[8];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) v[e] = 0.f;
+    for (int e = 0; e < 8; ++e) v[e] = 0.f;
     if (er < D) {
       if (a.S0 != nullptr) {
         const float4* src = reinterpret_cast<const float4*>(a.S0 + (bh * D + er) * D + j0);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float4 x = src[e];
-          v[4 * e] += x.x; v[4 * e + 1] += x.y; v[4 * e + 2] += x.z; v[4 * e + 3] += x.w;
-        }
+        const float4 x0 = src[0], x1 = src[1];
+        v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
+        v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
       }
       const float4* inc = reinterpret_cast<const float4*>(wsb) + (j0 / 4) * D + er;
       constexpr long R4 = Rec<D>::FLOATS / 4;
-      int g = 0;
-      for (; g + 1 < nblk; g += 2) {
-        float4 x[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          x[e] = __ldcg(inc + g * R4 + e * D);
-          x[4 + e] = __ldcg(inc + (g + 1) * R4 + e * D);
+#pragma unroll 1
+      for (int g = 0; g < nblk; g += 2) {
+        const bool two = g + 1 < nblk;
+        const float4 x0 = __ldcg(inc + g * R4), x1 = __ldcg(inc + g * R4 + D);
+        float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
+        if (two) {
+          y0 = __ldcg(inc + (g + 1) * R4);
+          y1 = __ldcg(inc + (g + 1) * R4 + D);
         }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int b = 4 * (e & 3);
-          v[b] += x[e].x; v[b + 1] += x[e].y; v[b + 2] += x[e].z; v[b + 3] += x[e].w;
-        }
-      }
-      if (g < nblk) {
-        float4 x[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[e] = __ldcg(inc + g * R4 + e * D);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          v[4 * e] += x[e].x; v[4 * e + 1] += x[e].y; v[4 * e + 2] += x[e].z; v[4 * e + 3] += x[e].w;
+        v[0] += x0.x; v[1] += x0.y; v[2] += x0.z; v[3] += x0.w;
+        v[4] += x1.x; v[5] += x1.y; v[6] += x1.z; v[7] += x1.w;
+        if (two) {
+          v[0] += y0.x; v[1] += y0.y; v[2] += y0.z; v[3] += y0.w;
+          v[4] += y1.x; v[5] += y1.y; v[6] += y1.z; v[7] += y1.w;
         }
       }
     }
+    uint32_t u[8];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(v[e]);
-    tc::tmem_st16(tmem_s + j0, u);
-    if (er < D) {
-      const uint32_t blk = ss + static_cast<uint32_t>(j0 / 64) * (D * 128);
-      const int cc = (j0 % 64) / 8;
-      sts16(blk + tc::sw128(er, cc), pack8(v));
-      sts16(blk + tc::sw128(er, cc + 1), pack8(v + 8));
-    }
+    for (int e = 0; e < 8; ++e) u[e] = __float_as_uint(v[e]);
+    tc::tmem_st8(tmem_s + j0, u);
+    if (er < D) sts16(ss + static_cast<uint32_t>(j0 / 64) * (D * 128) + tc::sw128(er, (j0 % 64) / 8), pack8(v));
   }
 }
 
@@ -608,13 +595,16 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const int er = 32 * q4 + lane;           // TMEM lane = tile row
     const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
     // initial state (the two warpgroups take half of the columns each)
-    if (nblk > 0) tc::grid_dep_wait();
-    init_state<D>(a, wsb, nblk, bh, er, tmem + tl + L::TS, base + L::SS, cons ? 0 : D / 2);
-    tc::tmem_wait_st();
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    tc::named_sync(kBarInit, kCons + 128);
+    auto init = [&](int c0) {
+      if (nblk > 0) tc::grid_dep_wait();
+      init_state<D>(a, wsb, nblk, bh, er, tmem + tl + L::TS, base + L::SS, c0);
+      tc::tmem_wait_st();
+      tc::fence_async_smem();
+      tc::fence_before_sync();
+      tc::named_sync(kBarInit, kCons + 128);
+    };
     if (cons) {
+      init(0);
 
     __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out);
     int bad = 0;
@@ -763,7 +753,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                                __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3]));
       }
     }
-    } else if (warp == (kProd + kCons) / 32 && lane == 0) {
+    } else {
+      init(D / 2);
+      if (warp == (kProd + kCons) / 32 && lane == 0) {
       // ========================================================== MMA issue (one thread)
       constexpr uint32_t ID_P = tc::idesc_bf16(128, 128, false, false);
       constexpr uint32_t ID_QS = tc::idesc_bf16(128, D, false, true);
@@ -820,6 +812,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         tc::mma_commit(bar_b);
       }
       if (!ok) atomicExch(s_abort, 1);
+      }
     }
   }
 
