@@ -24,12 +24,15 @@
 //   warps 16-19 (consumers): one TMEM lane quarter (32 tile rows) each: S -> S~, P -> P~ and its
 //                            row sums, then the output epilogue from one of two O accumulators;
 //   warp 20     (issuer):    one thread issues the MMAs (an issue blocks while the tensor core is
-//                            busy, so it gets a warp of its own); warps 21-23 only hold registers.
+//                            busy, so it gets a warp of its own);
+//   warps 21-23 (helpers):   z_c = z_{c-1} + the producer warps' column sums of k'_c, so that the
+//                            producers never wait for one another.
 // v tiles need no transformation: the tensor-memory accelerator (TMA) copies them from HBM straight
 // into the swizzled operand layout, one chunk ahead. q and k go through registers (a short load
 // ring) because the features are computed on the way.
-// Hand-offs go through mbarriers: full[2] (producers -> issuer), vfull[2] (TMA -> issuer),
-// empty[2] (output of chunk c staged and stored -> its buffers free), s_done / a_done / b_done (tensor core -> consumers),
+// Hand-offs go through mbarriers: full[2] (producers -> issuer, consumers, helpers), vfull[2] (TMA ->
+// issuer), zr (helpers -> producers: z updated),
+// empty[2] (chunk c's MMAs done -> its q' buffer free), s_done / a_done / b_done (tensor core -> consumers),
 // conv_done (consumers -> issuer: S~ and P~ written, S and P read). The recurrence step of chunk c
 // (O = Q'S~, then S += K'^T V) is issued first and committed on its own (s_done), so turning S
 // into the next chunk's operand, the one serial dependency between chunks, starts early.
@@ -64,6 +67,8 @@ constexpr long long kWaitCycles = 2000000000LL;  // ~1 s: a tensor-core step tha
 constexpr uint32_t kDevInternal = 2u;
 constexpr uint32_t kBarProd = 1, kBarCons = 2;   // named barriers of the producer / consumer groups
 constexpr uint32_t kBarInit = 3;                 // consumer + issuer warpgroups after the state set-up
+constexpr uint32_t kBarHelp = 4;                 // the three helper warps of the issuer warpgroup
+constexpr int kHelp = 96;                        // helper threads
 
 // One increment record: K'^T V of a block as D/4 column groups of [D rows][4 columns] (the float4
 // of row r and columns 4j..4j+3 at float4 index j * D + r, so that 32 threads reading their rows'
@@ -103,13 +108,13 @@ struct LayB {
   static constexpr uint32_t KS = 4 * TILE;                     // k' : 2 x 16 KB (d = 64: + zero block)
   static constexpr uint32_t PS = KS + 32768;                   // P~ at d = 64
   static constexpr uint32_t SS = PS + (D == 64 ? 32768 : 0);   // S~ : D/64 blocks of D rows x 128 B
-  static constexpr uint32_t ZP = SS + (D / 64) * D * 128;      // z partials [producer warps][D] fp32
-  static constexpr uint32_t ZS = ZP + Prod<D>::WARPS * D * 4;  // z [D] fp32
+  static constexpr uint32_t ZP = SS + (D / 64) * D * 128;      // z partials [2][producer warps][D] fp32
+  static constexpr uint32_t ZS = ZP + 2 * Prod<D>::WARPS * D * 4;  // z [D] fp32
   static constexpr uint32_t DI = ZS + D * 4;                   // q'.z [2][128] fp32
   static constexpr uint32_t TAB = DI + 2 * kC * 4;             // feature tables (FeatTab)
-  // full0 full1 empty0 empty1 vfull0 vfull1 s_done a_done b_done conv_done
+  // full0 full1 empty0 empty1 vfull0 vfull1 s_done a_done b_done conv_done z_ready
   static constexpr uint32_t BAR = TAB + 8 * D * 4;
-  static constexpr uint32_t MISC = BAR + 10 * 8;               // TMEM base, abort, ready flags
+  static constexpr uint32_t MISC = BAR + 11 * 8;               // TMEM base, abort flag
   static constexpr uint32_t BYTES = MISC + 16;
   // TMEM columns: P, two O accumulators, S
   static constexpr uint32_t TP = 0, TO0 = 128, TO1 = 128 + D, TS = 128 + 2 * D;
@@ -225,10 +230,11 @@ struct Rot {
   float2 c[2], s[2];  // cos / sin of pairs (2g, 2g+1)
 };
 
-// ReLU(RoPE(x * gamma)) * rinv (rinv > 0 commutes with ReLU), in place: x0 <- first elements,
-// x1 <- second elements of the rotated pairs.
+// ReLU(RoPE(x * gamma * rinv)), in place (the gains come multiplied by the row's 1 / rms: RoPE is
+// linear, so that is the same as normalising first): x0 <- first elements, x1 <- second elements
+// of the rotated pairs.
 __device__ __forceinline__ void rope_relu(Pairs& p, const float2 (&g0)[2], const float2 (&g1)[2],
-                                          const Rot& r, float rinv) {
+                                          const Rot& r) {
 #pragma unroll
   for (int g = 0; g < 2; ++g) {
     const float2 y0 = __fmul2_rn(p.x0[g], g0[g]);
@@ -236,8 +242,16 @@ __device__ __forceinline__ void rope_relu(Pairs& p, const float2 (&g0)[2], const
     const float2 ns = make_float2(-r.s[g].x, -r.s[g].y);
     const float2 u = __ffma2_rn(y0, r.c[g], __fmul2_rn(y1, ns));   // y0 c - y1 s
     const float2 v = __ffma2_rn(y0, r.s[g], __fmul2_rn(y1, r.c[g]));  // y0 s + y1 c
-    p.x0[g] = make_float2(fmaxf(u.x, 0.f) * rinv, fmaxf(u.y, 0.f) * rinv);
-    p.x1[g] = make_float2(fmaxf(v.x, 0.f) * rinv, fmaxf(v.y, 0.f) * rinv);
+    p.x0[g] = make_float2(fmaxf(u.x, 0.f), fmaxf(u.y, 0.f));
+    p.x1[g] = make_float2(fmaxf(v.x, 0.f), fmaxf(v.y, 0.f));
+  }
+}
+__device__ __forceinline__ void scale_gains(float2 (&g0)[2], float2 (&g1)[2], float s) {
+  const float2 s2 = make_float2(s, s);
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    g0[g] = __fmul2_rn(g0[g], s2);
+    g1[g] = __fmul2_rn(g1[g], s2);
   }
 }
 
@@ -432,7 +446,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   float* di = reinterpret_cast<float*>(smem + L::DI);
   const uint32_t bar_full = base + L::BAR, bar_empty = bar_full + 16, bar_vfull = bar_full + 32;
   const uint32_t bar_s = bar_full + 48, bar_a = bar_full + 56, bar_b = bar_full + 64;
-  const uint32_t bar_conv = bar_full + 72;
+  const uint32_t bar_conv = bar_full + 72, bar_zr = bar_full + 80;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::MISC);
   int* s_abort = reinterpret_cast<int*>(smem + L::MISC + 4);
 
@@ -451,6 +465,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     tc::mbar_init(bar_a, 1);
     tc::mbar_init(bar_b, 1);
     tc::mbar_init(bar_conv, kCons);
+    tc::mbar_init(bar_zr, kHelp);
     tc::mbar_fence_init();
     *s_abort = 0;
   }
@@ -472,14 +487,6 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const int prow = tid / TPR, part = tid % TPR, e0 = 8 * part;
     const uint32_t cblk = static_cast<uint32_t>(e0 / 64) * 16384;  // 64-column block
     const int cidx = (e0 % 64) / 8;                                 // 16-byte chunk in the row
-    // z at the segment start: z0 + the earlier blocks' sums of k' (kernel A's output: wait for it)
-    if (nblk > 0) tc::grid_dep_wait();
-    for (int i = tid; i < D; i += kProd) {
-      float z = a.z0 != nullptr ? a.z0[bh * D + i] : 0.f;
-      for (int g = 0; g < nblk; ++g) z += __ldcg(wsb + g * Rec<D>::FLOATS + Rec<D>::Z + i);
-      zs[split_idx<D>(i)] = z;
-    }
-    tc::named_sync(kBarProd, kProd);
 
     const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
     const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(a.k);
@@ -504,9 +511,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       int bad = 0;
       if (c >= 2 && !tc::mbar_wait(bar_empty + 8 * s, ((c >> 1) + 1) & 1, kWaitCycles)) bad = 1;
       const uint32_t qb = base + (s ? L::Q1 : L::Q0), vb = base + (s ? L::V1 : L::V0);
-      if (tid == 0) {
-        // v rows of this chunk, straight into the swizzled operand (rows past the segment are
-        // either other tokens or zero fill; their k' and P columns are zero)
+      if (tid == 0 && c < 2) {
+        // v rows of the first two chunks, straight into the swizzled operand (rows past the segment
+        // are either other tokens or zero fill; their k' and P columns are zero); the consumers
+        // load the later chunks' v into the buffer once its output staging is done
         tc::mbar_arrive_expect_tx(bar_vfull + 8 * s, L::TILE);
 #pragma unroll
         for (int jb = 0; jb < D / 64; ++jb)
@@ -539,10 +547,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         {
           float2 g0[2], g1[2];
           split_load<D>(tab.gq, part, g0, g1);
-          rope_relu(fq, g0, g1, rot, rinvq);
+          scale_gains(g0, g1, rinvq);
+          rope_relu(fq, g0, g1, rot);
           split_load<D>(tab.gk, part, g0, g1);
-          rope_relu(fk, g0, g1, rot, rinvk);
+          scale_gains(g0, g1, rinvk);
+          rope_relu(fk, g0, g1, rot);
         }
+        // z_{c-1} (the helpers' sum up to the previous chunk) is needed from here on
+        if (p == 0 && !tc::mbar_wait(bar_zr, c & 1, kWaitCycles)) bad = 1;
         float2 zfa[2], zfb[2];  // z of the pairs' first / second elements
         split_load<D>(zs, part, zfa, zfb);
         float2 d2 = __fmul2_rn(fq.x0[0], zfa[0]);
@@ -563,28 +575,19 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       if (c >= 1 && !tc::mbar_wait(bar_a, (c - 1) & 1, kWaitCycles)) bad = 1;
 #pragma unroll
       for (int p = 0; p < NPASS; ++p) sts16(base + L::KS + cblk + tc::sw128(p * RPP + prow, cidx), kreg[p]);
-      tc::fence_async_smem();
-      tc::mbar_arrive(bar_full + 8 * s);
-      // z_c = z_{c-1} + column sums of k'_c (fixed order: deterministic)
+      // this warp's column sums of k'_c (the helper warps add the warps' sums up in a fixed order)
       float zc[8];
       pairs_to8(Pairs{{zca[0], zca[1]}, {zcb[0], zcb[1]}}, zc);
       warp_colsum<TPR>(zc);
       if (lane < TPR) {
-        *reinterpret_cast<float4*>(zp + warp * D + e0) = make_float4(zc[0], zc[1], zc[2], zc[3]);
-        *reinterpret_cast<float4*>(zp + warp * D + e0 + 4) = make_float4(zc[4], zc[5], zc[6], zc[7]);
+        float* zw = zp + (s * PM::WARPS + warp) * D + e0;
+        *reinterpret_cast<float4*>(zw) = make_float4(zc[0], zc[1], zc[2], zc[3]);
+        *reinterpret_cast<float4*>(zw + 4) = make_float4(zc[4], zc[5], zc[6], zc[7]);
       }
+      tc::fence_async_smem();
+      tc::mbar_arrive(bar_full + 8 * s);
       if (bad) atomicExch(s_abort, 1);
-      tc::named_sync(kBarProd, kProd);
-      if (tid < D) {
-        float z = zs[split_idx<D>(tid)];
-#pragma unroll
-        for (int w = 0; w < PM::WARPS; ++w) z += zp[w * D + tid];
-        zs[split_idx<D>(tid)] = z;
-      }
-      if (group_sync_or(kBarProd, kProd, *s_abort)) break;
-    }
-    if (last_seg && a.z_final != nullptr && !*s_abort) {
-      for (int i = tid; i < D; i += kProd) a.z_final[bh * D + i] = zs[split_idx<D>(i)];
+      if (__any_sync(0xffffffffu, *reinterpret_cast<volatile int*>(s_abort))) break;
     }
   } else {
     // ============================================ consumers (warps 16-19), issuer warpgroup (20-23)
@@ -686,11 +689,11 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       // ---- out = O / den
       const int okb = tc::mbar_wait(bar_b, c & 1, kWaitCycles);
       if (__any_sync(0xffffffffu, !okb)) bad = 1;
-      // A whole chunk is staged in its q' buffer (free: q' and P~ were read by the finished MMAs)
-      // in the box layout of the output tensor map and written by TMA in full 128-byte lines; the
-      // ragged last chunk of a document is written row by row (its tile would reach past it).
+      // A whole chunk is staged in its v buffer (free: v was read by the finished MMAs) in the box
+      // layout of the output tensor map and written by TMA in full 128-byte lines; the ragged last
+      // chunk of a document is written row by row (its tile would reach past it).
       const bool whole = c * kC + kC <= seg_n;
-      const uint32_t ob = base + (s ? L::Q1 : L::Q0);
+      const uint32_t ob = base + (s ? L::V1 : L::V0);
       if (!bad) {
         tc::fence_after_sync();
         const uint32_t to = tmem + tl + (s ? L::TO1 : L::TO0);
@@ -734,7 +737,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           tc::bulk_commit();
           tc::bulk_wait_read0();  // the buffer may be refilled once the store has read it
         }
-        tc::mbar_arrive(bar_empty + 8 * s);  // q' and v buffers of this chunk are free
+        if (!stop && c + 2 < nchunks) {  // v of chunk c + 2 into the same buffer
+          tc::mbar_arrive_expect_tx(bar_vfull + 8 * s, L::TILE);
+#pragma unroll
+          for (int jb = 0; jb < D / 64; ++jb)
+            tc::tma_load_3d(ob + jb * 16384, &tmap_v, 64 * jb, h,
+                            static_cast<int>(row0 + seg_start + (c + 2) * kC), bar_vfull + 8 * s);
+        }
       }
       if (stop) break;
     }
@@ -753,9 +762,44 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                                __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3]));
       }
     }
+    } else if (warp > (kProd + kCons) / 32) {
+      // ========================================================== helpers (warps 21-23)
+      init(D / 2);
+      const int ht = tid - (kProd + kCons + 32);
+      // z at the segment start: z0 + the sums of k' of the blocks before the segment
+      for (int i = ht; i < D; i += kHelp) {
+        float z = a.z0 != nullptr ? a.z0[bh * D + i] : 0.f;
+        for (int g = 0; g < nblk; ++g) z += __ldcg(wsb + g * Rec<D>::FLOATS + Rec<D>::Z + i);
+        zs[split_idx<D>(i)] = z;
+      }
+      tc::mbar_arrive(bar_zr);  // z_{-1}
+      int bad = 0;
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c & 1;
+        if (!tc::mbar_wait(bar_full + 8 * s, (c >> 1) & 1, kWaitCycles)) bad = 1;
+        if (group_sync_or(kBarHelp, kHelp, bad | *s_abort)) {  // uniform over the helpers
+          bad = 1;
+          break;
+        }
+        // z_c = z_{c-1} + the producer warps' column sums of k'_c (fixed order: deterministic);
+        // the producers have finished reading z_{c-1} (full) and wait for this update (z_ready)
+        const float* zpc = zp + s * PM::WARPS * D;
+        for (int i = ht; i < D; i += kHelp) {
+          float z = zs[split_idx<D>(i)];
+#pragma unroll
+          for (int w = 0; w < PM::WARPS; ++w) z += zpc[w * D + i];
+          zs[split_idx<D>(i)] = z;
+        }
+        tc::mbar_arrive(bar_zr);
+      }
+      if (bad) atomicExch(s_abort, 1);
+      tc::named_sync(kBarHelp, kHelp);
+      if (last_seg && a.z_final != nullptr && !*s_abort) {
+        for (int i = ht; i < D; i += kHelp) a.z_final[bh * D + i] = zs[split_idx<D>(i)];
+      }
     } else {
       init(D / 2);
-      if (warp == (kProd + kCons) / 32 && lane == 0) {
+      if (lane == 0) {
       // ========================================================== MMA issue (one thread)
       constexpr uint32_t ID_P = tc::idesc_bf16(128, 128, false, false);
       constexpr uint32_t ID_QS = tc::idesc_bf16(128, D, false, true);
@@ -810,6 +854,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           tc::mma_bf16(to, d_p + kofs, d_v + static_cast<uint64_t>(k) * 128, ID_PV, 1u);
         }
         tc::mma_commit(bar_b);
+        tc::mma_commit(bar_empty + 8 * s);  // q' (and P~) buffer free for chunk c + 2
       }
       if (!ok) atomicExch(s_abort, 1);
       }
@@ -935,7 +980,9 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         if (p > 0) rot_step(rot, step);
         Pairs fk = unpack_pairs(xk);
         const float sk = row_sum<TPR>(sumsq(fk));
-        rope_relu(fk, gk0, gk1, rot, rsqrtf(sk * (1.0f / D) + a.fa.eps_norm));
+        float2 g0[2] = {gk0[0], gk0[1]}, g1[2] = {gk1[0], gk1[1]};
+        scale_gains(g0, g1, rsqrtf(sk * (1.0f / D) + a.fa.eps_norm));
+        rope_relu(fk, g0, g1, rot);
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           zca[g] = __fadd2_rn(zca[g], fk.x0[g]);
