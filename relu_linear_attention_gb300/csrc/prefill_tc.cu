@@ -25,13 +25,15 @@
 //                            row sums, then the output epilogue from one of two O accumulators;
 //   warp 20     (issuer):    one thread issues the MMAs (an issue blocks while the tensor core is
 //                            busy, so it gets a warp of its own);
-//   warps 21-23 (helpers):   z_c = z_{c-1} + the producer warps' column sums of k'_c, so that the
-//                            producers never wait for one another.
+//   warps 21-22 (helpers):   z_c = z_{c-1} + the producer warps' column sums of k'_c, so that the
+//                            producers never wait for one another;
+//   warp 23     (store):     one thread writes each staged output tile with TMA stores and, once the
+//                            store has read the buffer, loads the v tile of two chunks later into it.
 // v tiles need no transformation: the tensor-memory accelerator (TMA) copies them from HBM straight
 // into the swizzled operand layout, one chunk ahead. q and k go through registers (a short load
 // ring) because the features are computed on the way.
 // Hand-offs go through mbarriers: full[2] (producers -> issuer, consumers, helpers), vfull[2] (TMA ->
-// issuer), zr (helpers -> producers: z updated),
+// issuer), zr (helpers -> producers: z updated), staged[2] (consumers -> store thread),
 // empty[2] (chunk c's MMAs done -> its q' buffer free), s_done / a_done / b_done (tensor core -> consumers),
 // conv_done (consumers -> issuer: S~ and P~ written, S and P read). The recurrence step of chunk c
 // (O = Q'S~, then S += K'^T V) is issued first and committed on its own (s_done), so turning S
@@ -67,8 +69,8 @@ constexpr long long kWaitCycles = 2000000000LL;  // ~1 s: a tensor-core step tha
 constexpr uint32_t kDevInternal = 2u;
 constexpr uint32_t kBarProd = 1, kBarCons = 2;   // named barriers of the producer / consumer groups
 constexpr uint32_t kBarInit = 3;                 // consumer + issuer warpgroups after the state set-up
-constexpr uint32_t kBarHelp = 4;                 // the three helper warps of the issuer warpgroup
-constexpr int kHelp = 96;                        // helper threads
+constexpr uint32_t kBarHelp = 4;                 // the two z helper warps of the issuer warpgroup
+constexpr int kHelp = 64;                        // z helper threads
 
 // One increment record: K'^T V of a block as D/4 column groups of [D rows][4 columns] (the float4
 // of row r and columns 4j..4j+3 at float4 index j * D + r, so that 32 threads reading their rows'
@@ -112,9 +114,9 @@ struct LayB {
   static constexpr uint32_t ZS = ZP + 2 * Prod<D>::WARPS * D * 4;  // z [D] fp32
   static constexpr uint32_t DI = ZS + D * 4;                   // q'.z [2][128] fp32
   static constexpr uint32_t TAB = DI + 2 * kC * 4;             // feature tables (FeatTab)
-  // full0 full1 empty0 empty1 vfull0 vfull1 s_done a_done b_done conv_done z_ready
+  // full0 full1 empty0 empty1 vfull0 vfull1 s_done a_done b_done conv_done z_ready staged0 staged1
   static constexpr uint32_t BAR = TAB + 8 * D * 4;
-  static constexpr uint32_t MISC = BAR + 11 * 8;               // TMEM base, abort flag
+  static constexpr uint32_t MISC = BAR + 13 * 8;               // TMEM base, abort flag
   static constexpr uint32_t BYTES = MISC + 16;
   // TMEM columns: P, two O accumulators, S
   static constexpr uint32_t TP = 0, TO0 = 128, TO1 = 128 + D, TS = 128 + 2 * D;
@@ -446,7 +448,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   float* di = reinterpret_cast<float*>(smem + L::DI);
   const uint32_t bar_full = base + L::BAR, bar_empty = bar_full + 16, bar_vfull = bar_full + 32;
   const uint32_t bar_s = bar_full + 48, bar_a = bar_full + 56, bar_b = bar_full + 64;
-  const uint32_t bar_conv = bar_full + 72, bar_zr = bar_full + 80;
+  const uint32_t bar_conv = bar_full + 72, bar_zr = bar_full + 80, bar_staged = bar_full + 88;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::MISC);
   int* s_abort = reinterpret_cast<int*>(smem + L::MISC + 4);
 
@@ -466,6 +468,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     tc::mbar_init(bar_b, 1);
     tc::mbar_init(bar_conv, kCons);
     tc::mbar_init(bar_zr, kHelp);
+    tc::mbar_init(bar_staged, kCons);
+    tc::mbar_init(bar_staged + 8, kCons);
     tc::mbar_fence_init();
     *s_abort = 0;
   }
@@ -726,28 +730,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         if (whole) tc::fence_async_smem();
       }
       tc::fence_before_sync();
+      tc::mbar_arrive(bar_staged + 8 * s);  // the store thread takes it from here
       if (bad) atomicExch(s_abort, 1);
-      const int stop = group_sync_or(kBarCons, kCons, *s_abort);
-      if (q4 == 0 && lane == 0) {
-        if (!stop && whole) {
-#pragma unroll
-          for (int jb = 0; jb < D / 64; ++jb)
-            tc::tma_store_3d(&tmap_o, ob + jb * 16384, 64 * jb, h,
-                             static_cast<int>(row0 + seg_start + c * kC));
-          tc::bulk_commit();
-          tc::bulk_wait_read0();  // the buffer may be refilled once the store has read it
-        }
-        if (!stop && c + 2 < nchunks) {  // v of chunk c + 2 into the same buffer
-          tc::mbar_arrive_expect_tx(bar_vfull + 8 * s, L::TILE);
-#pragma unroll
-          for (int jb = 0; jb < D / 64; ++jb)
-            tc::tma_load_3d(ob + jb * 16384, &tmap_v, 64 * jb, h,
-                            static_cast<int>(row0 + seg_start + (c + 2) * kC), bar_vfull + 8 * s);
-        }
-      }
-      if (stop) break;
+      if (group_sync_or(kBarCons, kCons, *s_abort)) break;
     }
-    if (q4 == 0 && lane == 0) tc::bulk_wait0();
     if (bad) atomicExch(s_abort, 1);
     if (last_seg && a.S_final != nullptr && !*s_abort && 32 * q4 < D) {
       tc::fence_after_sync();
@@ -762,8 +748,37 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                                __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3]));
       }
     }
+    } else if (warp == (kProd + kCons) / 32 + 3) {
+      // ========================================================== output stores (warp 23)
+      init(D / 2);
+      if (lane == 0) {
+        int ok = 1;
+        for (int c = 0; c < nchunks; ++c) {
+          const int s = c & 1;
+          ok = tc::mbar_wait(bar_staged + 8 * s, (c >> 1) & 1, kWaitCycles);
+          if (!ok || *reinterpret_cast<volatile int*>(s_abort)) break;
+          const uint32_t ob = base + (s ? L::V1 : L::V0);
+          if (c * kC + kC <= seg_n) {  // a whole chunk was staged
+#pragma unroll
+            for (int jb = 0; jb < D / 64; ++jb)
+              tc::tma_store_3d(&tmap_o, ob + jb * 16384, 64 * jb, h,
+                               static_cast<int>(row0 + seg_start + c * kC));
+            tc::bulk_commit();
+            tc::bulk_wait_read0();  // the buffer may be refilled once the store has read it
+          }
+          if (c + 2 < nchunks) {  // v of chunk c + 2 into the same buffer
+            tc::mbar_arrive_expect_tx(bar_vfull + 8 * s, L::TILE);
+#pragma unroll
+            for (int jb = 0; jb < D / 64; ++jb)
+              tc::tma_load_3d(ob + jb * 16384, &tmap_v, 64 * jb, h,
+                              static_cast<int>(row0 + seg_start + (c + 2) * kC), bar_vfull + 8 * s);
+          }
+        }
+        tc::bulk_wait0();
+        if (!ok) atomicExch(s_abort, 1);
+      }
     } else if (warp > (kProd + kCons) / 32) {
-      // ========================================================== helpers (warps 21-23)
+      // ========================================================== helpers (warps 21-22)
       init(D / 2);
       const int ht = tid - (kProd + kCons + 32);
       // z at the segment start: z0 + the sums of k' of the blocks before the segment
