@@ -207,8 +207,8 @@ rapt_status rapt_decode_step(const void* q, const void* k, const void* v, rapt_d
 }
 
 size_t rla_l2_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype) {
-  (void)dtype;
-  if (B < 1 || L < 0 || H < 1 || !supported_d(d)) return 0;
+  if (B < 1 || L < 0 || H < 1 || !supported_d(d) || !known_dtype(dtype)) return 0;
+  if (rapt::l2_tc_supported(to_dt(dtype), d)) return rapt::l2_tc_workspace_bytes(B, L, H, d);
   return rapt::l2_workspace_bytes(B, L, H, d);
 }
 
@@ -231,7 +231,9 @@ rapt_status rla_l2_fwd(const void* q, const void* k, const void* v, rapt_dtype d
   a.q = q; a.k = k; a.v = v; a.out = out;
   a.ws = static_cast<float*>(workspace);
   a.B = B; a.L = L; a.H = H; a.eps = eps;
-  return from_cuda(rapt::launch_rla_l2(to_dt(dtype), d, a, reinterpret_cast<cudaStream_t>(stream)));
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (rapt::l2_tc_supported(to_dt(dtype), d)) return from_cuda(rapt::launch_rla_l2_tc(d, a, st));
+  return from_cuda(rapt::launch_rla_l2(to_dt(dtype), d, a, st));
 }
 
 }  // extern "C"

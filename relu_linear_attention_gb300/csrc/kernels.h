@@ -95,6 +95,12 @@ cudaError_t launch_rla_l2(DType dt, int d, const L2Args& a, cudaStream_t stream)
 
 // Split count launch_rla_l2 would choose, and the launch with an explicit split count
 // (workspace of l2_workspace_bytes_for_splits() bytes at a.ws).
+// Tensor-core L2 path (bf16, d in {64, 128}): three launches, workspace of
+// l2_tc_workspace_bytes() bytes at a.ws (fp32 split partials, then the bf16 moment operands).
+bool l2_tc_supported(DType dt, int d);
+size_t l2_tc_workspace_bytes(int B, int L, int H, int d);
+cudaError_t launch_rla_l2_tc(int d, const L2Args& a, cudaStream_t stream);
+
 int l2_default_splits(int B, int L, int H);
 size_t l2_workspace_bytes_for_splits(int B, int H, int d, int nsplit);
 cudaError_t launch_rla_l2_with_splits(DType dt, int d, const L2Args& a, int nsplit,

@@ -50,12 +50,12 @@
 // kernel A: its CTAs set up and compute their first features while kernel A finishes, and wait
 // for it only where they read the increments.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 
 #include <cstring>
 
 #include "kernels.h"
 #include "tc_utils.cuh"
+#include "tensor_map.h"
 
 namespace rapt {
 namespace {
@@ -1091,31 +1091,6 @@ cudaError_t set_smem(K kernel, uint32_t bytes, unsigned long long& configured) {
   return e;
 }
 
-// Tensor map of a [rows, H, D] bf16 tensor (rows = B * L or T; v or out) with 64 x 1 x 128 boxes,
-// 128-byte swizzle: one box is one 64-column block of a chunk's tile in the operand layout.
-cudaError_t make_tile_map(CUtensorMap* map, const void* v, long rows, int H, int D) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (encode == nullptr) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                     cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
-      return e != cudaSuccess ? e : cudaErrorNotSupported;
-    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
-                              static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
-  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kC)};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(v), dims,
-                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <int D>
 cudaError_t launch_tc_d(const TcArgs& ta, cudaStream_t stream) {
   static unsigned long long cfg_a = 0, cfg_b = 0;
@@ -1127,8 +1102,8 @@ cudaError_t launch_tc_d(const TcArgs& ta, cudaStream_t stream) {
   if (units == 0) return cudaSuccess;
   CUtensorMap tmap_v, tmap_o;
   if (ta.p.v != nullptr && ta.p.total_rows > 0) {
-    e = make_tile_map(&tmap_v, ta.p.v, ta.p.total_rows, ta.p.H, D);
-    if (e == cudaSuccess) e = make_tile_map(&tmap_o, ta.p.out, ta.p.total_rows, ta.p.H, D);
+    e = make_rows_map(&tmap_v, ta.p.v, ta.p.total_rows, ta.p.H, D);
+    if (e == cudaSuccess) e = make_rows_map(&tmap_o, ta.p.out, ta.p.total_rows, ta.p.H, D);
     if (e != cudaSuccess) return e;
   } else {
     memset(&tmap_v, 0, sizeof(tmap_v));  // no rows: the kernels issue no copy

@@ -156,6 +156,22 @@ def test_rla_l2_matches_oracle(cuda_device, lib, B, L, H, d, dtype):
     assert O.relative_error(to_host(out), ref)[0] <= TOL[dtype]
 
 
+@pytest.mark.parametrize("B,L,H,d", [(4, 3000, 16, 64), (1, 4100, 40, 128), (3, 2000, 7, 128)])
+def test_rla_l2_tensor_core_splits(cuda_device, lib, B, L, H, d):
+    """bf16 shapes where the tensor-core L2 path cuts every (batch row, head) into token splits of
+    several 128-token tiles (the stage ring wraps), L not a multiple of 128 (the last tile reads
+    zeros past L and stores nothing there), and several batch rows (no tile crosses into the next
+    row). Sampled rows, including the first and the ragged last ones, of every (batch row, head)."""
+    q, k, v = draw(80 + L, (B, L, H, d), "bf16")
+    out = R.rla_l2_fwd(to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16"), eps=1e-6)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([np.arange(3), np.arange(L - 3, L),
+                                     np.random.default_rng(L).integers(0, L, 40)]))
+    ref = O.rla_l2(widen(q, "bf16"), widen(k, "bf16"), widen(v, "bf16"), 1e-6, rows=rows)
+    got = to_host(out)[:, rows]
+    assert O.relative_error(got, ref[:, rows])[0] <= TOL["bf16"]
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_disjoint_supports_exact_zero(cuda_device, lib, dtype):
     """Scores are exactly 0 when the positive supports of q' and k' are disjoint
