@@ -242,6 +242,47 @@ def time_steps(fn, steps, warmup, flush, min_warm_s=0.0, counter=None):
     return (ms, launches) if counter else ms
 
 
+def profile_case(args):
+    """One workload's calls, ``--warmup`` + ``--steps`` times with no timing, for an ncu capture
+    (``--only``): a small, single-purpose command whose launches are easy to select."""
+    import torch
+
+    from relu_linear_attention_gb300 import _build, _lib, binding as R, synthetic as syn
+
+    _build.ensure_built()
+    lib = _lib.load()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    if args.only == "prefill":
+        w = syn.prefill_bf16(seed=1)
+        q, k, v = (_bf(x, device) for x in (w.q, w.k, w.v))
+        gq, gk = (torch.from_numpy(x).to(device) for x in (w.gamma_q, w.gamma_k))
+        out = torch.empty_like(q)
+        call = lambda: R.rapt_prefill_fwd(q, k, v, gq, gk, out=out)
+    elif args.only == "varlen":
+        wv = syn.varlen_bf16(seed=2)
+        q, k, v = (_bf(x, device) for x in (wv.q, wv.k, wv.v))
+        cu = torch.from_numpy(wv.cu_seqlens).to(device)
+        g = torch.ones(64, dtype=torch.float32, device=device)
+        out = torch.empty_like(q)
+        msl = int(wv.lengths.max())
+        call = lambda: R.rapt_varlen_fwd(q, k, v, cu, g, g, max_seqlen=msl, out=out)
+    elif args.only == "l2":
+        wl = syn.l2_bf16(seed=4)
+        q, k, v = (_bf(x, device) for x in (wl.q, wl.k, wl.v))
+        out = torch.empty_like(q)
+        call = lambda: R.rla_l2_fwd(q, k, v, eps=1e-6, out=out)
+    else:
+        raise SystemExit("unknown --only case %r" % args.only)
+    n0 = lib.rapt_launch_counter()
+    for _ in range(args.warmup + args.steps):
+        call()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": args.only, "calls": args.warmup + args.steps,
+                      "launches": int(lib.rapt_launch_counter() - n0)}))
+    return 0
+
+
 def run_gpu(args, rank, world, local):
     import torch
     import torch.distributed as dist
@@ -371,7 +412,9 @@ def run_gpu(args, rank, world, local):
               "roofline": {"bound": "hbm", "achieved": l_bytes / (l_mean * 1e-3) / 1e9,
                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": l_bytes / (l_mean * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                           "tflops": l_flops / (l_mean * 1e-3) / 1e12}}
+                           "tflops": l_flops / (l_mean * 1e-3) / 1e12,
+                           "traffic": read_traffic("l2_tc_moments", "l2_tc_readout"),
+                           "kernels": "l2_tc_moments + l2_tc_reduce + l2_tc_readout (one call)"}}
     del lq, lk, lv, lo, ws
 
     # ---------------- CPU baseline: the fp64 oracle on a bounded sample (rank 0, N=1 only)
@@ -383,7 +426,7 @@ def run_gpu(args, rank, world, local):
                          "each, fp64 quadratic form, %.1f s; numpy BLAS threads = host cores"
                          % (pairs, secs)}
 
-    traffic = read_traffic("prefill_tc_kernel")
+    traffic = read_traffic("segment_state_kernel", "prefill_tc_kernel")
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -396,6 +439,8 @@ def run_gpu(args, rank, world, local):
                    "l2": "256 MiB write before every timed step, outside the CUDA events"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernels": "segment_state_kernel + prefill_tc_kernel (one call; the second is "
+                                "a programmatic dependent of the first, so the call is timed whole)",
                      "peak_source": "%s hbm_gbs (copy bandwidth)" % peak_src,
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "tensor_tflops_algorithmic": prefill_flops(B, L, H, d) / (mean_ms * 1e-3) / 1e12,
@@ -414,23 +459,27 @@ def run_gpu(args, rank, world, local):
     return 0
 
 
-def read_traffic(kernel: str):
-    """Per-launch DRAM bytes of ``kernel`` from the committed ncu summary, if it was taken on
-    the kernel source as it is now (the summary records a hash of the source file)."""
+def read_traffic(*kernels: str):
+    """DRAM bytes per call, summed over ``kernels`` (the launches of one call), from the committed
+    ncu summary; None unless every kernel has a row taken on its source as it is now (each row
+    records a hash of the source file)."""
     import hashlib
 
     table = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(table):
         return None
+    found = {}
     for line in open(table):
         parts = [p.strip() for p in line.strip().strip("|").split("|")]
-        if len(parts) >= 4 and parts[0] == kernel:
+        if len(parts) >= 4 and parts[0] in kernels:
             src = os.path.join(ROOT, "relu_linear_attention_gb300", "csrc", parts[1])
             if not os.path.exists(src):
                 return None
             h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-            return float(parts[3]) if h == parts[2] else None
-    return None
+            if h != parts[2]:
+                return None
+            found[parts[0]] = float(parts[3])
+    return sum(found.values()) if len(found) == len(kernels) else None
 
 
 def main(argv=None):
@@ -440,12 +489,16 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--oracle-seconds", type=float, default=15.0)
+    ap.add_argument("--only", choices=["prefill", "varlen", "l2"], default=None,
+                    help="run one workload's calls without timing (for an ncu capture)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.only is not None:
+        return profile_case(args)
     return run_gpu(args, rank, world, local)
 
 
