@@ -23,8 +23,15 @@
  *     and 16-byte aligned.
  *   - Layouts: dense "BSND" [B, L, H, d]; packed varlen "TND" [T, H, d]; decode [N, H, d].
  *     States are fp32 and key-major: S[..., i, j] = sum_t k'_t[i] v_t[j]  ([.., H, d, d]); z [.., H, d].
- *   - Output dtype = input dtype (bf16 results are rounded to nearest even); all arithmetic and
- *     all accumulation are fp32.
+ *   - Output dtype = input dtype (bf16 results are rounded to nearest even).
+ *   - Precision. fp32 inputs (and bf16 at d = 16 or 32): all arithmetic and all accumulation are
+ *     fp32. bf16 inputs at d = 64 or 128: the products of the chunked form run on the tensor cores
+ *     with bf16 operands and fp32 accumulation: q', k' and the masked in-chunk scores are rounded
+ *     to bf16, and the state enters the inter-chunk product as a bf16 copy; the state itself, z,
+ *     RMSNorm, RoPE and the Sum denominator stay fp32. The L2 readout (rla_l2_fwd) uses bf16 copies
+ *     of its fp32 moments. Decode is fp32 throughout.
+ *   - Inputs must be finite. Tiles are read whole, so a non-finite value anywhere in q, k or v
+ *     may make any output of the same call non-finite.
  *   - d must be one of 16, 32, 64, 128 (d_v = d_k = d).
  *   - Every call is asynchronous on `stream` (NULL = the legacy default stream), launches only on
  *     that stream, allocates no device memory and never synchronises.
@@ -160,7 +167,11 @@ rapt_status rapt_decode_step(const void* q, const void* k, const void* v, rapt_d
  *   q' = ReLU(q), k' = ReLU(k) (no norm, no RoPE); M_V = K'^T V, M_K = K'^T K' over all L tokens
  *   of each (batch row, head); out_t = q'_t M_V / (sqrt(q'_t^T M_K q'_t) + eps).
  *   q, k, v, out  [B, L, H, d] of `dtype`; eps finite, > 0 (1e-6).
- *   workspace     at least rla_l2_workspace_size() bytes (fp32 partial moments).
+ *   workspace     at least rla_l2_workspace_size() bytes (fp32 partial moments of the token
+ *                 splits; on the tensor-core path also their sum as the bf16 readout operand).
+ * bf16 with d = 64 or 128 runs on the tensor cores (tcgen05): [M_V | M_K] = K'^T [V | K'] and
+ * q'[M_V | M_K] are GEMMs with bf16 operands and fp32 accumulation. fp32, and bf16 with d = 16 or
+ * 32, run on CUDA cores in fp32.
  */
 size_t rla_l2_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype);
 rapt_status rla_l2_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
@@ -177,7 +188,10 @@ rapt_status rla_l2_fwd(const void* q, const void* k, const void* v, rapt_dtype d
  * Same arguments and result as rla_l2_fwd, minus the workspace: the fp32 partial moments live in
  * a fixed device array of RAPT_L2_NOALLOC_SCRATCH_BYTES compiled into the library (every GPU that
  * loads the library holds it until the process exits). The number of token splits is reduced
- * until the moments fit, so results equal rla_l2_fwd's up to fp32 summation order.
+ * until the moments fit. It always runs the CUDA-core path with fp32 moments: for fp32 inputs and
+ * bf16 at d = 16 or 32 its results equal rla_l2_fwd's up to fp32 summation order; for bf16 at
+ * d = 64 or 128 (where rla_l2_fwd uses the tensor cores and bf16 copies of the moments) both stay
+ * within the bf16 tolerance of the exact result.
  *   - Returns RAPT_ERR_WORKSPACE, before launching anything, when even one split does not fit:
  *     B * H * 2 * d * 2d * 4 bytes must not exceed RAPT_L2_NOALLOC_SCRATCH_BYTES (at d = 128,
  *     B * H <= 64).
