@@ -13,8 +13,8 @@
 //   out = O / (q'.z_{c-1} + rowsum(P~_c) + eps)
 //
 // The denominator stays on the CUDA cores in fp32: z is a column sum of k' kept in shared memory,
-// q'.z is formed while the features are computed, and the row sums of the masked, rounded scores
-// (the same weights the numerator uses) while P is converted.
+// q'.z is formed while the features are computed, and the row sums of the masked fp32 scores
+// while P is converted to the bf16 operand of the intra-chunk product.
 //
 // Kernel B is warp-specialised (768 threads, six warpgroups):
 //   warps 0-15  (producers): features of chunk c+1 into one of two q' buffers while the tensor
@@ -495,16 +495,20 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
     const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(a.k);
     const int pos_base = a.pos_offset + seg_start;
+    const long rstride = static_cast<long>(a.H) * D;  // elements from one token row to the next
+    const long off0 = (row0 + seg_start + prow) * rstride + static_cast<long>(h) * D + e0;
+    const __nv_bfloat16* qrow = qg + off0;
+    const __nv_bfloat16* krow = kg + off0;
     auto load = [&](int c, int p, uint4& xq, uint4& xk) {
-      const int lt = c * kC + p * RPP + prow;
-      if (lt < seg_n) {
-        const long off = ((row0 + seg_start + lt) * a.H + h) * D + e0;
-        xq = ldg16(qg + off);
-        xk = ldg16(kg + off);
+      if (c * kC + p * RPP + prow < seg_n) {
+        const long off = static_cast<long>(c * kC + p * RPP) * rstride;
+        xq = ldg16(qrow + off);
+        xk = ldg16(krow + off);
       } else {
         xq = xk = make_uint4(0, 0, 0, 0);
       }
     };
+    Rot rot;  // RoPE cos / sin of this thread's current row
     uint4 rq[RING], rk[RING];
     if (nchunks > 0) {
 #pragma unroll
@@ -529,8 +533,15 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       uint4 kreg[NPASS];
       float2 zca[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       float2 zcb[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      Rot rot;
-      tab_rot_at(tab, pos_base + c * kC + prow, e0 / 2, rot);
+      // angles of the chunk's first row: exact every 8 chunks, otherwise one more step of the
+      // incremental rotation from the previous chunk's last pass (RPP positions further down)
+      if ((c & 7) == 0) {
+        tab_rot_at(tab, pos_base + c * kC + prow, e0 / 2, rot);
+      } else {
+        Rot step;
+        tab_step(tab, e0 / 2, step);
+        rot_step(rot, step);
+      }
 #pragma unroll
       for (int p = 0; p < NPASS; ++p) {
         const uint4 xq = rq[p % RING], xk = rk[p % RING];
@@ -640,7 +651,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           }
         }
       }
-      // ---- P -> masked bf16 P~ and its row sums (of the rounded values the numerator uses)
+      // ---- P -> masked bf16 P~, and the row sums of the masked fp32 scores
       ok = tc::mbar_wait(bar_a, c & 1, kWaitCycles);
       ok &= tc::mbar_wait(bar_full + 8 * s, (c >> 1) & 1, kWaitCycles);  // the q'.z values
       if (__any_sync(0xffffffffu, !ok)) bad = 1;
@@ -678,8 +689,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                 x1 = tau + 1 <= er ? x1 : 0.f;
               }
               w[e] = tc::pack_bf16x2(x0, x1);
-              const float2 r2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
-              rs += r2.x + r2.y;
+              rs += x0 + x1;
             }
             sts16(blk + tc::sw128(er, cc + 2 * m), make_uint4(w[0], w[1], w[2], w[3]));
             sts16(blk + tc::sw128(er, cc + 2 * m + 1), make_uint4(w[4], w[5], w[6], w[7]));
@@ -964,9 +974,12 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     tab_step(tab, e0 / 2, step);
     const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(a.k);
     const int pos_base = a.pos_offset + seg_start;
+    const long rstride = static_cast<long>(a.H) * D;
+    const __nv_bfloat16* krow = kg + (row0 + seg_start + prow) * rstride + static_cast<long>(h) * D + e0;
     auto load = [&](int c, int p, uint4& xk) {
-      xk = ldg16(kg + ((row0 + seg_start + c * kC + p * RPP + prow) * a.H + h) * D + e0);
+      xk = ldg16(krow + static_cast<long>(c * kC + p * RPP) * rstride);
     };
+    Rot rot;
     float2 zca[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     float2 zcb[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     uint4 rk[RING];
@@ -984,8 +997,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
           tc::tma_load_3d(vb + jb * 16384, &tmap_v, 64 * jb, h,
                           static_cast<int>(row0 + seg_start + c * kC), bar_vfull + 8 * s);
       }
-      Rot rot;
-      tab_rot_at(tab, pos_base + c * kC + prow, e0 / 2, rot);
+      if ((c & 7) == 0) tab_rot_at(tab, pos_base + c * kC + prow, e0 / 2, rot);
+      else rot_step(rot, step);
 #pragma unroll
       for (int p = 0; p < NPASS; ++p) {
         const uint4 xk = rk[p % RING];
