@@ -15,9 +15,11 @@
 //   2. reduce: the partials summed in split order, written as the bf16 [M_V | M_K] operand of
 //      launch 3 in the exact shared-memory layout the tensor core reads (one bulk copy there);
 //   3. readout (one CTA per batch row, head and token split): q tiles by TMA, ReLU in place, one
-//      GEMM per 128-token tile into one of two TMEM accumulators, and an epilogue that forms
-//      den = sqrt(sum_j q'_j (q'M_K)_j) + eps from the same bf16 q' the GEMM read, writes
-//      out = num / den over the q tile and hands it to a thread that stores it by TMA.
+//      GEMM per 128-token tile into one of two TMEM accumulators; eight epilogue warps (two per
+//      row, half of the columns each) form den = sqrt(sum_j q'_j (q'M_K)_j) + eps from the same
+//      bf16 q' the GEMM read and write out = num / den over the q tile; one thread stores it by TMA.
+// Launches 2 and 3 are programmatic dependents of the launch before them (set-up and the first
+// q tiles overlap the predecessor's tail).
 // Tensor maps are 4-D ([B, L, H, d]), so tiles past the end of a batch row read as zero and are
 // not written back. Every wait is bounded; a CTA whose wait gives up writes NaN results (the
 // moments of its split, or its output rows), so a failure cannot pass for a result.
@@ -35,7 +37,7 @@ namespace {
 constexpr int kC = 128;                        // tokens per tile = MMA M (readout) or K (moments)
 constexpr long long kWait = 2000000000LL;      // ~1 s
 constexpr int kP1Threads = 192;                // warps 0-3: ReLU + epilogue; 4: TMA; 5: MMA
-constexpr int kP2Threads = 320;                // warps 0-3: epilogue; 4-7: ReLU; 8: TMA; 9: MMA
+constexpr int kP2Threads = 448;                // warps 0-7: epilogue; 8-11: ReLU; 12: TMA; 13: MMA
 constexpr int kStages = 3;
 
 // In-place ReLU of 8 bf16 values.
@@ -49,6 +51,17 @@ __device__ __forceinline__ uint4 relu8(uint4 x) {
     w[i] = *reinterpret_cast<uint32_t*>(&v);
   }
   return x;
+}
+// bar.sync over a group, returning the OR of every member's flag (so all members agree).
+__device__ __forceinline__ int group_sync_or(uint32_t id, uint32_t n, int flag) {
+  int r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.s32 p, %3, 0;\n bar.red.or.pred q, %1, %2, p;\n"
+      " selp.s32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(id), "r"(n), "r"(flag)
+      : "memory");
+  return r;
 }
 __device__ __forceinline__ uint4 lds16(uint32_t addr) {
   uint4 v;
@@ -85,6 +98,7 @@ __global__ void __launch_bounds__(kP1Threads, 1)
   using L = P1<D>;
   constexpr int S = kStages, N = L::N;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  tc::grid_launch_dependents();  // the reduce launch may be scheduled; it waits for this grid
   const int sp = blockIdx.x % nsplit, bh = blockIdx.x / nsplit;
   const int b = bh / a.H, h = bh % a.H;
   const int t0 = sp * split_len;
@@ -217,6 +231,8 @@ __global__ void __launch_bounds__(256) l2_tc_reduce(const float* ws, int nsplit,
   constexpr int N = 2 * D;
   constexpr int Q = D * N / 4;  // float4 per partial
   const int bh = blockIdx.y;
+  tc::grid_launch_dependents();  // the readout may set up and load its first q tiles
+  tc::grid_dep_wait();           // the partials of the moments launch
   const float4* p = reinterpret_cast<const float4*>(ws) + static_cast<long>(bh) * nsplit * Q;
   uint8_t* img = reinterpret_cast<uint8_t*>(const_cast<float*>(ws) + img_offset) + static_cast<long>(bh) * D * N * 2;
   for (int e = blockIdx.x * 256 + threadIdx.x; e < Q; e += gridDim.x * 256) {
@@ -233,30 +249,35 @@ __global__ void __launch_bounds__(256) l2_tc_reduce(const float* ws, int nsplit,
 }
 
 // ------------------------------------------------------------------------------------------------
-// Launch 3: readout. Shared memory: the [M_V | M_K] image, then kStages q tiles (each 128 tokens x d,
-// K-major blocks of 64 columns); the epilogue writes out over the tile it read q' from.
+// Launch 3: readout. Shared memory: the [M_V | M_K] image, kStages q tiles (each 128 tokens x d,
+// K-major blocks of 64 columns; out is written over the tile q' was read from), and the partial
+// den^2 of the two column halves of every row. Warps 0-7 are the epilogue, two per TMEM lane
+// quarter (warp % 4), each taking half of a row's columns; warps 8-11 apply the ReLU.
 template <int D>
 struct P2 {
   static constexpr int DB = D / 64;
   static constexpr int N = 2 * D;
+  static constexpr int HALF = D / 2;
   static constexpr uint32_t MB = (N / 64) * D * 128;
   static constexpr uint32_t QT = DB * 16384;
   static constexpr uint32_t QS = MB;
+  static constexpr uint32_t DP = QS + kStages * QT;         // partial den^2 [2 halves][128 rows]
   // mfull, qfull[S], relu[S], staged[S], accf[2], accfree[2]
-  static constexpr uint32_t BAR = QS + kStages * QT;
+  static constexpr uint32_t BAR = DP + 2 * kC * 4;
   static constexpr uint32_t MISC = BAR + (1 + 3 * kStages + 4) * 8;
   static constexpr uint32_t BYTES = MISC + 16;
   static_assert(MB % 1024 == 0 && QT % 1024 == 0, "tile alignment");
   static_assert(BYTES <= 232448, "shared memory budget");
   static_assert(2 * N <= 512, "TMEM budget");
 };
+constexpr uint32_t kBarEpi = 1;  // named barrier of the 256 epilogue threads
 
 template <int D>
 __global__ void __launch_bounds__(kP2Threads, 1)
     l2_tc_readout(const L2Args a, int nsplit, int split_chunks, long img_offset,
                   const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap to) {
   using L = P2<D>;
-  constexpr int S = kStages, N = L::N;
+  constexpr int S = kStages, N = L::N, HALF = L::HALF;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sp = blockIdx.x % nsplit, bh = blockIdx.x / nsplit;
   const int b = bh / a.H, h = bh % a.H;
@@ -270,6 +291,7 @@ __global__ void __launch_bounds__(kP2Threads, 1)
   const uint32_t base = tc::smem_u32(smem);
   const uint32_t bar_m = base + L::BAR, bar_qfull = bar_m + 8, bar_relu = bar_qfull + 8 * S;
   const uint32_t bar_staged = bar_relu + 8 * S, bar_accf = bar_staged + 8 * S, bar_accfree = bar_accf + 16;
+  float* dpart = reinterpret_cast<float*>(smem + L::DP);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::MISC);
   int* s_abort = reinterpret_cast<int*>(smem + L::MISC + 4);
   const bool misaligned = (base & 1023u) != 0;
@@ -283,11 +305,11 @@ __global__ void __launch_bounds__(kP2Threads, 1)
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(bar_qfull + 8 * s, 1);
       tc::mbar_init(bar_relu + 8 * s, 128);
-      tc::mbar_init(bar_staged + 8 * s, 128);
+      tc::mbar_init(bar_staged + 8 * s, 256);
     }
     for (int x = 0; x < 2; ++x) {
       tc::mbar_init(bar_accf + 8 * x, 1);
-      tc::mbar_init(bar_accfree + 8 * x, 128);
+      tc::mbar_init(bar_accfree + 8 * x, 256);
     }
     tc::mbar_fence_init();
     *s_abort = misaligned ? 1 : 0;
@@ -299,17 +321,14 @@ __global__ void __launch_bounds__(kP2Threads, 1)
   const bool run = !*s_abort;
   auto tile = [&](int s) { return base + L::QS + s * L::QT; };
 
-  if (warp == 8) {
-    if (lane == 0 && run) {  // TMA: the moments once, then q tiles in and out tiles back
-      tc::mbar_arrive_expect_tx(bar_m, L::MB);
-      tc::bulk_g2s(base, img, L::MB, bar_m);
-      for (int i = 0; i < n + S; ++i) {
+  if (warp == 12) {
+    if (lane == 0 && run) {  // TMA: q tiles in, out tiles back, and the moments once
+      int ok = 1;
+      for (int i = 0; i < n + S && ok; ++i) {
         if (i >= S) {  // the tile S back is staged: store it, then its buffer is free
           const int j = i - S, s = j % S;
-          if (!tc::mbar_wait(bar_staged + 8 * s, (j / S) & 1, kWait)) {
-            atomicExch(s_abort, 1);
-            break;
-          }
+          ok = tc::mbar_wait(bar_staged + 8 * s, (j / S) & 1, kWait);
+          if (!ok) break;
 #pragma unroll
           for (int jb = 0; jb < L::DB; ++jb)
             tc::tma_store_4d(&to, tile(s) + jb * 16384, 64 * jb, h, (c0 + j) * kC, b);
@@ -323,10 +342,17 @@ __global__ void __launch_bounds__(kP2Threads, 1)
           for (int jb = 0; jb < L::DB; ++jb)
             tc::tma_load_4d(tile(s) + jb * 16384, &tq, 64 * jb, h, (c0 + i) * kC, b, bar_qfull + 8 * s);
         }
+        if (i == 0) {
+          // the moments come from the reduce launch, which may still be running
+          tc::grid_dep_wait();
+          tc::mbar_arrive_expect_tx(bar_m, L::MB);
+          tc::bulk_g2s(base, img, L::MB, bar_m);
+        }
       }
+      if (!ok) atomicExch(s_abort, 1);
       tc::bulk_wait0();
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     if (lane == 0 && run) {  // MMA: [num | q'M_K] = Q' [M_V | M_K], M = 128 tokens, N = 2d, K = d
       constexpr uint32_t ID = tc::idesc_bf16(128, N, false, true);
       const uint64_t dm = tc::desc_sw128(base, D * 128, 1024);
@@ -347,9 +373,9 @@ __global__ void __launch_bounds__(kP2Threads, 1)
       }
       if (!ok) atomicExch(s_abort, 1);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 8) {
     if (run) {  // ReLU of the q tiles, in place
-      const int rt = tid - 128;
+      const int rt = tid - 256;
       for (int i = 0; i < n; ++i) {
         const int s = i % S;
         if (!tc::mbar_wait(bar_qfull + 8 * s, (i / S) & 1, kWait)) {
@@ -364,23 +390,26 @@ __global__ void __launch_bounds__(kP2Threads, 1)
       }
     }
   } else if (run) {
-    // epilogue: TMEM lane = token row er of the tile
-    const int er = 32 * warp + lane;
-    const uint32_t tl = static_cast<uint32_t>(32 * warp) << 16;
+    // epilogue: TMEM lane = token row er of the tile; this thread owns columns [c0h, c0h + HALF)
+    const int q4 = warp & 3, g = warp >> 2;
+    const int er = 32 * q4 + lane;
+    const int c0h = g * HALF;
+    const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
     for (int i = 0; i < n; ++i) {
       const int s = i % S, x = i & 1;
       const int ok = tc::mbar_wait(bar_accf + 8 * x, (i >> 1) & 1, kWait);
-      if (!__all_sync(0xffffffffu, ok)) {
+      // uniform over the 256 epilogue threads (the named barriers below need all of them)
+      if (group_sync_or(kBarEpi, 256, !ok)) {
         atomicExch(s_abort, 1);
         break;
       }
       tc::fence_after_sync();
       const uint32_t acc = tmem + tl + x * N;
       const uint32_t qb = tile(s);
-      // den^2 = q'^T M_K q' = sum_j q'_j (q'M_K)_j, with the bf16 q' of the GEMM
+      // partial den^2 over this half: sum_j q'_j (q'M_K)_j with the bf16 q' of the GEMM
       float2 d2 = make_float2(0.f, 0.f);
 #pragma unroll 1
-      for (int j0 = 0; j0 < D; j0 += 16) {
+      for (int j0 = c0h; j0 < c0h + HALF; j0 += 16) {
         uint32_t y[16];
         tc::tmem_ld16(acc + D + j0, y);
         const uint32_t blk = qb + static_cast<uint32_t>(j0 / 64) * 16384;
@@ -393,10 +422,12 @@ __global__ void __launch_bounds__(kP2Threads, 1)
           d2 = __ffma2_rn(make_float2(__uint_as_float(qw[e] << 16), __uint_as_float(qw[e] & 0xffff0000u)),
                           make_float2(__uint_as_float(y[2 * e]), __uint_as_float(y[2 * e + 1])), d2);
       }
-      const float inv = 1.0f / (sqrtf(d2.x + d2.y) + a.eps);
-      // out = num / den over this row of the tile (only this thread reads or writes the row)
+      dpart[g * kC + er] = d2.x + d2.y;
+      tc::named_sync(kBarEpi, 256);
+      const float inv = 1.0f / (sqrtf(dpart[er] + dpart[kC + er]) + a.eps);  // fixed order
+      // out = num / den over this half of the row (the bytes this thread read q' from)
 #pragma unroll 1
-      for (int j0 = 0; j0 < D; j0 += 16) {
+      for (int j0 = c0h; j0 < c0h + HALF; j0 += 16) {
         uint32_t u[16];
         tc::tmem_ld16(acc + j0, u);
         tc::tmem_wait_ld();
@@ -473,15 +504,28 @@ cudaError_t launch_l2_tc_d(const L2Args& a, cudaStream_t stream) {
   note_launches(1);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  // the reduce and the readout are programmatic dependents of the launch before them: each starts
+  // while its predecessor finishes and waits for it (griddepcontrol.wait) before reading its output
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
   const int q4 = D * 2 * D / 4;
-  l2_tc_reduce<D><<<dim3(static_cast<unsigned>((q4 + 255) / 256), static_cast<unsigned>(n_bh)), 256, 0, stream>>>(
-      a.ws, nsplit, img_offset);
+  cfg.gridDim = dim3(static_cast<unsigned>((q4 + 255) / 256), static_cast<unsigned>(n_bh));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, l2_tc_reduce<D>, static_cast<const float*>(a.ws), nsplit, img_offset);
   note_launches(1);
-  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  l2_tc_readout<D><<<static_cast<unsigned>(n_bh * nsplit), kP2Threads, P2<D>::BYTES, stream>>>(
-      a, nsplit, split_chunks, img_offset, tq, to);
+  cfg.gridDim = dim3(static_cast<unsigned>(n_bh * nsplit));
+  cfg.blockDim = dim3(kP2Threads);
+  cfg.dynamicSmemBytes = P2<D>::BYTES;
+  e = cudaLaunchKernelEx(&cfg, l2_tc_readout<D>, a, nsplit, split_chunks, img_offset, tq, to);
   note_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
