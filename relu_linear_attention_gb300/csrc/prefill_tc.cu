@@ -297,7 +297,9 @@ __device__ __forceinline__ void pairs_to8(const Pairs& p, float* f) {
 // and for every RoPE pair the frequency (hi, lo turns) and the cos / sin of the rotation over
 // one producer pass (RPP positions). Gains are stored "split": the first 4 of a thread's 8
 // values for every thread part, then the last 4, so that a warp's 16-byte reads are contiguous
-// (no bank conflicts); split_idx maps an element index to that layout.
+// (no bank conflicts); inside each 4 the order is (pair 0 first, pair 1 first, pair 0 second,
+// pair 1 second), so that a 16-byte read lands directly on the float2 pairs the arithmetic uses.
+// split_idx maps an element index to that layout.
 struct FeatTab {
   float* gq;   // [D]
   float* gk;   // [D]
@@ -313,7 +315,7 @@ __device__ __forceinline__ FeatTab feat_tab(uint8_t* p) {
 }
 template <int D>
 __device__ __forceinline__ int split_idx(int i) {
-  return (i & 4) * (D / 8) + (i >> 3) * 4 + (i & 3);
+  return (i & 4) * (D / 8) + (i >> 3) * 4 + (((i & 1) << 1) | ((i >> 1) & 1));
 }
 template <int D>
 __device__ __forceinline__ void fill_tab(const FeatTab& t, const PrefillArgs& a, int h, int rpp,
@@ -336,10 +338,10 @@ template <int D>
 __device__ __forceinline__ void split_load(const float* t, int part, float2 (&x0)[2], float2 (&x1)[2]) {
   const float4 a = *reinterpret_cast<const float4*>(t + 4 * part);
   const float4 b = *reinterpret_cast<const float4*>(t + D / 2 + 4 * part);
-  x0[0] = make_float2(a.x, a.z);
-  x1[0] = make_float2(a.y, a.w);
-  x0[1] = make_float2(b.x, b.z);
-  x1[1] = make_float2(b.y, b.w);
+  x0[0] = make_float2(a.x, a.y);
+  x1[0] = make_float2(a.z, a.w);
+  x0[1] = make_float2(b.x, b.y);
+  x1[1] = make_float2(b.z, b.w);
 }
 __device__ __forceinline__ void tab_step(const FeatTab& t, int j0, Rot& st) {
   const float4 c = *reinterpret_cast<const float4*>(t.stc + j0);
