@@ -908,7 +908,9 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     segment_state_kernel(const TcArgs ta, const __grid_constant__ CUtensorMap tmap_v) {
   using L = LayA<D>;
   using PM = Prod<D>;
-  constexpr int TPR = PM::TPR, RPP = PM::RPP, NPASS = PM::NPASS, RING = PM::RING;
+  // a whole chunk of k loads in flight: this kernel's passes are short, so two would not cover
+  // the memory latency
+  constexpr int TPR = PM::TPR, RPP = PM::RPP, NPASS = PM::NPASS, RING = PM::NPASS;
   const PrefillArgs& a = ta.p;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1023,7 +1025,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
       tc::fence_async_smem();
       tc::mbar_arrive(bar_full + 8 * s);
       if (bad) atomicExch(s_abort, 1);
-      if (group_sync_or(kBarProd, kProd, *s_abort)) break;
+      if (__any_sync(0xffffffffu, *reinterpret_cast<volatile int*>(s_abort))) break;
     }
     // sums of k' over the segment (fixed order: deterministic)
     float zc[8];
