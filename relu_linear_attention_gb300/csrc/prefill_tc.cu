@@ -25,10 +25,12 @@
 //                            row sums, then the output epilogue from one of two O accumulators;
 //   warp 20     (issuer):    one thread issues the MMAs (an issue blocks while the tensor core is
 //                            busy, so it gets a warp of its own);
-//   warps 21-22 (helpers):   z_c = z_{c-1} + the producer warps' column sums of k'_c, so that the
-//                            producers never wait for one another;
-//   warp 23     (store):     one thread writes each staged output tile with TMA stores and, once the
-//                            store has read the buffer, loads the v tile of two chunks later into it.
+//   warp 21     (store):     one thread writes each staged output tile with TMA stores and, once the
+//                            store has read the buffer, loads the v tile of two chunks later into it;
+//   warps 22-23 (helpers):   z_c = z_{c-1} + the producer warps' column sums of k'_c, so that the
+//                            producers never wait for one another, and half of the score conversion
+//                            of TMEM lane quarters 2 and 3 (the rows whose masked scores span the
+//                            most columns).
 // v tiles need no transformation: the tensor-memory accelerator (TMA) copies them from HBM straight
 // into the swizzled operand layout, one chunk ahead. q and k go through registers (a short load
 // ring) because the features are computed on the way.
@@ -113,10 +115,11 @@ struct LayB {
   static constexpr uint32_t ZP = SS + (D / 64) * D * 128;      // z partials [2][producer warps][D] fp32
   static constexpr uint32_t ZS = ZP + 2 * Prod<D>::WARPS * D * 4;  // z [D] fp32
   static constexpr uint32_t DI = ZS + D * 4;                   // q'.z [2][128] fp32
-  static constexpr uint32_t TAB = DI + 2 * kC * 4;             // feature tables (FeatTab)
-  // full0 full1 empty0 empty1 vfull0 vfull1 s_done a_done b_done conv_done z_ready staged0 staged1
+  static constexpr uint32_t RSH = DI + 2 * kC * 4;             // helpers' partial row sums [128]
+  static constexpr uint32_t TAB = RSH + kC * 4;                // feature tables (FeatTab)
+  // full0 full1 empty0 empty1 vfull0 vfull1 s_done a_done b_done conv_done z_ready staged0 staged1 hp
   static constexpr uint32_t BAR = TAB + 8 * D * 4;
-  static constexpr uint32_t MISC = BAR + 13 * 8;               // TMEM base, abort flag
+  static constexpr uint32_t MISC = BAR + 14 * 8;               // TMEM base, abort flag
   static constexpr uint32_t BYTES = MISC + 16;
   // TMEM columns: P, two O accumulators, S
   static constexpr uint32_t TP = 0, TO0 = 128, TO1 = 128 + D, TS = 128 + 2 * D;
@@ -411,6 +414,36 @@ __device__ __forceinline__ void init_state(const PrefillArgs& a, const float* ws
   }
 }
 
+// One group of 32 score columns [col, col + 32) of the calling thread's tile row er: P (fp32, TMEM
+// at tp + col) -> bf16 P~ in the swizzled operand at pb, masked to tau <= er on the diagonal group;
+// the masked fp32 scores are added to rs.
+__device__ __forceinline__ void convert_p_group(uint32_t tp, uint32_t pb, int col, int er, bool diag, float& rs) {
+  const uint32_t blk = pb + (col / 64) * 16384;
+  const int cc = (col % 64) / 8;
+  uint32_t u[2][16];
+  tc::tmem_ld16(tp + col, u[0]);
+  tc::tmem_ld16(tp + col + 16, u[1]);
+  tc::tmem_wait_ld();
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    uint32_t w[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int tau = col + 16 * m + 2 * e;
+      float x0 = __uint_as_float(u[m][2 * e]);
+      float x1 = __uint_as_float(u[m][2 * e + 1]);
+      if (diag) {
+        x0 = tau <= er ? x0 : 0.f;
+        x1 = tau + 1 <= er ? x1 : 0.f;
+      }
+      w[e] = tc::pack_bf16x2(x0, x1);
+      rs += x0 + x1;
+    }
+    sts16(blk + tc::sw128(er, cc + 2 * m), make_uint4(w[0], w[1], w[2], w[3]));
+    sts16(blk + tc::sw128(er, cc + 2 * m + 1), make_uint4(w[4], w[5], w[6], w[7]));
+  }
+}
+
 // ------------------------------------------------------------------------------------------------
 // Kernel B: one CTA per (document, head, segment).
 template <int D>
@@ -451,6 +484,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const uint32_t bar_full = base + L::BAR, bar_empty = bar_full + 16, bar_vfull = bar_full + 32;
   const uint32_t bar_s = bar_full + 48, bar_a = bar_full + 56, bar_b = bar_full + 64;
   const uint32_t bar_conv = bar_full + 72, bar_zr = bar_full + 80, bar_staged = bar_full + 88;
+  const uint32_t bar_hp = bar_full + 104;  // helpers' half of the score conversion done
+  float* rsh = reinterpret_cast<float*>(smem + L::RSH);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::MISC);
   int* s_abort = reinterpret_cast<int*>(smem + L::MISC + 4);
 
@@ -468,7 +503,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     tc::mbar_init(bar_s, 1);
     tc::mbar_init(bar_a, 1);
     tc::mbar_init(bar_b, 1);
-    tc::mbar_init(bar_conv, kCons);
+    tc::mbar_init(bar_conv, kCons + kHelp);
+    tc::mbar_init(bar_hp, kHelp);
     tc::mbar_init(bar_zr, kHelp);
     tc::mbar_init(bar_staged, kCons);
     tc::mbar_init(bar_staged + 8, kCons);
@@ -664,38 +700,23 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         float rs = 0.f;
         // Column groups of 32 scores: those left of this warp's rows (col < 32 q4) are fully
         // visible, the group col == 32 q4 holds the diagonal, the rest are above it (all zero).
+        // Lane quarters 2 and 3 have a helper warp that converts their odd groups.
 #pragma unroll 1
         for (int col = 0; col < kC; col += 32) {
-          const uint32_t blk = pb + (col / 64) * 16384;
-          const int cc = (col % 64) / 8;
           if (col > 32 * q4) {  // warp-uniform: strictly above the diagonal
+            const uint32_t blk = pb + (col / 64) * 16384;
+            const int cc = (col % 64) / 8;
 #pragma unroll
             for (int m = 0; m < 4; ++m) sts16(blk + tc::sw128(er, cc + m), make_uint4(0, 0, 0, 0));
             continue;
           }
-          uint32_t u[2][16];
-          tc::tmem_ld16(tmem + tl + L::TP + col, u[0]);
-          tc::tmem_ld16(tmem + tl + L::TP + col + 16, u[1]);
-          tc::tmem_wait_ld();
-          const bool diag = col == 32 * q4;
-#pragma unroll
-          for (int m = 0; m < 2; ++m) {
-            uint32_t w[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int tau = col + 16 * m + 2 * e;
-              float x0 = __uint_as_float(u[m][2 * e]);
-              float x1 = __uint_as_float(u[m][2 * e + 1]);
-              if (diag) {
-                x0 = tau <= er ? x0 : 0.f;
-                x1 = tau + 1 <= er ? x1 : 0.f;
-              }
-              w[e] = tc::pack_bf16x2(x0, x1);
-              rs += x0 + x1;
-            }
-            sts16(blk + tc::sw128(er, cc + 2 * m), make_uint4(w[0], w[1], w[2], w[3]));
-            sts16(blk + tc::sw128(er, cc + 2 * m + 1), make_uint4(w[4], w[5], w[6], w[7]));
-          }
+          if (q4 >= 2 && ((col >> 5) & 1)) continue;  // the helper's group
+          convert_p_group(tmem + tl + L::TP, pb, col, er, col == 32 * q4, rs);
+        }
+        if (q4 >= 2) {  // add the helper's partial row sum
+          const int okh = tc::mbar_wait(bar_hp, c & 1, kWaitCycles);
+          if (__any_sync(0xffffffffu, !okh)) bad = 1;
+          rs += rsh[er];
         }
         den = di[s * kC + er] + rs + a.eps_den;
       }
@@ -760,8 +781,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                                __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3]));
       }
     }
-    } else if (warp == (kProd + kCons) / 32 + 3) {
-      // ========================================================== output stores (warp 23)
+    } else if (warp == (kProd + kCons) / 32 + 1) {
+      // ========================================================== output stores (warp 21)
       init(D / 2);
       if (lane == 0) {
         int ok = 1;
@@ -789,10 +810,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         tc::bulk_wait0();
         if (!ok) atomicExch(s_abort, 1);
       }
-    } else if (warp > (kProd + kCons) / 32) {
-      // ========================================================== helpers (warps 21-22)
+    } else if (warp > (kProd + kCons) / 32 + 1) {
+      // ========================================================== helpers (warps 22-23)
       init(D / 2);
-      const int ht = tid - (kProd + kCons + 32);
+      const int ht = tid - (kProd + kCons + 64);
+      const int q4 = warp & 3;                 // TMEM lane quarter (2 or 3)
+      const int er = 32 * q4 + lane;           // tile row
+      const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
       // z at the segment start: z0 + the sums of k' of the blocks before the segment
       for (int i = ht; i < D; i += kHelp) {
         float z = a.z0 != nullptr ? a.z0[bh * D + i] : 0.f;
@@ -818,6 +842,23 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           zs[split_idx<D>(i)] = z;
         }
         tc::mbar_arrive(bar_zr);
+        // the odd groups of this lane quarter's score conversion (its consumer warp takes the
+        // even ones), with their masked fp32 row sums
+        const int okp = tc::mbar_wait(bar_a, c & 1, kWaitCycles);
+        if (!__all_sync(0xffffffffu, okp)) {  // both helper warps leave at the next group check
+          bad = 1;
+          continue;
+        }
+        tc::fence_after_sync();
+        const uint32_t pb = D == 128 ? base + (s ? L::Q1 : L::Q0) : base + L::PS;
+        float rs = 0.f;
+        for (int col = 32; col <= 32 * q4; col += 64)
+          convert_p_group(tmem + tl + L::TP, pb, col, er, col == 32 * q4, rs);
+        rsh[er] = rs;
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        tc::mbar_arrive(bar_conv);
+        tc::mbar_arrive(bar_hp);
       }
       if (bad) atomicExch(s_abort, 1);
       tc::named_sync(kBarHelp, kHelp);
