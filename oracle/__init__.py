@@ -16,6 +16,8 @@ library matmul as its only building block. Sources (titles of the pages):
   document boundaries), §3 (RLA-2 core formula, eps 1e-4), §4.1 (inclusive
   prefix i <= t within the same document), §4.2 (forward_step: features,
   update the state first, then read out).
+  §4.1 also fixes the non-causal (bidirectional) mode: the same sums taken over the
+  whole document, one constant for every query.
 * ruDNN README (docs.rs ruDNN 0.1.93), §7: RMSNorm statistics in fp32 over the
   last axis, gamma an fp32 vector, epsilon finite and positive; §8: fp32
   initial/final state per sequence, never overwritten in place.
@@ -30,7 +32,8 @@ weights in [0, 1) with v == 1, convex-hull bounds, RoPE norm preservation and
 relative-position property, RMSNorm scale invariance and norm identity, the
 L = 1 and constant-v closed forms, linearity in v, the L2 identity
 sum(s^2) = q'^T (K'^T K') q', varlen == per-document dense runs, decode ==
-last prefill row, and an independent pure-Python brute force on L <= 16.
+last prefill row, bidirectional == causal on the last row and invariant under
+any reordering of the keys, and an independent pure-Python brute force on L <= 16.
 The RoPE frequency schedule theta_j = base^(-2j/d) is the textbook one; the
 pages name the base and the pairing but print no frequency formula, so the
 schedule is pinned only through its properties (pair 0 turns by exactly p
@@ -48,6 +51,9 @@ from .rla2 import (  # noqa: F401
     rla2_varlen,
     rla2_decode_step,
     rla2_decode_from_history,
+    rla2_bidir_doc,
+    rla2_bidir,
+    rla2_bidir_varlen,
     rla_l2,
     relative_error,
 )

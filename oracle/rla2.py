@@ -239,6 +239,72 @@ def rla2_decode_from_history(q_new, k_hist, v_hist, pos_new, gamma_q, gamma_k, e
     return (s @ _f64(v_hist)) / (s.sum() + float(eps_den))
 
 
+def rla2_bidir_doc(qf, kf, v, eps_den=1e-4, rows=None):
+    """Bidirectional (non-causal) RLA-2 output of one head of one document, quadratic form.
+
+    out_t = sum_{tau in doc} s_{t,tau} v_tau / (sum_{tau in doc} s_{t,tau} + eps_den),
+    s = q'_t . k'_tau: every token of the document is seen by every query.
+    08-rapt-algorithm.md §4.1 (the prefix scan's causal=false mode: the sums over the whole set,
+    one constant for every t) and §4.2 (the bidirectional branch of the Sum-denominator layer),
+    with the RLA-2 Sum denominator and eps of §3. qf, kf, v: [n, d]; ``rows``: optional query
+    indices (default all).
+    """
+    qf, kf, v = _f64(qf), _f64(kf), _f64(v)
+    n = qf.shape[0]
+    rows = np.arange(n) if rows is None else np.asarray(rows, dtype=np.int64)
+    out = np.zeros((len(rows), v.shape[1]), dtype=np.float64)
+    for r0 in range(0, len(rows), _ROW_BLOCK):
+        rr = rows[r0:r0 + _ROW_BLOCK]
+        s = qf[rr] @ kf.T  # [rows, n]
+        out[r0:r0 + len(rr)] = (s @ v) / (s.sum(axis=1) + float(eps_den))[:, None]
+    return out
+
+
+def rla2_bidir(q, k, v, gamma_q, gamma_k, eps_norm=1e-6, rope_base=1e4, eps_den=1e-4,
+               pos_offset=0, pairs=None, rows=None):
+    """Dense bidirectional RLA-2: q, k, v [B, L, H, d], one sequence per batch row, token t at
+    RoPE position pos_offset + t; features as in the causal form (08-rapt-algorithm.md §4.2).
+    ``pairs`` / ``rows`` restrict the evaluation; other entries are NaN.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, L, H, d = q.shape
+    out = np.full(q.shape[:3] + (v.shape[3],), np.nan)
+    pos = pos_offset + np.arange(L)
+    if pairs is None:
+        pairs = [(b, h) for b in range(B) for h in range(H)]
+    rr = np.arange(L) if rows is None else np.asarray(rows)
+    for b, h in pairs:
+        qf = features(q[b, :, h], _gamma_h(gamma_q, h), pos, eps_norm, rope_base)
+        kf = features(k[b, :, h], _gamma_h(gamma_k, h), pos, eps_norm, rope_base)
+        out[b, rr, h] = rla2_bidir_doc(qf, kf, v[b, :, h], eps_den, rows=rr)
+    return out
+
+
+def rla2_bidir_varlen(q, k, v, cu_seqlens, gamma_q, gamma_k, eps_norm=1e-6, rope_base=1e4,
+                      eps_den=1e-4, docs=None, heads=None, rows_per_doc=None):
+    """Packed varlen bidirectional RLA-2: q, k, v [T, H, d]; document n spans tokens
+    cu_seqlens[n] .. cu_seqlens[n+1]-1, sees only itself and starts at RoPE position 0
+    (the document boundary of 08-rapt-algorithm.md §2.2 and §4.1). Returns out [T, H, d].
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    T, H, d = q.shape
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    out = np.full(q.shape[:2] + (v.shape[2],), np.nan)
+    docs = range(len(cu) - 1) if docs is None else docs
+    heads = range(H) if heads is None else heads
+    for n in docs:
+        a, b = int(cu[n]), int(cu[n + 1])
+        if b == a:
+            continue
+        pos = np.arange(b - a)
+        rr = np.arange(b - a) if rows_per_doc is None else np.asarray(rows_per_doc[n])
+        for h in heads:
+            qf = features(q[a:b, h], _gamma_h(gamma_q, h), pos, eps_norm, rope_base)
+            kf = features(k[a:b, h], _gamma_h(gamma_k, h), pos, eps_norm, rope_base)
+            out[a + rr, h] = rla2_bidir_doc(qf, kf, v[a:b, h], eps_den, rows=rr)
+    return out
+
+
 def rla_l2(q, k, v, eps=1e-6, pairs=None, rows=None):
     """Original RLA, non-causal, L2 denominator (08-rapt-algorithm.md §2.1):
 

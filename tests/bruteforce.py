@@ -71,3 +71,20 @@ def l2_head(qf, kf, v, eps):
                 num[j] += s * float(v[i][j])
         out.append([num[j] / (math.sqrt(ss) + eps) for j in range(dv)])
     return out
+
+
+def bidir_head(qf, kf, v, eps_den):
+    """Every query sees every token of the sequence (non-causal Sum denominator)."""
+    n = len(qf)
+    dv = len(v[0]) if n else 0
+    out = []
+    for t in range(n):
+        num = [0.0] * dv
+        den = 0.0
+        for tau in range(n):
+            s = dot(qf[t], kf[tau])
+            for j in range(dv):
+                num[j] += s * float(v[tau][j])
+            den += s
+        out.append([num[j] / (den + eps_den) for j in range(dv)])
+    return out

@@ -12,6 +12,7 @@ _orig_rope = R.rope_adjacent
 _orig_rmsnorm = R.rmsnorm
 _orig_causal = R.rla2_causal_doc
 _orig_features = R.features
+_orig_bidir = R.rla2_bidir_doc
 
 
 def rope_wrong_sign(x, positions, base):
@@ -66,6 +67,23 @@ def causal_transposed_state(qf, kf, v, eps_den=1e-4, S0=None, z0=None, rows=None
     return _orig_causal(qf, kf, v, eps_den, None if S0 is None else np.asarray(S0).T, z0, rows)
 
 
+def bidir_causal_mask(qf, kf, v, eps_den=1e-4, rows=None):
+    # the non-causal form with the causal mask left in
+    return _orig_causal(qf, kf, v, eps_den, rows=rows)[0]
+
+
+def bidir_no_eps(qf, kf, v, eps_den=1e-4, rows=None):
+    return _orig_bidir(qf, kf, v, 0.0, rows)
+
+
+def bidir_l2_den(qf, kf, v, eps_den=1e-4, rows=None):
+    # the original RLA's L2 denominator in place of the Sum denominator
+    qf, kf, v = (np.asarray(a, np.float64) for a in (qf, kf, v))
+    s = qf @ kf.T
+    out = (s @ v) / (np.sqrt((s * s).sum(1)) + eps_den)[:, None]
+    return out if rows is None else out[np.asarray(rows)]
+
+
 def features_no_relu(x, gamma, positions, eps_norm, rope_base):
     return R.rope_adjacent(R.rmsnorm(x, gamma, eps_norm), positions, rope_base)
 
@@ -79,6 +97,9 @@ MUTANTS = {
     "causal_no_eps": ("rla2_causal_doc", causal_no_eps),
     "causal_transposed_state": ("rla2_causal_doc", causal_transposed_state),
     "features_no_relu": ("features", features_no_relu),
+    "bidir_causal_mask": ("rla2_bidir_doc", bidir_causal_mask),
+    "bidir_no_eps": ("rla2_bidir_doc", bidir_no_eps),
+    "bidir_l2_den": ("rla2_bidir_doc", bidir_l2_den),
 }
 
 
@@ -92,6 +113,9 @@ def _pins():
         P.test_rope_properties,
         P.test_rmsnorm_properties,
         P.test_decode_equals_prefill,
+        lambda: P.test_bidir_matches_bruteforce(5, 8, 2),
+        P.test_bidir_key_order_invariance,
+        P.test_bidir_constant_v_closed_form,
     ]
 
 

@@ -355,3 +355,76 @@ def test_tiny_fp32_golden_regression():
                                w.eps_den)
     ref = np.loadtxt(os.path.join(GOLDEN, "tiny_fp32_out.txt")).reshape(out.shape)
     np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- bidirectional (non-causal)
+
+
+@pytest.mark.parametrize("L,d,H", [(1, 2, 1), (5, 8, 2), (16, 8, 2), (16, 16, 1)])
+def test_bidir_matches_bruteforce(L, d, H):
+    """Non-causal RLA-2 (08-rapt-algorithm.md §4.1 causal=false, §3 Sum denominator) vs a
+    pure-Python brute force in which every query sees every token."""
+    B = 2
+    q, k, v = (_rand(s, (B, L, H, d)) for s in (41, 42, 43))
+    gq = syn.rng(44).uniform(0.8, 1.2, (H, d))
+    gk = syn.rng(45).uniform(0.8, 1.2, (H, d))
+    off = 3
+    out = O.rla2_bidir(q, k, v, gq, gk, 1e-6, 1e4, 1e-4, pos_offset=off)
+    for b in range(B):
+        for h in range(H):
+            qf = [BF.feature_row(q[b, t, h], gq[h], off + t, 1e-6, 1e4) for t in range(L)]
+            kf = [BF.feature_row(k[b, t, h], gk[h], off + t, 1e-6, 1e4) for t in range(L)]
+            ref = BF.bidir_head(qf, kf, v[b, :, h], 1e-4)
+            np.testing.assert_allclose(out[b, :, h], np.array(ref), rtol=1e-10, atol=1e-12)
+
+
+def test_bidir_last_row_is_causal_last_row():
+    """The inclusive causal prefix of the last token covers the whole sequence (§4.1 "i <= t"),
+    so the two modes agree exactly there and nowhere is the bidirectional row a causal one."""
+    B, L, H, d = 2, 40, 2, 16
+    q, k, v = (_rand(s, (B, L, H, d)) for s in (51, 52, 53))
+    g = np.ones(d)
+    bi = O.rla2_bidir(q, k, v, g, g)
+    ca, _, _ = O.rla2_prefill(q, k, v, g, g)
+    np.testing.assert_allclose(bi[:, -1], ca[:, -1], rtol=1e-12, atol=1e-14)
+    assert np.abs(bi[:, 0] - ca[:, 0]).max() > 1e-3  # the first query sees the future
+
+
+def test_bidir_key_order_invariance():
+    """Sums over the whole set: reordering the (k', v) rows together changes nothing; reordering
+    the queries reorders the output rows."""
+    n, d = 33, 16
+    qf = np.abs(_rand(61, (n, d)))
+    kf = np.abs(_rand(62, (n, d)))
+    v = _rand(63, (n, d))
+    ref = O.rla2_bidir_doc(qf, kf, v)
+    perm = syn.rng(64).permutation(n)
+    np.testing.assert_allclose(O.rla2_bidir_doc(qf, kf[perm], v[perm]), ref, rtol=1e-12)
+    np.testing.assert_allclose(O.rla2_bidir_doc(qf[perm], kf, v), ref[perm], rtol=1e-12)
+
+
+def test_bidir_constant_v_closed_form():
+    """v == 1: out = sum(s) / (sum(s) + eps), in [0, 1), equal across the row."""
+    n, d = 20, 8
+    qf = np.abs(_rand(71, (n, d)))
+    kf = np.abs(_rand(72, (n, d)))
+    out = O.rla2_bidir_doc(qf, kf, np.ones((n, 4)))
+    ssum = (qf @ kf.T).sum(axis=1)
+    np.testing.assert_allclose(out[:, 0], ssum / (ssum + 1e-4), rtol=1e-13)
+    assert np.all(out >= 0) and np.all(out < 1) and np.all(out == out[:, :1])
+
+
+def test_bidir_varlen_matches_dense_docs():
+    """Packed documents see only themselves and restart RoPE at 0 (§2.2, §4.1)."""
+    lens = [4, 0, 9, 1]
+    cu = syn.cu_seqlens_from_lengths(lens)
+    T, H, d = int(cu[-1]), 2, 8
+    q, k, v = (_rand(s, (T, H, d)) for s in (81, 82, 83))
+    g = syn.rng(84).uniform(0.8, 1.2, (H, d))
+    out = O.rla2_bidir_varlen(q, k, v, cu, g, g)
+    for n in range(len(lens)):
+        a, b = cu[n], cu[n + 1]
+        if b == a:
+            continue
+        ref = O.rla2_bidir(q[None, a:b], k[None, a:b], v[None, a:b], g, g)[0]
+        np.testing.assert_allclose(out[a:b], ref, rtol=1e-13)
