@@ -149,6 +149,38 @@ rapt_status rapt_varlen_fwd(const void* q, const void* k, const void* v, rapt_dt
                             rapt_stream_t stream);
 
 /*
+ * Bidirectional (non-causal) RLA-2 (08-rapt-algorithm.md §4.1: in its causal=false mode the prefix
+ * scan sums over the whole set; §4.2: the layer's bidirectional branch; formula and eps of §3).
+ * Features as in the causal form; for each (document, head), S = sum_tau k'_tau v_tau^T and
+ * z = sum_tau k'_tau over the WHOLE document, and out_t = q'_t S / (q'_t . z + eps_den).
+ *   Dense:  q, k, v, out [B, L, H, d]; one document per batch row; token t at RoPE position
+ *           pos_offset + t.
+ *   Varlen: q, k, v, out [T, H, d]; cu_seqlens and max_seqlen as for rapt_varlen_fwd; RoPE
+ *           positions restart at 0 in every document, and a document sees only its own tokens.
+ *   dev_status  nullable DEVICE uint32, as for rapt_prefill_fwd / rapt_varlen_fwd.
+ *   workspace   at least the matching *_workspace_size() bytes, 16-byte aligned (fp32 state of
+ *               every block of the documents, then the reduced state of every document).
+ * There is no carried-in or final state: the state is the document's own.
+ * Requirements as for the causal entry points. bf16 with d = 64 or 128 runs on the tensor cores
+ * (bf16 GEMM operands, fp32 accumulation, fp32 denominator); fp32, and bf16 with d = 16 or 32,
+ * run on CUDA cores in fp32 and need no workspace.
+ */
+size_t rapt_bidir_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype);
+rapt_status rapt_bidir_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
+                           int32_t B, int32_t L, int32_t H, int32_t d,
+                           const float* gamma_q, const float* gamma_k, rapt_params params,
+                           int32_t pos_offset, void* out, uint32_t* dev_status,
+                           void* workspace, size_t workspace_bytes, rapt_stream_t stream);
+size_t rapt_bidir_varlen_workspace_size(int32_t T, int32_t N, int32_t H, int32_t d,
+                                        int32_t max_seqlen, rapt_dtype dtype);
+rapt_status rapt_bidir_varlen_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
+                                  int32_t T, int32_t H, int32_t d, const int32_t* cu_seqlens,
+                                  int32_t N, int32_t max_seqlen, const float* gamma_q,
+                                  const float* gamma_k, rapt_params params, void* out,
+                                  uint32_t* dev_status, void* workspace, size_t workspace_bytes,
+                                  rapt_stream_t stream);
+
+/*
  * One decode step for N sequences (08-rapt-algorithm.md §4.2 forward_step): features of the new
  * token at positions[n]; S += k' v^T and z += k' IN PLACE; out = q' S / (q' . z + eps_den)
  * with the updated state (the new token sees itself, like the inclusive prefill).

@@ -141,6 +141,66 @@ def rapt_varlen_fwd(q, k, v, cu_seqlens, gamma_q, gamma_k, *, max_seqlen, eps_no
     return out, S_final, z_final
 
 
+def rapt_bidir_fwd(q, k, v, gamma_q, gamma_k, *, eps_norm=1e-6, rope_base=1e4, eps_den=1e-4,
+                   pos_offset=0, out=None, dev_status=None, workspace=None, stream=None):
+    """Dense bidirectional (non-causal) RLA-2; q, k, v [B, L, H, d] (fp32 or bf16). Returns out."""
+    _need(q.dim() == 4, "q must be [B, L, H, d]")
+    B, L, H, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _cuda_contig(name, t, q.dtype, q.shape)
+    _need(q.dtype in _DT, "dtype must be float32 or bfloat16")
+    stride = _gammas(gamma_q, gamma_k, H, d)
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, q.dtype, q.shape)
+    if dev_status is not None:
+        _cuda_contig("dev_status", dev_status, torch.int32)
+    lib = _lib.load()
+    need = lib.rapt_bidir_workspace_size(B, L, H, d, _DT[q.dtype])
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.rapt_bidir_fwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], B, L, H, d,
+                            _ptr(gamma_q), _ptr(gamma_k),
+                            make_params(eps_norm, rope_base, eps_den, stride), int(pos_offset),
+                            _ptr(out), _ptr(dev_status), _ptr(workspace), ws_bytes, _stream(stream))
+    _lib.check("rapt_bidir_fwd", st)
+    return out
+
+
+def rapt_bidir_varlen_fwd(q, k, v, cu_seqlens, gamma_q, gamma_k, *, max_seqlen, eps_norm=1e-6,
+                          rope_base=1e4, eps_den=1e-4, out=None, dev_status=None, workspace=None,
+                          stream=None):
+    """Packed varlen bidirectional RLA-2; q, k, v [T, H, d]; cu_seqlens int32 [N + 1] on the
+    device. Returns out."""
+    _need(q.dim() == 3, "q must be [T, H, d]")
+    T, H, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _cuda_contig(name, t, q.dtype, q.shape)
+    _need(q.dtype in _DT, "dtype must be float32 or bfloat16")
+    _cuda_contig("cu_seqlens", cu_seqlens, torch.int32)
+    _need(cu_seqlens.dim() == 1 and cu_seqlens.numel() >= 2, "cu_seqlens must be [N + 1]")
+    N = cu_seqlens.numel() - 1
+    stride = _gammas(gamma_q, gamma_k, H, d)
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, q.dtype, q.shape)
+    if dev_status is not None:
+        _cuda_contig("dev_status", dev_status, torch.int32)
+    lib = _lib.load()
+    need = lib.rapt_bidir_varlen_workspace_size(T, N, H, d, int(max_seqlen), _DT[q.dtype])
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.rapt_bidir_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], T, H, d,
+                                   _ptr(cu_seqlens), N, int(max_seqlen), _ptr(gamma_q),
+                                   _ptr(gamma_k), make_params(eps_norm, rope_base, eps_den, stride),
+                                   _ptr(out), _ptr(dev_status), _ptr(workspace), ws_bytes,
+                                   _stream(stream))
+    _lib.check("rapt_bidir_varlen_fwd", st)
+    return out
+
+
 def rapt_decode_step(q, k, v, positions, gamma_q, gamma_k, S, z, *, eps_norm=1e-6, rope_base=1e4,
                      eps_den=1e-4, out=None, stream=None):
     """One decode step; q, k, v [N, H, d]; positions int32 [N]; S [N, H, d, d] and z [N, H, d]

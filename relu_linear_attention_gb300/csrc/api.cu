@@ -81,7 +81,7 @@ const char* rapt_status_string(rapt_status s) {
   }
 }
 
-int32_t rapt_abi_version(void) { return 10000; }
+int32_t rapt_abi_version(void) { return 10100; }
 
 uint64_t rapt_launch_counter(void) { return rapt::launch_count(); }
 
@@ -178,6 +178,91 @@ rapt_status rapt_varlen_fwd(const void* q, const void* k, const void* v, rapt_dt
   if (rapt::tc_supported(to_dt(dtype), d))
     return from_cuda(rapt::launch_prefill_tc(d, a, rapt::tc_plan(N, H, max_seqlen, T, d),
                                              static_cast<float*>(workspace), s));
+  return from_cuda(rapt::launch_prefill_simt(to_dt(dtype), d, a, s));
+}
+
+size_t rapt_bidir_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype) {
+  if (!known_dtype(dtype) || !supported_d(d) || B < 1 || H < 1 || L < 0) return 0;
+  if (!rapt::tc_supported(to_dt(dtype), d) || L == 0) return 0;  // nothing runs for L = 0
+  return rapt::bidir_plan(B, H, L, d).ws_bytes;
+}
+
+rapt_status rapt_bidir_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
+                           int32_t B, int32_t L, int32_t H, int32_t d,
+                           const float* gamma_q, const float* gamma_k, rapt_params params,
+                           int32_t pos_offset, void* out, uint32_t* dev_status,
+                           void* workspace, size_t workspace_bytes, rapt_stream_t stream) {
+  if (!known_dtype(dtype) || !supported_d(d)) return RAPT_ERR_UNSUPPORTED;
+  if (B < 1 || H < 1 || L < 0 || pos_offset < 0) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(B) * L * H * d)) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(pos_offset) + L)) return RAPT_ERR_INVALID_ARG;
+  if (L > 0 && (q == nullptr || k == nullptr || v == nullptr || out == nullptr))
+    return RAPT_ERR_INVALID_ARG;
+  if (!opt_aligned16(q) || !opt_aligned16(k) || !opt_aligned16(v) || !opt_aligned16(out))
+    return RAPT_ERR_INVALID_ARG;
+  if (out != nullptr && (out == q || out == k || out == v)) return RAPT_ERR_INVALID_ARG;
+  if (dev_status != nullptr && !aligned4(dev_status)) return RAPT_ERR_INVALID_ARG;
+  rapt_status st = check_features(gamma_q, gamma_k, params, d);
+  if (st != RAPT_OK) return st;
+  const size_t need = rapt_bidir_workspace_size(B, L, H, d, dtype);
+  if (workspace_bytes < need || (need > 0 && (workspace == nullptr || !aligned16(workspace))))
+    return RAPT_ERR_WORKSPACE;
+  if (L == 0) return RAPT_OK;
+
+  rapt::PrefillArgs a{};
+  a.q = q; a.k = k; a.v = v; a.out = out;
+  a.gamma_q = gamma_q; a.gamma_k = gamma_k;
+  a.cu_seqlens = nullptr; a.dev_status = dev_status;
+  a.n_docs = B; a.doc_len = L; a.total_rows = B * L; a.max_seqlen = L;
+  a.H = H; a.pos_offset = pos_offset; a.eps_den = params.eps_den; a.bidir = 1;
+  a.fa = make_features(params, d);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (rapt::tc_supported(to_dt(dtype), d))
+    return from_cuda(rapt::launch_bidir_tc(d, a, rapt::bidir_plan(B, H, L, d), workspace, s));
+  return from_cuda(rapt::launch_prefill_simt(to_dt(dtype), d, a, s));
+}
+
+size_t rapt_bidir_varlen_workspace_size(int32_t T, int32_t N, int32_t H, int32_t d,
+                                        int32_t max_seqlen, rapt_dtype dtype) {
+  if (!known_dtype(dtype) || !supported_d(d) || N < 1 || H < 1 || max_seqlen < 0 || T < 0) return 0;
+  if (!rapt::tc_supported(to_dt(dtype), d) || T == 0) return 0;  // nothing runs for T = 0
+  return rapt::bidir_plan(N, H, max_seqlen, d).ws_bytes;
+}
+
+rapt_status rapt_bidir_varlen_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
+                                  int32_t T, int32_t H, int32_t d, const int32_t* cu_seqlens,
+                                  int32_t N, int32_t max_seqlen, const float* gamma_q,
+                                  const float* gamma_k, rapt_params params, void* out,
+                                  uint32_t* dev_status, void* workspace, size_t workspace_bytes,
+                                  rapt_stream_t stream) {
+  if (!known_dtype(dtype) || !supported_d(d)) return RAPT_ERR_UNSUPPORTED;
+  if (T < 0 || N < 1 || H < 1 || max_seqlen < 0) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(T) * H * d)) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(N) * H * 4)) return RAPT_ERR_INVALID_ARG;
+  if (cu_seqlens == nullptr || !aligned4(cu_seqlens)) return RAPT_ERR_INVALID_ARG;
+  if (dev_status != nullptr && !aligned4(dev_status)) return RAPT_ERR_INVALID_ARG;
+  if (T > 0 && (q == nullptr || k == nullptr || v == nullptr || out == nullptr))
+    return RAPT_ERR_INVALID_ARG;
+  if (!opt_aligned16(q) || !opt_aligned16(k) || !opt_aligned16(v) || !opt_aligned16(out))
+    return RAPT_ERR_INVALID_ARG;
+  if (out != nullptr && (out == q || out == k || out == v)) return RAPT_ERR_INVALID_ARG;
+  rapt_status st = check_features(gamma_q, gamma_k, params, d);
+  if (st != RAPT_OK) return st;
+  const size_t need = rapt_bidir_varlen_workspace_size(T, N, H, d, max_seqlen, dtype);
+  if (workspace_bytes < need || (need > 0 && (workspace == nullptr || !aligned16(workspace))))
+    return RAPT_ERR_WORKSPACE;
+  if (T == 0) return RAPT_OK;
+
+  rapt::PrefillArgs a{};
+  a.q = q; a.k = k; a.v = v; a.out = out;
+  a.gamma_q = gamma_q; a.gamma_k = gamma_k;
+  a.cu_seqlens = cu_seqlens; a.dev_status = dev_status;
+  a.n_docs = N; a.doc_len = 0; a.total_rows = T; a.max_seqlen = max_seqlen;
+  a.H = H; a.pos_offset = 0; a.eps_den = params.eps_den; a.bidir = 1;
+  a.fa = make_features(params, d);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (rapt::tc_supported(to_dt(dtype), d))
+    return from_cuda(rapt::launch_bidir_tc(d, a, rapt::bidir_plan(N, H, max_seqlen, d), workspace, s));
   return from_cuda(rapt::launch_prefill_simt(to_dt(dtype), d, a, s));
 }
 

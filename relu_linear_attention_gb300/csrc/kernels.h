@@ -40,6 +40,7 @@ struct PrefillArgs {
   int H;
   int pos_offset;  // dense only (0 for varlen)
   float eps_den;
+  int bidir;       // 0: causal; 1: bidirectional (every token sees its whole document; no S0 / z0)
   FeatureArgs fa;
 };
 
@@ -59,6 +60,37 @@ bool tc_supported(DType dt, int d);
 TcPlan tc_plan(int n_docs, int H, int max_seqlen, long total_tokens, int d);
 cudaError_t launch_prefill_tc(int d, const PrefillArgs& a, const TcPlan& plan, float* ws,
                               cudaStream_t stream);
+
+// Arguments of the tensor-core state and prefill kernels.
+struct TcArgs {
+  PrefillArgs p;
+  float* ws;        // increment records [n_docs][H][nblk_max] (K'^T V, then sum k'; D * (D + 1) floats)
+  int seg_len;      // tokens per segment (multiple of blk_len)
+  int nseg_max;     // segments per document slot in the grid of the prefill kernel
+  int blk_len;      // tokens per increment block (multiple of 128)
+  int blk_per_seg;  // seg_len / blk_len
+  int nblk_max;     // increment blocks per document slot
+  int whole_doc;    // 0: the blocks before each document's last segment, all full;
+                    // 1: every block of the document, the last one possibly ragged
+};
+// The state increments of TcArgs' blocks (one launch; later launches may depend on it
+// programmatically: it triggers its dependents at its start).
+cudaError_t launch_state_tc(int d, const TcArgs& ta, cudaStream_t stream);
+
+// Bidirectional (non-causal) RLA-2 over a set of documents on the tensor cores (bf16, d in
+// {64, 128}): out_t = q'_t S_doc / (q'_t . z_doc + eps) with S_doc, z_doc over the whole document.
+// Three launches; ws_bytes of workspace.
+struct BidirPlan {
+  int blk_len;   // tokens per state block
+  int nblk_max;  // state blocks per document slot
+  int nsplit;    // readout CTAs per (document, head)
+  int split_chunks;  // 128-token tiles per readout CTA
+  size_t img_offset;  // byte offset of the reduced operands in ws
+  size_t ws_bytes;
+};
+BidirPlan bidir_plan(int n_docs, int H, int max_seqlen, int d);
+cudaError_t launch_bidir_tc(int d, const PrefillArgs& a, const BidirPlan& plan, void* ws,
+                            cudaStream_t stream);
 
 struct DecodeArgs {
   const void* q;

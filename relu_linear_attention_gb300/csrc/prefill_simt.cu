@@ -10,7 +10,10 @@
 // which equals the per-token recurrence S_t = S_{t-1} + k'_t v_t^T, out_t = q'_t S_t / (q'_t z_t
 // + eps) exactly up to summation order. One CTA owns one (document, head, block of DVB value
 // columns) and walks the document's chunks in order with S (d x DVB) and z resident in shared
-// memory. Dense prefill is the same kernel with B documents of L tokens.
+// memory. Dense prefill is the same kernel with B documents of L tokens. The bidirectional form
+// (08-rapt-algorithm.md §4.1, causal=false: every token sees its whole document) walks the chunks
+// twice: first only the state update over the whole document, then num = Q'_c S, den = Q'_c z +
+// eps for every chunk.
 #include "kernels.h"
 
 namespace rapt {
@@ -110,6 +113,13 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
   constexpr int kRowsPerPass = (kThreads / 32) * FL::ROWS_PER_WARP;
   static_assert(kC % kRowsPerPass == 0, "every lane must run the same number of feature rows");
 
+  // Causal: one pass reads every chunk out and then adds it to the state. Bidirectional
+  // (08-rapt-algorithm.md §4.1, causal=false): a first pass sums the whole document's state, a
+  // second reads every chunk out against it (no intra-chunk scores). All flags are CTA-uniform.
+  const bool causal = !a.bidir;
+  for (int pass = 0; pass < (causal ? 1 : 2); ++pass) {
+  const bool upd = causal || pass == 0;  // this pass adds the chunks to the state
+  const bool rd = causal || pass == 1;   // this pass writes the output
   for (int t0 = 0; t0 < n; t0 += kC) {
     // ---- features of the chunk (tail rows become zeros: they add nothing anywhere)
     for (int rr = warp * FL::ROWS_PER_WARP + grp; rr < kC; rr += kRowsPerPass) {
@@ -117,17 +127,21 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
       const bool valid = t < n;
       const long off = ((row0 + (valid ? t : 0)) * a.H + h) * D;
       float f[EPT];
-      feature_row<D, T>(q + off, valid, gq, a.pos_offset + t, a.fa, r, f);
+      if (rd) {
+        feature_row<D, T>(q + off, valid, gq, a.pos_offset + t, a.fa, r, f);
 #pragma unroll
-      for (int e = 0; e < EPT; ++e) QsT[(r * EPT + e) * kC + rr] = f[e];
-      feature_row<D, T>(k + off, valid, gk, a.pos_offset + t, a.fa, r, f);
+        for (int e = 0; e < EPT; ++e) QsT[(r * EPT + e) * kC + rr] = f[e];
+      }
+      if (upd) {
+        feature_row<D, T>(k + off, valid, gk, a.pos_offset + t, a.fa, r, f);
 #pragma unroll
-      for (int e = 0; e < EPT; ++e) {
-        KsT[(r * EPT + e) * kC + rr] = f[e];
-        Ks[rr * D + r * EPT + e] = f[e];
+        for (int e = 0; e < EPT; ++e) {
+          KsT[(r * EPT + e) * kC + rr] = f[e];
+          Ks[rr * D + r * EPT + e] = f[e];
+        }
       }
     }
-    for (int idx = tid; idx < kC * CG; idx += kThreads) {
+    for (int idx = upd ? tid : kC * CG; idx < kC * CG; idx += kThreads) {
       const int rr = idx / CG, j4 = (idx % CG) * 4;
       const int t = t0 + rr;
       float f4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -137,7 +151,7 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
     __syncthreads();
 
     // ---- masked scores P[t][tau] = q'_t . k'_tau for tau <= t (stored transposed)
-    {
+    if (causal) {
       const int ty = tid / 16, tx = tid % 16;
       float acc[4][4] = {};
       for (int i = 0; i < D; ++i) {
@@ -161,17 +175,18 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
     __syncthreads();
 
     // ---- denominators and numerators (intra-chunk part + carried state)
-    if (tid < kC) {
+    if (rd && tid < kC) {
       float s = 0.f;
-      for (int tau = 0; tau < kC; ++tau) s += PsT[tau * kC + tid];
+      if (causal)
+        for (int tau = 0; tau < kC; ++tau) s += PsT[tau * kC + tid];
       for (int i = 0; i < D; ++i) s = fmaf(QsT[i * kC + tid], Zs[i], s);
       Dens[tid] = s + a.eps_den;
     }
-    const bool has_num = tid < 16 * CG;
+    const bool has_num = rd && tid < 16 * CG;
     const int ny = tid / CG, nx = tid % CG;
     float acc[4][4] = {};
     if (has_num) {
-      for (int tau = 0; tau < kC; ++tau) {
+      for (int tau = 0; tau < (causal ? kC : 0); ++tau) {
         const float4 p = ld4(PsT + tau * kC + 4 * ny);
         const float4 w = ld4(Vs + tau * DVB + 4 * nx);
         const float pv[4] = {p.x, p.y, p.z, p.w};
@@ -206,7 +221,7 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
     }
 
     // ---- state update S += K'^T V, z += colsum K'
-    for (int blk = tid; blk < (D / 4) * CG; blk += kThreads) {
+    for (int blk = upd ? tid : (D / 4) * CG; blk < (D / 4) * CG; blk += kThreads) {
       const int bi = blk / CG, bj = blk % CG;
       float u[4][4] = {};
       for (int tau = 0; tau < kC; ++tau) {
@@ -224,21 +239,22 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(const PrefillArg
 #pragma unroll
         for (int x = 0; x < 4; ++x) Ss[(4 * bi + y) * DVB + 4 * bj + x] += u[y][x];
     }
-    if (tid < D) {
+    if (upd && tid < D) {
       float s = 0.f;
       for (int tau = 0; tau < kC; ++tau) s += Ks[tau * D + tid];
       Zs[tid] += s;
     }
     __syncthreads();
   }
+  }
 
-  if (a.S_final != nullptr) {
+  if (a.S_final != nullptr && causal) {
     for (int idx = tid; idx < D * DVB; idx += kThreads) {
       const int i = idx / DVB, j = idx % DVB;
       a.S_final[(bh * D + i) * D + cb * DVB + j] = Ss[idx];
     }
   }
-  if (a.z_final != nullptr && cb == 0) {
+  if (a.z_final != nullptr && causal && cb == 0) {
     for (int i = tid; i < D; i += kThreads) a.z_final[bh * D + i] = Zs[i];
   }
 }

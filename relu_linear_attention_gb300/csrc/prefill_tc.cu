@@ -57,10 +57,13 @@
 
 #include "kernels.h"
 #include "tc_utils.cuh"
+#include "tc_features.cuh"
 #include "tensor_map.h"
 
 namespace rapt {
 namespace {
+
+using namespace feat;
 
 constexpr int kC = 128;          // chunk length = MMA M
 constexpr int kProd = 512;       // producer threads (16 warps)
@@ -73,15 +76,6 @@ constexpr uint32_t kBarProd = 1, kBarCons = 2;   // named barriers of the produc
 constexpr uint32_t kBarInit = 3;                 // consumer + issuer warpgroups after the state set-up
 constexpr uint32_t kBarHelp = 4;                 // the two z helper warps of the issuer warpgroup
 constexpr int kHelp = 64;                        // z helper threads
-
-// One increment record: K'^T V of a block as D/4 column groups of [D rows][4 columns] (the float4
-// of row r and columns 4j..4j+3 at float4 index j * D + r, so that 32 threads reading their rows'
-// same 4 columns read 512 contiguous bytes), then the block's column sums of k' (D floats).
-template <int D>
-struct Rec {
-  static constexpr long FLOATS = static_cast<long>(D) * (D + 1);
-  static constexpr long Z = static_cast<long>(D) * D;
-};
 
 // Register splits (setmaxnreg draws on the launch allocation: threads x launch registers).
 constexpr int kLaunchRegsB = 80, kRegsProdB = 88, kRegsConsB = 64, kRegsIssueB = 64;
@@ -139,234 +133,6 @@ struct LayA {
   static constexpr uint32_t MISC = BAR + 6 * 8;
   static constexpr uint32_t BYTES = MISC + 16;
 };
-
-struct TcArgs {
-  PrefillArgs p;
-  float* ws;        // increment records [n_docs][H][nblk_max] (Rec layout)
-  int seg_len;      // tokens per segment (multiple of blk_len)
-  int nseg_max;     // segments per document slot in the grid of kernel B
-  int blk_len;      // tokens per increment block (multiple of kC)
-  int blk_per_seg;  // seg_len / blk_len
-  int nblk_max;     // increment blocks per document slot: (nseg_max - 1) * blk_per_seg
-};
-
-__device__ __forceinline__ uint4 ldg16(const void* p) {
-  return __ldg(reinterpret_cast<const uint4*>(p));
-}
-__device__ __forceinline__ void sts16(uint32_t addr, const uint4& v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
-__device__ __forceinline__ uint4 pack8(const float* f) {
-  return make_uint4(tc::pack_bf16x2(f[0], f[1]), tc::pack_bf16x2(f[2], f[3]),
-                    tc::pack_bf16x2(f[4], f[5]), tc::pack_bf16x2(f[6], f[7]));
-}
-// bar.sync over a group, returning the OR of every member's flag (so all members agree).
-__device__ __forceinline__ int group_sync_or(uint32_t id, uint32_t n, int flag) {
-  int r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.s32 p, %3, 0;\n bar.red.or.pred q, %1, %2, p;\n"
-      " selp.s32 %0, 1, 0, q;\n}\n"
-      : "=r"(r)
-      : "r"(id), "r"(n), "r"(flag)
-      : "memory");
-  return r;
-}
-
-// Document bounds; false if the document is malformed (then treated as empty).
-__device__ __forceinline__ bool doc_bounds(const PrefillArgs& a, int doc, long& row0, int& n) {
-  if (a.cu_seqlens != nullptr) {
-    const int s = a.cu_seqlens[doc];
-    const int e = a.cu_seqlens[doc + 1];
-    const int prev = doc > 0 ? a.cu_seqlens[doc - 1] : 0;
-    const bool bad = s < 0 || e < s || prev > s || e > a.total_rows || (doc == 0 && s != 0) ||
-                     (doc == a.n_docs - 1 && e != a.total_rows) || (e - s) > a.max_seqlen;
-    if (bad) {
-      row0 = 0;
-      n = 0;
-      return false;
-    }
-    row0 = s;
-    n = e - s;
-  } else {
-    row0 = static_cast<long>(doc) * a.doc_len;
-    n = a.doc_len;
-  }
-  return true;
-}
-
-// ---------------------------------------------------------------------------------------------
-// Feature arithmetic on packed fp32 pairs. A thread's 8 elements are four RoPE pairs m = 0..3
-// (elements 2m, 2m+1). They are held as two "structure of arrays" groups g = 0, 1 covering pairs
-// 2g and 2g+1: x0[g] = (first element of pair 2g, first of pair 2g+1), x1[g] = the second
-// elements, so every rotation step is one packed operation over two pairs.
-struct Pairs {
-  float2 x0[2], x1[2];
-};
-
-__device__ __forceinline__ Pairs unpack_pairs(const uint4& u) {
-  // 32-bit word m of the 16 bytes holds pair m: element 2m in the low half, 2m+1 in the high half
-  Pairs p;
-  p.x0[0] = make_float2(__uint_as_float(u.x << 16), __uint_as_float(u.y << 16));
-  p.x1[0] = make_float2(__uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y & 0xffff0000u));
-  p.x0[1] = make_float2(__uint_as_float(u.z << 16), __uint_as_float(u.w << 16));
-  p.x1[1] = make_float2(__uint_as_float(u.z & 0xffff0000u), __uint_as_float(u.w & 0xffff0000u));
-  return p;
-}
-
-__device__ __forceinline__ float sumsq(const Pairs& p) {
-  float2 acc = __fmul2_rn(p.x0[0], p.x0[0]);
-  acc = __ffma2_rn(p.x1[0], p.x1[0], acc);
-  acc = __ffma2_rn(p.x0[1], p.x0[1], acc);
-  acc = __ffma2_rn(p.x1[1], p.x1[1], acc);
-  return acc.x + acc.y;
-}
-
-template <int TPR>
-__device__ __forceinline__ float row_sum(float x) {
-#pragma unroll
-  for (int off = TPR / 2; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-  return x;
-}
-
-// Per-thread RoPE constants: gains and the sin/cos of the current row's angles, in pair groups.
-struct Rot {
-  float2 c[2], s[2];  // cos / sin of pairs (2g, 2g+1)
-};
-
-// ReLU(RoPE(x * gamma * rinv)), in place (the gains come multiplied by the row's 1 / rms: RoPE is
-// linear, so that is the same as normalising first): x0 <- first elements, x1 <- second elements
-// of the rotated pairs.
-__device__ __forceinline__ void rope_relu(Pairs& p, const float2 (&g0)[2], const float2 (&g1)[2],
-                                          const Rot& r) {
-#pragma unroll
-  for (int g = 0; g < 2; ++g) {
-    const float2 y0 = __fmul2_rn(p.x0[g], g0[g]);
-    const float2 y1 = __fmul2_rn(p.x1[g], g1[g]);
-    const float2 ns = make_float2(-r.s[g].x, -r.s[g].y);
-    const float2 u = __ffma2_rn(y0, r.c[g], __fmul2_rn(y1, ns));   // y0 c - y1 s
-    const float2 v = __ffma2_rn(y0, r.s[g], __fmul2_rn(y1, r.c[g]));  // y0 s + y1 c
-    p.x0[g] = make_float2(fmaxf(u.x, 0.f), fmaxf(u.y, 0.f));
-    p.x1[g] = make_float2(fmaxf(v.x, 0.f), fmaxf(v.y, 0.f));
-  }
-}
-__device__ __forceinline__ void scale_gains(float2 (&g0)[2], float2 (&g1)[2], float s) {
-  const float2 s2 = make_float2(s, s);
-#pragma unroll
-  for (int g = 0; g < 2; ++g) {
-    g0[g] = __fmul2_rn(g0[g], s2);
-    g1[g] = __fmul2_rn(g1[g], s2);
-  }
-}
-
-__device__ __forceinline__ uint4 pack_pairs(const Pairs& p) {
-  return make_uint4(tc::pack_bf16x2(p.x0[0].x, p.x1[0].x), tc::pack_bf16x2(p.x0[0].y, p.x1[0].y),
-                    tc::pack_bf16x2(p.x0[1].x, p.x1[1].x), tc::pack_bf16x2(p.x0[1].y, p.x1[1].y));
-}
-
-// Advances the angles by a fixed step (cos / sin of the step in `st`): one exact rotation.
-__device__ __forceinline__ void rot_step(Rot& r, const Rot& st) {
-#pragma unroll
-  for (int g = 0; g < 2; ++g) {
-    const float2 ns = make_float2(-r.s[g].x, -r.s[g].y);
-    const float2 c = __ffma2_rn(r.c[g], st.c[g], __fmul2_rn(ns, st.s[g]));
-    const float2 s = __ffma2_rn(r.s[g], st.c[g], __fmul2_rn(r.c[g], st.s[g]));
-    r.c[g] = c;
-    r.s[g] = s;
-  }
-}
-
-// Column sums of the 8 per-thread values over the rows of a warp (lanes with equal lane % TPR).
-template <int TPR>
-__device__ __forceinline__ void warp_colsum(float* z) {
-#pragma unroll
-  for (int off = TPR; off < 32; off <<= 1)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) z[e] += __shfl_xor_sync(0xffffffffu, z[e], off);
-}
-__device__ __forceinline__ void pairs_to8(const Pairs& p, float* f) {
-#pragma unroll
-  for (int g = 0; g < 2; ++g) {
-    f[4 * g + 0] = p.x0[g].x;
-    f[4 * g + 1] = p.x1[g].x;
-    f[4 * g + 2] = p.x0[g].y;
-    f[4 * g + 3] = p.x1[g].y;
-  }
-}
-
-// Per-CTA feature constants in shared memory (8 * D floats), so that the producers need no
-// registers for them and no lane-divergent reads of the kernel parameters: the gains of q and k,
-// and for every RoPE pair the frequency (hi, lo turns) and the cos / sin of the rotation over
-// one producer pass (RPP positions). Gains are stored "split": the first 4 of a thread's 8
-// values for every thread part, then the last 4, so that a warp's 16-byte reads are contiguous
-// (no bank conflicts); inside each 4 the order is (pair 0 first, pair 1 first, pair 0 second,
-// pair 1 second), so that a 16-byte read lands directly on the float2 pairs the arithmetic uses.
-// split_idx maps an element index to that layout.
-struct FeatTab {
-  float* gq;   // [D]
-  float* gk;   // [D]
-  float* fhi;  // [D/2]
-  float* flo;  // [D/2]
-  float* stc;  // [D/2] cos of the per-pass rotation
-  float* sts;  // [D/2] sin
-};
-template <int D>
-__device__ __forceinline__ FeatTab feat_tab(uint8_t* p) {
-  float* f = reinterpret_cast<float*>(p);
-  return FeatTab{f, f + D, f + 2 * D, f + 2 * D + D / 2, f + 3 * D, f + 3 * D + D / 2};
-}
-template <int D>
-__device__ __forceinline__ int split_idx(int i) {
-  return (i & 4) * (D / 8) + (i >> 3) * 4 + (((i & 1) << 1) | ((i >> 1) & 1));
-}
-template <int D>
-__device__ __forceinline__ void fill_tab(const FeatTab& t, const PrefillArgs& a, int h, int rpp,
-                                         int tid, int nthreads) {
-  for (int i = tid; i < D; i += nthreads) {
-    t.gq[split_idx<D>(i)] = a.gamma_q[h * a.fa.gamma_stride + i];
-    t.gk[split_idx<D>(i)] = a.gamma_k[h * a.fa.gamma_stride + i];
-  }
-  for (int j = tid; j < D / 2; j += nthreads) {
-    t.fhi[j] = a.fa.rope_hi[j];
-    t.flo[j] = a.fa.rope_lo[j];
-    float sn, cs;
-    rope_sincos(rpp, a.fa.rope_hi[j], a.fa.rope_lo[j], sn, cs);
-    t.stc[j] = cs;
-    t.sts[j] = sn;
-  }
-}
-// Two float4 halves of a thread's 8 values in a split table, in pair groups.
-template <int D>
-__device__ __forceinline__ void split_load(const float* t, int part, float2 (&x0)[2], float2 (&x1)[2]) {
-  const float4 a = *reinterpret_cast<const float4*>(t + 4 * part);
-  const float4 b = *reinterpret_cast<const float4*>(t + D / 2 + 4 * part);
-  x0[0] = make_float2(a.x, a.y);
-  x1[0] = make_float2(a.z, a.w);
-  x0[1] = make_float2(b.x, b.y);
-  x1[1] = make_float2(b.z, b.w);
-}
-__device__ __forceinline__ void tab_step(const FeatTab& t, int j0, Rot& st) {
-  const float4 c = *reinterpret_cast<const float4*>(t.stc + j0);
-  const float4 sn = *reinterpret_cast<const float4*>(t.sts + j0);
-  st.c[0] = make_float2(c.x, c.y);
-  st.c[1] = make_float2(c.z, c.w);
-  st.s[0] = make_float2(sn.x, sn.y);
-  st.s[1] = make_float2(sn.z, sn.w);
-}
-__device__ __forceinline__ void tab_rot_at(const FeatTab& t, int pos, int j0, Rot& r) {
-  const float4 hi = *reinterpret_cast<const float4*>(t.fhi + j0);
-  const float4 lo = *reinterpret_cast<const float4*>(t.flo + j0);
-  float s0, c0, s1, c1, s2, c2, s3, c3;
-  rope_sincos(pos, hi.x, lo.x, s0, c0);
-  rope_sincos(pos, hi.y, lo.y, s1, c1);
-  rope_sincos(pos, hi.z, lo.z, s2, c2);
-  rope_sincos(pos, hi.w, lo.w, s3, c3);
-  r.c[0] = make_float2(c0, c1);
-  r.c[1] = make_float2(c2, c3);
-  r.s[0] = make_float2(s0, s1);
-  r.s[1] = make_float2(s2, s3);
-}
 
 // Initial state of a segment for columns [c0, c0 + D/2) of the calling thread's TMEM lane er:
 // S0 (if any) + the increments of the first nblk blocks, in block order, into the fp32 state in
@@ -942,7 +708,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
 // ------------------------------------------------------------------------------------------------
 // Kernel A: state increment (K'^T V and the column sums of k') of one block of blk_len tokens (every
-// block before a document's last segment). 16 producer warps fill one of two k' buffers (v arrives
+// block before a document's last segment; in whole-document mode, every block of the document, for
+// the bidirectional form). 16 producer warps fill one of two k' buffers (v arrives
 // by TMA) while the tensor core, fed by a dedicated issuer thread, accumulates the other into TMEM.
 template <int D>
 __global__ void __launch_bounds__(kThreadsA, 1)
@@ -962,10 +729,17 @@ __global__ void __launch_bounds__(kThreadsA, 1)
   long row0;
   int n;
   doc_bounds(a, doc, row0, n);  // a malformed document has n = 0 and is skipped
-  const int nseg_doc = n > 0 ? (n + ta.seg_len - 1) / ta.seg_len : 1;
-  if (blk >= (nseg_doc - 1) * ta.blk_per_seg) return;  // the last segment needs no increment
+  if (ta.whole_doc) {
+    if (static_cast<long>(blk) * ta.blk_len >= n) return;  // past the document's end
+  } else {
+    const int nseg_doc = n > 0 ? (n + ta.seg_len - 1) / ta.seg_len : 1;
+    if (blk >= (nseg_doc - 1) * ta.blk_per_seg) return;  // the last segment needs no increment
+  }
   const int seg_start = blk * ta.blk_len;
-  const int nchunks = ta.blk_len / kC;  // a block before the last segment is full
+  // a block before the last segment is full; in whole-document mode the last one may be ragged
+  // (its missing rows load as zeros, whose k' is zero: they add nothing)
+  const int blk_n = min(ta.blk_len, n - seg_start);
+  const int nchunks = (blk_n + kC - 1) / kC;
 
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t base = tc::smem_u32(smem);
@@ -1022,7 +796,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     const long rstride = static_cast<long>(a.H) * D;
     const __nv_bfloat16* krow = kg + (row0 + seg_start + prow) * rstride + static_cast<long>(h) * D + e0;
     auto load = [&](int c, int p, uint4& xk) {
-      xk = ldg16(krow + static_cast<long>(c * kC + p * RPP) * rstride);
+      if (c * kC + p * RPP + prow < blk_n) xk = ldg16(krow + static_cast<long>(c * kC + p * RPP) * rstride);
+      else xk = make_uint4(0, 0, 0, 0);
     };
     Rot rot;
     float2 zca[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -1150,11 +925,21 @@ cudaError_t set_smem(K kernel, uint32_t bytes, unsigned long long& configured) {
 }
 
 template <int D>
-cudaError_t launch_tc_d(const TcArgs& ta, cudaStream_t stream) {
-  static unsigned long long cfg_a = 0, cfg_b = 0;
-  cudaError_t e = set_smem(prefill_tc_kernel<D>, LayB<D>::BYTES, cfg_b);
+cudaError_t launch_state_d(const TcArgs& ta, const CUtensorMap& tmap_v, cudaStream_t stream) {
+  static unsigned long long cfg_a = 0;
+  cudaError_t e = set_smem(segment_state_kernel<D>, LayA<D>::BYTES, cfg_a);
   if (e != cudaSuccess) return e;
-  e = set_smem(segment_state_kernel<D>, LayA<D>::BYTES, cfg_a);
+  const long grid = static_cast<long>(ta.p.n_docs) * ta.p.H * ta.nblk_max;
+  if (grid == 0) return cudaSuccess;
+  segment_state_kernel<D><<<static_cast<unsigned>(grid), kThreadsA, LayA<D>::BYTES, stream>>>(ta, tmap_v);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_tc_d(const TcArgs& ta, cudaStream_t stream) {
+  static unsigned long long cfg_b = 0;
+  cudaError_t e = set_smem(prefill_tc_kernel<D>, LayB<D>::BYTES, cfg_b);
   if (e != cudaSuccess) return e;
   const long units = static_cast<long>(ta.p.n_docs) * ta.p.H;
   if (units == 0) return cudaSuccess;
@@ -1169,9 +954,7 @@ cudaError_t launch_tc_d(const TcArgs& ta, cudaStream_t stream) {
   }
   const bool with_a = ta.nblk_max > 0;
   if (with_a) {
-    segment_state_kernel<D><<<static_cast<unsigned>(units * ta.nblk_max), kThreadsA, LayA<D>::BYTES, stream>>>(ta, tmap_v);
-    note_launches(1);
-    e = cudaGetLastError();
+    e = launch_state_d<D>(ta, tmap_v, stream);
     if (e != cudaSuccess) return e;
   }
   // kernel B as a programmatic dependent of kernel A (only then: it must not overlap anything else)
@@ -1237,6 +1020,14 @@ TcPlan tc_plan(int n_docs, int H, int max_seqlen, long total_tokens, int d) {
                                           best.blk_per_seg * rec * sizeof(float)
                                     : 0;
   return best;
+}
+
+cudaError_t launch_state_tc(int d, const TcArgs& ta, cudaStream_t stream) {
+  if (static_cast<long>(ta.p.n_docs) * ta.p.H * ta.nblk_max == 0 || ta.p.total_rows == 0) return cudaSuccess;
+  CUtensorMap tmap_v;
+  const cudaError_t e = make_rows_map(&tmap_v, ta.p.v, ta.p.total_rows, ta.p.H, d);
+  if (e != cudaSuccess) return e;
+  return d == 128 ? launch_state_d<128>(ta, tmap_v, stream) : launch_state_d<64>(ta, tmap_v, stream);
 }
 
 cudaError_t launch_prefill_tc(int d, const PrefillArgs& a, const TcPlan& plan, float* ws,

@@ -161,3 +161,39 @@ def test_l2_rejects_bad_arguments(lib):
     assert call(ws=None) == _lib.RAPT_ERR_WORKSPACE
     assert call(wsb=16) == _lib.RAPT_ERR_WORKSPACE
     assert call(L=0) == _lib.RAPT_OK  # nothing to do, nothing launched
+
+
+def test_bidir_rejects_bad_arguments(lib):
+    out = ctypes.c_void_p(0x7F0000002000)
+
+    def dense(**kw):
+        a = dict(q=FAKE, B=1, L=8, d=16, dt=1, off=0, p=_params(), out=out, ws=None, wsb=0)
+        a.update(kw)
+        return lib.rapt_bidir_fwd(a["q"], FAKE, FAKE, a["dt"], a["B"], a["L"], 2, a["d"], FAKE, FAKE,
+                                  a["p"], a["off"], a["out"], None, a["ws"], a["wsb"], None)
+
+    assert dense(d=48) == _lib.RAPT_ERR_UNSUPPORTED
+    assert dense(dt=5) == _lib.RAPT_ERR_UNSUPPORTED
+    assert dense(q=None) == _lib.RAPT_ERR_INVALID_ARG
+    assert dense(B=0) == _lib.RAPT_ERR_INVALID_ARG
+    assert dense(off=-1) == _lib.RAPT_ERR_INVALID_ARG
+    assert dense(out=FAKE) == _lib.RAPT_ERR_INVALID_ARG  # aliases q
+    assert dense(q=FAKE_ODD) == _lib.RAPT_ERR_INVALID_ARG
+    assert dense(p=_params(eps_den=0.0)) == _lib.RAPT_ERR_INVALID_ARG
+    assert dense(d=128, L=4096) == _lib.RAPT_ERR_WORKSPACE  # the tensor-core path needs one
+    assert dense(d=128, L=0) == _lib.RAPT_OK  # nothing to do, nothing launched
+
+    def varlen(**kw):
+        a = dict(cu=FAKE, N=2, T=16, msl=16, d=64)
+        a.update(kw)
+        return lib.rapt_bidir_varlen_fwd(FAKE, FAKE, FAKE, 1, a["T"], 2, a["d"], a["cu"], a["N"],
+                                         a["msl"], FAKE, FAKE, _params(), out, None, None, 0, None)
+
+    assert varlen(cu=None) == _lib.RAPT_ERR_INVALID_ARG
+    assert varlen(N=0) == _lib.RAPT_ERR_INVALID_ARG
+    assert varlen(msl=-1) == _lib.RAPT_ERR_INVALID_ARG
+    assert varlen(d=96) == _lib.RAPT_ERR_UNSUPPORTED
+    assert varlen() == _lib.RAPT_ERR_WORKSPACE
+    assert lib.rapt_bidir_workspace_size(4, 4096, 16, 128, 1) > 0
+    assert lib.rapt_bidir_workspace_size(4, 4096, 16, 128, 0) == 0  # fp32: CUDA-core path
+    assert lib.rapt_bidir_varlen_workspace_size(65536, 17, 32, 64, 8192, 1) > 0
