@@ -267,6 +267,12 @@ def profile_case(args):
         out = torch.empty_like(q)
         msl = int(wv.lengths.max())
         call = lambda: R.rapt_varlen_fwd(q, k, v, cu, g, g, max_seqlen=msl, out=out)
+    elif args.only == "bidir":
+        w = syn.prefill_bf16(seed=1)
+        q, k, v = (_bf(x, device) for x in (w.q, w.k, w.v))
+        gq, gk = (torch.from_numpy(x).to(device) for x in (w.gamma_q, w.gamma_k))
+        out = torch.empty_like(q)
+        call = lambda: R.rapt_bidir_fwd(q, k, v, gq, gk, out=out)
     elif args.only == "l2":
         wl = syn.l2_bf16(seed=4)
         q, k, v = (_bf(x, device) for x in (wl.q, wl.k, wl.v))
@@ -376,7 +382,8 @@ def run_gpu(args, rank, world, local):
                           "64 consecutive steps at positions 512..575",
               "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"],
                            "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
-                           "bytes_per_step": dec_bytes}}
+                           "bytes_per_step": dec_bytes,
+                           "traffic": read_traffic("decode", "decode_kernel")}}
     del S, z, S_init, z_init, tq, tk, tv, tp, dout
 
     # ---------------- packed varlen (T=65536, H=32, d=64)
@@ -394,7 +401,9 @@ def run_gpu(args, rank, world, local):
               "workload": "varlen T=65536 H=32 d=64 bf16, %d documents U[128,8192]" % len(wv.lengths),
               "roofline": {"bound": "hbm", "achieved": v_bytes / (v_mean * 1e-3) / 1e9,
                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                           "frac": v_bytes / (v_mean * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
+                           "frac": v_bytes / (v_mean * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                           "traffic": read_traffic("varlen", "segment_state_kernel", "prefill_tc_kernel"),
+                           "kernels": "segment_state_kernel<64> + prefill_tc_kernel<64> (one call)"}}
     del vq, vk, vv, vo, wv
 
     # ---------------- original RLA, L2 denominator (B=2, L=16384, H=16, d=128)
@@ -413,9 +422,26 @@ def run_gpu(args, rank, world, local):
                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": l_bytes / (l_mean * 1e-3) / 1e9 / peaks["hbm_gbs"],
                            "tflops": l_flops / (l_mean * 1e-3) / 1e12,
-                           "traffic": read_traffic("l2_tc_moments", "l2_tc_readout"),
+                           "traffic": read_traffic("l2", "l2_tc_moments", "l2_tc_reduce", "l2_tc_readout"),
                            "kernels": "l2_tc_moments + l2_tc_reduce + l2_tc_readout (one call)"}}
     del lq, lk, lv, lo, ws
+
+    # ---------------- bidirectional RLA-2 on the headline's inputs (B=4, L=4096, H=16, d=128)
+    bws = torch.empty(lib.rapt_bidir_workspace_size(B, L, H, d, 1), dtype=torch.uint8, device=device)
+    b_ms, b_launch = time_steps(lambda: R.rapt_bidir_fwd(q, k, v, gq, gk, out=out, workspace=bws),
+                                max(3, args.steps // 2), args.warmup, flush,
+                                counter=lib.rapt_launch_counter)
+    b_mean = max_over_ranks(statistics.fmean(b_ms), device)
+    bidir = {"value": world * B * L / (b_mean * 1e-3), "unit": "tokens/s", "ms_per_step": b_mean,
+             "workload": "rla2_bidir B=4 L=4096 H=16 d=128 bf16 (non-causal, Sum denominator), "
+                         "the headline's inputs",
+             "launches_per_call": b_launch / max(3, args.steps // 2),
+             "roofline": {"bound": "hbm", "achieved": alg_bytes / (b_mean * 1e-3) / 1e9,
+                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": alg_bytes / (b_mean * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                          "traffic": read_traffic("bidir", "segment_state_kernel", "bidir_readout"),
+                          "kernels": "segment_state_kernel + bidir_readout (one call; the second is a programmatic dependent of the first)"}}
+    del bws
 
     # ---------------- CPU baseline: the fp64 oracle on a bounded sample (rank 0, N=1 only)
     cpu = None
@@ -426,7 +452,7 @@ def run_gpu(args, rank, world, local):
                          "each, fp64 quadratic form, %.1f s; numpy BLAS threads = host cores"
                          % (pairs, secs)}
 
-    traffic = read_traffic("segment_state_kernel", "prefill_tc_kernel")
+    traffic = read_traffic("prefill", "segment_state_kernel", "prefill_tc_kernel")
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -449,7 +475,7 @@ def run_gpu(args, rank, world, local):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(timed_launches),
         "clocks": clk,
-        "decode": decode, "varlen": varlen, "rla_l2": rla_l2,
+        "decode": decode, "varlen": varlen, "rla_l2": rla_l2, "bidir": bidir,
         "cpu_baseline": cpu,
     }
     if rank == 0:
@@ -459,10 +485,10 @@ def run_gpu(args, rank, world, local):
     return 0
 
 
-def read_traffic(*kernels: str):
-    """DRAM bytes per call, summed over ``kernels`` (the launches of one call), from the committed
-    ncu summary; None unless every kernel has a row taken on its source as it is now (each row
-    records a hash of the source file)."""
+def read_traffic(case: str, *kernels: str):
+    """DRAM bytes per call of workload ``case`` (a ``--only`` name), summed over ``kernels`` (the
+    launches of one call), from the committed ncu summary; None unless every kernel has a row for
+    that case taken on its source as it is now (each row records a hash of the source file)."""
     import hashlib
 
     table = os.path.join(ROOT, "profiles", "traffic.md")
@@ -471,14 +497,14 @@ def read_traffic(*kernels: str):
     found = {}
     for line in open(table):
         parts = [p.strip() for p in line.strip().strip("|").split("|")]
-        if len(parts) >= 4 and parts[0] in kernels:
-            src = os.path.join(ROOT, "relu_linear_attention_gb300", "csrc", parts[1])
+        if len(parts) >= 5 and parts[0] == case and parts[1] in kernels:
+            src = os.path.join(ROOT, "relu_linear_attention_gb300", "csrc", parts[2])
             if not os.path.exists(src):
                 return None
             h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-            if h != parts[2]:
+            if h != parts[3]:
                 return None
-            found[parts[0]] = float(parts[3])
+            found[parts[1]] = float(parts[4])
     return sum(found.values()) if len(found) == len(kernels) else None
 
 
@@ -489,7 +515,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--oracle-seconds", type=float, default=15.0)
-    ap.add_argument("--only", choices=["prefill", "varlen", "l2"], default=None,
+    ap.add_argument("--only", choices=["prefill", "varlen", "l2", "bidir"], default=None,
                     help="run one workload's calls without timing (for an ncu capture)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

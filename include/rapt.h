@@ -158,8 +158,8 @@ rapt_status rapt_varlen_fwd(const void* q, const void* k, const void* v, rapt_dt
  *   Varlen: q, k, v, out [T, H, d]; cu_seqlens and max_seqlen as for rapt_varlen_fwd; RoPE
  *           positions restart at 0 in every document, and a document sees only its own tokens.
  *   dev_status  nullable DEVICE uint32, as for rapt_prefill_fwd / rapt_varlen_fwd.
- *   workspace   at least the matching *_workspace_size() bytes, 16-byte aligned (fp32 state of
- *               every block of the documents, then the reduced state of every document).
+ *   workspace   at least the matching *_workspace_size() bytes, 16-byte aligned (the fp32
+ *               state K'^T V and sum k' of every block of every (document, head)).
  * There is no carried-in or final state: the state is the document's own.
  * Requirements as for the causal entry points. bf16 with d = 64 or 128 runs on the tensor cores
  * (bf16 GEMM operands, fp32 accumulation, fp32 denominator); fp32, and bf16 with d = 16 or 32,

@@ -5,20 +5,20 @@
 // bidirectional branch of the Sum-denominator layer; formula and eps of §3):
 //   q' = ReLU(RoPE(RMSNorm(q))), k' likewise;  over the whole document
 //   S = K'^T V (d x d),  z = sum_tau k'_tau,  out_t = q'_t S / (q'_t . z + eps)
-// so the L x L score matrix is never formed. Three launches on the caller's stream:
+// so the L x L score matrix is never formed. Two launches on the caller's stream:
 //   1. state blocks: the causal prefill's state kernel in whole-document mode, i.e. K'^T V and the
 //      column sums of k' of every block of blk_len tokens (features on 16 producer warps, one GEMM
-//      per 128-token chunk into TMEM);
-//   2. reduce: per (document, head), the blocks summed in block order (deterministic), written as
-//      the bf16 B operand of launch 3 in the exact shared-memory layout the tensor core reads, with
-//      z in fp32 after it (one bulk copy brings both into the readout CTA);
-//   3. readout, one CTA per (document, head, run of 128-token tiles): q tiles arrive by TMA; eight
-//      feature warps turn each tile into q' in place and form the fp32 q'.z of every row; one thread
-//      issues O = Q' S into one of two TMEM accumulators; four epilogue warps scale O by
-//      1 / (q'.z + eps) and stage whole tiles for a TMA store (the ragged last tile of a document
-//      is written row by row, so no store reaches past it).
-// Launches 2 and 3 are programmatic dependents of the launch before them. Every wait is bounded;
-// a readout CTA whose wait gives up writes NaN over its rows and sets RAPT_DEV_INTERNAL.
+//      per 128-token chunk into TMEM), fp32 records in the workspace;
+//   2. readout, one CTA per (document, head, run of 128-token tiles), a programmatic dependent of
+//      launch 1: q tiles arrive by TMA from the start; once launch 1 is complete, twelve warps sum
+//      the document's block records in block order (deterministic) straight into the bf16 B
+//      operand of S in shared memory (the layout the tensor core reads) and z in fp32; eight
+//      feature warps turn each q tile into q' in place, several rows at a time, and form the fp32
+//      q'.z of every row; one thread issues O = Q' S into one of two TMEM accumulators; four
+//      epilogue warps scale O by 1 / (q'.z + eps) and stage whole tiles for a TMA store (the
+//      ragged last tile of a document is written row by row, so no store reaches past it).
+// Every wait is bounded; a readout CTA whose wait gives up writes NaN over its rows and sets
+// RAPT_DEV_INTERNAL.
 #include <cuda.h>
 
 #include <cstring>
@@ -37,19 +37,21 @@ constexpr int kC = 128;                    // tokens per tile = MMA M
 constexpr long long kWait = 2000000000LL;  // ~1 s
 constexpr int kStages = 3;                 // q tiles in flight
 constexpr int kEpi = 128;                  // warps 0-3: epilogue (one TMEM lane quarter each)
-constexpr int kFeat = 256;                 // warps 4-11: features
-constexpr int kThreads = kEpi + kFeat + 64;  // warp 12: TMA, warp 13: MMA
+constexpr int kFeat = 512;                 // the next warps: features (16)
+constexpr int kWarpTma = (kEpi + kFeat) / 32;  // then one TMA warp and one MMA warp
+constexpr int kWarpMma = kWarpTma + 1;
+constexpr int kThreads = kEpi + kFeat + 64;
 constexpr uint32_t kDevBadDoc = 1u, kDevInternal = 2u;
 
-// Reduced operands of one (document, head): S as the bf16 B operand (rows = K = feature i, 64-column
-// blocks of N = value column j, each block D rows x 128 bytes, 16-byte chunk c of row i at
-// c ^ (i & 7)), then z (D floats).
+// The document's state in the readout CTA: S as the bf16 B operand (rows = K = feature i,
+// 64-column blocks of N = value column j, each block D rows x 128 bytes, 16-byte chunk c of row i
+// at c ^ (i & 7)), then z (D floats).
 template <int D>
 struct Img {
   static constexpr uint32_t S_BYTES = D * D * 2;
   static constexpr uint32_t BYTES = S_BYTES + D * 4;
-  static_assert(BYTES % 16 == 0, "bulk copy granularity");
 };
+constexpr int kBuild = kEpi + kFeat;  // threads that build the state operand
 
 // Feature mapping of the readout: a thread owns 8 consecutive elements (one 16-byte chunk, four
 // RoPE pairs) of one row; TPR threads per row, RPP rows per pass.
@@ -67,7 +69,7 @@ struct Lay {
   static constexpr uint32_t QS = (Img<D>::BYTES + 1023) / 1024 * 1024;  // q tiles (after S and z)
   static constexpr uint32_t INV = QS + kStages * QT;                  // 1 / den [stage][128]
   static constexpr uint32_t TAB = INV + kStages * kC * 4;             // FeatTab (8 D floats)
-  // mfull, qfull[S], feat[S], staged[S], accf[2], accfree[2]
+  // sready, qfull[S], feat[S], staged[S], accf[2], accfree[2]
   static constexpr uint32_t BAR = TAB + 8 * D * 4;
   static constexpr uint32_t MISC = BAR + (1 + 3 * kStages + 4) * 8;   // TMEM base, abort flag
   static constexpr uint32_t BYTES = MISC + 16;
@@ -76,47 +78,17 @@ struct Lay {
 };
 
 // ------------------------------------------------------------------------------------------------
-// Launch 2: the state of every (document, head), reduced over its blocks in block order.
-template <int D>
-__global__ void __launch_bounds__(256) bidir_reduce(const TcArgs ta, long img_offset) {
-  constexpr int Q = D * D / 4;  // float4 per K'^T V record
-  const int unit = blockIdx.y;  // document * H + head
-  tc::grid_launch_dependents();  // the readout may set up and load its first q tiles
-  long row0;
-  int n;
-  doc_bounds(ta.p, unit / ta.p.H, row0, n);
-  const int nblk = (n + ta.blk_len - 1) / ta.blk_len;
-  tc::grid_dep_wait();  // the state blocks
-  const float* rec = ta.ws + static_cast<long>(unit) * ta.nblk_max * Rec<D>::FLOATS;
-  uint8_t* img = reinterpret_cast<uint8_t*>(ta.ws) + img_offset + static_cast<long>(unit) * Img<D>::BYTES;
-  for (int e = blockIdx.x * 256 + threadIdx.x; e < Q; e += gridDim.x * 256) {
-    float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int b = 0; b < nblk; ++b) {
-      const float4 x = __ldcg(reinterpret_cast<const float4*>(rec + b * Rec<D>::FLOATS) + e);
-      m.x += x.x; m.y += x.y; m.z += x.z; m.w += x.w;
-    }
-    // record float4 e holds row i = e % D, columns 4 (e / D) .. + 3
-    const int i = e % D, j = 4 * (e / D);
-    const int jb = j / 64, cc = (j % 64) / 8, half = (j % 8) / 4;
-    *reinterpret_cast<uint2*>(img + jb * (D * 128) + i * 128 + ((cc ^ (i & 7)) << 4) + half * 8) =
-        make_uint2(tc::pack_bf16x2(m.x, m.y), tc::pack_bf16x2(m.z, m.w));
-  }
-  if (blockIdx.x == 0 && threadIdx.x < D) {
-    float z = 0.f;
-    for (int b = 0; b < nblk; ++b) z += __ldcg(rec + b * Rec<D>::FLOATS + Rec<D>::Z + threadIdx.x);
-    reinterpret_cast<float*>(img + Img<D>::S_BYTES)[threadIdx.x] = z;
-  }
-}
-
-// ------------------------------------------------------------------------------------------------
-// Launch 3: readout.
+// Launch 2: readout.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    bidir_readout(const PrefillArgs a, int nsplit, int split_chunks, const uint8_t* imgs,
-                  const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap to) {
+    bidir_readout(const PrefillArgs a, int nsplit, int split_chunks, const float* recs, int blk_len,
+                  int nblk_max, const __grid_constant__ CUtensorMap tq,
+                  const __grid_constant__ CUtensorMap to) {
   using L = Lay<D>;
   using FM = FeatMap<D>;
   constexpr int S = kStages, TPR = FM::TPR, RPP = FM::RPP, NPASS = FM::NPASS;
+  constexpr int NB = NPASS < 4 ? NPASS : 4;  // feature rows a thread works on at once
+  static_assert(NPASS % NB == 0, "feature batches");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sp = blockIdx.x % nsplit, unit = blockIdx.x / nsplit;
   const int doc = unit / a.H, h = unit % a.H;
@@ -129,7 +101,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int c0 = sp * split_chunks;
   const int ntile = min((n + kC - 1) / kC, c0 + split_chunks) - c0;
   if (ntile <= 0) return;  // uniform, before any allocation
-  const uint8_t* img = imgs + static_cast<long>(unit) * Img<D>::BYTES;
 
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t base = tc::smem_u32(smem);
@@ -146,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    tc::mbar_init(bar_m, 1);
+    tc::mbar_init(bar_m, kBuild);
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(bar_qfull + 8 * s, 1);
       tc::mbar_init(bar_feat + 8 * s, kFeat);
@@ -169,8 +140,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tile = [&](int s) { return base + L::QS + s * L::QT; };
   auto whole = [&](int i) { return (c0 + i) * kC + kC <= n; };
 
-  if (warp == 12) {
-    if (lane == 0 && run) {  // TMA: q tiles in, whole output tiles back, and S / z once
+  if (warp < kWarpTma) {
+    // S and z of the document: launch 1's block records, summed in block order
+    tc::grid_dep_wait();
+    if (run) {
+      const float* rec = recs + static_cast<long>(unit) * nblk_max * Rec<D>::FLOATS;
+      const int nblk = (n + blk_len - 1) / blk_len;
+      for (int e = tid; e < D * D / 4; e += kBuild) {
+        float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int b = 0; b < nblk; ++b) {
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(rec + b * Rec<D>::FLOATS) + e);
+          m.x += x.x; m.y += x.y; m.z += x.z; m.w += x.w;
+        }
+        // record float4 e holds row i = e % D, columns 4 (e / D) .. + 3
+        const int i = e % D, j = 4 * (e / D);
+        const int jb = j / 64, cc = (j % 64) / 8, half = (j % 8) / 4;
+        *reinterpret_cast<uint2*>(smem + jb * (D * 128) + i * 128 + ((cc ^ (i & 7)) << 4) + half * 8) =
+            make_uint2(tc::pack_bf16x2(m.x, m.y), tc::pack_bf16x2(m.z, m.w));
+      }
+      if (tid < D) {
+        float z = 0.f;
+        for (int b = 0; b < nblk; ++b) z += __ldcg(rec + b * Rec<D>::FLOATS + Rec<D>::Z + tid);
+        reinterpret_cast<float*>(smem + Img<D>::S_BYTES)[tid] = z;
+      }
+      tc::fence_async_smem();
+      tc::mbar_arrive(bar_m);
+    }
+  }
+  if (warp == kWarpTma) {
+    if (lane == 0 && run) {  // TMA: q tiles in, whole output tiles back
       int ok = 1;
       for (int i = 0; i < ntile + S && ok; ++i) {
         if (i >= S) {  // the tile S back is staged: store it (if whole), then its buffer is free
@@ -193,16 +191,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::tma_load_3d(tile(s) + jb * 16384, &tq, 64 * jb, h, static_cast<int>(row0 + (c0 + i) * kC),
                             bar_qfull + 8 * s);
         }
-        if (i == 0) {
-          tc::grid_dep_wait();  // S and z come from the reduce launch
-          tc::mbar_arrive_expect_tx(bar_m, Img<D>::BYTES);
-          tc::bulk_g2s(base, img, Img<D>::BYTES, bar_m);
-        }
       }
       if (!ok) atomicExch(s_abort, 1);
       tc::bulk_wait0();
     }
-  } else if (warp == 13) {
+  } else if (warp == kWarpMma) {
     if (lane == 0 && run) {  // MMA: O = Q' S, M = 128 tokens, N = K = d
       constexpr uint32_t ID = tc::idesc_bf16(128, D, false, true);
       const uint64_t dm = tc::desc_sw128(base, D * 128, 1024);
@@ -223,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) atomicExch(s_abort, 1);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= kEpi / 32) {
     if (run) {  // features of the q tiles, in place, and 1 / (q'.z + eps) of every row
       const int ft = tid - kEpi;
       const int prow = ft / TPR, part = ft % TPR, e0 = 8 * part;
@@ -247,23 +240,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         Rot rot;  // angles of this thread's first row of the tile, exact
         tab_rot_at(tab, a.pos_offset + (c0 + i) * kC + prow, e0 / 2, rot);
         float* inv = inv_den + s * kC;
-#pragma unroll 2
-        for (int p = 0; p < NPASS; ++p) {
-          const int r = p * RPP + prow;
-          if (p > 0) rot_step(rot, step);
-          const uint32_t addr = tile(s) + cblk + tc::sw128(r, cidx);
-          Pairs f = unpack_pairs(lds16(addr));
-          const float rinv = rsqrtf(row_sum<TPR>(sumsq(f)) * (1.0f / D) + a.fa.eps_norm);
-          float2 g0[2] = {gq0[0], gq0[1]}, g1[2] = {gq1[0], gq1[1]};
-          scale_gains(g0, g1, rinv);
-          rope_relu(f, g0, g1, rot);
-          float2 d2 = __fmul2_rn(f.x0[0], zx0[0]);
-          d2 = __ffma2_rn(f.x1[0], zx1[0], d2);
-          d2 = __ffma2_rn(f.x0[1], zx0[1], d2);
-          d2 = __ffma2_rn(f.x1[1], zx1[1], d2);
-          const float dq = row_sum<TPR>(d2.x + d2.y);
-          if (part == 0) inv[r] = 1.0f / (dq + a.eps_den);
-          sts16(addr, pack_pairs(f));
+        const uint32_t tb = tile(s) - base + cblk;  // byte offset of this thread's column block
+        // NB rows at a time: their loads, row reductions and shuffles are independent, so their
+        // latencies overlap (one row per pass would leave every step of the chain exposed)
+#pragma unroll 1
+        for (int p0 = 0; p0 < NPASS; p0 += NB) {
+          Pairs f[NB];
+          float red[NB];
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            f[b] = unpack_pairs(*reinterpret_cast<const uint4*>(smem + tb + tc::sw128((p0 + b) * RPP + prow, cidx)));
+            red[b] = sumsq(f[b]);
+          }
+#pragma unroll
+          for (int b = 0; b < NB; ++b) red[b] = row_sum<TPR>(red[b]);
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            if (p0 + b > 0) rot_step(rot, step);
+            float2 g0[2] = {gq0[0], gq0[1]}, g1[2] = {gq1[0], gq1[1]};
+            scale_gains(g0, g1, rsqrtf(red[b] * (1.0f / D) + a.fa.eps_norm));
+            rope_relu(f[b], g0, g1, rot);
+            float2 d2 = __fmul2_rn(f[b].x0[0], zx0[0]);
+            d2 = __ffma2_rn(f[b].x1[0], zx1[0], d2);
+            d2 = __ffma2_rn(f[b].x0[1], zx0[1], d2);
+            d2 = __ffma2_rn(f[b].x1[1], zx1[1], d2);
+            red[b] = d2.x + d2.y;
+          }
+#pragma unroll
+          for (int b = 0; b < NB; ++b) red[b] = row_sum<TPR>(red[b]);
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            const int r = (p0 + b) * RPP + prow;
+            if (part == 0) inv[r] = 1.0f / (red[b] + a.eps_den);
+            sts16(base + tb + tc::sw128(r, cidx), pack_pairs(f[b]));
+          }
         }
         tc::fence_async_smem();
         tc::mbar_arrive(bar_feat + 8 * s);
@@ -271,7 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) atomicExch(s_abort, 1);
     }
   } else if (run) {
-    // epilogue: TMEM lane = tile row er
+    // epilogue: TMEM lane = tile row er (warps 0-3, one lane quarter each)
+    static_assert(kEpi == 128, "one epilogue warp per TMEM lane quarter");
     const int er = 32 * warp + lane;
     const uint32_t tl = static_cast<uint32_t>(32 * warp) << 16;
     __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out);
@@ -366,7 +377,8 @@ cudaError_t launch_d(const PrefillArgs& a, const BidirPlan& plan, void* ws, cuda
   if (e != cudaSuccess) return e;
   e = launch_state_tc(D, ta, stream);
   if (e != cudaSuccess) return e;
-  // the reduce and the readout are programmatic dependents of the launch before them
+  // the readout is a programmatic dependent of the state launch: its CTAs start as that launch's
+  // finish and wait for it (griddepcontrol.wait) before reading the records
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -374,16 +386,11 @@ cudaError_t launch_d(const PrefillArgs& a, const BidirPlan& plan, void* ws, cuda
   c.stream = stream;
   c.attrs = pdl;
   c.numAttrs = 1;
-  c.gridDim = dim3(static_cast<unsigned>((D * D / 4 + 255) / 256), static_cast<unsigned>(units));
-  c.blockDim = dim3(256);
-  e = cudaLaunchKernelEx(&c, bidir_reduce<D>, ta, static_cast<long>(plan.img_offset));
-  note_launches(1);
-  if (e != cudaSuccess) return e;
   c.gridDim = dim3(static_cast<unsigned>(units * plan.nsplit));
   c.blockDim = dim3(kThreads);
   c.dynamicSmemBytes = Lay<D>::BYTES;
-  const uint8_t* imgs = static_cast<const uint8_t*>(ws) + plan.img_offset;
-  e = cudaLaunchKernelEx(&c, bidir_readout<D>, a, plan.nsplit, plan.split_chunks, imgs, tq, to);
+  e = cudaLaunchKernelEx(&c, bidir_readout<D>, a, plan.nsplit, plan.split_chunks,
+                         static_cast<const float*>(ws), plan.blk_len, plan.nblk_max, tq, to);
   note_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -420,9 +427,7 @@ BidirPlan bidir_plan(int n_docs, int H, int max_seqlen, int d) {
     }
   }
   const size_t rec = static_cast<size_t>(d) * (d + 1) * sizeof(float);
-  const size_t img = static_cast<size_t>(d) * d * 2 + static_cast<size_t>(d) * 4;
-  p.img_offset = (static_cast<size_t>(units) * p.nblk_max * rec + 1023) / 1024 * 1024;
-  p.ws_bytes = p.img_offset + static_cast<size_t>(units) * img;
+  p.ws_bytes = static_cast<size_t>(units) * p.nblk_max * rec;
   return p;
 }
 

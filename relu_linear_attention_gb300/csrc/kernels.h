@@ -79,13 +79,12 @@ cudaError_t launch_state_tc(int d, const TcArgs& ta, cudaStream_t stream);
 
 // Bidirectional (non-causal) RLA-2 over a set of documents on the tensor cores (bf16, d in
 // {64, 128}): out_t = q'_t S_doc / (q'_t . z_doc + eps) with S_doc, z_doc over the whole document.
-// Three launches; ws_bytes of workspace.
+// Two launches; ws_bytes of workspace (the fp32 state records of the blocks).
 struct BidirPlan {
-  int blk_len;   // tokens per state block
-  int nblk_max;  // state blocks per document slot
-  int nsplit;    // readout CTAs per (document, head)
+  int blk_len;       // tokens per state block
+  int nblk_max;      // state blocks per document slot
+  int nsplit;        // readout CTAs per (document, head)
   int split_chunks;  // 128-token tiles per readout CTA
-  size_t img_offset;  // byte offset of the reduced operands in ws
   size_t ws_bytes;
 };
 BidirPlan bidir_plan(int n_docs, int H, int max_seqlen, int d);
