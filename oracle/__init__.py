@@ -34,6 +34,10 @@ L = 1 and constant-v closed forms, linearity in v, the L2 identity
 sum(s^2) = q'^T (K'^T K') q', varlen == per-document dense runs, decode ==
 last prefill row, bidirectional == causal on the last row and invariant under
 any reordering of the keys, and an independent pure-Python brute force on L <= 16.
+The backward (rla2_bwd.py, gradients of sum dout . out) is pinned by central
+finite differences of the forward oracle and of the brute force, Euler's
+identity in v, the RMSNorm scale identity, the RoPE adjoint, shared gains =
+sum over heads, and varlen == per-document dense runs.
 The RoPE frequency schedule theta_j = base^(-2j/d) is the textbook one; the
 pages name the base and the pairing but print no frequency formula, so the
 schedule is pinned only through its properties (pair 0 turns by exactly p
@@ -56,4 +60,13 @@ from .rla2 import (  # noqa: F401
     rla2_bidir_varlen,
     rla_l2,
     relative_error,
+)
+from .rla2_bwd import (  # noqa: F401
+    relu_bwd,
+    rope_adjacent_bwd,
+    rmsnorm_bwd,
+    features_bwd,
+    rla2_causal_doc_bwd,
+    rla2_prefill_bwd,
+    rla2_varlen_bwd,
 )
