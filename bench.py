@@ -273,6 +273,12 @@ def profile_case(args):
         gq, gk = (torch.from_numpy(x).to(device) for x in (w.gamma_q, w.gamma_k))
         out = torch.empty_like(q)
         call = lambda: R.rapt_bidir_fwd(q, k, v, gq, gk, out=out)
+    elif args.only == "backward":
+        w = syn.prefill_bf16(seed=1)
+        q, k, v = (_bf(x, device) for x in (w.q, w.k, w.v))
+        gq, gk = (torch.from_numpy(x).to(device) for x in (w.gamma_q, w.gamma_k))
+        tg = torch.empty_like(q).normal_(generator=torch.Generator(device=device).manual_seed(5))
+        call = lambda: R.rapt_prefill_bwd(q, k, v, tg, gq, gk)
     elif args.only == "l2":
         wl = syn.l2_bf16(seed=4)
         q, k, v = (_bf(x, device) for x in (wl.q, wl.k, wl.v))
@@ -443,6 +449,31 @@ def run_gpu(args, rank, world, local):
                           "kernels": "segment_state_kernel + bidir_readout (one call; the second is a programmatic dependent of the first)"}}
     del bws
 
+    # ---------------- backward of the headline prefill (dq, dk, dv, dgamma; CUDA cores, fp32 math)
+    tg = torch.empty_like(q).normal_(generator=torch.Generator(device=device).manual_seed(5))
+    gws = torch.empty(lib.rapt_prefill_bwd_workspace_size(B, L, H, d, 1), dtype=torch.uint8,
+                      device=device)
+    grads = [torch.empty_like(q) for _ in range(3)] + [torch.empty_like(gq), torch.empty_like(gk)]
+    g_ms, g_launch = time_steps(
+        lambda: R.rapt_prefill_bwd(q, k, v, tg, gq, gk, dq=grads[0], dk=grads[1], dv=grads[2],
+                                   dgamma_q=grads[3], dgamma_k=grads[4], workspace=gws),
+        max(3, args.steps // 4), args.warmup, flush, counter=lib.rapt_launch_counter)
+    g_mean = max_over_ranks(statistics.fmean(g_ms), device)
+    g_flops = B * L * H * (12 * d * d)  # recurrence-form backward: q'S, S g, R v, R^T k', S and R updates
+    fp32_peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    backward = {"value": world * B * L / (g_mean * 1e-3), "unit": "tokens/s", "ms_per_step": g_mean,
+                "workload": "rla2_causal_prefill backward B=4 L=4096 H=16 d=128 bf16 (dq, dk, dv, "
+                            "dgamma_q, dgamma_k), the headline's inputs",
+                "launches_per_call": g_launch / max(3, args.steps // 4),
+                "roofline": {"bound": "alu", "achieved": g_flops / (g_mean * 1e-3) / 1e12,
+                             "peak": fp32_peak, "unit": "TFLOP/s",
+                             "frac": g_flops / (g_mean * 1e-3) / 1e12 / fp32_peak,
+                             "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x max SM clock",
+                             "algorithmic_flops_per_call": g_flops,
+                             "kernels": "bwd_state_kernel + bwd_forward_kernel + bwd_reverse_kernel "
+                                        "+ bwd_gain_kernel (one call)"}}
+    del tg, gws, grads
+
     # ---------------- CPU baseline: the fp64 oracle on a bounded sample (rank 0, N=1 only)
     cpu = None
     if rank == 0 and world == 1:
@@ -476,6 +507,7 @@ def run_gpu(args, rank, world, local):
         "gpu_launches": int(timed_launches),
         "clocks": clk,
         "decode": decode, "varlen": varlen, "rla_l2": rla_l2, "bidir": bidir,
+        "backward": backward,
         "cpu_baseline": cpu,
     }
     if rank == 0:
@@ -515,7 +547,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--oracle-seconds", type=float, default=15.0)
-    ap.add_argument("--only", choices=["prefill", "varlen", "l2", "bidir"], default=None,
+    ap.add_argument("--only", choices=["prefill", "varlen", "l2", "bidir", "backward"], default=None,
                     help="run one workload's calls without timing (for an ncu capture)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

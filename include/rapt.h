@@ -149,6 +149,48 @@ rapt_status rapt_varlen_fwd(const void* q, const void* k, const void* v, rapt_dt
                             rapt_stream_t stream);
 
 /*
+ * Backward of the causal forward (08-rapt-algorithm.md §4.2 "backward": one prefix scan and two
+ * suffix scans, then back through ReLU, RoPE and RMSNorm). For an upstream gradient dout = dL/dout
+ * it returns dL/dq, dL/dk, dL/dv and the gain gradients. With gnum_t = dout_t / den_t and
+ * scale_t = -(dout_t . num_t) / den_t^2 (num_t, den_t the forward's numerator and denominator):
+ *   dq'_t = S_t gnum_t + scale_t z_t,
+ *   dk'_tau = sum_{t >= tau} q'_t (gnum_t . v_tau + scale_t),   dv_tau = sum_{t >= tau} s_{t,tau} gnum_t,
+ * then dq, dk through the feature map (the gradient passes the ReLU where its input is > 0; RoPE
+ * is undone by the inverse rotation; RMSNorm: dx = r gamma dy - x r^3 (sum gamma dy x) / d).
+ * Sums run inside each document (the state restarts at document boundaries).
+ *   q, k, v, dout  as the forward's inputs (same dtype and layout); dout is dL/dout.
+ *   gamma_q, gamma_k, params, pos_offset: as for the forward call being differentiated.
+ *   dq, dk, dv     outputs of the inputs' dtype and layout; none may alias an input or another.
+ *   dgamma_q, dgamma_k  nullable fp32 outputs shaped like the gains ([d] when shared, summed over
+ *                  every token and head; [H, d] when per head): written, not accumulated.
+ *   workspace      at least the matching *_bwd_workspace_size() bytes, 16-byte aligned (state
+ *                  increments of the segments the documents are cut into, den and scale of every
+ *                  (token, head), and partial gain sums).
+ *   dev_status     (varlen) as for rapt_varlen_fwd: malformed documents are skipped and their
+ *                  gradients are not written.
+ * The forward has no carried-in state here (S0 = z0 = 0: documents start fresh). The computation
+ * is recomputed from q, k, v (no activations of the forward are kept). All arithmetic is fp32 on
+ * CUDA cores for every dtype and d; bf16 outputs are rounded to nearest even. Every sum has a
+ * fixed order: repeated calls give bitwise-identical results.
+ */
+size_t rapt_prefill_bwd_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype);
+rapt_status rapt_prefill_bwd(const void* q, const void* k, const void* v, const void* dout,
+                             rapt_dtype dtype, int32_t B, int32_t L, int32_t H, int32_t d,
+                             const float* gamma_q, const float* gamma_k, rapt_params params,
+                             int32_t pos_offset, void* dq, void* dk, void* dv, float* dgamma_q,
+                             float* dgamma_k, void* workspace, size_t workspace_bytes,
+                             rapt_stream_t stream);
+size_t rapt_varlen_bwd_workspace_size(int32_t T, int32_t N, int32_t H, int32_t d,
+                                      int32_t max_seqlen, rapt_dtype dtype);
+rapt_status rapt_varlen_bwd(const void* q, const void* k, const void* v, const void* dout,
+                            rapt_dtype dtype, int32_t T, int32_t H, int32_t d,
+                            const int32_t* cu_seqlens, int32_t N, int32_t max_seqlen,
+                            const float* gamma_q, const float* gamma_k, rapt_params params,
+                            void* dq, void* dk, void* dv, float* dgamma_q, float* dgamma_k,
+                            uint32_t* dev_status, void* workspace, size_t workspace_bytes,
+                            rapt_stream_t stream);
+
+/*
  * Bidirectional (non-causal) RLA-2 (08-rapt-algorithm.md §4.1: in its causal=false mode the prefix
  * scan sums over the whole set; §4.2: the layer's bidirectional branch; formula and eps of §3).
  * Features as in the causal form; for each (document, head), S = sum_tau k'_tau v_tau^T and

@@ -51,6 +51,18 @@ SIGNATURES = {
                                   c_void_p, rapt_params, c_void_p,
                                   c_void_p, c_void_p, c_void_p, c_void_p,
                                   c_void_p, c_void_p, c_size_t, c_void_p]),
+    "rapt_prefill_bwd_workspace_size": (c_size_t, [c_int32] * 4 + [c_int32]),
+    "rapt_prefill_bwd": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
+                                   c_int32, c_int32, c_int32, c_int32,
+                                   c_void_p, c_void_p, rapt_params, c_int32,
+                                   c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                   c_void_p, c_size_t, c_void_p]),
+    "rapt_varlen_bwd_workspace_size": (c_size_t, [c_int32] * 5 + [c_int32]),
+    "rapt_varlen_bwd": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
+                                  c_int32, c_int32, c_int32, c_void_p, c_int32, c_int32,
+                                  c_void_p, c_void_p, rapt_params,
+                                  c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                  c_void_p, c_void_p, c_size_t, c_void_p]),
     "rapt_bidir_workspace_size": (c_size_t, [c_int32] * 4 + [c_int32]),
     "rapt_bidir_fwd": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32,
                                  c_int32, c_int32, c_int32, c_int32,

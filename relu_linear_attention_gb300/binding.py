@@ -141,6 +141,81 @@ def rapt_varlen_fwd(q, k, v, cu_seqlens, gamma_q, gamma_k, *, max_seqlen, eps_no
     return out, S_final, z_final
 
 
+def _bwd_outputs(q, gamma_q, dq, dk, dv, dgamma_q, dgamma_k, need_gains):
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _cuda_contig(name, t, q.dtype, q.shape)
+    if need_gains:
+        dgamma_q = torch.empty_like(gamma_q) if dgamma_q is None else dgamma_q
+        dgamma_k = torch.empty_like(gamma_q) if dgamma_k is None else dgamma_k
+    for name, t in (("dgamma_q", dgamma_q), ("dgamma_k", dgamma_k)):
+        if t is not None:
+            _cuda_contig(name, t, torch.float32, gamma_q.shape)
+    return dq, dk, dv, dgamma_q, dgamma_k
+
+
+def rapt_prefill_bwd(q, k, v, dout, gamma_q, gamma_k, *, eps_norm=1e-6, rope_base=1e4,
+                     eps_den=1e-4, pos_offset=0, dq=None, dk=None, dv=None, dgamma_q=None,
+                     dgamma_k=None, need_gains=True, workspace=None, stream=None):
+    """Backward of the dense causal prefill: q, k, v, dout [B, L, H, d] (fp32 or bf16).
+    Returns (dq, dk, dv, dgamma_q, dgamma_k); the gain gradients are None when need_gains is
+    False and none is given."""
+    _need(q.dim() == 4, "q must be [B, L, H, d]")
+    B, L, H, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout)):
+        _cuda_contig(name, t, q.dtype, q.shape)
+    _need(q.dtype in _DT, "dtype must be float32 or bfloat16")
+    stride = _gammas(gamma_q, gamma_k, H, d)
+    dq, dk, dv, dgamma_q, dgamma_k = _bwd_outputs(q, gamma_q, dq, dk, dv, dgamma_q, dgamma_k,
+                                                  need_gains)
+    lib = _lib.load()
+    need = lib.rapt_prefill_bwd_workspace_size(B, L, H, d, _DT[q.dtype])
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.rapt_prefill_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _DT[q.dtype], B, L, H, d,
+                              _ptr(gamma_q), _ptr(gamma_k),
+                              make_params(eps_norm, rope_base, eps_den, stride), int(pos_offset),
+                              _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dgamma_q), _ptr(dgamma_k),
+                              _ptr(workspace), ws_bytes, _stream(stream))
+    _lib.check("rapt_prefill_bwd", st)
+    return dq, dk, dv, dgamma_q, dgamma_k
+
+
+def rapt_varlen_bwd(q, k, v, dout, cu_seqlens, gamma_q, gamma_k, *, max_seqlen, eps_norm=1e-6,
+                    rope_base=1e4, eps_den=1e-4, dq=None, dk=None, dv=None, dgamma_q=None,
+                    dgamma_k=None, need_gains=True, dev_status=None, workspace=None, stream=None):
+    """Backward of the packed varlen causal forward: q, k, v, dout [T, H, d]; cu_seqlens int32
+    [N + 1] on the device. Returns (dq, dk, dv, dgamma_q, dgamma_k)."""
+    _need(q.dim() == 3, "q must be [T, H, d]")
+    T, H, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout)):
+        _cuda_contig(name, t, q.dtype, q.shape)
+    _need(q.dtype in _DT, "dtype must be float32 or bfloat16")
+    _cuda_contig("cu_seqlens", cu_seqlens, torch.int32)
+    _need(cu_seqlens.dim() == 1 and cu_seqlens.numel() >= 2, "cu_seqlens must be [N + 1]")
+    N = cu_seqlens.numel() - 1
+    stride = _gammas(gamma_q, gamma_k, H, d)
+    dq, dk, dv, dgamma_q, dgamma_k = _bwd_outputs(q, gamma_q, dq, dk, dv, dgamma_q, dgamma_k,
+                                                  need_gains)
+    if dev_status is not None:
+        _cuda_contig("dev_status", dev_status, torch.int32)
+    lib = _lib.load()
+    need = lib.rapt_varlen_bwd_workspace_size(T, N, H, d, int(max_seqlen), _DT[q.dtype])
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.rapt_varlen_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _DT[q.dtype], T, H, d,
+                             _ptr(cu_seqlens), N, int(max_seqlen), _ptr(gamma_q), _ptr(gamma_k),
+                             make_params(eps_norm, rope_base, eps_den, stride),
+                             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dgamma_q), _ptr(dgamma_k),
+                             _ptr(dev_status), _ptr(workspace), ws_bytes, _stream(stream))
+    _lib.check("rapt_varlen_bwd", st)
+    return dq, dk, dv, dgamma_q, dgamma_k
+
+
 def rapt_bidir_fwd(q, k, v, gamma_q, gamma_k, *, eps_norm=1e-6, rope_base=1e4, eps_den=1e-4,
                    pos_offset=0, out=None, dev_status=None, workspace=None, stream=None):
     """Dense bidirectional (non-causal) RLA-2; q, k, v [B, L, H, d] (fp32 or bf16). Returns out."""

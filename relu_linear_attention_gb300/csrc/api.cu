@@ -81,7 +81,7 @@ const char* rapt_status_string(rapt_status s) {
   }
 }
 
-int32_t rapt_abi_version(void) { return 10100; }
+int32_t rapt_abi_version(void) { return 10200; }
 
 uint64_t rapt_launch_counter(void) { return rapt::launch_count(); }
 
@@ -264,6 +264,123 @@ rapt_status rapt_bidir_varlen_fwd(const void* q, const void* k, const void* v, r
   if (rapt::tc_supported(to_dt(dtype), d))
     return from_cuda(rapt::launch_bidir_tc(d, a, rapt::bidir_plan(N, H, max_seqlen, d), workspace, s));
   return from_cuda(rapt::launch_prefill_simt(to_dt(dtype), d, a, s));
+}
+
+namespace {
+
+// Shared tail of the two backward entry points: checks, workspace carving, launch.
+rapt_status backward_common(const void* q, const void* k, const void* v, const void* dout,
+                            rapt_dtype dtype, int n_docs, int doc_len, long total_rows, int H,
+                            int d, const int32_t* cu_seqlens, int max_seqlen, int pos_offset,
+                            const float* gamma_q, const float* gamma_k, const rapt_params& params,
+                            void* dq, void* dk, void* dv, float* dgamma_q, float* dgamma_k,
+                            uint32_t* dev_status, void* workspace, size_t workspace_bytes,
+                            size_t need, rapt_stream_t stream) {
+  if (total_rows > 0 && (q == nullptr || k == nullptr || v == nullptr || dout == nullptr ||
+                         dq == nullptr || dk == nullptr || dv == nullptr))
+    return RAPT_ERR_INVALID_ARG;
+  if (!opt_aligned16(q) || !opt_aligned16(k) || !opt_aligned16(v) || !opt_aligned16(dout) ||
+      !opt_aligned16(dq) || !opt_aligned16(dk) || !opt_aligned16(dv) ||
+      !opt_aligned16(dgamma_q) || !opt_aligned16(dgamma_k))
+    return RAPT_ERR_INVALID_ARG;
+  const void* ins[4] = {q, k, v, dout};
+  const void* outs[5] = {dq, dk, dv, dgamma_q, dgamma_k};
+  for (const void* o : outs) {
+    if (o == nullptr) continue;
+    for (const void* i : ins)
+      if (o == i) return RAPT_ERR_INVALID_ARG;
+  }
+  if ((dq != nullptr && (dq == dk || dq == dv)) || (dk != nullptr && dk == dv) ||
+      (dgamma_q != nullptr && dgamma_q == dgamma_k))
+    return RAPT_ERR_INVALID_ARG;
+  if (dev_status != nullptr && !aligned4(dev_status)) return RAPT_ERR_INVALID_ARG;
+  rapt_status st = check_features(gamma_q, gamma_k, params, d);
+  if (st != RAPT_OK) return st;
+  if (workspace_bytes < need || (need > 0 && (workspace == nullptr || !aligned16(workspace))))
+    return RAPT_ERR_WORKSPACE;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int n_gain = params.gamma_head_stride != 0 ? H * d : d;
+  if (total_rows == 0) {  // no token: the gain gradients are zero
+    if (dgamma_q != nullptr &&
+        cudaMemsetAsync(dgamma_q, 0, sizeof(float) * n_gain, s) != cudaSuccess)
+      return RAPT_ERR_CUDA;
+    if (dgamma_k != nullptr &&
+        cudaMemsetAsync(dgamma_k, 0, sizeof(float) * n_gain, s) != cudaSuccess)
+      return RAPT_ERR_CUDA;
+    return RAPT_OK;
+  }
+  const rapt::BwdPlan plan = rapt::bwd_plan(n_docs, H, max_seqlen, total_rows, d);
+  rapt::BwdArgs b{};
+  rapt::PrefillArgs& a = b.p;
+  a.q = q; a.k = k; a.v = v; a.out = nullptr;
+  a.gamma_q = gamma_q; a.gamma_k = gamma_k;
+  a.cu_seqlens = cu_seqlens; a.dev_status = dev_status;
+  a.n_docs = n_docs; a.doc_len = doc_len; a.total_rows = static_cast<int>(total_rows);
+  a.max_seqlen = max_seqlen; a.H = H; a.pos_offset = pos_offset; a.eps_den = params.eps_den;
+  a.fa = make_features(params, d);
+  b.dout = dout; b.dq = dq; b.dk = dk; b.dv = dv;
+  b.dgamma_q = dgamma_q; b.dgamma_k = dgamma_k;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  b.rec_fwd = reinterpret_cast<float*>(w);
+  b.rec_rev = reinterpret_cast<float*>(w + plan.off_rev);
+  b.den = reinterpret_cast<float*>(w + plan.off_den);
+  b.scl = reinterpret_cast<float*>(w + plan.off_scl);
+  b.sst = reinterpret_cast<float*>(w + plan.off_sst);
+  b.nst = reinterpret_cast<float*>(w + plan.off_nst);
+  b.dgp_q = reinterpret_cast<float*>(w + plan.off_dgq);
+  b.dgp_k = reinterpret_cast<float*>(w + plan.off_dgk);
+  b.nseg = plan.nseg;
+  b.seg_len = plan.seg_len;
+  return from_cuda(rapt::launch_backward_simt(to_dt(dtype), d, b, s));
+}
+
+}  // namespace
+
+size_t rapt_prefill_bwd_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d,
+                                       rapt_dtype dtype) {
+  if (!known_dtype(dtype) || !supported_d(d) || B < 1 || H < 1 || L < 1) return 0;
+  return rapt::bwd_plan(B, H, L, static_cast<long>(B) * L, d).ws_bytes;
+}
+
+rapt_status rapt_prefill_bwd(const void* q, const void* k, const void* v, const void* dout,
+                             rapt_dtype dtype, int32_t B, int32_t L, int32_t H, int32_t d,
+                             const float* gamma_q, const float* gamma_k, rapt_params params,
+                             int32_t pos_offset, void* dq, void* dk, void* dv, float* dgamma_q,
+                             float* dgamma_k, void* workspace, size_t workspace_bytes,
+                             rapt_stream_t stream) {
+  if (!known_dtype(dtype) || !supported_d(d)) return RAPT_ERR_UNSUPPORTED;
+  if (B < 1 || H < 1 || L < 0 || pos_offset < 0) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(B) * L * H * d)) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(pos_offset) + L)) return RAPT_ERR_INVALID_ARG;
+  return backward_common(q, k, v, dout, dtype, B, L, static_cast<long>(B) * L, H, d, nullptr, L,
+                         pos_offset, gamma_q, gamma_k, params, dq, dk, dv, dgamma_q, dgamma_k,
+                         nullptr, workspace, workspace_bytes,
+                         rapt_prefill_bwd_workspace_size(B, L, H, d, dtype), stream);
+}
+
+size_t rapt_varlen_bwd_workspace_size(int32_t T, int32_t N, int32_t H, int32_t d,
+                                      int32_t max_seqlen, rapt_dtype dtype) {
+  if (!known_dtype(dtype) || !supported_d(d) || N < 1 || H < 1 || max_seqlen < 0 || T < 1)
+    return 0;
+  return rapt::bwd_plan(N, H, max_seqlen, T, d).ws_bytes;
+}
+
+rapt_status rapt_varlen_bwd(const void* q, const void* k, const void* v, const void* dout,
+                            rapt_dtype dtype, int32_t T, int32_t H, int32_t d,
+                            const int32_t* cu_seqlens, int32_t N, int32_t max_seqlen,
+                            const float* gamma_q, const float* gamma_k, rapt_params params,
+                            void* dq, void* dk, void* dv, float* dgamma_q, float* dgamma_k,
+                            uint32_t* dev_status, void* workspace, size_t workspace_bytes,
+                            rapt_stream_t stream) {
+  if (!known_dtype(dtype) || !supported_d(d)) return RAPT_ERR_UNSUPPORTED;
+  if (T < 0 || N < 1 || H < 1 || max_seqlen < 0) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(T) * H * d)) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(N) * H * 4)) return RAPT_ERR_INVALID_ARG;
+  if (cu_seqlens == nullptr || !aligned4(cu_seqlens)) return RAPT_ERR_INVALID_ARG;
+  return backward_common(q, k, v, dout, dtype, N, 0, T, H, d, cu_seqlens, max_seqlen, 0, gamma_q,
+                         gamma_k, params, dq, dk, dv, dgamma_q, dgamma_k, dev_status, workspace,
+                         workspace_bytes,
+                         rapt_varlen_bwd_workspace_size(T, N, H, d, max_seqlen, dtype), stream);
 }
 
 rapt_status rapt_decode_step(const void* q, const void* k, const void* v, rapt_dtype dtype,

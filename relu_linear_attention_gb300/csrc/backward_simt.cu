@@ -1,0 +1,797 @@
+// Backward of causal RLA-2 on CUDA cores (fp32 arithmetic, fp32 or bf16 tensors), sm_103a.
+//
+// Gradients of a loss with upstream gradient g_t = dL/dout_t (08-rapt-algorithm.md §4.2
+// "backward": one prefix scan, two suffix scans, then the feature chain). Per document and head,
+// with s_{t,tau} = q'_t . k'_tau for tau <= t:
+//   den_t   = sum_{tau<=t} s_{t,tau} + eps,   num_t = sum_{tau<=t} s_{t,tau} v_tau
+//   gnum_t  = g_t / den_t,                     scale_t = -(g_t . num_t) / den_t^2
+//   dq'_t   = S_t gnum_t + scale_t z_t                       (prefix state S_t, z_t)
+//   dk'_tau = R_tau v_tau + w_tau,   dv_tau = R_tau^T k'_tau  (suffix state
+//             R_tau = sum_{t>=tau} q'_t gnum_t^T,  w_tau = sum_{t>=tau} scale_t q'_t)
+// then through ReLU (the gradient passes where the pre-activation is > 0), the inverse RoPE
+// rotation and RMSNorm (input and gain). In chunked form (C = 32 tokens), each chunk splits every
+// sum into the state carried in from earlier (later) chunks and a masked C x C block.
+//
+// The in-chunk block A[t][tau] = gnum_t . v_tau + scale_t (tau <= t) is a difference of two terms
+// that nearly cancel where a query sees few keys (for the first token of a document it is
+// (g . v) eps / den^2 while each term is ~ (g . v) / den). It is formed as
+//   A[t][tau] = ( sum_{sigma<=t in chunk} s_{t,sigma} (c_{t,tau} - c_{t,sigma})
+//                 + c_{t,tau} sst_t - nst_t + eps c_{t,tau} ) / den_t^2,   c_{t,tau} = g_t . v_tau,
+// with sst_t = q'_t . z and nst_t = g_t . (q'_t S) of the state before the chunk: the same value,
+// but the cancelling part is the difference of equal products inside a document's first chunk,
+// which is exact, so the gradient keeps its fp32 accuracy relative to its own size.
+//
+// Four launches on the caller's stream:
+//   1. bwd_state_kernel: K'^T V and sum k' of every segment but a document's last (the prefix
+//      states the segments of launch 2 start from);
+//   2. bwd_forward_kernel, one CTA per (document, head, segment), chunks in order: den, scale and
+//      gnum of every token (den and scale saved for launch 3), dq' and dq, the gain partials of q,
+//      and the segment's increment of the suffix state (Q'^T Gnum, sum scale q');
+//   3. bwd_reverse_kernel, one CTA per (document, head, segment), chunks in reverse: the suffix
+//      state from the later segments' increments, dk', dv, dk and the gain partials of k;
+//   4. bwd_gain_kernel: the gain partials summed in a fixed order.
+// No float atomics anywhere: every sum has a fixed order, so results are bitwise repeatable.
+#include "kernels.h"
+#include "tc_features.cuh"
+
+namespace rapt {
+namespace {
+
+using feat::doc_bounds;
+
+constexpr int kC = 32;  // chunk length (tokens)
+constexpr int kThreads = 256;
+constexpr int kSMs = 152;
+
+// Shared-memory layout in floats. Row strides are padded by 4 floats: float4 alignment is kept and
+// rows r, r+1, ..., r+7 start in eight different 4-bank groups (LD / 4 = D / 4 + 1 is odd).
+template <int D>
+struct BwdSmem {
+  static constexpr int LD = D + 4;
+  static constexpr int LC = kC + 4;
+  static constexpr int ST = 0;                  // [D][LD] carried state: S (launch 2) or R (launch 3)
+  static constexpr int RT = ST + D * LD;        // [D][LD] launch 2: the segment's increment of R
+  static constexpr int QF = RT + D * LD;        // [C][LD] q' (launch 2: later dq')
+  static constexpr int KF = QF + kC * LD;       // [C][LD] k' (launch 3: later dk')
+  static constexpr int VS = KF + kC * LD;       // [C][LD] v
+  static constexpr int GS = VS + kC * LD;       // [C][LD] g, then gnum = g / den
+  static constexpr int PS = GS + kC * LD;       // [C][LC] masked scores P[t][tau]
+  static constexpr int AS = PS + kC * LC;       // [C][LC] g_t . v_tau, then A[t][tau] (masked)
+  static constexpr int ZS = AS + kC * LC;       // [D] z (launch 2) or w (launch 3)
+  static constexpr int WS = ZS + D;             // [D] launch 2: the segment's increment of w
+  static constexpr int DEN = WS + D;            // [C] den_t
+  static constexpr int SCL = DEN + kC;          // [C] scale_t
+  static constexpr int SST = SCL + kC;          // [C] q'_t . z of the state before the chunk
+  static constexpr int NST = SST + kC;          // [C] g_t . (q'_t S) of the state before the chunk
+  static constexpr int total = NST + kC;
+  static constexpr size_t bytes = static_cast<size_t>(total) * sizeof(float);
+  static_assert(bytes <= 232448, "shared memory budget");
+  static_assert(PS + (kThreads / FeatureLayout<D>::TPR) * D <= ZS, "gain partials fit in PS + AS");
+};
+
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+// 4 x 4 micro-tiles of small shared-memory GEMMs; K is a multiple of 4. The tile's rows m are
+// A's rows (or columns) m0 .. m0+3, always contiguous; its columns are n0 + NS * x (x = 0..3): NS = 1
+// gives four contiguous columns (float4 loads of B), a larger NS spreads them so that neighbouring
+// lanes, which take neighbouring n0, touch neighbouring rows or columns of B (no bank conflicts).
+// acc[y][x] += sum_k A[y*lda + k] * B[(NS*x)*ldb + k]       (B contiguous along k)
+template <int NS>
+__device__ __forceinline__ void mt_dot(float (&acc)[4][4], const float* A, int lda, const float* B,
+                                       int ldb, int K) {
+  for (int k = 0; k < K; k += 4) {
+    float4 a[4], b[4];
+#pragma unroll
+    for (int y = 0; y < 4; ++y) a[y] = ld4(A + y * lda + k);
+#pragma unroll
+    for (int x = 0; x < 4; ++x) b[x] = ld4(B + NS * x * ldb + k);
+#pragma unroll
+    for (int y = 0; y < 4; ++y)
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        acc[y][x] = fmaf(a[y].x, b[x].x, acc[y][x]);
+        acc[y][x] = fmaf(a[y].y, b[x].y, acc[y][x]);
+        acc[y][x] = fmaf(a[y].z, b[x].z, acc[y][x]);
+        acc[y][x] = fmaf(a[y].w, b[x].w, acc[y][x]);
+      }
+  }
+}
+// B element (k, x) of the column forms below.
+template <int NS>
+__device__ __forceinline__ void ld_brow(const float* B, float (&b)[4]) {
+  if constexpr (NS == 1) {
+    const float4 t = ld4(B);
+    b[0] = t.x; b[1] = t.y; b[2] = t.z; b[3] = t.w;
+  } else {
+#pragma unroll
+    for (int x = 0; x < 4; ++x) b[x] = B[NS * x];
+  }
+}
+// acc[y][x] += sum_k A[y*lda + k] * B[k*ldb + NS*x]         (A along k, B along n)
+template <int NS>
+__device__ __forceinline__ void mt_outer(float (&acc)[4][4], const float* A, int lda,
+                                         const float* B, int ldb, int K) {
+  for (int k = 0; k < K; k += 4) {
+    float4 a[4];
+    float b[4][4];
+#pragma unroll
+    for (int y = 0; y < 4; ++y) a[y] = ld4(A + y * lda + k);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) ld_brow<NS>(B + (k + u) * ldb, b[u]);
+#pragma unroll
+    for (int y = 0; y < 4; ++y) {
+      const float av[4] = {a[y].x, a[y].y, a[y].z, a[y].w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) acc[y][x] = fmaf(av[u], b[u][x], acc[y][x]);
+    }
+  }
+}
+// acc[y][x] += sum_k A[k*lda + y] * B[k*ldb + NS*x]         (A along m, B along n)
+template <int NS>
+__device__ __forceinline__ void mt_tn(float (&acc)[4][4], const float* A, int lda, const float* B,
+                                      int ldb, int K) {
+  for (int k = 0; k < K; ++k) {
+    const float4 a = ld4(A + k * lda);
+    float b[4];
+    ld_brow<NS>(B + k * ldb, b);
+    const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int y = 0; y < 4; ++y)
+#pragma unroll
+      for (int x = 0; x < 4; ++x) acc[y][x] = fmaf(av[y], b[x], acc[y][x]);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void store2(T* p, float a, float b);
+template <>
+__device__ __forceinline__ void store2<float>(float* p, float a, float b) {
+  *reinterpret_cast<float2*>(p) = make_float2(a, b);
+}
+template <>
+__device__ __forceinline__ void store2<__nv_bfloat16>(__nv_bfloat16* p, float a, float b) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
+}
+
+// Backward of f = ReLU(RoPE(RMSNorm(x))) for one token row, the lane mapping of feature_row
+// (TPR lanes per row, lane r owns elements [r*EPT, (r+1)*EPT)). df: the row's gradient of f in
+// shared memory. Writes dx (valid rows only) and adds this row's gain gradient dy_hat * x * rinv
+// into dg. Every lane of the warp must call it together (shuffles over the full warp).
+template <int D, typename T>
+__device__ __forceinline__ void feature_row_bwd(const T* x, bool valid, const float* gamma,
+                                                int pos, const FeatureArgs& fa, int r,
+                                                const float* df, T* dx,
+                                                float (&dg)[FeatureLayout<D>::EPT]) {
+  using FL = FeatureLayout<D>;
+  constexpr int EPT = FL::EPT;
+  float f[EPT];
+  if (valid) {
+    RowLoad<T, EPT>::run(x + r * EPT, f);
+  } else {
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) f[i] = 0.f;
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) ss = fmaf(f[i], f[i], ss);
+#pragma unroll
+  for (int off = FL::TPR / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  const float rinv = rsqrtf(ss * (1.0f / D) + fa.eps_norm);
+  float u[EPT];  // gamma * dy_hat
+  float dot = 0.f;
+#pragma unroll
+  for (int m = 0; m < EPT / 2; ++m) {
+    const int e = r * EPT + 2 * m;
+    const float g0 = gamma[e], g1 = gamma[e + 1];
+    const float y0 = f[2 * m] * rinv * g0;
+    const float y1 = f[2 * m + 1] * rinv * g1;
+    float s, c;
+    rope_sincos(pos, fa.rope_hi[e >> 1], fa.rope_lo[e >> 1], s, c);
+    const float a = fmaf(y0, c, -y1 * s);  // the forward's pre-activation, same arithmetic
+    const float b = fmaf(y0, s, y1 * c);
+    const float da = (valid && a > 0.f) ? df[e] : 0.f;
+    const float db = (valid && b > 0.f) ? df[e + 1] : 0.f;
+    const float h0 = fmaf(da, c, db * s);   // inverse rotation
+    const float h1 = fmaf(-da, s, db * c);
+    dg[2 * m] = fmaf(h0, f[2 * m] * rinv, dg[2 * m]);
+    dg[2 * m + 1] = fmaf(h1, f[2 * m + 1] * rinv, dg[2 * m + 1]);
+    u[2 * m] = g0 * h0;
+    u[2 * m + 1] = g1 * h1;
+    dot = fmaf(u[2 * m], f[2 * m], dot);
+    dot = fmaf(u[2 * m + 1], f[2 * m + 1], dot);
+  }
+#pragma unroll
+  for (int off = FL::TPR / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+  const float c3 = rinv * rinv * rinv * dot * (1.0f / D);
+  if (valid) {
+#pragma unroll
+    for (int m = 0; m < EPT / 2; ++m)
+      store2<T>(dx + r * EPT + 2 * m, fmaf(rinv, u[2 * m], -f[2 * m] * c3),
+                fmaf(rinv, u[2 * m + 1], -f[2 * m + 1] * c3));
+  }
+}
+
+// Features of C rows starting at token t0 of the document into a [C][LD] tile (tail rows zero).
+template <int D, typename T>
+__device__ __forceinline__ void feature_tile(const T* x, long row0, int n, int t0, int H, int h,
+                                             const float* gamma, int pos0, const FeatureArgs& fa,
+                                             float* tile) {
+  using FL = FeatureLayout<D>;
+  constexpr int LD = BwdSmem<D>::LD;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = lane / FL::TPR, r = lane % FL::TPR;
+  constexpr int kRowsPerPass = (kThreads / 32) * FL::ROWS_PER_WARP;
+  for (int rr = warp * FL::ROWS_PER_WARP + grp; rr < kC; rr += kRowsPerPass) {
+    const int t = t0 + rr;
+    const bool valid = t < n;
+    float f[FL::EPT];
+    feature_row<D, T>(x + ((row0 + (valid ? t : 0)) * H + h) * D, valid, gamma, pos0 + t, fa, r, f);
+#pragma unroll
+    for (int e = 0; e < FL::EPT; ++e) tile[rr * LD + r * FL::EPT + e] = f[e];
+  }
+}
+
+// Raw rows (v or g) of C tokens into a [C][LD] tile as fp32 (tail rows zero).
+template <int D, typename T>
+__device__ __forceinline__ void raw_tile(const T* x, long row0, int n, int t0, int H, int h,
+                                         float* tile) {
+  constexpr int LD = BwdSmem<D>::LD;
+  for (int idx = threadIdx.x; idx < kC * (D / 4); idx += kThreads) {
+    const int rr = idx / (D / 4), j4 = 4 * (idx % (D / 4));
+    float f4[4] = {0.f, 0.f, 0.f, 0.f};
+    if (t0 + rr < n) RowLoad<T, 4>::run(x + ((row0 + t0 + rr) * H + h) * D + j4, f4);
+    *reinterpret_cast<float4*>(tile + rr * LD + j4) = make_float4(f4[0], f4[1], f4[2], f4[3]);
+  }
+}
+
+// Gain partials of one CTA: each thread's dg (its EPT elements) summed over the feature groups in
+// a fixed order into out[D]. scratch: kThreads / TPR * D floats of shared memory.
+template <int D>
+__device__ __forceinline__ void store_gain_partial(const float (&dg)[FeatureLayout<D>::EPT],
+                                                   float* scratch, float* out) {
+  using FL = FeatureLayout<D>;
+  constexpr int G = kThreads / FL::TPR;
+  const int grp = threadIdx.x / FL::TPR, r = threadIdx.x % FL::TPR;
+#pragma unroll
+  for (int e = 0; e < FL::EPT; ++e) scratch[grp * D + r * FL::EPT + e] = dg[e];
+  __syncthreads();
+  if (threadIdx.x < D) {
+    float s = 0.f;
+    for (int g = 0; g < G; ++g) s += scratch[g * D + threadIdx.x];
+    out[threadIdx.x] = s;
+  }
+}
+
+// P[t][tau] = q'_t . k'_tau (masked to tau <= t) into Ps, and c[t][tau] = g_t . v_tau into As (Gs
+// still holds the raw g). Warps 0-1 take P, warps 2-3 take c. Ends with a barrier.
+template <int D>
+__device__ __forceinline__ void score_tiles(const float* Qf, const float* Kf, const float* Vs,
+                                            const float* Gs, float* Ps, float* As) {
+  constexpr int LD = BwdSmem<D>::LD, LC = BwdSmem<D>::LC;
+  const int tid = threadIdx.x;
+  if (tid < 128) {
+    const bool p = tid < 64;
+    const int task = tid & 63, m0 = 4 * (task / 8), nb = task % 8;
+    float acc[4][4] = {};
+    mt_dot<8>(acc, (p ? Qf : Gs) + m0 * LD, LD, (p ? Kf : Vs) + nb * LD, LD, D);
+    float* out = p ? Ps : As;
+#pragma unroll
+    for (int y = 0; y < 4; ++y)
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int t = m0 + y, tau = nb + 8 * x;
+        out[t * LC + tau] = (!p || tau <= t) ? acc[y][x] : 0.f;
+      }
+  }
+  __syncthreads();
+}
+
+// A[t][tau] = gnum_t . v_tau + scale_t for tau <= t (0 above the diagonal), in the form whose
+// cancelling part is exact (see the file comment), written over c in As; and gnum = g / den over
+// Gs. Needs Ps, As = c, Den, Sst, Nst. Ends with a barrier.
+template <int D>
+__device__ __forceinline__ void build_a(const float* Ps, float* As, float* Gs, const float* Den,
+                                        const float* Sst, const float* Nst, float eps) {
+  constexpr int LD = BwdSmem<D>::LD, LC = BwdSmem<D>::LC;
+  static_assert(kThreads * 4 == kC * kC, "four elements of A per thread");
+  const int tid = threadIdx.x;
+  const int t = tid / 8, tau0 = 4 * (tid % 8);
+  const float den = Den[t];
+  const float inv2 = 1.0f / (den * den);
+  const float sst = Sst[t], nst = Nst[t];
+  float av[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int tau = tau0 + u;
+    float r = 0.f;
+    if (tau <= t) {
+      const float c = As[t * LC + tau];
+      float acc = 0.f;
+      for (int sg = 0; sg <= t; ++sg) acc = fmaf(Ps[t * LC + sg], c - As[t * LC + sg], acc);
+      r = (acc + fmaf(c, sst, -nst) + eps * c) * inv2;
+    }
+    av[u] = r;
+  }
+  for (int idx = tid; idx < kC * D; idx += kThreads) {
+    const int tt = idx / D;
+    Gs[tt * LD + idx % D] = Gs[tt * LD + idx % D] / Den[tt];
+  }
+  __syncthreads();
+  *reinterpret_cast<float4*>(As + t * LC + tau0) = make_float4(av[0], av[1], av[2], av[3]);
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------------------------------------
+// Launch 1: K'^T V and sum k' of every segment that another segment of its document follows.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const BwdArgs b) {
+  using SM = BwdSmem<D>;
+  constexpr int LD = SM::LD, NQ = D / 4;
+  extern __shared__ __align__(16) float sm[];
+  float* St = sm + SM::ST;
+  float* Kf = sm + SM::KF;
+  float* Vs = sm + SM::VS;
+  float* Zs = sm + SM::ZS;
+  const PrefillArgs& a = b.p;
+  const int tid = threadIdx.x;
+  const int seg = blockIdx.x % b.nseg, unit = blockIdx.x / b.nseg;
+  const int h = unit % a.H, doc = unit / a.H;
+  long row0;
+  int n;
+  doc_bounds(a, doc, row0, n);
+  const int s0 = seg * b.seg_len, s1 = min(n, s0 + b.seg_len);
+  if (s1 >= n) return;  // the document's last (or an empty) segment: nobody reads its increment
+  for (int idx = tid; idx < D * D; idx += kThreads) St[(idx / D) * LD + idx % D] = 0.f;
+  if (tid < D) Zs[tid] = 0.f;
+  const T* k = static_cast<const T*>(a.k);
+  const T* v = static_cast<const T*>(a.v);
+  const float* gk = a.gamma_k + h * a.fa.gamma_stride;
+  for (int t0 = s0; t0 < s1; t0 += kC) {
+    __syncthreads();  // the previous chunk's reads of Kf / Vs are done
+    feature_tile<D, T>(k, row0, n, t0, a.H, h, gk, a.pos_offset, a.fa, Kf);
+    raw_tile<D, T>(v, row0, n, t0, a.H, h, Vs);
+    __syncthreads();
+    for (int task = tid; task < NQ * NQ; task += kThreads) {
+      const int i0 = 4 * (task / NQ), j0 = 4 * (task % NQ);
+      float acc[4][4] = {};
+      mt_tn<1>(acc, Kf + i0, LD, Vs + j0, LD, kC);
+#pragma unroll
+      for (int y = 0; y < 4; ++y)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) St[(i0 + y) * LD + j0 + x] += acc[y][x];
+    }
+    if (tid < D) {
+      float s = 0.f;
+      for (int t = 0; t < kC; ++t) s += Kf[t * LD + tid];
+      Zs[tid] += s;
+    }
+  }
+  __syncthreads();
+  float* rec = b.rec_fwd + (static_cast<long>(unit) * b.nseg + seg) * (D * D + D);
+  for (int idx = tid; idx < D * D; idx += kThreads) rec[idx] = St[(idx / D) * LD + idx % D];
+  if (tid < D) rec[D * D + tid] = Zs[tid];
+}
+
+// ------------------------------------------------------------------------------------------------
+// Launch 2: chunks in order. den, scale, gnum; dq' = A K' + S gnum + scale z, then dq; the
+// segment's increment of the suffix state.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 1) bwd_forward_kernel(const BwdArgs b) {
+  using SM = BwdSmem<D>;
+  using FL = FeatureLayout<D>;
+  constexpr int LD = SM::LD, LC = SM::LC, NQ = D / 4;
+  extern __shared__ __align__(16) float sm[];
+  float* St = sm + SM::ST;
+  float* Rt = sm + SM::RT;
+  float* Qf = sm + SM::QF;
+  float* Kf = sm + SM::KF;
+  float* Vs = sm + SM::VS;
+  float* Gs = sm + SM::GS;
+  float* Ps = sm + SM::PS;
+  float* As = sm + SM::AS;
+  float* Zs = sm + SM::ZS;
+  float* Ws = sm + SM::WS;
+  float* Den = sm + SM::DEN;
+  float* Scl = sm + SM::SCL;
+  float* Sst = sm + SM::SST;
+  float* Nst = sm + SM::NST;
+  const PrefillArgs& a = b.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int seg = blockIdx.x % b.nseg, unit = blockIdx.x / b.nseg;
+  const int h = unit % a.H, doc = unit / a.H;
+  long row0;
+  int n;
+  if (!doc_bounds(a, doc, row0, n) && seg == 0 && h == 0 && tid == 0 && a.dev_status != nullptr)
+    atomicOr(a.dev_status, 1u);
+  const int s0 = seg * b.seg_len, s1 = min(n, s0 + b.seg_len);
+  const long rec = static_cast<long>(D) * D + D;
+  const float* rf = b.rec_fwd + static_cast<long>(unit) * b.nseg * rec;
+  // the prefix state at the segment's start: the earlier segments' increments, in order
+  for (int idx = tid; idx < D * D; idx += kThreads) {
+    float s = 0.f;
+    for (int sp = 0; sp < seg && s0 < n; ++sp) s += rf[sp * rec + idx];
+    St[(idx / D) * LD + idx % D] = s;
+    Rt[(idx / D) * LD + idx % D] = 0.f;
+  }
+  if (tid < D) {
+    float s = 0.f;
+    for (int sp = 0; sp < seg && s0 < n; ++sp) s += rf[sp * rec + D * D + tid];
+    Zs[tid] = s;
+    Ws[tid] = 0.f;
+  }
+  const T* q = static_cast<const T*>(a.q);
+  const T* k = static_cast<const T*>(a.k);
+  const T* v = static_cast<const T*>(a.v);
+  const T* g = static_cast<const T*>(b.dout);
+  T* dq = static_cast<T*>(b.dq);
+  const float* gq = a.gamma_q + h * a.fa.gamma_stride;
+  const float* gk = a.gamma_k + h * a.fa.gamma_stride;
+  float dg[FL::EPT] = {};
+  const int grp = lane / FL::TPR, r = lane % FL::TPR;
+  constexpr int kRowsPerPass = (kThreads / 32) * FL::ROWS_PER_WARP;
+
+  for (int t0 = s0; t0 < s1; t0 += kC) {
+    __syncthreads();  // the previous chunk is done with every tile (and the initial state is set)
+    feature_tile<D, T>(q, row0, n, t0, a.H, h, gq, a.pos_offset, a.fa, Qf);
+    feature_tile<D, T>(k, row0, n, t0, a.H, h, gk, a.pos_offset, a.fa, Kf);
+    raw_tile<D, T>(v, row0, n, t0, a.H, h, Vs);
+    raw_tile<D, T>(g, row0, n, t0, a.H, h, Gs);
+    __syncthreads();
+    score_tiles<D>(Qf, Kf, Vs, Gs, Ps, As);
+    // nst_t = g_t . (q'_t S): the state's part of g . num (the numerator itself is never stored)
+    if (tid < 8 * NQ) {
+      const int m0 = 4 * (tid / NQ), n0 = 4 * (tid % NQ);
+      float acc[4][4] = {};
+      mt_outer<1>(acc, Qf + m0 * LD, LD, St + n0, LD, D);
+      float part[4];
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const float4 gg = ld4(Gs + (m0 + y) * LD + n0);
+        part[y] = acc[y][0] * gg.x + acc[y][1] * gg.y + acc[y][2] * gg.z + acc[y][3] * gg.w;
+      }
+#pragma unroll
+      for (int off = NQ / 2; off > 0; off >>= 1)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) part[y] += __shfl_xor_sync(0xffffffffu, part[y], off);
+      if (tid % NQ == 0)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) Nst[m0 + y] = part[y];
+    }
+    __syncthreads();
+    // den_t = q'_t . z + sum_tau P[t][tau] + eps;  scale_t = -(g_t . num_t) / den_t^2
+    if (tid < kC) {
+      const int t = tid;
+      const bool valid = t0 + t < n;
+      float sst = 0.f;
+      for (int i = 0; i < D; ++i) sst = fmaf(Qf[t * LD + i], Zs[i], sst);
+      float ps = 0.f, pc = 0.f;
+      for (int tau = 0; tau < kC; ++tau) {
+        ps += Ps[t * LC + tau];
+        pc = fmaf(Ps[t * LC + tau], As[t * LC + tau], pc);
+      }
+      const float den = valid ? sst + ps + a.eps_den : 1.f;
+      const float scale = valid ? -(Nst[t] + pc) / (den * den) : 0.f;
+      Den[t] = den;
+      Scl[t] = scale;
+      Sst[t] = sst;
+      if (valid) {
+        const long o = (row0 + t0 + t) * a.H + h;
+        b.den[o] = den;
+        b.scl[o] = scale;
+        b.sst[o] = sst;
+        b.nst[o] = Nst[t];
+      }
+    }
+    __syncthreads();
+    build_a<D>(Ps, As, Gs, Den, Sst, Nst, a.eps_den);
+    // dq'[t][i] = sum_tau A[t][tau] k'_tau[i] + sum_j gnum_t[j] S[i][j] + scale_t z[i]  (columns
+    // i = nb + NQ x), kept in registers; the segment's increments R += Q'^T Gnum, w += sum scale q'
+    const bool has_dq = tid < 8 * NQ;
+    const int m0q = 4 * (tid / NQ), nbq = tid % NQ;
+    float dqa[4][4] = {};
+    if (has_dq) {
+      mt_outer<NQ>(dqa, As + m0q * LC, LC, Kf + nbq, LD, kC);
+      mt_dot<NQ>(dqa, Gs + m0q * LD, LD, St + nbq * LD, LD, D);
+#pragma unroll
+      for (int y = 0; y < 4; ++y)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) dqa[y][x] = fmaf(Scl[m0q + y], Zs[nbq + NQ * x], dqa[y][x]);
+    }
+    for (int task = tid; task < NQ * NQ; task += kThreads) {
+      const int i0 = 4 * (task / NQ), j0 = 4 * (task % NQ);
+      float acc[4][4] = {};
+      mt_tn<1>(acc, Qf + i0, LD, Gs + j0, LD, kC);
+#pragma unroll
+      for (int y = 0; y < 4; ++y)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) Rt[(i0 + y) * LD + j0 + x] += acc[y][x];
+    }
+    if (tid < D) {
+      float w = 0.f;
+      for (int t = 0; t < kC; ++t) w = fmaf(Scl[t], Qf[t * LD + tid], w);
+      Ws[tid] += w;
+    }
+    __syncthreads();
+    // dq' over q' (no longer needed); then the prefix state takes this chunk
+    if (has_dq)
+#pragma unroll
+      for (int y = 0; y < 4; ++y)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) Qf[(m0q + y) * LD + nbq + NQ * x] = dqa[y][x];
+    for (int task = tid; task < NQ * NQ; task += kThreads) {
+      const int i0 = 4 * (task / NQ), j0 = 4 * (task % NQ);
+      float acc[4][4] = {};
+      mt_tn<1>(acc, Kf + i0, LD, Vs + j0, LD, kC);
+#pragma unroll
+      for (int y = 0; y < 4; ++y)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) St[(i0 + y) * LD + j0 + x] += acc[y][x];
+    }
+    if (tid < D) {
+      float s = 0.f;
+      for (int t = 0; t < kC; ++t) s += Kf[t * LD + tid];
+      Zs[tid] += s;
+    }
+    __syncthreads();
+    // back through the features of q
+    for (int rr = warp * FL::ROWS_PER_WARP + grp; rr < kC; rr += kRowsPerPass) {
+      const int t = t0 + rr;
+      const bool valid = t < n;
+      const long off = ((row0 + (valid ? t : 0)) * a.H + h) * D;
+      feature_row_bwd<D, T>(q + off, valid, gq, a.pos_offset + t, a.fa, r, Qf + rr * LD, dq + off, dg);
+    }
+  }
+  __syncthreads();
+  if (seg > 0 && s0 < n) {  // the suffix-state increment this segment hands to earlier ones
+    float* rr = b.rec_rev + (static_cast<long>(unit) * b.nseg + seg) * rec;
+    for (int idx = tid; idx < D * D; idx += kThreads) rr[idx] = Rt[(idx / D) * LD + idx % D];
+    if (tid < D) rr[D * D + tid] = Ws[tid];
+  }
+  store_gain_partial<D>(dg, Ps, b.dgp_q + (static_cast<long>(unit) * b.nseg + seg) * D);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Launch 3: chunks in reverse. dv = P^T Gnum + K' R, dk' = A^T Q' + V R^T + w, then dk.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 1) bwd_reverse_kernel(const BwdArgs b) {
+  using SM = BwdSmem<D>;
+  using FL = FeatureLayout<D>;
+  constexpr int LD = SM::LD, LC = SM::LC, NQ = D / 4;
+  extern __shared__ __align__(16) float sm[];
+  float* St = sm + SM::ST;  // R
+  float* Qf = sm + SM::QF;
+  float* Kf = sm + SM::KF;
+  float* Vs = sm + SM::VS;
+  float* Gs = sm + SM::GS;
+  float* Ps = sm + SM::PS;
+  float* As = sm + SM::AS;
+  float* Zs = sm + SM::ZS;  // w
+  float* Den = sm + SM::DEN;
+  float* Scl = sm + SM::SCL;
+  float* Sst = sm + SM::SST;
+  float* Nst = sm + SM::NST;
+  const PrefillArgs& a = b.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int seg = blockIdx.x % b.nseg, unit = blockIdx.x / b.nseg;
+  const int h = unit % a.H, doc = unit / a.H;
+  long row0;
+  int n;
+  doc_bounds(a, doc, row0, n);
+  const int s0 = seg * b.seg_len, s1 = min(n, s0 + b.seg_len);
+  const long rec = static_cast<long>(D) * D + D;
+  const float* rr = b.rec_rev + static_cast<long>(unit) * b.nseg * rec;
+  // the suffix state at the segment's end: the later segments' increments, in segment order
+  for (int idx = tid; idx < D * D; idx += kThreads) {
+    float s = 0.f;
+    for (int sp = seg + 1; sp < b.nseg && sp * b.seg_len < n; ++sp) s += rr[sp * rec + idx];
+    St[(idx / D) * LD + idx % D] = s;
+  }
+  if (tid < D) {
+    float s = 0.f;
+    for (int sp = seg + 1; sp < b.nseg && sp * b.seg_len < n; ++sp) s += rr[sp * rec + D * D + tid];
+    Zs[tid] = s;
+  }
+  const T* q = static_cast<const T*>(a.q);
+  const T* k = static_cast<const T*>(a.k);
+  const T* v = static_cast<const T*>(a.v);
+  const T* g = static_cast<const T*>(b.dout);
+  T* dk = static_cast<T*>(b.dk);
+  T* dv = static_cast<T*>(b.dv);
+  const float* gq = a.gamma_q + h * a.fa.gamma_stride;
+  const float* gk = a.gamma_k + h * a.fa.gamma_stride;
+  float dg[FL::EPT] = {};
+  const int grp = lane / FL::TPR, r = lane % FL::TPR;
+  constexpr int kRowsPerPass = (kThreads / 32) * FL::ROWS_PER_WARP;
+  const int nch = s1 > s0 ? (s1 - s0 + kC - 1) / kC : 0;
+
+  for (int c = nch - 1; c >= 0; --c) {
+    const int t0 = s0 + c * kC;
+    __syncthreads();
+    feature_tile<D, T>(q, row0, n, t0, a.H, h, gq, a.pos_offset, a.fa, Qf);
+    feature_tile<D, T>(k, row0, n, t0, a.H, h, gk, a.pos_offset, a.fa, Kf);
+    raw_tile<D, T>(v, row0, n, t0, a.H, h, Vs);
+    raw_tile<D, T>(g, row0, n, t0, a.H, h, Gs);
+    if (tid < kC) {
+      const bool valid = t0 + tid < n;
+      const long o = (row0 + t0 + tid) * a.H + h;
+      Den[tid] = valid ? b.den[o] : 1.f;
+      Scl[tid] = valid ? b.scl[o] : 0.f;
+      Sst[tid] = valid ? b.sst[o] : 0.f;
+      Nst[tid] = valid ? b.nst[o] : 0.f;
+    }
+    __syncthreads();
+    score_tiles<D>(Qf, Kf, Vs, Gs, Ps, As);
+    build_a<D>(Ps, As, Gs, Den, Sst, Nst, a.eps_den);
+    // rows tau = m0 .. m0+3 of dv (columns n0 .. n0+3) and of dk' (columns nb + NQ x)
+    const bool has = tid < 8 * NQ;
+    const int m0 = 4 * (tid / NQ), nb = tid % NQ;
+    float dka[4][4] = {};
+    if (has) {
+      float acc[4][4] = {};
+      mt_tn<1>(acc, Ps + m0, LC, Gs + 4 * nb, LD, kC);
+      mt_outer<1>(acc, Kf + m0 * LD, LD, St + 4 * nb, LD, D);
+#pragma unroll
+      for (int y = 0; y < 4; ++y)
+        if (t0 + m0 + y < n)
+          store4(dv + ((row0 + t0 + m0 + y) * a.H + h) * D + 4 * nb, acc[y][0], acc[y][1],
+                 acc[y][2], acc[y][3]);
+      mt_tn<NQ>(dka, As + m0, LC, Qf + nb, LD, kC);
+      mt_dot<NQ>(dka, Vs + m0 * LD, LD, St + nb * LD, LD, D);
+#pragma unroll
+      for (int y = 0; y < 4; ++y)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) dka[y][x] += Zs[nb + NQ * x];
+    }
+    __syncthreads();
+    // dk' over k'; then the suffix state takes this chunk
+    if (has)
+#pragma unroll
+      for (int y = 0; y < 4; ++y)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) Kf[(m0 + y) * LD + nb + NQ * x] = dka[y][x];
+    for (int task = tid; task < NQ * NQ; task += kThreads) {
+      const int i0 = 4 * (task / NQ), j0 = 4 * (task % NQ);
+      float acc[4][4] = {};
+      mt_tn<1>(acc, Qf + i0, LD, Gs + j0, LD, kC);
+#pragma unroll
+      for (int y = 0; y < 4; ++y)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) St[(i0 + y) * LD + j0 + x] += acc[y][x];
+    }
+    if (tid < D) {
+      float w = 0.f;
+      for (int t = 0; t < kC; ++t) w = fmaf(Scl[t], Qf[t * LD + tid], w);
+      Zs[tid] += w;
+    }
+    __syncthreads();
+    for (int rw = warp * FL::ROWS_PER_WARP + grp; rw < kC; rw += kRowsPerPass) {
+      const int t = t0 + rw;
+      const bool valid = t < n;
+      const long off = ((row0 + (valid ? t : 0)) * a.H + h) * D;
+      feature_row_bwd<D, T>(k + off, valid, gk, a.pos_offset + t, a.fa, r, Kf + rw * LD, dk + off, dg);
+    }
+  }
+  __syncthreads();
+  store_gain_partial<D>(dg, Ps, b.dgp_k + (static_cast<long>(unit) * b.nseg + seg) * D);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Launch 4: gains. dgamma[h][c] (or dgamma[c] when shared) = the partials of every (document,
+// segment) (and head, when shared), summed in that order. blockIdx.y: 0 = q, 1 = k.
+__global__ void __launch_bounds__(256) bwd_gain_kernel(const BwdArgs b, int D) {
+  const PrefillArgs& a = b.p;
+  const bool per_head = a.fa.gamma_stride != 0;
+  const int n_out = per_head ? a.H * D : D;
+  const int e = blockIdx.x * 256 + threadIdx.x;
+  if (e >= n_out) return;
+  const float* part = blockIdx.y == 0 ? b.dgp_q : b.dgp_k;
+  float* out = blockIdx.y == 0 ? b.dgamma_q : b.dgamma_k;
+  if (out == nullptr) return;
+  const int c = e % D;
+  float s = 0.f;
+  for (int doc = 0; doc < a.n_docs; ++doc)
+    for (int h = per_head ? e / D : 0; h < (per_head ? e / D + 1 : a.H); ++h)
+      for (int seg = 0; seg < b.nseg; ++seg)
+        s += part[((static_cast<long>(doc) * a.H + h) * b.nseg + seg) * D + c];
+  out[e] = s;
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(bytes));
+}
+
+template <typename T, int D>
+cudaError_t launch_t(const BwdArgs& b, cudaStream_t stream) {
+  constexpr size_t smem = BwdSmem<D>::bytes;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static unsigned long long configured = 0;  // bit per device (idempotent; races are benign)
+  if (dev < 64 && !((configured >> dev) & 1ull)) {
+    if ((e = set_smem(bwd_state_kernel<T, D>, smem)) != cudaSuccess) return e;
+    if ((e = set_smem(bwd_forward_kernel<T, D>, smem)) != cudaSuccess) return e;
+    if ((e = set_smem(bwd_reverse_kernel<T, D>, smem)) != cudaSuccess) return e;
+    configured |= 1ull << dev;
+  }
+  const long grid = static_cast<long>(b.p.n_docs) * b.p.H * b.nseg;
+  if (grid == 0) return cudaSuccess;
+  if (b.nseg > 1) {
+    bwd_state_kernel<T, D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(b);
+    note_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  bwd_forward_kernel<T, D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(b);
+  note_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  bwd_reverse_kernel<T, D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(b);
+  note_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (b.dgamma_q != nullptr || b.dgamma_k != nullptr) {
+    const int n_out = b.p.fa.gamma_stride != 0 ? b.p.H * D : D;
+    bwd_gain_kernel<<<dim3(static_cast<unsigned>((n_out + 255) / 256), 2), 256, 0, stream>>>(b, D);
+    note_launches(1);
+  }
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_d(int d, const BwdArgs& b, cudaStream_t stream) {
+  switch (d) {
+    case 16: return launch_t<T, 16>(b, stream);
+    case 32: return launch_t<T, 32>(b, stream);
+    case 64: return launch_t<T, 64>(b, stream);
+    case 128: return launch_t<T, 128>(b, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d) {
+  // One CTA per SM (the kernels take most of the shared memory). A document is cut into nseg
+  // segments of seg_len tokens (a multiple of the chunk); the cost of a plan is its waves of
+  // kSMs CTAs times the chunks of a segment (plus one chunk of set-up per wave).
+  BwdPlan p{};
+  const int chunks_max = max_seqlen > 0 ? (max_seqlen + kC - 1) / kC : 1;
+  const long units = static_cast<long>(n_docs) * H;
+  double best = 1e300;
+  for (int nseg = 1; nseg <= 64 && nseg <= chunks_max; ++nseg) {
+    const int seg_chunks = (chunks_max + nseg - 1) / nseg;
+    const long ctas = units * nseg;
+    const double waves = static_cast<double>((ctas + kSMs - 1) / kSMs);
+    const double cost = waves * (seg_chunks + 1.0);
+    if (cost < 0.95 * best) {
+      best = cost;
+      p.nseg = nseg;
+      p.seg_len = seg_chunks * kC;
+    }
+  }
+  if (p.nseg == 0) {
+    p.nseg = 1;
+    p.seg_len = chunks_max * kC;
+  }
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t rec = static_cast<size_t>(d) * (d + 1) * sizeof(float);
+  const size_t recs = up(static_cast<size_t>(units) * p.nseg * rec);
+  const size_t rows = up(static_cast<size_t>(total_rows) * H * sizeof(float));
+  const size_t gp = up(static_cast<size_t>(units) * p.nseg * d * sizeof(float));
+  p.off_rev = recs;
+  p.off_den = p.off_rev + recs;
+  p.off_scl = p.off_den + rows;
+  p.off_sst = p.off_scl + rows;
+  p.off_nst = p.off_sst + rows;
+  p.off_dgq = p.off_nst + rows;
+  p.off_dgk = p.off_dgq + gp;
+  p.ws_bytes = p.off_dgk + gp;
+  return p;
+}
+
+cudaError_t launch_backward_simt(DType dt, int d, const BwdArgs& b, cudaStream_t stream) {
+  return dt == DType::F32 ? launch_d<float>(d, b, stream) : launch_d<__nv_bfloat16>(d, b, stream);
+}
+
+}  // namespace rapt

@@ -46,6 +46,39 @@ struct PrefillArgs {
 
 cudaError_t launch_prefill_simt(DType dt, int d, const PrefillArgs& a, cudaStream_t stream);
 
+// Backward of the causal forward (CUDA cores, fp32 arithmetic) over a set of documents described
+// by `p` (p.out, S0/z0 and S_final/z_final unused): gradients of sum dout . out. Documents are cut
+// into nseg segments of seg_len tokens; the workspace holds, at the offsets below, the prefix-state
+// increments of the segments (from 0), their suffix-state increments, den and scale of every
+// (token, head), and the per-(document, head, segment) gain partials of q and k.
+struct BwdArgs {
+  PrefillArgs p;
+  const void* dout;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dgamma_q;  // nullable
+  float* dgamma_k;  // nullable
+  float* rec_fwd;
+  float* rec_rev;
+  float* den;  // per (token, head): den_t, scale_t, sst_t, nst_t (see backward_simt.cu)
+  float* scl;
+  float* sst;
+  float* nst;
+  float* dgp_q;
+  float* dgp_k;
+  int nseg;
+  int seg_len;
+};
+struct BwdPlan {
+  int nseg;
+  int seg_len;
+  size_t off_rev, off_den, off_scl, off_sst, off_nst, off_dgq, off_dgk;
+  size_t ws_bytes;
+};
+BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d);
+cudaError_t launch_backward_simt(DType dt, int d, const BwdArgs& b, cudaStream_t stream);
+
 // Tensor-core (tcgen05) chunked prefill for bf16 and d in {64, 128}. Documents are cut into
 // nseg_max segments of seg_len tokens; the state increments of every segment but a document's
 // last are computed first, in blocks of seg_len / blk_per_seg tokens, and ws_bytes of workspace

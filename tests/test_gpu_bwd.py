@@ -1,0 +1,180 @@
+"""GPU parity of the causal RLA-2 backward (rapt_prefill_bwd / rapt_varlen_bwd) against the fp64
+oracle (oracle/rla2_bwd.py), through the C ABI.
+
+Gradients of sum dout . out w.r.t. q, k, v and the RMSNorm gains (08-rapt-algorithm.md §4.2
+"backward"). Tolerance as for the forward: max per-row relative error 1e-4 for fp32 tensors and
+2e-2 for bf16 tensors (fp32 arithmetic). The ReLU's derivative jumps at 0, so a row of dq (dk)
+whose fp64 pre-activation has an element within 1e-5 of the row's largest magnitude is a decision
+the two precisions may take differently; such rows (rare) are left out of the element-wise
+comparison, and the gain gradients, which sum over every row, are compared whole. The shapes cover
+one and many segments per document (segment boundaries inside and at the end of documents),
+ragged last chunks, L = 1, empty and one-token documents, shared and per-head gains, and the full
+size of the dense prefill workload on sampled (batch row, head) pairs.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from gpu_helpers import TOL, draw, gammas, to_dev, to_host, widen
+from relu_linear_attention_gb300 import binding as R
+from relu_linear_attention_gb300 import synthetic as syn
+
+pytestmark = pytest.mark.gpu
+
+EPS_N, BASE, EPS_D = 1e-6, 1e4, 1e-4
+
+
+def _ambiguous(x, gamma, positions):
+    """[n, H] rows whose pre-activation RoPE(RMSNorm(x)) has an element near 0 (relative 1e-5)."""
+    n, H, d = x.shape
+    bad = np.zeros((n, H), dtype=bool)
+    for h in range(H):
+        g = gamma[h] if np.ndim(gamma) == 2 else gamma
+        y = O.rope_adjacent(O.rmsnorm(x[:, h], g, EPS_N), positions, BASE)
+        bad[:, h] = np.min(np.abs(y), axis=1) < 1e-5 * np.max(np.abs(y), axis=1)
+    return bad
+
+
+def _row_err(got, ref, keep):
+    return O.relative_error(got[keep], ref[keep])[0]
+
+
+def _vec_err(got, ref):
+    return float(np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+DENSE_CASES = [
+    # (B, L, H, d, dtype, per_head_gamma, pos_offset)
+    (1, 64, 2, 16, "f32", False, 0),
+    (2, 65, 2, 32, "f32", True, 5),
+    (1, 200, 2, 64, "f32", False, 0),
+    (1, 129, 1, 128, "f32", True, 1000),
+    (2, 63, 2, 16, "bf16", False, 0),
+    (1, 1, 1, 128, "bf16", False, 0),
+    (2, 300, 2, 64, "bf16", True, 0),
+    (1, 1000, 3, 128, "bf16", True, 7),
+    (3, 257, 5, 128, "f32", True, 0),
+]
+
+
+@pytest.mark.parametrize("case", DENSE_CASES, ids=lambda c: "B%dL%dH%dd%d-%s" % c[:5])
+def test_prefill_bwd_matches_oracle(cuda_device, lib, case):
+    B, L, H, d, dtype, per_head, off = case
+    q, k, v = draw(300 + L, (B, L, H, d), dtype)
+    (g,) = draw(301 + L, (B, L, H, d), dtype)[:1]
+    gq, gk = gammas(302, H, d, per_head)
+    dev = lambda x: torch.from_numpy(x).to(cuda_device)
+    dq, dk, dv, dgq, dgk = R.rapt_prefill_bwd(to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype),
+                                              to_dev(g, dtype), dev(gq), dev(gk), pos_offset=off)
+    torch.cuda.synchronize()
+    wq, wk, wv, wg = (widen(x, dtype) for x in (q, k, v, g))
+    rq, rk, rv, rgq, rgk = O.rla2_prefill_bwd(wq, wk, wv, wg, gq, gk, EPS_N, BASE, EPS_D,
+                                              pos_offset=off)
+    pos = off + np.arange(L)
+    for b in range(B):
+        keep_q = ~_ambiguous(wq[b], gq, pos)
+        keep_k = ~_ambiguous(wk[b], gk, pos)
+        assert _row_err(to_host(dq)[b], rq[b], keep_q) <= TOL[dtype]
+        assert _row_err(to_host(dk)[b], rk[b], keep_k) <= TOL[dtype]
+        assert O.relative_error(to_host(dv)[b], rv[b])[0] <= TOL[dtype]
+    assert _vec_err(to_host(dgq), rgq) <= TOL[dtype]
+    assert _vec_err(to_host(dgk), rgk) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [16, 64, 128])
+def test_varlen_bwd_matches_oracle(cuda_device, lib, dtype, d):
+    lens = [1, 0, 65, 130, 3, 0, 64, 257]
+    cu = syn.cu_seqlens_from_lengths(lens)
+    T, H = int(cu[-1]), 2
+    q, k, v = draw(310 + d, (T, H, d), dtype)
+    (g,) = draw(311 + d, (T, H, d), dtype)[:1]
+    gq, gk = gammas(312, H, d, d != 64)
+    dev = lambda x: torch.from_numpy(x).to(cuda_device)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    dq, dk, dv, dgq, dgk = R.rapt_varlen_bwd(to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype),
+                                             to_dev(g, dtype), dev(cu), dev(gq), dev(gk),
+                                             max_seqlen=max(lens), dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    wq, wk, wv, wg = (widen(x, dtype) for x in (q, k, v, g))
+    rq, rk, rv, rgq, rgk = O.rla2_varlen_bwd(wq, wk, wv, wg, cu, gq, gk, EPS_N, BASE, EPS_D)
+    pos = np.concatenate([np.arange(n) for n in lens])
+    keep_q = ~_ambiguous(wq, gq, pos)
+    keep_k = ~_ambiguous(wk, gk, pos)
+    assert _row_err(to_host(dq), rq, keep_q) <= TOL[dtype]
+    assert _row_err(to_host(dk), rk, keep_k) <= TOL[dtype]
+    assert O.relative_error(to_host(dv), rv)[0] <= TOL[dtype]
+    assert _vec_err(to_host(dgq), rgq) <= TOL[dtype]
+    assert _vec_err(to_host(dgk), rgk) <= TOL[dtype]
+
+
+def test_prefill_bwd_full_size_sampled(cuda_device, lib):
+    """The dense prefill workload (B=4, L=4096, H=16, d=128, bf16, per-head gains) in the bench's
+    launch configuration; the oracle checks two whole (batch row, head) pairs. The gains' gradients
+    depend on every pair, so they are checked through the one-head restriction: a second call whose
+    dout is zero outside the sampled head of the sampled row gives, for that head's gain row, the
+    oracle's value of that (row, head) alone."""
+    w = syn.prefill_bf16(seed=1)
+    B, L, H, d = w.q.shape
+    (g,) = draw(320, (B, L, H, d), "bf16")[:1]
+    dev = lambda x: torch.from_numpy(x).to(cuda_device)
+    tq, tk, tv, tg = (to_dev(x, "bf16") for x in (w.q, w.k, w.v, g))
+    dq, dk, dv, _, _ = R.rapt_prefill_bwd(tq, tk, tv, tg, dev(w.gamma_q), dev(w.gamma_k))
+    torch.cuda.synchronize()
+    pos = np.arange(L)
+    for b, h in [(0, 0), (3, 15)]:
+        qs, ks, vs, gs = (syn.bf16_bits_to_f64(x[b:b + 1, :, h:h + 1]) for x in (w.q, w.k, w.v, g))
+        rq, rk, rv, _, _ = O.rla2_prefill_bwd(qs, ks, vs, gs, w.gamma_q[h:h + 1], w.gamma_k[h:h + 1],
+                                              EPS_N, BASE, EPS_D)
+        keep_q = ~_ambiguous(qs[0], w.gamma_q[h:h + 1], pos)
+        keep_k = ~_ambiguous(ks[0], w.gamma_k[h:h + 1], pos)
+        assert _row_err(to_host(dq[b:b + 1, :, h:h + 1])[0], rq[0], keep_q) <= TOL["bf16"]
+        assert _row_err(to_host(dk[b:b + 1, :, h:h + 1])[0], rk[0], keep_k) <= TOL["bf16"]
+        assert O.relative_error(to_host(dv[b:b + 1, :, h:h + 1])[0], rv[0])[0] <= TOL["bf16"]
+    # gains through one (row, head): dout zero elsewhere
+    b, h = 2, 9
+    g1 = torch.zeros_like(tg)
+    g1[b, :, h] = tg[b, :, h]
+    _, _, _, dgq, dgk = R.rapt_prefill_bwd(tq, tk, tv, g1, dev(w.gamma_q), dev(w.gamma_k))
+    torch.cuda.synchronize()
+    qs, ks, vs, gs = (syn.bf16_bits_to_f64(x[b:b + 1, :, h:h + 1]) for x in (w.q, w.k, w.v, g))
+    _, _, _, rgq, rgk = O.rla2_prefill_bwd(qs, ks, vs, gs, w.gamma_q[h:h + 1], w.gamma_k[h:h + 1],
+                                           EPS_N, BASE, EPS_D)
+    assert _vec_err(to_host(dgq)[h], rgq[0]) <= TOL["bf16"]
+    assert _vec_err(to_host(dgk)[h], rgk[0]) <= TOL["bf16"]
+    others = np.delete(to_host(dgq), h, axis=0)
+    assert np.all(others == 0.0)
+
+
+def test_prefill_bwd_repeats_bitwise(cuda_device, lib):
+    q, k, v = draw(330, (2, 700, 3, 64), "bf16")
+    (g,) = draw(331, (2, 700, 3, 64), "bf16")[:1]
+    gq, gk = gammas(332, 3, 64, True)
+    dev = lambda x: torch.from_numpy(x).to(cuda_device)
+    args = [to_dev(x, "bf16") for x in (q, k, v, g)] + [dev(gq), dev(gk)]
+    first = R.rapt_prefill_bwd(*args)
+    for _ in range(3):
+        again = R.rapt_prefill_bwd(*args)
+        for a, b in zip(first, again):
+            assert torch.equal(a, b)
+
+
+def test_prefill_bwd_without_gains_and_empty(cuda_device, lib):
+    q, k, v = draw(340, (1, 40, 2, 32), "f32")
+    (g,) = draw(341, (1, 40, 2, 32), "f32")[:1]
+    gq, gk = gammas(342, 2, 32, False)
+    dev = lambda x: torch.from_numpy(x).to(cuda_device)
+    dq, dk, dv, dgq, dgk = R.rapt_prefill_bwd(to_dev(q, "f32"), to_dev(k, "f32"), to_dev(v, "f32"),
+                                              to_dev(g, "f32"), dev(gq), dev(gk), need_gains=False)
+    torch.cuda.synchronize()
+    assert dgq is None and dgk is None
+    rq, rk, rv, _, _ = O.rla2_prefill_bwd(q, k, v, g, gq, gk, EPS_N, BASE, EPS_D)
+    assert O.relative_error(to_host(dv), rv)[0] <= TOL["f32"]
+    # L = 0: nothing to differentiate, the gain gradients are zero
+    z = torch.zeros((2, 0, 2, 32), device=cuda_device)
+    _, _, _, dgq, dgk = R.rapt_prefill_bwd(z, z, z, z, dev(gq), dev(gk))
+    torch.cuda.synchronize()
+    assert torch.all(dgq == 0) and torch.all(dgk == 0)
