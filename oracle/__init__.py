@@ -34,6 +34,9 @@ L = 1 and constant-v closed forms, linearity in v, the L2 identity
 sum(s^2) = q'^T (K'^T K') q', varlen == per-document dense runs, decode ==
 last prefill row, bidirectional == causal on the last row and invariant under
 any reordering of the keys, and an independent pure-Python brute force on L <= 16.
+The causal L2 form (rla_l2_causal*) is pinned by brute force, the recurrence
+with the A = sum k'k'^T state, the last row = the non-causal L2 row, homogeneity
+of degree 0 in q' (up to eps), the v == 1 bound sqrt(t+1) and per-document runs.
 The backward (rla2_bwd.py, gradients of sum dout . out) is pinned by central
 finite differences of the forward oracle and of the brute force, Euler's
 identity in v, the RMSNorm scale identity, the RoPE adjoint, shared gains =
@@ -59,6 +62,10 @@ from .rla2 import (  # noqa: F401
     rla2_bidir,
     rla2_bidir_varlen,
     rla_l2,
+    rla_l2_causal_doc,
+    rla_l2_causal_recurrent_doc,
+    rla_l2_causal,
+    rla_l2_causal_varlen,
     relative_error,
 )
 from .rla2_bwd import (  # noqa: F401

@@ -349,3 +349,75 @@ def relative_error(y, r, zero_tol=1e-6):
         rel = np.where(small, np.where(yn <= zero_tol, 0.0, np.inf), ry / np.where(small, 1, rn))
     glob = float(np.abs(y - r).max() / max(np.abs(r).max(), 1e-300)) if r.size else 0.0
     return (float(rel.max()) if rel.size else 0.0), glob
+
+
+def rla_l2_causal_doc(qf, kf, v, eps=1e-6, rows=None):
+    """Causal original RLA (L2 denominator) of one head of one document, quadratic form.
+
+    out_t = sum_{i<=t} s_ti v_i / (sqrt(sum_{i<=t} s_ti^2) + eps), s_ti = q'_t . k'_i: the §2.1
+    closed form with the sums restricted to the causal prefix of the document (§2.2: a new query
+    reads the accumulated state, which restarts only at document boundaries; §4.1: the prefix scan
+    keeps A_t = sum_{i<=t} k'_i k'_i^T, whose quadratic form q'^T A_t q' is the denominator's sum of
+    squares). qf, kf, v: [n, d]; ``rows``: optional query indices (default all).
+    """
+    qf, kf, v = _f64(qf), _f64(kf), _f64(v)
+    n = qf.shape[0]
+    rows = np.arange(n) if rows is None else np.asarray(rows, dtype=np.int64)
+    out = np.zeros((len(rows), v.shape[1]), dtype=np.float64)
+    for r0 in range(0, len(rows), _ROW_BLOCK):
+        rr = rows[r0:r0 + _ROW_BLOCK]
+        hi = int(rr.max()) + 1 if len(rr) else 0
+        s = qf[rr] @ kf[:hi].T
+        s = np.where(np.arange(hi)[None, :] <= rr[:, None], s, 0.0)
+        out[r0:r0 + len(rr)] = (s @ v[:hi]) / (np.sqrt((s * s).sum(axis=1)) + float(eps))[:, None]
+    return out
+
+
+def rla_l2_causal_recurrent_doc(qf, kf, v, eps=1e-6):
+    """The same in recurrence form (self-check only): S_t = S_{t-1} + k'_t v_t^T,
+    A_t = A_{t-1} + k'_t k'_t^T, out_t = q'_t S_t / (sqrt(q'_t^T A_t q'_t) + eps)
+    (08-rapt-algorithm.md §4.1, the A and B prefix states of the scan)."""
+    qf, kf, v = _f64(qf), _f64(kf), _f64(v)
+    n, d = qf.shape
+    S = np.zeros((d, v.shape[1]))
+    A = np.zeros((d, d))
+    out = np.zeros((n, v.shape[1]))
+    for t in range(n):
+        S += np.outer(kf[t], v[t])
+        A += np.outer(kf[t], kf[t])
+        out[t] = (qf[t] @ S) / (np.sqrt(qf[t] @ A @ qf[t]) + float(eps))
+    return out
+
+
+def rla_l2_causal(q, k, v, eps=1e-6, pairs=None, rows=None):
+    """Dense causal original RLA: q, k, v [B, L, H, d], one document per batch row; features
+    ReLU(q), ReLU(k) with no norm and no RoPE (§2.1's global view Q' = ReLU(Q W_q)). ``pairs`` /
+    ``rows`` restrict the evaluation; other entries are NaN."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, L, H, d = q.shape
+    out = np.full(q.shape[:3] + (v.shape[3],), np.nan)
+    if pairs is None:
+        pairs = [(b, h) for b in range(B) for h in range(H)]
+    rr = np.arange(L) if rows is None else np.asarray(rows)
+    for b, h in pairs:
+        out[b, rr, h] = rla_l2_causal_doc(relu(q[b, :, h]), relu(k[b, :, h]), v[b, :, h], eps,
+                                          rows=rr)
+    return out
+
+
+def rla_l2_causal_varlen(q, k, v, cu_seqlens, eps=1e-6, docs=None, heads=None):
+    """Packed varlen causal original RLA: q, k, v [T, H, d]; document n spans tokens
+    cu_seqlens[n] .. cu_seqlens[n+1]-1 and sees only itself (§2.2). Returns out [T, H, d]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    T, H, d = q.shape
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    out = np.full(q.shape[:2] + (v.shape[2],), np.nan)
+    docs = range(len(cu) - 1) if docs is None else docs
+    heads = range(H) if heads is None else heads
+    for n in docs:
+        a, b = int(cu[n]), int(cu[n + 1])
+        if b == a:
+            continue
+        for h in heads:
+            out[a:b, h] = rla_l2_causal_doc(relu(q[a:b, h]), relu(k[a:b, h]), v[a:b, h], eps)
+    return out

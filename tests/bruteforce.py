@@ -88,3 +88,20 @@ def bidir_head(qf, kf, v, eps_den):
             den += s
         out.append([num[j] / (den + eps_den) for j in range(dv)])
     return out
+
+
+def l2_causal_head(qf, kf, v, eps):
+    """Causal L2 denominator: query t sees keys 0..t; out = sum s v / (sqrt(sum s^2) + eps)."""
+    n = len(qf)
+    dv = len(v[0]) if n else 0
+    out = []
+    for t in range(n):
+        num = [0.0] * dv
+        ss = 0.0
+        for i in range(t + 1):
+            s = dot(qf[t], kf[i])
+            ss += s * s
+            for j in range(dv):
+                num[j] += s * float(v[i][j])
+        out.append([num[j] / (math.sqrt(ss) + eps) for j in range(dv)])
+    return out
