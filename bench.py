@@ -432,6 +432,32 @@ def run_gpu(args, rank, world, local):
                            "kernels": "l2_tc_moments + l2_tc_reduce + l2_tc_readout (one call)"}}
     del lq, lk, lv, lo, ws
 
+    # ---------------- causal original RLA (L2 denominator) on the L2 workload's shapes
+    wl = syn.l2_bf16(seed=rank_seed(4, rank))
+    lq, lk, lv = (_bf(x, device) for x in (wl.q, wl.k, wl.v))
+    lo = torch.empty_like(lq)
+    ws = torch.empty(max(1, lib.rla_l2_causal_workspace_size(2, 16384, 16, 128, 1)),
+                     dtype=torch.uint8, device=device)
+    c_ms, c_launch = time_steps(lambda: R.rla_l2_causal_fwd(lq, lk, lv, eps=1e-6, out=lo, workspace=ws),
+                                max(3, args.steps // 4), args.warmup, flush,
+                                counter=lib.rapt_launch_counter)
+    c_mean = max_over_ranks(statistics.fmean(c_ms), device)
+    c_flops = 2 * 16384 * 16 * (8 * 128 * 128 + 2 * 128)  # q'S, q'A q', S and A updates
+    fp32_peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    l2_causal = {"value": world * 2 * 16384 / (c_mean * 1e-3), "unit": "tokens/s",
+                 "ms_per_step": c_mean,
+                 "workload": "rla_l2_causal B=2 L=16384 H=16 d=128 bf16 (causal L2 denominator)",
+                 "launches_per_call": c_launch / max(3, args.steps // 4),
+                 "roofline": {"bound": "alu", "achieved": c_flops / (c_mean * 1e-3) / 1e12,
+                              "peak": fp32_peak, "unit": "TFLOP/s",
+                              "frac": c_flops / (c_mean * 1e-3) / 1e12 / fp32_peak,
+                              "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x max SM clock",
+                              "algorithmic_flops_per_call": c_flops,
+                              "hbm_frac": prefill_bytes(2, 16384, 16, 128) / (c_mean * 1e-3) / 1e9
+                              / peaks["hbm_gbs"],
+                              "kernels": "l2c_state_kernel + l2c_kernel (one call)"}}
+    del lq, lk, lv, lo, ws, wl
+
     # ---------------- bidirectional RLA-2 on the headline's inputs (B=4, L=4096, H=16, d=128)
     bws = torch.empty(lib.rapt_bidir_workspace_size(B, L, H, d, 1), dtype=torch.uint8, device=device)
     b_ms, b_launch = time_steps(lambda: R.rapt_bidir_fwd(q, k, v, gq, gk, out=out, workspace=bws),
@@ -460,7 +486,6 @@ def run_gpu(args, rank, world, local):
         max(3, args.steps // 4), args.warmup, flush, counter=lib.rapt_launch_counter)
     g_mean = max_over_ranks(statistics.fmean(g_ms), device)
     g_flops = B * L * H * (12 * d * d)  # recurrence-form backward: q'S, S g, R v, R^T k', S and R updates
-    fp32_peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
     backward = {"value": world * B * L / (g_mean * 1e-3), "unit": "tokens/s", "ms_per_step": g_mean,
                 "workload": "rla2_causal_prefill backward B=4 L=4096 H=16 d=128 bf16 (dq, dk, dv, "
                             "dgamma_q, dgamma_k), the headline's inputs",
@@ -507,7 +532,7 @@ def run_gpu(args, rank, world, local):
         "gpu_launches": int(timed_launches),
         "clocks": clk,
         "decode": decode, "varlen": varlen, "rla_l2": rla_l2, "bidir": bidir,
-        "backward": backward,
+        "backward": backward, "l2_causal": l2_causal,
         "cpu_baseline": cpu,
     }
     if rank == 0:

@@ -191,6 +191,32 @@ rapt_status rapt_varlen_bwd(const void* q, const void* k, const void* v, const v
                             rapt_stream_t stream);
 
 /*
+ * Causal original RLA with the L2 denominator (08-rapt-algorithm.md §2.1 closed form, eps outside
+ * the root; §2.2 a query reads the accumulated causal state, which restarts at document
+ * boundaries; §4.1 the prefix scan's A_t = sum k'k'^T state):
+ *   q' = ReLU(q), k' = ReLU(k) (no norm, no RoPE),
+ *   out_t = sum_{i<=t} s_ti v_i / (sqrt(sum_{i<=t} s_ti^2) + eps) = q'_t S_t / (sqrt(q'_t^T A_t q'_t) + eps).
+ *   Dense:  q, k, v, out [B, L, H, d]; one document per batch row.
+ *   Varlen: q, k, v, out [T, H, d]; cu_seqlens, N, max_seqlen and dev_status as for rapt_varlen_fwd.
+ *   eps       finite, > 0 (1e-6 on the page).
+ *   workspace at least the matching *_workspace_size() bytes, 16-byte aligned (the states K'^T V and
+ *             K'^T K' of the segments the documents are cut into; may be NULL when that size is 0).
+ * All arithmetic is fp32 on CUDA cores for every dtype and d; bf16 outputs are rounded to nearest
+ * even. Results are bitwise repeatable (fixed summation order).
+ */
+size_t rla_l2_causal_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype);
+rapt_status rla_l2_causal_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
+                              int32_t B, int32_t L, int32_t H, int32_t d, float eps, void* out,
+                              void* workspace, size_t workspace_bytes, rapt_stream_t stream);
+size_t rla_l2_causal_varlen_workspace_size(int32_t T, int32_t N, int32_t H, int32_t d,
+                                           int32_t max_seqlen, rapt_dtype dtype);
+rapt_status rla_l2_causal_varlen_fwd(const void* q, const void* k, const void* v,
+                                     rapt_dtype dtype, int32_t T, int32_t H, int32_t d,
+                                     const int32_t* cu_seqlens, int32_t N, int32_t max_seqlen,
+                                     float eps, void* out, uint32_t* dev_status, void* workspace,
+                                     size_t workspace_bytes, rapt_stream_t stream);
+
+/*
  * Bidirectional (non-causal) RLA-2 (08-rapt-algorithm.md §4.1: in its causal=false mode the prefix
  * scan sums over the whole set; §4.2: the layer's bidirectional branch; formula and eps of §3).
  * Features as in the causal form; for each (document, head), S = sum_tau k'_tau v_tau^T and

@@ -63,6 +63,15 @@ SIGNATURES = {
                                   c_void_p, c_void_p, rapt_params,
                                   c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                   c_void_p, c_void_p, c_size_t, c_void_p]),
+    "rla_l2_causal_workspace_size": (c_size_t, [c_int32] * 4 + [c_int32]),
+    "rla_l2_causal_fwd": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32,
+                                    c_int32, c_int32, c_int32, c_int32, c_float, c_void_p,
+                                    c_void_p, c_size_t, c_void_p]),
+    "rla_l2_causal_varlen_workspace_size": (c_size_t, [c_int32] * 5 + [c_int32]),
+    "rla_l2_causal_varlen_fwd": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32,
+                                           c_int32, c_int32, c_int32, c_void_p, c_int32, c_int32,
+                                           c_float, c_void_p, c_void_p, c_void_p, c_size_t,
+                                           c_void_p]),
     "rapt_bidir_workspace_size": (c_size_t, [c_int32] * 4 + [c_int32]),
     "rapt_bidir_fwd": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32,
                                  c_int32, c_int32, c_int32, c_int32,

@@ -216,6 +216,56 @@ def rapt_varlen_bwd(q, k, v, dout, cu_seqlens, gamma_q, gamma_k, *, max_seqlen, 
     return dq, dk, dv, dgamma_q, dgamma_k
 
 
+def rla_l2_causal_fwd(q, k, v, *, eps=1e-6, out=None, workspace=None, stream=None):
+    """Causal original RLA (L2 denominator): q, k, v [B, L, H, d] (fp32 or bf16). Returns out."""
+    _need(q.dim() == 4, "q must be [B, L, H, d]")
+    B, L, H, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _cuda_contig(name, t, q.dtype, q.shape)
+    _need(q.dtype in _DT, "dtype must be float32 or bfloat16")
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, q.dtype, q.shape)
+    lib = _lib.load()
+    need = lib.rla_l2_causal_workspace_size(B, L, H, d, _DT[q.dtype])
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.rla_l2_causal_fwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], B, L, H, d, float(eps),
+                               _ptr(out), _ptr(workspace), ws_bytes, _stream(stream))
+    _lib.check("rla_l2_causal_fwd", st)
+    return out
+
+
+def rla_l2_causal_varlen_fwd(q, k, v, cu_seqlens, *, max_seqlen, eps=1e-6, out=None,
+                             dev_status=None, workspace=None, stream=None):
+    """Packed varlen causal original RLA: q, k, v [T, H, d]; cu_seqlens int32 [N + 1] on the
+    device. Returns out."""
+    _need(q.dim() == 3, "q must be [T, H, d]")
+    T, H, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _cuda_contig(name, t, q.dtype, q.shape)
+    _need(q.dtype in _DT, "dtype must be float32 or bfloat16")
+    _cuda_contig("cu_seqlens", cu_seqlens, torch.int32)
+    _need(cu_seqlens.dim() == 1 and cu_seqlens.numel() >= 2, "cu_seqlens must be [N + 1]")
+    N = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, q.dtype, q.shape)
+    if dev_status is not None:
+        _cuda_contig("dev_status", dev_status, torch.int32)
+    lib = _lib.load()
+    need = lib.rla_l2_causal_varlen_workspace_size(T, N, H, d, int(max_seqlen), _DT[q.dtype])
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.rla_l2_causal_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], T, H, d,
+                                      _ptr(cu_seqlens), N, int(max_seqlen), float(eps), _ptr(out),
+                                      _ptr(dev_status), _ptr(workspace), ws_bytes, _stream(stream))
+    _lib.check("rla_l2_causal_varlen_fwd", st)
+    return out
+
+
 def rapt_bidir_fwd(q, k, v, gamma_q, gamma_k, *, eps_norm=1e-6, rope_base=1e4, eps_den=1e-4,
                    pos_offset=0, out=None, dev_status=None, workspace=None, stream=None):
     """Dense bidirectional (non-causal) RLA-2; q, k, v [B, L, H, d] (fp32 or bf16). Returns out."""

@@ -383,6 +383,79 @@ rapt_status rapt_varlen_bwd(const void* q, const void* k, const void* v, const v
                          rapt_varlen_bwd_workspace_size(T, N, H, d, max_seqlen, dtype), stream);
 }
 
+namespace {
+
+rapt_status l2_causal_common(const void* q, const void* k, const void* v, rapt_dtype dtype,
+                             int n_docs, int doc_len, long total_rows, int H, int d,
+                             const int32_t* cu_seqlens, int max_seqlen, float eps, void* out,
+                             uint32_t* dev_status, void* workspace, size_t workspace_bytes,
+                             size_t need, rapt_stream_t stream) {
+  if (!std::isfinite(eps) || eps <= 0.f) return RAPT_ERR_INVALID_ARG;
+  if (total_rows > 0 && (q == nullptr || k == nullptr || v == nullptr || out == nullptr))
+    return RAPT_ERR_INVALID_ARG;
+  if (!opt_aligned16(q) || !opt_aligned16(k) || !opt_aligned16(v) || !opt_aligned16(out))
+    return RAPT_ERR_INVALID_ARG;
+  if (out != nullptr && (out == q || out == k || out == v)) return RAPT_ERR_INVALID_ARG;
+  if (dev_status != nullptr && !aligned4(dev_status)) return RAPT_ERR_INVALID_ARG;
+  if (workspace_bytes < need || (need > 0 && (workspace == nullptr || !aligned16(workspace))))
+    return RAPT_ERR_WORKSPACE;
+  if (total_rows == 0) return RAPT_OK;
+  const rapt::L2cPlan plan = rapt::l2c_plan(n_docs, H, max_seqlen, d);
+  rapt::L2cArgs b{};
+  rapt::PrefillArgs& a = b.p;
+  a.q = q; a.k = k; a.v = v; a.out = out;
+  a.cu_seqlens = cu_seqlens; a.dev_status = dev_status;
+  a.n_docs = n_docs; a.doc_len = doc_len; a.total_rows = static_cast<int>(total_rows);
+  a.max_seqlen = max_seqlen; a.H = H;
+  b.eps = eps;
+  b.rec = static_cast<float*>(workspace);
+  b.nseg = plan.nseg;
+  b.seg_len = plan.seg_len;
+  return from_cuda(rapt::launch_l2_causal_simt(to_dt(dtype), d, b,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+size_t rla_l2_causal_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype) {
+  if (!known_dtype(dtype) || !supported_d(d) || B < 1 || H < 1 || L < 1) return 0;
+  return rapt::l2c_plan(B, H, L, d).ws_bytes;
+}
+
+rapt_status rla_l2_causal_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
+                              int32_t B, int32_t L, int32_t H, int32_t d, float eps, void* out,
+                              void* workspace, size_t workspace_bytes, rapt_stream_t stream) {
+  if (!known_dtype(dtype) || !supported_d(d)) return RAPT_ERR_UNSUPPORTED;
+  if (B < 1 || H < 1 || L < 0) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(B) * L * H * d)) return RAPT_ERR_INVALID_ARG;
+  return l2_causal_common(q, k, v, dtype, B, L, static_cast<long>(B) * L, H, d, nullptr, L, eps,
+                          out, nullptr, workspace, workspace_bytes,
+                          rla_l2_causal_workspace_size(B, L, H, d, dtype), stream);
+}
+
+size_t rla_l2_causal_varlen_workspace_size(int32_t T, int32_t N, int32_t H, int32_t d,
+                                           int32_t max_seqlen, rapt_dtype dtype) {
+  if (!known_dtype(dtype) || !supported_d(d) || N < 1 || H < 1 || max_seqlen < 0 || T < 1)
+    return 0;
+  return rapt::l2c_plan(N, H, max_seqlen, d).ws_bytes;
+}
+
+rapt_status rla_l2_causal_varlen_fwd(const void* q, const void* k, const void* v,
+                                     rapt_dtype dtype, int32_t T, int32_t H, int32_t d,
+                                     const int32_t* cu_seqlens, int32_t N, int32_t max_seqlen,
+                                     float eps, void* out, uint32_t* dev_status, void* workspace,
+                                     size_t workspace_bytes, rapt_stream_t stream) {
+  if (!known_dtype(dtype) || !supported_d(d)) return RAPT_ERR_UNSUPPORTED;
+  if (T < 0 || N < 1 || H < 1 || max_seqlen < 0) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(T) * H * d)) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(N) * H * 4)) return RAPT_ERR_INVALID_ARG;
+  if (cu_seqlens == nullptr || !aligned4(cu_seqlens)) return RAPT_ERR_INVALID_ARG;
+  return l2_causal_common(q, k, v, dtype, N, 0, T, H, d, cu_seqlens, max_seqlen, eps, out,
+                          dev_status, workspace, workspace_bytes,
+                          rla_l2_causal_varlen_workspace_size(T, N, H, d, max_seqlen, dtype),
+                          stream);
+}
+
 rapt_status rapt_decode_step(const void* q, const void* k, const void* v, rapt_dtype dtype,
                              int32_t N, int32_t H, int32_t d, const int32_t* positions,
                              const float* gamma_q, const float* gamma_k, rapt_params params,

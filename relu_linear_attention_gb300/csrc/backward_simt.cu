@@ -32,12 +32,14 @@
 //   4. bwd_gain_kernel: the gain partials summed in a fixed order.
 // No float atomics anywhere: every sum has a fixed order, so results are bitwise repeatable.
 #include "kernels.h"
+#include "simt_tiles.cuh"
 #include "tc_features.cuh"
 
 namespace rapt {
 namespace {
 
 using feat::doc_bounds;
+using namespace simt;
 
 constexpr int kC = 32;  // chunk length (tokens)
 constexpr int kThreads = 256;
@@ -68,81 +70,6 @@ struct BwdSmem {
   static_assert(bytes <= 232448, "shared memory budget");
   static_assert(PS + (kThreads / FeatureLayout<D>::TPR) * D <= ZS, "gain partials fit in PS + AS");
 };
-
-__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-
-// 4 x 4 micro-tiles of small shared-memory GEMMs; K is a multiple of 4. The tile's rows m are
-// A's rows (or columns) m0 .. m0+3, always contiguous; its columns are n0 + NS * x (x = 0..3): NS = 1
-// gives four contiguous columns (float4 loads of B), a larger NS spreads them so that neighbouring
-// lanes, which take neighbouring n0, touch neighbouring rows or columns of B (no bank conflicts).
-// acc[y][x] += sum_k A[y*lda + k] * B[(NS*x)*ldb + k]       (B contiguous along k)
-template <int NS>
-__device__ __forceinline__ void mt_dot(float (&acc)[4][4], const float* A, int lda, const float* B,
-                                       int ldb, int K) {
-  for (int k = 0; k < K; k += 4) {
-    float4 a[4], b[4];
-#pragma unroll
-    for (int y = 0; y < 4; ++y) a[y] = ld4(A + y * lda + k);
-#pragma unroll
-    for (int x = 0; x < 4; ++x) b[x] = ld4(B + NS * x * ldb + k);
-#pragma unroll
-    for (int y = 0; y < 4; ++y)
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        acc[y][x] = fmaf(a[y].x, b[x].x, acc[y][x]);
-        acc[y][x] = fmaf(a[y].y, b[x].y, acc[y][x]);
-        acc[y][x] = fmaf(a[y].z, b[x].z, acc[y][x]);
-        acc[y][x] = fmaf(a[y].w, b[x].w, acc[y][x]);
-      }
-  }
-}
-// B element (k, x) of the column forms below.
-template <int NS>
-__device__ __forceinline__ void ld_brow(const float* B, float (&b)[4]) {
-  if constexpr (NS == 1) {
-    const float4 t = ld4(B);
-    b[0] = t.x; b[1] = t.y; b[2] = t.z; b[3] = t.w;
-  } else {
-#pragma unroll
-    for (int x = 0; x < 4; ++x) b[x] = B[NS * x];
-  }
-}
-// acc[y][x] += sum_k A[y*lda + k] * B[k*ldb + NS*x]         (A along k, B along n)
-template <int NS>
-__device__ __forceinline__ void mt_outer(float (&acc)[4][4], const float* A, int lda,
-                                         const float* B, int ldb, int K) {
-  for (int k = 0; k < K; k += 4) {
-    float4 a[4];
-    float b[4][4];
-#pragma unroll
-    for (int y = 0; y < 4; ++y) a[y] = ld4(A + y * lda + k);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) ld_brow<NS>(B + (k + u) * ldb, b[u]);
-#pragma unroll
-    for (int y = 0; y < 4; ++y) {
-      const float av[4] = {a[y].x, a[y].y, a[y].z, a[y].w};
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int x = 0; x < 4; ++x) acc[y][x] = fmaf(av[u], b[u][x], acc[y][x]);
-    }
-  }
-}
-// acc[y][x] += sum_k A[k*lda + y] * B[k*ldb + NS*x]         (A along m, B along n)
-template <int NS>
-__device__ __forceinline__ void mt_tn(float (&acc)[4][4], const float* A, int lda, const float* B,
-                                      int ldb, int K) {
-  for (int k = 0; k < K; ++k) {
-    const float4 a = ld4(A + k * lda);
-    float b[4];
-    ld_brow<NS>(B + k * ldb, b);
-    const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-    for (int y = 0; y < 4; ++y)
-#pragma unroll
-      for (int x = 0; x < 4; ++x) acc[y][x] = fmaf(av[y], b[x], acc[y][x]);
-  }
-}
 
 template <typename T>
 __device__ __forceinline__ void store2(T* p, float a, float b);

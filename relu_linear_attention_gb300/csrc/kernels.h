@@ -79,6 +79,24 @@ struct BwdPlan {
 BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d);
 cudaError_t launch_backward_simt(DType dt, int d, const BwdArgs& b, cudaStream_t stream);
 
+// Causal original RLA (L2 denominator) on CUDA cores over the documents of `p` (features ReLU(q),
+// ReLU(k); gammas, RoPE, states and eps_den unused). rec: the workspace, 2 d^2 floats (K'^T V, then
+// K'^T K') per (document, head, segment).
+struct L2cArgs {
+  PrefillArgs p;
+  float eps;
+  float* rec;
+  int nseg;
+  int seg_len;
+};
+struct L2cPlan {
+  int nseg;
+  int seg_len;
+  size_t ws_bytes;
+};
+L2cPlan l2c_plan(int n_docs, int H, int max_seqlen, int d);
+cudaError_t launch_l2_causal_simt(DType dt, int d, const L2cArgs& b, cudaStream_t stream);
+
 // Tensor-core (tcgen05) chunked prefill for bf16 and d in {64, 128}. Documents are cut into
 // nseg_max segments of seg_len tokens; the state increments of every segment but a document's
 // last are computed first, in blocks of seg_len / blk_per_seg tokens, and ws_bytes of workspace
