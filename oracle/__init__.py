@@ -37,6 +37,10 @@ any reordering of the keys, and an independent pure-Python brute force on L <= 1
 The causal L2 form (rla_l2_causal*) is pinned by brute force, the recurrence
 with the A = sum k'k'^T state, the last row = the non-causal L2 row, homogeneity
 of degree 0 in q' (up to eps), the v == 1 bound sqrt(t+1) and per-document runs.
+The layer (rapt_layer: projections, attention, output projection) is pinned by
+its special cases: identity projections give the attention itself, zero W_v or
+W_q give exact zeros (which fixes the q | k | v row order), and a permutation
+W_o permutes the output columns.
 The backward (rla2_bwd.py, gradients of sum dout . out) is pinned by central
 finite differences of the forward oracle and of the brute force, Euler's
 identity in v, the RMSNorm scale identity, the RoPE adjoint, shared gains =
@@ -66,6 +70,8 @@ from .rla2 import (  # noqa: F401
     rla_l2_causal_recurrent_doc,
     rla_l2_causal,
     rla_l2_causal_varlen,
+    linear,
+    rapt_layer,
     relative_error,
 )
 from .rla2_bwd import (  # noqa: F401

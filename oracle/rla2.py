@@ -421,3 +421,36 @@ def rla_l2_causal_varlen(q, k, v, cu_seqlens, eps=1e-6, docs=None, heads=None):
         for h in heads:
             out[a:b, h] = rla_l2_causal_doc(relu(q[a:b, h]), relu(k[a:b, h]), v[a:b, h], eps)
     return out
+
+
+def linear(x, w):
+    """y = x W^T (a linear map with weight W [N, K]; the layer's projections, 08-rapt-algorithm.md
+    §3 q = W_q x and §4.2 the output projection w_o). A library matmul in fp64."""
+    return _f64(x) @ _f64(w).T
+
+
+def rapt_layer(x, w_qkv, w_o, gamma_q, gamma_k, H, eps_norm=1e-6, rope_base=1e4, eps_den=1e-4,
+               pos_offset=0, pairs_rows=None):
+    """One RAPT attention layer (08-rapt-algorithm.md §3 core formula with the projections, §4.2
+    forward: projections, RMSNorm -> RoPE -> ReLU, the causal scan, the division, w_o).
+
+    x [B, L, d_model]; w_qkv [3 H d, d_model] (rows: W_q, then W_k, then W_v, each head-major
+    h d + j); w_o [d_model, H d]. Returns y [B, L, d_model]. ``pairs_rows``: optional (b, rows) to
+    evaluate only those rows of batch row b (other entries NaN).
+    """
+    x = _f64(x)
+    B, L, dm = x.shape
+    d = _f64(w_qkv).shape[0] // (3 * H)
+    bs = range(B) if pairs_rows is None else [pairs_rows[0]]
+    y = np.full((B, L, _f64(w_o).shape[0]), np.nan)
+    for b in bs:
+        qkv = linear(x[b], w_qkv)  # [L, 3 H d]
+        q = qkv[:, :H * d].reshape(1, L, H, d)
+        k = qkv[:, H * d:2 * H * d].reshape(1, L, H, d)
+        v = qkv[:, 2 * H * d:].reshape(1, L, H, d)
+        rows = None if pairs_rows is None else np.asarray(pairs_rows[1])
+        a, _, _ = rla2_prefill(q, k, v, gamma_q, gamma_k, eps_norm, rope_base, eps_den,
+                               pos_offset=pos_offset, rows=rows)
+        rr = np.arange(L) if rows is None else rows
+        y[b, rr] = linear(a[0, rr].reshape(len(rr), H * d), w_o)
+    return y

@@ -141,3 +141,50 @@ def test_a_pin_catches_the_mistake(kind, monkeypatch):
         except AssertionError:
             caught += 1
     assert caught > 0, kind
+
+
+# ---------------------------------------------------------------- the layer (projections)
+
+def _layer_case(seed, B=1, L=20, H=2, d=8):
+    dm = H * d
+    x = _rand(seed, (B, L, dm))
+    gq = syn.rng(seed + 1).uniform(0.8, 1.2, (H, d))
+    gk = syn.rng(seed + 2).uniform(0.8, 1.2, (H, d))
+    return x, gq, gk, dm
+
+
+def test_layer_with_identity_projections_is_the_attention():
+    x, gq, gk, dm = _layer_case(50)
+    eye = np.eye(dm)
+    y = O.rapt_layer(x, np.vstack([eye, eye, eye]), eye, gq, gk, 2, pos_offset=3)
+    q = x.reshape(1, 20, 2, 8)
+    a, _, _ = O.rla2_prefill(q, q, q, gq, gk, 1e-6, 1e4, 1e-4, pos_offset=3)
+    np.testing.assert_allclose(y, a.reshape(1, 20, dm), rtol=1e-12, atol=1e-14)
+
+
+def test_layer_with_diagonal_projections():
+    """W_qkv = [diag(a); diag(b); diag(c)] and W_o = diag(e) reduce the layer to the attention of
+    the element-wise scaled inputs, scaled by e: this fixes the q | k | v order of the rows (the
+    three scalings differ, and RMSNorm keeps a per-element scaling) and the head-major columns."""
+    x, gq, gk, dm = _layer_case(51)
+    a, b, c, e = (syn.rng(60 + i).uniform(0.2, 2.0, dm) for i in range(4))
+    y = O.rapt_layer(x, np.vstack([np.diag(a), np.diag(b), np.diag(c)]), np.diag(e), gq, gk, 2)
+    sh = (1, 20, 2, 8)
+    att, _, _ = O.rla2_prefill((x * a).reshape(sh), (x * b).reshape(sh), (x * c).reshape(sh),
+                               gq, gk, 1e-6, 1e4, 1e-4)
+    np.testing.assert_allclose(y, att.reshape(1, 20, dm) * e, rtol=1e-12, atol=1e-14)
+    swapped, _, _ = O.rla2_prefill((x * b).reshape(sh), (x * a).reshape(sh), (x * c).reshape(sh),
+                                   gq, gk, 1e-6, 1e4, 1e-4)
+    assert not np.allclose(y, swapped.reshape(1, 20, dm) * e, rtol=1e-6)
+
+
+def test_layer_output_projection_permutes():
+    x, gq, gk, dm = _layer_case(54)
+    w = _rand(55, (3 * dm, dm))
+    perm = syn.rng(56).permutation(dm)
+    base = O.rapt_layer(x, w, np.eye(dm), gq, gk, 2)
+    np.testing.assert_allclose(O.rapt_layer(x, w, np.eye(dm)[perm], gq, gk, 2), base[..., perm],
+                               rtol=1e-12, atol=1e-14)
+    # sampled rows agree with the full evaluation
+    part = O.rapt_layer(x, w, np.eye(dm), gq, gk, 2, pairs_rows=(0, [0, 7, 19]))
+    np.testing.assert_allclose(part[0, [0, 7, 19]], base[0, [0, 7, 19]], rtol=1e-12)
