@@ -279,6 +279,12 @@ def profile_case(args):
         gq, gk = (torch.from_numpy(x).to(device) for x in (w.gamma_q, w.gamma_k))
         tg = torch.empty_like(q).normal_(generator=torch.Generator(device=device).manual_seed(5))
         call = lambda: R.rapt_prefill_bwd(q, k, v, tg, gq, gk)
+    elif args.only == "linear":
+        gen = torch.Generator(device=device).manual_seed(6)
+        x = torch.empty((16384, 2048), dtype=torch.bfloat16, device=device).normal_(generator=gen)
+        w = torch.empty((6144, 2048), dtype=torch.bfloat16, device=device).normal_(generator=gen)
+        y = torch.empty((16384, 6144), dtype=torch.bfloat16, device=device)
+        call = lambda: R.rapt_linear_fwd(x, w, out=y)
     elif args.only == "l2":
         wl = syn.l2_bf16(seed=4)
         q, k, v = (_bf(x, device) for x in (wl.q, wl.k, wl.v))
@@ -499,6 +505,43 @@ def run_gpu(args, rank, world, local):
                                         "+ bwd_gain_kernel (one call)"}}
     del tg, gws, grads
 
+    # ---------------- one RAPT layer around the headline attention (d_model = H d = 2048), and its
+    # q | k | v projection alone (the tensor-core GEMM)
+    dm = H * d
+    gen = torch.Generator(device=device).manual_seed(6)
+    x = torch.empty((B, L, dm), dtype=torch.bfloat16, device=device).normal_(generator=gen)
+    w_qkv = torch.empty((3 * H * d, dm), dtype=torch.bfloat16, device=device).normal_(
+        std=dm ** -0.5, generator=gen)
+    w_o = torch.empty((dm, H * d), dtype=torch.bfloat16, device=device).normal_(
+        std=(H * d) ** -0.5, generator=gen)
+    y = torch.empty_like(x)
+    lws = torch.empty(lib.rapt_layer_workspace_size(B, L, H, d, dm), dtype=torch.uint8,
+                      device=device)
+    y_ms, y_launch = time_steps(
+        lambda: R.rapt_layer_fwd(x, w_qkv, w_o, gq, gk, heads=H, out=y, workspace=lws),
+        max(3, args.steps // 2), args.warmup, flush, counter=lib.rapt_launch_counter)
+    y_mean = max_over_ranks(statistics.fmean(y_ms), device)
+    qkv_out = torch.empty((B * L, 3 * H * d), dtype=torch.bfloat16, device=device)
+    x2 = x.view(B * L, dm)
+    p_ms = time_steps(lambda: R.rapt_linear_fwd(x2, w_qkv, out=qkv_out), max(3, args.steps // 2),
+                      args.warmup, flush)
+    p_mean = max_over_ranks(statistics.fmean(p_ms), device)
+    p_flops = 2.0 * B * L * dm * 3 * H * d
+    layer_flops = p_flops + 2.0 * B * L * H * d * dm + B * L * H * (4 * d * d + 4 * d)
+    layer = {"value": world * B * L / (y_mean * 1e-3), "unit": "tokens/s", "ms_per_step": y_mean,
+             "workload": "rapt_layer B=4 L=4096 H=16 d=128 d_model=2048 bf16 (q|k|v projection, "
+                         "causal RLA-2, output projection), synthetic N(0, 1/fan_in) weights",
+             "launches_per_call": y_launch / max(3, args.steps // 2),
+             "tflops": layer_flops / (y_mean * 1e-3) / 1e12,
+             "projection": {"ms": p_mean, "workload": "y = x W^T, M=16384 N=6144 K=2048 bf16",
+                            "roofline": {"bound": "tensor",
+                                         "achieved": p_flops / (p_mean * 1e-3) / 1e12,
+                                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                         "frac": p_flops / (p_mean * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                                         "peak_source": "measured bf16_tflops (cuBLAS burst)",
+                                         "kernels": "linear_tc_kernel"}}}
+    del x, w_qkv, w_o, y, lws, qkv_out, x2
+
     # ---------------- CPU baseline: the fp64 oracle on a bounded sample (rank 0, N=1 only)
     cpu = None
     if rank == 0 and world == 1:
@@ -532,7 +575,7 @@ def run_gpu(args, rank, world, local):
         "gpu_launches": int(timed_launches),
         "clocks": clk,
         "decode": decode, "varlen": varlen, "rla_l2": rla_l2, "bidir": bidir,
-        "backward": backward, "l2_causal": l2_causal,
+        "backward": backward, "l2_causal": l2_causal, "layer": layer,
         "cpu_baseline": cpu,
     }
     if rank == 0:
@@ -572,7 +615,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--oracle-seconds", type=float, default=15.0)
-    ap.add_argument("--only", choices=["prefill", "varlen", "l2", "bidir", "backward"], default=None,
+    ap.add_argument("--only", choices=["prefill", "varlen", "l2", "bidir", "backward", "linear"], default=None,
                     help="run one workload's calls without timing (for an ncu capture)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

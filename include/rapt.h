@@ -217,6 +217,37 @@ rapt_status rla_l2_causal_varlen_fwd(const void* q, const void* k, const void* v
                                      size_t workspace_bytes, rapt_stream_t stream);
 
 /*
+ * Projection y = x W^T (the layer's linear maps: q = W_q x, k = W_k x, v = W_v x before the
+ * features, 08-rapt-algorithm.md §3; the output projection w_o after the division, §4.2).
+ *   x  [M, K] bf16, W [N, K] bf16 (row-major, K contiguous: a linear layer's weight), y [M, N] bf16.
+ * Tensor cores (tcgen05), bf16 operands, fp32 accumulation, result rounded to nearest even.
+ * Requirements: M >= 0, K % 8 == 0, N % 16 == 0; y must not alias x or W. dev_status (nullable,
+ * DEVICE uint32) gets RAPT_DEV_INTERNAL if a tensor-core wait gave up (never expected).
+ */
+rapt_status rapt_linear_fwd(const void* x, const void* w, void* y, int32_t M, int32_t N,
+                            int32_t K, uint32_t* dev_status, rapt_stream_t stream);
+
+/*
+ * One RAPT attention layer (08-rapt-algorithm.md §3, §4.2 forward): projections, the causal RLA-2
+ * attention of rapt_prefill_fwd, output projection:
+ *   [q | k | v] = x W_qkv^T   (x [B, L, d_model] bf16; W_qkv [3 H d, d_model] bf16 whose rows are
+ *                              W_q, then W_k, then W_v, each H d rows in head-major order h d + j),
+ *   a = RLA-2(q, k, v) per head ([B, L, H, d], features and denominator as for rapt_prefill_fwd,
+ *       one document per batch row, RoPE position pos_offset + t),
+ *   y = a W_o^T               (W_o [d_model, H d] bf16, y [B, L, d_model] bf16).
+ * q, k, v and a are bf16 tensors in the workspace (rapt_layer_workspace_size() bytes, 16-byte
+ * aligned): four [B, L, H, d] activations, then the attention's own workspace. The projections run
+ * on the tensor cores; the attention as rapt_prefill_fwd with dtype bf16.
+ * Requirements: d in {16, 32, 64, 128}, d_model % 16 == 0; y must not alias an input.
+ */
+size_t rapt_layer_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, int32_t d_model);
+rapt_status rapt_layer_fwd(const void* x, const void* w_qkv, const void* w_o, int32_t B,
+                           int32_t L, int32_t H, int32_t d, int32_t d_model,
+                           const float* gamma_q, const float* gamma_k, rapt_params params,
+                           int32_t pos_offset, void* y, uint32_t* dev_status, void* workspace,
+                           size_t workspace_bytes, rapt_stream_t stream);
+
+/*
  * Bidirectional (non-causal) RLA-2 (08-rapt-algorithm.md §4.1: in its causal=false mode the prefix
  * scan sums over the whole set; §4.2: the layer's bidirectional branch; formula and eps of §3).
  * Features as in the causal form; for each (document, head), S = sum_tau k'_tau v_tau^T and

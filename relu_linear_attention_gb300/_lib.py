@@ -72,6 +72,12 @@ SIGNATURES = {
                                            c_int32, c_int32, c_int32, c_void_p, c_int32, c_int32,
                                            c_float, c_void_p, c_void_p, c_void_p, c_size_t,
                                            c_void_p]),
+    "rapt_linear_fwd": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32,
+                                  c_void_p, c_void_p]),
+    "rapt_layer_workspace_size": (c_size_t, [c_int32] * 5),
+    "rapt_layer_fwd": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
+                                 c_int32, c_void_p, c_void_p, rapt_params, c_int32, c_void_p,
+                                 c_void_p, c_void_p, c_size_t, c_void_p]),
     "rapt_bidir_workspace_size": (c_size_t, [c_int32] * 4 + [c_int32]),
     "rapt_bidir_fwd": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32,
                                  c_int32, c_int32, c_int32, c_int32,

@@ -266,6 +266,57 @@ def rla_l2_causal_varlen_fwd(q, k, v, cu_seqlens, *, max_seqlen, eps=1e-6, out=N
     return out
 
 
+def rapt_linear_fwd(x, w, *, out=None, dev_status=None, stream=None):
+    """y = x W^T on the tensor cores: x [M, K] bf16, w [N, K] bf16. Returns y [M, N] bf16."""
+    _need(x.dim() == 2 and w.dim() == 2 and x.shape[1] == w.shape[1], "x [M, K], w [N, K]")
+    M, K = x.shape
+    N = w.shape[0]
+    _cuda_contig("x", x, torch.bfloat16, x.shape)
+    _cuda_contig("w", w, torch.bfloat16, w.shape)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _cuda_contig("out", out, torch.bfloat16, (M, N))
+    if dev_status is not None:
+        _cuda_contig("dev_status", dev_status, torch.int32)
+    st = _lib.load().rapt_linear_fwd(_ptr(x), _ptr(w), _ptr(out), M, N, K, _ptr(dev_status),
+                                     _stream(stream))
+    _lib.check("rapt_linear_fwd", st)
+    return out
+
+
+def rapt_layer_fwd(x, w_qkv, w_o, gamma_q, gamma_k, *, heads, eps_norm=1e-6, rope_base=1e4,
+                   eps_den=1e-4, pos_offset=0, out=None, dev_status=None, workspace=None,
+                   stream=None):
+    """One RAPT attention layer: x [B, L, d_model] bf16, w_qkv [3 H d, d_model], w_o [d_model, H d].
+    Returns y [B, L, d_model] bf16."""
+    _need(x.dim() == 3, "x must be [B, L, d_model]")
+    B, L, dm = x.shape
+    H = int(heads)
+    _need(w_qkv.dim() == 2 and w_qkv.shape[1] == dm and w_qkv.shape[0] % (3 * H) == 0,
+          "w_qkv must be [3 H d, d_model]")
+    d = w_qkv.shape[0] // (3 * H)
+    _need(tuple(w_o.shape) == (dm, H * d), "w_o must be [d_model, H d]")
+    for name, t in (("x", x), ("w_qkv", w_qkv), ("w_o", w_o)):
+        _cuda_contig(name, t, torch.bfloat16, t.shape)
+    stride = _gammas(gamma_q, gamma_k, H, d)
+    if out is None:
+        out = torch.empty_like(x)
+    _cuda_contig("out", out, torch.bfloat16, x.shape)
+    if dev_status is not None:
+        _cuda_contig("dev_status", dev_status, torch.int32)
+    lib = _lib.load()
+    need = lib.rapt_layer_workspace_size(B, L, H, d, dm)
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, device=x.device, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.rapt_layer_fwd(_ptr(x), _ptr(w_qkv), _ptr(w_o), B, L, H, d, dm, _ptr(gamma_q),
+                            _ptr(gamma_k), make_params(eps_norm, rope_base, eps_den, stride),
+                            int(pos_offset), _ptr(out), _ptr(dev_status), _ptr(workspace), ws_bytes,
+                            _stream(stream))
+    _lib.check("rapt_layer_fwd", st)
+    return out
+
+
 def rapt_bidir_fwd(q, k, v, gamma_q, gamma_k, *, eps_norm=1e-6, rope_base=1e4, eps_den=1e-4,
                    pos_offset=0, out=None, dev_status=None, workspace=None, stream=None):
     """Dense bidirectional (non-causal) RLA-2; q, k, v [B, L, H, d] (fp32 or bf16). Returns out."""

@@ -456,6 +456,81 @@ rapt_status rla_l2_causal_varlen_fwd(const void* q, const void* k, const void* v
                           stream);
 }
 
+rapt_status rapt_linear_fwd(const void* x, const void* w, void* y, int32_t M, int32_t N,
+                            int32_t K, uint32_t* dev_status, rapt_stream_t stream) {
+  if (M < 0 || N < 1 || K < 1) return RAPT_ERR_INVALID_ARG;
+  if (K % 8 != 0 || N % 16 != 0) return RAPT_ERR_UNSUPPORTED;
+  if (!fits_i32(static_cast<long long>(M) * K) || !fits_i32(static_cast<long long>(N) * K) ||
+      !fits_i32(static_cast<long long>(M) * N))
+    return RAPT_ERR_INVALID_ARG;
+  if (M > 0 && (x == nullptr || w == nullptr || y == nullptr)) return RAPT_ERR_INVALID_ARG;
+  if (!opt_aligned16(x) || !opt_aligned16(w) || !opt_aligned16(y)) return RAPT_ERR_INVALID_ARG;
+  if (y != nullptr && (y == x || y == w)) return RAPT_ERR_INVALID_ARG;
+  if (dev_status != nullptr && !aligned4(dev_status)) return RAPT_ERR_INVALID_ARG;
+  void* outs[1] = {y};
+  return from_cuda(rapt::launch_linear_tc(x, w, outs, M, N, K, N, dev_status,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+}  // namespace
+
+size_t rapt_layer_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, int32_t d_model) {
+  if (!supported_d(d) || B < 1 || H < 1 || L < 0 || d_model < 1) return 0;
+  const size_t act = up256(static_cast<size_t>(B) * L * H * d * 2);
+  return 4 * act + rapt_prefill_workspace_size(B, L, H, d, RAPT_BF16);
+}
+
+rapt_status rapt_layer_fwd(const void* x, const void* w_qkv, const void* w_o, int32_t B,
+                           int32_t L, int32_t H, int32_t d, int32_t d_model,
+                           const float* gamma_q, const float* gamma_k, rapt_params params,
+                           int32_t pos_offset, void* y, uint32_t* dev_status, void* workspace,
+                           size_t workspace_bytes, rapt_stream_t stream) {
+  if (!supported_d(d)) return RAPT_ERR_UNSUPPORTED;
+  if (B < 1 || H < 1 || L < 0 || d_model < 1 || pos_offset < 0) return RAPT_ERR_INVALID_ARG;
+  if (d_model % 16 != 0) return RAPT_ERR_UNSUPPORTED;
+  const long long T = static_cast<long long>(B) * L;
+  if (!fits_i32(T * d_model) || !fits_i32(T * 3 * H * d) ||
+      !fits_i32(static_cast<long long>(3) * H * d * d_model) ||
+      !fits_i32(static_cast<long long>(pos_offset) + L))
+    return RAPT_ERR_INVALID_ARG;
+  if (T > 0 && (x == nullptr || w_qkv == nullptr || w_o == nullptr || y == nullptr))
+    return RAPT_ERR_INVALID_ARG;
+  if (!opt_aligned16(x) || !opt_aligned16(w_qkv) || !opt_aligned16(w_o) || !opt_aligned16(y))
+    return RAPT_ERR_INVALID_ARG;
+  if (y != nullptr && (y == x || y == w_qkv || y == w_o)) return RAPT_ERR_INVALID_ARG;
+  if (dev_status != nullptr && !aligned4(dev_status)) return RAPT_ERR_INVALID_ARG;
+  rapt_status st = check_features(gamma_q, gamma_k, params, d);
+  if (st != RAPT_OK) return st;
+  const size_t need = rapt_layer_workspace_size(B, L, H, d, d_model);
+  if (workspace_bytes < need || (need > 0 && (workspace == nullptr || !aligned16(workspace))))
+    return RAPT_ERR_WORKSPACE;
+  if (T == 0) return RAPT_OK;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* wb = static_cast<uint8_t*>(workspace);
+  const size_t act = up256(static_cast<size_t>(T) * H * d * 2);
+  void* q = wb;
+  void* k = wb + act;
+  void* v = wb + 2 * act;
+  void* attn = wb + 3 * act;
+  void* pws = wb + 4 * act;
+  // q | k | v = x W_qkv^T, split into three [T, H, d] tensors
+  void* qkv[3] = {q, k, v};
+  cudaError_t e = rapt::launch_linear_tc(x, w_qkv, qkv, static_cast<int>(T), 3 * H * d, d_model,
+                                         H * d, dev_status, s);
+  if (e != cudaSuccess) return RAPT_ERR_CUDA;
+  st = rapt_prefill_fwd(q, k, v, RAPT_BF16, B, L, H, d, gamma_q, gamma_k, params, pos_offset,
+                        nullptr, nullptr, attn, nullptr, nullptr, dev_status, pws,
+                        workspace_bytes - 4 * act, stream);
+  if (st != RAPT_OK) return st;
+  // y = attn W_o^T
+  void* outs[1] = {y};
+  e = rapt::launch_linear_tc(attn, w_o, outs, static_cast<int>(T), d_model, H * d, d_model,
+                             dev_status, s);
+  return from_cuda(e);
+}
+
 rapt_status rapt_decode_step(const void* q, const void* k, const void* v, rapt_dtype dtype,
                              int32_t N, int32_t H, int32_t d, const int32_t* positions,
                              const float* gamma_q, const float* gamma_k, rapt_params params,

@@ -97,6 +97,14 @@ struct L2cPlan {
 L2cPlan l2c_plan(int n_docs, int H, int max_seqlen, int d);
 cudaError_t launch_l2_causal_simt(DType dt, int d, const L2cArgs& b, cudaStream_t stream);
 
+// y = x W^T on the tensor cores (bf16 in and out, fp32 accumulation): x [M, K], W [N, K] row-major.
+// The N output columns are split into N / split_n (<= 3) tensors outs[i] of [M, split_n].
+// Shapes: K % 8 == 0, N % 16 == 0, split_n % 16 == 0 and divides N. dev_status (nullable) gets
+// RAPT_DEV_INTERNAL if a wait gave up.
+bool linear_shape_ok(int M, int N, int K, int split_n);
+cudaError_t launch_linear_tc(const void* x, const void* w, void* const* outs, int M, int N, int K,
+                             int split_n, uint32_t* dev_status, cudaStream_t stream);
+
 // Tensor-core (tcgen05) chunked prefill for bf16 and d in {64, 128}. Documents are cut into
 // nseg_max segments of seg_len tokens; the state increments of every segment but a document's
 // last are computed first, in blocks of seg_len / blk_per_seg tokens, and ws_bytes of workspace
