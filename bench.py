@@ -285,6 +285,11 @@ def profile_case(args):
         w = torch.empty((6144, 2048), dtype=torch.bfloat16, device=device).normal_(generator=gen)
         y = torch.empty((16384, 6144), dtype=torch.bfloat16, device=device)
         call = lambda: R.rapt_linear_fwd(x, w, out=y)
+    elif args.only == "l2_causal":
+        wl = syn.l2_bf16(seed=4)
+        q, k, v = (_bf(x, device) for x in (wl.q, wl.k, wl.v))
+        out = torch.empty_like(q)
+        call = lambda: R.rla_l2_causal_fwd(q, k, v, eps=1e-6, out=out)
     elif args.only == "l2":
         wl = syn.l2_bf16(seed=4)
         q, k, v = (_bf(x, device) for x in (wl.q, wl.k, wl.v))
@@ -615,7 +620,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--oracle-seconds", type=float, default=15.0)
-    ap.add_argument("--only", choices=["prefill", "varlen", "l2", "bidir", "backward", "linear"], default=None,
+    ap.add_argument("--only", choices=["prefill", "varlen", "l2", "bidir", "backward", "linear", "l2_causal"], default=None,
                     help="run one workload's calls without timing (for an ncu capture)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

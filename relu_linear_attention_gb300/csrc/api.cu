@@ -309,7 +309,8 @@ rapt_status backward_common(const void* q, const void* k, const void* v, const v
       return RAPT_ERR_CUDA;
     return RAPT_OK;
   }
-  const rapt::BwdPlan plan = rapt::bwd_plan(n_docs, H, max_seqlen, total_rows, d);
+  const bool tc = rapt::bwd_tc_supported(to_dt(dtype), d);
+  const rapt::BwdPlan plan = rapt::bwd_plan(n_docs, H, max_seqlen, total_rows, d, tc);
   rapt::BwdArgs b{};
   rapt::PrefillArgs& a = b.p;
   a.q = q; a.k = k; a.v = v; a.out = nullptr;
@@ -331,6 +332,7 @@ rapt_status backward_common(const void* q, const void* k, const void* v, const v
   b.dgp_k = reinterpret_cast<float*>(w + plan.off_dgk);
   b.nseg = plan.nseg;
   b.seg_len = plan.seg_len;
+  if (tc) return from_cuda(rapt::launch_backward_tc(b, s));
   return from_cuda(rapt::launch_backward_simt(to_dt(dtype), d, b, s));
 }
 
@@ -339,7 +341,8 @@ rapt_status backward_common(const void* q, const void* k, const void* v, const v
 size_t rapt_prefill_bwd_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d,
                                        rapt_dtype dtype) {
   if (!known_dtype(dtype) || !supported_d(d) || B < 1 || H < 1 || L < 1) return 0;
-  return rapt::bwd_plan(B, H, L, static_cast<long>(B) * L, d).ws_bytes;
+  return rapt::bwd_plan(B, H, L, static_cast<long>(B) * L, d,
+                        rapt::bwd_tc_supported(to_dt(dtype), d)).ws_bytes;
 }
 
 rapt_status rapt_prefill_bwd(const void* q, const void* k, const void* v, const void* dout,
@@ -362,7 +365,7 @@ size_t rapt_varlen_bwd_workspace_size(int32_t T, int32_t N, int32_t H, int32_t d
                                       int32_t max_seqlen, rapt_dtype dtype) {
   if (!known_dtype(dtype) || !supported_d(d) || N < 1 || H < 1 || max_seqlen < 0 || T < 1)
     return 0;
-  return rapt::bwd_plan(N, H, max_seqlen, T, d).ws_bytes;
+  return rapt::bwd_plan(N, H, max_seqlen, T, d, rapt::bwd_tc_supported(to_dt(dtype), d)).ws_bytes;
 }
 
 rapt_status rapt_varlen_bwd(const void* q, const void* k, const void* v, const void* dout,

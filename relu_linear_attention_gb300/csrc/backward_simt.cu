@@ -31,6 +31,7 @@
 //      state from the later segments' increments, dk', dv, dk and the gain partials of k;
 //   4. bwd_gain_kernel: the gain partials summed in a fixed order.
 // No float atomics anywhere: every sum has a fixed order, so results are bitwise repeatable.
+#include "feature_bwd.cuh"
 #include "kernels.h"
 #include "simt_tiles.cuh"
 #include "tc_features.cuh"
@@ -70,75 +71,6 @@ struct BwdSmem {
   static_assert(bytes <= 232448, "shared memory budget");
   static_assert(PS + (kThreads / FeatureLayout<D>::TPR) * D <= ZS, "gain partials fit in PS + AS");
 };
-
-template <typename T>
-__device__ __forceinline__ void store2(T* p, float a, float b);
-template <>
-__device__ __forceinline__ void store2<float>(float* p, float a, float b) {
-  *reinterpret_cast<float2*>(p) = make_float2(a, b);
-}
-template <>
-__device__ __forceinline__ void store2<__nv_bfloat16>(__nv_bfloat16* p, float a, float b) {
-  *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
-}
-
-// Backward of f = ReLU(RoPE(RMSNorm(x))) for one token row, the lane mapping of feature_row
-// (TPR lanes per row, lane r owns elements [r*EPT, (r+1)*EPT)). df: the row's gradient of f in
-// shared memory. Writes dx (valid rows only) and adds this row's gain gradient dy_hat * x * rinv
-// into dg. Every lane of the warp must call it together (shuffles over the full warp).
-template <int D, typename T>
-__device__ __forceinline__ void feature_row_bwd(const T* x, bool valid, const float* gamma,
-                                                int pos, const FeatureArgs& fa, int r,
-                                                const float* df, T* dx,
-                                                float (&dg)[FeatureLayout<D>::EPT]) {
-  using FL = FeatureLayout<D>;
-  constexpr int EPT = FL::EPT;
-  float f[EPT];
-  if (valid) {
-    RowLoad<T, EPT>::run(x + r * EPT, f);
-  } else {
-#pragma unroll
-    for (int i = 0; i < EPT; ++i) f[i] = 0.f;
-  }
-  float ss = 0.f;
-#pragma unroll
-  for (int i = 0; i < EPT; ++i) ss = fmaf(f[i], f[i], ss);
-#pragma unroll
-  for (int off = FL::TPR / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-  const float rinv = rsqrtf(ss * (1.0f / D) + fa.eps_norm);
-  float u[EPT];  // gamma * dy_hat
-  float dot = 0.f;
-#pragma unroll
-  for (int m = 0; m < EPT / 2; ++m) {
-    const int e = r * EPT + 2 * m;
-    const float g0 = gamma[e], g1 = gamma[e + 1];
-    const float y0 = f[2 * m] * rinv * g0;
-    const float y1 = f[2 * m + 1] * rinv * g1;
-    float s, c;
-    rope_sincos(pos, fa.rope_hi[e >> 1], fa.rope_lo[e >> 1], s, c);
-    const float a = fmaf(y0, c, -y1 * s);  // the forward's pre-activation, same arithmetic
-    const float b = fmaf(y0, s, y1 * c);
-    const float da = (valid && a > 0.f) ? df[e] : 0.f;
-    const float db = (valid && b > 0.f) ? df[e + 1] : 0.f;
-    const float h0 = fmaf(da, c, db * s);   // inverse rotation
-    const float h1 = fmaf(-da, s, db * c);
-    dg[2 * m] = fmaf(h0, f[2 * m] * rinv, dg[2 * m]);
-    dg[2 * m + 1] = fmaf(h1, f[2 * m + 1] * rinv, dg[2 * m + 1]);
-    u[2 * m] = g0 * h0;
-    u[2 * m + 1] = g1 * h1;
-    dot = fmaf(u[2 * m], f[2 * m], dot);
-    dot = fmaf(u[2 * m + 1], f[2 * m + 1], dot);
-  }
-#pragma unroll
-  for (int off = FL::TPR / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-  const float c3 = rinv * rinv * rinv * dot * (1.0f / D);
-  if (valid) {
-#pragma unroll
-    for (int m = 0; m < EPT / 2; ++m)
-      store2<T>(dx + r * EPT + 2 * m, fmaf(rinv, u[2 * m], -f[2 * m] * c3),
-                fmaf(rinv, u[2 * m + 1], -f[2 * m + 1] * c3));
-  }
-}
 
 // Features of C rows starting at token t0 of the document into a [C][LD] tile (tail rows zero).
 template <int D, typename T>
@@ -657,12 +589,7 @@ cudaError_t launch_t(const BwdArgs& b, cudaStream_t stream) {
   bwd_reverse_kernel<T, D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(b);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (b.dgamma_q != nullptr || b.dgamma_k != nullptr) {
-    const int n_out = b.p.fa.gamma_stride != 0 ? b.p.H * D : D;
-    bwd_gain_kernel<<<dim3(static_cast<unsigned>((n_out + 255) / 256), 2), 256, 0, stream>>>(b, D);
-    note_launches(1);
-  }
-  return cudaGetLastError();
+  return launch_bwd_gain(b, D, stream);
 }
 
 template <typename T>
@@ -678,7 +605,7 @@ cudaError_t launch_d(int d, const BwdArgs& b, cudaStream_t stream) {
 
 }  // namespace
 
-BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d) {
+BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d, bool tc) {
   // One CTA per SM (the kernels take most of the shared memory). A document is cut into nseg
   // segments of seg_len tokens (a multiple of the chunk); the cost of a plan is its waves of
   // kSMs CTAs times the chunks of a segment (plus one chunk of set-up per wave).
@@ -697,13 +624,13 @@ BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d) {
       p.seg_len = seg_chunks * kC;
     }
   }
-  if (p.nseg == 0) {
+  if (p.nseg == 0 || tc) {
     p.nseg = 1;
     p.seg_len = chunks_max * kC;
   }
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t rec = static_cast<size_t>(d) * (d + 1) * sizeof(float);
-  const size_t recs = up(static_cast<size_t>(units) * p.nseg * rec);
+  const size_t recs = tc ? 0 : up(static_cast<size_t>(units) * p.nseg * rec);
   const size_t rows = up(static_cast<size_t>(total_rows) * H * sizeof(float));
   const size_t gp = up(static_cast<size_t>(units) * p.nseg * d * sizeof(float));
   p.off_rev = recs;
@@ -715,6 +642,14 @@ BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d) {
   p.off_dgk = p.off_dgq + gp;
   p.ws_bytes = p.off_dgk + gp;
   return p;
+}
+
+cudaError_t launch_bwd_gain(const BwdArgs& b, int d, cudaStream_t stream) {
+  if (b.dgamma_q == nullptr && b.dgamma_k == nullptr) return cudaSuccess;
+  const int n_out = b.p.fa.gamma_stride != 0 ? b.p.H * d : d;
+  bwd_gain_kernel<<<dim3(static_cast<unsigned>((n_out + 255) / 256), 2), 256, 0, stream>>>(b, d);
+  note_launches(1);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_backward_simt(DType dt, int d, const BwdArgs& b, cudaStream_t stream) {

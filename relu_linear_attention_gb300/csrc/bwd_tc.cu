@@ -1,0 +1,708 @@
+// Backward of causal RLA-2 on the 5th-generation tensor cores (tcgen05 + TMEM), sm_103a; bf16
+// tensors, d = 128, fp32 accumulation and fp32 states.
+//
+// The gradients of sum dout . out (08-rapt-algorithm.md §4.2 "backward": the main and z scans,
+// gnum = g / den and scale = -(g . num) / den^2, two suffix scans, then ReLU, RoPE and RMSNorm
+// backwards) in chunked form, C = 128 tokens per chunk (the MMA's M). Per document and head:
+//
+// Pass A (chunks in order; prefix state S = sum k'v^T in TMEM, its bf16 copy S~ in shared memory):
+//   P  = Q'K'^T,  Cv = G V^T,  U = G S~^T,  S += K'^T V                     (one MMA group)
+//   per row t: den = q'.z + sum_{tau<=t} P + eps,  nst = q'_t . U_t = g_t . (q'_t S~),
+//              pc = sum_{tau<=t} P Cv,  scale = -(nst + pc) / den^2
+//   A'[t][tau] = (c ps - pc + c sst - nst + eps c) / den  (c = Cv[t][tau], ps = sum P, sst = q'.z)
+//              = den (gnum_t . v_tau + scale_t), in the form whose cancelling part is exact for a
+//              query that sees a single key (see backward_simt.cu)
+//   U += A'~ K'                                                                (second MMA group)
+//   dq'_t = U_t / den_t + scale_t z,  then dq through the feature map; den, scale, sst, nst of every
+//   row go to the workspace for pass B.
+// Pass B (chunks in reverse; suffix state R = sum q' gnum^T in TMEM, bf16 copy R~, w = sum scale q'):
+//   P = Q'K'^T,  Gv = Gnum V^T                                              (first group)
+//   P~ = P masked to tau <= t;  A[t][tau] = A'/den, with c = den Gv
+//   dv  = P~^T Gnum + K' R~                                                  (second group)
+//   dk' = A^T Q' + V R~^T (+ w),  R += Q'^T Gnum                             (third group)
+//   then dk through the feature map.
+// One CTA per (document, head), 512 threads in lockstep phases: all threads compute features, read
+// TMEM rows (thread = TMEM lane = tile row, four warps per lane quarter splitting the columns) and
+// run the feature backward; one thread issues the MMAs and commits them to an mbarrier. Every
+// wait is bounded (~1 s); a CTA whose wait gives up sets RAPT_DEV_INTERNAL in the status word and
+// writes NaN gain partials, so a failure cannot pass for a result.
+#include <cuda.h>
+
+#include "feature_bwd.cuh"
+#include "kernels.h"
+#include "tc_features.cuh"
+#include "tc_utils.cuh"
+
+namespace rapt {
+namespace {
+
+using feat::doc_bounds;
+using feat::lds16;
+using feat::ldg16;
+using feat::sts16;
+
+constexpr int kD = 128;
+constexpr int kC = 128;
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr long long kWait = 2000000000LL;  // ~1 s of SM cycles
+constexpr uint32_t kTile = 32768;          // 128 rows x 128 bf16 columns (two 64-column blocks)
+constexpr int kSL = kD + 1;                // row stride (floats) of the fp32 staging of dq' / dk'
+
+// Shared memory (bytes from a 1024-byte aligned base). Both passes use the same map: six bf16
+// tiles (the fifth, XS, holds S~ in pass A and R~ in pass B; the last, AS, holds A' in pass A and
+// P~ then A in pass B), then fp32 vectors.
+struct Lay {
+  static constexpr uint32_t QF = 0, KF = kTile, VS = 2 * kTile, GS = 3 * kTile, XS = 4 * kTile;
+  static constexpr uint32_t AS = 5 * kTile;
+  static constexpr uint32_t STG = 0;                          // fp32 [128][kSL] over QF..VS
+  static constexpr uint32_t ZS = 6 * kTile;                   // z (pass A) / w (pass B) [D]
+  static constexpr uint32_t ZP = ZS + kD * 4;                 // per-warp k' column sums [16][D]
+  static constexpr uint32_t ROW = ZP + kWarps * kD * 4;       // den, scale, sst, nst [4][128]
+  static constexpr uint32_t RED = ROW + 4 * kC * 4;           // partial row sums [3][4][128]
+  static constexpr uint32_t BAR = RED + 3 * 4 * kC * 4;       // three mbarriers
+  static constexpr uint32_t MISC = BAR + 3 * 8;               // TMEM base, abort flag
+  static constexpr uint32_t BYTES = MISC + 16;
+  static_assert(static_cast<uint32_t>(kC) * kSL * 4 <= 3 * kTile, "staging fits over QF..VS");
+  static_assert(BYTES <= 232448, "shared memory budget");
+};
+
+// TMEM columns.
+constexpr uint32_t kTP = 0, kTG = 128, kTU = 256, kTS = 384;  // pass A: P, Cv, U, S
+constexpr uint32_t kTDV = 0, kTDK = 128, kTR = 256;           // pass B: dv (over P), dk' (over Gv), R
+
+// Byte offset of 16-byte chunk m (0..15, 8 bf16 each) of row r in a 128-row tile of 128 columns.
+__device__ __forceinline__ uint32_t tile_off(int r, int m) {
+  return static_cast<uint32_t>(m >> 3) * 16384u + tc::sw128(r, m & 7);
+}
+// The same in a D-row tile (S~ / R~: rows = D).
+__device__ __forceinline__ uint32_t dtile_off(int r, int m) {
+  return static_cast<uint32_t>(m >> 3) * (kD * 128u) + tc::sw128(r, m & 7);
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    f[2 * i] = p.x;
+    f[2 * i + 1] = p.y;
+  }
+}
+
+// K-major operand descriptor of a 128-row tile, K step k (16 elements).
+__device__ __forceinline__ uint64_t kmaj(uint32_t tile, int k) {
+  return tc::desc_sw128(tile, 16, 1024) + static_cast<uint64_t>((k >> 2) * 1024 + (k & 3) * 2);
+}
+// K-major operand descriptor of a D-row tile (S~ / R~ as N x K).
+__device__ __forceinline__ uint64_t kmaj_d(uint32_t tile, int k) {
+  return tc::desc_sw128(tile, 16, 1024) + static_cast<uint64_t>((k >> 2) * (kD * 8) + (k & 3) * 2);
+}
+// MN-major operand descriptor (rows = K): 128-row tile (LBO 16 KB) or D-row tile (LBO D*128 B).
+__device__ __forceinline__ uint64_t mnmaj(uint32_t tile, int k, uint32_t lbo) {
+  return tc::desc_sw128(tile, lbo, 1024) + static_cast<uint64_t>(k) * 128;
+}
+
+// Features of the chunk's 128 rows of x (q or k) into a bf16 tile: warp w takes rows w, w + 16, ...
+// (FeatureLayout: lane r owns elements 4r .. 4r+3); the loads of all its rows are issued before
+// any is used. With z given, also q'_t . z of every row into sst[]; the lane's column sums of the
+// features are added to zc.
+constexpr int kRPW = kC / kWarps;  // rows per warp
+
+__device__ __forceinline__ void load_rows(const __nv_bfloat16* x, long row0, int n, int t0, int H,
+                                          int h, float (&f)[kRPW][4]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint2 raw[kRPW];
+#pragma unroll
+  for (int i = 0; i < kRPW; ++i) {
+    const int t = t0 + warp + kWarps * i;
+    raw[i] = t < n ? __ldg(reinterpret_cast<const uint2*>(x + ((row0 + t) * H + h) * kD + 4 * lane))
+                   : make_uint2(0, 0);
+  }
+#pragma unroll
+  for (int i = 0; i < kRPW; ++i) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[i].x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[i].y));
+    f[i][0] = a.x; f[i][1] = a.y; f[i][2] = b.x; f[i][3] = b.y;
+  }
+}
+
+__device__ __forceinline__ void feature_tile_tc(const __nv_bfloat16* x, long row0, int n, int t0,
+                                                int H, int h, const float* gamma, int pos0,
+                                                const FeatureArgs& fa, uint32_t tile,
+                                                const float* z, float* sst, float (&zc)[4]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float f[kRPW][4];
+  load_rows(x, row0, n, t0, H, h, f);
+#pragma unroll 2
+  for (int i = 0; i < kRPW; ++i) {
+    const int rr = warp + kWarps * i;
+    const int t = t0 + rr;
+    const bool valid = t < n;
+    feature_vals<kD>(f[i], valid, gamma, pos0 + t, fa, lane);
+    const uint32_t addr = tile + tile_off(rr, lane >> 1) + (lane & 1) * 8;
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr),
+                 "r"(tc::pack_bf16x2(f[i][0], f[i][1])), "r"(tc::pack_bf16x2(f[i][2], f[i][3]))
+                 : "memory");
+    if (z != nullptr) {
+      float s = f[i][0] * z[4 * lane] + f[i][1] * z[4 * lane + 1] + f[i][2] * z[4 * lane + 2] +
+                f[i][3] * z[4 * lane + 3];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      if (lane == 0) sst[rr] = valid ? s : 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) zc[e] += f[i][e];
+  }
+}
+
+// Back through the features of the chunk's rows of x (q or k): warp w takes rows w, w + 16, ...
+// with their loads issued first; df rows come from the fp32 staging.
+__device__ __forceinline__ void feature_tile_bwd_tc(const __nv_bfloat16* x, long row0, int n,
+                                                    int t0, int H, int h, const float* gamma,
+                                                    int pos0, const FeatureArgs& fa,
+                                                    const float* stg, __nv_bfloat16* dx,
+                                                    float (&dg)[4]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float f[kRPW][4];
+  load_rows(x, row0, n, t0, H, h, f);
+#pragma unroll 2
+  for (int i = 0; i < kRPW; ++i) {
+    const int rr = warp + kWarps * i;
+    const int t = t0 + rr;
+    const bool valid = t < n;
+    const long off = ((row0 + (valid ? t : 0)) * H + h) * kD;
+    feature_vals_bwd<kD, __nv_bfloat16>(f[i], valid, gamma, pos0 + t, fa, lane, stg + rr * kSL,
+                                        dx + off, dg);
+  }
+}
+
+// Raw rows of v (or g) into a bf16 tile (rows past the document are zero); with den given, every
+// row is divided by its den (gnum = g / den) and rounded to bf16.
+__device__ __forceinline__ void raw_tile_tc(const __nv_bfloat16* x, long row0, int n, int t0, int H,
+                                            int h, uint32_t tile, const float* den) {
+  constexpr int kPer = kC * 16 / kThreads;  // 16-byte chunks per thread
+  uint4 v[kPer];
+  float dn[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int idx = threadIdx.x + kThreads * i, r = idx >> 4, m = idx & 15;
+    const bool valid = t0 + r < n;
+    v[i] = valid ? ldg16(x + ((row0 + t0 + r) * H + h) * kD + 8 * m) : make_uint4(0, 0, 0, 0);
+    dn[i] = (den != nullptr && valid) ? den[(row0 + t0 + r) * H + h] : 1.f;
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int idx = threadIdx.x + kThreads * i, r = idx >> 4, m = idx & 15;
+    if (den != nullptr) {
+      float f[8];
+      unpack8(v[i], f);
+      const float inv = 1.0f / dn[i];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] *= inv;
+      v[i] = feat::pack8(f);
+    }
+    sts16(tile + tile_off(r, m), v[i]);
+  }
+}
+
+// Reads 32 consecutive fp32 TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t u[2][16];
+  tc::tmem_ld16(taddr, u[0]);
+  tc::tmem_ld16(taddr + 16, u[1]);
+  tc::tmem_wait_ld();
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    v[e] = __uint_as_float(u[0][e]);
+    v[16 + e] = __uint_as_float(u[1][e]);
+  }
+}
+
+// 32 fp32 values as bf16 into row r, columns 32 g .. 32 g + 31 of a tile (tile_off or dtile_off).
+template <bool DROWS>
+__device__ __forceinline__ void store_row32(uint32_t tile, int r, int g, const float (&v)[32]) {
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t off = DROWS ? dtile_off(r, 4 * g + m) : tile_off(r, 4 * g + m);
+    sts16(tile + off, feat::pack8(v + 8 * m));
+  }
+}
+
+// Waits for an mbarrier phase; returns false when the wait gave up.
+__device__ __forceinline__ bool wait_mma(uint32_t bar, int parity) {
+  const bool ok = tc::mbar_wait(bar, parity, kWait);
+  tc::fence_after_sync();
+  return ok;
+}
+
+// Gain partials of this CTA (each lane's dg over the rows it took) summed over the warps in order.
+__device__ __forceinline__ void store_gain(const float (&dg)[4], float* scratch, float* out, bool bad) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) scratch[warp * kD + 4 * lane + e] = dg[e];
+  __syncthreads();
+  if (threadIdx.x < kD) {
+    float s = 0.f;
+    for (int w = 0; w < kWarps; ++w) s += scratch[w * kD + threadIdx.x];
+    out[threadIdx.x] = bad ? __int_as_float(0x7fc00000) : s;
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Pass A: chunks in order.
+__global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
+  const PrefillArgs& a = b.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int unit = blockIdx.x, h = unit % a.H, doc = unit / a.H;
+  long row0;
+  int n;
+  if (!doc_bounds(a, doc, row0, n) && h == 0 && tid == 0 && a.dev_status != nullptr)
+    atomicOr(a.dev_status, 1u);
+  const int nch = (n + kC - 1) / kC;
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t base = tc::smem_u32(smem);
+  float* zs = reinterpret_cast<float*>(smem + Lay::ZS);
+  float* zp = reinterpret_cast<float*>(smem + Lay::ZP);
+  float* den_s = reinterpret_cast<float*>(smem + Lay::ROW);
+  float* scl_s = den_s + kC;
+  float* sst_s = scl_s + kC;
+  float* red = reinterpret_cast<float*>(smem + Lay::RED);
+  float* stg = reinterpret_cast<float*>(smem + Lay::STG);
+  const uint32_t bar1 = base + Lay::BAR, bar2 = bar1 + 8;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + Lay::MISC);
+  int* s_abort = reinterpret_cast<int*>(smem + Lay::MISC + 4);
+  const bool misaligned = (base & 1023u) != 0;
+
+  if (warp == 0 && !misaligned && nch > 0) {
+    tc::tmem_alloc(tc::smem_u32(s_tmem), 512);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    tc::mbar_init(bar1, 1);
+    tc::mbar_init(bar2, 1);
+    tc::mbar_fence_init();
+    *s_abort = misaligned ? 1 : 0;
+  }
+  for (int i = tid; i < kD * kD * 2 / 16; i += kThreads)
+    sts16(base + Lay::XS + 16 * i, make_uint4(0, 0, 0, 0));  // S~ = 0
+  if (tid < kD) zs[tid] = 0.f;
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *s_tmem;
+
+  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+  const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
+  const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v);
+  const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(b.dout);
+  __nv_bfloat16* dq = static_cast<__nv_bfloat16*>(b.dq);
+  const float* gq = a.gamma_q + h * a.fa.gamma_stride;
+  const float* gk = a.gamma_k + h * a.fa.gamma_stride;
+  const int q4 = warp & 3, gw = warp >> 2;  // TMEM lane quarter, column group (32 columns)
+  const int t = 32 * q4 + lane;             // this thread's tile row (= TMEM lane)
+  const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
+  float dg[4] = {0.f, 0.f, 0.f, 0.f};
+  bool bad = *s_abort != 0;
+
+  for (int c = 0; c < nch && !bad; ++c) {
+    const int t0 = c * kC;
+    // ---- phase 1: features (q'.z of every row), column sums of k', v and g tiles
+    float zc[4] = {0.f, 0.f, 0.f, 0.f}, dummy[4] = {0.f, 0.f, 0.f, 0.f};
+    feature_tile_tc(q, row0, n, t0, a.H, h, gq, a.pos_offset, a.fa, base + Lay::QF, zs, sst_s,
+                    dummy);
+    feature_tile_tc(k, row0, n, t0, a.H, h, gk, a.pos_offset, a.fa, base + Lay::KF, nullptr,
+                    nullptr, zc);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) zp[warp * kD + 4 * lane + e] = zc[e];
+    raw_tile_tc(v, row0, n, t0, a.H, h, base + Lay::VS, nullptr);
+    raw_tile_tc(g, row0, n, t0, a.H, h, base + Lay::GS, nullptr);
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    // ---- phase 2: P = Q'K'^T, Cv = G V^T, U = G S~^T, S += K'^T V
+    if (tid == 0) {
+      constexpr uint32_t ID_KK = tc::idesc_bf16(128, 128, false, false);
+      constexpr uint32_t ID_MM = tc::idesc_bf16(128, 128, true, true);
+#pragma unroll 1
+      for (int kk = 0; kk < kD / 16; ++kk) {
+        tc::mma_bf16(tmem + kTP, kmaj(base + Lay::QF, kk), kmaj(base + Lay::KF, kk), ID_KK, kk > 0);
+        tc::mma_bf16(tmem + kTG, kmaj(base + Lay::GS, kk), kmaj(base + Lay::VS, kk), ID_KK, kk > 0);
+        tc::mma_bf16(tmem + kTU, kmaj(base + Lay::GS, kk), kmaj_d(base + Lay::XS, kk), ID_KK, kk > 0);
+      }
+#pragma unroll 1
+      for (int kk = 0; kk < kC / 16; ++kk)
+        tc::mma_bf16(tmem + kTS, mnmaj(base + Lay::KF, kk, 16384), mnmaj(base + Lay::VS, kk, 16384),
+                     ID_MM, (c > 0 || kk > 0) ? 1u : 0u);
+      tc::mma_commit(bar1);
+    }
+    if (!wait_mma(bar1, c & 1)) atomicExch(s_abort, 1);
+    // ---- phase 3: row sums, den, scale, A'
+    const bool valid = t0 + t < n;
+    float pv[32], cv[32];
+    tmem_ld32(tmem + tl + kTP + 32 * gw, pv);
+    tmem_ld32(tmem + tl + kTG + 32 * gw, cv);
+    float ps = 0.f, pc = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const bool vis = 32 * gw + j <= t;
+      ps += vis ? pv[j] : 0.f;
+      pc += vis ? pv[j] * cv[j] : 0.f;
+    }
+    float nst = 0.f;
+    {
+      float u[32];
+      tmem_ld32(tmem + tl + kTU + 32 * gw, u);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        float f[8];
+        unpack8(lds16(base + Lay::QF + tile_off(t, 4 * gw + m)), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) nst += f[e] * u[8 * m + e];
+      }
+    }
+    red[(0 * 4 + gw) * kC + t] = ps;
+    red[(1 * 4 + gw) * kC + t] = pc;
+    red[(2 * 4 + gw) * kC + t] = nst;
+    tc::fence_before_sync();
+    __syncthreads();
+    ps = red[t] + red[kC + t] + red[2 * kC + t] + red[3 * kC + t];
+    pc = red[4 * kC + t] + red[5 * kC + t] + red[6 * kC + t] + red[7 * kC + t];
+    nst = red[8 * kC + t] + red[9 * kC + t] + red[10 * kC + t] + red[11 * kC + t];
+    const float sst = sst_s[t];
+    const float den = valid ? sst + ps + a.eps_den : 1.f;
+    const float scale = valid ? -(nst + pc) / (den * den) : 0.f;
+    if (gw == 0) {
+      den_s[t] = den;
+      scl_s[t] = scale;
+      if (valid) {
+        const long o = (row0 + t0 + t) * a.H + h;
+        b.den[o] = den;
+        b.scl[o] = scale;
+        b.sst[o] = sst;
+        b.nst[o] = nst;
+      }
+    }
+    {
+      const float inv = 1.0f / den;
+      float av[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float cc = cv[j];
+        const float num = (cc * ps - pc) + (fmaf(cc, sst, -nst) + a.eps_den * cc);
+        av[j] = (32 * gw + j <= t) ? num * inv : 0.f;
+      }
+      store_row32<false>(base + Lay::AS, t, gw, av);
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
+    // ---- phase 4: U += A'~ K'
+    if (tid == 0) {
+      constexpr uint32_t ID = tc::idesc_bf16(128, 128, false, true);
+#pragma unroll 1
+      for (int kk = 0; kk < kC / 16; ++kk)
+        tc::mma_bf16(tmem + kTU, kmaj(base + Lay::AS, kk), mnmaj(base + Lay::KF, kk, 16384), ID, 1u);
+      tc::mma_commit(bar2);
+    }
+    if (!wait_mma(bar2, c & 1)) atomicExch(s_abort, 1);
+    // ---- phase 5: dq' = U / den + scale z into the staging; S -> S~
+    {
+      float u[32];
+      tmem_ld32(tmem + tl + kTU + 32 * gw, u);
+      const float inv = 1.0f / den;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) u[j] = fmaf(u[j], inv, scale * zs[32 * gw + j]);
+      // the staging overlays q', k', v: every MMA that read them has completed (bar2)
+      tc::fence_before_sync();
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) stg[t * kSL + 32 * gw + j] = u[j];
+      float sv[32];
+      tmem_ld32(tmem + tl + kTS + 32 * gw, sv);
+      store_row32<true>(base + Lay::XS, t, gw, sv);
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
+    // ---- phase 6: z += column sums of k'; back through the features of q
+    if (tid < kD) {
+      float s = zs[tid];
+      for (int w = 0; w < kWarps; ++w) s += zp[w * kD + tid];
+      zs[tid] = s;
+    }
+    feature_tile_bwd_tc(q, row0, n, t0, a.H, h, gq, a.pos_offset, a.fa, stg, dq, dg);
+    __syncthreads();  // the staging and zs are read before the next chunk overwrites them
+  }
+  bad = bad || *reinterpret_cast<volatile int*>(s_abort) != 0;
+  __syncthreads();
+  store_gain(dg, zp, b.dgp_q + static_cast<long>(unit) * kD, bad);
+  if (bad && tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, 2u);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0 && !misaligned && nch > 0) tc::tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Pass B: chunks in reverse.
+__global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
+  const PrefillArgs& a = b.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int unit = blockIdx.x, h = unit % a.H, doc = unit / a.H;
+  long row0;
+  int n;
+  doc_bounds(a, doc, row0, n);
+  const int nch = (n + kC - 1) / kC;
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t base = tc::smem_u32(smem);
+  float* ws = reinterpret_cast<float*>(smem + Lay::ZS);  // w
+  float* scratch = reinterpret_cast<float*>(smem + Lay::ZP);
+  float* den_s = reinterpret_cast<float*>(smem + Lay::ROW);
+  float* scl_s = den_s + kC;
+  float* sst_s = scl_s + kC;
+  float* nst_s = sst_s + kC;
+  float* red = reinterpret_cast<float*>(smem + Lay::RED);
+  float* stg = reinterpret_cast<float*>(smem + Lay::STG);
+  const uint32_t bar1 = base + Lay::BAR, bar2 = bar1 + 8, bar3 = bar2 + 8;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + Lay::MISC);
+  int* s_abort = reinterpret_cast<int*>(smem + Lay::MISC + 4);
+  const bool misaligned = (base & 1023u) != 0;
+
+  if (warp == 0 && !misaligned && nch > 0) {
+    tc::tmem_alloc(tc::smem_u32(s_tmem), 512);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    tc::mbar_init(bar1, 1);
+    tc::mbar_init(bar2, 1);
+    tc::mbar_init(bar3, 1);
+    tc::mbar_fence_init();
+    *s_abort = misaligned ? 1 : 0;
+  }
+  for (int i = tid; i < kD * kD * 2 / 16; i += kThreads)
+    sts16(base + Lay::XS + 16 * i, make_uint4(0, 0, 0, 0));  // R~ = 0
+  if (tid < kD) ws[tid] = 0.f;
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *s_tmem;
+
+  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+  const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
+  const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v);
+  const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(b.dout);
+  __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(b.dk);
+  __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(b.dv);
+  const float* gq = a.gamma_q + h * a.fa.gamma_stride;
+  const float* gk = a.gamma_k + h * a.fa.gamma_stride;
+  const int q4 = warp & 3, gw = warp >> 2;
+  const int t = 32 * q4 + lane;
+  const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
+  float dg[4] = {0.f, 0.f, 0.f, 0.f};
+  bool bad = *s_abort != 0;
+  int it = 0;  // chunks done (the mbarrier phases)
+
+  for (int c = nch - 1; c >= 0 && !bad; --c, ++it) {
+    const int t0 = c * kC;
+    // ---- phase 1: features, v, gnum = g / den, and the row scalars of pass A
+    float dummy[4] = {0.f, 0.f, 0.f, 0.f};
+    feature_tile_tc(q, row0, n, t0, a.H, h, gq, a.pos_offset, a.fa, base + Lay::QF, nullptr,
+                    nullptr, dummy);
+    feature_tile_tc(k, row0, n, t0, a.H, h, gk, a.pos_offset, a.fa, base + Lay::KF, nullptr,
+                    nullptr, dummy);
+    raw_tile_tc(v, row0, n, t0, a.H, h, base + Lay::VS, nullptr);
+    raw_tile_tc(g, row0, n, t0, a.H, h, base + Lay::GS, b.den);
+    if (tid < kC) {
+      const bool vr = t0 + tid < n;
+      const long o = (row0 + t0 + tid) * a.H + h;
+      den_s[tid] = vr ? b.den[o] : 1.f;
+      scl_s[tid] = vr ? b.scl[o] : 0.f;
+      sst_s[tid] = vr ? b.sst[o] : 0.f;
+      nst_s[tid] = vr ? b.nst[o] : 0.f;
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    // ---- phase 2: P = Q'K'^T, Gv = Gnum V^T
+    if (tid == 0) {
+      constexpr uint32_t ID = tc::idesc_bf16(128, 128, false, false);
+#pragma unroll 1
+      for (int kk = 0; kk < kD / 16; ++kk) {
+        tc::mma_bf16(tmem + kTP, kmaj(base + Lay::QF, kk), kmaj(base + Lay::KF, kk), ID, kk > 0);
+        tc::mma_bf16(tmem + kTG, kmaj(base + Lay::GS, kk), kmaj(base + Lay::VS, kk), ID, kk > 0);
+      }
+      tc::mma_commit(bar1);
+    }
+    if (!wait_mma(bar1, it & 1)) atomicExch(s_abort, 1);
+    // ---- phase 3: P~ (masked) into AS; A kept in registers
+    const float den = den_s[t], sst = sst_s[t], nst = nst_s[t];
+    float pv[32], av[32];
+    tmem_ld32(tmem + tl + kTP + 32 * gw, pv);
+    tmem_ld32(tmem + tl + kTG + 32 * gw, av);  // Gnum . v, times den below = g . v
+    float ps = 0.f, pc = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const bool vis = 32 * gw + j <= t;
+      av[j] *= den;
+      pv[j] = vis ? pv[j] : 0.f;
+      ps += pv[j];
+      pc += pv[j] * av[j];
+    }
+    red[(0 * 4 + gw) * kC + t] = ps;
+    red[(1 * 4 + gw) * kC + t] = pc;
+    store_row32<false>(base + Lay::AS, t, gw, pv);
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
+    ps = red[t] + red[kC + t] + red[2 * kC + t] + red[3 * kC + t];
+    pc = red[4 * kC + t] + red[5 * kC + t] + red[6 * kC + t] + red[7 * kC + t];
+    {
+      const float inv2 = 1.0f / (den * den);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float cc = av[j];
+        const float num = (cc * ps - pc) + (fmaf(cc, sst, -nst) + a.eps_den * cc);
+        av[j] = (32 * gw + j <= t) ? num * inv2 : 0.f;
+      }
+    }
+    // ---- phase 4: dv = P~^T Gnum + K' R~
+    if (tid == 0) {
+      constexpr uint32_t ID_MM = tc::idesc_bf16(128, 128, true, true);
+      constexpr uint32_t ID_KM = tc::idesc_bf16(128, 128, false, true);
+#pragma unroll 1
+      for (int kk = 0; kk < kC / 16; ++kk)
+        tc::mma_bf16(tmem + kTDV, mnmaj(base + Lay::AS, kk, 16384), mnmaj(base + Lay::GS, kk, 16384),
+                     ID_MM, kk > 0);
+#pragma unroll 1
+      for (int kk = 0; kk < kD / 16; ++kk)
+        tc::mma_bf16(tmem + kTDV, kmaj(base + Lay::KF, kk), mnmaj(base + Lay::XS, kk, kD * 128),
+                     ID_KM, 1u);
+      tc::mma_commit(bar2);
+    }
+    if (!wait_mma(bar2, it & 1)) atomicExch(s_abort, 1);
+    // ---- phase 5: A over P~ (the dv MMAs have read it); dv out
+    store_row32<false>(base + Lay::AS, t, gw, av);
+    {
+      float o[32];
+      tmem_ld32(tmem + tl + kTDV + 32 * gw, o);
+      if (t0 + t < n) {
+        __nv_bfloat16* dst = dv + ((row0 + t0 + t) * a.H + h) * kD + 32 * gw;
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(o + 8 * m);
+      }
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
+    // ---- phase 6: dk' = A^T Q' + V R~^T, then R += Q'^T Gnum
+    if (tid == 0) {
+      constexpr uint32_t ID_MM = tc::idesc_bf16(128, 128, true, true);
+      constexpr uint32_t ID_KK = tc::idesc_bf16(128, 128, false, false);
+#pragma unroll 1
+      for (int kk = 0; kk < kC / 16; ++kk)
+        tc::mma_bf16(tmem + kTDK, mnmaj(base + Lay::AS, kk, 16384), mnmaj(base + Lay::QF, kk, 16384),
+                     ID_MM, kk > 0);
+#pragma unroll 1
+      for (int kk = 0; kk < kD / 16; ++kk)
+        tc::mma_bf16(tmem + kTDK, kmaj(base + Lay::VS, kk), kmaj_d(base + Lay::XS, kk), ID_KK, 1u);
+#pragma unroll 1
+      for (int kk = 0; kk < kC / 16; ++kk)
+        tc::mma_bf16(tmem + kTR, mnmaj(base + Lay::QF, kk, 16384), mnmaj(base + Lay::GS, kk, 16384),
+                     ID_MM, (it > 0 || kk > 0) ? 1u : 0u);
+      tc::mma_commit(bar3);
+    }
+    if (!wait_mma(bar3, it & 1)) atomicExch(s_abort, 1);
+    // ---- phase 7: dk' + w into the staging, w += sum_t scale_t q'_t, R -> R~
+    {
+      float o[32];
+      tmem_ld32(tmem + tl + kTDK + 32 * gw, o);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] += ws[32 * gw + j];
+      {  // partial increment of w: column i of q', rows 32 (tid / 128) .. + 31
+        const int i = tid & (kD - 1), r0 = 32 * (tid >> 7);
+        const int m = i >> 3, e = i & 7;
+        float dw = 0.f;
+#pragma unroll 4
+        for (int r = r0; r < r0 + 32; ++r) {
+          uint32_t word;
+          asm volatile("ld.shared.b32 %0, [%1];"
+                       : "=r"(word)
+                       : "r"(base + Lay::QF + tile_off(r, m) + 4 * (e >> 1))
+                       : "memory");
+          const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&word));
+          dw = fmaf(scl_s[r], (e & 1) ? p.y : p.x, dw);
+        }
+        red[(tid >> 7) * kC + i] = dw;
+      }
+      tc::fence_before_sync();
+      __syncthreads();  // q' and w are read; the staging may overlay q', k', v
+#pragma unroll
+      for (int j = 0; j < 32; ++j) stg[t * kSL + 32 * gw + j] = o[j];
+      if (tid < kD) ws[tid] += red[tid] + red[kC + tid] + red[2 * kC + tid] + red[3 * kC + tid];
+      float rv[32];
+      tmem_ld32(tmem + tl + kTR + 32 * gw, rv);
+      store_row32<true>(base + Lay::XS, t, gw, rv);
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
+    // ---- phase 8: back through the features of k
+    feature_tile_bwd_tc(k, row0, n, t0, a.H, h, gk, a.pos_offset, a.fa, stg, dk, dg);
+    __syncthreads();
+  }
+  bad = bad || *reinterpret_cast<volatile int*>(s_abort) != 0;
+  __syncthreads();
+  store_gain(dg, scratch, b.dgp_k + static_cast<long>(unit) * kD, bad);
+  if (bad && tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, 2u);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0 && !misaligned && nch > 0) tc::tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+bool bwd_tc_supported(DType dt, int d) { return dt == DType::BF16 && d == kD; }
+
+cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static unsigned long long configured = 0;  // bit per device (idempotent; races are benign)
+  if (dev < 64 && !((configured >> dev) & 1ull)) {
+    e = cudaFuncSetAttribute(bwd_tc_forward, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Lay::BYTES));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(bwd_tc_reverse, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Lay::BYTES));
+    if (e != cudaSuccess) return e;
+    configured |= 1ull << dev;
+  }
+  const long grid = static_cast<long>(b.p.n_docs) * b.p.H;
+  if (grid == 0) return cudaSuccess;
+  bwd_tc_forward<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b);
+  note_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  bwd_tc_reverse<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b);
+  note_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return launch_bwd_gain(b, kD, stream);
+}
+
+}  // namespace rapt

@@ -130,18 +130,14 @@ struct FeatureLayout {
   static constexpr int ROWS_PER_WARP = 32 / TPR;
 };
 
-template <int D, typename T>
-__device__ __forceinline__ void feature_row(const T* x, bool valid, const float* gamma, int pos,
-                                            const FeatureArgs& fa, int r,
-                                            float (&f)[FeatureLayout<D>::EPT]) {
+// The arithmetic of feature_row on values already loaded into f (the lane's EPT elements; zeros
+// for an invalid row), so that a caller can issue the loads of several rows before using them.
+template <int D>
+__device__ __forceinline__ void feature_vals(float (&f)[FeatureLayout<D>::EPT], bool valid,
+                                             const float* gamma, int pos, const FeatureArgs& fa,
+                                             int r) {
   using FL = FeatureLayout<D>;
   constexpr int EPT = FL::EPT;
-  if (valid) {
-    RowLoad<T, EPT>::run(x + r * EPT, f);
-  } else {
-#pragma unroll
-    for (int i = 0; i < EPT; ++i) f[i] = 0.f;
-  }
   float ss = 0.f;
 #pragma unroll
   for (int i = 0; i < EPT; ++i) ss = fmaf(f[i], f[i], ss);
@@ -160,6 +156,21 @@ __device__ __forceinline__ void feature_row(const T* x, bool valid, const float*
     f[2 * m] = valid ? fmaxf(a, 0.f) : 0.f;
     f[2 * m + 1] = valid ? fmaxf(b, 0.f) : 0.f;
   }
+}
+
+template <int D, typename T>
+__device__ __forceinline__ void feature_row(const T* x, bool valid, const float* gamma, int pos,
+                                            const FeatureArgs& fa, int r,
+                                            float (&f)[FeatureLayout<D>::EPT]) {
+  using FL = FeatureLayout<D>;
+  constexpr int EPT = FL::EPT;
+  if (valid) {
+    RowLoad<T, EPT>::run(x + r * EPT, f);
+  } else {
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) f[i] = 0.f;
+  }
+  feature_vals<D>(f, valid, gamma, pos, fa, r);
 }
 
 }  // namespace rapt

@@ -76,8 +76,14 @@ struct BwdPlan {
   size_t off_rev, off_den, off_scl, off_sst, off_nst, off_dgq, off_dgk;
   size_t ws_bytes;
 };
-BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d);
+// tc: the tensor-core path (one CTA per (document, head), no segment increments).
+BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d, bool tc);
 cudaError_t launch_backward_simt(DType dt, int d, const BwdArgs& b, cudaStream_t stream);
+// The gain gradients from the per-(document, head, segment) partials (launched by both paths).
+cudaError_t launch_bwd_gain(const BwdArgs& b, int d, cudaStream_t stream);
+// Tensor-core backward (bf16, d = 128): two passes, then the gains.
+bool bwd_tc_supported(DType dt, int d);
+cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream);
 
 // Causal original RLA (L2 denominator) on CUDA cores over the documents of `p` (features ReLU(q),
 // ReLU(k); gammas, RoPE, states and eps_den unused). rec: the workspace, 2 d^2 floats (K'^T V, then
