@@ -332,6 +332,10 @@ rapt_status backward_common(const void* q, const void* k, const void* v, const v
   b.dgp_k = reinterpret_cast<float*>(w + plan.off_dgk);
   b.nseg = plan.nseg;
   b.seg_len = plan.seg_len;
+  b.qf = w + plan.off_qf;
+  b.kf = w + plan.off_kf;
+  b.blk_per_seg = plan.blk_per_seg;
+  b.nblk_max = plan.nblk_max;
   if (tc) return from_cuda(rapt::launch_backward_tc(b, s));
   return from_cuda(rapt::launch_backward_simt(to_dt(dtype), d, b, s));
 }

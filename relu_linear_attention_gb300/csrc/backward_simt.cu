@@ -607,10 +607,12 @@ cudaError_t launch_d(int d, const BwdArgs& b, cudaStream_t stream) {
 
 BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d, bool tc) {
   // One CTA per SM (the kernels take most of the shared memory). A document is cut into nseg
-  // segments of seg_len tokens (a multiple of the chunk); the cost of a plan is its waves of
-  // kSMs CTAs times the chunks of a segment (plus one chunk of set-up per wave).
+  // segments of seg_len tokens (a multiple of the chunk: 32 tokens on the CUDA cores, 128 on the
+  // tensor cores); the cost of a plan is its waves of kSMs CTAs times the chunks of a segment
+  // (plus one chunk of set-up per wave).
   BwdPlan p{};
-  const int chunks_max = max_seqlen > 0 ? (max_seqlen + kC - 1) / kC : 1;
+  const int ck = tc ? 128 : kC;
+  const int chunks_max = max_seqlen > 0 ? (max_seqlen + ck - 1) / ck : 1;
   const long units = static_cast<long>(n_docs) * H;
   double best = 1e300;
   for (int nseg = 1; nseg <= 64 && nseg <= chunks_max; ++nseg) {
@@ -621,24 +623,38 @@ BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d, bool
     if (cost < 0.95 * best) {
       best = cost;
       p.nseg = nseg;
-      p.seg_len = seg_chunks * kC;
+      p.seg_len = seg_chunks * ck;
     }
   }
-  if (p.nseg == 0 || tc) {
+  if (p.nseg == 0) {
     p.nseg = 1;
-    p.seg_len = chunks_max * kC;
+    p.seg_len = chunks_max * ck;
   }
+  p.blk_per_seg = 1;
+  if (tc) {  // state-kernel blocks: the largest of 8, 4, 2, 1 that divides the segment's chunks
+    const int sc = p.seg_len / ck;
+    for (int f = 8; f > 1; f /= 2)
+      if (sc % f == 0) {
+        p.blk_per_seg = f;
+        break;
+      }
+  }
+  p.nblk_max = (p.nseg - 1) * p.blk_per_seg;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t rec = static_cast<size_t>(d) * (d + 1) * sizeof(float);
-  const size_t recs = tc ? 0 : up(static_cast<size_t>(units) * p.nseg * rec);
+  const size_t recs_f = up(static_cast<size_t>(units) * (tc ? p.nblk_max : p.nseg) * rec);
+  const size_t recs_r = up(static_cast<size_t>(units) * p.nseg * rec);
   const size_t rows = up(static_cast<size_t>(total_rows) * H * sizeof(float));
+  const size_t feats = tc ? up(static_cast<size_t>(total_rows) * H * d * 2) : 0;
   const size_t gp = up(static_cast<size_t>(units) * p.nseg * d * sizeof(float));
-  p.off_rev = recs;
-  p.off_den = p.off_rev + recs;
+  p.off_rev = recs_f;
+  p.off_den = p.off_rev + recs_r;
   p.off_scl = p.off_den + rows;
   p.off_sst = p.off_scl + rows;
   p.off_nst = p.off_sst + rows;
-  p.off_dgq = p.off_nst + rows;
+  p.off_qf = p.off_nst + rows;
+  p.off_kf = p.off_qf + feats;
+  p.off_dgq = p.off_kf + feats;
   p.off_dgk = p.off_dgq + gp;
   p.ws_bytes = p.off_dgk + gp;
   return p;

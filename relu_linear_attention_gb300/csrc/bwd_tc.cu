@@ -106,7 +106,8 @@ __device__ __forceinline__ uint64_t mnmaj(uint32_t tile, int k, uint32_t lbo) {
 // Features of the chunk's 128 rows of x (q or k) into a bf16 tile: warp w takes rows w, w + 16, ...
 // (FeatureLayout: lane r owns elements 4r .. 4r+3); the loads of all its rows are issued before
 // any is used. With z given, also q'_t . z of every row into sst[]; the lane's column sums of the
-// features are added to zc.
+// features are added to zc; with out given, the bf16 features of the valid rows are stored there
+// ([T, H, D], for pass B).
 constexpr int kRPW = kC / kWarps;  // rows per warp
 
 __device__ __forceinline__ void load_rows(const __nv_bfloat16* x, long row0, int n, int t0, int H,
@@ -130,7 +131,8 @@ __device__ __forceinline__ void load_rows(const __nv_bfloat16* x, long row0, int
 __device__ __forceinline__ void feature_tile_tc(const __nv_bfloat16* x, long row0, int n, int t0,
                                                 int H, int h, const float* gamma, int pos0,
                                                 const FeatureArgs& fa, uint32_t tile,
-                                                const float* z, float* sst, float (&zc)[4]) {
+                                                const float* z, float* sst, float (&zc)[4],
+                                                __nv_bfloat16* out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float f[kRPW][4];
   load_rows(x, row0, n, t0, H, h, f);
@@ -141,9 +143,10 @@ __device__ __forceinline__ void feature_tile_tc(const __nv_bfloat16* x, long row
     const bool valid = t < n;
     feature_vals<kD>(f[i], valid, gamma, pos0 + t, fa, lane);
     const uint32_t addr = tile + tile_off(rr, lane >> 1) + (lane & 1) * 8;
-    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr),
-                 "r"(tc::pack_bf16x2(f[i][0], f[i][1])), "r"(tc::pack_bf16x2(f[i][2], f[i][3]))
-                 : "memory");
+    const uint32_t lo = tc::pack_bf16x2(f[i][0], f[i][1]), hi = tc::pack_bf16x2(f[i][2], f[i][3]);
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(lo), "r"(hi) : "memory");
+    if (out != nullptr && valid)
+      *reinterpret_cast<uint2*>(out + ((row0 + t) * H + h) * kD + 4 * lane) = make_uint2(lo, hi);
     if (z != nullptr) {
       float s = f[i][0] * z[4 * lane] + f[i][1] * z[4 * lane + 1] + f[i][2] * z[4 * lane + 2] +
                 f[i][3] * z[4 * lane + 3];
@@ -236,6 +239,21 @@ __device__ __forceinline__ bool wait_mma(uint32_t bar, int parity) {
   return ok;
 }
 
+// A state (S or R) into TMEM lane t (this thread's lane), columns 32 gw .. 32 gw + 31 (taddr points
+// there), and its bf16 copy into row t of the D-row tile xs.
+__device__ __forceinline__ void state_put(uint32_t taddr, uint32_t xs, int t, int gw,
+                                          const float (&v)[32]) {
+  uint32_t u[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(v[e]);
+  tc::tmem_st16(taddr, u);
+#pragma unroll
+  for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(v[16 + e]);
+  tc::tmem_st16(taddr + 16, u);
+  tc::tmem_wait_st();
+  store_row32<true>(xs, t, gw, v);
+}
+
 // Gain partials of this CTA (each lane's dg over the rows it took) summed over the warps in order.
 __device__ __forceinline__ void store_gain(const float (&dg)[4], float* scratch, float* out, bool bad) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -254,12 +272,14 @@ __device__ __forceinline__ void store_gain(const float (&dg)[4], float* scratch,
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int unit = blockIdx.x, h = unit % a.H, doc = unit / a.H;
+  const int seg = blockIdx.x % b.nseg, unit = blockIdx.x / b.nseg;
+  const int h = unit % a.H, doc = unit / a.H;
   long row0;
   int n;
-  if (!doc_bounds(a, doc, row0, n) && h == 0 && tid == 0 && a.dev_status != nullptr)
+  if (!doc_bounds(a, doc, row0, n) && h == 0 && seg == 0 && tid == 0 && a.dev_status != nullptr)
     atomicOr(a.dev_status, 1u);
-  const int nch = (n + kC - 1) / kC;
+  const int s0 = seg * b.seg_len, s1 = min(n, s0 + b.seg_len);
+  const int nch = s1 > s0 ? (s1 - s0 + kC - 1) / kC : 0;
 
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t base = tc::smem_u32(smem);
@@ -285,14 +305,39 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
     tc::mbar_fence_init();
     *s_abort = misaligned ? 1 : 0;
   }
-  for (int i = tid; i < kD * kD * 2 / 16; i += kThreads)
-    sts16(base + Lay::XS + 16 * i, make_uint4(0, 0, 0, 0));  // S~ = 0
-  if (tid < kD) zs[tid] = 0.f;
-  tc::fence_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *s_tmem;
+  const int q4 = warp & 3, gw = warp >> 2;  // TMEM lane quarter, column group (32 columns)
+  const int t = 32 * q4 + lane;             // this thread's tile row (= TMEM lane)
+  const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
+  // the prefix state at the segment's start: the increments of the blocks before it, in order
+  if (nch > 0) {
+    const int nb = seg * b.blk_per_seg;
+    constexpr long R4 = static_cast<long>(kD) * (kD + 1) / 4;
+    const float4* rec = reinterpret_cast<const float4*>(b.rec_fwd) + static_cast<long>(unit) * b.nblk_max * R4;
+    float sv[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) sv[e] = 0.f;
+    for (int blk = 0; blk < nb; ++blk) {
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const float4 x = __ldcg(rec + blk * R4 + (8 * gw + jj) * kD + t);
+        sv[4 * jj] += x.x; sv[4 * jj + 1] += x.y; sv[4 * jj + 2] += x.z; sv[4 * jj + 3] += x.w;
+      }
+    }
+    state_put(tmem + tl + kTS + 32 * gw, base + Lay::XS, t, gw, sv);
+    if (tid < kD) {
+      float z = 0.f;
+      for (int blk = 0; blk < nb; ++blk) z += __ldcg(b.rec_fwd + (static_cast<long>(unit) * b.nblk_max + blk) * (R4 * 4) + kD * kD + tid);
+      zs[tid] = z;
+    }
+  }
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
 
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
   const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
@@ -301,20 +346,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
   __nv_bfloat16* dq = static_cast<__nv_bfloat16*>(b.dq);
   const float* gq = a.gamma_q + h * a.fa.gamma_stride;
   const float* gk = a.gamma_k + h * a.fa.gamma_stride;
-  const int q4 = warp & 3, gw = warp >> 2;  // TMEM lane quarter, column group (32 columns)
-  const int t = 32 * q4 + lane;             // this thread's tile row (= TMEM lane)
-  const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
+  __nv_bfloat16* qf_out = static_cast<__nv_bfloat16*>(b.qf);
+  __nv_bfloat16* kf_out = static_cast<__nv_bfloat16*>(b.kf);
   float dg[4] = {0.f, 0.f, 0.f, 0.f};
   bool bad = *s_abort != 0;
 
   for (int c = 0; c < nch && !bad; ++c) {
-    const int t0 = c * kC;
+    const int t0 = s0 + c * kC;
     // ---- phase 1: features (q'.z of every row), column sums of k', v and g tiles
     float zc[4] = {0.f, 0.f, 0.f, 0.f}, dummy[4] = {0.f, 0.f, 0.f, 0.f};
     feature_tile_tc(q, row0, n, t0, a.H, h, gq, a.pos_offset, a.fa, base + Lay::QF, zs, sst_s,
-                    dummy);
+                    dummy, qf_out);
     feature_tile_tc(k, row0, n, t0, a.H, h, gk, a.pos_offset, a.fa, base + Lay::KF, nullptr,
-                    nullptr, zc);
+                    nullptr, zc, kf_out);
 #pragma unroll
     for (int e = 0; e < 4; ++e) zp[warp * kD + 4 * lane + e] = zc[e];
     raw_tile_tc(v, row0, n, t0, a.H, h, base + Lay::VS, nullptr);
@@ -336,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
 #pragma unroll 1
       for (int kk = 0; kk < kC / 16; ++kk)
         tc::mma_bf16(tmem + kTS, mnmaj(base + Lay::KF, kk, 16384), mnmaj(base + Lay::VS, kk, 16384),
-                     ID_MM, (c > 0 || kk > 0) ? 1u : 0u);
+                     ID_MM, 1u);
       tc::mma_commit(bar1);
     }
     if (!wait_mma(bar1, c & 1)) atomicExch(s_abort, 1);
@@ -442,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
   }
   bad = bad || *reinterpret_cast<volatile int*>(s_abort) != 0;
   __syncthreads();
-  store_gain(dg, zp, b.dgp_q + static_cast<long>(unit) * kD, bad);
+  store_gain(dg, zp, b.dgp_q + (static_cast<long>(unit) * b.nseg + seg) * kD, bad);
   if (bad && tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, 2u);
   tc::fence_before_sync();
   __syncthreads();
@@ -455,11 +499,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int unit = blockIdx.x, h = unit % a.H, doc = unit / a.H;
+  const int seg = blockIdx.x % b.nseg, unit = blockIdx.x / b.nseg;
+  const int h = unit % a.H, doc = unit / a.H;
   long row0;
   int n;
   doc_bounds(a, doc, row0, n);
-  const int nch = (n + kC - 1) / kC;
+  const int s0 = seg * b.seg_len, s1 = min(n, s0 + b.seg_len);
+  const int nch = s1 > s0 ? (s1 - s0 + kC - 1) / kC : 0;
 
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t base = tc::smem_u32(smem);
@@ -487,38 +533,58 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
     tc::mbar_fence_init();
     *s_abort = misaligned ? 1 : 0;
   }
-  for (int i = tid; i < kD * kD * 2 / 16; i += kThreads)
-    sts16(base + Lay::XS + 16 * i, make_uint4(0, 0, 0, 0));  // R~ = 0
-  if (tid < kD) ws[tid] = 0.f;
-  tc::fence_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *s_tmem;
+  const int q4 = warp & 3, gw = warp >> 2;
+  const int t = 32 * q4 + lane;
+  const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
+  // the suffix state at the segment's end: the later segments' increments, in segment order
+  if (nch > 0) {
+    constexpr long REC = static_cast<long>(kD) * kD + kD;
+    const float* rr = b.rec_rev + static_cast<long>(unit) * b.nseg * REC;
+    float rv[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) rv[e] = 0.f;
+    for (int sp = seg + 1; sp < b.nseg && sp * b.seg_len < n; ++sp) {
+      const float4* src = reinterpret_cast<const float4*>(rr + sp * REC + t * kD + 32 * gw);
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const float4 x = __ldcg(src + jj);
+        rv[4 * jj] += x.x; rv[4 * jj + 1] += x.y; rv[4 * jj + 2] += x.z; rv[4 * jj + 3] += x.w;
+      }
+    }
+    state_put(tmem + tl + kTR + 32 * gw, base + Lay::XS, t, gw, rv);
+    if (tid < kD) {
+      float w = 0.f;
+      for (int sp = seg + 1; sp < b.nseg && sp * b.seg_len < n; ++sp)
+        w += __ldcg(rr + sp * REC + kD * kD + tid);
+      ws[tid] = w;
+    }
+  }
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
 
-  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
   const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
   const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v);
   const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(b.dout);
   __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(b.dk);
   __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(b.dv);
-  const float* gq = a.gamma_q + h * a.fa.gamma_stride;
   const float* gk = a.gamma_k + h * a.fa.gamma_stride;
-  const int q4 = warp & 3, gw = warp >> 2;
-  const int t = 32 * q4 + lane;
-  const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
+  const __nv_bfloat16* qf_in = static_cast<const __nv_bfloat16*>(b.qf);
+  const __nv_bfloat16* kf_in = static_cast<const __nv_bfloat16*>(b.kf);
   float dg[4] = {0.f, 0.f, 0.f, 0.f};
   bool bad = *s_abort != 0;
   int it = 0;  // chunks done (the mbarrier phases)
 
   for (int c = nch - 1; c >= 0 && !bad; --c, ++it) {
-    const int t0 = c * kC;
-    // ---- phase 1: features, v, gnum = g / den, and the row scalars of pass A
-    float dummy[4] = {0.f, 0.f, 0.f, 0.f};
-    feature_tile_tc(q, row0, n, t0, a.H, h, gq, a.pos_offset, a.fa, base + Lay::QF, nullptr,
-                    nullptr, dummy);
-    feature_tile_tc(k, row0, n, t0, a.H, h, gk, a.pos_offset, a.fa, base + Lay::KF, nullptr,
-                    nullptr, dummy);
+    const int t0 = s0 + c * kC;
+    // ---- phase 1: q', k' (stored by pass A), v, gnum = g / den, and the row scalars of pass A
+    raw_tile_tc(qf_in, row0, n, t0, a.H, h, base + Lay::QF, nullptr);
+    raw_tile_tc(kf_in, row0, n, t0, a.H, h, base + Lay::KF, nullptr);
     raw_tile_tc(v, row0, n, t0, a.H, h, base + Lay::VS, nullptr);
     raw_tile_tc(g, row0, n, t0, a.H, h, base + Lay::GS, b.den);
     if (tid < kC) {
@@ -623,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
 #pragma unroll 1
       for (int kk = 0; kk < kC / 16; ++kk)
         tc::mma_bf16(tmem + kTR, mnmaj(base + Lay::QF, kk, 16384), mnmaj(base + Lay::GS, kk, 16384),
-                     ID_MM, (it > 0 || kk > 0) ? 1u : 0u);
+                     ID_MM, 1u);
       tc::mma_commit(bar3);
     }
     if (!wait_mma(bar3, it & 1)) atomicExch(s_abort, 1);
@@ -668,12 +734,117 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
   }
   bad = bad || *reinterpret_cast<volatile int*>(s_abort) != 0;
   __syncthreads();
-  store_gain(dg, scratch, b.dgp_k + static_cast<long>(unit) * kD, bad);
+  store_gain(dg, scratch, b.dgp_k + (static_cast<long>(unit) * b.nseg + seg) * kD, bad);
   if (bad && tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, 2u);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   if (warp == 0 && !misaligned && nch > 0) tc::tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Between the passes: the suffix-state increment of every segment after a document's first,
+// R_seg = sum_{t in seg} q'_t gnum_t^T and w_seg = sum scale_t q'_t (q' stored by pass A, gnum =
+// g / den), written as fp32 records [R row-major | w] for pass B.
+__global__ void __launch_bounds__(kThreads, 1) bwd_tc_revstate(const BwdArgs b) {
+  const PrefillArgs& a = b.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int seg = blockIdx.x % b.nseg, unit = blockIdx.x / b.nseg;
+  const int h = unit % a.H, doc = unit / a.H;
+  long row0;
+  int n;
+  doc_bounds(a, doc, row0, n);
+  const int s0 = seg * b.seg_len, s1 = min(n, s0 + b.seg_len);
+  if (seg == 0 || s0 >= s1) return;  // nobody reads the first segment's increment
+  const int nch = (s1 - s0 + kC - 1) / kC;
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t base = tc::smem_u32(smem);
+  float* ws = reinterpret_cast<float*>(smem + Lay::ZS);
+  float* scl_s = reinterpret_cast<float*>(smem + Lay::ROW);
+  float* red = reinterpret_cast<float*>(smem + Lay::RED);
+  const uint32_t bar1 = base + Lay::BAR;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + Lay::MISC);
+  int* s_abort = reinterpret_cast<int*>(smem + Lay::MISC + 4);
+  const bool misaligned = (base & 1023u) != 0;
+  if (warp == 0 && !misaligned) {
+    tc::tmem_alloc(tc::smem_u32(s_tmem), 128);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    tc::mbar_init(bar1, 1);
+    tc::mbar_fence_init();
+    *s_abort = misaligned ? 1 : 0;
+  }
+  if (tid < kD) ws[tid] = 0.f;
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *s_tmem;
+  const __nv_bfloat16* qf_in = static_cast<const __nv_bfloat16*>(b.qf);
+  const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(b.dout);
+  bool bad = *s_abort != 0;
+  for (int c = 0; c < nch && !bad; ++c) {
+    const int t0 = s0 + c * kC;
+    raw_tile_tc(qf_in, row0, n, t0, a.H, h, base + Lay::QF, nullptr);
+    raw_tile_tc(g, row0, n, t0, a.H, h, base + Lay::GS, b.den);
+    if (tid < kC) scl_s[tid] = t0 + tid < n ? b.scl[(row0 + t0 + tid) * a.H + h] : 0.f;
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (tid == 0) {
+      constexpr uint32_t ID_MM = tc::idesc_bf16(128, 128, true, true);
+#pragma unroll 1
+      for (int kk = 0; kk < kC / 16; ++kk)
+        tc::mma_bf16(tmem, mnmaj(base + Lay::QF, kk, 16384), mnmaj(base + Lay::GS, kk, 16384), ID_MM,
+                     (c > 0 || kk > 0) ? 1u : 0u);
+      tc::mma_commit(bar1);
+    }
+    {  // partial increment of w: column i of q', rows 32 (tid / 128) .. + 31
+      const int i = tid & (kD - 1), r0 = 32 * (tid >> 7);
+      const int m = i >> 3, e = i & 7;
+      float dw = 0.f;
+#pragma unroll 4
+      for (int r = r0; r < r0 + 32; ++r) {
+        uint32_t word;
+        asm volatile("ld.shared.b32 %0, [%1];"
+                     : "=r"(word)
+                     : "r"(base + Lay::QF + tile_off(r, m) + 4 * (e >> 1))
+                     : "memory");
+        const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&word));
+        dw = fmaf(scl_s[r], (e & 1) ? p.y : p.x, dw);
+      }
+      red[(tid >> 7) * kC + i] = dw;
+    }
+    if (!wait_mma(bar1, c & 1)) atomicExch(s_abort, 1);
+    __syncthreads();
+    if (tid < kD) ws[tid] += red[tid] + red[kC + tid] + red[2 * kC + tid] + red[3 * kC + tid];
+    bad = *reinterpret_cast<volatile int*>(s_abort) != 0;
+    __syncthreads();
+  }
+  // the record: R (TMEM lane i = row i) row-major, then w; NaN if a wait gave up
+  constexpr long REC = static_cast<long>(kD) * kD + kD;
+  float* rec = b.rec_rev + (static_cast<long>(unit) * b.nseg + seg) * REC;
+  const int q4 = warp & 3, gw = warp >> 2;
+  const int t = 32 * q4 + lane;
+  float rv[32];
+  if (!bad) {
+    tmem_ld32(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 32 * gw, rv);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) rv[e] = __int_as_float(0x7fc00000);
+  }
+#pragma unroll
+  for (int jj = 0; jj < 8; ++jj)
+    *reinterpret_cast<float4*>(rec + t * kD + 32 * gw + 4 * jj) =
+        make_float4(rv[4 * jj], rv[4 * jj + 1], rv[4 * jj + 2], rv[4 * jj + 3]);
+  if (tid < kD) rec[kD * kD + tid] = bad ? __int_as_float(0x7fc00000) : ws[tid];
+  if (bad && tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, 2u);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0 && !misaligned) tc::tmem_dealloc(tmem, 128);
 }
 
 }  // namespace
@@ -686,19 +857,37 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   static unsigned long long configured = 0;  // bit per device (idempotent; races are benign)
   if (dev < 64 && !((configured >> dev) & 1ull)) {
-    e = cudaFuncSetAttribute(bwd_tc_forward, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(Lay::BYTES));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(bwd_tc_reverse, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(Lay::BYTES));
-    if (e != cudaSuccess) return e;
+    for (const void* f : {reinterpret_cast<const void*>(bwd_tc_forward),
+                          reinterpret_cast<const void*>(bwd_tc_reverse),
+                          reinterpret_cast<const void*>(bwd_tc_revstate)}) {
+      e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(Lay::BYTES));
+      if (e != cudaSuccess) return e;
+    }
     configured |= 1ull << dev;
   }
-  const long grid = static_cast<long>(b.p.n_docs) * b.p.H;
+  const long grid = static_cast<long>(b.p.n_docs) * b.p.H * b.nseg;
   if (grid == 0) return cudaSuccess;
+  if (b.nseg > 1) {  // the prefix-state increments of the blocks before each document's last segment
+    TcArgs ta{};
+    ta.p = b.p;
+    ta.ws = b.rec_fwd;
+    ta.seg_len = b.seg_len;
+    ta.nseg_max = b.nseg;
+    ta.blk_per_seg = b.blk_per_seg;
+    ta.blk_len = b.seg_len / b.blk_per_seg;
+    ta.nblk_max = b.nblk_max;
+    ta.whole_doc = 0;
+    if ((e = launch_state_tc(kD, ta, stream)) != cudaSuccess) return e;
+  }
   bwd_tc_forward<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (b.nseg > 1) {
+    bwd_tc_revstate<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b);
+    note_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   bwd_tc_reverse<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

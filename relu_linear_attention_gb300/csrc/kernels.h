@@ -69,11 +69,20 @@ struct BwdArgs {
   float* dgp_k;
   int nseg;
   int seg_len;
+  // tensor-core path: q', k' of every (token, head) in bf16 (written by pass A, read by pass B),
+  // and the prefix-state increments in the prefill state kernel's record format (rec_fwd), in
+  // blocks of seg_len / blk_per_seg tokens, nblk_max per (document, head)
+  void* qf;
+  void* kf;
+  int blk_per_seg;
+  int nblk_max;
 };
 struct BwdPlan {
   int nseg;
   int seg_len;
-  size_t off_rev, off_den, off_scl, off_sst, off_nst, off_dgq, off_dgk;
+  int blk_per_seg;  // tensor-core path
+  int nblk_max;     // tensor-core path
+  size_t off_rev, off_den, off_scl, off_sst, off_nst, off_dgq, off_dgk, off_qf, off_kf;
   size_t ws_bytes;
 };
 // tc: the tensor-core path (one CTA per (document, head), no segment increments).
