@@ -455,17 +455,18 @@ def run_gpu(args, rank, world, local):
     c_mean = max_over_ranks(statistics.fmean(c_ms), device)
     c_flops = 2 * 16384 * 16 * (8 * 128 * 128 + 2 * 128)  # q'S, q'A q', S and A updates
     fp32_peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    c_bytes = prefill_bytes(2, 16384, 16, 128)
     l2_causal = {"value": world * 2 * 16384 / (c_mean * 1e-3), "unit": "tokens/s",
                  "ms_per_step": c_mean,
                  "workload": "rla_l2_causal B=2 L=16384 H=16 d=128 bf16 (causal L2 denominator)",
                  "launches_per_call": c_launch / max(3, args.steps // 4),
-                 "roofline": {"bound": "alu", "achieved": c_flops / (c_mean * 1e-3) / 1e12,
-                              "peak": fp32_peak, "unit": "TFLOP/s",
-                              "frac": c_flops / (c_mean * 1e-3) / 1e12 / fp32_peak,
-                              "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x max SM clock",
+                 "roofline": {"bound": "hbm", "achieved": c_bytes / (c_mean * 1e-3) / 1e9,
+                              "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                              "frac": c_bytes / (c_mean * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                              "algorithmic_bytes_per_call": c_bytes,
                               "algorithmic_flops_per_call": c_flops,
-                              "hbm_frac": prefill_bytes(2, 16384, 16, 128) / (c_mean * 1e-3) / 1e9
-                              / peaks["hbm_gbs"],
+                              "fp32_alu_frac": c_flops / (c_mean * 1e-3) / 1e12 / fp32_peak,
+                              "fp32_alu_peak_source": "152 SMs x 128 lanes x 2 flop x max SM clock",
                               "kernels": "l2c_state_kernel + l2c_kernel (one call)"}}
     del lq, lk, lv, lo, ws, wl
 
@@ -497,17 +498,19 @@ def run_gpu(args, rank, world, local):
         max(3, args.steps // 4), args.warmup, flush, counter=lib.rapt_launch_counter)
     g_mean = max_over_ranks(statistics.fmean(g_ms), device)
     g_flops = B * L * H * (12 * d * d)  # recurrence-form backward: q'S, S g, R v, R^T k', S and R updates
+    g_bytes = 7 * B * L * H * d * 2     # q, k, v, dout read; dq, dk, dv written (bf16)
     backward = {"value": world * B * L / (g_mean * 1e-3), "unit": "tokens/s", "ms_per_step": g_mean,
                 "workload": "rla2_causal_prefill backward B=4 L=4096 H=16 d=128 bf16 (dq, dk, dv, "
                             "dgamma_q, dgamma_k), the headline's inputs",
                 "launches_per_call": g_launch / max(3, args.steps // 4),
-                "roofline": {"bound": "alu", "achieved": g_flops / (g_mean * 1e-3) / 1e12,
-                             "peak": fp32_peak, "unit": "TFLOP/s",
-                             "frac": g_flops / (g_mean * 1e-3) / 1e12 / fp32_peak,
-                             "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x max SM clock",
-                             "algorithmic_flops_per_call": g_flops,
-                             "kernels": "bwd_state_kernel + bwd_forward_kernel + bwd_reverse_kernel "
-                                        "+ bwd_gain_kernel (one call)"}}
+                "roofline": {"bound": "hbm", "achieved": g_bytes / (g_mean * 1e-3) / 1e9,
+                             "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": g_bytes / (g_mean * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                             "peak_source": "measured hbm_gbs (copy bandwidth)",
+                             "algorithmic_bytes_per_call": g_bytes,
+                             "tensor_tflops_algorithmic": g_flops / (g_mean * 1e-3) / 1e12,
+                             "kernels": "segment_state_kernel + bwd_tc_forward + bwd_tc_revstate + "
+                                        "bwd_tc_reverse + bwd_gain_kernel (one call; tensor cores)"}}
     del tg, gws, grads
 
     # ---------------- one RAPT layer around the headline attention (d_model = H d = 2048), and its

@@ -201,8 +201,10 @@ rapt_status rapt_varlen_bwd(const void* q, const void* k, const void* v, const v
  *   eps       finite, > 0 (1e-6 on the page).
  *   workspace at least the matching *_workspace_size() bytes, 16-byte aligned (the states K'^T V and
  *             K'^T K' of the segments the documents are cut into; may be NULL when that size is 0).
- * All arithmetic is fp32 on CUDA cores for every dtype and d; bf16 outputs are rounded to nearest
- * even. Results are bitwise repeatable (fixed summation order).
+ * Dense bf16 with d = 128 runs on the tensor cores (bf16 operands, fp32 accumulation and states;
+ * the products with the states use bf16 copies of them; the sum of squared scores is fp32 from the
+ * exact bf16 features). Everything else (fp32, other d, varlen) is fp32 on CUDA cores. bf16
+ * outputs are rounded to nearest even. Results are bitwise repeatable (fixed summation order).
  */
 size_t rla_l2_causal_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype);
 rapt_status rla_l2_causal_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,

@@ -407,6 +407,15 @@ rapt_status l2_causal_common(const void* q, const void* k, const void* v, rapt_d
   if (workspace_bytes < need || (need > 0 && (workspace == nullptr || !aligned16(workspace))))
     return RAPT_ERR_WORKSPACE;
   if (total_rows == 0) return RAPT_OK;
+  if (cu_seqlens == nullptr && rapt::l2c_tc_supported(to_dt(dtype), d, false)) {
+    const rapt::L2cPlan plan = rapt::l2c_tc_plan(n_docs, doc_len, H);
+    rapt::L2Args a{};
+    a.q = q; a.k = k; a.v = v; a.out = out;
+    a.ws = static_cast<float*>(workspace);
+    a.B = n_docs; a.L = doc_len; a.H = H; a.eps = eps;
+    return from_cuda(rapt::launch_l2_causal_tc(a, plan.nseg, plan.seg_len,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+  }
   const rapt::L2cPlan plan = rapt::l2c_plan(n_docs, H, max_seqlen, d);
   rapt::L2cArgs b{};
   rapt::PrefillArgs& a = b.p;
@@ -426,6 +435,7 @@ rapt_status l2_causal_common(const void* q, const void* k, const void* v, rapt_d
 
 size_t rla_l2_causal_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype) {
   if (!known_dtype(dtype) || !supported_d(d) || B < 1 || H < 1 || L < 1) return 0;
+  if (rapt::l2c_tc_supported(to_dt(dtype), d, false)) return rapt::l2c_tc_plan(B, L, H).ws_bytes;
   return rapt::l2c_plan(B, H, L, d).ws_bytes;
 }
 

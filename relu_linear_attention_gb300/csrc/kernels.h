@@ -196,6 +196,14 @@ struct L2Args {
 };
 
 size_t l2_workspace_bytes(int B, int L, int H, int d);
+// The moments [K'^T V | K'^T K'] of every (batch row, head, split of split_len tokens) into a.ws as
+// fp32 partials (bf16, d = 128; float4 (i, 4c .. 4c+3) of a split at index c * d + i, 2d columns).
+cudaError_t launch_l2_moments_tc(const L2Args& a, int nsplit, int split_len, cudaStream_t stream);
+// Causal L2 on the tensor cores (dense bf16, d = 128): segments of seg_len tokens start from the
+// moments of the splits before them (ws, written by launch_l2_moments_tc with split_len = seg_len).
+bool l2c_tc_supported(DType dt, int d, bool varlen);
+L2cPlan l2c_tc_plan(int B, int L, int H);
+cudaError_t launch_l2_causal_tc(const L2Args& a, int nseg, int seg_len, cudaStream_t stream);
 cudaError_t launch_rla_l2(DType dt, int d, const L2Args& a, cudaStream_t stream);
 
 // Split count launch_rla_l2 would choose, and the launch with an explicit split count
