@@ -223,7 +223,7 @@ def time_steps(fn, steps, warmup, flush, min_warm_s=0.0, counter=None):
     t0 = time.perf_counter()
     i = 0
     while i < warmup or (time.perf_counter() - t0) < min_warm_s:
-        flush.zero_()
+        flush()
         fn()
         i += 1
         if i % 16 == 0:
@@ -232,7 +232,7 @@ def time_steps(fn, steps, warmup, flush, min_warm_s=0.0, counter=None):
     ev0, ev1 = _events(steps), _events(steps)
     c0 = counter() if counter else 0
     for s in range(steps):
-        flush.zero_()
+        flush()
         ev0[s].record()
         fn()
         ev1[s].record()
@@ -319,7 +319,16 @@ def run_gpu(args, rank, world, local):
     if world > 1:
         dist.init_process_group("nccl", device_id=device)
     peaks, peak_src = load_peaks()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    # L2 flush before every timed step: write a buffer larger than L2, then read another one, so
+    # that the timed step starts with none of its data in L2 and with no dirty flush lines left to
+    # write back inside its events
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    flush_sink = torch.empty((), dtype=torch.float32, device=device)
+
+    def flush():
+        flush_w.zero_()
+        torch.sum(flush_r, dim=0, out=flush_sink)
 
     # ---------------- headline: dense causal prefill
     B, L, H, d = WORKLOAD["B"], WORKLOAD["L"], WORKLOAD["H"], WORKLOAD["d"]
@@ -569,7 +578,7 @@ def run_gpu(args, rank, world, local):
                    "model": "RLA-2/RAPT attention layer (no projections)", "global_batch": B * world,
                    "seq_len": L, "heads": H, "d_head": d,
                    "parallelism": "dp%d (independent batch per GPU)" % world,
-                   "l2": "256 MiB write before every timed step, outside the CUDA events"},
+                   "l2": "256 MiB write, then 256 MiB read, before every timed step, outside the CUDA events"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "kernels": "segment_state_kernel + prefill_tc_kernel (one call; the second is "
