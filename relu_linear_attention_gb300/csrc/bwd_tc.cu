@@ -96,28 +96,122 @@ __device__ __forceinline__ void load_rows(const __nv_bfloat16* x, long row0, int
   }
 }
 
+// RoPE rotations of a lane's two pairs (elements 4 lane .. 4 lane + 3 are pairs 2 lane, 2 lane + 1)
+// for the rows a warp takes (positions p, p + 16, ...): exact sin / cos at the chunk's first row of
+// the warp, then one complex multiplication by the rotation over 16 positions per row.
+struct LaneRope {
+  float c[2], s[2];    // the current row
+  float cs[2], ss[2];  // the step over kWarps positions
+};
+__device__ __forceinline__ void rope_start(LaneRope& r, int pos, const FeatureArgs& fa, int lane) {
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const int j = 2 * lane + m;
+    rope_sincos(pos, fa.rope_hi[j], fa.rope_lo[j], r.s[m], r.c[m]);
+    rope_sincos(kWarps, fa.rope_hi[j], fa.rope_lo[j], r.ss[m], r.cs[m]);
+  }
+}
+__device__ __forceinline__ void rope_next(LaneRope& r) {
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const float c = fmaf(r.c[m], r.cs[m], -r.s[m] * r.ss[m]);
+    const float s = fmaf(r.s[m], r.cs[m], r.c[m] * r.ss[m]);
+    r.c[m] = c;
+    r.s[m] = s;
+  }
+}
+
+// f = ReLU(RoPE(RMSNorm(x))) of one row on a lane's four elements (the warp together: the row's sum
+// of squares is reduced by shuffles); g: the lane's four gains.
+__device__ __forceinline__ void feat_lane(float (&f)[4], bool valid, const float (&g)[4],
+                                          const LaneRope& r, float eps) {
+  float ss = f[0] * f[0] + f[1] * f[1] + f[2] * f[2] + f[3] * f[3];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  const float rinv = rsqrtf(ss * (1.0f / kD) + eps);
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const float y0 = f[2 * m] * rinv * g[2 * m];
+    const float y1 = f[2 * m + 1] * rinv * g[2 * m + 1];
+    const float a = fmaf(y0, r.c[m], -y1 * r.s[m]);
+    const float b = fmaf(y0, r.s[m], y1 * r.c[m]);
+    f[2 * m] = valid ? fmaxf(a, 0.f) : 0.f;
+    f[2 * m + 1] = valid ? fmaxf(b, 0.f) : 0.f;
+  }
+}
+
+// Backward of feat_lane for one row (x values in f, the row's gradient of the features in df):
+// writes dx (valid rows) and adds the gain gradient to dg.
+__device__ __forceinline__ void feat_lane_bwd(const float (&f)[4], bool valid, const float (&g)[4],
+                                              const LaneRope& r, float eps, const float* df,
+                                              __nv_bfloat16* dx, float (&dg)[4]) {
+  float ss = f[0] * f[0] + f[1] * f[1] + f[2] * f[2] + f[3] * f[3];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  const float rinv = rsqrtf(ss * (1.0f / kD) + eps);
+  float u[4], dot = 0.f;
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const float y0 = f[2 * m] * rinv * g[2 * m];
+    const float y1 = f[2 * m + 1] * rinv * g[2 * m + 1];
+    const float a = fmaf(y0, r.c[m], -y1 * r.s[m]);  // the forward's pre-activation
+    const float b = fmaf(y0, r.s[m], y1 * r.c[m]);
+    const float da = (valid && a > 0.f) ? df[2 * m] : 0.f;
+    const float db = (valid && b > 0.f) ? df[2 * m + 1] : 0.f;
+    const float h0 = fmaf(da, r.c[m], db * r.s[m]);  // inverse rotation
+    const float h1 = fmaf(-da, r.s[m], db * r.c[m]);
+    dg[2 * m] = fmaf(h0, f[2 * m] * rinv, dg[2 * m]);
+    dg[2 * m + 1] = fmaf(h1, f[2 * m + 1] * rinv, dg[2 * m + 1]);
+    u[2 * m] = g[2 * m] * h0;
+    u[2 * m + 1] = g[2 * m + 1] * h1;
+    dot = fmaf(u[2 * m], f[2 * m], dot);
+    dot = fmaf(u[2 * m + 1], f[2 * m + 1], dot);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+  const float c3 = rinv * rinv * rinv * dot * (1.0f / kD);
+  if (valid) {
+    const uint32_t lo = tc::pack_bf16x2(fmaf(rinv, u[0], -f[0] * c3), fmaf(rinv, u[1], -f[1] * c3));
+    const uint32_t hi = tc::pack_bf16x2(fmaf(rinv, u[2], -f[2] * c3), fmaf(rinv, u[3], -f[3] * c3));
+    *reinterpret_cast<uint2*>(dx) = make_uint2(lo, hi);
+  }
+}
+
+__device__ __forceinline__ void lane_gains(const float* gamma, int lane, float (&g)[4]) {
+  const float4 v = *reinterpret_cast<const float4*>(gamma + 4 * lane);
+  g[0] = v.x; g[1] = v.y; g[2] = v.z; g[3] = v.w;
+}
+
 __device__ __forceinline__ void feature_tile_tc(const __nv_bfloat16* x, long row0, int n, int t0,
                                                 int H, int h, const float* gamma, int pos0,
                                                 const FeatureArgs& fa, uint32_t tile,
                                                 const float* z, float* sst, float (&zc)[4],
                                                 __nv_bfloat16* out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float f[kRPW][4];
+  float f[kRPW][4], g[4];
   load_rows(x, row0, n, t0, H, h, f);
+  lane_gains(gamma, lane, g);
+  LaneRope rope;
+  rope_start(rope, pos0 + t0 + warp, fa, lane);
+  float zl[4] = {0.f, 0.f, 0.f, 0.f};
+  if (z != nullptr) {
+    const float4 zz = *reinterpret_cast<const float4*>(z + 4 * lane);
+    zl[0] = zz.x; zl[1] = zz.y; zl[2] = zz.z; zl[3] = zz.w;
+  }
 #pragma unroll 2
   for (int i = 0; i < kRPW; ++i) {
     const int rr = warp + kWarps * i;
     const int t = t0 + rr;
     const bool valid = t < n;
-    feature_vals<kD>(f[i], valid, gamma, pos0 + t, fa, lane);
+    if (i > 0) rope_next(rope);
+    feat_lane(f[i], valid, g, rope, fa.eps_norm);
     const uint32_t addr = tile + tile_off(rr, lane >> 1) + (lane & 1) * 8;
     const uint32_t lo = tc::pack_bf16x2(f[i][0], f[i][1]), hi = tc::pack_bf16x2(f[i][2], f[i][3]);
     asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(lo), "r"(hi) : "memory");
     if (out != nullptr && valid)
       *reinterpret_cast<uint2*>(out + ((row0 + t) * H + h) * kD + 4 * lane) = make_uint2(lo, hi);
     if (z != nullptr) {
-      float s = f[i][0] * z[4 * lane] + f[i][1] * z[4 * lane + 1] + f[i][2] * z[4 * lane + 2] +
-                f[i][3] * z[4 * lane + 3];
+      float s = f[i][0] * zl[0] + f[i][1] * zl[1] + f[i][2] * zl[2] + f[i][3] * zl[3];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
       if (lane == 0) sst[rr] = valid ? s : 0.f;
@@ -128,23 +222,27 @@ __device__ __forceinline__ void feature_tile_tc(const __nv_bfloat16* x, long row
 }
 
 // Back through the features of the chunk's rows of x (q or k): warp w takes rows w, w + 16, ...
-// with their loads issued first; df rows come from the fp32 staging.
+// (the rows and rotations of feature_tile_tc) with their loads issued first; df rows come from the
+// fp32 staging.
 __device__ __forceinline__ void feature_tile_bwd_tc(const __nv_bfloat16* x, long row0, int n,
                                                     int t0, int H, int h, const float* gamma,
                                                     int pos0, const FeatureArgs& fa,
                                                     const float* stg, __nv_bfloat16* dx,
                                                     float (&dg)[4]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float f[kRPW][4];
+  float f[kRPW][4], g[4];
   load_rows(x, row0, n, t0, H, h, f);
+  lane_gains(gamma, lane, g);
+  LaneRope rope;
+  rope_start(rope, pos0 + t0 + warp, fa, lane);
 #pragma unroll 2
   for (int i = 0; i < kRPW; ++i) {
     const int rr = warp + kWarps * i;
     const int t = t0 + rr;
     const bool valid = t < n;
-    const long off = ((row0 + (valid ? t : 0)) * H + h) * kD;
-    feature_vals_bwd<kD, __nv_bfloat16>(f[i], valid, gamma, pos0 + t, fa, lane, stg + rr * kSL,
-                                        dx + off, dg);
+    if (i > 0) rope_next(rope);
+    const long off = ((row0 + (valid ? t : 0)) * H + h) * kD + 4 * lane;
+    feat_lane_bwd(f[i], valid, g, rope, fa.eps_norm, stg + rr * kSL + 4 * lane, dx + off, dg);
   }
 }
 
