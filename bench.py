@@ -476,7 +476,8 @@ def run_gpu(args, rank, world, local):
                               "algorithmic_flops_per_call": c_flops,
                               "fp32_alu_frac": c_flops / (c_mean * 1e-3) / 1e12 / fp32_peak,
                               "fp32_alu_peak_source": "152 SMs x 128 lanes x 2 flop x max SM clock",
-                              "kernels": "l2c_state_kernel + l2c_kernel (one call)"}}
+                              "traffic": read_traffic("l2_causal", "l2_tc_moments", "l2c_tc_kernel"),
+                              "kernels": "l2_tc_moments + l2c_tc_kernel (one call; tensor cores)"}}
     del lq, lk, lv, lo, ws, wl
 
     # ---------------- bidirectional RLA-2 on the headline's inputs (B=4, L=4096, H=16, d=128)
@@ -518,6 +519,9 @@ def run_gpu(args, rank, world, local):
                              "peak_source": "measured hbm_gbs (copy bandwidth)",
                              "algorithmic_bytes_per_call": g_bytes,
                              "tensor_tflops_algorithmic": g_flops / (g_mean * 1e-3) / 1e12,
+                             "traffic": read_traffic("backward", "segment_state_kernel",
+                                                     "bwd_tc_forward", "bwd_tc_revstate",
+                                                     "bwd_tc_reverse", "bwd_gain_kernel"),
                              "kernels": "segment_state_kernel + bwd_tc_forward + bwd_tc_revstate + "
                                         "bwd_tc_reverse + bwd_gain_kernel (one call; tensor cores)"}}
     del tg, gws, grads
@@ -556,6 +560,7 @@ def run_gpu(args, rank, world, local):
                                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                          "frac": p_flops / (p_mean * 1e-3) / 1e12 / peaks["bf16_tflops"],
                                          "peak_source": "measured bf16_tflops (cuBLAS burst)",
+                                         "traffic": read_traffic("linear", "linear_tc_kernel"),
                                          "kernels": "linear_tc_kernel"}}}
     del x, w_qkv, w_o, y, lws, qkv_out, x2
 
