@@ -60,8 +60,8 @@ struct Lay {
   static constexpr uint32_t ZP = ZS + kD * 4;                 // per-warp k' column sums [16][D]
   static constexpr uint32_t ROW = ZP + kWarps * kD * 4;       // den, scale, sst, nst [4][128]
   static constexpr uint32_t RED = ROW + 4 * kC * 4;           // partial row sums [3][4][128]
-  static constexpr uint32_t BAR = RED + 3 * 4 * kC * 4;       // three mbarriers
-  static constexpr uint32_t MISC = BAR + 3 * 8;               // TMEM base, abort flag
+  static constexpr uint32_t BAR = RED + 3 * 4 * kC * 4;       // four mbarriers
+  static constexpr uint32_t MISC = BAR + 4 * 8;               // TMEM base, abort flag
   static constexpr uint32_t BYTES = MISC + 16;
   static_assert(static_cast<uint32_t>(kC) * kSL * 4 <= 3 * kTile, "staging fits over QF..VS");
   static_assert(BYTES <= 232448, "shared memory budget");
@@ -78,18 +78,21 @@ constexpr uint32_t kTDV = 0, kTDK = 128, kTR = 256;           // pass B: dv (ove
 // ([T, H, D], for pass B).
 constexpr int kRPW = kC / kWarps;  // rows per warp
 
+constexpr int kRB = kRPW / 2;  // rows of a warp loaded together (two batches per tile)
+
+// Rows i0, i0 + 1, ... (of this warp's rows w + 16 i) of x, as floats.
 __device__ __forceinline__ void load_rows(const __nv_bfloat16* x, long row0, int n, int t0, int H,
-                                          int h, float (&f)[kRPW][4]) {
+                                          int h, int i0, float (&f)[kRB][4]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint2 raw[kRPW];
+  uint2 raw[kRB];
 #pragma unroll
-  for (int i = 0; i < kRPW; ++i) {
-    const int t = t0 + warp + kWarps * i;
+  for (int i = 0; i < kRB; ++i) {
+    const int t = t0 + warp + kWarps * (i0 + i);
     raw[i] = t < n ? __ldg(reinterpret_cast<const uint2*>(x + ((row0 + t) * H + h) * kD + 4 * lane))
                    : make_uint2(0, 0);
   }
 #pragma unroll
-  for (int i = 0; i < kRPW; ++i) {
+  for (int i = 0; i < kRB; ++i) {
     const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[i].x));
     const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[i].y));
     f[i][0] = a.x; f[i][1] = a.y; f[i][2] = b.x; f[i][3] = b.y;
@@ -188,8 +191,7 @@ __device__ __forceinline__ void feature_tile_tc(const __nv_bfloat16* x, long row
                                                 const float* z, float* sst, float (&zc)[4],
                                                 __nv_bfloat16* out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float f[kRPW][4], g[4];
-  load_rows(x, row0, n, t0, H, h, f);
+  float g[4];
   lane_gains(gamma, lane, g);
   LaneRope rope;
   rope_start(rope, pos0 + t0 + warp, fa, lane);
@@ -198,12 +200,17 @@ __device__ __forceinline__ void feature_tile_tc(const __nv_bfloat16* x, long row
     const float4 zz = *reinterpret_cast<const float4*>(z + 4 * lane);
     zl[0] = zz.x; zl[1] = zz.y; zl[2] = zz.z; zl[3] = zz.w;
   }
-#pragma unroll 2
-  for (int i = 0; i < kRPW; ++i) {
-    const int rr = warp + kWarps * i;
+#pragma unroll 1
+  for (int i0 = 0; i0 < kRPW; i0 += kRB) {
+  float f[kRB][4];
+  load_rows(x, row0, n, t0, H, h, i0, f);
+#pragma unroll
+  for (int ii = 0; ii < kRB; ++ii) {
+    const int i = ii;
+    const int rr = warp + kWarps * (i0 + ii);
     const int t = t0 + rr;
     const bool valid = t < n;
-    if (i > 0) rope_next(rope);
+    if (i0 + ii > 0) rope_next(rope);
     feat_lane(f[i], valid, g, rope, fa.eps_norm);
     const uint32_t addr = tile + tile_off(rr, lane >> 1) + (lane & 1) * 8;
     const uint32_t lo = tc::pack_bf16x2(f[i][0], f[i][1]), hi = tc::pack_bf16x2(f[i][2], f[i][3]);
@@ -219,6 +226,7 @@ __device__ __forceinline__ void feature_tile_tc(const __nv_bfloat16* x, long row
 #pragma unroll
     for (int e = 0; e < 4; ++e) zc[e] += f[i][e];
   }
+  }
 }
 
 // Back through the features of the chunk's rows of x (q or k): warp w takes rows w, w + 16, ...
@@ -230,19 +238,23 @@ __device__ __forceinline__ void feature_tile_bwd_tc(const __nv_bfloat16* x, long
                                                     const float* stg, __nv_bfloat16* dx,
                                                     float (&dg)[4]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float f[kRPW][4], g[4];
-  load_rows(x, row0, n, t0, H, h, f);
+  float g[4];
   lane_gains(gamma, lane, g);
   LaneRope rope;
   rope_start(rope, pos0 + t0 + warp, fa, lane);
-#pragma unroll 2
-  for (int i = 0; i < kRPW; ++i) {
-    const int rr = warp + kWarps * i;
-    const int t = t0 + rr;
-    const bool valid = t < n;
-    if (i > 0) rope_next(rope);
-    const long off = ((row0 + (valid ? t : 0)) * H + h) * kD + 4 * lane;
-    feat_lane_bwd(f[i], valid, g, rope, fa.eps_norm, stg + rr * kSL + 4 * lane, dx + off, dg);
+#pragma unroll 1
+  for (int i0 = 0; i0 < kRPW; i0 += kRB) {
+    float f[kRB][4];
+    load_rows(x, row0, n, t0, H, h, i0, f);
+#pragma unroll
+    for (int ii = 0; ii < kRB; ++ii) {
+      const int rr = warp + kWarps * (i0 + ii);
+      const int t = t0 + rr;
+      const bool valid = t < n;
+      if (i0 + ii > 0) rope_next(rope);
+      const long off = ((row0 + (valid ? t : 0)) * H + h) * kD + 4 * lane;
+      feat_lane_bwd(f[ii], valid, g, rope, fa.eps_norm, stg + rr * kSL + 4 * lane, dx + off, dg);
+    }
   }
 }
 
@@ -288,6 +300,16 @@ __device__ __forceinline__ void store_gain(const float (&dg)[4], float* scratch,
   }
 }
 
+// L2 prefetch of the 128 rows of a chunk of x (one 128-byte line per thread and call; two calls
+// per tensor), so that the next chunk's loads do not wait for DRAM.
+__device__ __forceinline__ void prefetch_rows(const __nv_bfloat16* x, long row0, int n, int t0,
+                                              int H, int h, int part) {
+  const int idx = threadIdx.x + kThreads * part;  // 0 .. 2 kThreads - 1 over two calls
+  const int r = idx >> 1;
+  if (r < kC && t0 + r < n)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(x + ((row0 + t0 + r) * H + h) * kD + 64 * (idx & 1)));
+}
+
 // ------------------------------------------------------------------------------------------------
 // Pass A: chunks in order.
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
@@ -311,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
   float* sst_s = scl_s + kC;
   float* red = reinterpret_cast<float*>(smem + Lay::RED);
   float* stg = reinterpret_cast<float*>(smem + Lay::STG);
-  const uint32_t bar1 = base + Lay::BAR, bar2 = bar1 + 8;
+  const uint32_t bar1 = base + Lay::BAR, bar2 = bar1 + 8, bar1b = bar1 + 16;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + Lay::MISC);
   int* s_abort = reinterpret_cast<int*>(smem + Lay::MISC + 4);
   const bool misaligned = (base & 1023u) != 0;
@@ -323,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
   if (tid == 0) {
     tc::mbar_init(bar1, 1);
     tc::mbar_init(bar2, 1);
+    tc::mbar_init(bar1b, 1);
     tc::mbar_fence_init();
     *s_abort = misaligned ? 1 : 0;
   }
@@ -396,13 +419,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
       for (int kk = 0; kk < kD / 16; ++kk) {
         tc::mma_bf16(tmem + kTP, kmaj(base + Lay::QF, kk), kmaj(base + Lay::KF, kk), ID_KK, kk > 0);
         tc::mma_bf16(tmem + kTG, kmaj(base + Lay::GS, kk), kmaj(base + Lay::VS, kk), ID_KK, kk > 0);
-        tc::mma_bf16(tmem + kTU, kmaj(base + Lay::GS, kk), kmaj_d(base + Lay::XS, kk), ID_KK, kk > 0);
       }
+      tc::mma_commit(bar1);  // P and Cv: the row sums can start
+#pragma unroll 1
+      for (int kk = 0; kk < kD / 16; ++kk)
+        tc::mma_bf16(tmem + kTU, kmaj(base + Lay::GS, kk), kmaj_d(base + Lay::XS, kk), ID_KK, kk > 0);
+      tc::mma_commit(bar1b);
+      // the state update is waited for only through bar2 (phase 4 commits after it)
 #pragma unroll 1
       for (int kk = 0; kk < kC / 16; ++kk)
         tc::mma_bf16(tmem + kTS, mnmaj(base + Lay::KF, kk, 16384), mnmaj(base + Lay::VS, kk, 16384),
                      ID_MM, 1u);
-      tc::mma_commit(bar1);
+    }
+    if (c + 1 < nch) {  // the next chunk's rows into L2 while the tensor core works
+      for (int part = 0; part < 2; ++part) {
+        prefetch_rows(q, row0, n, t0 + kC, a.H, h, part);
+        prefetch_rows(k, row0, n, t0 + kC, a.H, h, part);
+        prefetch_rows(v, row0, n, t0 + kC, a.H, h, part);
+        prefetch_rows(g, row0, n, t0 + kC, a.H, h, part);
+      }
     }
     if (!wait_mma(bar1, c & 1)) atomicExch(s_abort, 1);
     // ---- phase 3: row sums, den, scale, A'
@@ -418,6 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
       pc += vis ? pv[j] * cv[j] : 0.f;
     }
     float nst = 0.f;
+    if (!wait_mma(bar1b, c & 1)) atomicExch(s_abort, 1);
     {
       float u[32];
       tmem_ld32(tmem + tl + kTU + 32 * gw, u);
@@ -538,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
   float* nst_s = sst_s + kC;
   float* red = reinterpret_cast<float*>(smem + Lay::RED);
   float* stg = reinterpret_cast<float*>(smem + Lay::STG);
-  const uint32_t bar1 = base + Lay::BAR, bar2 = bar1 + 8, bar3 = bar2 + 8;
+  const uint32_t bar1 = base + Lay::BAR, bar2 = bar1 + 8, bar3 = bar2 + 8, bar4 = bar3 + 8;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + Lay::MISC);
   int* s_abort = reinterpret_cast<int*>(smem + Lay::MISC + 4);
   const bool misaligned = (base & 1023u) != 0;
@@ -551,6 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
     tc::mbar_init(bar1, 1);
     tc::mbar_init(bar2, 1);
     tc::mbar_init(bar3, 1);
+    tc::mbar_init(bar4, 1);
     tc::mbar_fence_init();
     *s_abort = misaligned ? 1 : 0;
   }
@@ -707,11 +744,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
 #pragma unroll 1
       for (int kk = 0; kk < kD / 16; ++kk)
         tc::mma_bf16(tmem + kTDK, kmaj(base + Lay::VS, kk), kmaj_d(base + Lay::XS, kk), ID_KK, 1u);
+      tc::mma_commit(bar3);  // dk' done: its read-out can start while R is updated
 #pragma unroll 1
       for (int kk = 0; kk < kC / 16; ++kk)
         tc::mma_bf16(tmem + kTR, mnmaj(base + Lay::QF, kk, 16384), mnmaj(base + Lay::GS, kk, 16384),
                      ID_MM, 1u);
-      tc::mma_commit(bar3);
+      tc::mma_commit(bar4);
+    }
+    if (c > 0) {  // the next (earlier) chunk's rows into L2 while the tensor core works
+      for (int part = 0; part < 2; ++part) {
+        prefetch_rows(qf_in, row0, n, t0 - kC, a.H, h, part);
+        prefetch_rows(kf_in, row0, n, t0 - kC, a.H, h, part);
+        prefetch_rows(v, row0, n, t0 - kC, a.H, h, part);
+        prefetch_rows(g, row0, n, t0 - kC, a.H, h, part);
+        prefetch_rows(k, row0, n, t0 - kC, a.H, h, part);
+      }
     }
     if (!wait_mma(bar3, it & 1)) atomicExch(s_abort, 1);
     // ---- phase 7: dk' + w into the staging, w += sum_t scale_t q'_t, R -> R~
@@ -736,6 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
         }
         red[(tid >> 7) * kC + i] = dw;
       }
+      if (!wait_mma(bar4, it & 1)) atomicExch(s_abort, 1);  // R updated; q', gnum read
       tc::fence_before_sync();
       __syncthreads();  // q' and w are read; the staging may overlay q', k', v
 #pragma unroll
