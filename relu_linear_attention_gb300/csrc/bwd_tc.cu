@@ -258,35 +258,6 @@ __device__ __forceinline__ void feature_tile_bwd_tc(const __nv_bfloat16* x, long
   }
 }
 
-// Raw rows of v (or g) into a bf16 tile (rows past the document are zero); with den given, every
-// row is divided by its den (gnum = g / den) and rounded to bf16.
-__device__ __forceinline__ void raw_tile_tc(const __nv_bfloat16* x, long row0, int n, int t0, int H,
-                                            int h, uint32_t tile, const float* den) {
-  constexpr int kPer = kC * 16 / kThreads;  // 16-byte chunks per thread
-  uint4 v[kPer];
-  float dn[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int idx = threadIdx.x + kThreads * i, r = idx >> 4, m = idx & 15;
-    const bool valid = t0 + r < n;
-    v[i] = valid ? ldg16(x + ((row0 + t0 + r) * H + h) * kD + 8 * m) : make_uint4(0, 0, 0, 0);
-    dn[i] = (den != nullptr && valid) ? den[(row0 + t0 + r) * H + h] : 1.f;
-  }
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int idx = threadIdx.x + kThreads * i, r = idx >> 4, m = idx & 15;
-    if (den != nullptr) {
-      float f[8];
-      unpack8(v[i], f);
-      const float inv = 1.0f / dn[i];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] *= inv;
-      v[i] = feat::pack8(f);
-    }
-    sts16(tile + tile_off(r, m), v[i]);
-  }
-}
-
 // Gain partials of this CTA (each lane's dg over the rows it took) summed over the warps in order.
 __device__ __forceinline__ void store_gain(const float (&dg)[4], float* scratch, float* out, bool bad) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -297,6 +268,42 @@ __device__ __forceinline__ void store_gain(const float (&dg)[4], float* scratch,
     float s = 0.f;
     for (int w = 0; w < kWarps; ++w) s += scratch[w * kD + threadIdx.x];
     out[threadIdx.x] = bad ? __int_as_float(0x7fc00000) : s;
+  }
+}
+
+// Several raw tiles at once (all loads in flight before any is stored): tile i gets rows of src[i];
+// with dv[i] set, its rows are divided by their den (gnum = g / den) and rounded to bf16.
+template <int NT>
+__device__ __forceinline__ void raw_tiles_tc(const __nv_bfloat16* const (&src)[NT],
+                                             const uint32_t (&tile)[NT], const bool (&dv)[NT],
+                                             long row0, int n, int t0, int H, int h, const float* den) {
+  constexpr int kPer = kC * 16 / kThreads;
+  uint4 v[NT][kPer];
+  float dn[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int idx = threadIdx.x + kThreads * i, r = idx >> 4, m = idx & 15;
+    const bool valid = t0 + r < n;
+#pragma unroll
+    for (int x = 0; x < NT; ++x)
+      v[x][i] = valid ? ldg16(src[x] + ((row0 + t0 + r) * H + h) * kD + 8 * m) : make_uint4(0, 0, 0, 0);
+    dn[i] = (den != nullptr && valid) ? den[(row0 + t0 + r) * H + h] : 1.f;
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int idx = threadIdx.x + kThreads * i, r = idx >> 4, m = idx & 15;
+#pragma unroll
+    for (int x = 0; x < NT; ++x) {
+      if (dv[x]) {
+        float f[8];
+        unpack8(v[x][i], f);
+        const float inv = 1.0f / dn[i];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] *= inv;
+        v[x][i] = feat::pack8(f);
+      }
+      sts16(tile[x] + tile_off(r, m), v[x][i]);
+    }
   }
 }
 
@@ -405,8 +412,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
                     nullptr, zc, kf_out);
 #pragma unroll
     for (int e = 0; e < 4; ++e) zp[warp * kD + 4 * lane + e] = zc[e];
-    raw_tile_tc(v, row0, n, t0, a.H, h, base + Lay::VS, nullptr);
-    raw_tile_tc(g, row0, n, t0, a.H, h, base + Lay::GS, nullptr);
+    {
+      const __nv_bfloat16* const src[2] = {v, g};
+      const uint32_t tiles[2] = {base + Lay::VS, base + Lay::GS};
+      const bool dv[2] = {false, false};
+      raw_tiles_tc<2>(src, tiles, dv, row0, n, t0, a.H, h, nullptr);
+    }
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
@@ -641,10 +652,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
   for (int c = nch - 1; c >= 0 && !bad; --c, ++it) {
     const int t0 = s0 + c * kC;
     // ---- phase 1: q', k' (stored by pass A), v, gnum = g / den, and the row scalars of pass A
-    raw_tile_tc(qf_in, row0, n, t0, a.H, h, base + Lay::QF, nullptr);
-    raw_tile_tc(kf_in, row0, n, t0, a.H, h, base + Lay::KF, nullptr);
-    raw_tile_tc(v, row0, n, t0, a.H, h, base + Lay::VS, nullptr);
-    raw_tile_tc(g, row0, n, t0, a.H, h, base + Lay::GS, b.den);
+    {
+      const __nv_bfloat16* const src[4] = {qf_in, kf_in, v, g};
+      const uint32_t tiles[4] = {base + Lay::QF, base + Lay::KF, base + Lay::VS, base + Lay::GS};
+      const bool dv[4] = {false, false, false, true};
+      raw_tiles_tc<4>(src, tiles, dv, row0, n, t0, a.H, h, b.den);
+    }
     if (tid < kC) {
       const bool vr = t0 + tid < n;
       const long o = (row0 + t0 + tid) * a.H + h;
@@ -855,8 +868,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_revstate(const BwdArgs b) 
   bool bad = *s_abort != 0;
   for (int c = 0; c < nch && !bad; ++c) {
     const int t0 = s0 + c * kC;
-    raw_tile_tc(qf_in, row0, n, t0, a.H, h, base + Lay::QF, nullptr);
-    raw_tile_tc(g, row0, n, t0, a.H, h, base + Lay::GS, b.den);
+    {
+      const __nv_bfloat16* const src[2] = {qf_in, g};
+      const uint32_t tiles[2] = {base + Lay::QF, base + Lay::GS};
+      const bool dv[2] = {false, true};
+      raw_tiles_tc<2>(src, tiles, dv, row0, n, t0, a.H, h, b.den);
+    }
     if (tid < kC) scl_s[tid] = t0 + tid < n ? b.scl[(row0 + t0 + tid) * a.H + h] : 0.f;
     tc::fence_async_smem();
     tc::fence_before_sync();

@@ -48,29 +48,56 @@ struct LayC {
 constexpr uint32_t kTP = 0, kTX = 128, kTS = 256, kTA = 384;  // TMEM columns: P, X, S, A
 
 // Raw rows of x into a bf16 tile (rows past the batch row's L are zero), optionally rectified.
-__device__ __forceinline__ void load_tile(const __nv_bfloat16* x, long row0, int n, int t0, int H,
-                                          int h, uint32_t tile, bool relu) {
+// The chunk's rows of q, k and v into their bf16 tiles, all loads in flight before any store; q and
+// k rectified (bf16 max(0, x) on the bit patterns: a set sign bit, negative or -0, becomes +0).
+__device__ __forceinline__ void load_tiles(const __nv_bfloat16* q, const __nv_bfloat16* k,
+                                           const __nv_bfloat16* vv, long row0, int n, int t0, int H,
+                                           int h, uint32_t base) {
   constexpr int kPer = kC * 16 / kThreads;
-  uint4 v[kPer];
+  const __nv_bfloat16* src[3] = {q, k, vv};
+  const uint32_t tile[3] = {base + LayC::QF, base + LayC::KF, base + LayC::VS};
+  uint4 v[3][kPer];
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int idx = threadIdx.x + kThreads * i, r = idx >> 4, m = idx & 15;
-    v[i] = t0 + r < n ? ldg16(x + ((row0 + t0 + r) * H + h) * kD + 8 * m) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int x = 0; x < 3; ++x)
+      v[x][i] = t0 + r < n ? ldg16(src[x] + ((row0 + t0 + r) * H + h) * kD + 8 * m)
+                           : make_uint4(0, 0, 0, 0);
   }
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int idx = threadIdx.x + kThreads * i, r = idx >> 4, m = idx & 15;
-    if (relu) {  // bf16 max(0, x) on the bit patterns: a set sign bit (negative, -0) becomes +0
-      uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t lo = (w[e] & 0x8000u) ? 0u : (w[e] & 0xFFFFu);
-        const uint32_t hi = (w[e] & 0x80000000u) ? 0u : (w[e] & 0xFFFF0000u);
-        w[e] = lo | hi;
+    for (int x = 0; x < 3; ++x) {
+      if (x < 2) {
+        uint32_t w[4] = {v[x][i].x, v[x][i].y, v[x][i].z, v[x][i].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t lo = (w[e] & 0x8000u) ? 0u : (w[e] & 0xFFFFu);
+          const uint32_t hi = (w[e] & 0x80000000u) ? 0u : (w[e] & 0xFFFF0000u);
+          w[e] = lo | hi;
+        }
+        v[x][i] = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      v[i] = make_uint4(w[0], w[1], w[2], w[3]);
+      sts16(tile[x] + tile_off(r, m), v[x][i]);
     }
-    sts16(tile + tile_off(r, m), v[i]);
+  }
+}
+
+// L2 prefetch of a chunk's rows of q, k and v (so that the next chunk's loads do not wait for DRAM).
+__device__ __forceinline__ void prefetch_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k,
+                                               const __nv_bfloat16* v, long row0, int n, int t0,
+                                               int H, int h) {
+  const int r = threadIdx.x >> 2, part = threadIdx.x & 3;  // 128 rows x 2 lines, 3 tensors
+  if (r < kC && t0 + r < n) {
+    const long off = ((row0 + t0 + r) * H + h) * kD + 64 * (part & 1);
+    if (part < 2) {
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(q + off));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(k + off));
+    } else {
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(v + off));
+    }
   }
 }
 
@@ -143,9 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int c = 0; c < nch && !bad; ++c) {
     const int t0 = s0 + c * kC;
     // ---- phase 1: q' = ReLU(q), k' = ReLU(k), v
-    load_tile(q, row0, n, t0, a.H, h, base + LayC::QF, true);
-    load_tile(k, row0, n, t0, a.H, h, base + LayC::KF, true);
-    load_tile(v, row0, n, t0, a.H, h, base + LayC::VS, false);
+    load_tiles(q, k, v, row0, n, t0, a.H, h, base);
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
@@ -170,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::mma_commit(bar1);
     }
+    if (c + 1 < nch) prefetch_chunk(q, k, v, row0, n, t0 + kC, a.H, h);
     if (!wait_mma(bar1, c & 1)) atomicExch(s_abort, 1);
     // ---- phase 3: den^2 = sum P^2 + q' . X;  P~ (masked, bf16)
     float den;
