@@ -178,3 +178,51 @@ def test_prefill_bwd_without_gains_and_empty(cuda_device, lib):
     _, _, _, dgq, dgk = R.rapt_prefill_bwd(z, z, z, z, dev(gq), dev(gk))
     torch.cuda.synchronize()
     assert torch.all(dgq == 0) and torch.all(dgk == 0)
+
+
+@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (32, "f32")])
+def test_varlen_bwd_reports_malformed_cu_seqlens(cuda_device, lib, d, dtype):
+    """A decreasing cu_seqlens is reported through dev_status; the well-formed first document is
+    still differentiated correctly and nothing is read or written out of bounds."""
+    T, H = 300, 2
+    q, k, v = draw(350 + d, (T, H, d), dtype)
+    (g,) = draw(351 + d, (T, H, d), dtype)[:1]
+    gq, gk = gammas(352, H, d, True)
+    dev = lambda x: torch.from_numpy(x).to(cuda_device)
+    cu = torch.tensor([0, 200, 150, T], dtype=torch.int32, device=cuda_device)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    dq, dk, dv, _, _ = R.rapt_varlen_bwd(to_dev(q, dtype), to_dev(k, dtype), to_dev(v, dtype),
+                                         to_dev(g, dtype), cu, dev(gq), dev(gk), max_seqlen=T,
+                                         need_gains=False, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 1
+    wq, wk, wv, wg = (widen(x, dtype)[:200] for x in (q, k, v, g))
+    rq, rk, rv, _, _ = O.rla2_varlen_bwd(wq, wk, wv, wg, np.array([0, 200]), gq, gk, EPS_N, BASE,
+                                         EPS_D)
+    assert O.relative_error(to_host(dv)[:200], rv)[0] <= TOL[dtype]
+    keep_k = ~_ambiguous(wk, gk, np.arange(200))
+    assert _row_err(to_host(dk)[:200], rk, keep_k) <= TOL[dtype]
+
+
+def test_prefill_bwd_tensor_cores_shared_gains_many_segments(cuda_device, lib):
+    """bf16 d = 128 (the tensor-core path) with gains shared by the heads, a RoPE offset and two
+    (batch row, head) pairs only, so that every document is cut into many segments."""
+    B, L, H, d, off = 2, 900, 1, 128, 9
+    q, k, v = draw(360, (B, L, H, d), "bf16")
+    (g,) = draw(361, (B, L, H, d), "bf16")[:1]
+    gq, gk = gammas(362, H, d, False)
+    dev = lambda x: torch.from_numpy(x).to(cuda_device)
+    dq, dk, dv, dgq, dgk = R.rapt_prefill_bwd(to_dev(q, "bf16"), to_dev(k, "bf16"),
+                                              to_dev(v, "bf16"), to_dev(g, "bf16"), dev(gq),
+                                              dev(gk), pos_offset=off)
+    torch.cuda.synchronize()
+    wq, wk, wv, wg = (widen(x, "bf16") for x in (q, k, v, g))
+    rq, rk, rv, rgq, rgk = O.rla2_prefill_bwd(wq, wk, wv, wg, gq, gk, EPS_N, BASE, EPS_D,
+                                              pos_offset=off)
+    pos = off + np.arange(L)
+    for b in range(B):
+        assert _row_err(to_host(dq)[b], rq[b], ~_ambiguous(wq[b], gq, pos)) <= TOL["bf16"]
+        assert _row_err(to_host(dk)[b], rk[b], ~_ambiguous(wk[b], gk, pos)) <= TOL["bf16"]
+        assert O.relative_error(to_host(dv)[b], rv[b])[0] <= TOL["bf16"]
+    assert _vec_err(to_host(dgq), rgq) <= TOL["bf16"]
+    assert _vec_err(to_host(dgk), rgk) <= TOL["bf16"]

@@ -30,6 +30,9 @@ CASES = [
     (2, 300, 2, 64, "bf16"),
     (1, 1000, 3, 128, "bf16"),
     (3, 257, 5, 128, "f32"),
+    (3, 128, 2, 128, "bf16"),   # one whole chunk per row
+    (1, 256, 1, 128, "bf16"),   # two chunks, each its own segment
+    (2, 4000, 1, 128, "bf16"),  # many chunks per segment, ragged last chunk
 ]
 
 
