@@ -336,6 +336,9 @@ rapt_status backward_common(const void* q, const void* k, const void* v, const v
   b.kf = w + plan.off_kf;
   b.blk_per_seg = plan.blk_per_seg;
   b.nblk_max = plan.nblk_max;
+  b.dqf = w + plan.off_dqf;
+  b.dkf = w + plan.off_dkf;
+  b.chunks_max = plan.chunks_max;
   if (tc) return from_cuda(rapt::launch_backward_tc(b, s));
   return from_cuda(rapt::launch_backward_simt(to_dt(dtype), d, b, s));
 }

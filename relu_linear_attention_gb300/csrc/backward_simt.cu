@@ -646,7 +646,8 @@ BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d, bool
   const size_t recs_r = up(static_cast<size_t>(units) * p.nseg * rec);
   const size_t rows = up(static_cast<size_t>(total_rows) * H * sizeof(float));
   const size_t feats = tc ? up(static_cast<size_t>(total_rows) * H * d * 2) : 0;
-  const size_t gp = up(static_cast<size_t>(units) * p.nseg * d * sizeof(float));
+  p.chunks_max = tc ? chunks_max : 0;
+  const size_t gp = up(static_cast<size_t>(units) * (tc ? chunks_max : p.nseg) * d * sizeof(float));
   p.off_rev = recs_f;
   p.off_den = p.off_rev + recs_r;
   p.off_scl = p.off_den + rows;
@@ -654,7 +655,9 @@ BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d, bool
   p.off_nst = p.off_sst + rows;
   p.off_qf = p.off_nst + rows;
   p.off_kf = p.off_qf + feats;
-  p.off_dgq = p.off_kf + feats;
+  p.off_dqf = p.off_kf + feats;
+  p.off_dkf = p.off_dqf + feats;
+  p.off_dgq = p.off_dkf + feats;
   p.off_dgk = p.off_dgq + gp;
   p.ws_bytes = p.off_dgk + gp;
   return p;

@@ -13,14 +13,16 @@
 //              = den (gnum_t . v_tau + scale_t), in the form whose cancelling part is exact for a
 //              query that sees a single key (see backward_simt.cu)
 //   U += A'~ K'                                                                (second MMA group)
-//   dq'_t = U_t / den_t + scale_t z,  then dq through the feature map; den, scale, sst, nst of every
-//   row go to the workspace for pass B.
+//   dq'_t = U_t / den_t + scale_t z (bf16, to the workspace); den, scale, sst, nst of every row go
+//   to the workspace for pass B.
 // Pass B (chunks in reverse; suffix state R = sum q' gnum^T in TMEM, bf16 copy R~, w = sum scale q'):
 //   P = Q'K'^T,  Gv = Gnum V^T                                              (first group)
 //   P~ = P masked to tau <= t;  A[t][tau] = A'/den, with c = den Gv
 //   dv  = P~^T Gnum + K' R~                                                  (second group)
 //   dk' = A^T Q' + V R~^T (+ w),  R += Q'^T Gnum                             (third group)
-//   then dk through the feature map.
+//   dk' (bf16) to the workspace.
+// Then, fully parallel over (document, head, chunk), dq and dk through the feature map (ReLU mask,
+// inverse RoPE rotation, RMSNorm backward) from dq', dk' and the raw q, k, with gain partials.
 // One CTA per (document, head), 512 threads in lockstep phases: all threads compute features, read
 // TMEM rows (thread = TMEM lane = tile row, four warps per lane quarter splitting the columns) and
 // run the feature backward; one thread issues the MMAs and commits them to an mbarrier. Every
@@ -47,7 +49,6 @@ constexpr int kC = 128;
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr uint32_t kTile = 32768;          // 128 rows x 128 bf16 columns (two 64-column blocks)
-constexpr int kSL = kD + 1;                // row stride (floats) of the fp32 staging of dq' / dk'
 
 // Shared memory (bytes from a 1024-byte aligned base). Both passes use the same map: six bf16
 // tiles (the fifth, XS, holds S~ in pass A and R~ in pass B; the last, AS, holds A' in pass A and
@@ -55,7 +56,6 @@ constexpr int kSL = kD + 1;                // row stride (floats) of the fp32 st
 struct Lay {
   static constexpr uint32_t QF = 0, KF = kTile, VS = 2 * kTile, GS = 3 * kTile, XS = 4 * kTile;
   static constexpr uint32_t AS = 5 * kTile;
-  static constexpr uint32_t STG = 0;                          // fp32 [128][kSL] over QF..VS
   static constexpr uint32_t ZS = 6 * kTile;                   // z (pass A) / w (pass B) [D]
   static constexpr uint32_t ZP = ZS + kD * 4;                 // per-warp k' column sums [16][D]
   static constexpr uint32_t ROW = ZP + kWarps * kD * 4;       // den, scale, sst, nst [4][128]
@@ -63,7 +63,6 @@ struct Lay {
   static constexpr uint32_t BAR = RED + 3 * 4 * kC * 4;       // four mbarriers
   static constexpr uint32_t MISC = BAR + 4 * 8;               // TMEM base, abort flag
   static constexpr uint32_t BYTES = MISC + 16;
-  static_assert(static_cast<uint32_t>(kC) * kSL * 4 <= 3 * kTile, "staging fits over QF..VS");
   static_assert(BYTES <= 232448, "shared memory budget");
 };
 
@@ -104,14 +103,15 @@ __device__ __forceinline__ void load_rows(const __nv_bfloat16* x, long row0, int
 // the warp, then one complex multiplication by the rotation over 16 positions per row.
 struct LaneRope {
   float c[2], s[2];    // the current row
-  float cs[2], ss[2];  // the step over kWarps positions
+  float cs[2], ss[2];  // the step to the warp's next row
 };
-__device__ __forceinline__ void rope_start(LaneRope& r, int pos, const FeatureArgs& fa, int lane) {
+__device__ __forceinline__ void rope_start(LaneRope& r, int pos, const FeatureArgs& fa, int lane,
+                                           int step = kWarps) {
 #pragma unroll
   for (int m = 0; m < 2; ++m) {
     const int j = 2 * lane + m;
     rope_sincos(pos, fa.rope_hi[j], fa.rope_lo[j], r.s[m], r.c[m]);
-    rope_sincos(kWarps, fa.rope_hi[j], fa.rope_lo[j], r.ss[m], r.cs[m]);
+    rope_sincos(step, fa.rope_hi[j], fa.rope_lo[j], r.ss[m], r.cs[m]);
   }
 }
 __device__ __forceinline__ void rope_next(LaneRope& r) {
@@ -229,48 +229,6 @@ __device__ __forceinline__ void feature_tile_tc(const __nv_bfloat16* x, long row
   }
 }
 
-// Back through the features of the chunk's rows of x (q or k): warp w takes rows w, w + 16, ...
-// (the rows and rotations of feature_tile_tc) with their loads issued first; df rows come from the
-// fp32 staging.
-__device__ __forceinline__ void feature_tile_bwd_tc(const __nv_bfloat16* x, long row0, int n,
-                                                    int t0, int H, int h, const float* gamma,
-                                                    int pos0, const FeatureArgs& fa,
-                                                    const float* stg, __nv_bfloat16* dx,
-                                                    float (&dg)[4]) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float g[4];
-  lane_gains(gamma, lane, g);
-  LaneRope rope;
-  rope_start(rope, pos0 + t0 + warp, fa, lane);
-#pragma unroll 1
-  for (int i0 = 0; i0 < kRPW; i0 += kRB) {
-    float f[kRB][4];
-    load_rows(x, row0, n, t0, H, h, i0, f);
-#pragma unroll
-    for (int ii = 0; ii < kRB; ++ii) {
-      const int rr = warp + kWarps * (i0 + ii);
-      const int t = t0 + rr;
-      const bool valid = t < n;
-      if (i0 + ii > 0) rope_next(rope);
-      const long off = ((row0 + (valid ? t : 0)) * H + h) * kD + 4 * lane;
-      feat_lane_bwd(f[ii], valid, g, rope, fa.eps_norm, stg + rr * kSL + 4 * lane, dx + off, dg);
-    }
-  }
-}
-
-// Gain partials of this CTA (each lane's dg over the rows it took) summed over the warps in order.
-__device__ __forceinline__ void store_gain(const float (&dg)[4], float* scratch, float* out, bool bad) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) scratch[warp * kD + 4 * lane + e] = dg[e];
-  __syncthreads();
-  if (threadIdx.x < kD) {
-    float s = 0.f;
-    for (int w = 0; w < kWarps; ++w) s += scratch[w * kD + threadIdx.x];
-    out[threadIdx.x] = bad ? __int_as_float(0x7fc00000) : s;
-  }
-}
-
 // Several raw tiles at once (all loads in flight before any is stored): tile i gets rows of src[i];
 // with dv[i] set, its rows are divided by their den (gnum = g / den) and rounded to bf16.
 template <int NT>
@@ -339,7 +297,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
   float* scl_s = den_s + kC;
   float* sst_s = scl_s + kC;
   float* red = reinterpret_cast<float*>(smem + Lay::RED);
-  float* stg = reinterpret_cast<float*>(smem + Lay::STG);
   const uint32_t bar1 = base + Lay::BAR, bar2 = bar1 + 8, bar1b = bar1 + 16;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + Lay::MISC);
   int* s_abort = reinterpret_cast<int*>(smem + Lay::MISC + 4);
@@ -394,12 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
   const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
   const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v);
   const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(b.dout);
-  __nv_bfloat16* dq = static_cast<__nv_bfloat16*>(b.dq);
   const float* gq = a.gamma_q + h * a.fa.gamma_stride;
   const float* gk = a.gamma_k + h * a.fa.gamma_stride;
   __nv_bfloat16* qf_out = static_cast<__nv_bfloat16*>(b.qf);
   __nv_bfloat16* kf_out = static_cast<__nv_bfloat16*>(b.kf);
-  float dg[4] = {0.f, 0.f, 0.f, 0.f};
+  __nv_bfloat16* dqf_out = static_cast<__nv_bfloat16*>(b.dqf);
   bool bad = *s_abort != 0;
 
   for (int c = 0; c < nch && !bad; ++c) {
@@ -523,18 +479,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
       tc::mma_commit(bar2);
     }
     if (!wait_mma(bar2, c & 1)) atomicExch(s_abort, 1);
-    // ---- phase 5: dq' = U / den + scale z into the staging; S -> S~
+    // ---- phase 5: dq' = U / den + scale z (bf16, to the workspace); S -> S~
     {
       float u[32];
       tmem_ld32(tmem + tl + kTU + 32 * gw, u);
       const float inv = 1.0f / den;
 #pragma unroll
       for (int j = 0; j < 32; ++j) u[j] = fmaf(u[j], inv, scale * zs[32 * gw + j]);
-      // the staging overlays q', k', v: every MMA that read them has completed (bar2)
-      tc::fence_before_sync();
-      __syncthreads();
+      if (valid) {
+        __nv_bfloat16* dst = dqf_out + ((row0 + t0 + t) * a.H + h) * kD + 32 * gw;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) stg[t * kSL + 32 * gw + j] = u[j];
+        for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(u + 8 * m);
+      }
       float sv[32];
       tmem_ld32(tmem + tl + kTS + 32 * gw, sv);
       store_row32<true>(base + Lay::XS, t, gw, sv);
@@ -543,19 +499,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
     tc::fence_before_sync();
     __syncthreads();
     if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
-    // ---- phase 6: z += column sums of k'; back through the features of q
+    // ---- phase 6: z += column sums of k'
     if (tid < kD) {
-      float s = zs[tid];
-      for (int w = 0; w < kWarps; ++w) s += zp[w * kD + tid];
-      zs[tid] = s;
+      float zz = zs[tid];
+      for (int w = 0; w < kWarps; ++w) zz += zp[w * kD + tid];
+      zs[tid] = zz;
     }
-    feature_tile_bwd_tc(q, row0, n, t0, a.H, h, gq, a.pos_offset, a.fa, stg, dq, dg);
-    __syncthreads();  // the staging and zs are read before the next chunk overwrites them
+    __syncthreads();  // zs is read before the next chunk uses it
   }
   bad = bad || *reinterpret_cast<volatile int*>(s_abort) != 0;
   __syncthreads();
-  store_gain(dg, zp, b.dgp_q + (static_cast<long>(unit) * b.nseg + seg) * kD, bad);
-  if (bad && tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, 2u);
+  if (bad) {  // a wait gave up: NaN dq' over the segment, so the failure cannot pass for a result
+    for (long r = s0 + tid / 16; r < s1; r += kThreads / 16)
+      *reinterpret_cast<uint4*>(dqf_out + ((row0 + r) * a.H + h) * kD + 8 * (tid % 16)) =
+          make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
+    if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, 2u);
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -578,13 +537,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t base = tc::smem_u32(smem);
   float* ws = reinterpret_cast<float*>(smem + Lay::ZS);  // w
-  float* scratch = reinterpret_cast<float*>(smem + Lay::ZP);
   float* den_s = reinterpret_cast<float*>(smem + Lay::ROW);
   float* scl_s = den_s + kC;
   float* sst_s = scl_s + kC;
   float* nst_s = sst_s + kC;
   float* red = reinterpret_cast<float*>(smem + Lay::RED);
-  float* stg = reinterpret_cast<float*>(smem + Lay::STG);
   const uint32_t bar1 = base + Lay::BAR, bar2 = bar1 + 8, bar3 = bar2 + 8, bar4 = bar3 + 8;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + Lay::MISC);
   int* s_abort = reinterpret_cast<int*>(smem + Lay::MISC + 4);
@@ -640,12 +597,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
   const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
   const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v);
   const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(b.dout);
-  __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(b.dk);
   __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(b.dv);
-  const float* gk = a.gamma_k + h * a.fa.gamma_stride;
   const __nv_bfloat16* qf_in = static_cast<const __nv_bfloat16*>(b.qf);
   const __nv_bfloat16* kf_in = static_cast<const __nv_bfloat16*>(b.kf);
-  float dg[4] = {0.f, 0.f, 0.f, 0.f};
+  __nv_bfloat16* dkf_out = static_cast<__nv_bfloat16*>(b.dkf);
   bool bad = *s_abort != 0;
   int it = 0;  // chunks done (the mbarrier phases)
 
@@ -796,11 +751,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
         }
         red[(tid >> 7) * kC + i] = dw;
       }
-      if (!wait_mma(bar4, it & 1)) atomicExch(s_abort, 1);  // R updated; q', gnum read
-      tc::fence_before_sync();
-      __syncthreads();  // q' and w are read; the staging may overlay q', k', v
+      if (t0 + t < n) {  // dk' (bf16) to the workspace
+        __nv_bfloat16* dst = dkf_out + ((row0 + t0 + t) * a.H + h) * kD + 32 * gw;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) stg[t * kSL + 32 * gw + j] = o[j];
+        for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(o + 8 * m);
+      }
+      if (!wait_mma(bar4, it & 1)) atomicExch(s_abort, 1);  // R updated
+      tc::fence_before_sync();
+      __syncthreads();  // w is read
       if (tid < kD) ws[tid] += red[tid] + red[kC + tid] + red[2 * kC + tid] + red[3 * kC + tid];
       float rv[32];
       tmem_ld32(tmem + tl + kTR + 32 * gw, rv);
@@ -810,14 +768,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
     tc::fence_before_sync();
     __syncthreads();
     if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
-    // ---- phase 8: back through the features of k
-    feature_tile_bwd_tc(k, row0, n, t0, a.H, h, gk, a.pos_offset, a.fa, stg, dk, dg);
-    __syncthreads();
   }
   bad = bad || *reinterpret_cast<volatile int*>(s_abort) != 0;
   __syncthreads();
-  store_gain(dg, scratch, b.dgp_k + (static_cast<long>(unit) * b.nseg + seg) * kD, bad);
-  if (bad && tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, 2u);
+  if (bad) {  // a wait gave up: NaN dk' and dv over the segment
+    for (long r = s0 + tid / 16; r < s1; r += kThreads / 16) {
+      const long o = ((row0 + r) * a.H + h) * kD + 8 * (tid % 16);
+      const uint4 nan = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
+      *reinterpret_cast<uint4*>(dkf_out + o) = nan;
+      *reinterpret_cast<uint4*>(dv + o) = nan;
+    }
+    if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, 2u);
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -933,6 +895,72 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_revstate(const BwdArgs b) 
   if (warp == 0 && !misaligned) tc::tmem_dealloc(tmem, 128);
 }
 
+// ------------------------------------------------------------------------------------------------
+// After the passes, fully parallel: dq and dk through the feature map from dq', dk' (bf16, in the
+// workspace) and the raw q, k, with the gain partials of every (document, head, 128-token chunk).
+// One CTA of 8 warps per (document, head, chunk, q or k); warp w takes rows w, w + 8, ...
+constexpr int kFWarps = 8;
+constexpr int kFRows = kC / kFWarps;  // 16 rows per warp, in batches of 4
+
+__global__ void __launch_bounds__(kFWarps * 32) bwd_tc_features(const BwdArgs b) {
+  const PrefillArgs& a = b.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int which = blockIdx.x & 1;  // 0: q, 1: k
+  const int chunk = (blockIdx.x >> 1) % b.chunks_max, unit = (blockIdx.x >> 1) / b.chunks_max;
+  const int h = unit % a.H, doc = unit / a.H;
+  long row0;
+  int n;
+  doc_bounds(a, doc, row0, n);
+  const int t0 = chunk * kC;
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(which ? a.k : a.q);
+  const __nv_bfloat16* df = static_cast<const __nv_bfloat16*>(which ? b.dkf : b.dqf);
+  __nv_bfloat16* dx = static_cast<__nv_bfloat16*>(which ? b.dk : b.dq);
+  const float* gamma = (which ? a.gamma_k : a.gamma_q) + h * a.fa.gamma_stride;
+  __shared__ float scratch[kFWarps * kD];
+  float dg[4] = {0.f, 0.f, 0.f, 0.f};
+  if (t0 < n) {
+    float g[4];
+    lane_gains(gamma, lane, g);
+    LaneRope rope;
+    rope_start(rope, a.pos_offset + t0 + warp, a.fa, lane, kFWarps);
+#pragma unroll 1
+    for (int i0 = 0; i0 < kFRows; i0 += 4) {
+      uint2 rx[4], rd[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int t = t0 + warp + kFWarps * (i0 + i);
+        const long off = ((row0 + t) * a.H + h) * kD + 4 * lane;
+        rx[i] = t < n ? __ldg(reinterpret_cast<const uint2*>(x + off)) : make_uint2(0, 0);
+        rd[i] = t < n ? __ldg(reinterpret_cast<const uint2*>(df + off)) : make_uint2(0, 0);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int t = t0 + warp + kFWarps * (i0 + i);
+        const bool valid = t < n;
+        if (i0 + i > 0) rope_next(rope);
+        float f[4], d4[4];
+        const float2 x0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rx[i].x));
+        const float2 x1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rx[i].y));
+        const float2 d0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rd[i].x));
+        const float2 d1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rd[i].y));
+        f[0] = x0.x; f[1] = x0.y; f[2] = x1.x; f[3] = x1.y;
+        d4[0] = d0.x; d4[1] = d0.y; d4[2] = d1.x; d4[3] = d1.y;
+        const long off = ((row0 + (valid ? t : 0)) * a.H + h) * kD + 4 * lane;
+        feat_lane_bwd(f, valid, g, rope, a.fa.eps_norm, d4, dx + off, dg);
+      }
+    }
+  }
+  // the CTA's gain partial, summed over the warps in order (zeros past the document's end)
+#pragma unroll
+  for (int e = 0; e < 4; ++e) scratch[warp * kD + 4 * lane + e] = dg[e];
+  __syncthreads();
+  if (tid < kD) {
+    float sum = 0.f;
+    for (int w = 0; w < kFWarps; ++w) sum += scratch[w * kD + tid];
+    (which ? b.dgp_k : b.dgp_q)[(static_cast<long>(unit) * b.chunks_max + chunk) * kD + tid] = sum;
+  }
+}
+
 }  // namespace
 
 bool bwd_tc_supported(DType dt, int d) { return dt == DType::BF16 && d == kD; }
@@ -977,7 +1005,13 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   bwd_tc_reverse<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  return launch_bwd_gain(b, kD, stream);
+  const long fgrid = static_cast<long>(b.p.n_docs) * b.p.H * b.chunks_max * 2;
+  bwd_tc_features<<<static_cast<unsigned>(fgrid), kFWarps * 32, 0, stream>>>(b);
+  note_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  BwdArgs g = b;  // the gain partials are per (document, head, chunk)
+  g.nseg = b.chunks_max;
+  return launch_bwd_gain(g, kD, stream);
 }
 
 }  // namespace rapt

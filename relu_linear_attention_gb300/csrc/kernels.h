@@ -76,13 +76,20 @@ struct BwdArgs {
   void* kf;
   int blk_per_seg;
   int nblk_max;
+  // tensor-core path: dq', dk' in bf16 (written by the passes, turned into dq, dk by the feature
+  // kernel, whose gain partials are per (document, head, 128-token chunk): chunks_max per pair)
+  void* dqf;
+  void* dkf;
+  int chunks_max;
 };
 struct BwdPlan {
   int nseg;
   int seg_len;
   int blk_per_seg;  // tensor-core path
   int nblk_max;     // tensor-core path
-  size_t off_rev, off_den, off_scl, off_sst, off_nst, off_dgq, off_dgk, off_qf, off_kf;
+  int chunks_max;   // tensor-core path: 128-token chunks of the longest document
+  size_t off_rev, off_den, off_scl, off_sst, off_nst, off_dgq, off_dgk, off_qf, off_kf, off_dqf,
+      off_dkf;
   size_t ws_bytes;
 };
 // tc: the tensor-core path (one CTA per (document, head), no segment increments).
