@@ -35,6 +35,7 @@
 #include "tc_features.cuh"
 #include "tc_tiles.cuh"
 #include "tc_utils.cuh"
+#include "tensor_map.h"
 
 namespace rapt {
 namespace {
@@ -60,8 +61,8 @@ struct Lay {
   static constexpr uint32_t ZP = ZS + kD * 4;                 // per-warp k' column sums [16][D]
   static constexpr uint32_t ROW = ZP + kWarps * kD * 4;       // den, scale, sst, nst [4][128]
   static constexpr uint32_t RED = ROW + 4 * kC * 4;           // partial row sums [3][4][128]
-  static constexpr uint32_t BAR = RED + 3 * 4 * kC * 4;       // four mbarriers
-  static constexpr uint32_t MISC = BAR + 4 * 8;               // TMEM base, abort flag
+  static constexpr uint32_t BAR = RED + 3 * 4 * kC * 4;       // five mbarriers
+  static constexpr uint32_t MISC = BAR + 5 * 8;               // TMEM base, abort flag
   static constexpr uint32_t BYTES = MISC + 16;
   static_assert(BYTES <= 232448, "shared memory budget");
 };
@@ -79,24 +80,6 @@ constexpr int kRPW = kC / kWarps;  // rows per warp
 
 constexpr int kRB = kRPW / 2;  // rows of a warp loaded together (two batches per tile)
 
-// Rows i0, i0 + 1, ... (of this warp's rows w + 16 i) of x, as floats.
-__device__ __forceinline__ void load_rows(const __nv_bfloat16* x, long row0, int n, int t0, int H,
-                                          int h, int i0, float (&f)[kRB][4]) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint2 raw[kRB];
-#pragma unroll
-  for (int i = 0; i < kRB; ++i) {
-    const int t = t0 + warp + kWarps * (i0 + i);
-    raw[i] = t < n ? __ldg(reinterpret_cast<const uint2*>(x + ((row0 + t) * H + h) * kD + 4 * lane))
-                   : make_uint2(0, 0);
-  }
-#pragma unroll
-  for (int i = 0; i < kRB; ++i) {
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[i].x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[i].y));
-    f[i][0] = a.x; f[i][1] = a.y; f[i][2] = b.x; f[i][3] = b.y;
-  }
-}
 
 // RoPE rotations of a lane's two pairs (elements 4 lane .. 4 lane + 3 are pairs 2 lane, 2 lane + 1)
 // for the rows a warp takes (positions p, p + 16, ...): exact sin / cos at the chunk's first row of
@@ -185,11 +168,35 @@ __device__ __forceinline__ void lane_gains(const float* gamma, int lane, float (
   g[0] = v.x; g[1] = v.y; g[2] = v.z; g[3] = v.w;
 }
 
-__device__ __forceinline__ void feature_tile_tc(const __nv_bfloat16* x, long row0, int n, int t0,
-                                                int H, int h, const float* gamma, int pos0,
-                                                const FeatureArgs& fa, uint32_t tile,
-                                                const float* z, float* sst, float (&zc)[4],
-                                                __nv_bfloat16* out) {
+
+// One chunk's 128 rows of nt [rows, H, D] tensors into their tiles by TMA (two 64-column boxes
+// each, in the swizzled operand layout), completing on one mbarrier; one thread calls it. Rows
+// past the tensor read as zero; rows past the document but inside the tensor are other tokens,
+// which the caller clears after the wait.
+template <int NT>
+__device__ __forceinline__ void tma_chunk(const CUtensorMap* const (&maps)[NT],
+                                          const uint32_t (&tiles)[NT], int h, int row, uint32_t bar) {
+  tc::mbar_arrive_expect_tx(bar, NT * kTile);
+#pragma unroll
+  for (int i = 0; i < NT; ++i)
+#pragma unroll
+    for (int jb = 0; jb < 2; ++jb) tc::tma_load_3d(tiles[i] + jb * 16384, maps[i], 64 * jb, h, row, bar);
+}
+
+// Rows nvalid .. 127 of a tile set to zero (all threads).
+__device__ __forceinline__ void clear_rows(uint32_t tile, int nvalid) {
+  for (int idx = threadIdx.x + nvalid * 16; idx < kC * 16; idx += kThreads)
+    sts16(tile + tile_off(idx >> 4, idx & 15), make_uint4(0, 0, 0, 0));
+}
+
+// Features of the chunk's rows in place: the tile holds raw rows (by TMA); warp w takes rows w,
+// w + 16, ... (lane r: elements 4r .. 4r+3) and writes the bf16 features over them (zeros for rows
+// past the document). With z given, q'.z of every row into sst[]; the column sums go to zc; with
+// out given, the valid rows' features are stored there too.
+__device__ __forceinline__ void features_in_place(uint32_t tile, long row0, int n, int t0, int H,
+                                                  int h, const float* gamma, int pos0,
+                                                  const FeatureArgs& fa, const float* z, float* sst,
+                                                  float (&zc)[4], __nv_bfloat16* out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float g[4];
   lane_gains(gamma, lane, g);
@@ -202,30 +209,37 @@ __device__ __forceinline__ void feature_tile_tc(const __nv_bfloat16* x, long row
   }
 #pragma unroll 1
   for (int i0 = 0; i0 < kRPW; i0 += kRB) {
-  float f[kRB][4];
-  load_rows(x, row0, n, t0, H, h, i0, f);
+    uint32_t lo[kRB], hi[kRB];
 #pragma unroll
-  for (int ii = 0; ii < kRB; ++ii) {
-    const int i = ii;
-    const int rr = warp + kWarps * (i0 + ii);
-    const int t = t0 + rr;
-    const bool valid = t < n;
-    if (i0 + ii > 0) rope_next(rope);
-    feat_lane(f[i], valid, g, rope, fa.eps_norm);
-    const uint32_t addr = tile + tile_off(rr, lane >> 1) + (lane & 1) * 8;
-    const uint32_t lo = tc::pack_bf16x2(f[i][0], f[i][1]), hi = tc::pack_bf16x2(f[i][2], f[i][3]);
-    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(lo), "r"(hi) : "memory");
-    if (out != nullptr && valid)
-      *reinterpret_cast<uint2*>(out + ((row0 + t) * H + h) * kD + 4 * lane) = make_uint2(lo, hi);
-    if (z != nullptr) {
-      float s = f[i][0] * zl[0] + f[i][1] * zl[1] + f[i][2] * zl[2] + f[i][3] * zl[3];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-      if (lane == 0) sst[rr] = valid ? s : 0.f;
+    for (int i = 0; i < kRB; ++i) {
+      const uint32_t addr = tile + tile_off(warp + kWarps * (i0 + i), lane >> 1) + (lane & 1) * 8;
+      asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(lo[i]), "=r"(hi[i]) : "r"(addr) : "memory");
     }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) zc[e] += f[i][e];
-  }
+    for (int i = 0; i < kRB; ++i) {
+      const int rr = warp + kWarps * (i0 + i);
+      const int t = t0 + rr;
+      const bool valid = t < n;
+      if (i0 + i > 0) rope_next(rope);
+      float f[4];
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&lo[i]));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi[i]));
+      f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+      feat_lane(f, valid, g, rope, fa.eps_norm);
+      const uint32_t plo = tc::pack_bf16x2(f[0], f[1]), phi = tc::pack_bf16x2(f[2], f[3]);
+      const uint32_t addr = tile + tile_off(rr, lane >> 1) + (lane & 1) * 8;
+      asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(plo), "r"(phi) : "memory");
+      if (out != nullptr && valid)
+        *reinterpret_cast<uint2*>(out + ((row0 + t) * H + h) * kD + 4 * lane) = make_uint2(plo, phi);
+      if (z != nullptr) {
+        float sdot = f[0] * zl[0] + f[1] * zl[1] + f[2] * zl[2] + f[3] * zl[3];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sdot += __shfl_xor_sync(0xffffffffu, sdot, off);
+        if (lane == 0) sst[rr] = valid ? sdot : 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) zc[e] += f[e];
+    }
   }
 }
 
@@ -265,19 +279,13 @@ __device__ __forceinline__ void raw_tiles_tc(const __nv_bfloat16* const (&src)[N
   }
 }
 
-// L2 prefetch of the 128 rows of a chunk of x (one 128-byte line per thread and call; two calls
-// per tensor), so that the next chunk's loads do not wait for DRAM.
-__device__ __forceinline__ void prefetch_rows(const __nv_bfloat16* x, long row0, int n, int t0,
-                                              int H, int h, int part) {
-  const int idx = threadIdx.x + kThreads * part;  // 0 .. 2 kThreads - 1 over two calls
-  const int r = idx >> 1;
-  if (r < kC && t0 + r < n)
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(x + ((row0 + t0 + r) * H + h) * kD + 64 * (idx & 1)));
-}
 
 // ------------------------------------------------------------------------------------------------
 // Pass A: chunks in order.
-__global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_tc_forward(const BwdArgs b, const __grid_constant__ CUtensorMap tmq,
+                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                   const __grid_constant__ CUtensorMap tmg) {
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int seg = blockIdx.x % b.nseg, unit = blockIdx.x / b.nseg;
@@ -297,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
   float* scl_s = den_s + kC;
   float* sst_s = scl_s + kC;
   float* red = reinterpret_cast<float*>(smem + Lay::RED);
-  const uint32_t bar1 = base + Lay::BAR, bar2 = bar1 + 8, bar1b = bar1 + 16;
+  const uint32_t bar1 = base + Lay::BAR, bar2 = bar1 + 8, bar1b = bar1 + 16, bar_ld = bar1 + 24;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + Lay::MISC);
   int* s_abort = reinterpret_cast<int*>(smem + Lay::MISC + 4);
   const bool misaligned = (base & 1023u) != 0;
@@ -310,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
     tc::mbar_init(bar1, 1);
     tc::mbar_init(bar2, 1);
     tc::mbar_init(bar1b, 1);
+    tc::mbar_init(bar_ld, 1);
     tc::mbar_fence_init();
     *s_abort = misaligned ? 1 : 0;
   }
@@ -347,12 +356,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
   __syncthreads();
   tc::fence_after_sync();
 
-  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-  const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
-  const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v);
-  const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(b.dout);
   const float* gq = a.gamma_q + h * a.fa.gamma_stride;
   const float* gk = a.gamma_k + h * a.fa.gamma_stride;
+  const CUtensorMap* const maps[4] = {&tmq, &tmk, &tmv, &tmg};
+  const uint32_t ld_tiles[4] = {base + Lay::QF, base + Lay::KF, base + Lay::VS, base + Lay::GS};
+  int tma_issued = 0;  // chunks whose tiles have been requested (thread 0)
+  if (tid == 0 && nch > 0 && !*s_abort) {
+    tma_chunk<4>(maps, ld_tiles, h, static_cast<int>(row0 + s0), bar_ld);
+    tma_issued = 1;
+  }
   __nv_bfloat16* qf_out = static_cast<__nv_bfloat16*>(b.qf);
   __nv_bfloat16* kf_out = static_cast<__nv_bfloat16*>(b.kf);
   __nv_bfloat16* dqf_out = static_cast<__nv_bfloat16*>(b.dqf);
@@ -360,24 +372,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
 
   for (int c = 0; c < nch && !bad; ++c) {
     const int t0 = s0 + c * kC;
-    // ---- phase 1: features (q'.z of every row), column sums of k', v and g tiles
+    // ---- phase 1: the chunk's raw tiles (TMA); features in place (q'.z of every row, column
+    // sums of k'); rows past the document cleared
+    if (!tc::mbar_wait(bar_ld, c & 1, kWait)) atomicExch(s_abort, 1);
     float zc[4] = {0.f, 0.f, 0.f, 0.f}, dummy[4] = {0.f, 0.f, 0.f, 0.f};
-    feature_tile_tc(q, row0, n, t0, a.H, h, gq, a.pos_offset, a.fa, base + Lay::QF, zs, sst_s,
-                    dummy, qf_out);
-    feature_tile_tc(k, row0, n, t0, a.H, h, gk, a.pos_offset, a.fa, base + Lay::KF, nullptr,
-                    nullptr, zc, kf_out);
+    features_in_place(base + Lay::QF, row0, n, t0, a.H, h, gq, a.pos_offset, a.fa, zs, sst_s, dummy,
+                      qf_out);
+    features_in_place(base + Lay::KF, row0, n, t0, a.H, h, gk, a.pos_offset, a.fa, nullptr, nullptr,
+                      zc, kf_out);
 #pragma unroll
     for (int e = 0; e < 4; ++e) zp[warp * kD + 4 * lane + e] = zc[e];
-    {
-      const __nv_bfloat16* const src[2] = {v, g};
-      const uint32_t tiles[2] = {base + Lay::VS, base + Lay::GS};
-      const bool dv[2] = {false, false};
-      raw_tiles_tc<2>(src, tiles, dv, row0, n, t0, a.H, h, nullptr);
+    if (t0 + kC > n) {
+      clear_rows(base + Lay::VS, n - t0);
+      clear_rows(base + Lay::GS, n - t0);
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
     // ---- phase 2: P = Q'K'^T, Cv = G V^T, U = G S~^T, S += K'^T V
     if (tid == 0) {
       constexpr uint32_t ID_KK = tc::idesc_bf16(128, 128, false, false);
@@ -397,14 +410,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
       for (int kk = 0; kk < kC / 16; ++kk)
         tc::mma_bf16(tmem + kTS, mnmaj(base + Lay::KF, kk, 16384), mnmaj(base + Lay::VS, kk, 16384),
                      ID_MM, 1u);
-    }
-    if (c + 1 < nch) {  // the next chunk's rows into L2 while the tensor core works
-      for (int part = 0; part < 2; ++part) {
-        prefetch_rows(q, row0, n, t0 + kC, a.H, h, part);
-        prefetch_rows(k, row0, n, t0 + kC, a.H, h, part);
-        prefetch_rows(v, row0, n, t0 + kC, a.H, h, part);
-        prefetch_rows(g, row0, n, t0 + kC, a.H, h, part);
-      }
     }
     if (!wait_mma(bar1, c & 1)) atomicExch(s_abort, 1);
     // ---- phase 3: row sums, den, scale, A'
@@ -479,6 +484,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
       tc::mma_commit(bar2);
     }
     if (!wait_mma(bar2, c & 1)) atomicExch(s_abort, 1);
+    // every MMA has read the tiles: the next chunk's raw tiles may arrive while this one finishes
+    if (tid == 0 && c + 1 < nch && !*reinterpret_cast<volatile int*>(s_abort)) {
+      tma_chunk<4>(maps, ld_tiles, h, static_cast<int>(row0 + t0 + kC), bar_ld);
+      ++tma_issued;
+    }
     // ---- phase 5: dq' = U / den + scale z (bf16, to the workspace); S -> S~
     {
       float u[32];
@@ -508,6 +518,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
     __syncthreads();  // zs is read before the next chunk uses it
   }
   bad = bad || *reinterpret_cast<volatile int*>(s_abort) != 0;
+  // a copy requested but not waited for (an early exit) must land before the CTA leaves
+  if (tid == 0 && tma_issued > 0) tc::mbar_wait(bar_ld, (tma_issued - 1) & 1, kWait);
   __syncthreads();
   if (bad) {  // a wait gave up: NaN dq' over the segment, so the failure cannot pass for a result
     for (long r = s0 + tid / 16; r < s1; r += kThreads / 16)
@@ -523,7 +535,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_forward(const BwdArgs b) {
 
 // ------------------------------------------------------------------------------------------------
 // Pass B: chunks in reverse.
-__global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_tc_reverse(const BwdArgs b, const __grid_constant__ CUtensorMap tmqf,
+                   const __grid_constant__ CUtensorMap tmkf, const __grid_constant__ CUtensorMap tmv,
+                   const __grid_constant__ CUtensorMap tmg) {
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int seg = blockIdx.x % b.nseg, unit = blockIdx.x / b.nseg;
@@ -543,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
   float* nst_s = sst_s + kC;
   float* red = reinterpret_cast<float*>(smem + Lay::RED);
   const uint32_t bar1 = base + Lay::BAR, bar2 = bar1 + 8, bar3 = bar2 + 8, bar4 = bar3 + 8;
+  const uint32_t bar_ld = bar4 + 8;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + Lay::MISC);
   int* s_abort = reinterpret_cast<int*>(smem + Lay::MISC + 4);
   const bool misaligned = (base & 1023u) != 0;
@@ -556,6 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
     tc::mbar_init(bar2, 1);
     tc::mbar_init(bar3, 1);
     tc::mbar_init(bar4, 1);
+    tc::mbar_init(bar_ld, 1);
     tc::mbar_fence_init();
     *s_abort = misaligned ? 1 : 0;
   }
@@ -594,25 +611,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
   __syncthreads();
   tc::fence_after_sync();
 
-  const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
-  const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v);
-  const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(b.dout);
   __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(b.dv);
-  const __nv_bfloat16* qf_in = static_cast<const __nv_bfloat16*>(b.qf);
-  const __nv_bfloat16* kf_in = static_cast<const __nv_bfloat16*>(b.kf);
   __nv_bfloat16* dkf_out = static_cast<__nv_bfloat16*>(b.dkf);
+  const CUtensorMap* const maps[4] = {&tmqf, &tmkf, &tmv, &tmg};
+  const uint32_t ld_tiles[4] = {base + Lay::QF, base + Lay::KF, base + Lay::VS, base + Lay::GS};
+  int tma_issued = 0;  // chunks whose tiles have been requested (thread 0)
+  if (tid == 0 && nch > 0 && !*s_abort) {
+    tma_chunk<4>(maps, ld_tiles, h, static_cast<int>(row0 + s0 + (nch - 1) * kC), bar_ld);
+    tma_issued = 1;
+  }
   bool bad = *s_abort != 0;
   int it = 0;  // chunks done (the mbarrier phases)
 
   for (int c = nch - 1; c >= 0 && !bad; --c, ++it) {
     const int t0 = s0 + c * kC;
-    // ---- phase 1: q', k' (stored by pass A), v, gnum = g / den, and the row scalars of pass A
-    {
-      const __nv_bfloat16* const src[4] = {qf_in, kf_in, v, g};
-      const uint32_t tiles[4] = {base + Lay::QF, base + Lay::KF, base + Lay::VS, base + Lay::GS};
-      const bool dv[4] = {false, false, false, true};
-      raw_tiles_tc<4>(src, tiles, dv, row0, n, t0, a.H, h, b.den);
-    }
+    // ---- phase 1: q', k' (stored by pass A), v and g by TMA; the row scalars of pass A; gnum =
+    // g / den in place; rows past the document cleared
     if (tid < kC) {
       const bool vr = t0 + tid < n;
       const long o = (row0 + t0 + tid) * a.H + h;
@@ -621,10 +635,30 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
       sst_s[tid] = vr ? b.sst[o] : 0.f;
       nst_s[tid] = vr ? b.nst[o] : 0.f;
     }
+    if (!tc::mbar_wait(bar_ld, it & 1, kWait)) atomicExch(s_abort, 1);
+    __syncthreads();  // den_s
+    for (int idx = tid; idx < kC * 16; idx += kThreads) {
+      const int r = idx >> 4, m = idx & 15;
+      const uint32_t ga = base + Lay::GS + tile_off(r, m);
+      if (t0 + r < n) {
+        float f[8];
+        unpack8(lds16(ga), f);
+        const float inv = 1.0f / den_s[r];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] *= inv;
+        sts16(ga, feat::pack8(f));
+      } else {
+        sts16(ga, make_uint4(0, 0, 0, 0));
+        sts16(base + Lay::QF + tile_off(r, m), make_uint4(0, 0, 0, 0));
+        sts16(base + Lay::KF + tile_off(r, m), make_uint4(0, 0, 0, 0));
+        sts16(base + Lay::VS + tile_off(r, m), make_uint4(0, 0, 0, 0));
+      }
+    }
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
     // ---- phase 2: P = Q'K'^T, Gv = Gnum V^T
     if (tid == 0) {
       constexpr uint32_t ID = tc::idesc_bf16(128, 128, false, false);
@@ -719,15 +753,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
                      ID_MM, 1u);
       tc::mma_commit(bar4);
     }
-    if (c > 0) {  // the next (earlier) chunk's rows into L2 while the tensor core works
-      for (int part = 0; part < 2; ++part) {
-        prefetch_rows(qf_in, row0, n, t0 - kC, a.H, h, part);
-        prefetch_rows(kf_in, row0, n, t0 - kC, a.H, h, part);
-        prefetch_rows(v, row0, n, t0 - kC, a.H, h, part);
-        prefetch_rows(g, row0, n, t0 - kC, a.H, h, part);
-        prefetch_rows(k, row0, n, t0 - kC, a.H, h, part);
-      }
-    }
     if (!wait_mma(bar3, it & 1)) atomicExch(s_abort, 1);
     // ---- phase 7: dk' + w into the staging, w += sum_t scale_t q'_t, R -> R~
     {
@@ -756,9 +781,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
 #pragma unroll
         for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(o + 8 * m);
       }
-      if (!wait_mma(bar4, it & 1)) atomicExch(s_abort, 1);  // R updated
+      if (!wait_mma(bar4, it & 1)) atomicExch(s_abort, 1);  // R updated: every MMA read its tiles
+      tc::fence_async_smem();
       tc::fence_before_sync();
-      __syncthreads();  // w is read
+      __syncthreads();  // w and q' are read
+      if (tid == 0 && c > 0 && !*reinterpret_cast<volatile int*>(s_abort)) {
+        // the earlier chunk's tiles arrive while this one finishes
+        tma_chunk<4>(maps, ld_tiles, h, static_cast<int>(row0 + t0 - kC), bar_ld);
+        ++tma_issued;
+      }
       if (tid < kD) ws[tid] += red[tid] + red[kC + tid] + red[2 * kC + tid] + red[3 * kC + tid];
       float rv[32];
       tmem_ld32(tmem + tl + kTR + 32 * gw, rv);
@@ -770,6 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_reverse(const BwdArgs b) {
     if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
   }
   bad = bad || *reinterpret_cast<volatile int*>(s_abort) != 0;
+  if (tid == 0 && tma_issued > 0) tc::mbar_wait(bar_ld, (tma_issued - 1) & 1, kWait);
   __syncthreads();
   if (bad) {  // a wait gave up: NaN dk' and dv over the segment
     for (long r = s0 + tid / 16; r < s1; r += kThreads / 16) {
@@ -994,7 +1026,16 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
     ta.whole_doc = 0;
     if ((e = launch_state_tc(kD, ta, stream)) != cudaSuccess) return e;
   }
-  bwd_tc_forward<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b);
+  // TMA maps of the row-major [rows, H, D] tensors the passes stream
+  CUtensorMap tmq, tmk, tmv, tmg, tmqf, tmkf;
+  const long rows = b.p.total_rows;
+  if ((e = make_rows_map(&tmq, b.p.q, rows, b.p.H, kD)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmk, b.p.k, rows, b.p.H, kD)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmv, b.p.v, rows, b.p.H, kD)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmg, b.dout, rows, b.p.H, kD)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmqf, b.qf, rows, b.p.H, kD)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmkf, b.kf, rows, b.p.H, kD)) != cudaSuccess) return e;
+  bwd_tc_forward<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b, tmq, tmk, tmv, tmg);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (b.nseg > 1) {
@@ -1002,7 +1043,8 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
     note_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  bwd_tc_reverse<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b);
+  bwd_tc_reverse<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b, tmqf, tmkf, tmv,
+                                                                                 tmg);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long fgrid = static_cast<long>(b.p.n_docs) * b.p.H * b.chunks_max * 2;
