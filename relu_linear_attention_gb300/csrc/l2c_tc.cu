@@ -15,7 +15,9 @@
 // Documents (batch rows) are cut into segments of seg_len tokens; segment s starts from the
 // moments [K'^T V | K'^T K'] of the splits before it, computed by the non-causal L2 path's moments
 // kernel with the same split length (summed in split order: deterministic). One CTA per (batch row,
-// head, segment), 512 threads in lockstep phases, one thread issuing the MMAs. Every wait is
+// head, segment), 512 threads in lockstep phases, one thread issuing the MMAs and the TMA copies:
+// the next chunk's q, k, v tiles are requested as soon as the current chunk's last MMA has read
+// its tiles, so they arrive while the chunk's output and state copies are written. Every wait is
 // bounded (~1 s); a CTA whose wait gives up writes NaN over its rows.
 #include <cuda.h>
 
@@ -23,11 +25,11 @@
 #include "tc_features.cuh"
 #include "tc_tiles.cuh"
 #include "tc_utils.cuh"
+#include "tensor_map.h"
 
 namespace rapt {
 namespace {
 
-using feat::ldg16;
 using feat::lds16;
 using feat::sts16;
 using namespace tct;
@@ -40,69 +42,48 @@ struct LayC {
   static constexpr uint32_t QF = 0, KF = kTile, VS = 2 * kTile, SS = 3 * kTile, AS = 4 * kTile;
   static constexpr uint32_t PS = 5 * kTile;
   static constexpr uint32_t RED = 6 * kTile;         // partial den^2 [4][128]
-  static constexpr uint32_t BAR = RED + 4 * kC * 4;  // two mbarriers
-  static constexpr uint32_t MISC = BAR + 16;         // TMEM base, abort flag
+  static constexpr uint32_t BAR = RED + 4 * kC * 4;  // three mbarriers
+  static constexpr uint32_t MISC = BAR + 24;         // TMEM base, abort flag
   static constexpr uint32_t BYTES = MISC + 16;
   static_assert(BYTES <= 232448, "shared memory budget");
 };
 constexpr uint32_t kTP = 0, kTX = 128, kTS = 256, kTA = 384;  // TMEM columns: P, X, S, A
 
-// Raw rows of x into a bf16 tile (rows past the batch row's L are zero), optionally rectified.
-// The chunk's rows of q, k and v into their bf16 tiles, all loads in flight before any store; q and
-// k rectified (bf16 max(0, x) on the bit patterns: a set sign bit, negative or -0, becomes +0).
-__device__ __forceinline__ void load_tiles(const __nv_bfloat16* q, const __nv_bfloat16* k,
-                                           const __nv_bfloat16* vv, long row0, int n, int t0, int H,
-                                           int h, uint32_t base) {
-  constexpr int kPer = kC * 16 / kThreads;
-  const __nv_bfloat16* src[3] = {q, k, vv};
-  const uint32_t tile[3] = {base + LayC::QF, base + LayC::KF, base + LayC::VS};
-  uint4 v[3][kPer];
+// The chunk's raw q, k, v rows into their tiles by TMA (two 64-column boxes each), completing on
+// one mbarrier; one thread calls it. Rows past the tensor read as zero.
+__device__ __forceinline__ void tma_qkv(const CUtensorMap* tq, const CUtensorMap* tk,
+                                        const CUtensorMap* tv, uint32_t base, int h, int t, int bb,
+                                        uint32_t bar) {
+  tc::mbar_arrive_expect_tx(bar, 3 * kTile);
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int idx = threadIdx.x + kThreads * i, r = idx >> 4, m = idx & 15;
-#pragma unroll
-    for (int x = 0; x < 3; ++x)
-      v[x][i] = t0 + r < n ? ldg16(src[x] + ((row0 + t0 + r) * H + h) * kD + 8 * m)
-                           : make_uint4(0, 0, 0, 0);
-  }
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int idx = threadIdx.x + kThreads * i, r = idx >> 4, m = idx & 15;
-#pragma unroll
-    for (int x = 0; x < 3; ++x) {
-      if (x < 2) {
-        uint32_t w[4] = {v[x][i].x, v[x][i].y, v[x][i].z, v[x][i].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t lo = (w[e] & 0x8000u) ? 0u : (w[e] & 0xFFFFu);
-          const uint32_t hi = (w[e] & 0x80000000u) ? 0u : (w[e] & 0xFFFF0000u);
-          w[e] = lo | hi;
-        }
-        v[x][i] = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      sts16(tile[x] + tile_off(r, m), v[x][i]);
-    }
+  for (int jb = 0; jb < 2; ++jb) {
+    tc::tma_load_4d(base + LayC::QF + jb * 16384, tq, 64 * jb, h, t, bb, bar);
+    tc::tma_load_4d(base + LayC::KF + jb * 16384, tk, 64 * jb, h, t, bb, bar);
+    tc::tma_load_4d(base + LayC::VS + jb * 16384, tv, 64 * jb, h, t, bb, bar);
   }
 }
 
-// L2 prefetch of a chunk's rows of q, k and v (so that the next chunk's loads do not wait for DRAM).
-__device__ __forceinline__ void prefetch_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k,
-                                               const __nv_bfloat16* v, long row0, int n, int t0,
-                                               int H, int h) {
-  const int r = threadIdx.x >> 2, part = threadIdx.x & 3;  // 128 rows x 2 lines, 3 tensors
-  if (r < kC && t0 + r < n) {
-    const long off = ((row0 + t0 + r) * H + h) * kD + 64 * (part & 1);
-    if (part < 2) {
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(q + off));
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(k + off));
-    } else {
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(v + off));
+// In place: q and k tiles rectified (bf16 max(0, x) on the bit patterns: a set sign bit, negative
+// or -0, becomes +0). The 4-D maps read rows past the batch row's end as zero already.
+__device__ __forceinline__ void rectify_qk(uint32_t base) {
+  for (int idx = threadIdx.x; idx < 2 * kC * 16; idx += kThreads) {
+    const uint32_t addr =
+        base + (idx < kC * 16 ? LayC::QF : LayC::KF) + tile_off((idx >> 4) & (kC - 1), idx & 15);
+    uint4 v = lds16(addr);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t lo = (w[e] & 0x8000u) ? 0u : (w[e] & 0xFFFFu);
+      const uint32_t hi = (w[e] & 0x80000000u) ? 0u : (w[e] & 0xFFFF0000u);
+      w[e] = lo | hi;
     }
+    sts16(addr, make_uint4(w[0], w[1], w[2], w[3]));
   }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    l2c_tc_kernel(const L2Args a, int nseg, int seg_len) {
+    l2c_tc_kernel(const L2Args a, int nseg, int seg_len, const __grid_constant__ CUtensorMap tq,
+                  const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int seg = blockIdx.x % nseg, bh = blockIdx.x / nseg;
   const int bb = bh / a.H, h = bh % a.H;
@@ -115,7 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t base = tc::smem_u32(smem);
   float* red = reinterpret_cast<float*>(smem + LayC::RED);
-  const uint32_t bar1 = base + LayC::BAR, bar2 = bar1 + 8;
+  const uint32_t bar1 = base + LayC::BAR, bar2 = bar1 + 8, bar_ld = bar1 + 16;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + LayC::MISC);
   int* s_abort = reinterpret_cast<int*>(smem + LayC::MISC + 4);
   const bool misaligned = (base & 1023u) != 0;
@@ -126,6 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     tc::mbar_init(bar1, 1);
     tc::mbar_init(bar2, 1);
+    tc::mbar_init(bar_ld, 1);
     tc::mbar_fence_init();
     *s_abort = misaligned ? 1 : 0;
   }
@@ -163,14 +145,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
 
-  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-  const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
-  const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v);
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+  int tma_issued = 0;  // chunks whose tiles have been requested (thread 0)
+  if (tid == 0 && !bad) {
+    tma_qkv(&tq, &tk, &tv, base, h, s0, bb, bar_ld);
+    tma_issued = 1;
+  }
   for (int c = 0; c < nch && !bad; ++c) {
     const int t0 = s0 + c * kC;
-    // ---- phase 1: q' = ReLU(q), k' = ReLU(k), v
-    load_tiles(q, k, v, row0, n, t0, a.H, h, base);
+    // ---- phase 1: the chunk's q, k, v (TMA, requested one chunk ahead); q' = ReLU(q), k' = ReLU(k)
+    if (!tc::mbar_wait(bar_ld, c & 1, kWait)) atomicExch(s_abort, 1);
+    rectify_qk(base);
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
@@ -195,7 +180,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::mma_commit(bar1);
     }
-    if (c + 1 < nch) prefetch_chunk(q, k, v, row0, n, t0 + kC, a.H, h);
     if (!wait_mma(bar1, c & 1)) atomicExch(s_abort, 1);
     // ---- phase 3: den^2 = sum P^2 + q' . X;  P~ (masked, bf16)
     float den;
@@ -240,6 +224,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mma_commit(bar2);
     }
     if (!wait_mma(bar2, c & 1)) atomicExch(s_abort, 1);
+    // every MMA has read q', k', v: the next chunk's tiles may arrive while this one finishes
+    if (tid == 0 && c + 1 < nch && !*reinterpret_cast<volatile int*>(s_abort)) {
+      tma_qkv(&tq, &tk, &tv, base, h, t0 + kC, bb, bar_ld);
+      ++tma_issued;
+    }
     // ---- phase 5: out = X / den; S, A -> S~, A~
     {
       float xv[32];
@@ -265,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
   }
   bad = bad || *reinterpret_cast<volatile int*>(s_abort) != 0;
+  if (tid == 0 && tma_issued > 0) tc::mbar_wait(bar_ld, (tma_issued - 1) & 1, kWait);
   __syncthreads();
   if (bad) {  // a wait gave up: NaN over this segment's rows, so the failure cannot pass for a result
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out);
@@ -318,7 +308,12 @@ cudaError_t launch_l2_causal_tc(const L2Args& a, int nseg, int seg_len, cudaStre
   const long grid = static_cast<long>(a.B) * a.H * nseg;
   if (grid == 0 || a.L == 0) return cudaSuccess;
   if (nseg > 1 && (e = launch_l2_moments_tc(a, nseg, seg_len, stream)) != cudaSuccess) return e;
-  l2c_tc_kernel<<<static_cast<unsigned>(grid), kThreads, LayC::BYTES, stream>>>(a, nseg, seg_len);
+  CUtensorMap tq, tk, tv;
+  if ((e = make_bshd_map(&tq, a.q, a.B, a.L, a.H, kD)) != cudaSuccess) return e;
+  if ((e = make_bshd_map(&tk, a.k, a.B, a.L, a.H, kD)) != cudaSuccess) return e;
+  if ((e = make_bshd_map(&tv, a.v, a.B, a.L, a.H, kD)) != cudaSuccess) return e;
+  l2c_tc_kernel<<<static_cast<unsigned>(grid), kThreads, LayC::BYTES, stream>>>(a, nseg, seg_len, tq,
+                                                                              tk, tv);
   note_launches(1);
   return cudaGetLastError();
 }
