@@ -521,9 +521,11 @@ def run_gpu(args, rank, world, local):
                              "tensor_tflops_algorithmic": g_flops / (g_mean * 1e-3) / 1e12,
                              "traffic": read_traffic("backward", "segment_state_kernel",
                                                      "bwd_tc_forward", "bwd_tc_revstate",
-                                                     "bwd_tc_reverse", "bwd_gain_kernel"),
+                                                     "bwd_tc_reverse", "bwd_tc_features",
+                                                     "bwd_gain_kernel"),
                              "kernels": "segment_state_kernel + bwd_tc_forward + bwd_tc_revstate + "
-                                        "bwd_tc_reverse + bwd_gain_kernel (one call; tensor cores)"}}
+                                        "bwd_tc_reverse + bwd_tc_features + bwd_gain_kernel (one "
+                                        "call; tensor cores)"}}
     del tg, gws, grads
 
     # ---------------- one RAPT layer around the headline attention (d_model = H d = 2048), and its
