@@ -3,7 +3,8 @@
 //
 // The gradients of sum dout . out (08-rapt-algorithm.md §4.2 "backward": the main and z scans,
 // gnum = g / den and scale = -(g . num) / den^2, two suffix scans, then ReLU, RoPE and RMSNorm
-// backwards) in chunked form, C = 128 tokens per chunk (the MMA's M). Per document and head:
+// backwards) in chunked form, C = 128 tokens per chunk (the MMA's M). First, fully parallel over
+// (document, head, chunk): q' and k' (bf16) of every row into the workspace. Per document and head:
 //
 // Pass A (chunks in order; prefix state S = sum k'v^T in TMEM, its bf16 copy S~ in shared memory):
 //   P  = Q'K'^T,  Cv = G V^T,  U = G S~^T,  S += K'^T V                     (one MMA group)
@@ -23,9 +24,10 @@
 //   dk' (bf16) to the workspace.
 // Then, fully parallel over (document, head, chunk), dq and dk through the feature map (ReLU mask,
 // inverse RoPE rotation, RMSNorm backward) from dq', dk' and the raw q, k, with gain partials.
-// One CTA per (document, head), 512 threads in lockstep phases: all threads compute features, read
-// TMEM rows (thread = TMEM lane = tile row, four warps per lane quarter splitting the columns) and
-// run the feature backward; one thread issues the MMAs and commits them to an mbarrier. Every
+// The passes run one CTA per (document, head, segment), 512 threads in lockstep phases: all threads
+// read TMEM rows (thread = TMEM lane = tile row, four warps per lane quarter splitting the columns)
+// and do the per-row arithmetic; one thread issues the MMAs and the TMA copies of the next chunk's
+// tiles and commits them to mbarriers. Every
 // wait is bounded (~1 s); a CTA whose wait gives up sets RAPT_DEV_INTERNAL in the status word and
 // writes NaN gain partials, so a failure cannot pass for a result.
 #include <cuda.h>
@@ -189,19 +191,12 @@ __device__ __forceinline__ void clear_rows(uint32_t tile, int nvalid) {
     sts16(tile + tile_off(idx >> 4, idx & 15), make_uint4(0, 0, 0, 0));
 }
 
-// Features of the chunk's rows in place: the tile holds raw rows (by TMA); warp w takes rows w,
-// w + 16, ... (lane r: elements 4r .. 4r+3) and writes the bf16 features over them (zeros for rows
-// past the document). With z given, q'.z of every row into sst[]; the column sums go to zc; with
-// out given, the valid rows' features are stored there too.
-__device__ __forceinline__ void features_in_place(uint32_t tile, long row0, int n, int t0, int H,
-                                                  int h, const float* gamma, int pos0,
-                                                  const FeatureArgs& fa, const float* z, float* sst,
-                                                  float (&zc)[4], __nv_bfloat16* out) {
+// Sums over the features of a chunk (bf16 in the tile, by TMA from the workspace; warp w takes rows
+// w, w + 16, ..., lane r elements 4r .. 4r+3): with z given, q'.z of every row into sst[] (zero past
+// the document); the column sums of the rows inside the document are added to zc.
+__device__ __forceinline__ void feature_sums(uint32_t tile, int n, int t0, const float* z, float* sst,
+                                             float (&zc)[4]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float g[4];
-  lane_gains(gamma, lane, g);
-  LaneRope rope;
-  rope_start(rope, pos0 + t0 + warp, fa, lane);
   float zl[4] = {0.f, 0.f, 0.f, 0.f};
   if (z != nullptr) {
     const float4 zz = *reinterpret_cast<const float4*>(z + 4 * lane);
@@ -218,24 +213,15 @@ __device__ __forceinline__ void features_in_place(uint32_t tile, long row0, int 
 #pragma unroll
     for (int i = 0; i < kRB; ++i) {
       const int rr = warp + kWarps * (i0 + i);
-      const int t = t0 + rr;
-      const bool valid = t < n;
-      if (i0 + i > 0) rope_next(rope);
-      float f[4];
+      const bool valid = t0 + rr < n;
       const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&lo[i]));
       const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi[i]));
-      f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-      feat_lane(f, valid, g, rope, fa.eps_norm);
-      const uint32_t plo = tc::pack_bf16x2(f[0], f[1]), phi = tc::pack_bf16x2(f[2], f[3]);
-      const uint32_t addr = tile + tile_off(rr, lane >> 1) + (lane & 1) * 8;
-      asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(plo), "r"(phi) : "memory");
-      if (out != nullptr && valid)
-        *reinterpret_cast<uint2*>(out + ((row0 + t) * H + h) * kD + 4 * lane) = make_uint2(plo, phi);
+      const float f[4] = {valid ? a.x : 0.f, valid ? a.y : 0.f, valid ? b.x : 0.f, valid ? b.y : 0.f};
       if (z != nullptr) {
         float sdot = f[0] * zl[0] + f[1] * zl[1] + f[2] * zl[2] + f[3] * zl[3];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) sdot += __shfl_xor_sync(0xffffffffu, sdot, off);
-        if (lane == 0) sst[rr] = valid ? sdot : 0.f;
+        if (lane == 0) sst[rr] = sdot;
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) zc[e] += f[e];
@@ -283,8 +269,8 @@ __device__ __forceinline__ void raw_tiles_tc(const __nv_bfloat16* const (&src)[N
 // ------------------------------------------------------------------------------------------------
 // Pass A: chunks in order.
 __global__ void __launch_bounds__(kThreads, 1)
-    bwd_tc_forward(const BwdArgs b, const __grid_constant__ CUtensorMap tmq,
-                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+    bwd_tc_forward(const BwdArgs b, const __grid_constant__ CUtensorMap tmqf,
+                   const __grid_constant__ CUtensorMap tmkf, const __grid_constant__ CUtensorMap tmv,
                    const __grid_constant__ CUtensorMap tmg) {
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -356,36 +342,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
 
-  const float* gq = a.gamma_q + h * a.fa.gamma_stride;
-  const float* gk = a.gamma_k + h * a.fa.gamma_stride;
-  const CUtensorMap* const maps[4] = {&tmq, &tmk, &tmv, &tmg};
+  const CUtensorMap* const maps[4] = {&tmqf, &tmkf, &tmv, &tmg};
   const uint32_t ld_tiles[4] = {base + Lay::QF, base + Lay::KF, base + Lay::VS, base + Lay::GS};
   int tma_issued = 0;  // chunks whose tiles have been requested (thread 0)
   if (tid == 0 && nch > 0 && !*s_abort) {
     tma_chunk<4>(maps, ld_tiles, h, static_cast<int>(row0 + s0), bar_ld);
     tma_issued = 1;
   }
-  __nv_bfloat16* qf_out = static_cast<__nv_bfloat16*>(b.qf);
-  __nv_bfloat16* kf_out = static_cast<__nv_bfloat16*>(b.kf);
   __nv_bfloat16* dqf_out = static_cast<__nv_bfloat16*>(b.dqf);
   bool bad = *s_abort != 0;
 
   for (int c = 0; c < nch && !bad; ++c) {
     const int t0 = s0 + c * kC;
-    // ---- phase 1: the chunk's raw tiles (TMA); features in place (q'.z of every row, column
-    // sums of k'); rows past the document cleared
+    // ---- phase 1: the chunk's tiles (TMA; q' and k' from the feature kernel); q'.z of every
+    // row and the column sums of k'; rows past the document cleared
     if (!tc::mbar_wait(bar_ld, c & 1, kWait)) atomicExch(s_abort, 1);
-    float zc[4] = {0.f, 0.f, 0.f, 0.f}, dummy[4] = {0.f, 0.f, 0.f, 0.f};
-    features_in_place(base + Lay::QF, row0, n, t0, a.H, h, gq, a.pos_offset, a.fa, zs, sst_s, dummy,
-                      qf_out);
-    features_in_place(base + Lay::KF, row0, n, t0, a.H, h, gk, a.pos_offset, a.fa, nullptr, nullptr,
-                      zc, kf_out);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) zp[warp * kD + 4 * lane + e] = zc[e];
-    if (t0 + kC > n) {
+    if (t0 + kC > n) {  // uniform over the CTA
+      clear_rows(base + Lay::QF, n - t0);
+      clear_rows(base + Lay::KF, n - t0);
       clear_rows(base + Lay::VS, n - t0);
       clear_rows(base + Lay::GS, n - t0);
+      __syncthreads();
     }
+    float zc[4] = {0.f, 0.f, 0.f, 0.f}, dummy[4] = {0.f, 0.f, 0.f, 0.f};
+    feature_sums(base + Lay::QF, n, t0, zs, sst_s, dummy);
+    feature_sums(base + Lay::KF, n, t0, nullptr, nullptr, zc);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) zp[warp * kD + 4 * lane + e] = zc[e];
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
@@ -928,12 +911,60 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_revstate(const BwdArgs b) 
 }
 
 // ------------------------------------------------------------------------------------------------
-// After the passes, fully parallel: dq and dk through the feature map from dq', dk' (bf16, in the
-// workspace) and the raw q, k, with the gain partials of every (document, head, 128-token chunk).
-// One CTA of 8 warps per (document, head, chunk, q or k); warp w takes rows w, w + 8, ...
+// The fully parallel kernels around the passes: one CTA of 8 warps per (document, head, chunk,
+// q or k).
 constexpr int kFWarps = 8;
-constexpr int kFRows = kC / kFWarps;  // 16 rows per warp, in batches of 4
+constexpr int kFRows = kC / kFWarps;  // 16 rows per warp
 
+// Before the passes, fully parallel: q' = ReLU(RoPE(RMSNorm(q))) and k' likewise (bf16) of every
+// row into the workspace, where the forward and reverse passes take their q', k' tiles from. One
+// CTA of 8 warps per (document, head, chunk, q or k); warp w takes rows w, w + 8, ...
+__global__ void __launch_bounds__(kFWarps * 32) bwd_tc_featmap(const BwdArgs b) {
+  const PrefillArgs& a = b.p;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int which = blockIdx.x & 1;  // 0: q, 1: k
+  const int chunk = (blockIdx.x >> 1) % b.chunks_max, unit = (blockIdx.x >> 1) / b.chunks_max;
+  const int h = unit % a.H, doc = unit / a.H;
+  long row0;
+  int n;
+  doc_bounds(a, doc, row0, n);
+  const int t0 = chunk * kC;
+  if (t0 >= n) return;
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(which ? a.k : a.q);
+  __nv_bfloat16* xf = static_cast<__nv_bfloat16*>(which ? b.kf : b.qf);
+  const float* gamma = (which ? a.gamma_k : a.gamma_q) + h * a.fa.gamma_stride;
+  float g[4];
+  lane_gains(gamma, lane, g);
+  LaneRope rope;
+  rope_start(rope, a.pos_offset + t0 + warp, a.fa, lane, kFWarps);
+#pragma unroll 1
+  for (int i0 = 0; i0 < kFRows; i0 += 8) {
+    uint2 rx[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int t = t0 + warp + kFWarps * (i0 + i);
+      rx[i] = t < n ? __ldg(reinterpret_cast<const uint2*>(x + ((row0 + t) * a.H + h) * kD + 4 * lane))
+                    : make_uint2(0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int t = t0 + warp + kFWarps * (i0 + i);
+      const bool valid = t < n;
+      if (i0 + i > 0) rope_next(rope);
+      const float2 x0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rx[i].x));
+      const float2 x1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rx[i].y));
+      float f[4] = {x0.x, x0.y, x1.x, x1.y};
+      feat_lane(f, valid, g, rope, a.fa.eps_norm);
+      if (valid)
+        *reinterpret_cast<uint2*>(xf + ((row0 + t) * a.H + h) * kD + 4 * lane) =
+            make_uint2(tc::pack_bf16x2(f[0], f[1]), tc::pack_bf16x2(f[2], f[3]));
+    }
+  }
+}
+
+// After the passes: dq and dk through the feature map from dq', dk' (bf16, in the workspace) and the
+// raw q, k, with the gain partials of every (document, head, 128-token chunk); warp w takes rows w,
+// w + 8, ... in batches of 4.
 __global__ void __launch_bounds__(kFWarps * 32) bwd_tc_features(const BwdArgs b) {
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1014,6 +1045,10 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   }
   const long grid = static_cast<long>(b.p.n_docs) * b.p.H * b.nseg;
   if (grid == 0) return cudaSuccess;
+  const long fgrid = static_cast<long>(b.p.n_docs) * b.p.H * b.chunks_max * 2;
+  bwd_tc_featmap<<<static_cast<unsigned>(fgrid), kFWarps * 32, 0, stream>>>(b);  // q', k'
+  note_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (b.nseg > 1) {  // the prefix-state increments of the blocks before each document's last segment
     TcArgs ta{};
     ta.p = b.p;
@@ -1027,15 +1062,14 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
     if ((e = launch_state_tc(kD, ta, stream)) != cudaSuccess) return e;
   }
   // TMA maps of the row-major [rows, H, D] tensors the passes stream
-  CUtensorMap tmq, tmk, tmv, tmg, tmqf, tmkf;
+  CUtensorMap tmv, tmg, tmqf, tmkf;
   const long rows = b.p.total_rows;
-  if ((e = make_rows_map(&tmq, b.p.q, rows, b.p.H, kD)) != cudaSuccess) return e;
-  if ((e = make_rows_map(&tmk, b.p.k, rows, b.p.H, kD)) != cudaSuccess) return e;
   if ((e = make_rows_map(&tmv, b.p.v, rows, b.p.H, kD)) != cudaSuccess) return e;
   if ((e = make_rows_map(&tmg, b.dout, rows, b.p.H, kD)) != cudaSuccess) return e;
   if ((e = make_rows_map(&tmqf, b.qf, rows, b.p.H, kD)) != cudaSuccess) return e;
   if ((e = make_rows_map(&tmkf, b.kf, rows, b.p.H, kD)) != cudaSuccess) return e;
-  bwd_tc_forward<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b, tmq, tmk, tmv, tmg);
+  bwd_tc_forward<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b, tmqf, tmkf, tmv,
+                                                                                 tmg);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (b.nseg > 1) {
@@ -1047,7 +1081,6 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
                                                                                  tmg);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const long fgrid = static_cast<long>(b.p.n_docs) * b.p.H * b.chunks_max * 2;
   bwd_tc_features<<<static_cast<unsigned>(fgrid), kFWarps * 32, 0, stream>>>(b);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
