@@ -109,27 +109,9 @@ __device__ __forceinline__ void rope_next(LaneRope& r) {
   }
 }
 
-// f = ReLU(RoPE(RMSNorm(x))) of one row on a lane's four elements (the warp together: the row's sum
-// of squares is reduced by shuffles); g: the lane's four gains.
-__device__ __forceinline__ void feat_lane(float (&f)[4], bool valid, const float (&g)[4],
-                                          const LaneRope& r, float eps) {
-  float ss = f[0] * f[0] + f[1] * f[1] + f[2] * f[2] + f[3] * f[3];
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-  const float rinv = rsqrtf(ss * (1.0f / kD) + eps);
-#pragma unroll
-  for (int m = 0; m < 2; ++m) {
-    const float y0 = f[2 * m] * rinv * g[2 * m];
-    const float y1 = f[2 * m + 1] * rinv * g[2 * m + 1];
-    const float a = fmaf(y0, r.c[m], -y1 * r.s[m]);
-    const float b = fmaf(y0, r.s[m], y1 * r.c[m]);
-    f[2 * m] = valid ? fmaxf(a, 0.f) : 0.f;
-    f[2 * m + 1] = valid ? fmaxf(b, 0.f) : 0.f;
-  }
-}
-
-// Backward of feat_lane for one row (x values in f, the row's gradient of the features in df):
-// writes dx (valid rows) and adds the gain gradient to dg.
+// Backward of the feature map f = ReLU(RoPE(RMSNorm(x))) for one row on a lane's four elements (the
+// warp together: the row's sums are reduced by shuffles; x values in f, the row's gradient of the
+// features in df): writes dx (valid rows) and adds the gain gradient to dg.
 __device__ __forceinline__ void feat_lane_bwd(const float (&f)[4], bool valid, const float (&g)[4],
                                               const LaneRope& r, float eps, const float* df,
                                               __nv_bfloat16* dx, float (&dg)[4]) {
@@ -918,10 +900,15 @@ constexpr int kFRows = kC / kFWarps;  // 16 rows per warp
 
 // Before the passes, fully parallel: q' = ReLU(RoPE(RMSNorm(q))) and k' likewise (bf16) of every
 // row into the workspace, where the forward and reverse passes take their q', k' tiles from. One
-// CTA of 8 warps per (document, head, chunk, q or k); warp w takes rows w, w + 8, ...
-__global__ void __launch_bounds__(kFWarps * 32) bwd_tc_featmap(const BwdArgs b) {
+// CTA of 256 threads per (document, head, chunk, q or k); a thread owns 8 consecutive elements of a
+// row (16 threads per row, 16 rows per pass, all 8 passes' loads in flight at once) and works on
+// packed fp32 pairs, with the gains and the RoPE frequencies and per-pass rotation in shared memory.
+constexpr int kMThreads = 256;
+
+__global__ void __launch_bounds__(kMThreads) bwd_tc_featmap(const BwdArgs b) {
+  constexpr int TPR = kD / 8, RPP = kMThreads / TPR, NPASS = kC / RPP;
   const PrefillArgs& a = b.p;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
   const int which = blockIdx.x & 1;  // 0: q, 1: k
   const int chunk = (blockIdx.x >> 1) % b.chunks_max, unit = (blockIdx.x >> 1) / b.chunks_max;
   const int h = unit % a.H, doc = unit / a.H;
@@ -929,36 +916,35 @@ __global__ void __launch_bounds__(kFWarps * 32) bwd_tc_featmap(const BwdArgs b) 
   int n;
   doc_bounds(a, doc, row0, n);
   const int t0 = chunk * kC;
-  if (t0 >= n) return;
-  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(which ? a.k : a.q);
-  __nv_bfloat16* xf = static_cast<__nv_bfloat16*>(which ? b.kf : b.qf);
-  const float* gamma = (which ? a.gamma_k : a.gamma_q) + h * a.fa.gamma_stride;
-  float g[4];
-  lane_gains(gamma, lane, g);
-  LaneRope rope;
-  rope_start(rope, a.pos_offset + t0 + warp, a.fa, lane, kFWarps);
-#pragma unroll 1
-  for (int i0 = 0; i0 < kFRows; i0 += 8) {
-    uint2 rx[8];
+  if (t0 >= n) return;  // uniform
+  __shared__ __align__(16) float tabmem[4 * kD];
+  const feat::FeatTab tab = feat::feat_tab<kD>(reinterpret_cast<uint8_t*>(tabmem));
+  feat::fill_tab<kD>(tab, a, h, RPP, tid, kMThreads);
+  __syncthreads();
+  const int prow = tid / TPR, part = tid % TPR, e0 = 8 * part;
+  const long rstride = static_cast<long>(a.H) * kD;
+  const long off0 = (row0 + t0 + prow) * rstride + static_cast<long>(h) * kD + e0;
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(which ? a.k : a.q) + off0;
+  __nv_bfloat16* xf = static_cast<__nv_bfloat16*>(which ? b.kf : b.qf) + off0;
+  uint4 raw[NPASS];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int t = t0 + warp + kFWarps * (i0 + i);
-      rx[i] = t < n ? __ldg(reinterpret_cast<const uint2*>(x + ((row0 + t) * a.H + h) * kD + 4 * lane))
-                    : make_uint2(0, 0);
-    }
+  for (int p = 0; p < NPASS; ++p)
+    raw[p] = t0 + p * RPP + prow < n ? feat::ldg16(x + p * RPP * rstride) : make_uint4(0, 0, 0, 0);
+  float2 g0[2], g1[2];
+  feat::split_load<kD>(which ? tab.gk : tab.gq, part, g0, g1);
+  feat::Rot step, rot;
+  feat::tab_step(tab, e0 / 2, step);
+  feat::tab_rot_at(tab, a.pos_offset + t0 + prow, e0 / 2, rot);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int t = t0 + warp + kFWarps * (i0 + i);
-      const bool valid = t < n;
-      if (i0 + i > 0) rope_next(rope);
-      const float2 x0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rx[i].x));
-      const float2 x1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rx[i].y));
-      float f[4] = {x0.x, x0.y, x1.x, x1.y};
-      feat_lane(f, valid, g, rope, a.fa.eps_norm);
-      if (valid)
-        *reinterpret_cast<uint2*>(xf + ((row0 + t) * a.H + h) * kD + 4 * lane) =
-            make_uint2(tc::pack_bf16x2(f[0], f[1]), tc::pack_bf16x2(f[2], f[3]));
-    }
+  for (int p = 0; p < NPASS; ++p) {
+    if (p > 0) feat::rot_step(rot, step);
+    feat::Pairs f = feat::unpack_pairs(raw[p]);
+    const float ss = feat::row_sum<TPR>(feat::sumsq(f));
+    float2 ga[2] = {g0[0], g0[1]}, gb[2] = {g1[0], g1[1]};
+    feat::scale_gains(ga, gb, rsqrtf(ss * (1.0f / kD) + a.fa.eps_norm));
+    feat::rope_relu(f, ga, gb, rot);
+    if (t0 + p * RPP + prow < n)
+      *reinterpret_cast<uint4*>(xf + p * RPP * rstride) = feat::pack_pairs(f);
   }
 }
 
@@ -1046,7 +1032,7 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   const long grid = static_cast<long>(b.p.n_docs) * b.p.H * b.nseg;
   if (grid == 0) return cudaSuccess;
   const long fgrid = static_cast<long>(b.p.n_docs) * b.p.H * b.chunks_max * 2;
-  bwd_tc_featmap<<<static_cast<unsigned>(fgrid), kFWarps * 32, 0, stream>>>(b);  // q', k'
+  bwd_tc_featmap<<<static_cast<unsigned>(fgrid), kMThreads, 0, stream>>>(b);  // q', k'
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (b.nseg > 1) {  // the prefix-state increments of the blocks before each document's last segment
