@@ -83,76 +83,6 @@ constexpr int kRPW = kC / kWarps;  // rows per warp
 constexpr int kRB = kRPW / 2;  // rows of a warp loaded together (two batches per tile)
 
 
-// RoPE rotations of a lane's two pairs (elements 4 lane .. 4 lane + 3 are pairs 2 lane, 2 lane + 1)
-// for the rows a warp takes (positions p, p + 16, ...): exact sin / cos at the chunk's first row of
-// the warp, then one complex multiplication by the rotation over 16 positions per row.
-struct LaneRope {
-  float c[2], s[2];    // the current row
-  float cs[2], ss[2];  // the step to the warp's next row
-};
-__device__ __forceinline__ void rope_start(LaneRope& r, int pos, const FeatureArgs& fa, int lane,
-                                           int step = kWarps) {
-#pragma unroll
-  for (int m = 0; m < 2; ++m) {
-    const int j = 2 * lane + m;
-    rope_sincos(pos, fa.rope_hi[j], fa.rope_lo[j], r.s[m], r.c[m]);
-    rope_sincos(step, fa.rope_hi[j], fa.rope_lo[j], r.ss[m], r.cs[m]);
-  }
-}
-__device__ __forceinline__ void rope_next(LaneRope& r) {
-#pragma unroll
-  for (int m = 0; m < 2; ++m) {
-    const float c = fmaf(r.c[m], r.cs[m], -r.s[m] * r.ss[m]);
-    const float s = fmaf(r.s[m], r.cs[m], r.c[m] * r.ss[m]);
-    r.c[m] = c;
-    r.s[m] = s;
-  }
-}
-
-// Backward of the feature map f = ReLU(RoPE(RMSNorm(x))) for one row on a lane's four elements (the
-// warp together: the row's sums are reduced by shuffles; x values in f, the row's gradient of the
-// features in df): writes dx (valid rows) and adds the gain gradient to dg.
-__device__ __forceinline__ void feat_lane_bwd(const float (&f)[4], bool valid, const float (&g)[4],
-                                              const LaneRope& r, float eps, const float* df,
-                                              __nv_bfloat16* dx, float (&dg)[4]) {
-  float ss = f[0] * f[0] + f[1] * f[1] + f[2] * f[2] + f[3] * f[3];
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-  const float rinv = rsqrtf(ss * (1.0f / kD) + eps);
-  float u[4], dot = 0.f;
-#pragma unroll
-  for (int m = 0; m < 2; ++m) {
-    const float y0 = f[2 * m] * rinv * g[2 * m];
-    const float y1 = f[2 * m + 1] * rinv * g[2 * m + 1];
-    const float a = fmaf(y0, r.c[m], -y1 * r.s[m]);  // the forward's pre-activation
-    const float b = fmaf(y0, r.s[m], y1 * r.c[m]);
-    const float da = (valid && a > 0.f) ? df[2 * m] : 0.f;
-    const float db = (valid && b > 0.f) ? df[2 * m + 1] : 0.f;
-    const float h0 = fmaf(da, r.c[m], db * r.s[m]);  // inverse rotation
-    const float h1 = fmaf(-da, r.s[m], db * r.c[m]);
-    dg[2 * m] = fmaf(h0, f[2 * m] * rinv, dg[2 * m]);
-    dg[2 * m + 1] = fmaf(h1, f[2 * m + 1] * rinv, dg[2 * m + 1]);
-    u[2 * m] = g[2 * m] * h0;
-    u[2 * m + 1] = g[2 * m + 1] * h1;
-    dot = fmaf(u[2 * m], f[2 * m], dot);
-    dot = fmaf(u[2 * m + 1], f[2 * m + 1], dot);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-  const float c3 = rinv * rinv * rinv * dot * (1.0f / kD);
-  if (valid) {
-    const uint32_t lo = tc::pack_bf16x2(fmaf(rinv, u[0], -f[0] * c3), fmaf(rinv, u[1], -f[1] * c3));
-    const uint32_t hi = tc::pack_bf16x2(fmaf(rinv, u[2], -f[2] * c3), fmaf(rinv, u[3], -f[3] * c3));
-    *reinterpret_cast<uint2*>(dx) = make_uint2(lo, hi);
-  }
-}
-
-__device__ __forceinline__ void lane_gains(const float* gamma, int lane, float (&g)[4]) {
-  const float4 v = *reinterpret_cast<const float4*>(gamma + 4 * lane);
-  g[0] = v.x; g[1] = v.y; g[2] = v.z; g[3] = v.w;
-}
-
-
 // One chunk's 128 rows of nt [rows, H, D] tensors into their tiles by TMA (two 64-column boxes
 // each, in the swizzled operand layout), completing on one mbarrier; one thread calls it. Rows
 // past the tensor read as zero; rows past the document but inside the tensor are other tokens,
@@ -893,11 +823,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_revstate(const BwdArgs b) 
 }
 
 // ------------------------------------------------------------------------------------------------
-// The fully parallel kernels around the passes: one CTA of 8 warps per (document, head, chunk,
-// q or k).
-constexpr int kFWarps = 8;
-constexpr int kFRows = kC / kFWarps;  // 16 rows per warp
-
 // Before the passes, fully parallel: q' = ReLU(RoPE(RMSNorm(q))) and k' likewise (bf16) of every
 // row into the workspace, where the forward and reverse passes take their q', k' tiles from. One
 // CTA of 256 threads per (document, head, chunk, q or k); a thread owns 8 consecutive elements of a
@@ -949,9 +874,15 @@ __global__ void __launch_bounds__(kMThreads) bwd_tc_featmap(const BwdArgs b) {
 }
 
 // After the passes: dq and dk through the feature map from dq', dk' (bf16, in the workspace) and the
-// raw q, k, with the gain partials of every (document, head, 128-token chunk); warp w takes rows w,
-// w + 8, ... in batches of 4.
-__global__ void __launch_bounds__(kFWarps * 32) bwd_tc_features(const BwdArgs b) {
+// raw q, k, with the gain partials of every (document, head, 128-token chunk). Same layout as the
+// feature kernel (256 threads, 16 per row, packed fp32 pairs). Per row, with r = 1/rms(x) and the
+// forward's pre-activations (a, b) = R(y) of y = x r gamma (R: the pair's rotation):
+//   (da, db) = the feature gradient where the pre-activation is positive, else 0 (ReLU),
+//   h = R^T (da, db) (the inverse rotation), u = gamma h,
+//   dx = r u - x r^3 (u . x) / d,   dgamma += h x r.
+__global__ void __launch_bounds__(kMThreads, 3) bwd_tc_features(const BwdArgs b) {
+  constexpr int TPR = kD / 8, RPP = kMThreads / TPR, NPASS = kC / RPP;
+  constexpr int WARPS = kMThreads / 32;
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int which = blockIdx.x & 1;  // 0: q, 1: k
@@ -961,51 +892,87 @@ __global__ void __launch_bounds__(kFWarps * 32) bwd_tc_features(const BwdArgs b)
   int n;
   doc_bounds(a, doc, row0, n);
   const int t0 = chunk * kC;
-  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(which ? a.k : a.q);
-  const __nv_bfloat16* df = static_cast<const __nv_bfloat16*>(which ? b.dkf : b.dqf);
-  __nv_bfloat16* dx = static_cast<__nv_bfloat16*>(which ? b.dk : b.dq);
-  const float* gamma = (which ? a.gamma_k : a.gamma_q) + h * a.fa.gamma_stride;
-  __shared__ float scratch[kFWarps * kD];
-  float dg[4] = {0.f, 0.f, 0.f, 0.f};
-  if (t0 < n) {
-    float g[4];
-    lane_gains(gamma, lane, g);
-    LaneRope rope;
-    rope_start(rope, a.pos_offset + t0 + warp, a.fa, lane, kFWarps);
+  __shared__ __align__(16) float tabmem[4 * kD];
+  __shared__ __align__(16) float scratch[WARPS * kD];
+  const int prow = tid / TPR, part = tid % TPR, e0 = 8 * part;
+  float2 dga[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // gain gradient, Pairs layout
+  float2 dgb[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  if (t0 < n) {  // uniform; a chunk past the document's end contributes zero partials
+    const feat::FeatTab tab = feat::feat_tab<kD>(reinterpret_cast<uint8_t*>(tabmem));
+    feat::fill_tab<kD>(tab, a, h, RPP, tid, kMThreads);
+    __syncthreads();
+    const long rstride = static_cast<long>(a.H) * kD;
+    const long off0 = (row0 + t0 + prow) * rstride + static_cast<long>(h) * kD + e0;
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(which ? a.k : a.q) + off0;
+    const __nv_bfloat16* df = static_cast<const __nv_bfloat16*>(which ? b.dkf : b.dqf) + off0;
+    __nv_bfloat16* dx = static_cast<__nv_bfloat16*>(which ? b.dk : b.dq) + off0;
+    float2 g0[2], g1[2];
+    feat::split_load<kD>(which ? tab.gk : tab.gq, part, g0, g1);
+    feat::Rot step, rot;
+    feat::tab_step(tab, e0 / 2, step);
+    feat::tab_rot_at(tab, a.pos_offset + t0 + prow, e0 / 2, rot);
 #pragma unroll 1
-    for (int i0 = 0; i0 < kFRows; i0 += 4) {
-      uint2 rx[4], rd[4];
+    for (int p0 = 0; p0 < NPASS; p0 += 2) {  // two passes' loads in flight at a time
+      uint4 rx[2], rd[2];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int t = t0 + warp + kFWarps * (i0 + i);
-        const long off = ((row0 + t) * a.H + h) * kD + 4 * lane;
-        rx[i] = t < n ? __ldg(reinterpret_cast<const uint2*>(x + off)) : make_uint2(0, 0);
-        rd[i] = t < n ? __ldg(reinterpret_cast<const uint2*>(df + off)) : make_uint2(0, 0);
+      for (int i = 0; i < 2; ++i) {
+        const bool valid = t0 + (p0 + i) * RPP + prow < n;
+        rx[i] = valid ? feat::ldg16(x + (p0 + i) * RPP * rstride) : make_uint4(0, 0, 0, 0);
+        rd[i] = valid ? feat::ldg16(df + (p0 + i) * RPP * rstride) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int t = t0 + warp + kFWarps * (i0 + i);
-        const bool valid = t < n;
-        if (i0 + i > 0) rope_next(rope);
-        float f[4], d4[4];
-        const float2 x0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rx[i].x));
-        const float2 x1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rx[i].y));
-        const float2 d0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rd[i].x));
-        const float2 d1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rd[i].y));
-        f[0] = x0.x; f[1] = x0.y; f[2] = x1.x; f[3] = x1.y;
-        d4[0] = d0.x; d4[1] = d0.y; d4[2] = d1.x; d4[3] = d1.y;
-        const long off = ((row0 + (valid ? t : 0)) * a.H + h) * kD + 4 * lane;
-        feat_lane_bwd(f, valid, g, rope, a.fa.eps_norm, d4, dx + off, dg);
+      for (int i = 0; i < 2; ++i) {
+        const int p = p0 + i;
+        if (p > 0) feat::rot_step(rot, step);
+        const bool valid = t0 + p * RPP + prow < n;
+        const feat::Pairs f = feat::unpack_pairs(rx[i]), d = feat::unpack_pairs(rd[i]);
+        const float r = rsqrtf(feat::row_sum<TPR>(feat::sumsq(f)) * (1.0f / kD) + a.fa.eps_norm);
+        const float2 r2 = make_float2(r, r);
+        float2 dotv = make_float2(0.f, 0.f);
+        float2 u0[2], u1[2];
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          const float2 xr0 = __fmul2_rn(f.x0[g], r2), xr1 = __fmul2_rn(f.x1[g], r2);
+          const float2 y0 = __fmul2_rn(xr0, g0[g]), y1 = __fmul2_rn(xr1, g1[g]);
+          const float2 ns = make_float2(-rot.s[g].x, -rot.s[g].y);
+          const float2 pa = __ffma2_rn(y0, rot.c[g], __fmul2_rn(y1, ns));   // pre-activations
+          const float2 pb = __ffma2_rn(y0, rot.s[g], __fmul2_rn(y1, rot.c[g]));
+          const float2 da = make_float2(pa.x > 0.f ? d.x0[g].x : 0.f, pa.y > 0.f ? d.x0[g].y : 0.f);
+          const float2 db = make_float2(pb.x > 0.f ? d.x1[g].x : 0.f, pb.y > 0.f ? d.x1[g].y : 0.f);
+          const float2 h0 = __ffma2_rn(da, rot.c[g], __fmul2_rn(db, rot.s[g]));  // R^T (da, db)
+          const float2 h1 = __ffma2_rn(db, rot.c[g], __fmul2_rn(da, ns));
+          dga[g] = __ffma2_rn(h0, xr0, dga[g]);
+          dgb[g] = __ffma2_rn(h1, xr1, dgb[g]);
+          u0[g] = __fmul2_rn(g0[g], h0);
+          u1[g] = __fmul2_rn(g1[g], h1);
+          dotv = __ffma2_rn(u0[g], f.x0[g], dotv);
+          dotv = __ffma2_rn(u1[g], f.x1[g], dotv);
+        }
+        const float dot = feat::row_sum<TPR>(dotv.x + dotv.y);
+        const float c3 = r * r * r * dot * (1.0f / kD);
+        const float2 c32 = make_float2(-c3, -c3);
+        feat::Pairs o;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          o.x0[g] = __ffma2_rn(f.x0[g], c32, __fmul2_rn(r2, u0[g]));
+          o.x1[g] = __ffma2_rn(f.x1[g], c32, __fmul2_rn(r2, u1[g]));
+        }
+        if (valid) *reinterpret_cast<uint4*>(dx + p * RPP * rstride) = feat::pack_pairs(o);
       }
     }
   }
-  // the CTA's gain partial, summed over the warps in order (zeros past the document's end)
+  // the CTA's gain partial: each thread's rows, then the warp's two rows, then the warps in order
+  float dg[8];
+  feat::pairs_to8(feat::Pairs{{dga[0], dga[1]}, {dgb[0], dgb[1]}}, dg);
+  feat::warp_colsum<TPR>(dg);
+  if (lane < TPR) {
 #pragma unroll
-  for (int e = 0; e < 4; ++e) scratch[warp * kD + 4 * lane + e] = dg[e];
+    for (int e = 0; e < 8; ++e) scratch[warp * kD + e0 + e] = dg[e];
+  }
   __syncthreads();
   if (tid < kD) {
     float sum = 0.f;
-    for (int w = 0; w < kFWarps; ++w) sum += scratch[w * kD + tid];
+    for (int w = 0; w < WARPS; ++w) sum += scratch[w * kD + tid];
     (which ? b.dgp_k : b.dgp_q)[(static_cast<long>(unit) * b.chunks_max + chunk) * kD + tid] = sum;
   }
 }
@@ -1067,7 +1034,7 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
                                                                                  tmg);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_tc_features<<<static_cast<unsigned>(fgrid), kFWarps * 32, 0, stream>>>(b);
+  bwd_tc_features<<<static_cast<unsigned>(fgrid), kMThreads, 0, stream>>>(b);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   BwdArgs g = b;  // the gain partials are per (document, head, chunk)
