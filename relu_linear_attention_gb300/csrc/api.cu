@@ -335,6 +335,7 @@ rapt_status backward_common(const void* q, const void* k, const void* v, const v
   b.qf = w + plan.off_qf;
   b.kf = w + plan.off_kf;
   b.blk_per_seg = plan.blk_per_seg;
+  b.rblk_per_seg = plan.rblk_per_seg;
   b.nblk_max = plan.nblk_max;
   b.dqf = w + plan.off_dqf;
   b.dkf = w + plan.off_dkf;

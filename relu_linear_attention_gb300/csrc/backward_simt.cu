@@ -639,11 +639,21 @@ BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d, bool
         break;
       }
   }
+  // suffix-state blocks: the later segments' blocks should fill one wave of CTAs
+  p.rblk_per_seg = 1;
+  if (tc && p.nseg > 1) {
+    const int sc = p.seg_len / ck;
+    for (int f = 8; f > 1; f /= 2)
+      if (sc % f == 0 && units * (p.nseg - 1) * f <= kSMs) {
+        p.rblk_per_seg = f;
+        break;
+      }
+  }
   p.nblk_max = (p.nseg - 1) * p.blk_per_seg;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t rec = static_cast<size_t>(d) * (d + 1) * sizeof(float);
   const size_t recs_f = up(static_cast<size_t>(units) * (tc ? p.nblk_max : p.nseg) * rec);
-  const size_t recs_r = up(static_cast<size_t>(units) * p.nseg * rec);
+  const size_t recs_r = up(static_cast<size_t>(units) * p.nseg * p.rblk_per_seg * rec);
   const size_t rows = up(static_cast<size_t>(total_rows) * H * sizeof(float));
   const size_t feats = tc ? up(static_cast<size_t>(total_rows) * H * d * 2) : 0;
   p.chunks_max = tc ? chunks_max : 0;

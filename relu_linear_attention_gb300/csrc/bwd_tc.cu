@@ -481,12 +481,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the suffix state at the segment's end: the later segments' increments, in segment order
   if (nch > 0) {
     constexpr long REC = static_cast<long>(kD) * kD + kD;
-    const float* rr = b.rec_rev + static_cast<long>(unit) * b.nseg * REC;
+    // the records of the blocks that start inside the document, in block order
+    const int rlen = b.seg_len / b.rblk_per_seg;
+    const float* rr = b.rec_rev + static_cast<long>(unit) * b.nseg * b.rblk_per_seg * REC;
+    const int k0 = (seg + 1) * b.rblk_per_seg, k1 = min(b.nseg * b.rblk_per_seg, (n + rlen - 1) / rlen);
     float rv[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) rv[e] = 0.f;
-    for (int sp = seg + 1; sp < b.nseg && sp * b.seg_len < n; ++sp) {
-      const float4* src = reinterpret_cast<const float4*>(rr + sp * REC + t * kD + 32 * gw);
+    for (int kb = k0; kb < k1; ++kb) {
+      const float4* src = reinterpret_cast<const float4*>(rr + kb * REC + t * kD + 32 * gw);
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
         const float4 x = __ldcg(src + jj);
@@ -496,8 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     state_put(tmem + tl + kTR + 32 * gw, base + Lay::XS, t, gw, rv);
     if (tid < kD) {
       float w = 0.f;
-      for (int sp = seg + 1; sp < b.nseg && sp * b.seg_len < n; ++sp)
-        w += __ldcg(rr + sp * REC + kD * kD + tid);
+      for (int kb = k0; kb < k1; ++kb) w += __ldcg(rr + kb * REC + kD * kD + tid);
       ws[tid] = w;
     }
   }
@@ -714,19 +716,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------------------------------------
-// Between the passes: the suffix-state increment of every segment after a document's first,
-// R_seg = sum_{t in seg} q'_t gnum_t^T and w_seg = sum scale_t q'_t (q' stored by pass A, gnum =
-// g / den), written as fp32 records [R row-major | w] for pass B.
+// Between the passes: the suffix-state increment of every block of the segments after a document's
+// first (rblk_per_seg blocks per segment), R_blk = sum_{t in blk} q'_t gnum_t^T and w_blk = sum
+// scale_t q'_t (q' from the feature kernel, gnum = g / den), written as fp32 records [R row-major |
+// w] for pass B.
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_revstate(const BwdArgs b) {
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int seg = blockIdx.x % b.nseg, unit = blockIdx.x / b.nseg;
+  const int blk = blockIdx.x % b.rblk_per_seg;
+  const int seg = (blockIdx.x / b.rblk_per_seg) % b.nseg, unit = blockIdx.x / (b.rblk_per_seg * b.nseg);
   const int h = unit % a.H, doc = unit / a.H;
   long row0;
   int n;
   doc_bounds(a, doc, row0, n);
-  const int s0 = seg * b.seg_len, s1 = min(n, s0 + b.seg_len);
-  if (seg == 0 || s0 >= s1) return;  // nobody reads the first segment's increment
+  const int rlen = b.seg_len / b.rblk_per_seg;
+  const int s0 = seg * b.seg_len + blk * rlen, s1 = min(n, s0 + rlen);
+  if (seg == 0 || s0 >= s1) return;  // nobody reads the first segment's increments
   const int nch = (s1 - s0 + kC - 1) / kC;
 
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -800,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_revstate(const BwdArgs b) 
   }
   // the record: R (TMEM lane i = row i) row-major, then w; NaN if a wait gave up
   constexpr long REC = static_cast<long>(kD) * kD + kD;
-  float* rec = b.rec_rev + (static_cast<long>(unit) * b.nseg + seg) * REC;
+  float* rec = b.rec_rev + ((static_cast<long>(unit) * b.nseg + seg) * b.rblk_per_seg + blk) * REC;
   const int q4 = warp & 3, gw = warp >> 2;
   const int t = 32 * q4 + lane;
   float rv[32];
@@ -1026,7 +1031,7 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (b.nseg > 1) {
-    bwd_tc_revstate<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b);
+    bwd_tc_revstate<<<static_cast<unsigned>(grid * b.rblk_per_seg), kThreads, Lay::BYTES, stream>>>(b);
     note_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

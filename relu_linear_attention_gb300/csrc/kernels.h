@@ -69,6 +69,9 @@ struct BwdArgs {
   float* dgp_k;
   int nseg;
   int seg_len;
+  // tensor-core path: the suffix-state increments (rec_rev) are per block of seg_len / rblk_per_seg
+  // tokens, rblk_per_seg blocks per segment, nseg * rblk_per_seg records per (document, head)
+  int rblk_per_seg;
   // tensor-core path: q', k' of every (token, head) in bf16 (written by pass A, read by pass B),
   // and the prefix-state increments in the prefill state kernel's record format (rec_fwd), in
   // blocks of seg_len / blk_per_seg tokens, nblk_max per (document, head)
@@ -85,8 +88,9 @@ struct BwdArgs {
 struct BwdPlan {
   int nseg;
   int seg_len;
-  int blk_per_seg;  // tensor-core path
-  int nblk_max;     // tensor-core path
+  int blk_per_seg;   // tensor-core path
+  int rblk_per_seg;  // tensor-core path: suffix-state blocks per segment
+  int nblk_max;      // tensor-core path
   int chunks_max;   // tensor-core path: 128-token chunks of the longest document
   size_t off_rev, off_den, off_scl, off_sst, off_nst, off_dgq, off_dgk, off_qf, off_kf, off_dqf,
       off_dkf;
