@@ -71,7 +71,7 @@ struct Lay {
 
 // TMEM columns.
 constexpr uint32_t kTP = 0, kTG = 128, kTU = 256, kTS = 384;  // pass A: P, Cv, U, S
-constexpr uint32_t kTDV = 0, kTDK = 128, kTR = 256;           // pass B: dv (over P), dk' (over Gv), R
+constexpr uint32_t kTDV = 384, kTDK = 0, kTR = 256;           // pass B: dv, dk' (over P), R
 
 // Features of the chunk's 128 rows of x (q or k) into a bf16 tile: warp w takes rows w, w + 16, ...
 // (FeatureLayout: lane r owns elements 4r .. 4r+3); the loads of all its rows are issued before
@@ -510,12 +510,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(b.dv);
   __nv_bfloat16* dkf_out = static_cast<__nv_bfloat16*>(b.dkf);
-  const CUtensorMap* const maps[4] = {&tmqf, &tmkf, &tmv, &tmg};
-  const uint32_t ld_tiles[4] = {base + Lay::QF, base + Lay::KF, base + Lay::VS, base + Lay::GS};
-  int tma_issued = 0;  // chunks whose tiles have been requested (thread 0)
+  // the tiles arrive in two groups, each as soon as the previous chunk's MMAs are done with them:
+  // k', v, gnum after the dv group (bar_ld), q' after the last group (bar4)
+  const CUtensorMap* const maps3[3] = {&tmkf, &tmv, &tmg};
+  const uint32_t ld_tiles3[3] = {base + Lay::KF, base + Lay::VS, base + Lay::GS};
+  const CUtensorMap* const maps1[1] = {&tmqf};
+  const uint32_t ld_tiles1[1] = {base + Lay::QF};
+  const uint32_t bar_ldq = bar4;
+  int tma_issued = 0, tmaq_issued = 0;  // chunks whose tiles have been requested (thread 0)
   if (tid == 0 && nch > 0 && !*s_abort) {
-    tma_chunk<4>(maps, ld_tiles, h, static_cast<int>(row0 + s0 + (nch - 1) * kC), bar_ld);
-    tma_issued = 1;
+    tma_chunk<3>(maps3, ld_tiles3, h, static_cast<int>(row0 + s0 + (nch - 1) * kC), bar_ld);
+    tma_chunk<1>(maps1, ld_tiles1, h, static_cast<int>(row0 + s0 + (nch - 1) * kC), bar_ldq);
+    tma_issued = tmaq_issued = 1;
   }
   bool bad = *s_abort != 0;
   int it = 0;  // chunks done (the mbarrier phases)
@@ -532,7 +538,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       sst_s[tid] = vr ? b.sst[o] : 0.f;
       nst_s[tid] = vr ? b.nst[o] : 0.f;
     }
-    if (!tc::mbar_wait(bar_ld, it & 1, kWait)) atomicExch(s_abort, 1);
+    if (!tc::mbar_wait(bar_ld, it & 1, kWait) || !tc::mbar_wait(bar_ldq, it & 1, kWait))
+      atomicExch(s_abort, 1);
     __syncthreads();  // den_s
     for (int idx = tid; idx < kC * 16; idx += kThreads) {
       const int r = idx >> 4, m = idx & 15;
@@ -556,15 +563,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
-    // ---- phase 2: P = Q'K'^T, Gv = Gnum V^T
+    // ---- phase 2: P = Q'K'^T, Gv = Gnum V^T; then, while phase 3 runs on the CUDA cores, the
+    // products that need no P~ or A: dv = K' R~ and R += Q'^T Gnum (R~ in XS is not touched)
     if (tid == 0) {
       constexpr uint32_t ID = tc::idesc_bf16(128, 128, false, false);
+      constexpr uint32_t ID_MM = tc::idesc_bf16(128, 128, true, true);
+      constexpr uint32_t ID_KM = tc::idesc_bf16(128, 128, false, true);
 #pragma unroll 1
       for (int kk = 0; kk < kD / 16; ++kk) {
         tc::mma_bf16(tmem + kTP, kmaj(base + Lay::QF, kk), kmaj(base + Lay::KF, kk), ID, kk > 0);
         tc::mma_bf16(tmem + kTG, kmaj(base + Lay::GS, kk), kmaj(base + Lay::VS, kk), ID, kk > 0);
       }
       tc::mma_commit(bar1);
+#pragma unroll 1
+      for (int kk = 0; kk < kD / 16; ++kk)
+        tc::mma_bf16(tmem + kTDV, kmaj(base + Lay::KF, kk), mnmaj(base + Lay::XS, kk, kD * 128),
+                     ID_KM, kk > 0);
+#pragma unroll 1
+      for (int kk = 0; kk < kC / 16; ++kk)
+        tc::mma_bf16(tmem + kTR, mnmaj(base + Lay::QF, kk, 16384), mnmaj(base + Lay::GS, kk, 16384),
+                     ID_MM, 1u);
+    }
+    {  // meanwhile the partial increment of w = sum_t scale_t q'_t: column i, rows 32 (tid / 128) ..
+       // + 31, into the third section of RED (added to w once this chunk's dk' has used it)
+      const int i = tid & (kD - 1), r0 = 32 * (tid >> 7);
+      const int m = i >> 3, e = i & 7;
+      float dw = 0.f;
+#pragma unroll 4
+      for (int r = r0; r < r0 + 32; ++r) {
+        uint32_t word;
+        asm volatile("ld.shared.b32 %0, [%1];"
+                     : "=r"(word)
+                     : "r"(base + Lay::QF + tile_off(r, m) + 4 * (e >> 1))
+                     : "memory");
+        const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&word));
+        dw = fmaf(scl_s[r], (e & 1) ? p.y : p.x, dw);
+      }
+      red[(8 + (tid >> 7)) * kC + i] = dw;
     }
     if (!wait_mma(bar1, it & 1)) atomicExch(s_abort, 1);
     // ---- phase 3: P~ (masked) into AS; A kept in registers
@@ -600,23 +635,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         av[j] = (32 * gw + j <= t) ? num * inv2 : 0.f;
       }
     }
-    // ---- phase 4: dv = P~^T Gnum + K' R~
+    // ---- phase 4: dv += P~^T Gnum; dk' = V R~^T (over P, which phase 3 has read)
     if (tid == 0) {
       constexpr uint32_t ID_MM = tc::idesc_bf16(128, 128, true, true);
-      constexpr uint32_t ID_KM = tc::idesc_bf16(128, 128, false, true);
+      constexpr uint32_t ID_KK = tc::idesc_bf16(128, 128, false, false);
 #pragma unroll 1
       for (int kk = 0; kk < kC / 16; ++kk)
         tc::mma_bf16(tmem + kTDV, mnmaj(base + Lay::AS, kk, 16384), mnmaj(base + Lay::GS, kk, 16384),
-                     ID_MM, kk > 0);
+                     ID_MM, 1u);
 #pragma unroll 1
       for (int kk = 0; kk < kD / 16; ++kk)
-        tc::mma_bf16(tmem + kTDV, kmaj(base + Lay::KF, kk), mnmaj(base + Lay::XS, kk, kD * 128),
-                     ID_KM, 1u);
+        tc::mma_bf16(tmem + kTDK, kmaj(base + Lay::VS, kk), kmaj_d(base + Lay::XS, kk), ID_KK, kk > 0);
       tc::mma_commit(bar2);
     }
     if (!wait_mma(bar2, it & 1)) atomicExch(s_abort, 1);
-    // ---- phase 5: A over P~ (the dv MMAs have read it); dv out
+    // k', v and gnum are read by every MMA that needs them: the earlier chunk's may arrive
+    if (tid == 0 && c > 0 && !*reinterpret_cast<volatile int*>(s_abort)) {
+      tma_chunk<3>(maps3, ld_tiles3, h, static_cast<int>(row0 + t0 - kC), bar_ld);
+      ++tma_issued;
+    }
+    // ---- phase 5: A over P~ (the dv MMAs have read it)
     store_row32<false>(base + Lay::AS, t, gw, av);
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
+    // ---- phase 6: dk' += A^T Q'; dv (complete) out meanwhile
+    if (tid == 0) {
+      constexpr uint32_t ID_MM = tc::idesc_bf16(128, 128, true, true);
+#pragma unroll 1
+      for (int kk = 0; kk < kC / 16; ++kk)
+        tc::mma_bf16(tmem + kTDK, mnmaj(base + Lay::AS, kk, 16384), mnmaj(base + Lay::QF, kk, 16384),
+                     ID_MM, 1u);
+      tc::mma_commit(bar3);  // dk' done, and with it every MMA of the chunk (R included)
+    }
     {
       float o[32];
       tmem_ld32(tmem + tl + kTDV + 32 * gw, o);
@@ -627,67 +680,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(o + 8 * m);
       }
     }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
-    // ---- phase 6: dk' = A^T Q' + V R~^T, then R += Q'^T Gnum
-    if (tid == 0) {
-      constexpr uint32_t ID_MM = tc::idesc_bf16(128, 128, true, true);
-      constexpr uint32_t ID_KK = tc::idesc_bf16(128, 128, false, false);
-#pragma unroll 1
-      for (int kk = 0; kk < kC / 16; ++kk)
-        tc::mma_bf16(tmem + kTDK, mnmaj(base + Lay::AS, kk, 16384), mnmaj(base + Lay::QF, kk, 16384),
-                     ID_MM, kk > 0);
-#pragma unroll 1
-      for (int kk = 0; kk < kD / 16; ++kk)
-        tc::mma_bf16(tmem + kTDK, kmaj(base + Lay::VS, kk), kmaj_d(base + Lay::XS, kk), ID_KK, 1u);
-      tc::mma_commit(bar3);  // dk' done: its read-out can start while R is updated
-#pragma unroll 1
-      for (int kk = 0; kk < kC / 16; ++kk)
-        tc::mma_bf16(tmem + kTR, mnmaj(base + Lay::QF, kk, 16384), mnmaj(base + Lay::GS, kk, 16384),
-                     ID_MM, 1u);
-      tc::mma_commit(bar4);
-    }
     if (!wait_mma(bar3, it & 1)) atomicExch(s_abort, 1);
+    // every MMA of the chunk has completed and no CUDA-core read of q' is left: the earlier
+    // chunk's q' may arrive while this one finishes
+    if (tid == 0 && c > 0 && !*reinterpret_cast<volatile int*>(s_abort)) {
+      tma_chunk<1>(maps1, ld_tiles1, h, static_cast<int>(row0 + t0 - kC), bar_ldq);
+      ++tmaq_issued;
+    }
     // ---- phase 7: dk' + w into the staging, w += sum_t scale_t q'_t, R -> R~
     {
       float o[32];
       tmem_ld32(tmem + tl + kTDK + 32 * gw, o);
 #pragma unroll
       for (int j = 0; j < 32; ++j) o[j] += ws[32 * gw + j];
-      {  // partial increment of w: column i of q', rows 32 (tid / 128) .. + 31
-        const int i = tid & (kD - 1), r0 = 32 * (tid >> 7);
-        const int m = i >> 3, e = i & 7;
-        float dw = 0.f;
-#pragma unroll 4
-        for (int r = r0; r < r0 + 32; ++r) {
-          uint32_t word;
-          asm volatile("ld.shared.b32 %0, [%1];"
-                       : "=r"(word)
-                       : "r"(base + Lay::QF + tile_off(r, m) + 4 * (e >> 1))
-                       : "memory");
-          const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&word));
-          dw = fmaf(scl_s[r], (e & 1) ? p.y : p.x, dw);
-        }
-        red[(tid >> 7) * kC + i] = dw;
-      }
       if (t0 + t < n) {  // dk' (bf16) to the workspace
         __nv_bfloat16* dst = dkf_out + ((row0 + t0 + t) * a.H + h) * kD + 32 * gw;
 #pragma unroll
         for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(o + 8 * m);
       }
-      if (!wait_mma(bar4, it & 1)) atomicExch(s_abort, 1);  // R updated: every MMA read its tiles
       tc::fence_async_smem();
       tc::fence_before_sync();
-      __syncthreads();  // w and q' are read
-      if (tid == 0 && c > 0 && !*reinterpret_cast<volatile int*>(s_abort)) {
-        // the earlier chunk's tiles arrive while this one finishes
-        tma_chunk<4>(maps, ld_tiles, h, static_cast<int>(row0 + t0 - kC), bar_ld);
-        ++tma_issued;
-      }
-      if (tid < kD) ws[tid] += red[tid] + red[kC + tid] + red[2 * kC + tid] + red[3 * kC + tid];
+      __syncthreads();  // w is read
+      if (tid < kD)
+        ws[tid] += red[8 * kC + tid] + red[9 * kC + tid] + red[10 * kC + tid] + red[11 * kC + tid];
       float rv[32];
       tmem_ld32(tmem + tl + kTR + 32 * gw, rv);
       store_row32<true>(base + Lay::XS, t, gw, rv);
@@ -699,6 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   bad = bad || *reinterpret_cast<volatile int*>(s_abort) != 0;
   if (tid == 0 && tma_issued > 0) tc::mbar_wait(bar_ld, (tma_issued - 1) & 1, kWait);
+  if (tid == 0 && tmaq_issued > 0) tc::mbar_wait(bar_ldq, (tmaq_issued - 1) & 1, kWait);
   __syncthreads();
   if (bad) {  // a wait gave up: NaN dk' and dv over the segment
     for (long r = s0 + tid / 16; r < s1; r += kThreads / 16) {
