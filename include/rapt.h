@@ -122,6 +122,38 @@ rapt_status rapt_prefill_fwd(const void* q, const void* k, const void* v, rapt_d
                              void* workspace, size_t workspace_bytes, rapt_stream_t stream);
 
 /*
+ * rapt_prefill_fwd with q, k, v and out in HOST memory (page-locked for full speed; any memory
+ * the CUDA runtime can copy from works). The batch rows are pipelined: row b is copied in on
+ * `copy_in` while row b - 1 is computed on `stream` and row b - 2 is copied out on `copy_out`, so
+ * the host -> device copies, the device -> host copies and the kernels overlap. Each row is
+ * computed by rapt_prefill_fwd with B = 1, so the result is that of rapt_prefill_fwd on each
+ * batch row alone (the same values a B-row call gives up to the segment split of the plan).
+ *   q, k, v   host [B, L, H, d] of `dtype`; out host [B, L, H, d] of `dtype`.
+ *   gamma_q, gamma_k, S0, z0, S_final, z_final, dev_status: DEVICE pointers, as for
+ *             rapt_prefill_fwd (S0 / z0 / S_final / z_final are [B, H, d, d] / [B, H, d]).
+ *   workspace / workspace_bytes: device scratch of at least rapt_prefill_host_workspace_size()
+ *             bytes, 16-byte aligned: two staging slots of a row's q, k, v and out, then the
+ *             B = 1 prefill workspace. Contents on entry do not matter.
+ *   stream, copy_in, copy_out: the compute stream and the two copy streams (they may be the
+ *             same stream; then nothing overlaps). All three first wait for the work already
+ *             queued on `stream`, and `stream` waits for the last copy out before the call
+ *             returns, so synchronising `stream` makes out and the states complete. The call
+ *             creates and releases its own CUDA events and allocates no memory.
+ * Errors: as rapt_prefill_fwd (checked before anything is queued), RAPT_ERR_WORKSPACE, and
+ * RAPT_ERR_CUDA if queuing a copy, an event or a kernel fails (work queued before the failure
+ * stays queued).
+ */
+size_t rapt_prefill_host_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d,
+                                        rapt_dtype dtype);
+rapt_status rapt_prefill_fwd_host(const void* q, const void* k, const void* v, rapt_dtype dtype,
+                                  int32_t B, int32_t L, int32_t H, int32_t d,
+                                  const float* gamma_q, const float* gamma_k, rapt_params params,
+                                  int32_t pos_offset, const float* S0, const float* z0, void* out,
+                                  float* S_final, float* z_final, uint32_t* dev_status,
+                                  void* workspace, size_t workspace_bytes, rapt_stream_t stream,
+                                  rapt_stream_t copy_in, rapt_stream_t copy_out);
+
+/*
  * Packed variable-length causal RLA-2 (08-rapt-algorithm.md §2.2, §4.1: the state restarts at
  * every document; RoPE positions restart at 0 in every document).
  *   q, k, v   [T, H, d] of `dtype`.

@@ -44,6 +44,13 @@ SIGNATURES = {
                                    c_void_p, c_void_p, rapt_params,
                                    c_int32, c_void_p, c_void_p, c_void_p,
                                    c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "rapt_prefill_host_workspace_size": (c_size_t, [c_int32] * 4 + [c_int32]),
+    "rapt_prefill_fwd_host": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32,
+                                        c_int32, c_int32, c_int32, c_int32,
+                                        c_void_p, c_void_p, rapt_params,
+                                        c_int32, c_void_p, c_void_p, c_void_p,
+                                        c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                        c_void_p, c_void_p, c_void_p]),
     "rapt_varlen_workspace_size": (c_size_t, [c_int32] * 5 + [c_int32]),
     "rapt_varlen_fwd": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32,
                                   c_int32, c_int32, c_int32, c_void_p,

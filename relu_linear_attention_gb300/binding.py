@@ -100,6 +100,54 @@ def rapt_prefill_fwd(q, k, v, gamma_q, gamma_k, *, eps_norm=1e-6, rope_base=1e4,
     return out, S_final, z_final
 
 
+def rapt_prefill_fwd_host(q, k, v, gamma_q, gamma_k, *, out=None, eps_norm=1e-6, rope_base=1e4,
+                          eps_den=1e-4, pos_offset=0, S0=None, z0=None, final_state=False,
+                          S_final=None, z_final=None, dev_status=None, workspace=None, device=None,
+                          stream=None, copy_in=None, copy_out=None):
+    """rapt_prefill_fwd with q, k, v and out in host memory (CPU tensors, page-locked for full
+    speed): the batch rows are copied in, computed and copied out in a pipeline over three CUDA
+    streams (copy_in and copy_out default to the compute stream, which then overlaps nothing).
+    gammas and states are CUDA tensors. Returns (out, S_final, z_final); out is complete once
+    `stream` (default: the current stream) is synchronised."""
+    _need(q.dim() == 4, "q must be [B, L, H, d]")
+    B, L, H, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(not t.is_cuda, "%s must be a host tensor" % name)
+        _need(t.is_contiguous() and t.dtype == q.dtype and tuple(t.shape) == tuple(q.shape),
+              "%s must be contiguous with q's dtype and shape" % name)
+    _need(q.dtype in _DT, "dtype must be float32 or bfloat16")
+    dev = gamma_q.device if device is None else torch.device(device)
+    stride = _gammas(gamma_q, gamma_k, H, d)
+    _state("S0", S0, (B, H, d, d))
+    _state("z0", z0, (B, H, d))
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    _need(not out.is_cuda and out.is_contiguous() and out.dtype == q.dtype and
+          tuple(out.shape) == tuple(q.shape), "out must be a contiguous host tensor like q")
+    if final_state and S_final is None:
+        S_final = torch.empty((B, H, d, d), device=dev, dtype=torch.float32)
+    if final_state and z_final is None:
+        z_final = torch.empty((B, H, d), device=dev, dtype=torch.float32)
+    _state("S_final", S_final, (B, H, d, d))
+    _state("z_final", z_final, (B, H, d))
+    if dev_status is not None:
+        _cuda_contig("dev_status", dev_status, torch.int32)
+    lib = _lib.load()
+    need = lib.rapt_prefill_host_workspace_size(B, L, H, d, _DT[q.dtype])
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=dev, dtype=torch.uint8)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.rapt_prefill_fwd_host(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], B, L, H, d,
+                                   _ptr(gamma_q), _ptr(gamma_k),
+                                   make_params(eps_norm, rope_base, eps_den, stride),
+                                   int(pos_offset), _ptr(S0), _ptr(z0), _ptr(out), _ptr(S_final),
+                                   _ptr(z_final), _ptr(dev_status), _ptr(workspace), ws_bytes,
+                                   _stream(stream), _stream(copy_in if copy_in is not None else stream),
+                                   _stream(copy_out if copy_out is not None else stream))
+    _lib.check("rapt_prefill_fwd_host", st)
+    return out, S_final, z_final
+
+
 def rapt_varlen_fwd(q, k, v, cu_seqlens, gamma_q, gamma_k, *, max_seqlen, eps_norm=1e-6,
                     rope_base=1e4, eps_den=1e-4, S0=None, z0=None, out=None, final_state=False,
                     S_final=None, z_final=None, dev_status=None, workspace=None, stream=None):

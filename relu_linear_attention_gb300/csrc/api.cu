@@ -81,7 +81,7 @@ const char* rapt_status_string(rapt_status s) {
   }
 }
 
-int32_t rapt_abi_version(void) { return 10200; }
+int32_t rapt_abi_version(void) { return 10300; }
 
 uint64_t rapt_launch_counter(void) { return rapt::launch_count(); }
 
@@ -130,6 +130,111 @@ rapt_status rapt_prefill_fwd(const void* q, const void* k, const void* v, rapt_d
     return from_cuda(rapt::launch_prefill_tc(d, a, rapt::tc_plan(B, H, L, static_cast<long>(B) * L, d),
                                              static_cast<float*>(workspace), s));
   return from_cuda(rapt::launch_prefill_simt(to_dt(dtype), d, a, s));
+}
+
+// ---- host buffers: batch rows pipelined over two copy streams and the compute stream
+
+namespace {
+size_t up16(size_t x) { return (x + 15) / 16 * 16; }
+// Bytes of one batch row of a [B, L, H, d] tensor.
+size_t host_row_bytes(int32_t L, int32_t H, int32_t d, rapt_dtype dtype) {
+  return static_cast<size_t>(L) * H * d * (dtype == RAPT_F32 ? 4 : 2);
+}
+// The events of one call (created and released by the call).
+struct HostEvents {
+  cudaEvent_t start = nullptr, in[2] = {nullptr, nullptr}, comp[2] = {nullptr, nullptr},
+              out[2] = {nullptr, nullptr};
+  cudaError_t create() {
+    cudaError_t e = cudaSuccess;
+    for (cudaEvent_t* ev : {&start, &in[0], &in[1], &comp[0], &comp[1], &out[0], &out[1]})
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    return e;
+  }
+  ~HostEvents() {  // a pending event is released once it completes
+    for (cudaEvent_t ev : {start, in[0], in[1], comp[0], comp[1], out[0], out[1]})
+      if (ev != nullptr) cudaEventDestroy(ev);
+  }
+};
+}  // namespace
+
+size_t rapt_prefill_host_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d,
+                                        rapt_dtype dtype) {
+  if (!known_dtype(dtype) || !supported_d(d) || B < 1 || H < 1 || L < 0) return 0;
+  return 8 * up16(host_row_bytes(L, H, d, dtype)) + up16(rapt_prefill_workspace_size(1, L, H, d, dtype));
+}
+
+rapt_status rapt_prefill_fwd_host(const void* q, const void* k, const void* v, rapt_dtype dtype,
+                                  int32_t B, int32_t L, int32_t H, int32_t d,
+                                  const float* gamma_q, const float* gamma_k, rapt_params params,
+                                  int32_t pos_offset, const float* S0, const float* z0, void* out,
+                                  float* S_final, float* z_final, uint32_t* dev_status,
+                                  void* workspace, size_t workspace_bytes, rapt_stream_t stream,
+                                  rapt_stream_t copy_in, rapt_stream_t copy_out) {
+  if (!known_dtype(dtype) || !supported_d(d)) return RAPT_ERR_UNSUPPORTED;
+  if (B < 1 || H < 1 || L < 0 || pos_offset < 0) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(B) * L * H * d)) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(pos_offset) + L)) return RAPT_ERR_INVALID_ARG;
+  if (L > 0 && (q == nullptr || k == nullptr || v == nullptr || out == nullptr))
+    return RAPT_ERR_INVALID_ARG;
+  if (out != nullptr && (out == q || out == k || out == v)) return RAPT_ERR_INVALID_ARG;
+  if (!opt_aligned16(S0) || !opt_aligned16(z0) || !opt_aligned16(S_final) || !opt_aligned16(z_final))
+    return RAPT_ERR_INVALID_ARG;
+  if ((S_final != nullptr && S_final == S0) || (z_final != nullptr && z_final == z0))
+    return RAPT_ERR_INVALID_ARG;
+  if (dev_status != nullptr && !aligned4(dev_status)) return RAPT_ERR_INVALID_ARG;
+  rapt_status st = check_features(gamma_q, gamma_k, params, d);
+  if (st != RAPT_OK) return st;
+  const size_t need = rapt_prefill_host_workspace_size(B, L, H, d, dtype);
+  if (workspace_bytes < need || workspace == nullptr || !aligned16(workspace)) return RAPT_ERR_WORKSPACE;
+  if (L == 0)  // nothing to copy: the states only
+    return rapt_prefill_fwd(nullptr, nullptr, nullptr, dtype, B, 0, H, d, gamma_q, gamma_k, params,
+                            pos_offset, S0, z0, nullptr, S_final, z_final, dev_status, workspace,
+                            workspace_bytes, stream);
+
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const cudaStream_t si = reinterpret_cast<cudaStream_t>(copy_in);
+  const cudaStream_t so = reinterpret_cast<cudaStream_t>(copy_out);
+  const size_t row = host_row_bytes(L, H, d, dtype), slot_stride = 4 * up16(row);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* ws_pre = ws + 2 * slot_stride;
+  const size_t pre_bytes = workspace_bytes - 2 * slot_stride;
+  const long sdd = static_cast<long>(H) * d * d, sd = static_cast<long>(H) * d;
+  HostEvents ev;
+  cudaError_t e = ev.create();
+  if (e == cudaSuccess) e = cudaEventRecord(ev.start, s);  // after the work already on `stream`
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(si, ev.start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(so, ev.start, 0);
+  for (int32_t b = 0; b < B && e == cudaSuccess; ++b) {
+    const int slot = b & 1;
+    uint8_t* sl = ws + slot * slot_stride;
+    uint8_t *qd = sl, *kd = sl + up16(row), *vd = sl + 2 * up16(row), *od = sl + 3 * up16(row);
+    const size_t off = static_cast<size_t>(b) * row;
+    // copy in (once the row two back has been computed: it read this slot's inputs)
+    if (b >= 2) e = cudaStreamWaitEvent(si, ev.comp[slot], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(qd, static_cast<const uint8_t*>(q) + off, row, cudaMemcpyDefault, si);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(kd, static_cast<const uint8_t*>(k) + off, row, cudaMemcpyDefault, si);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(vd, static_cast<const uint8_t*>(v) + off, row, cudaMemcpyDefault, si);
+    if (e == cudaSuccess) e = cudaEventRecord(ev.in[slot], si);
+    // compute (once the row is in and the row two back has been copied out of this slot)
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev.in[slot], 0);
+    if (e == cudaSuccess && b >= 2) e = cudaStreamWaitEvent(s, ev.out[slot], 0);
+    if (e != cudaSuccess) break;
+    st = rapt_prefill_fwd(qd, kd, vd, dtype, 1, L, H, d, gamma_q, gamma_k, params, pos_offset,
+                          S0 != nullptr ? S0 + b * sdd : nullptr, z0 != nullptr ? z0 + b * sd : nullptr,
+                          od, S_final != nullptr ? S_final + b * sdd : nullptr,
+                          z_final != nullptr ? z_final + b * sd : nullptr, dev_status, ws_pre,
+                          pre_bytes, stream);
+    if (st != RAPT_OK) return st;
+    e = cudaEventRecord(ev.comp[slot], s);
+    // copy out
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(so, ev.comp[slot], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(static_cast<uint8_t*>(out) + off, od, row, cudaMemcpyDefault, so);
+    if (e == cudaSuccess) e = cudaEventRecord(ev.out[slot], so);
+  }
+  // `stream` covers everything: it waits for the last copies out
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev.out[(B - 1) & 1], 0);
+  if (e == cudaSuccess && B >= 2) e = cudaStreamWaitEvent(s, ev.out[B & 1], 0);
+  return from_cuda(e);
 }
 
 size_t rapt_varlen_workspace_size(int32_t T, int32_t N, int32_t H, int32_t d, int32_t max_seqlen,
