@@ -522,12 +522,12 @@ def run_gpu(args, rank, world, local):
                              "algorithmic_bytes_per_call": g_bytes,
                              "tensor_tflops_algorithmic": g_flops / (g_mean * 1e-3) / 1e12,
                              "traffic": read_traffic("backward", "bwd_tc_featmap",
-                                                     "segment_state_kernel", "bwd_tc_forward",
-                                                     "bwd_tc_revstate", "bwd_tc_reverse",
+                                                     "bwd_tc_blockstate<true>", "bwd_tc_forward",
+                                                     "bwd_tc_blockstate<false>", "bwd_tc_reverse",
                                                      "bwd_tc_features", "bwd_gain_kernel"),
-                             "kernels": "bwd_tc_featmap + segment_state_kernel + bwd_tc_forward + "
-                                        "bwd_tc_revstate + bwd_tc_reverse + bwd_tc_features + "
-                                        "bwd_gain_kernel (one call; tensor cores)"}}
+                             "kernels": "bwd_tc_featmap + bwd_tc_blockstate<true> + bwd_tc_forward + "
+                                        "bwd_tc_blockstate<false> + bwd_tc_reverse + "
+                                        "bwd_tc_features + bwd_gain_kernel (one call; tensor cores)"}}
     del tg, gws, grads
 
     # ---------------- one RAPT layer around the headline attention (d_model = H d = 2048), and its

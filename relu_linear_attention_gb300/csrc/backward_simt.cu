@@ -631,10 +631,10 @@ BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d, bool
     p.seg_len = chunks_max * ck;
   }
   p.blk_per_seg = 1;
-  if (tc) {  // state-kernel blocks: the largest of 8, 4, 2, 1 that divides the segment's chunks
+  if (tc && p.nseg > 1) {  // prefix-state blocks: the earlier segments' blocks should fill one wave
     const int sc = p.seg_len / ck;
     for (int f = 8; f > 1; f /= 2)
-      if (sc % f == 0) {
+      if (sc % f == 0 && units * (p.nseg - 1) * f <= kSMs) {
         p.blk_per_seg = f;
         break;
       }

@@ -732,30 +732,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------------------------------------
-// Between the passes: the suffix-state increment of every block of the segments after a document's
-// first (rblk_per_seg blocks per segment), R_blk = sum_{t in blk} q'_t gnum_t^T and w_blk = sum
-// scale_t q'_t (q' from the feature kernel, gnum = g / den), written as fp32 records [R row-major |
-// w] for pass B.
-__global__ void __launch_bounds__(kThreads, 1) bwd_tc_revstate(const BwdArgs b) {
+// The state increments of blocks of a document, both of the form X_blk = sum_{t in blk} a_t b_t^T
+// and x_blk = sum_t s_t a_t, accumulated chunk by chunk on the tensor core:
+//   kFwd (before pass A): the prefix-state increments of the blocks before a document's last
+//     segment (blk_per_seg per segment), S = sum k' v^T and z = sum k' (k' from the feature
+//     kernel), in the prefill state kernel's record format (float4 j * D + i holds S[i][4j..4j+3],
+//     then z);
+//   otherwise (between the passes): the suffix-state increments of the blocks of the segments
+//     after a document's first (rblk_per_seg per segment), R = sum q' gnum^T and w = sum scale q'
+//     (gnum = g / den), as records [R row-major | w].
+template <bool kFwd>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_tc_blockstate(const BwdArgs b, const __grid_constant__ CUtensorMap tma_a,
+                      const __grid_constant__ CUtensorMap tma_b) {
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int blk = blockIdx.x % b.rblk_per_seg;
-  const int seg = (blockIdx.x / b.rblk_per_seg) % b.nseg, unit = blockIdx.x / (b.rblk_per_seg * b.nseg);
+  const int per_seg = kFwd ? b.blk_per_seg : b.rblk_per_seg;
+  const int nblk = kFwd ? b.nblk_max : b.nseg * b.rblk_per_seg;  // records per (document, head)
+  const int kb = blockIdx.x % nblk, unit = blockIdx.x / nblk;
+  const int seg = kb / per_seg;
   const int h = unit % a.H, doc = unit / a.H;
   long row0;
   int n;
   doc_bounds(a, doc, row0, n);
-  const int rlen = b.seg_len / b.rblk_per_seg;
-  const int s0 = seg * b.seg_len + blk * rlen, s1 = min(n, s0 + rlen);
-  if (seg == 0 || s0 >= s1) return;  // nobody reads the first segment's increments
+  const int blen = b.seg_len / per_seg;
+  const int s0 = kb * blen, s1 = min(n, s0 + blen);
+  if (s0 >= s1) return;
+  if (kFwd) {  // only the blocks before the document's last segment are read
+    if (seg >= (n + b.seg_len - 1) / b.seg_len - 1) return;
+  } else {
+    if (seg == 0) return;  // nobody reads the first segment's increments
+  }
   const int nch = (s1 - s0 + kC - 1) / kC;
 
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t base = tc::smem_u32(smem);
   float* ws = reinterpret_cast<float*>(smem + Lay::ZS);
-  float* scl_s = reinterpret_cast<float*>(smem + Lay::ROW);
+  float* scl_s = reinterpret_cast<float*>(smem + Lay::ROW);  // [2][128]: scale, 1 / den
   float* red = reinterpret_cast<float*>(smem + Lay::RED);
-  const uint32_t bar1 = base + Lay::BAR;
+  const uint32_t bar1 = base + Lay::BAR, bar_ld0 = bar1 + 8;  // MMA done; tiles of set 0 / 1
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + Lay::MISC);
   int* s_abort = reinterpret_cast<int*>(smem + Lay::MISC + 4);
   const bool misaligned = (base & 1023u) != 0;
@@ -765,6 +780,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_revstate(const BwdArgs b) 
   }
   if (tid == 0) {
     tc::mbar_init(bar1, 1);
+    tc::mbar_init(bar_ld0, 1);
+    tc::mbar_init(bar_ld0 + 8, 1);
     tc::mbar_fence_init();
     *s_abort = misaligned ? 1 : 0;
   }
@@ -773,18 +790,60 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_revstate(const BwdArgs b) 
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *s_tmem;
-  const __nv_bfloat16* qf_in = static_cast<const __nv_bfloat16*>(b.qf);
-  const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(b.dout);
+  // a_t and b_t of even chunks in tiles QF / GS, of odd chunks in KF / VS, by TMA two chunks ahead
+  const CUtensorMap* const maps[2] = {&tma_a, &tma_b};
+  auto tiles = [&](int set, uint32_t (&t)[2]) {
+    t[0] = base + (set ? Lay::KF : Lay::QF);
+    t[1] = base + (set ? Lay::VS : Lay::GS);
+  };
+  int issued0 = 0, issued1 = 0;  // chunks requested per set (thread 0)
+  if (tid == 0 && !*s_abort) {
+    for (int c = 0; c < 2 && c < nch; ++c) {
+      uint32_t t[2];
+      tiles(c, t);
+      tma_chunk<2>(maps, t, h, static_cast<int>(row0 + s0 + c * kC), bar_ld0 + 8 * c);
+    }
+    issued0 = 1;
+    issued1 = nch > 1 ? 1 : 0;
+  }
+  // the row scalars (scale and 1 / den) of a chunk, loaded one chunk ahead into registers
+  auto row_scalars = [&](int t0, float& sc, float& id) {
+    const bool vr = tid < kC && t0 + tid < n;
+    const long o = (row0 + t0 + tid) * a.H + h;
+    sc = vr ? (kFwd ? 1.f : __ldg(b.scl + o)) : 0.f;
+    id = (vr && !kFwd) ? __ldg(b.den + o) : 1.f;
+  };
+  float sc_next, den_next;
+  row_scalars(s0, sc_next, den_next);
   bool bad = *s_abort != 0;
   for (int c = 0; c < nch && !bad; ++c) {
-    const int t0 = s0 + c * kC;
-    {
-      const __nv_bfloat16* const src[2] = {qf_in, g};
-      const uint32_t tiles[2] = {base + Lay::QF, base + Lay::GS};
-      const bool dv[2] = {false, true};
-      raw_tiles_tc<2>(src, tiles, dv, row0, n, t0, a.H, h, b.den);
+    const int t0 = s0 + c * kC, set = c & 1;
+    uint32_t t[2];
+    tiles(set, t);
+    if (tid < kC) {
+      scl_s[tid] = sc_next;
+      scl_s[kC + tid] = 1.0f / den_next;
     }
-    if (tid < kC) scl_s[tid] = t0 + tid < n ? b.scl[(row0 + t0 + tid) * a.H + h] : 0.f;
+    if (c + 1 < nch) row_scalars(t0 + kC, sc_next, den_next);
+    if (!tc::mbar_wait(bar_ld0 + 8 * set, (c >> 1) & 1, kWait)) atomicExch(s_abort, 1);
+    __syncthreads();  // scl_s
+    // rows past the document cleared; reverse: b = g / den in place
+    if (!kFwd || t0 + kC > n) {
+      for (int idx = tid; idx < kC * 16; idx += kThreads) {
+        const int r = idx >> 4, m = idx & 15;
+        const uint32_t ga = t[1] + tile_off(r, m);
+        if (t0 + r >= n) {
+          sts16(ga, make_uint4(0, 0, 0, 0));
+          sts16(t[0] + tile_off(r, m), make_uint4(0, 0, 0, 0));
+        } else if (!kFwd) {
+          float f[8];
+          unpack8(lds16(ga), f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] *= scl_s[kC + r];
+          sts16(ga, feat::pack8(f));
+        }
+      }
+    }
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
@@ -793,11 +852,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_revstate(const BwdArgs b) 
       constexpr uint32_t ID_MM = tc::idesc_bf16(128, 128, true, true);
 #pragma unroll 1
       for (int kk = 0; kk < kC / 16; ++kk)
-        tc::mma_bf16(tmem, mnmaj(base + Lay::QF, kk, 16384), mnmaj(base + Lay::GS, kk, 16384), ID_MM,
+        tc::mma_bf16(tmem, mnmaj(t[0], kk, 16384), mnmaj(t[1], kk, 16384), ID_MM,
                      (c > 0 || kk > 0) ? 1u : 0u);
       tc::mma_commit(bar1);
     }
-    {  // partial increment of w: column i of q', rows 32 (tid / 128) .. + 31
+    {  // partial increment of x: column i of a, rows 32 (tid / 128) .. + 31
       const int i = tid & (kD - 1), r0 = 32 * (tid >> 7);
       const int m = i >> 3, e = i & 7;
       float dw = 0.f;
@@ -806,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_revstate(const BwdArgs b) 
         uint32_t word;
         asm volatile("ld.shared.b32 %0, [%1];"
                      : "=r"(word)
-                     : "r"(base + Lay::QF + tile_off(r, m) + 4 * (e >> 1))
+                     : "r"(t[0] + tile_off(r, m) + 4 * (e >> 1))
                      : "memory");
         const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&word));
         dw = fmaf(scl_s[r], (e & 1) ? p.y : p.x, dw);
@@ -814,16 +873,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_revstate(const BwdArgs b) 
       red[(tid >> 7) * kC + i] = dw;
     }
     if (!wait_mma(bar1, c & 1)) atomicExch(s_abort, 1);
-    __syncthreads();
+    __syncthreads();  // the MMA and every thread are done with this set's tiles
+    if (tid == 0 && c + 2 < nch && !*reinterpret_cast<volatile int*>(s_abort)) {
+      tma_chunk<2>(maps, t, h, static_cast<int>(row0 + t0 + 2 * kC), bar_ld0 + 8 * set);
+      if (set) ++issued1;
+      else ++issued0;
+    }
     if (tid < kD) ws[tid] += red[tid] + red[kC + tid] + red[2 * kC + tid] + red[3 * kC + tid];
     bad = *reinterpret_cast<volatile int*>(s_abort) != 0;
     __syncthreads();
   }
-  // the record: R (TMEM lane i = row i) row-major, then w; NaN if a wait gave up
+  if (tid == 0) {  // copies still in flight land before the CTA leaves
+    if (issued0 > 0) tc::mbar_wait(bar_ld0, (issued0 - 1) & 1, kWait);
+    if (issued1 > 0) tc::mbar_wait(bar_ld0 + 8, (issued1 - 1) & 1, kWait);
+  }
+  // the record (TMEM lane i = row i of X), then x; NaN if a wait gave up
   constexpr long REC = static_cast<long>(kD) * kD + kD;
-  float* rec = b.rec_rev + ((static_cast<long>(unit) * b.nseg + seg) * b.rblk_per_seg + blk) * REC;
+  float* rec = (kFwd ? b.rec_fwd : b.rec_rev) + (static_cast<long>(unit) * nblk + kb) * REC;
   const int q4 = warp & 3, gw = warp >> 2;
-  const int t = 32 * q4 + lane;
+  const int tr = 32 * q4 + lane;
   float rv[32];
   if (!bad) {
     tmem_ld32(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 32 * gw, rv);
@@ -832,9 +900,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_revstate(const BwdArgs b) 
     for (int e = 0; e < 32; ++e) rv[e] = __int_as_float(0x7fc00000);
   }
 #pragma unroll
-  for (int jj = 0; jj < 8; ++jj)
-    *reinterpret_cast<float4*>(rec + t * kD + 32 * gw + 4 * jj) =
-        make_float4(rv[4 * jj], rv[4 * jj + 1], rv[4 * jj + 2], rv[4 * jj + 3]);
+  for (int jj = 0; jj < 8; ++jj) {
+    const float4 x4 = make_float4(rv[4 * jj], rv[4 * jj + 1], rv[4 * jj + 2], rv[4 * jj + 3]);
+    if (kFwd) reinterpret_cast<float4*>(rec)[(8 * gw + jj) * kD + tr] = x4;
+    else *reinterpret_cast<float4*>(rec + tr * kD + 32 * gw + 4 * jj) = x4;
+  }
   if (tid < kD) rec[kD * kD + tid] = bad ? __int_as_float(0x7fc00000) : ws[tid];
   if (bad && tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, 2u);
   tc::fence_before_sync();
@@ -1010,7 +1080,8 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   if (dev < 64 && !((configured >> dev) & 1ull)) {
     for (const void* f : {reinterpret_cast<const void*>(bwd_tc_forward),
                           reinterpret_cast<const void*>(bwd_tc_reverse),
-                          reinterpret_cast<const void*>(bwd_tc_revstate)}) {
+                          reinterpret_cast<const void*>(bwd_tc_blockstate<true>),
+                          reinterpret_cast<const void*>(bwd_tc_blockstate<false>)}) {
       e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(Lay::BYTES));
       if (e != cudaSuccess) return e;
@@ -1023,31 +1094,26 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   bwd_tc_featmap<<<static_cast<unsigned>(fgrid), kMThreads, 0, stream>>>(b);  // q', k'
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (b.nseg > 1) {  // the prefix-state increments of the blocks before each document's last segment
-    TcArgs ta{};
-    ta.p = b.p;
-    ta.ws = b.rec_fwd;
-    ta.seg_len = b.seg_len;
-    ta.nseg_max = b.nseg;
-    ta.blk_per_seg = b.blk_per_seg;
-    ta.blk_len = b.seg_len / b.blk_per_seg;
-    ta.nblk_max = b.nblk_max;
-    ta.whole_doc = 0;
-    if ((e = launch_state_tc(kD, ta, stream)) != cudaSuccess) return e;
-  }
-  // TMA maps of the row-major [rows, H, D] tensors the passes stream
+  // TMA maps of the row-major [rows, H, D] tensors the kernels stream
   CUtensorMap tmv, tmg, tmqf, tmkf;
   const long rows = b.p.total_rows;
   if ((e = make_rows_map(&tmv, b.p.v, rows, b.p.H, kD)) != cudaSuccess) return e;
   if ((e = make_rows_map(&tmg, b.dout, rows, b.p.H, kD)) != cudaSuccess) return e;
   if ((e = make_rows_map(&tmqf, b.qf, rows, b.p.H, kD)) != cudaSuccess) return e;
   if ((e = make_rows_map(&tmkf, b.kf, rows, b.p.H, kD)) != cudaSuccess) return e;
+  if (b.nseg > 1) {  // the prefix-state increments of the blocks before each document's last segment
+    bwd_tc_blockstate<true><<<static_cast<unsigned>(static_cast<long>(b.p.n_docs) * b.p.H * b.nblk_max),
+                              kThreads, Lay::BYTES, stream>>>(b, tmkf, tmv);
+    note_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   bwd_tc_forward<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b, tmqf, tmkf, tmv,
                                                                                  tmg);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (b.nseg > 1) {
-    bwd_tc_revstate<<<static_cast<unsigned>(grid * b.rblk_per_seg), kThreads, Lay::BYTES, stream>>>(b);
+    bwd_tc_blockstate<false><<<static_cast<unsigned>(grid * b.rblk_per_seg), kThreads, Lay::BYTES,
+                               stream>>>(b, tmqf, tmg);
     note_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
