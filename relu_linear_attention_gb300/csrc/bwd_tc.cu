@@ -526,18 +526,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool bad = *s_abort != 0;
   int it = 0;  // chunks done (the mbarrier phases)
 
+  // the row scalars of pass A (den, scale, sst, nst) of a chunk, loaded one chunk ahead
+  auto row_scalars = [&](int tc0, float (&v)[4]) {
+    const bool vr = tid < kC && tc0 + tid < n;
+    const long o = (row0 + tc0 + tid) * a.H + h;
+    v[0] = vr ? __ldg(b.den + o) : 1.f;
+    v[1] = vr ? __ldg(b.scl + o) : 0.f;
+    v[2] = vr ? __ldg(b.sst + o) : 0.f;
+    v[3] = vr ? __ldg(b.nst + o) : 0.f;
+  };
+  float rs_next[4];
+  row_scalars(s0 + (nch - 1) * kC, rs_next);
   for (int c = nch - 1; c >= 0 && !bad; --c, ++it) {
     const int t0 = s0 + c * kC;
     // ---- phase 1: q', k' (stored by pass A), v and g by TMA; the row scalars of pass A; gnum =
     // g / den in place; rows past the document cleared
     if (tid < kC) {
-      const bool vr = t0 + tid < n;
-      const long o = (row0 + t0 + tid) * a.H + h;
-      den_s[tid] = vr ? b.den[o] : 1.f;
-      scl_s[tid] = vr ? b.scl[o] : 0.f;
-      sst_s[tid] = vr ? b.sst[o] : 0.f;
-      nst_s[tid] = vr ? b.nst[o] : 0.f;
+      den_s[tid] = rs_next[0];
+      scl_s[tid] = rs_next[1];
+      sst_s[tid] = rs_next[2];
+      nst_s[tid] = rs_next[3];
     }
+    if (c > 0) row_scalars(t0 - kC, rs_next);  // the earlier chunk's, one chunk ahead
     if (!tc::mbar_wait(bar_ld, it & 1, kWait) || !tc::mbar_wait(bar_ldq, it & 1, kWait))
       atomicExch(s_abort, 1);
     __syncthreads();  // den_s
