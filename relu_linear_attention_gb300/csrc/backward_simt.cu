@@ -538,23 +538,48 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_kernel(const BwdArgs 
 
 // ------------------------------------------------------------------------------------------------
 // Launch 4: gains. dgamma[h][c] (or dgamma[c] when shared) = the partials of every (document,
-// segment) (and head, when shared), summed in that order. blockIdx.y: 0 = q, 1 = k.
+// segment) (and head, when shared). One CTA of 8 warps per 32 outputs (lane = output): warp w
+// sums the items w, w + 8, ... of the (document, [head,] segment) list in order, then the eight
+// warp sums are added in warp order, so the result is bitwise repeatable. blockIdx.y: 0 = q, 1 = k.
 __global__ void __launch_bounds__(256) bwd_gain_kernel(const BwdArgs b, int D) {
   const PrefillArgs& a = b.p;
   const bool per_head = a.fa.gamma_stride != 0;
   const int n_out = per_head ? a.H * D : D;
-  const int e = blockIdx.x * 256 + threadIdx.x;
-  if (e >= n_out) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 32 + lane;
   const float* part = blockIdx.y == 0 ? b.dgp_q : b.dgp_k;
   float* out = blockIdx.y == 0 ? b.dgamma_q : b.dgamma_k;
-  if (out == nullptr) return;
-  const int c = e % D;
+  if (out == nullptr) return;  // uniform
+  __shared__ float ws[8][32];
   float s = 0.f;
-  for (int doc = 0; doc < a.n_docs; ++doc)
-    for (int h = per_head ? e / D : 0; h < (per_head ? e / D + 1 : a.H); ++h)
-      for (int seg = 0; seg < b.nseg; ++seg)
-        s += part[((static_cast<long>(doc) * a.H + h) * b.nseg + seg) * D + c];
-  out[e] = s;
+  if (e < n_out) {
+    const int c = e % D;
+    const int nh = per_head ? 1 : a.H;        // heads per output
+    const int h0 = per_head ? e / D : 0;
+    // item it = (doc * nh + (h - h0)) * nseg + seg; walked with counters (no divisions in the loop)
+    const int items = a.n_docs * nh * b.nseg;
+    int seg = warp % b.nseg, dh = warp / b.nseg;
+    const int dseg = 8 % b.nseg, ddh = 8 / b.nseg;
+#pragma unroll 4
+    for (int it = warp; it < items; it += 8) {  // (unrolled: the loads are issued ahead of the adds)
+      const int doc = dh / nh, h = h0 + dh % nh;
+      s += __ldg(part + ((static_cast<long>(doc) * a.H + h) * b.nseg + seg) * D + c);
+      seg += dseg;
+      dh += ddh;
+      if (seg >= b.nseg) {
+        seg -= b.nseg;
+        ++dh;
+      }
+    }
+  }
+  ws[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && e < n_out) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += ws[w][lane];
+    out[e] = t;
+  }
 }
 
 template <typename K>
@@ -676,7 +701,7 @@ BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d, bool
 cudaError_t launch_bwd_gain(const BwdArgs& b, int d, cudaStream_t stream) {
   if (b.dgamma_q == nullptr && b.dgamma_k == nullptr) return cudaSuccess;
   const int n_out = b.p.fa.gamma_stride != 0 ? b.p.H * d : d;
-  bwd_gain_kernel<<<dim3(static_cast<unsigned>((n_out + 255) / 256), 2), 256, 0, stream>>>(b, d);
+  bwd_gain_kernel<<<dim3(static_cast<unsigned>((n_out + 31) / 32), 2), 256, 0, stream>>>(b, d);
   note_launches(1);
   return cudaGetLastError();
 }
