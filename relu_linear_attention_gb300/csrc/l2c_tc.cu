@@ -7,7 +7,7 @@
 //   out_t = q'_t S_t / (sqrt(q'_t^T A_t q'_t) + eps).
 // Chunked (C = 128 tokens), with P = Q'K'^T masked to tau <= t and S~, A~ bf16 copies of the fp32
 // states before the chunk:
-//   phase 2:  P = Q'K'^T,  X = Q' A~,  then S += K'^T V,  A += K'^T K'
+//   phase 2:  P = Q'K'^T,  X = Q' A~ (committed), then S += K'^T V,  A += K'^T K' (run during phase 3)
 //   phase 3:  den_t = sqrt(sum_tau P^2 + q'_t . X_t) + eps (fp32; P from exact bf16 features),
 //             P~ = P masked, in bf16
 //   phase 4:  X = Q' S~ + P~ V
@@ -171,6 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mma_bf16(tmem + kTX, kmaj(base + LayC::QF, kk), mnmaj(base + LayC::AS, kk, kD * 128),
                      ID_KM, kk > 0);
       }
+      tc::mma_commit(bar1);  // P and X: the row sums can start while the states are updated
+      // (the state updates complete before phase 4's products, whose commit covers them)
 #pragma unroll 1
       for (int kk = 0; kk < kC / 16; ++kk) {
         tc::mma_bf16(tmem + kTS, mnmaj(base + LayC::KF, kk, 16384), mnmaj(base + LayC::VS, kk, 16384),
@@ -178,7 +180,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mma_bf16(tmem + kTA, mnmaj(base + LayC::KF, kk, 16384), mnmaj(base + LayC::KF, kk, 16384),
                      ID_MM, 1u);
       }
-      tc::mma_commit(bar1);
     }
     if (!wait_mma(bar1, c & 1)) atomicExch(s_abort, 1);
     // ---- phase 3: den^2 = sum P^2 + q' . X;  P~ (masked, bf16)
