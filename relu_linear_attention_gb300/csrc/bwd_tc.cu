@@ -981,7 +981,14 @@ __global__ void __launch_bounds__(kMThreads) bwd_tc_featmap(const BwdArgs b) {
 //   (da, db) = the feature gradient where the pre-activation is positive, else 0 (ReLU),
 //   h = R^T (da, db) (the inverse rotation), u = gamma h,
 //   dx = r u - x r^3 (u . x) / d,   dgamma += h x r.
-__global__ void __launch_bounds__(kMThreads, 3) bwd_tc_features(const BwdArgs b) {
+// The chunk's rows of x and of its feature gradient are staged in shared memory by TMA (two 32 KB
+// tiles per CTA, three CTAs per SM), so that each SM has ~200 KB of loads in flight.
+constexpr uint32_t kFeatSmem = 2 * kTile + 1024;  // two tiles (+ alignment slack)
+
+__global__ void __launch_bounds__(kMThreads, 3)
+    bwd_tc_features(const BwdArgs b, const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_dq,
+                    const __grid_constant__ CUtensorMap tm_dk) {
   constexpr int TPR = kD / 8, RPP = kMThreads / TPR, NPASS = kC / RPP;
   constexpr int WARPS = kMThreads / 32;
   const PrefillArgs& a = b.p;
@@ -995,31 +1002,46 @@ __global__ void __launch_bounds__(kMThreads, 3) bwd_tc_features(const BwdArgs b)
   const int t0 = chunk * kC;
   __shared__ __align__(16) float tabmem[4 * kD];
   __shared__ __align__(16) float scratch[WARPS * kD];
+  __shared__ __align__(8) uint64_t bar_storage;
+  extern __shared__ __align__(1024) uint8_t fsmem[];
+  const uint32_t tiles_base = (tc::smem_u32(fsmem) + 1023u) & ~1023u;  // 1024-byte aligned
+  const uint32_t bar = tc::smem_u32(&bar_storage);
   const int prow = tid / TPR, part = tid % TPR, e0 = 8 * part;
   float2 dga[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // gain gradient, Pairs layout
   float2 dgb[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  bool failed = false;
   if (t0 < n) {  // uniform; a chunk past the document's end contributes zero partials
+    if (tid == 0) {
+      tc::mbar_init(bar, 1);
+      tc::mbar_fence_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const CUtensorMap* const maps[2] = {which ? &tm_k : &tm_q, which ? &tm_dk : &tm_dq};
+      const uint32_t tl[2] = {tiles_base, tiles_base + kTile};
+      tma_chunk<2>(maps, tl, h, static_cast<int>(row0 + t0), bar);
+    }
     const feat::FeatTab tab = feat::feat_tab<kD>(reinterpret_cast<uint8_t*>(tabmem));
     feat::fill_tab<kD>(tab, a, h, RPP, tid, kMThreads);
     __syncthreads();
     const long rstride = static_cast<long>(a.H) * kD;
     const long off0 = (row0 + t0 + prow) * rstride + static_cast<long>(h) * kD + e0;
-    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(which ? a.k : a.q) + off0;
-    const __nv_bfloat16* df = static_cast<const __nv_bfloat16*>(which ? b.dkf : b.dqf) + off0;
     __nv_bfloat16* dx = static_cast<__nv_bfloat16*>(which ? b.dk : b.dq) + off0;
     float2 g0[2], g1[2];
     feat::split_load<kD>(which ? tab.gk : tab.gq, part, g0, g1);
     feat::Rot step, rot;
     feat::tab_step(tab, e0 / 2, step);
     feat::tab_rot_at(tab, a.pos_offset + t0 + prow, e0 / 2, rot);
+    failed = !tc::mbar_wait(bar, 0, kWait);
 #pragma unroll 1
-    for (int p0 = 0; p0 < NPASS; p0 += 2) {  // two passes' loads in flight at a time
+    for (int p0 = 0; p0 < NPASS && !failed; p0 += 2) {
       uint4 rx[2], rd[2];
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const bool valid = t0 + (p0 + i) * RPP + prow < n;
-        rx[i] = valid ? feat::ldg16(x + (p0 + i) * RPP * rstride) : make_uint4(0, 0, 0, 0);
-        rd[i] = valid ? feat::ldg16(df + (p0 + i) * RPP * rstride) : make_uint4(0, 0, 0, 0);
+      for (int i = 0; i < 2; ++i) {  // rows past the document (other tokens or zero fill) are masked
+        const int r = (p0 + i) * RPP + prow;
+        const bool valid = t0 + r < n;
+        rx[i] = valid ? feat::lds16(tiles_base + tile_off(r, part)) : make_uint4(0, 0, 0, 0);
+        rd[i] = valid ? feat::lds16(tiles_base + kTile + tile_off(r, part)) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
@@ -1074,8 +1096,10 @@ __global__ void __launch_bounds__(kMThreads, 3) bwd_tc_features(const BwdArgs b)
   if (tid < kD) {
     float sum = 0.f;
     for (int w = 0; w < WARPS; ++w) sum += scratch[w * kD + tid];
-    (which ? b.dgp_k : b.dgp_q)[(static_cast<long>(unit) * b.chunks_max + chunk) * kD + tid] = sum;
+    (which ? b.dgp_k : b.dgp_q)[(static_cast<long>(unit) * b.chunks_max + chunk) * kD + tid] =
+        failed ? __int_as_float(0x7fc00000) : sum;  // a wait that gave up cannot pass for a result
   }
+  if (failed && tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, 2u);
 }
 
 }  // namespace
@@ -1096,6 +1120,9 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
                                static_cast<int>(Lay::BYTES));
       if (e != cudaSuccess) return e;
     }
+    e = cudaFuncSetAttribute(bwd_tc_features, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kFeatSmem));
+    if (e != cudaSuccess) return e;
     configured |= 1ull << dev;
   }
   const long grid = static_cast<long>(b.p.n_docs) * b.p.H * b.nseg;
@@ -1131,7 +1158,13 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
                                                                                  tmg);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_tc_features<<<static_cast<unsigned>(fgrid), kMThreads, 0, stream>>>(b);
+  CUtensorMap tmq, tmk, tmdq, tmdk;
+  if ((e = make_rows_map(&tmq, b.p.q, rows, b.p.H, kD)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmk, b.p.k, rows, b.p.H, kD)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmdq, b.dqf, rows, b.p.H, kD)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmdk, b.dkf, rows, b.p.H, kD)) != cudaSuccess) return e;
+  bwd_tc_features<<<static_cast<unsigned>(fgrid), kMThreads, kFeatSmem, stream>>>(b, tmq, tmk, tmdq,
+                                                                                  tmdk);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   BwdArgs g = b;  // the gain partials are per (document, head, chunk)
