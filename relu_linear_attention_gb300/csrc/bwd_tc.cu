@@ -926,12 +926,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------------------------------------
 // Before the passes, fully parallel: q' = ReLU(RoPE(RMSNorm(q))) and k' likewise (bf16) of every
 // row into the workspace, where the forward and reverse passes take their q', k' tiles from. One
-// CTA of 256 threads per (document, head, chunk, q or k); a thread owns 8 consecutive elements of a
-// row (16 threads per row, 16 rows per pass, all 8 passes' loads in flight at once) and works on
-// packed fp32 pairs, with the gains and the RoPE frequencies and per-pass rotation in shared memory.
+// CTA of 256 threads per (document, head, chunk, q or k): the chunk's raw rows arrive in shared
+// memory by TMA; a thread owns 8 consecutive elements of a row (16 threads per row, 16 rows per
+// pass) and works on packed fp32 pairs, with the gains and the RoPE frequencies and per-pass
+// rotation in shared memory.
 constexpr int kMThreads = 256;
 
-__global__ void __launch_bounds__(kMThreads) bwd_tc_featmap(const BwdArgs b) {
+__global__ void __launch_bounds__(kMThreads)
+    bwd_tc_featmap(const BwdArgs b, const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_k) {
   constexpr int TPR = kD / 8, RPP = kMThreads / TPR, NPASS = kC / RPP;
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x;
@@ -944,33 +947,50 @@ __global__ void __launch_bounds__(kMThreads) bwd_tc_featmap(const BwdArgs b) {
   const int t0 = chunk * kC;
   if (t0 >= n) return;  // uniform
   __shared__ __align__(16) float tabmem[4 * kD];
+  __shared__ __align__(8) uint64_t bar_storage;
+  extern __shared__ __align__(1024) uint8_t fsmem[];
+  const uint32_t tile = (tc::smem_u32(fsmem) + 1023u) & ~1023u;  // the chunk's raw rows (TMA)
+  const uint32_t bar = tc::smem_u32(&bar_storage);
+  if (tid == 0) {
+    tc::mbar_init(bar, 1);
+    tc::mbar_fence_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const CUtensorMap* const maps[1] = {which ? &tm_k : &tm_q};
+    const uint32_t tl[1] = {tile};
+    tma_chunk<1>(maps, tl, h, static_cast<int>(row0 + t0), bar);
+  }
   const feat::FeatTab tab = feat::feat_tab<kD>(reinterpret_cast<uint8_t*>(tabmem));
   feat::fill_tab<kD>(tab, a, h, RPP, tid, kMThreads);
   __syncthreads();
   const int prow = tid / TPR, part = tid % TPR, e0 = 8 * part;
   const long rstride = static_cast<long>(a.H) * kD;
   const long off0 = (row0 + t0 + prow) * rstride + static_cast<long>(h) * kD + e0;
-  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(which ? a.k : a.q) + off0;
   __nv_bfloat16* xf = static_cast<__nv_bfloat16*>(which ? b.kf : b.qf) + off0;
-  uint4 raw[NPASS];
-#pragma unroll
-  for (int p = 0; p < NPASS; ++p)
-    raw[p] = t0 + p * RPP + prow < n ? feat::ldg16(x + p * RPP * rstride) : make_uint4(0, 0, 0, 0);
   float2 g0[2], g1[2];
   feat::split_load<kD>(which ? tab.gk : tab.gq, part, g0, g1);
   feat::Rot step, rot;
   feat::tab_step(tab, e0 / 2, step);
   feat::tab_rot_at(tab, a.pos_offset + t0 + prow, e0 / 2, rot);
+  if (!tc::mbar_wait(bar, 0, kWait)) {  // NaN features, so the failure cannot pass for a result
+    for (int p = 0; p < NPASS; ++p)
+      if (t0 + p * RPP + prow < n)
+        *reinterpret_cast<uint4*>(xf + p * RPP * rstride) =
+            make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
+    if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, 2u);
+    return;
+  }
 #pragma unroll
   for (int p = 0; p < NPASS; ++p) {
     if (p > 0) feat::rot_step(rot, step);
-    feat::Pairs f = feat::unpack_pairs(raw[p]);
+    const int r = p * RPP + prow;
+    feat::Pairs f = feat::unpack_pairs(feat::lds16(tile + tile_off(r, part)));
     const float ss = feat::row_sum<TPR>(feat::sumsq(f));
     float2 ga[2] = {g0[0], g0[1]}, gb[2] = {g1[0], g1[1]};
     feat::scale_gains(ga, gb, rsqrtf(ss * (1.0f / kD) + a.fa.eps_norm));
     feat::rope_relu(f, ga, gb, rot);
-    if (t0 + p * RPP + prow < n)
-      *reinterpret_cast<uint4*>(xf + p * RPP * rstride) = feat::pack_pairs(f);
+    if (t0 + r < n) *reinterpret_cast<uint4*>(xf + p * RPP * rstride) = feat::pack_pairs(f);
   }
 }
 
@@ -1128,7 +1148,10 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   const long grid = static_cast<long>(b.p.n_docs) * b.p.H * b.nseg;
   if (grid == 0) return cudaSuccess;
   const long fgrid = static_cast<long>(b.p.n_docs) * b.p.H * b.chunks_max * 2;
-  bwd_tc_featmap<<<static_cast<unsigned>(fgrid), kMThreads, 0, stream>>>(b);  // q', k'
+  CUtensorMap tmq, tmk;
+  if ((e = make_rows_map(&tmq, b.p.q, b.p.total_rows, b.p.H, kD)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmk, b.p.k, b.p.total_rows, b.p.H, kD)) != cudaSuccess) return e;
+  bwd_tc_featmap<<<static_cast<unsigned>(fgrid), kMThreads, kTile + 1024, stream>>>(b, tmq, tmk);  // q', k'
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // TMA maps of the row-major [rows, H, D] tensors the kernels stream
@@ -1158,9 +1181,7 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
                                                                                  tmg);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  CUtensorMap tmq, tmk, tmdq, tmdk;
-  if ((e = make_rows_map(&tmq, b.p.q, rows, b.p.H, kD)) != cudaSuccess) return e;
-  if ((e = make_rows_map(&tmk, b.p.k, rows, b.p.H, kD)) != cudaSuccess) return e;
+  CUtensorMap tmdq, tmdk;
   if ((e = make_rows_map(&tmdq, b.dqf, rows, b.p.H, kD)) != cudaSuccess) return e;
   if ((e = make_rows_map(&tmdk, b.dkf, rows, b.p.H, kD)) != cudaSuccess) return e;
   bwd_tc_features<<<static_cast<unsigned>(fgrid), kMThreads, kFeatSmem, stream>>>(b, tmq, tmk, tmdq,
