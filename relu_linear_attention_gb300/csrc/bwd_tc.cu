@@ -3,8 +3,11 @@
 //
 // The gradients of sum dout . out (08-rapt-algorithm.md §4.2 "backward": the main and z scans,
 // gnum = g / den and scale = -(g . num) / den^2, two suffix scans, then ReLU, RoPE and RMSNorm
-// backwards) in chunked form, C = 128 tokens per chunk (the MMA's M). First, fully parallel over
-// (document, head, chunk): q' and k' (bf16) of every row into the workspace. Per document and head:
+// backwards) in chunked form, C = 128 tokens per chunk (the MMA's M), in seven launches. First,
+// fully parallel over (document, head, chunk): q' and k' (bf16) of every row into the workspace
+// (bwd_tc_featmap). Documents are cut into segments; the prefix state at each segment's start is the
+// sum of per-block increments S = sum k'v^T, z = sum k' of the blocks before it (bwd_tc_blockstate
+// <true>). Per document, head and segment:
 //
 // Pass A (chunks in order; prefix state S = sum k'v^T in TMEM, its bf16 copy S~ in shared memory):
 //   P  = Q'K'^T,  Cv = G V^T,  U = G S~^T,  S += K'^T V                     (one MMA group)
@@ -16,20 +19,23 @@
 //   U += A'~ K'                                                                (second MMA group)
 //   dq'_t = U_t / den_t + scale_t z (bf16, to the workspace); den, scale, sst, nst of every row go
 //   to the workspace for pass B.
+// Between the passes, the suffix state at each segment's end is the sum of per-block increments
+// R = sum q' gnum^T, w = sum scale q' of the later blocks (bwd_tc_blockstate<false>).
 // Pass B (chunks in reverse; suffix state R = sum q' gnum^T in TMEM, bf16 copy R~, w = sum scale q'):
 //   P = Q'K'^T,  Gv = Gnum V^T                                              (first group)
+//   then, while P~ and A are formed:  dv = K' R~,  R += Q'^T Gnum
 //   P~ = P masked to tau <= t;  A[t][tau] = A'/den, with c = den Gv
-//   dv  = P~^T Gnum + K' R~                                                  (second group)
-//   dk' = A^T Q' + V R~^T (+ w),  R += Q'^T Gnum                             (third group)
-//   dk' (bf16) to the workspace.
+//   dv += P~^T Gnum,  dk' = V R~^T                                           (second group)
+//   dk' += A^T Q' (+ w)                                                      (third group)
+//   dk' (bf16) to the workspace, dv out.
 // Then, fully parallel over (document, head, chunk), dq and dk through the feature map (ReLU mask,
-// inverse RoPE rotation, RMSNorm backward) from dq', dk' and the raw q, k, with gain partials.
+// inverse RoPE rotation, RMSNorm backward) from dq', dk' and the raw q, k, with gain partials
+// (bwd_tc_features), and the gains summed in a fixed order.
 // The passes run one CTA per (document, head, segment), 512 threads in lockstep phases: all threads
 // read TMEM rows (thread = TMEM lane = tile row, four warps per lane quarter splitting the columns)
 // and do the per-row arithmetic; one thread issues the MMAs and the TMA copies of the next chunk's
-// tiles and commits them to mbarriers. Every
-// wait is bounded (~1 s); a CTA whose wait gives up sets RAPT_DEV_INTERNAL in the status word and
-// writes NaN gain partials, so a failure cannot pass for a result.
+// tiles and commits them to mbarriers. Every wait is bounded (~1 s); a CTA whose wait gives up sets
+// RAPT_DEV_INTERNAL in the status word and writes NaN results, so a failure cannot pass for one.
 #include <cuda.h>
 
 #include "feature_bwd.cuh"
