@@ -226,3 +226,35 @@ def test_prefill_bwd_tensor_cores_shared_gains_many_segments(cuda_device, lib):
         assert O.relative_error(to_host(dv)[b], rv[b])[0] <= TOL["bf16"]
     assert _vec_err(to_host(dgq), rgq) <= TOL["bf16"]
     assert _vec_err(to_host(dgk), rgk) <= TOL["bf16"]
+
+
+def test_varlen_bwd_multi_block_segments_sampled(cuda_device, lib):
+    """Tensor-core backward over 4 documents x 16 heads (64 (document, head) pairs, so the plan
+    cuts documents into two segments of several blocks each): a full-length document, one whose
+    second segment ends inside its first suffix block, one whose second segment ends inside its
+    second block, and one shorter than a segment (no prefix or suffix blocks at all). The oracle
+    checks whole (document, head) pairs; positions restart at every document."""
+    lens = [4096, 3000, 4005, 1500]
+    cu = syn.cu_seqlens_from_lengths(lens)
+    T, H, d = int(cu[-1]), 16, 128
+    q, k, v = draw(370, (T, H, d), "bf16")
+    (g,) = draw(371, (T, H, d), "bf16")[:1]
+    gq, gk = gammas(372, H, d, True)
+    dev = lambda x: torch.from_numpy(x).to(cuda_device)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    dq, dk, dv, _, _ = R.rapt_varlen_bwd(to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16"),
+                                         to_dev(g, "bf16"), dev(cu), dev(gq), dev(gk),
+                                         max_seqlen=max(lens), dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for doc, h in [(1, 3), (2, 10), (3, 0), (0, 15)]:
+        s, e = int(cu[doc]), int(cu[doc + 1])
+        pos = np.arange(e - s)
+        qs, ks, vs, gs = (widen(x[s:e, h:h + 1][None], "bf16") for x in (q, k, v, g))
+        rq, rk, rv, _, _ = O.rla2_prefill_bwd(qs, ks, vs, gs, gq[h:h + 1], gk[h:h + 1], EPS_N, BASE,
+                                              EPS_D)
+        keep_q = ~_ambiguous(qs[0], gq[h:h + 1], pos)
+        keep_k = ~_ambiguous(ks[0], gk[h:h + 1], pos)
+        assert _row_err(to_host(dq[s:e, h:h + 1]), rq[0], keep_q) <= TOL["bf16"]
+        assert _row_err(to_host(dk[s:e, h:h + 1]), rk[0], keep_k) <= TOL["bf16"]
+        assert O.relative_error(to_host(dv[s:e, h:h + 1]), rv[0])[0] <= TOL["bf16"]
