@@ -255,16 +255,17 @@ __global__ void __launch_bounds__(256) l2_tc_reduce(const float* ws, int nsplit,
 // quarter (warp % 4), each taking half of a row's columns; warps 8-11 apply the ReLU.
 template <int D>
 struct P2 {
+  static constexpr int S = 4;  // q tile stages (four tiles of loads and stores in flight)
   static constexpr int DB = D / 64;
   static constexpr int N = 2 * D;
   static constexpr int HALF = D / 2;
   static constexpr uint32_t MB = (N / 64) * D * 128;
   static constexpr uint32_t QT = DB * 16384;
   static constexpr uint32_t QS = MB;
-  static constexpr uint32_t DP = QS + kStages * QT;         // partial den^2 [2 halves][128 rows]
+  static constexpr uint32_t DP = QS + S * QT;               // partial den^2 [2 halves][128 rows]
   // mfull, qfull[S], relu[S], staged[S], accf[2], accfree[2]
   static constexpr uint32_t BAR = DP + 2 * kC * 4;
-  static constexpr uint32_t MISC = BAR + (1 + 3 * kStages + 4) * 8;
+  static constexpr uint32_t MISC = BAR + (1 + 3 * S + 4) * 8;
   static constexpr uint32_t BYTES = MISC + 16;
   static_assert(MB % 1024 == 0 && QT % 1024 == 0, "tile alignment");
   static_assert(BYTES <= 232448, "shared memory budget");
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(kP2Threads, 1)
     l2_tc_readout(const L2Args a, int nsplit, int split_chunks, long img_offset,
                   const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap to) {
   using L = P2<D>;
-  constexpr int S = kStages, N = L::N, HALF = L::HALF;
+  constexpr int S = L::S, N = L::N, HALF = L::HALF;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sp = blockIdx.x % nsplit, bh = blockIdx.x / nsplit;
   const int b = bh / a.H, h = bh % a.H;
@@ -406,34 +407,46 @@ __global__ void __launch_bounds__(kP2Threads, 1)
       tc::fence_after_sync();
       const uint32_t acc = tmem + tl + x * N;
       const uint32_t qb = tile(s);
-      // partial den^2 over this half: sum_j q'_j (q'M_K)_j with the bf16 q' of the GEMM
+      // partial den^2 over this half: sum_j q'_j (q'M_K)_j with the bf16 q' of the GEMM, 32
+      // columns per TMEM round trip
       float2 d2 = make_float2(0.f, 0.f);
 #pragma unroll 1
-      for (int j0 = c0h; j0 < c0h + HALF; j0 += 16) {
-        uint32_t y[16];
-        tc::tmem_ld16(acc + D + j0, y);
+      for (int j0 = c0h; j0 < c0h + HALF; j0 += 32) {
+        uint32_t y[2][16];
+        tc::tmem_ld16(acc + D + j0, y[0]);
+        tc::tmem_ld16(acc + D + j0 + 16, y[1]);
         const uint32_t blk = qb + static_cast<uint32_t>(j0 / 64) * 16384;
-        const uint4 qa = lds16(blk + tc::sw128(er, (j0 % 64) / 8));
-        const uint4 qc = lds16(blk + tc::sw128(er, (j0 % 64) / 8 + 1));
-        tc::tmem_wait_ld();
-        const uint32_t qw[8] = {qa.x, qa.y, qa.z, qa.w, qc.x, qc.y, qc.z, qc.w};
+        uint4 qv[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          d2 = __ffma2_rn(make_float2(__uint_as_float(qw[e] << 16), __uint_as_float(qw[e] & 0xffff0000u)),
-                          make_float2(__uint_as_float(y[2 * e]), __uint_as_float(y[2 * e + 1])), d2);
+        for (int m = 0; m < 4; ++m) qv[m] = lds16(blk + tc::sw128(er, (j0 % 64) / 8 + m));
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const uint32_t qw[4] = {qv[m].x, qv[m].y, qv[m].z, qv[m].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            d2 = __ffma2_rn(make_float2(__uint_as_float(qw[e] << 16), __uint_as_float(qw[e] & 0xffff0000u)),
+                            make_float2(__uint_as_float(y[m >> 1][8 * (m & 1) + 2 * e]),
+                                        __uint_as_float(y[m >> 1][8 * (m & 1) + 2 * e + 1])),
+                            d2);
+        }
       }
       dpart[g * kC + er] = d2.x + d2.y;
+      // the numerator's half row is requested from TMEM before the barrier: its latency overlaps
+      // the wait for the other half's den partial
+      uint32_t u[HALF / 16][16];
+#pragma unroll
+      for (int m = 0; m < HALF / 16; ++m) tc::tmem_ld16(acc + c0h + 16 * m, u[m]);
       tc::named_sync(kBarEpi, 256);
       const float inv = 1.0f / (sqrtf(dpart[er] + dpart[kC + er]) + a.eps);  // fixed order
+      tc::tmem_wait_ld();
       // out = num / den over this half of the row (the bytes this thread read q' from)
-#pragma unroll 1
-      for (int j0 = c0h; j0 < c0h + HALF; j0 += 16) {
-        uint32_t u[16];
-        tc::tmem_ld16(acc + j0, u);
-        tc::tmem_wait_ld();
+#pragma unroll
+      for (int m = 0; m < HALF / 16; ++m) {
+        const int j0 = c0h + 16 * m;
         float f[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(u[e]) * inv;
+        for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(u[m][e]) * inv;
         const uint32_t blk = qb + static_cast<uint32_t>(j0 / 64) * 16384;
         sts16(blk + tc::sw128(er, (j0 % 64) / 8),
               make_uint4(tc::pack_bf16x2(f[0], f[1]), tc::pack_bf16x2(f[2], f[3]),
