@@ -35,7 +35,7 @@ using namespace feat;
 
 constexpr int kC = 128;                    // tokens per tile = MMA M
 constexpr long long kWait = 2000000000LL;  // ~1 s
-constexpr int kStages = 3;                 // q tiles in flight
+constexpr int kStages = 5;                 // q tiles in flight
 constexpr int kEpi = 128;                  // warps 0-3: epilogue (one TMEM lane quarter each)
 constexpr int kFeat = 512;                 // the next warps: features (16)
 constexpr int kWarpTma = (kEpi + kFeat) / 32;  // then one TMA warp and one MMA warp
