@@ -28,6 +28,9 @@
 //   dv += P~^T Gnum,  dk' = V R~^T                                           (second group)
 //   dk' += A^T Q' (+ w)                                                      (third group)
 //   dk' (bf16) to the workspace, dv out.
+// The passes stage a whole chunk's dq' (pass A) and dk', dv (pass B) in shared memory that the
+// chunk's MMAs no longer read and write them with TMA tile stores; a document's ragged last chunk
+// is written row by row.
 // Then, fully parallel over (document, head, chunk), dq and dk through the feature map (ReLU mask,
 // inverse RoPE rotation, RMSNorm backward) from dq', dk' and the raw q, k, with gain partials
 // (bwd_tc_features), and the gains summed in a fixed order.
@@ -189,7 +192,7 @@ __device__ __forceinline__ void raw_tiles_tc(const __nv_bfloat16* const (&src)[N
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_forward(const BwdArgs b, const __grid_constant__ CUtensorMap tmqf,
                    const __grid_constant__ CUtensorMap tmkf, const __grid_constant__ CUtensorMap tmv,
-                   const __grid_constant__ CUtensorMap tmg) {
+                   const __grid_constant__ CUtensorMap tmg, const __grid_constant__ CUtensorMap tmdq) {
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int seg = blockIdx.x % b.nseg, unit = blockIdx.x / b.nseg;
@@ -287,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     feature_sums(base + Lay::KF, n, t0, nullptr, nullptr, zc);
 #pragma unroll
     for (int e = 0; e < 4; ++e) zp[warp * kD + 4 * lane + e] = zc[e];
+    if (tid == 0) tc::bulk_wait_read0();  // the previous chunk's dq' store has read AS
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
@@ -397,7 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = 1.0f / den;
 #pragma unroll
       for (int j = 0; j < 32; ++j) u[j] = fmaf(u[j], inv, scale * zs[32 * gw + j]);
-      if (valid) {
+      if (t0 + kC <= n) {  // a whole chunk: staged in AS (its last reader, phase 4, is done)
+        store_row32<false>(base + Lay::AS, t, gw, u);
+      } else if (valid) {  // the ragged last chunk row by row (a tile store would reach past it)
         __nv_bfloat16* dst = dqf_out + ((row0 + t0 + t) * a.H + h) * kD + 32 * gw;
 #pragma unroll
         for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(u + 8 * m);
@@ -409,6 +415,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
+    if (tid == 0 && t0 + kC <= n) {
+#pragma unroll
+      for (int jb = 0; jb < 2; ++jb)
+        tc::tma_store_3d(&tmdq, base + Lay::AS + jb * 16384, 64 * jb, h, static_cast<int>(row0 + t0));
+      tc::bulk_commit();
+    }
     if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
     // ---- phase 6: z += column sums of k'
     if (tid < kD) {
@@ -421,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   bad = bad || *reinterpret_cast<volatile int*>(s_abort) != 0;
   // a copy requested but not waited for (an early exit) must land before the CTA leaves
   if (tid == 0 && tma_issued > 0) tc::mbar_wait(bar_ld, (tma_issued - 1) & 1, kWait);
+  if (tid == 0) tc::bulk_wait0();  // the dq' tile stores are complete before the NaN fill or exit
   __syncthreads();
   if (bad) {  // a wait gave up: NaN dq' over the segment, so the failure cannot pass for a result
     for (long r = s0 + tid / 16; r < s1; r += kThreads / 16)
@@ -439,7 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_reverse(const BwdArgs b, const __grid_constant__ CUtensorMap tmqf,
                    const __grid_constant__ CUtensorMap tmkf, const __grid_constant__ CUtensorMap tmv,
-                   const __grid_constant__ CUtensorMap tmg) {
+                   const __grid_constant__ CUtensorMap tmg, const __grid_constant__ CUtensorMap tmdv,
+                   const __grid_constant__ CUtensorMap tmdk) {
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int seg = blockIdx.x % b.nseg, unit = blockIdx.x / b.nseg;
@@ -556,6 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (c > 0) row_scalars(t0 - kC, rs_next);  // the earlier chunk's, one chunk ahead
     if (!tc::mbar_wait(bar_ld, it & 1, kWait) || !tc::mbar_wait(bar_ldq, it & 1, kWait))
       atomicExch(s_abort, 1);
+    if (tid == 0) tc::bulk_wait_read0();  // the previous chunk's dk' store has read AS
     __syncthreads();  // den_s
     for (int idx = tid; idx < kC * 16; idx += kThreads) {
       const int r = idx >> 4, m = idx & 15;
@@ -686,14 +701,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                      ID_MM, 1u);
       tc::mma_commit(bar3);  // dk' done, and with it every MMA of the chunk (R included)
     }
+    // a whole chunk's dv and dk' are staged in shared memory and written by TMA (full lines); the
+    // ragged last chunk of a document is written row by row (a tile store would reach past it)
+    const bool whole = t0 + kC <= n;
     {
       float o[32];
       tmem_ld32(tmem + tl + kTDV + 32 * gw, o);
-      if (t0 + t < n) {
+      if (whole) {  // into XS: R~'s last readers (the first two groups) are done
+        store_row32<false>(base + Lay::XS, t, gw, o);
+      } else if (t0 + t < n) {
         __nv_bfloat16* dst = dv + ((row0 + t0 + t) * a.H + h) * kD + 32 * gw;
 #pragma unroll
         for (int m = 0; m < 4; ++m)
           *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(o + 8 * m);
+      }
+    }
+    if (whole) {
+      tc::fence_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+#pragma unroll
+        for (int jb = 0; jb < 2; ++jb)
+          tc::tma_store_3d(&tmdv, base + Lay::XS + jb * 16384, 64 * jb, h, static_cast<int>(row0 + t0));
+        tc::bulk_commit();
       }
     }
     if (!wait_mma(bar3, it & 1)) atomicExch(s_abort, 1);
@@ -709,14 +739,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tmem + tl + kTDK + 32 * gw, o);
 #pragma unroll
       for (int j = 0; j < 32; ++j) o[j] += ws[32 * gw + j];
-      if (t0 + t < n) {  // dk' (bf16) to the workspace
+      if (whole) {  // into AS: A's last reader (the third group) is done
+        store_row32<false>(base + Lay::AS, t, gw, o);
+      } else if (t0 + t < n) {  // dk' (bf16) to the workspace
         __nv_bfloat16* dst = dkf_out + ((row0 + t0 + t) * a.H + h) * kD + 32 * gw;
 #pragma unroll
         for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(o + 8 * m);
       }
       tc::fence_async_smem();
+      if (tid == 0) tc::bulk_wait_read0();  // the dv store has read XS (R~ is rewritten below)
       tc::fence_before_sync();
       __syncthreads();  // w is read
+      if (whole && tid == 0) {
+#pragma unroll
+        for (int jb = 0; jb < 2; ++jb)
+          tc::tma_store_3d(&tmdk, base + Lay::AS + jb * 16384, 64 * jb, h, static_cast<int>(row0 + t0));
+        tc::bulk_commit();
+      }
       if (tid < kD)
         ws[tid] += red[8 * kC + tid] + red[9 * kC + tid] + red[10 * kC + tid] + red[11 * kC + tid];
       float rv[32];
@@ -731,6 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   bad = bad || *reinterpret_cast<volatile int*>(s_abort) != 0;
   if (tid == 0 && tma_issued > 0) tc::mbar_wait(bar_ld, (tma_issued - 1) & 1, kWait);
   if (tid == 0 && tmaq_issued > 0) tc::mbar_wait(bar_ldq, (tmaq_issued - 1) & 1, kWait);
+  if (tid == 0) tc::bulk_wait0();  // the tile stores are complete before the NaN fill or exit
   __syncthreads();
   if (bad) {  // a wait gave up: NaN dk' and dv over the segment
     for (long r = s0 + tid / 16; r < s1; r += kThreads / 16) {
@@ -1173,8 +1213,13 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
     note_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  // dq', dk' (written by the passes, read by the feature kernel) and dv
+  CUtensorMap tmdq, tmdk, tmdv;
+  if ((e = make_rows_map(&tmdq, b.dqf, rows, b.p.H, kD)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmdk, b.dkf, rows, b.p.H, kD)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmdv, b.dv, rows, b.p.H, kD)) != cudaSuccess) return e;
   bwd_tc_forward<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b, tmqf, tmkf, tmv,
-                                                                                 tmg);
+                                                                                 tmg, tmdq);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (b.nseg > 1) {
@@ -1184,12 +1229,9 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   bwd_tc_reverse<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b, tmqf, tmkf, tmv,
-                                                                                 tmg);
+                                                                                 tmg, tmdv, tmdk);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  CUtensorMap tmdq, tmdk;
-  if ((e = make_rows_map(&tmdq, b.dqf, rows, b.p.H, kD)) != cudaSuccess) return e;
-  if ((e = make_rows_map(&tmdk, b.dkf, rows, b.p.H, kD)) != cudaSuccess) return e;
   bwd_tc_features<<<static_cast<unsigned>(fgrid), kMThreads, kFeatSmem, stream>>>(b, tmq, tmk, tmdq,
                                                                                   tmdk);
   note_launches(1);
