@@ -55,6 +55,7 @@ DENSE_CASES = [
     (1, 1, 1, 128, "bf16", False, 0),
     (2, 300, 2, 64, "bf16", True, 0),
     (1, 1000, 3, 128, "bf16", True, 7),
+    (2, 384, 2, 128, "bf16", False, 3),   # whole chunks only: every tile leaves by TMA stores
     (3, 257, 5, 128, "f32", True, 0),
 ]
 
