@@ -236,6 +236,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q4 = warp & 3, gw = warp >> 2;  // TMEM lane quarter, column group (32 columns)
   const int t = 32 * q4 + lane;             // this thread's tile row (= TMEM lane)
   const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
+  // the first chunk's tiles are requested before the state is summed (they do not overlap it)
+  const CUtensorMap* const maps[4] = {&tmqf, &tmkf, &tmv, &tmg};
+  const uint32_t ld_tiles[4] = {base + Lay::QF, base + Lay::KF, base + Lay::VS, base + Lay::GS};
+  int tma_issued = 0;  // chunks whose tiles have been requested (thread 0)
+  if (tid == 0 && nch > 0 && !*s_abort) {
+    tma_chunk<4>(maps, ld_tiles, h, static_cast<int>(row0 + s0), bar_ld);
+    tma_issued = 1;
+  }
   // the prefix state at the segment's start: the increments of the blocks before it, in order
   if (nch > 0) {
     const int nb = seg * b.blk_per_seg;
@@ -263,13 +271,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
 
-  const CUtensorMap* const maps[4] = {&tmqf, &tmkf, &tmv, &tmg};
-  const uint32_t ld_tiles[4] = {base + Lay::QF, base + Lay::KF, base + Lay::VS, base + Lay::GS};
-  int tma_issued = 0;  // chunks whose tiles have been requested (thread 0)
-  if (tid == 0 && nch > 0 && !*s_abort) {
-    tma_chunk<4>(maps, ld_tiles, h, static_cast<int>(row0 + s0), bar_ld);
-    tma_issued = 1;
-  }
   __nv_bfloat16* dqf_out = static_cast<__nv_bfloat16*>(b.dqf);
   bool bad = *s_abort != 0;
 
@@ -498,6 +499,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q4 = warp & 3, gw = warp >> 2;
   const int t = 32 * q4 + lane;
   const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
+  // the tiles arrive in two groups, each as soon as the previous chunk's MMAs are done with them:
+  // k', v, gnum after the dv group (bar_ld), q' after the last group (bar4); the first chunk's
+  // are requested before the suffix state is summed (they do not overlap it)
+  const CUtensorMap* const maps3[3] = {&tmkf, &tmv, &tmg};
+  const uint32_t ld_tiles3[3] = {base + Lay::KF, base + Lay::VS, base + Lay::GS};
+  const CUtensorMap* const maps1[1] = {&tmqf};
+  const uint32_t ld_tiles1[1] = {base + Lay::QF};
+  const uint32_t bar_ldq = bar4;
+  int tma_issued = 0, tmaq_issued = 0;  // chunks whose tiles have been requested (thread 0)
+  if (tid == 0 && nch > 0 && !*s_abort) {
+    tma_chunk<3>(maps3, ld_tiles3, h, static_cast<int>(row0 + s0 + (nch - 1) * kC), bar_ld);
+    tma_chunk<1>(maps1, ld_tiles1, h, static_cast<int>(row0 + s0 + (nch - 1) * kC), bar_ldq);
+    tma_issued = tmaq_issued = 1;
+  }
   // the suffix state at the segment's end: the later segments' increments, in segment order
   if (nch > 0) {
     constexpr long REC = static_cast<long>(kD) * kD + kD;
@@ -530,19 +545,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(b.dv);
   __nv_bfloat16* dkf_out = static_cast<__nv_bfloat16*>(b.dkf);
-  // the tiles arrive in two groups, each as soon as the previous chunk's MMAs are done with them:
-  // k', v, gnum after the dv group (bar_ld), q' after the last group (bar4)
-  const CUtensorMap* const maps3[3] = {&tmkf, &tmv, &tmg};
-  const uint32_t ld_tiles3[3] = {base + Lay::KF, base + Lay::VS, base + Lay::GS};
-  const CUtensorMap* const maps1[1] = {&tmqf};
-  const uint32_t ld_tiles1[1] = {base + Lay::QF};
-  const uint32_t bar_ldq = bar4;
-  int tma_issued = 0, tmaq_issued = 0;  // chunks whose tiles have been requested (thread 0)
-  if (tid == 0 && nch > 0 && !*s_abort) {
-    tma_chunk<3>(maps3, ld_tiles3, h, static_cast<int>(row0 + s0 + (nch - 1) * kC), bar_ld);
-    tma_chunk<1>(maps1, ld_tiles1, h, static_cast<int>(row0 + s0 + (nch - 1) * kC), bar_ldq);
-    tma_issued = tmaq_issued = 1;
-  }
   bool bad = *s_abort != 0;
   int it = 0;  // chunks done (the mbarrier phases)
 
