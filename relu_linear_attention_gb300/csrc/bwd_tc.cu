@@ -252,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float sv[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) sv[e] = 0.f;
+#pragma unroll 2  // two records' loads in flight together
     for (int blk = 0; blk < nb; ++blk) {
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
@@ -523,6 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float rv[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) rv[e] = 0.f;
+#pragma unroll 2  // two records' loads in flight together
     for (int kb = k0; kb < k1; ++kb) {
       const float4* src = reinterpret_cast<const float4*>(rr + kb * REC + t * kD + 32 * gw);
 #pragma unroll
