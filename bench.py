@@ -44,6 +44,30 @@ L2_FLUSH_BYTES = 256 << 20  # > 129 MB of L2
 
 
 # ----------------------------------------------------------------------------- host helpers
+def headline_config(world: int) -> dict:
+    """The workload dictionary both arms print (the GPU arm and the oracle reference arm)."""
+    return {"workload": "rla2_causal_prefill B=4 L=4096 H=16 d=128 bf16 (fp32 state)",
+            "model": "RLA-2/RAPT attention layer (no projections)",
+            "global_batch": WORKLOAD["B"] * world, "seq_len": WORKLOAD["L"],
+            "heads": WORKLOAD["H"], "d_head": WORKLOAD["d"],
+            "parallelism": "dp%d (independent batch per GPU)" % world,
+            "l2": "256 MiB write, then 256 MiB read, before every timed step, outside the CUDA events"}
+
+
+def host_cpu_model() -> str:
+    """The host CPU's model name (lscpu), for the CPU baseline's record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+
+    return platform.processor() or platform.machine()
+
+
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
@@ -189,10 +213,10 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "rla2_causal_prefill B=4 L=4096 H=16 d=128 bf16 inputs",
-                   "global_batch": 4, "seq_len": 4096, "parallelism": "host oracle, rank 0 only"},
+        "config": headline_config(world),
+        "runs_on": "host cores, fp64 numpy oracle, rank 0 only",
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(),
-                         "kind": "oracle", "sample": sample},
+                         "cpu_model": host_cpu_model(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -572,7 +596,8 @@ def run_gpu(args, rank, world, local):
     cpu = None
     if rank == 0 and world == 1:
         tps, pairs, secs, cores = oracle_sample(args.oracle_seconds, rank_seed(1, 0))
-        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "cpu_model": host_cpu_model(),
+               "kind": "oracle",
                "sample": "%d of 64 (batch row, head) pairs of the headline workload, all 4096 rows "
                          "each, fp64 quadratic form, %.1f s; numpy BLAS threads = host cores"
                          % (pairs, secs)}
@@ -583,11 +608,7 @@ def run_gpu(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "rla2_causal_prefill B=4 L=4096 H=16 d=128 bf16 (fp32 state)",
-                   "model": "RLA-2/RAPT attention layer (no projections)", "global_batch": B * world,
-                   "seq_len": L, "heads": H, "d_head": d,
-                   "parallelism": "dp%d (independent batch per GPU)" % world,
-                   "l2": "256 MiB write, then 256 MiB read, before every timed step, outside the CUDA events"},
+        "config": headline_config(world),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "kernels": "segment_state_kernel + prefill_tc_kernel (one call; the second is "
@@ -600,9 +621,17 @@ def run_gpu(args, rank, world, local):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(timed_launches),
         "clocks": clk,
-        "decode": decode, "varlen": varlen, "rla_l2": rla_l2, "bidir": bidir,
-        "backward": backward, "l2_causal": l2_causal, "layer": layer,
         "cpu_baseline": cpu,
+        "rla_l2": rla_l2, "bidir": bidir, "backward": backward, "l2_causal": l2_causal,
+        "layer": layer, "varlen": varlen, "decode": decode,
+        # the headline numbers once more, compactly, at the end of the line
+        "summary": {"prefill_tokens_per_s": value, "prefill_hbm_frac": achieved / peaks["hbm_gbs"],
+                    "decode_tokens_per_s": decode["value"],
+                    "decode_hbm_frac": decode["roofline"]["frac"],
+                    "varlen_tokens_per_s": varlen["value"],
+                    "varlen_hbm_frac": varlen["roofline"]["frac"],
+                    "l2_hbm_frac": rla_l2["roofline"]["frac"],
+                    "e2e_tokens_per_s": e2e_value},
     }
     if rank == 0:
         print(json.dumps(line))

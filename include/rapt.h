@@ -360,8 +360,10 @@ rapt_status rla_l2_fwd(const void* q, const void* k, const void* v, rapt_dtype d
  *   - Returns RAPT_ERR_WORKSPACE, before launching anything, when even one split does not fit:
  *     B * H * 2 * d * 2d * 4 bytes must not exceed RAPT_L2_NOALLOC_SCRATCH_BYTES (at d = 128,
  *     B * H <= 64).
- *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
- *     with that device current); make that first call before any stream capture.
+ *   - Every call looks up the array's device address on the current device
+ *     (cudaGetSymbolAddress), so an address never outlives its context (after cudaDeviceReset the
+ *     module is loaded again and the array may move). The first call on a device also loads the
+ *     library's kernels there; make that first call before any stream capture.
  *   - Every call on a device uses the same array. Calls whose kernels overlap on the GPU (for
  *     example on two streams without ordering between them) race on it and give wrong results;
  *     serialise them. Nothing has to be cleared between calls: every element of the array that a

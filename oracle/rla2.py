@@ -205,21 +205,19 @@ def rla2_decode_step(q, k, v, positions, gamma_q, gamma_k, S, z, eps_norm=1e-6,
     update the state first (S += k' v^T, z += k'), then read out
     q' S / (q' . z + eps). q, k, v: [N, H, d]; S [N, H, d, d]; z [N, H, d].
     Returns (out [N, H, d], S_new, z_new); the inputs are not modified.
+    Every (sequence, head) is independent; the arrays hold all of them at once.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
-    N, H, d = q.shape
+    pos = np.asarray(positions).reshape(-1)
+    qf = features(q, gamma_q, pos, eps_norm, rope_base)  # [N, H, d]
+    kf = features(k, gamma_k, pos, eps_norm, rope_base)
     S = _f64(S).copy()
-    z = _f64(z).copy()
-    out = np.zeros((N, H, v.shape[2]))
-    for n in range(N):
-        pos = np.array([positions[n]])
-        for h in range(H):
-            qf = features(q[n:n + 1, h], _gamma_h(gamma_q, h), pos, eps_norm, rope_base)[0]
-            kf = features(k[n:n + 1, h], _gamma_h(gamma_k, h), pos, eps_norm, rope_base)[0]
-            S[n, h] += np.outer(kf, v[n, h])
-            z[n, h] += kf
-            out[n, h] = (qf @ S[n, h]) / (qf @ z[n, h] + float(eps_den))
-    return out, S, z
+    for n in range(S.shape[0]):  # one sequence at a time (bounds the temporary)
+        S[n] += kf[n, :, :, None] * v[n, :, None, :]     # S[n, h, i, j] += k'_i v_j
+    z = _f64(z) + kf
+    num = (qf[..., None, :] @ S)[..., 0, :]              # q' S per (sequence, head)
+    den = (qf * z).sum(axis=-1) + float(eps_den)
+    return num / den[..., None], S, z
 
 
 def rla2_decode_from_history(q_new, k_hist, v_hist, pos_new, gamma_q, gamma_k, eps_norm=1e-6,

@@ -200,6 +200,8 @@ rapt_status rapt_prefill_fwd_host(const void* q, const void* k, const void* v, r
   const size_t pre_bytes = workspace_bytes - 2 * slot_stride;
   const long sdd = static_cast<long>(H) * d * d, sd = static_cast<long>(H) * d;
   HostEvents ev;
+  bool in_rec[2] = {false, false}, out_rec[2] = {false, false};  // events recorded per slot
+  rapt_status fail = RAPT_OK;
   cudaError_t e = ev.create();
   if (e == cudaSuccess) e = cudaEventRecord(ev.start, s);  // after the work already on `stream`
   if (e == cudaSuccess) e = cudaStreamWaitEvent(si, ev.start, 0);
@@ -215,6 +217,7 @@ rapt_status rapt_prefill_fwd_host(const void* q, const void* k, const void* v, r
     if (e == cudaSuccess) e = cudaMemcpyAsync(kd, static_cast<const uint8_t*>(k) + off, row, cudaMemcpyDefault, si);
     if (e == cudaSuccess) e = cudaMemcpyAsync(vd, static_cast<const uint8_t*>(v) + off, row, cudaMemcpyDefault, si);
     if (e == cudaSuccess) e = cudaEventRecord(ev.in[slot], si);
+    if (e == cudaSuccess) in_rec[slot] = true;
     // compute (once the row is in and the row two back has been copied out of this slot)
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev.in[slot], 0);
     if (e == cudaSuccess && b >= 2) e = cudaStreamWaitEvent(s, ev.out[slot], 0);
@@ -224,16 +227,26 @@ rapt_status rapt_prefill_fwd_host(const void* q, const void* k, const void* v, r
                           od, S_final != nullptr ? S_final + b * sdd : nullptr,
                           z_final != nullptr ? z_final + b * sd : nullptr, dev_status, ws_pre,
                           pre_bytes, stream);
-    if (st != RAPT_OK) return st;
+    if (st != RAPT_OK) {
+      fail = st;
+      break;
+    }
     e = cudaEventRecord(ev.comp[slot], s);
     // copy out
     if (e == cudaSuccess) e = cudaStreamWaitEvent(so, ev.comp[slot], 0);
     if (e == cudaSuccess) e = cudaMemcpyAsync(static_cast<uint8_t*>(out) + off, od, row, cudaMemcpyDefault, so);
     if (e == cudaSuccess) e = cudaEventRecord(ev.out[slot], so);
+    if (e == cudaSuccess) out_rec[slot] = true;
   }
-  // `stream` covers everything: it waits for the last copies out
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev.out[(B - 1) & 1], 0);
-  if (e == cudaSuccess && B >= 2) e = cudaStreamWaitEvent(s, ev.out[B & 1], 0);
+  // `stream` covers everything queued, also when a row failed: it waits for the last copies in
+  // and out of both slots, so a caller that synchronises `stream` may then free the buffers
+  for (int slot = 0; slot < 2; ++slot) {
+    cudaError_t w = cudaSuccess;
+    if (in_rec[slot]) w = cudaStreamWaitEvent(s, ev.in[slot], 0);
+    if (w == cudaSuccess && out_rec[slot]) w = cudaStreamWaitEvent(s, ev.out[slot], 0);
+    if (e == cudaSuccess) e = w;
+  }
+  if (fail != RAPT_OK) return fail;
   return from_cuda(e);
 }
 

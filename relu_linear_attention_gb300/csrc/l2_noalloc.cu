@@ -5,36 +5,26 @@
 // that must never call cudaMalloc (it can synchronise the device). For them the fp32 partial
 // moments of the L2 kernels live in a fixed array compiled into the library, instead of a
 // caller-provided workspace. The split count over tokens is lowered until the moments fit.
-#include <mutex>
-
 #include "../../include/rapt.h"
 #include "kernels.h"
 
 namespace {
 
 constexpr size_t kScratchFloats = RAPT_L2_NOALLOC_SCRATCH_BYTES / sizeof(float);
-constexpr int kMaxDevices = 128;
 
 // Scratch for the partial and reduced moments. Host code must not use this name as a pointer:
 // on the host it is only a stand-in for the symbol, whose device address comes from
 // cudaGetSymbolAddress below.
 static __device__ __align__(256) float g_l2_scratch[kScratchFloats];
 
-std::mutex g_mu;
-float* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_l2_scratch on the current device, looked up once per device.
+// Device address of g_l2_scratch in the current device's context. It is looked up on every call
+// (a lookup allocates nothing): a cached address would go stale once the context is destroyed and
+// created again (cudaDeviceReset), because the module is then loaded anew and may move. The first
+// call on a device loads the module (lazy loading), so make it before any stream capture.
 rapt_status scratch_on_current_device(float** ptr) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return RAPT_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return RAPT_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_l2_scratch) != cudaSuccess || p == nullptr) return RAPT_ERR_CUDA;
-    g_scratch_ptr[dev] = static_cast<float*>(p);
-  }
-  *ptr = g_scratch_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_l2_scratch) != cudaSuccess || p == nullptr) return RAPT_ERR_CUDA;
+  *ptr = static_cast<float*>(p);
   return RAPT_OK;
 }
 

@@ -37,7 +37,22 @@ def _ambiguous(x, gamma, positions):
     return bad
 
 
+# Largest share of rows the ReLU-decision carve-out may take: a row needs an element within
+# 1e-5 of its largest magnitude, which for d <= 128 normal entries happens in well under 1 % of
+# rows; a wider carve-out means the mask itself went wrong (gains or positions passed to it).
+MAX_AMBIGUOUS = 0.02
+
+
+def _keep(x, gamma, positions):
+    """Rows compared element by element: all but the ambiguous ones, whose count is bounded."""
+    bad = _ambiguous(x, gamma, positions)
+    assert bad.sum() <= max(1, MAX_AMBIGUOUS * bad.size), \
+        "carve-out too wide: %d of %d rows" % (bad.sum(), bad.size)
+    return ~bad
+
+
 def _row_err(got, ref, keep):
+    assert np.isfinite(got).all()  # the rows left out of the comparison included
     return O.relative_error(got[keep], ref[keep])[0]
 
 
@@ -75,8 +90,8 @@ def test_prefill_bwd_matches_oracle(cuda_device, lib, case):
                                               pos_offset=off)
     pos = off + np.arange(L)
     for b in range(B):
-        keep_q = ~_ambiguous(wq[b], gq, pos)
-        keep_k = ~_ambiguous(wk[b], gk, pos)
+        keep_q = _keep(wq[b], gq, pos)
+        keep_k = _keep(wk[b], gk, pos)
         assert _row_err(to_host(dq)[b], rq[b], keep_q) <= TOL[dtype]
         assert _row_err(to_host(dk)[b], rk[b], keep_k) <= TOL[dtype]
         assert O.relative_error(to_host(dv)[b], rv[b])[0] <= TOL[dtype]
@@ -103,8 +118,8 @@ def test_varlen_bwd_matches_oracle(cuda_device, lib, dtype, d):
     wq, wk, wv, wg = (widen(x, dtype) for x in (q, k, v, g))
     rq, rk, rv, rgq, rgk = O.rla2_varlen_bwd(wq, wk, wv, wg, cu, gq, gk, EPS_N, BASE, EPS_D)
     pos = np.concatenate([np.arange(n) for n in lens])
-    keep_q = ~_ambiguous(wq, gq, pos)
-    keep_k = ~_ambiguous(wk, gk, pos)
+    keep_q = _keep(wq, gq, pos)
+    keep_k = _keep(wk, gk, pos)
     assert _row_err(to_host(dq), rq, keep_q) <= TOL[dtype]
     assert _row_err(to_host(dk), rk, keep_k) <= TOL[dtype]
     assert O.relative_error(to_host(dv), rv)[0] <= TOL[dtype]
@@ -130,8 +145,8 @@ def test_prefill_bwd_full_size_sampled(cuda_device, lib):
         qs, ks, vs, gs = (syn.bf16_bits_to_f64(x[b:b + 1, :, h:h + 1]) for x in (w.q, w.k, w.v, g))
         rq, rk, rv, _, _ = O.rla2_prefill_bwd(qs, ks, vs, gs, w.gamma_q[h:h + 1], w.gamma_k[h:h + 1],
                                               EPS_N, BASE, EPS_D)
-        keep_q = ~_ambiguous(qs[0], w.gamma_q[h:h + 1], pos)
-        keep_k = ~_ambiguous(ks[0], w.gamma_k[h:h + 1], pos)
+        keep_q = _keep(qs[0], w.gamma_q[h:h + 1], pos)
+        keep_k = _keep(ks[0], w.gamma_k[h:h + 1], pos)
         assert _row_err(to_host(dq[b:b + 1, :, h:h + 1])[0], rq[0], keep_q) <= TOL["bf16"]
         assert _row_err(to_host(dk[b:b + 1, :, h:h + 1])[0], rk[0], keep_k) <= TOL["bf16"]
         assert O.relative_error(to_host(dv[b:b + 1, :, h:h + 1])[0], rv[0])[0] <= TOL["bf16"]
@@ -201,7 +216,7 @@ def test_varlen_bwd_reports_malformed_cu_seqlens(cuda_device, lib, d, dtype):
     rq, rk, rv, _, _ = O.rla2_varlen_bwd(wq, wk, wv, wg, np.array([0, 200]), gq, gk, EPS_N, BASE,
                                          EPS_D)
     assert O.relative_error(to_host(dv)[:200], rv)[0] <= TOL[dtype]
-    keep_k = ~_ambiguous(wk, gk, np.arange(200))
+    keep_k = _keep(wk, gk, np.arange(200))
     assert _row_err(to_host(dk)[:200], rk, keep_k) <= TOL[dtype]
 
 
@@ -222,8 +237,8 @@ def test_prefill_bwd_tensor_cores_shared_gains_many_segments(cuda_device, lib):
                                               pos_offset=off)
     pos = off + np.arange(L)
     for b in range(B):
-        assert _row_err(to_host(dq)[b], rq[b], ~_ambiguous(wq[b], gq, pos)) <= TOL["bf16"]
-        assert _row_err(to_host(dk)[b], rk[b], ~_ambiguous(wk[b], gk, pos)) <= TOL["bf16"]
+        assert _row_err(to_host(dq)[b], rq[b], _keep(wq[b], gq, pos)) <= TOL["bf16"]
+        assert _row_err(to_host(dk)[b], rk[b], _keep(wk[b], gk, pos)) <= TOL["bf16"]
         assert O.relative_error(to_host(dv)[b], rv[b])[0] <= TOL["bf16"]
     assert _vec_err(to_host(dgq), rgq) <= TOL["bf16"]
     assert _vec_err(to_host(dgk), rgk) <= TOL["bf16"]
@@ -254,8 +269,8 @@ def test_varlen_bwd_multi_block_segments_sampled(cuda_device, lib):
         qs, ks, vs, gs = (widen(x[s:e, h:h + 1][None], "bf16") for x in (q, k, v, g))
         rq, rk, rv, _, _ = O.rla2_prefill_bwd(qs, ks, vs, gs, gq[h:h + 1], gk[h:h + 1], EPS_N, BASE,
                                               EPS_D)
-        keep_q = ~_ambiguous(qs[0], gq[h:h + 1], pos)
-        keep_k = ~_ambiguous(ks[0], gk[h:h + 1], pos)
+        keep_q = _keep(qs[0], gq[h:h + 1], pos)
+        keep_k = _keep(ks[0], gk[h:h + 1], pos)
         assert _row_err(to_host(dq[s:e, h:h + 1]), rq[0], keep_q) <= TOL["bf16"]
         assert _row_err(to_host(dk[s:e, h:h + 1]), rk[0], keep_k) <= TOL["bf16"]
         assert O.relative_error(to_host(dv[s:e, h:h + 1]), rv[0])[0] <= TOL["bf16"]
