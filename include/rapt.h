@@ -344,6 +344,70 @@ rapt_status rla_l2_fwd(const void* q, const void* k, const void* v, rapt_dtype d
                        void* workspace, size_t workspace_bytes, rapt_stream_t stream);
 
 /*
+ * One sequence split across GPUs. The RLA-2 state is a sum over tokens (08-rapt-algorithm.md §3:
+ * S_t = sum_{i<=t} k'_i v_i^T, z_t = sum_{i<=t} k'_i), which the page notes can be accumulated
+ * chunk by chunk in parallel (§1, §3). A sequence cut into W consecutive shards of L tokens, shard
+ * r on GPU r, is computed exactly as one sequence by:
+ *   1. rapt_prefill_state on every shard: its increment (dS_r, dz_r) over its own tokens;
+ *   2. an all-gather of the W increments (by the caller, e.g. NCCL; W * B * H * d * (d + 1) fp32);
+ *   3. rapt_state_prefix: shard r's initial state S0 + dS_0 + ... + dS_{r-1} (rank order);
+ *   4. rapt_prefill_fwd on shard r with that initial state and pos_offset = the global position of
+ *      its first token (RoPE positions continue across shards).
+ * The whole sequence's final state is rapt_state_prefix with r = W.
+ *
+ * rapt_prefill_state: S_inc[b, h] = sum_t k'_t v_t^T and z_inc[b, h] = sum_t k'_t over the L
+ * tokens of batch row b (token t at RoPE position pos_offset + t); k' as in rapt_prefill_fwd
+ * (gamma_k, params.eps_norm, params.rope_base, params.gamma_head_stride; eps_den unused).
+ *   k, v          [B, L, H, d] of `dtype` (may be null when L == 0: the increments are zero).
+ *   S_inc, z_inc  fp32 [B, H, d, d], [B, H, d] (written; key-major like every state).
+ *   workspace     rapt_prefill_state_workspace_size() bytes (the per-block partial sums).
+ * Precision: bf16 at d = 64 or 128 runs on the tensor cores (bf16 k' and v operands, fp32
+ * accumulation, as the prefill's own state); otherwise fp32 arithmetic. Bitwise repeatable.
+ */
+size_t rapt_prefill_state_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d,
+                                         rapt_dtype dtype);
+rapt_status rapt_prefill_state(const void* k, const void* v, rapt_dtype dtype, int32_t B,
+                               int32_t L, int32_t H, int32_t d, const float* gamma_k,
+                               rapt_params params, int32_t pos_offset, float* S_inc, float* z_inc,
+                               void* workspace, size_t workspace_bytes, rapt_stream_t stream);
+/*
+ * rapt_state_prefix: S_start = S0 + S_parts[0] + ... + S_parts[r-1] and the same for z, added in
+ * rank order (fp32; deterministic).
+ *   S_parts, z_parts  fp32 [W, B, H, d, d], [W, B, H, d]: the gathered shard increments (may be
+ *                     null when r == 0).
+ *   r                 0 <= r <= W: the number of leading shards to add.
+ *   S0, z0            nullable fp32 [B, H, d, d], [B, H, d]: the state before shard 0.
+ *   S_start, z_start  fp32 [B, H, d, d], [B, H, d] (written; must not alias the parts).
+ */
+rapt_status rapt_state_prefix(const float* S_parts, const float* z_parts, int32_t W, int32_t r,
+                              int32_t B, int32_t H, int32_t d, const float* S0, const float* z0,
+                              float* S_start, float* z_start, rapt_stream_t stream);
+
+/*
+ * The original RLA L2 path (rla_l2_fwd) in two halves, for a sequence whose L tokens are split
+ * across GPUs: the moments M_V = K'^T V and M_K = K'^T K' are sums over tokens (08-rapt-algorithm.md
+ * §2.1, §2.2), so each GPU computes its shard's moments with rla_l2_moments, the caller sums them
+ * over the GPUs (an all-reduce of B * H * d * 2d fp32), and each GPU reads out its own queries with
+ * rla_l2_readout. On one GPU, moments then readout equals rla_l2_fwd.
+ *   rla_l2_moments:  M fp32 [B, H, d, 2d] (written): row i holds (M_V[i, 0..d), M_K[i, 0..d));
+ *                    k' = ReLU(k). Workspace rla_l2_moments_workspace_size() (split partials).
+ *                    L == 0 gives zero moments.
+ *   rla_l2_readout:  out_t = q'_t M_V / (sqrt(q'_t^T M_K q'_t) + eps), q' = ReLU(q), for the L
+ *                    queries of q [B, L, H, d] and the moments M [B, H, d, 2d] (read only).
+ *                    Workspace rla_l2_readout_workspace_size() (bf16 at d = 64 or 128: the bf16
+ *                    copy of M the tensor cores read; 0 otherwise).
+ * Precision as rla_l2_fwd: fp32 moments; the tensor-core readout reads bf16 copies of them.
+ */
+size_t rla_l2_moments_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype);
+rapt_status rla_l2_moments(const void* k, const void* v, rapt_dtype dtype, int32_t B, int32_t L,
+                           int32_t H, int32_t d, float* M, void* workspace, size_t workspace_bytes,
+                           rapt_stream_t stream);
+size_t rla_l2_readout_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype);
+rapt_status rla_l2_readout(const void* q, const float* M, rapt_dtype dtype, int32_t B, int32_t L,
+                           int32_t H, int32_t d, float eps, void* out, void* workspace,
+                           size_t workspace_bytes, rapt_stream_t stream);
+
+/*
  * Allocation-free variant of rla_l2_fwd. The pages have no counterpart to this entry point: it
  * exists for callers that cannot allocate device memory at all, such as a plugin inside an
  * inference engine that owns every byte of device memory and hands the plugin only its input

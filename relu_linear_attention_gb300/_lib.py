@@ -104,6 +104,18 @@ SIGNATURES = {
     "rla_l2_fwd": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32,
                              c_int32, c_int32, c_int32, c_int32, c_float, c_void_p,
                              c_void_p, c_size_t, c_void_p]),
+    "rapt_prefill_state_workspace_size": (c_size_t, [c_int32] * 4 + [c_int32]),
+    "rapt_prefill_state": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
+                                     c_int32, c_void_p, rapt_params, c_int32, c_void_p, c_void_p,
+                                     c_void_p, c_size_t, c_void_p]),
+    "rapt_state_prefix": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32,
+                                    c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "rla_l2_moments_workspace_size": (c_size_t, [c_int32] * 4 + [c_int32]),
+    "rla_l2_moments": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32,
+                                 c_void_p, c_void_p, c_size_t, c_void_p]),
+    "rla_l2_readout_workspace_size": (c_size_t, [c_int32] * 4 + [c_int32]),
+    "rla_l2_readout": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32,
+                                 c_float, c_void_p, c_void_p, c_size_t, c_void_p]),
     "rla_l2_fwd_noalloc": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32,
                                      c_int32, c_int32, c_int32, c_int32, c_float, c_void_p,
                                      c_void_p]),

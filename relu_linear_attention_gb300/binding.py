@@ -468,3 +468,169 @@ def rla_l2_fwd(q, k, v, *, eps=1e-6, out=None, workspace=None, stream=None):
                         _ptr(workspace), ws_bytes, _stream(stream))
     _lib.check("rla_l2_fwd", st)
     return out
+
+
+# ---------------------------------------------------------------- one sequence split across GPUs
+def rapt_prefill_state(k, v, gamma_k, *, eps_norm=1e-6, rope_base=1e4, pos_offset=0, S_inc=None,
+                       z_inc=None, workspace=None, stream=None):
+    """State increment of a shard: S_inc = sum_t k'_t v_t^T, z_inc = sum_t k'_t over the L tokens of
+    every batch row of k, v [B, L, H, d] (token t at RoPE position pos_offset + t). Returns
+    (S_inc [B, H, d, d], z_inc [B, H, d]) in fp32."""
+    _need(k.dim() == 4, "k must be [B, L, H, d]")
+    B, L, H, d = k.shape
+    for name, t in (("k", k), ("v", v)):
+        _cuda_contig(name, t, k.dtype, k.shape)
+    _need(k.dtype in _DT, "dtype must be float32 or bfloat16")
+    stride = _gammas(gamma_k, gamma_k, H, d)
+    if S_inc is None:
+        S_inc = torch.empty((B, H, d, d), device=k.device, dtype=torch.float32)
+    if z_inc is None:
+        z_inc = torch.empty((B, H, d), device=k.device, dtype=torch.float32)
+    _state("S_inc", S_inc, (B, H, d, d))
+    _state("z_inc", z_inc, (B, H, d))
+    lib = _lib.load()
+    need = lib.rapt_prefill_state_workspace_size(B, L, H, d, _DT[k.dtype])
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=k.device, dtype=torch.uint8)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.rapt_prefill_state(_ptr(k), _ptr(v), _DT[k.dtype], B, L, H, d, _ptr(gamma_k),
+                                make_params(eps_norm, rope_base, 1e-4, stride), int(pos_offset),
+                                _ptr(S_inc), _ptr(z_inc), _ptr(workspace), ws_bytes,
+                                _stream(stream))
+    _lib.check("rapt_prefill_state", st)
+    return S_inc, z_inc
+
+
+def rapt_state_prefix(S_parts, z_parts, r, *, S0=None, z0=None, S_start=None, z_start=None,
+                      stream=None):
+    """S_start = S0 + S_parts[0] + ... + S_parts[r-1] (and z likewise), in rank order, for the
+    gathered shard increments S_parts [W, B, H, d, d], z_parts [W, B, H, d]."""
+    _need(S_parts.dim() == 5, "S_parts must be [W, B, H, d, d]")
+    W, B, H, d, _ = S_parts.shape
+    _cuda_contig("S_parts", S_parts, torch.float32)
+    _cuda_contig("z_parts", z_parts, torch.float32, (W, B, H, d))
+    _state("S0", S0, (B, H, d, d))
+    _state("z0", z0, (B, H, d))
+    if S_start is None:
+        S_start = torch.empty((B, H, d, d), device=S_parts.device, dtype=torch.float32)
+    if z_start is None:
+        z_start = torch.empty((B, H, d), device=S_parts.device, dtype=torch.float32)
+    _state("S_start", S_start, (B, H, d, d))
+    _state("z_start", z_start, (B, H, d))
+    st = _lib.load().rapt_state_prefix(_ptr(S_parts), _ptr(z_parts), W, int(r), B, H, d, _ptr(S0),
+                                       _ptr(z0), _ptr(S_start), _ptr(z_start), _stream(stream))
+    _lib.check("rapt_state_prefix", st)
+    return S_start, z_start
+
+
+def gather_shard_states(S_inc, z_inc, group=None):
+    """All-gathers every rank's shard increment, in rank order: returns (S_parts [W, ...],
+    z_parts [W, ...]). Without an initialised process group (or with one rank) W = 1."""
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size(group) == 1:
+        return S_inc.unsqueeze(0), z_inc.unsqueeze(0)
+    W = dist.get_world_size(group)
+    out = []
+    for t in (S_inc.contiguous(), z_inc.contiguous()):
+        # gathered along the leading axis (rank r's tensor at rows [r n, (r + 1) n)), then viewed
+        # as [W, ...]
+        g = torch.empty((W * t.shape[0],) + tuple(t.shape[1:]), dtype=t.dtype, device=t.device)
+        dist.all_gather_into_tensor(g, t, group=group)
+        out.append(g.view((W,) + tuple(t.shape)))
+    return out[0], out[1]
+
+
+def shard_rank(group=None):
+    """(rank, world size) of this process in ``group`` ((0, 1) without a process group)."""
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return 0, 1
+    return dist.get_rank(group), dist.get_world_size(group)
+
+
+def rapt_prefill_fwd_sharded(q, k, v, gamma_q, gamma_k, *, group=None, eps_norm=1e-6,
+                             rope_base=1e4, eps_den=1e-4, pos_offset=0, S0=None, z0=None,
+                             out=None, final_state=False, stream=None):
+    """Causal RLA-2 prefill of sequences split across the ranks of ``group``: rank r holds tokens
+    [r L, (r + 1) L) of every batch row in q, k, v [B, L, H, d] (equal L on every rank; pos_offset
+    is the position of rank 0's first token). One all-gather of the shard states is the only
+    exchange. Returns (out, S_final, z_final) with the final state of the whole sequence when
+    requested (the same on every rank)."""
+    r, W = shard_rank(group)
+    B, L, H, d = q.shape
+    first = int(pos_offset) + r * L
+    S_inc, z_inc = rapt_prefill_state(k, v, gamma_k, eps_norm=eps_norm, rope_base=rope_base,
+                                      pos_offset=first, stream=stream)
+    S_parts, z_parts = gather_shard_states(S_inc, z_inc, group)
+    S_start, z_start = rapt_state_prefix(S_parts, z_parts, r, S0=S0, z0=z0, stream=stream)
+    out, _, _ = rapt_prefill_fwd(q, k, v, gamma_q, gamma_k, eps_norm=eps_norm, rope_base=rope_base,
+                                 eps_den=eps_den, pos_offset=first, S0=S_start, z0=z_start, out=out,
+                                 stream=stream)
+    S_fin = z_fin = None
+    if final_state:
+        S_fin, z_fin = rapt_state_prefix(S_parts, z_parts, W, S0=S0, z0=z0, stream=stream)
+    return out, S_fin, z_fin
+
+
+def rla_l2_moments(k, v, *, M=None, workspace=None, stream=None):
+    """The moments [M_V | M_K] = K'^T [V | K'] (k' = ReLU(k)) over the L tokens of k, v
+    [B, L, H, d]: fp32 [B, H, d, 2d]."""
+    _need(k.dim() == 4, "k must be [B, L, H, d]")
+    B, L, H, d = k.shape
+    for name, t in (("k", k), ("v", v)):
+        _cuda_contig(name, t, k.dtype, k.shape)
+    _need(k.dtype in _DT, "dtype must be float32 or bfloat16")
+    if M is None:
+        M = torch.empty((B, H, d, 2 * d), device=k.device, dtype=torch.float32)
+    _state("M", M, (B, H, d, 2 * d))
+    lib = _lib.load()
+    need = lib.rla_l2_moments_workspace_size(B, L, H, d, _DT[k.dtype])
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=k.device, dtype=torch.uint8)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.rla_l2_moments(_ptr(k), _ptr(v), _DT[k.dtype], B, L, H, d, _ptr(M), _ptr(workspace),
+                            ws_bytes, _stream(stream))
+    _lib.check("rla_l2_moments", st)
+    return M
+
+
+def rla_l2_readout(q, M, *, eps=1e-6, out=None, workspace=None, stream=None):
+    """out = q'M_V / (sqrt(q'^T M_K q') + eps), q' = ReLU(q), for q [B, L, H, d] and the moments
+    M [B, H, d, 2d] (fp32)."""
+    _need(q.dim() == 4, "q must be [B, L, H, d]")
+    B, L, H, d = q.shape
+    _cuda_contig("q", q, None, None)
+    _need(q.dtype in _DT, "dtype must be float32 or bfloat16")
+    _state("M", M, (B, H, d, 2 * d))
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, q.dtype, q.shape)
+    lib = _lib.load()
+    need = lib.rla_l2_readout_workspace_size(B, L, H, d, _DT[q.dtype])
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.rla_l2_readout(_ptr(q), _ptr(M), _DT[q.dtype], B, L, H, d, float(eps), _ptr(out),
+                            _ptr(workspace), ws_bytes, _stream(stream))
+    _lib.check("rla_l2_readout", st)
+    return out
+
+
+def allreduce_moments(M, group=None):
+    """Sums the moments over the ranks of ``group`` in place (the identity without one)."""
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size(group) > 1:
+        dist.all_reduce(M, op=dist.ReduceOp.SUM, group=group)
+    return M
+
+
+def rla_l2_fwd_sharded(q, k, v, *, group=None, eps=1e-6, out=None, stream=None):
+    """Non-causal L2 of sequences whose tokens are split across the ranks of ``group`` (rank r
+    holds its own tokens of q, k, v [B, L, H, d]): the moments of every shard are summed by one
+    all-reduce, then every rank reads out its own queries. Returns out for this rank's tokens."""
+    M = rla_l2_moments(k, v, stream=stream)
+    allreduce_moments(M, group)
+    return rla_l2_readout(q, M, eps=eps, out=out, stream=stream)

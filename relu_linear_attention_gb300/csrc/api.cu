@@ -725,4 +725,121 @@ rapt_status rla_l2_fwd(const void* q, const void* k, const void* v, rapt_dtype d
   return from_cuda(rapt::launch_rla_l2(to_dt(dtype), d, a, st));
 }
 
+// ---- one sequence split across GPUs: shard state, start state, and the L2 path in two halves
+
+size_t rapt_prefill_state_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d,
+                                         rapt_dtype dtype) {
+  if (!known_dtype(dtype) || !supported_d(d) || B < 1 || H < 1 || L < 0) return 0;
+  return rapt::shard_state_plan(to_dt(dtype), B, L, H, d).ws_bytes;
+}
+
+rapt_status rapt_prefill_state(const void* k, const void* v, rapt_dtype dtype, int32_t B,
+                               int32_t L, int32_t H, int32_t d, const float* gamma_k,
+                               rapt_params params, int32_t pos_offset, float* S_inc, float* z_inc,
+                               void* workspace, size_t workspace_bytes, rapt_stream_t stream) {
+  if (!known_dtype(dtype) || !supported_d(d)) return RAPT_ERR_UNSUPPORTED;
+  if (B < 1 || H < 1 || L < 0 || pos_offset < 0) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(B) * L * H * d)) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(pos_offset) + L)) return RAPT_ERR_INVALID_ARG;
+  if (S_inc == nullptr || z_inc == nullptr || !aligned16(S_inc) || !aligned16(z_inc))
+    return RAPT_ERR_INVALID_ARG;
+  if (L > 0 && (k == nullptr || v == nullptr || !aligned16(k) || !aligned16(v)))
+    return RAPT_ERR_INVALID_ARG;
+  rapt_status st = check_features(gamma_k, gamma_k, params, d);
+  if (st != RAPT_OK) return st;
+  const size_t need = rapt_prefill_state_workspace_size(B, L, H, d, dtype);
+  if (workspace_bytes < need || workspace == nullptr || !aligned16(workspace))
+    return RAPT_ERR_WORKSPACE;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const long n_bh = static_cast<long>(B) * H;
+  if (L == 0) {  // an empty shard adds nothing: zero increments
+    cudaError_t e = rapt::launch_state_prefix(nullptr, n_bh * d * d, 0, nullptr, S_inc, s);
+    if (e == cudaSuccess) e = rapt::launch_state_prefix(nullptr, n_bh * d, 0, nullptr, z_inc, s);
+    return from_cuda(e);
+  }
+  rapt::PrefillArgs a{};
+  a.k = k; a.v = v;
+  a.gamma_q = gamma_k; a.gamma_k = gamma_k;
+  a.n_docs = B; a.doc_len = L; a.total_rows = B * L; a.max_seqlen = L;
+  a.H = H; a.pos_offset = pos_offset; a.eps_den = params.eps_den;
+  a.fa = make_features(params, d);
+  const rapt::ShardPlan plan = rapt::shard_state_plan(to_dt(dtype), B, L, H, d);
+  return from_cuda(rapt::launch_shard_state(to_dt(dtype), d, a, plan,
+                                            static_cast<float*>(workspace), S_inc, z_inc, s));
+}
+
+rapt_status rapt_state_prefix(const float* S_parts, const float* z_parts, int32_t W, int32_t r,
+                              int32_t B, int32_t H, int32_t d, const float* S0, const float* z0,
+                              float* S_start, float* z_start, rapt_stream_t stream) {
+  if (!supported_d(d)) return RAPT_ERR_UNSUPPORTED;
+  if (B < 1 || H < 1 || W < 1 || r < 0 || r > W) return RAPT_ERR_INVALID_ARG;
+  if (S_start == nullptr || z_start == nullptr || !aligned16(S_start) || !aligned16(z_start))
+    return RAPT_ERR_INVALID_ARG;
+  if (r > 0 && (S_parts == nullptr || z_parts == nullptr)) return RAPT_ERR_INVALID_ARG;
+  if (!opt_aligned16(S_parts) || !opt_aligned16(z_parts) || !opt_aligned16(S0) || !opt_aligned16(z0))
+    return RAPT_ERR_INVALID_ARG;
+  if (S_start == S_parts || z_start == z_parts) return RAPT_ERR_INVALID_ARG;
+  const long n_bh = static_cast<long>(B) * H;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = rapt::launch_state_prefix(S_parts, n_bh * d * d, r, S0, S_start, s);
+  if (e == cudaSuccess) e = rapt::launch_state_prefix(z_parts, n_bh * d, r, z0, z_start, s);
+  return from_cuda(e);
+}
+
+size_t rla_l2_moments_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype) {
+  if (B < 1 || L < 0 || H < 1 || !supported_d(d) || !known_dtype(dtype)) return 0;
+  if (rapt::l2_tc_supported(to_dt(dtype), d)) return rapt::l2_tc_moments_ws_bytes(B, L, H, d);
+  return rapt::l2_moments_ws_bytes(B, L, H, d);
+}
+
+rapt_status rla_l2_moments(const void* k, const void* v, rapt_dtype dtype, int32_t B, int32_t L,
+                           int32_t H, int32_t d, float* M, void* workspace, size_t workspace_bytes,
+                           rapt_stream_t stream) {
+  if (!known_dtype(dtype) || !supported_d(d)) return RAPT_ERR_UNSUPPORTED;
+  if (B < 1 || H < 1 || L < 0) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(B) * L * H * d)) return RAPT_ERR_INVALID_ARG;
+  if (M == nullptr || !aligned16(M)) return RAPT_ERR_INVALID_ARG;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const long n_mat = static_cast<long>(B) * H * d * 2 * d;
+  if (L == 0) return from_cuda(rapt::launch_state_prefix(nullptr, n_mat, 0, nullptr, M, s));
+  if (k == nullptr || v == nullptr || !aligned16(k) || !aligned16(v)) return RAPT_ERR_INVALID_ARG;
+  const size_t need = rla_l2_moments_workspace_size(B, L, H, d, dtype);
+  if (workspace_bytes < need || workspace == nullptr || !aligned16(workspace))
+    return RAPT_ERR_WORKSPACE;
+  rapt::L2Args a{};
+  a.k = k; a.v = v;
+  a.ws = static_cast<float*>(workspace);
+  a.B = B; a.L = L; a.H = H; a.eps = 1.f;
+  if (rapt::l2_tc_supported(to_dt(dtype), d)) return from_cuda(rapt::launch_l2_tc_moments_plain(d, a, M, s));
+  return from_cuda(rapt::launch_l2_moments_plain(to_dt(dtype), d, a, M, s));
+}
+
+size_t rla_l2_readout_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype) {
+  if (B < 1 || L < 0 || H < 1 || !supported_d(d) || !known_dtype(dtype)) return 0;
+  if (rapt::l2_tc_supported(to_dt(dtype), d)) return rapt::l2_tc_readout_ws_bytes(B, H, d);
+  return 0;
+}
+
+rapt_status rla_l2_readout(const void* q, const float* M, rapt_dtype dtype, int32_t B, int32_t L,
+                           int32_t H, int32_t d, float eps, void* out, void* workspace,
+                           size_t workspace_bytes, rapt_stream_t stream) {
+  if (!known_dtype(dtype) || !supported_d(d)) return RAPT_ERR_UNSUPPORTED;
+  if (B < 1 || H < 1 || L < 0) return RAPT_ERR_INVALID_ARG;
+  if (!fits_i32(static_cast<long long>(B) * L * H * d)) return RAPT_ERR_INVALID_ARG;
+  if (!finite_pos(eps)) return RAPT_ERR_INVALID_ARG;
+  if (L == 0) return RAPT_OK;
+  if (q == nullptr || M == nullptr || out == nullptr) return RAPT_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(M) || !aligned16(out) || out == q) return RAPT_ERR_INVALID_ARG;
+  const size_t need = rla_l2_readout_workspace_size(B, L, H, d, dtype);
+  if (workspace_bytes < need || (need > 0 && workspace == nullptr) || !opt_aligned16(workspace))
+    return RAPT_ERR_WORKSPACE;
+  rapt::L2Args a{};
+  a.q = q; a.out = out;
+  a.ws = static_cast<float*>(workspace);
+  a.B = B; a.L = L; a.H = H; a.eps = eps;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (rapt::l2_tc_supported(to_dt(dtype), d)) return from_cuda(rapt::launch_l2_tc_readout_plain(d, a, M, s));
+  return from_cuda(rapt::launch_l2_readout_plain(to_dt(dtype), d, a, M, s));
+}
+
 }  // extern "C"

@@ -225,6 +225,38 @@ bool l2_tc_supported(DType dt, int d);
 size_t l2_tc_workspace_bytes(int B, int L, int H, int d);
 cudaError_t launch_rla_l2_tc(int d, const L2Args& a, cudaStream_t stream);
 
+// The L2 path in two halves, for a sequence whose tokens are split across GPUs (the moments
+// are sums over tokens, so the shards' moments add up): the moments [M_V | M_K] as plain fp32
+// (row i, column j at i * 2d + j, per (batch row, head)), and the readout from such moments.
+// CUDA-core path: moments workspace l2_moments_ws_bytes(), readout none.
+size_t l2_moments_ws_bytes(int B, int L, int H, int d);
+cudaError_t launch_l2_moments_plain(DType dt, int d, const L2Args& a, float* M, cudaStream_t stream);
+cudaError_t launch_l2_readout_plain(DType dt, int d, const L2Args& a, const float* M, cudaStream_t stream);
+// Tensor-core path (bf16, d in {64, 128}): workspaces l2_tc_moments_ws_bytes() (split partials)
+// and l2_tc_readout_ws_bytes() (the bf16 operand image).
+size_t l2_tc_moments_ws_bytes(int B, int L, int H, int d);
+size_t l2_tc_readout_ws_bytes(int B, int H, int d);
+cudaError_t launch_l2_tc_moments_plain(int d, const L2Args& a, float* M, cudaStream_t stream);
+cudaError_t launch_l2_tc_readout_plain(int d, const L2Args& a, const float* M, cudaStream_t stream);
+
+// One sequence split into consecutive shards (one per GPU): the state increment of a shard
+// (sum of k' v^T and of k' over its tokens, per (batch row, head)), in blocks of blk_len tokens
+// whose records (ws_bytes of workspace, the tensor-core state kernel's layout) are summed in
+// block order into plain S [bh][d][d] and z [bh][d].
+struct ShardPlan {
+  bool tc;
+  int blk_len;
+  int nblk;
+  size_t ws_bytes;
+};
+ShardPlan shard_state_plan(DType dt, int B, int L, int H, int d);
+cudaError_t launch_shard_state(DType dt, int d, const PrefillArgs& a, const ShardPlan& p, float* ws,
+                               float* S, float* z, cudaStream_t stream);
+// out[i] = init[i] (0 if null) + parts[0][i] + ... + parts[r-1][i] over n floats (n % 4 == 0),
+// parts holding consecutive arrays of n floats, added in rank order.
+cudaError_t launch_state_prefix(const float* parts, long n, int r, const float* init, float* out,
+                                cudaStream_t stream);
+
 int l2_default_splits(int B, int L, int H);
 size_t l2_workspace_bytes_for_splits(int B, int H, int d, int nsplit);
 cudaError_t launch_rla_l2_with_splits(DType dt, int d, const L2Args& a, int nsplit,

@@ -248,6 +248,43 @@ __global__ void __launch_bounds__(256) l2_tc_reduce(const float* ws, int nsplit,
   }
 }
 
+// The split partials of one (batch row, head), summed in split order, as the plain fp32
+// [M_V | M_K] (row i, column j at i * 2D + j) of the moments-only entry point.
+template <int D>
+__global__ void __launch_bounds__(256) l2_tc_plain(const float* ws, int nsplit, float* M) {
+  constexpr int N = 2 * D;
+  constexpr int Q = D * N / 4;
+  const int bh = blockIdx.y;
+  const float4* p = reinterpret_cast<const float4*>(ws) + static_cast<long>(bh) * nsplit * Q;
+  for (int e = blockIdx.x * 256 + threadIdx.x; e < Q; e += gridDim.x * 256) {
+    float4 m = __ldcg(p + e);
+    for (int s = 1; s < nsplit; ++s) {
+      const float4 x = __ldcg(p + static_cast<long>(s) * Q + e);
+      m.x += x.x; m.y += x.y; m.z += x.z; m.w += x.w;
+    }
+    const int i = e % D, j = 4 * (e / D);
+    *reinterpret_cast<float4*>(M + (static_cast<long>(bh) * D + i) * N + j) = m;
+  }
+}
+
+// The plain fp32 [M_V | M_K] of the readout-only entry point as the bf16 B operand image of the
+// readout GEMM (the layout l2_tc_reduce writes).
+template <int D>
+__global__ void __launch_bounds__(256) l2_tc_image(const float* M, uint8_t* img_all) {
+  constexpr int N = 2 * D;
+  constexpr int Q = D * N / 4;
+  const int bh = blockIdx.y;
+  tc::grid_launch_dependents();  // the readout may set up and load its first q tiles
+  uint8_t* img = img_all + static_cast<long>(bh) * D * N * 2;
+  for (int e = blockIdx.x * 256 + threadIdx.x; e < Q; e += gridDim.x * 256) {
+    const int i = e / (N / 4), j = 4 * (e % (N / 4));
+    const float4 m = __ldg(reinterpret_cast<const float4*>(M + (static_cast<long>(bh) * D + i) * N + j));
+    const int jb = j / 64, cc = (j % 64) / 8, half = (j % 8) / 4;
+    const uint2 w = make_uint2(tc::pack_bf16x2(m.x, m.y), tc::pack_bf16x2(m.z, m.w));
+    *reinterpret_cast<uint2*>(img + jb * (D * 128) + i * 128 + ((cc ^ (i & 7)) << 4) + half * 8) = w;
+  }
+}
+
 // ------------------------------------------------------------------------------------------------
 // Launch 3: readout. Shared memory: the [M_V | M_K] image, kStages q tiles (each 128 tokens x d,
 // K-major blocks of 64 columns; out is written over the tile q' was read from), and the partial
@@ -571,6 +608,82 @@ cudaError_t launch_l2_moments_tc(const L2Args& a, int nsplit, int split_len, cud
 
 cudaError_t launch_rla_l2_tc(int d, const L2Args& a, cudaStream_t stream) {
   return d == 128 ? launch_l2_tc_d<128>(a, stream) : launch_l2_tc_d<64>(a, stream);
+}
+
+namespace {
+template <int D>
+cudaError_t launch_moments_plain_d(const L2Args& a, float* M, cudaStream_t stream) {
+  static unsigned long long cfg1 = 0;
+  cudaError_t e = set_smem(l2_tc_moments<D>, P1<D>::BYTES, cfg1);
+  if (e != cudaSuccess) return e;
+  const long n_bh = static_cast<long>(a.B) * a.H;
+  if (n_bh == 0 || a.L == 0) return cudaSuccess;
+  CUtensorMap tk, tv;
+  e = make_bshd_map(&tk, a.k, a.B, a.L, a.H, D);
+  if (e == cudaSuccess) e = make_bshd_map(&tv, a.v, a.B, a.L, a.H, D);
+  if (e != cudaSuccess) return e;
+  const int tiles = (a.L + kC - 1) / kC;
+  const int nsplit = l2_tc_splits(a.B, a.L, a.H);
+  const int split_chunks = (tiles + nsplit - 1) / nsplit;
+  l2_tc_moments<D><<<static_cast<unsigned>(n_bh * nsplit), kP1Threads, P1<D>::BYTES, stream>>>(
+      a, nsplit, split_chunks * kC, tk, tv);
+  note_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int q4 = D * 2 * D / 4;
+  l2_tc_plain<D><<<dim3(static_cast<unsigned>((q4 + 255) / 256), static_cast<unsigned>(n_bh)), 256, 0,
+                   stream>>>(a.ws, nsplit, M);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_readout_plain_d(const L2Args& a, const float* M, cudaStream_t stream) {
+  static unsigned long long cfg2 = 0;
+  cudaError_t e = set_smem(l2_tc_readout<D>, P2<D>::BYTES, cfg2);
+  if (e != cudaSuccess) return e;
+  const long n_bh = static_cast<long>(a.B) * a.H;
+  if (n_bh == 0 || a.L == 0) return cudaSuccess;
+  CUtensorMap tq, to;
+  e = make_bshd_map(&tq, a.q, a.B, a.L, a.H, D);
+  if (e == cudaSuccess) e = make_bshd_map(&to, a.out, a.B, a.L, a.H, D);
+  if (e != cudaSuccess) return e;
+  const int tiles = (a.L + kC - 1) / kC;
+  const int nsplit = l2_tc_splits(a.B, a.L, a.H);
+  const int split_chunks = (tiles + nsplit - 1) / nsplit;
+  const int q4 = D * 2 * D / 4;
+  l2_tc_image<D><<<dim3(static_cast<unsigned>((q4 + 255) / 256), static_cast<unsigned>(n_bh)), 256, 0,
+                   stream>>>(M, reinterpret_cast<uint8_t*>(a.ws));
+  note_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // the readout is a programmatic dependent of the image launch (set-up and q tiles overlap it)
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(n_bh * nsplit));
+  cfg.blockDim = dim3(kP2Threads);
+  cfg.dynamicSmemBytes = P2<D>::BYTES;
+  e = cudaLaunchKernelEx(&cfg, l2_tc_readout<D>, a, nsplit, split_chunks, 0L, tq, to);
+  note_launches(1);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+}  // namespace
+
+size_t l2_tc_moments_ws_bytes(int B, int L, int H, int d) {
+  return static_cast<size_t>(B) * H * l2_tc_splits(B, L, H) * d * 2 * d * sizeof(float);
+}
+size_t l2_tc_readout_ws_bytes(int B, int H, int d) {
+  return static_cast<size_t>(B) * H * d * 2 * d * 2;
+}
+cudaError_t launch_l2_tc_moments_plain(int d, const L2Args& a, float* M, cudaStream_t stream) {
+  return d == 128 ? launch_moments_plain_d<128>(a, M, stream) : launch_moments_plain_d<64>(a, M, stream);
+}
+cudaError_t launch_l2_tc_readout_plain(int d, const L2Args& a, const float* M, cudaStream_t stream) {
+  return d == 128 ? launch_readout_plain_d<128>(a, M, stream) : launch_readout_plain_d<64>(a, M, stream);
 }
 
 }  // namespace rapt

@@ -111,8 +111,8 @@ __global__ void __launch_bounds__(kThreads) l2_moments_kernel(const L2Args a, in
 }
 
 // M[bh] = sum over splits (in order) of the partials.
-__global__ void __launch_bounds__(kThreads) l2_reduce_kernel(float* ws, long n_bh, int nsplit, int mat4) {
-  float* M = ws + n_bh * nsplit * static_cast<long>(mat4) * 4;
+__global__ void __launch_bounds__(kThreads) l2_reduce_kernel(const float* ws, long n_bh, int nsplit,
+                                                             int mat4, float* M) {
   const long total = n_bh * mat4;
   for (long idx = blockIdx.x * static_cast<long>(kThreads) + threadIdx.x; idx < total;
        idx += static_cast<long>(gridDim.x) * kThreads) {
@@ -210,7 +210,8 @@ cudaError_t launch_t(const L2Args& a, cudaStream_t stream) {
   const long red_total = n_bh * mat4;
   long red_grid = (red_total + kThreads - 1) / kThreads;
   if (red_grid > 152L * 16) red_grid = 152L * 16;
-  l2_reduce_kernel<<<static_cast<unsigned>(red_grid), kThreads, 0, stream>>>(a.ws, n_bh, nsplit, mat4);
+  l2_reduce_kernel<<<static_cast<unsigned>(red_grid), kThreads, 0, stream>>>(
+      a.ws, n_bh, nsplit, mat4, a.ws + n_bh * nsplit * static_cast<long>(mat4) * 4);
   note_launches(1);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -259,7 +260,8 @@ cudaError_t launch_t_splits(const L2Args& a, int nsplit, cudaStream_t stream) {
   const long red_total = n_bh * mat4;
   long red_grid = (red_total + kThreads - 1) / kThreads;
   if (red_grid > 152L * 16) red_grid = 152L * 16;
-  l2_reduce_kernel<<<static_cast<unsigned>(red_grid), kThreads, 0, stream>>>(a.ws, n_bh, nsplit, mat4);
+  l2_reduce_kernel<<<static_cast<unsigned>(red_grid), kThreads, 0, stream>>>(
+      a.ws, n_bh, nsplit, mat4, a.ws + n_bh * nsplit * static_cast<long>(mat4) * 4);
   note_launches(1);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -288,7 +290,68 @@ cudaError_t launch_d_splits(int d, const L2Args& a, int nsplit, cudaStream_t str
   }
 }
 
+// The moments only: partials into a.ws, then their sum into M (plain [bh][D][2D] fp32).
+template <typename T, int D>
+cudaError_t launch_moments_plain_t(const L2Args& a, float* M, cudaStream_t stream) {
+  const int nsplit = l2_nsplit(a.B, a.L, a.H);
+  const int split_len = l2_split_len(a.L, nsplit);
+  const long n_bh = static_cast<long>(a.B) * a.H;
+  const int mat4 = D * 2 * D / 4;
+  if (n_bh == 0 || a.L == 0) return cudaSuccess;
+  l2_moments_kernel<T, D><<<dim3(nsplit, static_cast<unsigned>(n_bh)), kThreads, 0, stream>>>(a, nsplit, split_len);
+  note_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long red_total = n_bh * mat4;
+  long red_grid = (red_total + kThreads - 1) / kThreads;
+  if (red_grid > 152L * 16) red_grid = 152L * 16;
+  l2_reduce_kernel<<<static_cast<unsigned>(red_grid), kThreads, 0, stream>>>(a.ws, n_bh, nsplit, mat4, M);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+// The readout only, from the plain moments M (the same layout).
+template <typename T, int D>
+cudaError_t launch_readout_plain_t(const L2Args& a, const float* M, cudaStream_t stream) {
+  const long n_bh = static_cast<long>(a.B) * a.H;
+  if (n_bh == 0 || a.L == 0) return cudaSuccess;
+  constexpr size_t smem = OutSmem<D>::bytes;
+  cudaError_t e = cudaFuncSetAttribute(l2_out_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  L2Args b = a;
+  b.ws = const_cast<float*>(M);  // read only
+  const unsigned tiles = static_cast<unsigned>((a.L + kOutTile - 1) / kOutTile);
+  l2_out_kernel<T, D><<<dim3(tiles, static_cast<unsigned>(n_bh)), kThreads, smem, stream>>>(b, 0L);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_plain_d(int d, const L2Args& a, float* Mout, const float* Min, cudaStream_t s) {
+  const bool mom = Mout != nullptr;
+  switch (d) {
+    case 16: return mom ? launch_moments_plain_t<T, 16>(a, Mout, s) : launch_readout_plain_t<T, 16>(a, Min, s);
+    case 32: return mom ? launch_moments_plain_t<T, 32>(a, Mout, s) : launch_readout_plain_t<T, 32>(a, Min, s);
+    case 64: return mom ? launch_moments_plain_t<T, 64>(a, Mout, s) : launch_readout_plain_t<T, 64>(a, Min, s);
+    case 128: return mom ? launch_moments_plain_t<T, 128>(a, Mout, s) : launch_readout_plain_t<T, 128>(a, Min, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace
+
+size_t l2_moments_ws_bytes(int B, int L, int H, int d) {
+  return static_cast<size_t>(B) * H * l2_nsplit(B, L, H) * d * 2 * d * sizeof(float);
+}
+cudaError_t launch_l2_moments_plain(DType dt, int d, const L2Args& a, float* M, cudaStream_t stream) {
+  return dt == DType::F32 ? launch_plain_d<float>(d, a, M, nullptr, stream)
+                          : launch_plain_d<__nv_bfloat16>(d, a, M, nullptr, stream);
+}
+cudaError_t launch_l2_readout_plain(DType dt, int d, const L2Args& a, const float* M, cudaStream_t stream) {
+  return dt == DType::F32 ? launch_plain_d<float>(d, a, nullptr, M, stream)
+                          : launch_plain_d<__nv_bfloat16>(d, a, nullptr, M, stream);
+}
 
 int l2_default_splits(int B, int L, int H) { return l2_nsplit(B, L, H); }
 

@@ -197,3 +197,53 @@ def test_bidir_rejects_bad_arguments(lib):
     assert lib.rapt_bidir_workspace_size(4, 4096, 16, 128, 1) > 0
     assert lib.rapt_bidir_workspace_size(4, 4096, 16, 128, 0) == 0  # fp32: CUDA-core path
     assert lib.rapt_bidir_varlen_workspace_size(65536, 17, 32, 64, 8192, 1) > 0
+
+
+def test_shard_entry_points_reject_bad_arguments(lib):
+    S = ctypes.c_void_p(0x7F0000003000)
+    z = ctypes.c_void_p(0x7F0000004000)
+
+    def state(**kw):
+        a = dict(k=FAKE, B=2, L=256, d=128, dt=1, off=0, p=_params(), S=S, z=z, ws=FAKE, wsb=16)
+        a.update(kw)
+        return lib.rapt_prefill_state(a["k"], FAKE, a["dt"], a["B"], a["L"], 2, a["d"], FAKE,
+                                      a["p"], a["off"], a["S"], a["z"], a["ws"], a["wsb"], None)
+
+    assert state(d=48) == _lib.RAPT_ERR_UNSUPPORTED
+    assert state(B=0) == _lib.RAPT_ERR_INVALID_ARG
+    assert state(off=-1) == _lib.RAPT_ERR_INVALID_ARG
+    assert state(S=None) == _lib.RAPT_ERR_INVALID_ARG
+    assert state(z=FAKE_ODD) == _lib.RAPT_ERR_INVALID_ARG
+    assert state(k=None) == _lib.RAPT_ERR_INVALID_ARG
+    assert state(p=_params(eps_norm=-1.0)) == _lib.RAPT_ERR_INVALID_ARG
+    assert state() == _lib.RAPT_ERR_WORKSPACE
+    assert lib.rapt_prefill_state_workspace_size(2, 256, 2, 128, 1) >= 2 * 2 * 128 * 129 * 4
+    assert lib.rapt_prefill_state_workspace_size(2, 256, 2, 48, 1) == 0
+
+    def prefix(**kw):
+        a = dict(W=4, r=2, d=64, out=S)
+        a.update(kw)
+        return lib.rapt_state_prefix(FAKE, FAKE_ODD if kw.get("odd") else FAKE, a["W"], a["r"], 2, 2,
+                                     a["d"], None, None, a["out"], z, None)
+
+    assert prefix(r=5) == _lib.RAPT_ERR_INVALID_ARG
+    assert prefix(r=-1) == _lib.RAPT_ERR_INVALID_ARG
+    assert prefix(W=0) == _lib.RAPT_ERR_INVALID_ARG
+    assert prefix(d=40) == _lib.RAPT_ERR_UNSUPPORTED
+    assert prefix(out=FAKE) == _lib.RAPT_ERR_INVALID_ARG  # aliases the parts
+    assert prefix(odd=True) == _lib.RAPT_ERR_INVALID_ARG
+
+    out = ctypes.c_void_p(0x7F0000002000)
+    assert lib.rla_l2_moments(FAKE, FAKE, 1, 1, 64, 2, 128, None, FAKE, 1 << 40, None) == \
+        _lib.RAPT_ERR_INVALID_ARG
+    assert lib.rla_l2_moments(FAKE, FAKE, 1, 1, 64, 2, 128, S, FAKE, 16, None) == \
+        _lib.RAPT_ERR_WORKSPACE
+    assert lib.rla_l2_moments(FAKE, FAKE, 1, 1, 64, 2, 24, S, FAKE, 1 << 40, None) == \
+        _lib.RAPT_ERR_UNSUPPORTED
+    assert lib.rla_l2_readout(FAKE, S, 1, 1, 64, 2, 128, 0.0, out, FAKE, 1 << 40, None) == \
+        _lib.RAPT_ERR_INVALID_ARG
+    assert lib.rla_l2_readout(FAKE, S, 1, 1, 64, 2, 128, 1e-6, out, None, 0, None) == \
+        _lib.RAPT_ERR_WORKSPACE
+    assert lib.rla_l2_readout(FAKE, S, 1, 1, 0, 2, 128, 1e-6, out, None, 0, None) == _lib.RAPT_OK
+    assert lib.rla_l2_readout_workspace_size(1, 64, 2, 128, 1) == 2 * 128 * 256 * 2
+    assert lib.rla_l2_readout_workspace_size(1, 64, 2, 128, 0) == 0
