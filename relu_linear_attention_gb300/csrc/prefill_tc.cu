@@ -67,19 +67,21 @@ using namespace feat;
 
 constexpr int kC = 128;          // chunk length = MMA M
 constexpr int kProd = 512;       // producer threads (16 warps)
-constexpr int kCons = 128;       // consumer threads of kernel B (4 warps)
-constexpr int kThreadsB = kProd + kCons + 128;  // + issuer warpgroup
+constexpr int kConv = 256;       // converter threads of kernel B (8 warps, two per TMEM lane quarter)
+constexpr int kHelp = 64;        // z helper threads of kernel B (2 warps)
+constexpr int kThreadsB = kProd + kConv + 128;  // + issuer, store and z helper warps
+constexpr int kWarpIssue = (kProd + kConv) / 32;  // kernel B's MMA issuer warp
+constexpr int kWarpStore = kWarpIssue + 1;        // kernel B's TMA store / v load warp
 constexpr int kThreadsA = kProd + 128;          // kernel A: producers + issuer warpgroup
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s: a tensor-core step that is not done by then never will be
 constexpr uint32_t kDevInternal = 2u;
-constexpr uint32_t kBarProd = 1, kBarCons = 2;   // named barriers of the producer / consumer groups
-constexpr uint32_t kBarInit = 3;                 // consumer + issuer warpgroups after the state set-up
-constexpr uint32_t kBarHelp = 4;                 // the two z helper warps of the issuer warpgroup
-constexpr int kHelp = 64;                        // z helper threads
+constexpr uint32_t kBarProd = 1, kBarConv = 2;   // named barriers of the producer / converter groups
+constexpr uint32_t kBarHelp = 4;                 // the two z helper warps
+constexpr uint32_t kBarQuarter = 5;              // 5..8: the two converter warps of a lane quarter
 
 // Register splits (setmaxnreg draws on the launch allocation: threads x launch registers).
-constexpr int kLaunchRegsB = 80, kRegsProdB = 88, kRegsConsB = 64, kRegsIssueB = 64;
-static_assert(kProd * kRegsProdB + kCons * kRegsConsB + 128 * kRegsIssueB <= kThreadsB * kLaunchRegsB,
+constexpr int kLaunchRegsB = 72, kRegsProdB = 80, kRegsConvB = 64, kRegsIssueB = 56;
+static_assert(kProd * kRegsProdB + kConv * kRegsConvB + 128 * kRegsIssueB <= kThreadsB * kLaunchRegsB,
               "kernel B register split exceeds the launch allocation");
 constexpr int kLaunchRegsA = 96, kRegsProdA = 96, kRegsIssueA = 96;
 static_assert(kProd * kRegsProdA + 128 * kRegsIssueA <= kThreadsA * kLaunchRegsA,
@@ -92,7 +94,6 @@ struct Prod {
   static constexpr int TPR = D / 8;          // threads per row
   static constexpr int RPP = kProd / TPR;    // rows per pass
   static constexpr int NPASS = kC / RPP;     // passes per chunk
-  static constexpr int RING = 2 < NPASS ? 2 : NPASS;  // passes of q / k loads in flight
   static constexpr int WARPS = kProd / 32;
   static constexpr uint32_t TILE = (D / 64) * 16384;  // one 128-row bf16 tile of d columns
 };
@@ -101,21 +102,23 @@ struct Prod {
 template <int D>
 struct LayB {
   static constexpr uint32_t TILE = Prod<D>::TILE;
-  static constexpr uint32_t Q0 = 0, Q1 = TILE;                 // q' (P~ reuses them at d = 128)
-  static constexpr uint32_t V0 = 2 * TILE, V1 = 3 * TILE;      // v
+  static constexpr uint32_t Q0 = 0, Q1 = TILE;                 // raw q (TMA), turned into q' in place
+  static constexpr uint32_t V0 = 2 * TILE, V1 = 3 * TILE;      // v, then the staged output
   static constexpr uint32_t KS = 4 * TILE;                     // k' : 2 x 16 KB (d = 64: + zero block)
-  static constexpr uint32_t PS = KS + 32768;                   // P~ at d = 64
-  static constexpr uint32_t SS = PS + (D == 64 ? 32768 : 0);   // S~ : D/64 blocks of D rows x 128 B
-  static constexpr uint32_t ZP = SS + (D / 64) * D * 128;      // z partials [2][producer warps][D] fp32
-  static constexpr uint32_t ZS = ZP + 2 * Prod<D>::WARPS * D * 4;  // z [D] fp32
-  static constexpr uint32_t DI = ZS + D * 4;                   // q'.z [2][128] fp32
-  static constexpr uint32_t RSH = DI + 2 * kC * 4;             // helpers' partial row sums [128]
-  static constexpr uint32_t TAB = RSH + kC * 4;                // feature tables (FeatTab)
-  // full0 full1 empty0 empty1 vfull0 vfull1 s_done a_done b_done conv_done z_ready staged0 staged1 hp
+  static constexpr uint32_t SS = KS + 32768;                   // S~ : D/64 blocks of D rows x 128 B
+  static constexpr uint32_t ZS = SS + (D / 64) * D * 128;      // z ring [3][D] fp32
+  static constexpr uint32_t DI = ZS + 3 * D * 4;               // q'.z halves [2 buffers][2 halves][128]
+  static constexpr uint32_t RS = DI + 2 * 2 * kC * 4;          // masked score row sums, same shape
+  static constexpr uint32_t ZH = RS + 2 * 2 * kC * 4;          // helpers' partial column sums [64 / (D / 8)][D]
+  static constexpr uint32_t TAB = ZH + (64 / (D / 8)) * D * 4;  // feature tables (FeatTab)
+  // full[2] vfull[2] empty[2] p_done kv_done kfree pconv sconv b_done ofree[2] staged[2]
+  // zfull[3] zempty[3] qfull[2]
   static constexpr uint32_t BAR = TAB + 8 * D * 4;
-  static constexpr uint32_t MISC = BAR + 14 * 8;               // TMEM base, abort flag
+  static constexpr int NBAR = 24;
+  static constexpr uint32_t MISC = BAR + NBAR * 8;             // TMEM base, abort flag
   static constexpr uint32_t BYTES = MISC + 16;
-  // TMEM columns: P, two O accumulators, S
+  // TMEM columns: P (fp32 scores; the bf16 P~ is written over columns [0, 32) and [64, 96)), two
+  // O accumulators, S
   static constexpr uint32_t TP = 0, TO0 = 128, TO1 = 128 + D, TS = 128 + 2 * D;
   static_assert(TS + D <= 512, "TMEM budget");
   static_assert(BYTES <= 232448, "shared memory budget");
@@ -180,19 +183,18 @@ __device__ __forceinline__ void init_state(const PrefillArgs& a, const float* ws
   }
 }
 
-// One group of 32 score columns [col, col + 32) of the calling thread's tile row er: P (fp32, TMEM
-// at tp + col) -> bf16 P~ in the swizzled operand at pb, masked to tau <= er on the diagonal group;
-// the masked fp32 scores are added to rs.
-__device__ __forceinline__ void convert_p_group(uint32_t tp, uint32_t pb, int col, int er, bool diag, float& rs) {
-  const uint32_t blk = pb + (col / 64) * 16384;
-  const int cc = (col % 64) / 8;
+// Scores of one group of 32 keys [col, col + 32) of the calling thread's tile row er (its TMEM lane):
+// P (fp32, TMEM at tp + col) -> bf16 P~ pairs written back into TMEM at tp + dst (16 columns that
+// this thread has already read; the A operand of the P~V product), masked to tau <= er on the
+// diagonal group. The masked fp32 scores are added to rs.
+__device__ __forceinline__ void convert_p_group(uint32_t tp, int col, int dst, int er, bool diag, float& rs) {
   uint32_t u[2][16];
   tc::tmem_ld16(tp + col, u[0]);
   tc::tmem_ld16(tp + col + 16, u[1]);
   tc::tmem_wait_ld();
+  uint32_t w[16];
 #pragma unroll
   for (int m = 0; m < 2; ++m) {
-    uint32_t w[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int tau = col + 16 * m + 2 * e;
@@ -202,23 +204,46 @@ __device__ __forceinline__ void convert_p_group(uint32_t tp, uint32_t pb, int co
         x0 = tau <= er ? x0 : 0.f;
         x1 = tau + 1 <= er ? x1 : 0.f;
       }
-      w[e] = tc::pack_bf16x2(x0, x1);
+      w[8 * m + e] = tc::pack_bf16x2(x0, x1);
       rs += x0 + x1;
     }
-    sts16(blk + tc::sw128(er, cc + 2 * m), make_uint4(w[0], w[1], w[2], w[3]));
-    sts16(blk + tc::sw128(er, cc + 2 * m + 1), make_uint4(w[4], w[5], w[6], w[7]));
   }
+  tc::tmem_st16(tp + dst, w);
+}
+
+// q'_er . z over the columns [hf D/2, (hf + 1) D/2) of row er of the swizzled bf16 q' tile at qb
+// (fp32 products and sum; z is fp32 [D]).
+template <int D>
+__device__ __forceinline__ float qz_half(const uint8_t* qb, const float* z, int er, int hf) {
+  float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i) {
+    const int col = hf * (D / 2) + 8 * i;
+    const uint4 x = *reinterpret_cast<const uint4*>(qb + (col / 64) * 16384 + tc::sw128(er, (col % 64) / 8));
+    const float4 za = *reinterpret_cast<const float4*>(z + col);
+    const float4 zb = *reinterpret_cast<const float4*>(z + col + 4);
+    acc0 = fmaf(__uint_as_float(x.x << 16), za.x, acc0);
+    acc1 = fmaf(__uint_as_float(x.x & 0xffff0000u), za.y, acc1);
+    acc0 = fmaf(__uint_as_float(x.y << 16), za.z, acc0);
+    acc1 = fmaf(__uint_as_float(x.y & 0xffff0000u), za.w, acc1);
+    acc0 = fmaf(__uint_as_float(x.z << 16), zb.x, acc0);
+    acc1 = fmaf(__uint_as_float(x.z & 0xffff0000u), zb.y, acc1);
+    acc0 = fmaf(__uint_as_float(x.w << 16), zb.z, acc0);
+    acc1 = fmaf(__uint_as_float(x.w & 0xffff0000u), zb.w, acc1);
+  }
+  return acc0 + acc1;
 }
 
 // ------------------------------------------------------------------------------------------------
 // Kernel B: one CTA per (document, head, segment).
 template <int D>
 __global__ void __launch_bounds__(kThreadsB, 1)
-    prefill_tc_kernel(const TcArgs ta, const __grid_constant__ CUtensorMap tmap_v,
+    prefill_tc_kernel(const TcArgs ta, const __grid_constant__ CUtensorMap tmap_q,
+                      const __grid_constant__ CUtensorMap tmap_v,
                       const __grid_constant__ CUtensorMap tmap_o) {
   using L = LayB<D>;
   using PM = Prod<D>;
-  constexpr int TPR = PM::TPR, RPP = PM::RPP, NPASS = PM::NPASS, RING = PM::RING;
+  constexpr int TPR = PM::TPR, RPP = PM::RPP, NPASS = PM::NPASS;
   const PrefillArgs& a = ta.p;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -244,14 +269,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, kDevInternal);
     return;
   }
-  float* zp = reinterpret_cast<float*>(smem + L::ZP);
   float* zs = reinterpret_cast<float*>(smem + L::ZS);
   float* di = reinterpret_cast<float*>(smem + L::DI);
-  const uint32_t bar_full = base + L::BAR, bar_empty = bar_full + 16, bar_vfull = bar_full + 32;
-  const uint32_t bar_s = bar_full + 48, bar_a = bar_full + 56, bar_b = bar_full + 64;
-  const uint32_t bar_conv = bar_full + 72, bar_zr = bar_full + 80, bar_staged = bar_full + 88;
-  const uint32_t bar_hp = bar_full + 104;  // helpers' half of the score conversion done
-  float* rsh = reinterpret_cast<float*>(smem + L::RSH);
+  float* rsm = reinterpret_cast<float*>(smem + L::RS);
+  const uint32_t bar_full = base + L::BAR, bar_vfull = bar_full + 16, bar_empty = bar_full + 32;
+  const uint32_t bar_p = bar_full + 48, bar_kv = bar_full + 56, bar_kfree = bar_full + 64;
+  const uint32_t bar_pconv = bar_full + 72, bar_sconv = bar_full + 80, bar_b = bar_full + 88;
+  const uint32_t bar_ofree = bar_full + 96, bar_staged = bar_full + 112;
+  const uint32_t bar_zfull = bar_full + 128, bar_zempty = bar_full + 152, bar_qfull = bar_full + 176;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::MISC);
   int* s_abort = reinterpret_cast<int*>(smem + L::MISC + 4);
 
@@ -260,20 +285,24 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    tc::mbar_init(bar_full, kProd);
-    tc::mbar_init(bar_full + 8, kProd);
-    tc::mbar_init(bar_empty, 1);
-    tc::mbar_init(bar_empty + 8, 1);
-    tc::mbar_init(bar_vfull, 1);
-    tc::mbar_init(bar_vfull + 8, 1);
-    tc::mbar_init(bar_s, 1);
-    tc::mbar_init(bar_a, 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(bar_full + 8 * i, kProd);
+      tc::mbar_init(bar_vfull + 8 * i, 1);
+      tc::mbar_init(bar_empty + 8 * i, 1 + kConv);  // the MMAs' commit + the converters' q'.z reads
+      tc::mbar_init(bar_ofree + 8 * i, kConv);
+      tc::mbar_init(bar_staged + 8 * i, kConv);
+      tc::mbar_init(bar_qfull + 8 * i, 1);
+    }
+    tc::mbar_init(bar_p, 1);
+    tc::mbar_init(bar_kv, 1);
+    tc::mbar_init(bar_kfree, 1 + kHelp);  // the MMAs' commit + the helpers' column sums
+    tc::mbar_init(bar_pconv, kConv);
+    tc::mbar_init(bar_sconv, kConv);
     tc::mbar_init(bar_b, 1);
-    tc::mbar_init(bar_conv, kCons + kHelp);
-    tc::mbar_init(bar_hp, kHelp);
-    tc::mbar_init(bar_zr, kHelp);
-    tc::mbar_init(bar_staged, kCons);
-    tc::mbar_init(bar_staged + 8, kCons);
+    for (int i = 0; i < 3; ++i) {
+      tc::mbar_init(bar_zfull + 8 * i, kHelp);
+      tc::mbar_init(bar_zempty + 8 * i, kConv);
+    }
     tc::mbar_fence_init();
     *s_abort = 0;
   }
@@ -296,47 +325,42 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const uint32_t cblk = static_cast<uint32_t>(e0 / 64) * 16384;  // 64-column block
     const int cidx = (e0 % 64) / 8;                                 // 16-byte chunk in the row
 
-    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
+    // raw q arrives by TMA in the q' buffer (the transform overwrites it in place); k goes through
+    // registers, two passes of loads in flight (the ring index p % RK needs NPASS % RK == 0)
+    constexpr int RK = NPASS < 2 ? NPASS : 2;
+    static_assert(NPASS % RK == 0, "k load ring");
     const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(a.k);
     const int pos_base = a.pos_offset + seg_start;
     const long rstride = static_cast<long>(a.H) * D;  // elements from one token row to the next
-    const long off0 = (row0 + seg_start + prow) * rstride + static_cast<long>(h) * D + e0;
-    const __nv_bfloat16* qrow = qg + off0;
-    const __nv_bfloat16* krow = kg + off0;
-    auto load = [&](int c, int p, uint4& xq, uint4& xk) {
-      if (c * kC + p * RPP + prow < seg_n) {
-        const long off = static_cast<long>(c * kC + p * RPP) * rstride;
-        xq = ldg16(qrow + off);
-        xk = ldg16(krow + off);
-      } else {
-        xq = xk = make_uint4(0, 0, 0, 0);
-      }
+    const __nv_bfloat16* krow = kg + (row0 + seg_start + prow) * rstride + static_cast<long>(h) * D + e0;
+    auto load = [&](int c, int p, uint4& xk) {
+      if (c * kC + p * RPP + prow < seg_n) xk = ldg16(krow + static_cast<long>(c * kC + p * RPP) * rstride);
+      else xk = make_uint4(0, 0, 0, 0);
     };
     Rot rot;  // RoPE cos / sin of this thread's current row
-    uint4 rq[RING], rk[RING];
+    uint4 rk[RK];
     if (nchunks > 0) {
 #pragma unroll
-      for (int p = 0; p < RING; ++p) load(0, p, rq[p], rk[p]);
+      for (int p = 0; p < RK; ++p) load(0, p, rk[p]);
     }
     for (int c = 0; c < nchunks; ++c) {
       const int s = c & 1;
       int bad = 0;
-      if (c >= 2 && !tc::mbar_wait(bar_empty + 8 * s, ((c >> 1) + 1) & 1, kWaitCycles)) bad = 1;
+      // the raw q of this chunk (loaded once the buffer's previous q' had been read by both of its
+      // products and by the converters)
+      if (!tc::mbar_wait(bar_qfull + 8 * s, (c >> 1) & 1, kWaitCycles)) bad = 1;
       const uint32_t qb = base + (s ? L::Q1 : L::Q0), vb = base + (s ? L::V1 : L::V0);
       if (tid == 0 && c < 2) {
         // v rows of the first two chunks, straight into the swizzled operand (rows past the segment
-        // are either other tokens or zero fill; their k' and P columns are zero); the consumers
-        // load the later chunks' v into the buffer once its output staging is done
+        // are either other tokens or zero fill; their k' and P columns are zero); the store thread
+        // loads the later chunks' v into the buffer once its output staging is done
         tc::mbar_arrive_expect_tx(bar_vfull + 8 * s, L::TILE);
 #pragma unroll
         for (int jb = 0; jb < D / 64; ++jb)
           tc::tma_load_3d(vb + jb * 16384, &tmap_v, 64 * jb, h,
                           static_cast<int>(row0 + seg_start + c * kC), bar_vfull + 8 * s);
       }
-      float* dis = di + s * kC;
       uint4 kreg[NPASS];
-      float2 zca[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      float2 zcb[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       // angles of the chunk's first row: exact every 8 chunks, otherwise one more step of the
       // incremental rotation from the previous chunk's last pass (RPP positions further down)
       if ((c & 7) == 0) {
@@ -346,11 +370,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         tab_step(tab, e0 / 2, step);
         rot_step(rot, step);
       }
+      uint4 xq_next = lds16(qb + cblk + tc::sw128(prow, cidx));
 #pragma unroll
       for (int p = 0; p < NPASS; ++p) {
-        const uint4 xq = rq[p % RING], xk = rk[p % RING];
-        if (p + RING < NPASS) load(c, p + RING, rq[p % RING], rk[p % RING]);
-        else if (c + 1 < nchunks) load(c + 1, p + RING - NPASS, rq[p % RING], rk[p % RING]);
+        const uint4 xq = xq_next, xk = rk[p % RK];
+        if (p + 1 < NPASS) xq_next = lds16(qb + cblk + tc::sw128((p + 1) * RPP + prow, cidx));
+        if (p + RK < NPASS) load(c, p + RK, rk[p % RK]);
+        else if (c + 1 < nchunks) load(c + 1, p + RK - NPASS, rk[p % RK]);
         const int r = p * RPP + prow;
         const bool valid = c * kC + r < seg_n;
         if (p > 0) {
@@ -367,78 +393,86 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           float2 g0[2], g1[2];
           split_load<D>(tab.gq, part, g0, g1);
           scale_gains(g0, g1, rinvq);
-          rope_relu(fq, g0, g1, rot);
+          rope_scaled(fq, g0, g1, rot);
           split_load<D>(tab.gk, part, g0, g1);
           scale_gains(g0, g1, rinvk);
-          rope_relu(fk, g0, g1, rot);
+          rope_scaled(fk, g0, g1, rot);
         }
-        // z_{c-1} (the helpers' sum up to the previous chunk) is needed from here on
-        if (p == 0 && !tc::mbar_wait(bar_zr, c & 1, kWaitCycles)) bad = 1;
-        float2 zfa[2], zfb[2];  // z of the pairs' first / second elements
-        split_load<D>(zs, part, zfa, zfb);
-        float2 d2 = __fmul2_rn(fq.x0[0], zfa[0]);
-        d2 = __ffma2_rn(fq.x1[0], zfb[0], d2);
-        d2 = __ffma2_rn(fq.x0[1], zfa[1], d2);
-        d2 = __ffma2_rn(fq.x1[1], zfb[1], d2);
-        const float dq = row_sum<TPR>(d2.x + d2.y);
-        if (part == 0) dis[r] = dq;
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          zca[g] = __fadd2_rn(zca[g], fk.x0[g]);
-          zcb[g] = __fadd2_rn(zcb[g], fk.x1[g]);
-        }
-        sts16(qb + cblk + tc::sw128(r, cidx), pack_pairs(fq));
-        kreg[p] = pack_pairs(fk);
+        sts16(qb + cblk + tc::sw128(r, cidx), pack_pairs_relu(fq));
+        kreg[p] = pack_pairs_relu(fk);
       }
-      // the single k' buffer is free once the previous chunk's MMAs have completed
-      if (c >= 1 && !tc::mbar_wait(bar_a, (c - 1) & 1, kWaitCycles)) bad = 1;
+      // the single k' buffer is free once the previous chunk's MMAs have read it and the helpers
+      // have summed its columns
+      if (c >= 1 && !tc::mbar_wait(bar_kfree, (c - 1) & 1, kWaitCycles)) bad = 1;
 #pragma unroll
       for (int p = 0; p < NPASS; ++p) sts16(base + L::KS + cblk + tc::sw128(p * RPP + prow, cidx), kreg[p]);
-      // this warp's column sums of k'_c (the helper warps add the warps' sums up in a fixed order)
-      float zc[8];
-      pairs_to8(Pairs{{zca[0], zca[1]}, {zcb[0], zcb[1]}}, zc);
-      warp_colsum<TPR>(zc);
-      if (lane < TPR) {
-        float* zw = zp + (s * PM::WARPS + warp) * D + e0;
-        *reinterpret_cast<float4*>(zw) = make_float4(zc[0], zc[1], zc[2], zc[3]);
-        *reinterpret_cast<float4*>(zw + 4) = make_float4(zc[4], zc[5], zc[6], zc[7]);
-      }
       tc::fence_async_smem();
       tc::mbar_arrive(bar_full + 8 * s);
       if (bad) atomicExch(s_abort, 1);
       if (__any_sync(0xffffffffu, *reinterpret_cast<volatile int*>(s_abort))) break;
     }
-  } else {
-    // ============================================ consumers (warps 16-19), issuer warpgroup (20-23)
-    const bool cons = warp < (kProd + kCons) / 32;
-    if (cons) tc::regs_dec<kRegsConsB>();
-    else tc::regs_dec<kRegsIssueB>();
-    const int q4 = warp & 3;                 // TMEM lane quarter
-    const int er = 32 * q4 + lane;           // TMEM lane = tile row
+  } else if (warp < (kProd + kConv) / 32) {
+    // ============================================ converters (warps 16-23): two per lane quarter
+    tc::regs_dec<kRegsConvB>();
+    const int q4 = warp & 3;                       // TMEM lane quarter
+    const int hf = (warp - kProd / 32) >> 2;       // half of the columns
+    const int er = 32 * q4 + lane;                 // TMEM lane = tile row
     const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
-    // initial state (the two warpgroups take half of the columns each)
-    auto init = [&](int c0) {
-      if (nblk > 0) tc::grid_dep_wait();
-      init_state<D>(a, wsb, nblk, bh, er, tmem + tl + L::TS, base + L::SS, c0);
-      tc::tmem_wait_st();
-      tc::fence_async_smem();
-      tc::fence_before_sync();
-      tc::named_sync(kBarInit, kCons + 128);
-    };
-    if (cons) {
-      init(0);
+    const int j_lo = hf * (D / 2), j_hi = j_lo + D / 2;
+    // initial state of this half of the columns: S (TMEM) and S~ (completion 0 of sconv)
+    if (nblk > 0) tc::grid_dep_wait();
+    init_state<D>(a, wsb, nblk, bh, er, tmem + tl + L::TS, base + L::SS, j_lo);
+    tc::tmem_wait_st();
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    tc::mbar_arrive(bar_sconv);
 
     __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out);
     int bad = 0;
     for (int c = 0; c < nchunks; ++c) {
-      const int s = c & 1;
-      // ---- S (this chunk's state) -> bf16 S~ for the next chunk; the serial step comes first
-      int ok = tc::mbar_wait(bar_s, c & 1, kWaitCycles);
-      if (__any_sync(0xffffffffu, !ok)) bad = 1;  // warp-uniform, so TMEM loads stay converged
+      const int s = c & 1, zj = c % 3;
+      // ---- q'_t . z_{c-1} over this half's columns, read before the q' buffer is released
+      int ok = tc::mbar_wait(bar_full + 8 * s, (c >> 1) & 1, kWaitCycles);
+      ok &= tc::mbar_wait(bar_zfull + 8 * zj, (c / 3) & 1, kWaitCycles);
+      if (__any_sync(0xffffffffu, !ok)) bad = 1;
+      float dq = 0.f;
+      if (!bad) dq = qz_half<D>(smem + (s ? L::Q1 : L::Q0), zs + zj * D, er, hf);
+      di[(2 * s + hf) * kC + er] = dq;
+      tc::mbar_arrive(bar_zempty + 8 * zj);
+      tc::mbar_arrive(bar_empty + 8 * s);
+      // ---- P -> masked bf16 P~ in TMEM, and the row sums of the masked fp32 scores
+      ok = tc::mbar_wait(bar_p, c & 1, kWaitCycles);
+      if (__any_sync(0xffffffffu, !ok)) bad = 1;  // warp-uniform, so TMEM accesses stay converged
+      tc::fence_after_sync();
+      float rs = 0.f;
+      if (!bad) {
+        // Key groups of 32: left of this warp's rows (col < 32 q4) fully visible, col == 32 q4 the
+        // diagonal, the rest above it (all zero). This half's keys [64 hf, 64 hf + 64) become the
+        // bf16 pairs in TMEM columns [64 hf, 64 hf + 32).
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          const int col = 64 * hf + 32 * g;
+          if (col > 32 * q4) {  // warp-uniform: strictly above the diagonal
+            uint32_t zero[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) zero[e] = 0u;
+            tc::tmem_st16(tmem + tl + L::TP + 64 * hf + 16 * g, zero);
+          } else {
+            convert_p_group(tmem + tl + L::TP, col, 64 * hf + 16 * g, er, col == 32 * q4, rs);
+          }
+        }
+        tc::tmem_wait_st();
+      }
+      rsm[(2 * s + hf) * kC + er] = rs;
+      tc::fence_before_sync();
+      tc::mbar_arrive(bar_pconv);
+      // ---- S (the state after this chunk) -> bf16 S~, the operand of the next chunk's Q'S~
+      ok = tc::mbar_wait(bar_kv, c & 1, kWaitCycles);
+      if (__any_sync(0xffffffffu, !ok)) bad = 1;
       tc::fence_after_sync();
       if (!bad && 32 * q4 < D) {
 #pragma unroll 1
-        for (int j0 = 0; j0 < D; j0 += 32) {
+        for (int j0 = j_lo; j0 < j_hi; j0 += 32) {
           uint32_t u[2][16];
           tc::tmem_ld16(tmem + tl + L::TS + j0, u[0]);
           tc::tmem_ld16(tmem + tl + L::TS + j0 + 16, u[1]);
@@ -455,43 +489,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           }
         }
       }
-      // ---- P -> masked bf16 P~, and the row sums of the masked fp32 scores
-      ok = tc::mbar_wait(bar_a, c & 1, kWaitCycles);
-      ok &= tc::mbar_wait(bar_full + 8 * s, (c >> 1) & 1, kWaitCycles);  // the q'.z values
-      if (__any_sync(0xffffffffu, !ok)) bad = 1;
-      tc::fence_after_sync();
-      float den = 1.f;
-      if (!bad) {
-        const uint32_t pb = D == 128 ? base + (s ? L::Q1 : L::Q0) : base + L::PS;
-        float rs = 0.f;
-        // Column groups of 32 scores: those left of this warp's rows (col < 32 q4) are fully
-        // visible, the group col == 32 q4 holds the diagonal, the rest are above it (all zero).
-        // Lane quarters 2 and 3 have a helper warp that converts their odd groups.
-#pragma unroll 1
-        for (int col = 0; col < kC; col += 32) {
-          if (col > 32 * q4) {  // warp-uniform: strictly above the diagonal
-            const uint32_t blk = pb + (col / 64) * 16384;
-            const int cc = (col % 64) / 8;
-#pragma unroll
-            for (int m = 0; m < 4; ++m) sts16(blk + tc::sw128(er, cc + m), make_uint4(0, 0, 0, 0));
-            continue;
-          }
-          if (q4 >= 2 && ((col >> 5) & 1)) continue;  // the helper's group
-          convert_p_group(tmem + tl + L::TP, pb, col, er, col == 32 * q4, rs);
-        }
-        if (q4 >= 2) {  // add the helper's partial row sum
-          const int okh = tc::mbar_wait(bar_hp, c & 1, kWaitCycles);
-          if (__any_sync(0xffffffffu, !okh)) bad = 1;
-          rs += rsh[er];
-        }
-        den = di[s * kC + er] + rs + a.eps_den;
-      }
       tc::fence_async_smem();
       tc::fence_before_sync();
-      tc::mbar_arrive(bar_conv);
-      // ---- out = O / den
-      const int okb = tc::mbar_wait(bar_b, c & 1, kWaitCycles);
-      if (__any_sync(0xffffffffu, !okb)) bad = 1;
+      tc::mbar_arrive(bar_sconv);
+      // ---- out = O / (q'.z_{c-1} + rowsum(P) + eps), this half's columns
+      ok = tc::mbar_wait(bar_b, c & 1, kWaitCycles);
+      if (__any_sync(0xffffffffu, !ok)) bad = 1;
+      tc::named_sync(kBarQuarter + q4, 64);  // the other half's q'.z and row sums are written
       // A whole chunk is staged in its v buffer (free: v was read by the finished MMAs) in the box
       // layout of the output tensor map and written by TMA in full 128-byte lines; the ragged last
       // chunk of a document is written row by row (its tile would reach past it).
@@ -499,12 +503,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       const uint32_t ob = base + (s ? L::V1 : L::V0);
       if (!bad) {
         tc::fence_after_sync();
+        const float den = di[(2 * s) * kC + er] + di[(2 * s + 1) * kC + er] +
+                          rsm[(2 * s) * kC + er] + rsm[(2 * s + 1) * kC + er] + a.eps_den;
         const uint32_t to = tmem + tl + (s ? L::TO1 : L::TO0);
         const float inv = 1.0f / den;
         const int lt = c * kC + er;
         __nv_bfloat16* orow = og + ((row0 + seg_start + lt) * a.H + h) * D;
 #pragma unroll 1
-        for (int j0 = 0; j0 < D; j0 += 32) {
+        for (int j0 = j_lo; j0 < j_hi; j0 += 32) {
           uint32_t u[2][16];
           tc::tmem_ld16(to + j0, u[0]);
           tc::tmem_ld16(to + j0 + 16, u[1]);
@@ -520,9 +526,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
               sts16(blk + tc::sw128(er, cc + 2 * m), pack8(f));
               sts16(blk + tc::sw128(er, cc + 2 * m + 1), pack8(f + 8));
             } else if (lt < seg_n) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + j0);
-              dst[2 * m] = pack8(f);
-              dst[2 * m + 1] = pack8(f + 8);
+              uint4* dst = reinterpret_cast<uint4*>(orow + j0 + 16 * m);
+              dst[0] = pack8(f);
+              dst[1] = pack8(f + 8);
             }
           }
         }
@@ -530,13 +536,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       }
       tc::fence_before_sync();
       tc::mbar_arrive(bar_staged + 8 * s);  // the store thread takes it from here
+      tc::mbar_arrive(bar_ofree + 8 * s);   // the O accumulator may take chunk c + 2
       if (bad) atomicExch(s_abort, 1);
-      if (group_sync_or(kBarCons, kCons, *s_abort)) break;
+      if (group_sync_or(kBarConv, kConv, *s_abort)) break;
     }
     if (bad) atomicExch(s_abort, 1);
     if (last_seg && a.S_final != nullptr && !*s_abort && 32 * q4 < D) {
       tc::fence_after_sync();
-      for (int j0 = 0; j0 < D; j0 += 16) {
+      for (int j0 = j_lo; j0 < j_hi; j0 += 16) {
         uint32_t u[16];
         tc::tmem_ld16(tmem + tl + L::TS + j0, u);
         tc::tmem_wait_ld();
@@ -547,99 +554,15 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                                __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3]));
       }
     }
-    } else if (warp == (kProd + kCons) / 32 + 1) {
-      // ========================================================== output stores (warp 21)
-      init(D / 2);
-      if (lane == 0) {
-        int ok = 1;
-        for (int c = 0; c < nchunks; ++c) {
-          const int s = c & 1;
-          ok = tc::mbar_wait(bar_staged + 8 * s, (c >> 1) & 1, kWaitCycles);
-          if (!ok || *reinterpret_cast<volatile int*>(s_abort)) break;
-          const uint32_t ob = base + (s ? L::V1 : L::V0);
-          if (c * kC + kC <= seg_n) {  // a whole chunk was staged
-#pragma unroll
-            for (int jb = 0; jb < D / 64; ++jb)
-              tc::tma_store_3d(&tmap_o, ob + jb * 16384, 64 * jb, h,
-                               static_cast<int>(row0 + seg_start + c * kC));
-            tc::bulk_commit();
-            tc::bulk_wait_read0();  // the buffer may be refilled once the store has read it
-          }
-          if (c + 2 < nchunks) {  // v of chunk c + 2 into the same buffer
-            tc::mbar_arrive_expect_tx(bar_vfull + 8 * s, L::TILE);
-#pragma unroll
-            for (int jb = 0; jb < D / 64; ++jb)
-              tc::tma_load_3d(ob + jb * 16384, &tmap_v, 64 * jb, h,
-                              static_cast<int>(row0 + seg_start + (c + 2) * kC), bar_vfull + 8 * s);
-          }
-        }
-        tc::bulk_wait0();
-        if (!ok) atomicExch(s_abort, 1);
-      }
-    } else if (warp > (kProd + kCons) / 32 + 1) {
-      // ========================================================== helpers (warps 22-23)
-      init(D / 2);
-      const int ht = tid - (kProd + kCons + 64);
-      const int q4 = warp & 3;                 // TMEM lane quarter (2 or 3)
-      const int er = 32 * q4 + lane;           // tile row
-      const uint32_t tl = static_cast<uint32_t>(32 * q4) << 16;
-      // z at the segment start: z0 + the sums of k' of the blocks before the segment
-      for (int i = ht; i < D; i += kHelp) {
-        float z = a.z0 != nullptr ? a.z0[bh * D + i] : 0.f;
-        for (int g = 0; g < nblk; ++g) z += __ldcg(wsb + g * Rec<D>::FLOATS + Rec<D>::Z + i);
-        zs[split_idx<D>(i)] = z;
-      }
-      tc::mbar_arrive(bar_zr);  // z_{-1}
-      int bad = 0;
-      for (int c = 0; c < nchunks; ++c) {
-        const int s = c & 1;
-        if (!tc::mbar_wait(bar_full + 8 * s, (c >> 1) & 1, kWaitCycles)) bad = 1;
-        if (group_sync_or(kBarHelp, kHelp, bad | *s_abort)) {  // uniform over the helpers
-          bad = 1;
-          break;
-        }
-        // z_c = z_{c-1} + the producer warps' column sums of k'_c (fixed order: deterministic);
-        // the producers have finished reading z_{c-1} (full) and wait for this update (z_ready)
-        const float* zpc = zp + s * PM::WARPS * D;
-        for (int i = ht; i < D; i += kHelp) {
-          float z = zs[split_idx<D>(i)];
-#pragma unroll
-          for (int w = 0; w < PM::WARPS; ++w) z += zpc[w * D + i];
-          zs[split_idx<D>(i)] = z;
-        }
-        tc::mbar_arrive(bar_zr);
-        // the odd groups of this lane quarter's score conversion (its consumer warp takes the
-        // even ones), with their masked fp32 row sums
-        const int okp = tc::mbar_wait(bar_a, c & 1, kWaitCycles);
-        if (!__all_sync(0xffffffffu, okp)) {  // both helper warps leave at the next group check
-          bad = 1;
-          continue;
-        }
-        tc::fence_after_sync();
-        const uint32_t pb = D == 128 ? base + (s ? L::Q1 : L::Q0) : base + L::PS;
-        float rs = 0.f;
-        for (int col = 32; col <= 32 * q4; col += 64)
-          convert_p_group(tmem + tl + L::TP, pb, col, er, col == 32 * q4, rs);
-        rsh[er] = rs;
-        tc::fence_async_smem();
-        tc::fence_before_sync();
-        tc::mbar_arrive(bar_conv);
-        tc::mbar_arrive(bar_hp);
-      }
-      if (bad) atomicExch(s_abort, 1);
-      tc::named_sync(kBarHelp, kHelp);
-      if (last_seg && a.z_final != nullptr && !*s_abort) {
-        for (int i = ht; i < D; i += kHelp) a.z_final[bh * D + i] = zs[split_idx<D>(i)];
-      }
-    } else {
-      init(D / 2);
-      if (lane == 0) {
-      // ========================================================== MMA issue (one thread)
+  } else {
+    tc::regs_dec<kRegsIssueB>();  // one call site for the whole warpgroup (warps 24-27)
+  if (warp == kWarpIssue) {
+    // ========================================================== MMA issue (one thread)
+    if (lane == 0) {
       constexpr uint32_t ID_P = tc::idesc_bf16(128, 128, false, false);
       constexpr uint32_t ID_QS = tc::idesc_bf16(128, D, false, true);
       constexpr uint32_t ID_KV = tc::idesc_bf16(128, D, true, true);
       constexpr uint32_t ID_PV = tc::idesc_bf16(128, D, false, true);
-      tc::fence_after_sync();
       int ok = 1;
       // descriptors: k-major operands advance 32 bytes per K=16 step inside a 64-column block and
       // 16 KB per block; MN-major operands advance 2 KB (16 rows) per step
@@ -653,46 +576,169 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         const uint64_t d_q = tc::desc_sw128(qb, 16, 1024);
         const uint64_t d_v = tc::desc_sw128(vb, 16384, 1024);
         ok = tc::mbar_wait(bar_full + 8 * s, ph, kWaitCycles) &&
-             tc::mbar_wait(bar_vfull + 8 * s, ph, kWaitCycles) &&
-             (c == 0 || tc::mbar_wait(bar_conv, (c - 1) & 1, kWaitCycles));
+             tc::mbar_wait(bar_vfull + 8 * s, ph, kWaitCycles);
         if (!ok) break;
         tc::fence_after_sync();
-        // O = Q' S~_{c-1}, then S += K'^T V: the recurrence step; once both are done (s_done) S~
-        // may be overwritten with the new state
-#pragma unroll 1
-        for (int k = 0; k < D / 16; ++k) {
-          const uint64_t kofs = static_cast<uint64_t>((k / 4) * 1024 + (k % 4) * 2);
-          tc::mma_bf16(to, d_q + kofs, d_ss + static_cast<uint64_t>(k) * 128, ID_QS, k > 0);
-        }
-#pragma unroll 1
-        for (int k = 0; k < kC / 16; ++k) {
-          tc::mma_bf16(tmem + L::TS, d_ks_mn + static_cast<uint64_t>(k) * 128,
-                       d_v + static_cast<uint64_t>(k) * 128, ID_KV, 1u);
-        }
-        tc::mma_commit(bar_s);
-        // P = Q' K'^T
+        // P = Q' K'^T (the converters turn it into P~ while the next two products run)
 #pragma unroll 1
         for (int k = 0; k < D / 16; ++k) {
           const uint64_t kofs = static_cast<uint64_t>((k / 4) * 1024 + (k % 4) * 2);
           tc::mma_bf16(tmem + L::TP, d_q + kofs, d_ks_k + kofs, ID_P, k > 0);
         }
-        tc::mma_commit(bar_a);
-        // O += P~ V once the consumers have written P~ (and S~, and read P and S)
-        ok = tc::mbar_wait(bar_conv, c & 1, kWaitCycles);
+        tc::mma_commit(bar_p);
+        // O = Q' S~_{c-1}, once S~ holds the state before this chunk and the O buffer is free
+        ok = tc::mbar_wait(bar_sconv, c & 1, kWaitCycles) &&
+             (c < 2 || tc::mbar_wait(bar_ofree + 8 * s, ((c >> 1) + 1) & 1, kWaitCycles));
         if (!ok) break;
         tc::fence_after_sync();
-        const uint64_t d_p = tc::desc_sw128(D == 128 ? qb : base + L::PS, 16, 1024);
+#pragma unroll 1
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t kofs = static_cast<uint64_t>((k / 4) * 1024 + (k % 4) * 2);
+          tc::mma_bf16(to, d_q + kofs, d_ss + static_cast<uint64_t>(k) * 128, ID_QS, k > 0);
+        }
+        tc::mma_commit(bar_empty + 8 * s);  // q' of this chunk read by both of its products
+        // S += K'^T V (the fp32 master state, never leaves TMEM)
 #pragma unroll 1
         for (int k = 0; k < kC / 16; ++k) {
-          const uint64_t kofs = static_cast<uint64_t>((k / 4) * 1024 + (k % 4) * 2);
-          tc::mma_bf16(to, d_p + kofs, d_v + static_cast<uint64_t>(k) * 128, ID_PV, 1u);
+          tc::mma_bf16(tmem + L::TS, d_ks_mn + static_cast<uint64_t>(k) * 128,
+                       d_v + static_cast<uint64_t>(k) * 128, ID_KV, 1u);
+        }
+        tc::mma_commit(bar_kv);
+        tc::mma_commit(bar_kfree);
+        // O += P~ V, with P~ read from TMEM (keys 16 k .. 16 k + 15 in columns 64 (k / 4) + 8 (k % 4))
+        ok = tc::mbar_wait(bar_pconv, c & 1, kWaitCycles);
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll 1
+        for (int k = 0; k < kC / 16; ++k) {
+          tc::mma_bf16_ta(to, tmem + L::TP + 64 * (k / 4) + 8 * (k % 4),
+                          d_v + static_cast<uint64_t>(k) * 128, ID_PV, 1u);
         }
         tc::mma_commit(bar_b);
-        tc::mma_commit(bar_empty + 8 * s);  // q' (and P~) buffer free for chunk c + 2
       }
       if (!ok) atomicExch(s_abort, 1);
-      }
     }
+  } else if (warp == kWarpStore) {
+    // ========================================================== output stores, v loads
+    if (lane == 0) {
+      // raw q of the first two chunks into the q' buffers
+      for (int c = 0; c < 2 && c < nchunks; ++c) {
+        tc::mbar_arrive_expect_tx(bar_qfull + 8 * c, L::TILE);
+#pragma unroll
+        for (int jb = 0; jb < D / 64; ++jb)
+          tc::tma_load_3d(base + (c ? L::Q1 : L::Q0) + jb * 16384, &tmap_q, 64 * jb, h,
+                          static_cast<int>(row0 + seg_start + c * kC), bar_qfull + 8 * c);
+      }
+      int ok = 1;
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c & 1;
+        if (c + 2 < nchunks) {
+          // q' of chunk c has been read by both of its products and by the converters: the raw q of
+          // chunk c + 2 goes into the same buffer
+          ok = tc::mbar_wait(bar_empty + 8 * s, (c >> 1) & 1, kWaitCycles);
+          if (!ok || *reinterpret_cast<volatile int*>(s_abort)) break;
+          tc::mbar_arrive_expect_tx(bar_qfull + 8 * s, L::TILE);
+#pragma unroll
+          for (int jb = 0; jb < D / 64; ++jb)
+            tc::tma_load_3d(base + (s ? L::Q1 : L::Q0) + jb * 16384, &tmap_q, 64 * jb, h,
+                            static_cast<int>(row0 + seg_start + (c + 2) * kC), bar_qfull + 8 * s);
+        }
+        ok = tc::mbar_wait(bar_staged + 8 * s, (c >> 1) & 1, kWaitCycles);
+        if (!ok || *reinterpret_cast<volatile int*>(s_abort)) break;
+        const uint32_t ob = base + (s ? L::V1 : L::V0);
+        if (c * kC + kC <= seg_n) {  // a whole chunk was staged
+#pragma unroll
+          for (int jb = 0; jb < D / 64; ++jb)
+            tc::tma_store_3d(&tmap_o, ob + jb * 16384, 64 * jb, h,
+                             static_cast<int>(row0 + seg_start + c * kC));
+          tc::bulk_commit();
+          tc::bulk_wait_read0();  // the buffer may be refilled once the store has read it
+        }
+        if (c + 2 < nchunks) {  // v of chunk c + 2 into the same buffer
+          tc::mbar_arrive_expect_tx(bar_vfull + 8 * s, L::TILE);
+#pragma unroll
+          for (int jb = 0; jb < D / 64; ++jb)
+            tc::tma_load_3d(ob + jb * 16384, &tmap_v, 64 * jb, h,
+                            static_cast<int>(row0 + seg_start + (c + 2) * kC), bar_vfull + 8 * s);
+        }
+      }
+      tc::bulk_wait0();
+      if (!ok) atomicExch(s_abort, 1);
+    }
+  } else {
+    // ========================================================== z helpers (warps 26-27)
+    // z_c = z_{c-1} + the column sums of the bf16 k' tile of chunk c (the values the products
+    // read); each z goes into a ring of three slots for the converters' q'.z. A helper sums one
+    // 16-byte column chunk (8 columns) over one group of rows; the groups' partials are then added
+    // in a fixed order by the owner of each column pair.
+    constexpr int NCQ = D / 8, NRG = 64 / NCQ, RPG = kC / NRG;
+    const int ht = tid - (kProd + kConv + 64);
+    const int cq = ht % NCQ, rg = ht / NCQ;
+    const bool own = ht < D / 2;  // the owner of columns 2 ht and 2 ht + 1
+    float* zh = reinterpret_cast<float*>(smem + L::ZH);
+    float z0 = 0.f, z1 = 0.f;
+    if (own) {
+      if (nblk > 0) tc::grid_dep_wait();
+      if (a.z0 != nullptr) {
+        z0 = a.z0[bh * D + 2 * ht];
+        z1 = a.z0[bh * D + 2 * ht + 1];
+      }
+      for (int g = 0; g < nblk; ++g) {
+        z0 += __ldcg(wsb + g * Rec<D>::FLOATS + Rec<D>::Z + 2 * ht);
+        z1 += __ldcg(wsb + g * Rec<D>::FLOATS + Rec<D>::Z + 2 * ht + 1);
+      }
+      zs[2 * ht] = z0;  // slot 0: z before the segment, read by chunk 0
+      zs[2 * ht + 1] = z1;
+    }
+    tc::mbar_arrive(bar_zfull);
+    const uint8_t* kt = smem + L::KS + (cq / 8) * 16384;
+    int bad = 0;
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c & 1, zj = (c + 1) % 3;
+      int ok = tc::mbar_wait(bar_full + 8 * s, (c >> 1) & 1, kWaitCycles);
+      // the slot's previous z (chunk c - 2's) has been read by the converters
+      if (c + 1 >= 3) ok &= tc::mbar_wait(bar_zempty + 8 * zj, ((c + 1) / 3 - 1) & 1, kWaitCycles);
+      if (group_sync_or(kBarHelp, kHelp, !ok || *reinterpret_cast<volatile int*>(s_abort))) {
+        bad = 1;
+        break;
+      }
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll 8
+      for (int r = rg * RPG; r < rg * RPG + RPG; ++r) {
+        const uint4 x = *reinterpret_cast<const uint4*>(kt + tc::sw128(r, cq % 8));
+        acc[0] += __uint_as_float(x.x << 16);
+        acc[1] += __uint_as_float(x.x & 0xffff0000u);
+        acc[2] += __uint_as_float(x.y << 16);
+        acc[3] += __uint_as_float(x.y & 0xffff0000u);
+        acc[4] += __uint_as_float(x.z << 16);
+        acc[5] += __uint_as_float(x.z & 0xffff0000u);
+        acc[6] += __uint_as_float(x.w << 16);
+        acc[7] += __uint_as_float(x.w & 0xffff0000u);
+      }
+      tc::mbar_arrive(bar_kfree);  // done reading k' of chunk c
+#pragma unroll
+      for (int e = 0; e < 8; ++e) zh[rg * D + 8 * cq + e] = acc[e];
+      tc::named_sync(kBarHelp, kHelp);
+      if (own) {
+#pragma unroll
+        for (int g = 0; g < NRG; ++g) {
+          z0 += zh[g * D + 2 * ht];
+          z1 += zh[g * D + 2 * ht + 1];
+        }
+        zs[zj * D + 2 * ht] = z0;
+        zs[zj * D + 2 * ht + 1] = z1;
+      }
+      tc::mbar_arrive(bar_zfull + 8 * zj);
+    }
+    if (bad) atomicExch(s_abort, 1);
+    tc::named_sync(kBarHelp, kHelp);
+    if (last_seg && a.z_final != nullptr && !*s_abort && own) {
+      a.z_final[bh * D + 2 * ht] = z0;
+      a.z_final[bh * D + 2 * ht + 1] = z1;
+    }
+  }
   }
 
   tc::fence_before_sync();
@@ -943,13 +989,15 @@ cudaError_t launch_tc_d(const TcArgs& ta, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const long units = static_cast<long>(ta.p.n_docs) * ta.p.H;
   if (units == 0) return cudaSuccess;
-  CUtensorMap tmap_v, tmap_o;
+  CUtensorMap tmap_q, tmap_v, tmap_o;
   if (ta.p.v != nullptr && ta.p.total_rows > 0) {
-    e = make_rows_map(&tmap_v, ta.p.v, ta.p.total_rows, ta.p.H, D);
+    e = make_rows_map(&tmap_q, ta.p.q, ta.p.total_rows, ta.p.H, D);
+    if (e == cudaSuccess) e = make_rows_map(&tmap_v, ta.p.v, ta.p.total_rows, ta.p.H, D);
     if (e == cudaSuccess) e = make_rows_map(&tmap_o, ta.p.out, ta.p.total_rows, ta.p.H, D);
     if (e != cudaSuccess) return e;
   } else {
-    memset(&tmap_v, 0, sizeof(tmap_v));  // no rows: the kernels issue no copy
+    memset(&tmap_q, 0, sizeof(tmap_q));  // no rows: the kernels issue no copy
+    memset(&tmap_v, 0, sizeof(tmap_v));
     memset(&tmap_o, 0, sizeof(tmap_o));
   }
   const bool with_a = ta.nblk_max > 0;
@@ -968,7 +1016,7 @@ cudaError_t launch_tc_d(const TcArgs& ta, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = with_a ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D>, ta, tmap_v, tmap_o);
+  e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D>, ta, tmap_q, tmap_v, tmap_o);
   note_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

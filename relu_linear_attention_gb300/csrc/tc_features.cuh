@@ -130,6 +130,18 @@ __device__ __forceinline__ void rope_relu(Pairs& p, const float2 (&g0)[2], const
     p.x1[g] = make_float2(fmaxf(v.x, 0.f), fmaxf(v.y, 0.f));
   }
 }
+// RoPE(x * gamma * rinv) in place, without the ReLU (pack_pairs_relu applies it while rounding).
+__device__ __forceinline__ void rope_scaled(Pairs& p, const float2 (&g0)[2], const float2 (&g1)[2],
+                                            const Rot& r) {
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    const float2 y0 = __fmul2_rn(p.x0[g], g0[g]);
+    const float2 y1 = __fmul2_rn(p.x1[g], g1[g]);
+    const float2 ns = make_float2(-r.s[g].x, -r.s[g].y);
+    p.x0[g] = __ffma2_rn(y0, r.c[g], __fmul2_rn(y1, ns));    // y0 c - y1 s
+    p.x1[g] = __ffma2_rn(y0, r.s[g], __fmul2_rn(y1, r.c[g]));  // y0 s + y1 c
+  }
+}
 __device__ __forceinline__ void scale_gains(float2 (&g0)[2], float2 (&g1)[2], float s) {
   const float2 s2 = make_float2(s, s);
 #pragma unroll
@@ -142,6 +154,12 @@ __device__ __forceinline__ void scale_gains(float2 (&g0)[2], float2 (&g1)[2], fl
 __device__ __forceinline__ uint4 pack_pairs(const Pairs& p) {
   return make_uint4(tc::pack_bf16x2(p.x0[0].x, p.x1[0].x), tc::pack_bf16x2(p.x0[0].y, p.x1[0].y),
                     tc::pack_bf16x2(p.x0[1].x, p.x1[1].x), tc::pack_bf16x2(p.x0[1].y, p.x1[1].y));
+}
+
+// max(0, x) of the pairs, rounded to bf16 and packed in element order (one conversion per pair).
+__device__ __forceinline__ uint4 pack_pairs_relu(const Pairs& p) {
+  return make_uint4(tc::pack_bf16x2_relu(p.x0[0].x, p.x1[0].x), tc::pack_bf16x2_relu(p.x0[0].y, p.x1[0].y),
+                    tc::pack_bf16x2_relu(p.x0[1].x, p.x1[1].x), tc::pack_bf16x2_relu(p.x0[1].y, p.x1[1].y));
 }
 
 // Advances the angles by a fixed step (cos / sin of the step in `st`): one exact rotation.
