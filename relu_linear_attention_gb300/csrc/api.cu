@@ -88,7 +88,7 @@ uint64_t rapt_launch_counter(void) { return rapt::launch_count(); }
 size_t rapt_prefill_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype) {
   if (!known_dtype(dtype) || !supported_d(d) || B < 1 || H < 1 || L < 0) return 0;
   if (!rapt::tc_supported(to_dt(dtype), d)) return 0;
-  return rapt::tc_plan(B, H, L, static_cast<long>(B) * L, d).ws_bytes;
+  return rapt::tc_plan(B, H, L, static_cast<long>(B) * L, d, false).ws_bytes;
 }
 
 rapt_status rapt_prefill_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
@@ -127,7 +127,7 @@ rapt_status rapt_prefill_fwd(const void* q, const void* k, const void* v, rapt_d
   if (L == 0 && S_final == nullptr && z_final == nullptr) return RAPT_OK;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (rapt::tc_supported(to_dt(dtype), d))
-    return from_cuda(rapt::launch_prefill_tc(d, a, rapt::tc_plan(B, H, L, static_cast<long>(B) * L, d),
+    return from_cuda(rapt::launch_prefill_tc(d, a, rapt::tc_plan(B, H, L, static_cast<long>(B) * L, d, false),
                                              static_cast<float*>(workspace), s));
   return from_cuda(rapt::launch_prefill_simt(to_dt(dtype), d, a, s));
 }
@@ -254,7 +254,7 @@ size_t rapt_varlen_workspace_size(int32_t T, int32_t N, int32_t H, int32_t d, in
                                   rapt_dtype dtype) {
   if (!known_dtype(dtype) || !supported_d(d) || N < 1 || H < 1 || max_seqlen < 0 || T < 0) return 0;
   if (!rapt::tc_supported(to_dt(dtype), d)) return 0;
-  return rapt::tc_plan(N, H, max_seqlen, T, d).ws_bytes;
+  return rapt::tc_plan(N, H, max_seqlen, T, d, true).ws_bytes;
 }
 
 rapt_status rapt_varlen_fwd(const void* q, const void* k, const void* v, rapt_dtype dtype,
@@ -294,7 +294,7 @@ rapt_status rapt_varlen_fwd(const void* q, const void* k, const void* v, rapt_dt
   a.fa = make_features(params, d);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (rapt::tc_supported(to_dt(dtype), d))
-    return from_cuda(rapt::launch_prefill_tc(d, a, rapt::tc_plan(N, H, max_seqlen, T, d),
+    return from_cuda(rapt::launch_prefill_tc(d, a, rapt::tc_plan(N, H, max_seqlen, T, d, true),
                                              static_cast<float*>(workspace), s));
   return from_cuda(rapt::launch_prefill_simt(to_dt(dtype), d, a, s));
 }

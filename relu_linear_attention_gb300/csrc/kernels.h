@@ -135,14 +135,19 @@ cudaError_t launch_linear_tc(const void* x, const void* w, void* const* outs, in
 // nseg_max segments of seg_len tokens; the state increments of every segment but a document's
 // last are computed first, in blocks of seg_len / blk_per_seg tokens, and ws_bytes of workspace
 // hold them.
+// With sort_docs (varlen, one segment per document), the workspace ends with an int32 order of
+// the documents by decreasing length at order_off, so that the longest (document, head) units
+// are dispatched first.
 struct TcPlan {
   int nseg_max;
   int seg_len;
   int blk_per_seg;
   size_t ws_bytes;
+  bool sort_docs;
+  size_t order_off;
 };
 bool tc_supported(DType dt, int d);
-TcPlan tc_plan(int n_docs, int H, int max_seqlen, long total_tokens, int d);
+TcPlan tc_plan(int n_docs, int H, int max_seqlen, long total_tokens, int d, bool varlen);
 cudaError_t launch_prefill_tc(int d, const PrefillArgs& a, const TcPlan& plan, float* ws,
                               cudaStream_t stream);
 
@@ -157,6 +162,7 @@ struct TcArgs {
   int nblk_max;     // increment blocks per document slot
   int whole_doc;    // 0: the blocks before each document's last segment, all full;
                     // 1: every block of the document, the last one possibly ragged
+  const int* order; // nullable: prefill CTA slot -> document (longest first)
 };
 // The state increments of TcArgs' blocks (one launch; later launches may depend on it
 // programmatically: it triggers its dependents at its start).

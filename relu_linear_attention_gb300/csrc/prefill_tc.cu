@@ -65,6 +65,16 @@ namespace {
 
 using namespace feat;
 
+// 16-byte shared-memory accesses as plain C++ (at byte offset off from the dynamic shared base), so
+// that the compiler may schedule them freely; ordering with the tensor core and the TMA comes from
+// the fences and barriers, which are compiler barriers.
+__device__ __forceinline__ void st_shared16(uint8_t* sm, uint32_t off, const uint4& v) {
+  *reinterpret_cast<uint4*>(sm + off) = v;
+}
+__device__ __forceinline__ uint4 ld_shared16(const uint8_t* sm, uint32_t off) {
+  return *reinterpret_cast<const uint4*>(sm + off);
+}
+
 constexpr int kC = 128;          // chunk length = MMA M
 constexpr int kProd = 512;       // producer threads (16 warps)
 constexpr int kConv = 256;       // converter threads of kernel B (8 warps, two per TMEM lane quarter)
@@ -124,17 +134,21 @@ struct LayB {
   static_assert(BYTES <= 232448, "shared memory budget");
 };
 
-// Kernel A shared memory.
+// Kernel A shared memory: a ring of kStagesA stages, each the raw k tile (TMA; turned into k' in
+// place; d = 64 adds the zero block that pads k'^T to M = 128) and the v tile.
+constexpr int kStagesA = 3;
 template <int D>
 struct LayA {
   static constexpr uint32_t TILE = Prod<D>::TILE;
-  static constexpr uint32_t K0 = 0, K1 = 32768;                // k' sets, 2 x 16 KB each
-  static constexpr uint32_t V0 = 65536, V1 = V0 + TILE;
-  static constexpr uint32_t ZP = V1 + TILE;                    // z partials [producer warps][D]
-  static constexpr uint32_t TAB = ZP + Prod<D>::WARPS * D * 4; // feature tables (FeatTab)
-  static constexpr uint32_t BAR = TAB + 8 * D * 4;             // full0 full1 empty0 empty1 vfull0 vfull1
-  static constexpr uint32_t MISC = BAR + 6 * 8;
+  static constexpr uint32_t KT = 32768;                                // one k' stage
+  static constexpr uint32_t K0 = 0;                                    // k' stages
+  static constexpr uint32_t V0 = kStagesA * KT;                        // v stages
+  static constexpr uint32_t ZP = V0 + kStagesA * TILE;                 // z partials [producer warps][D]
+  static constexpr uint32_t TAB = ZP + Prod<D>::WARPS * D * 4;         // feature tables (FeatTab)
+  static constexpr uint32_t BAR = TAB + 8 * D * 4;  // kfull[S] vfull[S] ready[S] free[S]
+  static constexpr uint32_t MISC = BAR + 4 * kStagesA * 8;
   static constexpr uint32_t BYTES = MISC + 16;
+  static_assert(BYTES <= 232448, "shared memory budget");
 };
 
 // Initial state of a segment for columns [c0, c0 + D/2) of the calling thread's TMEM lane er:
@@ -249,7 +263,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int seg = blockIdx.x % ta.nseg_max;
   const int h = (blockIdx.x / ta.nseg_max) % a.H;
-  const int doc = blockIdx.x / (ta.nseg_max * a.H);
+  const int slot = blockIdx.x / (ta.nseg_max * a.H);
+  const int doc = ta.order != nullptr ? ta.order[slot] : slot;
 
   long row0;
   int n;
@@ -370,11 +385,11 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         tab_step(tab, e0 / 2, step);
         rot_step(rot, step);
       }
-      uint4 xq_next = lds16(qb + cblk + tc::sw128(prow, cidx));
+      uint4 xq_next = ld_shared16(smem, qb - base + cblk + tc::sw128(prow, cidx));
 #pragma unroll
       for (int p = 0; p < NPASS; ++p) {
         const uint4 xq = xq_next, xk = rk[p % RK];
-        if (p + 1 < NPASS) xq_next = lds16(qb + cblk + tc::sw128((p + 1) * RPP + prow, cidx));
+        if (p + 1 < NPASS) xq_next = ld_shared16(smem, qb - base + cblk + tc::sw128((p + 1) * RPP + prow, cidx));
         if (p + RK < NPASS) load(c, p + RK, rk[p % RK]);
         else if (c + 1 < nchunks) load(c + 1, p + RK - NPASS, rk[p % RK]);
         const int r = p * RPP + prow;
@@ -398,14 +413,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           scale_gains(g0, g1, rinvk);
           rope_scaled(fk, g0, g1, rot);
         }
-        sts16(qb + cblk + tc::sw128(r, cidx), pack_pairs_relu(fq));
+        st_shared16(smem, qb - base + cblk + tc::sw128(r, cidx), pack_pairs_relu(fq));
         kreg[p] = pack_pairs_relu(fk);
       }
       // the single k' buffer is free once the previous chunk's MMAs have read it and the helpers
       // have summed its columns
       if (c >= 1 && !tc::mbar_wait(bar_kfree, (c - 1) & 1, kWaitCycles)) bad = 1;
 #pragma unroll
-      for (int p = 0; p < NPASS; ++p) sts16(base + L::KS + cblk + tc::sw128(p * RPP + prow, cidx), kreg[p]);
+      for (int p = 0; p < NPASS; ++p) st_shared16(smem, L::KS + cblk + tc::sw128(p * RPP + prow, cidx), kreg[p]);
       tc::fence_async_smem();
       tc::mbar_arrive(bar_full + 8 * s);
       if (bad) atomicExch(s_abort, 1);
@@ -484,8 +499,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             float v[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(u[m][e]);
-            sts16(blk + tc::sw128(er, cc + 2 * m), pack8(v));
-            sts16(blk + tc::sw128(er, cc + 2 * m + 1), pack8(v + 8));
+            st_shared16(smem, blk - base + tc::sw128(er, cc + 2 * m), pack8(v));
+            st_shared16(smem, blk - base + tc::sw128(er, cc + 2 * m + 1), pack8(v + 8));
           }
         }
       }
@@ -523,8 +538,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(u[m][e]) * inv;
             if (whole) {
-              sts16(blk + tc::sw128(er, cc + 2 * m), pack8(f));
-              sts16(blk + tc::sw128(er, cc + 2 * m + 1), pack8(f + 8));
+              st_shared16(smem, blk - base + tc::sw128(er, cc + 2 * m), pack8(f));
+              st_shared16(smem, blk - base + tc::sw128(er, cc + 2 * m + 1), pack8(f + 8));
             } else if (lt < seg_n) {
               uint4* dst = reinterpret_cast<uint4*>(orow + j0 + 16 * m);
               dst[0] = pack8(f);
@@ -755,16 +770,18 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 // ------------------------------------------------------------------------------------------------
 // Kernel A: state increment (K'^T V and the column sums of k') of one block of blk_len tokens (every
 // block before a document's last segment; in whole-document mode, every block of the document, for
-// the bidirectional form). 16 producer warps fill one of two k' buffers (v arrives
-// by TMA) while the tensor core, fed by a dedicated issuer thread, accumulates the other into TMEM.
+// the bidirectional form and for the state of a shard). One thread streams the raw k and v tiles of
+// the block's chunks by TMA into a ring of stages; 16 producer warps turn each k tile into k' in
+// place (RMSNorm, RoPE, ReLU) and sum its columns; one thread accumulates K'^T V into TMEM, and the
+// stage is refilled once its product has completed.
 template <int D>
 __global__ void __launch_bounds__(kThreadsA, 1)
-    segment_state_kernel(const TcArgs ta, const __grid_constant__ CUtensorMap tmap_v) {
+    segment_state_kernel(const TcArgs ta, const __grid_constant__ CUtensorMap tmap_k,
+                         const __grid_constant__ CUtensorMap tmap_v) {
   using L = LayA<D>;
   using PM = Prod<D>;
-  // a whole chunk of k loads in flight: this kernel's passes are short, so two would not cover
-  // the memory latency
-  constexpr int TPR = PM::TPR, RPP = PM::RPP, NPASS = PM::NPASS, RING = PM::NPASS;
+  constexpr int S = kStagesA;
+  constexpr int TPR = PM::TPR, RPP = PM::RPP, NPASS = PM::NPASS;
   const PrefillArgs& a = ta.p;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -783,7 +800,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
   }
   const int seg_start = blk * ta.blk_len;
   // a block before the last segment is full; in whole-document mode the last one may be ragged
-  // (its missing rows load as zeros, whose k' is zero: they add nothing)
+  // (its missing rows are zeroed by the features: they add nothing)
   const int blk_n = min(ta.blk_len, n - seg_start);
   const int nchunks = (blk_n + kC - 1) / kC;
 
@@ -794,7 +811,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     return;
   }
   float* zp = reinterpret_cast<float*>(smem + L::ZP);
-  const uint32_t bar_full = base + L::BAR, bar_empty = bar_full + 16, bar_vfull = bar_full + 32;
+  const uint32_t bar_kfull = base + L::BAR, bar_vfull = bar_kfull + 8 * S;
+  const uint32_t bar_ready = bar_vfull + 8 * S, bar_free = bar_ready + 8 * S;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::MISC);
   int* s_abort = reinterpret_cast<int*>(smem + L::MISC + 4);
 
@@ -803,20 +821,20 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    tc::mbar_init(bar_full, kProd);
-    tc::mbar_init(bar_full + 8, kProd);
-    tc::mbar_init(bar_empty, 1);
-    tc::mbar_init(bar_empty + 8, 1);
-    tc::mbar_init(bar_vfull, 1);
-    tc::mbar_init(bar_vfull + 8, 1);
+    for (int i = 0; i < S; ++i) {
+      tc::mbar_init(bar_kfull + 8 * i, 1);
+      tc::mbar_init(bar_vfull + 8 * i, 1);
+      tc::mbar_init(bar_ready + 8 * i, kProd);
+      tc::mbar_init(bar_free + 8 * i, 1);
+    }
     tc::mbar_fence_init();
     *s_abort = 0;
     *reinterpret_cast<int*>(smem + L::MISC + 8) = 0;
   }
   if (D == 64) {
-    for (int i = tid; i < 16384 / 16; i += kThreadsA) {
-      sts16(base + L::K0 + 16384 + i * 16, make_uint4(0, 0, 0, 0));
-      sts16(base + L::K1 + 16384 + i * 16, make_uint4(0, 0, 0, 0));
+    for (int i = tid; i < S * 16384 / 16; i += kThreadsA) {
+      const int st = i / (16384 / 16), j = i % (16384 / 16);
+      sts16(base + L::K0 + st * L::KT + 16384 + j * 16, make_uint4(0, 0, 0, 0));
     }
   }
   const FeatTab tab = feat_tab<D>(smem + L::TAB);
@@ -837,59 +855,43 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     split_load<D>(tab.gk, part, gk0, gk1);
     Rot step;
     tab_step(tab, e0 / 2, step);
-    const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(a.k);
     const int pos_base = a.pos_offset + seg_start;
-    const long rstride = static_cast<long>(a.H) * D;
-    const __nv_bfloat16* krow = kg + (row0 + seg_start + prow) * rstride + static_cast<long>(h) * D + e0;
-    auto load = [&](int c, int p, uint4& xk) {
-      if (c * kC + p * RPP + prow < blk_n) xk = ldg16(krow + static_cast<long>(c * kC + p * RPP) * rstride);
-      else xk = make_uint4(0, 0, 0, 0);
-    };
     Rot rot;
     float2 zca[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     float2 zcb[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-    uint4 rk[RING];
-#pragma unroll
-    for (int p = 0; p < RING; ++p) load(0, p, rk[p]);
     int bad = 0;
     for (int c = 0; c < nchunks; ++c) {
-      const int s = c & 1;
-      if (c >= 2 && !tc::mbar_wait(bar_empty + 8 * s, ((c >> 1) + 1) & 1, kWaitCycles)) bad = 1;
-      const uint32_t kb = base + (s ? L::K1 : L::K0), vb = base + (s ? L::V1 : L::V0);
-      if (tid == 0) {
-        tc::mbar_arrive_expect_tx(bar_vfull + 8 * s, L::TILE);
-#pragma unroll
-        for (int jb = 0; jb < D / 64; ++jb)
-          tc::tma_load_3d(vb + jb * 16384, &tmap_v, 64 * jb, h,
-                          static_cast<int>(row0 + seg_start + c * kC), bar_vfull + 8 * s);
-      }
+      const int st = c % S;
+      if (!tc::mbar_wait(bar_kfull + 8 * st, (c / S) & 1, kWaitCycles)) bad = 1;
+      const uint32_t kb = base + L::K0 + st * L::KT + cblk;
       if ((c & 7) == 0) tab_rot_at(tab, pos_base + c * kC + prow, e0 / 2, rot);
       else rot_step(rot, step);
+      uint4 xk_next = ld_shared16(smem, kb - base + tc::sw128(prow, cidx));
 #pragma unroll
       for (int p = 0; p < NPASS; ++p) {
-        const uint4 xk = rk[p % RING];
-        if (p + RING < NPASS) load(c, p + RING, rk[p % RING]);
-        else if (c + 1 < nchunks) load(c + 1, p + RING - NPASS, rk[p % RING]);
+        const uint4 xk = xk_next;
         const int r = p * RPP + prow;
+        if (p + 1 < NPASS) xk_next = ld_shared16(smem, kb - base + tc::sw128(r + RPP, cidx));
+        const bool valid = c * kC + r < blk_n;
         if (p > 0) rot_step(rot, step);
         Pairs fk = unpack_pairs(xk);
         const float sk = row_sum<TPR>(sumsq(fk));
         float2 g0[2] = {gk0[0], gk0[1]}, g1[2] = {gk1[0], gk1[1]};
-        scale_gains(g0, g1, rsqrtf(sk * (1.0f / D) + a.fa.eps_norm));
+        scale_gains(g0, g1, valid ? rsqrtf(sk * (1.0f / D) + a.fa.eps_norm) : 0.f);
         rope_relu(fk, g0, g1, rot);
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           zca[g] = __fadd2_rn(zca[g], fk.x0[g]);
           zcb[g] = __fadd2_rn(zcb[g], fk.x1[g]);
         }
-        sts16(kb + cblk + tc::sw128(r, cidx), pack_pairs(fk));
+        st_shared16(smem, kb - base + tc::sw128(r, cidx), pack_pairs(fk));
       }
       tc::fence_async_smem();
-      tc::mbar_arrive(bar_full + 8 * s);
+      tc::mbar_arrive(bar_ready + 8 * st);
       if (bad) atomicExch(s_abort, 1);
       if (__any_sync(0xffffffffu, *reinterpret_cast<volatile int*>(s_abort))) break;
     }
-    // sums of k' over the segment (fixed order: deterministic)
+    // sums of k' over the block (fixed order: deterministic)
     float zc[8];
     pairs_to8(Pairs{{zca[0], zca[1]}, {zcb[0], zcb[1]}}, zc);
     warp_colsum<TPR>(zc);
@@ -908,27 +910,46 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     tc::regs_dec<kRegsIssueA>();
     const int q4 = warp & 3;
     if (warp == kProd / 32 && lane == 0) {
+      // ======================================================= MMA issue
       constexpr uint32_t ID_KV = tc::idesc_bf16(128, D, true, true);
       int ok = 1;
       for (int c = 0; c < nchunks && ok; ++c) {
-        const int s = c & 1, ph = (c >> 1) & 1;
-        const uint32_t kb = base + (s ? L::K1 : L::K0), vb = base + (s ? L::V1 : L::V0);
-        ok = tc::mbar_wait(bar_full + 8 * s, ph, kWaitCycles) &&
-             tc::mbar_wait(bar_vfull + 8 * s, ph, kWaitCycles);
+        const int st = c % S, ph = (c / S) & 1;
+        ok = tc::mbar_wait(bar_ready + 8 * st, ph, kWaitCycles) &&
+             tc::mbar_wait(bar_vfull + 8 * st, ph, kWaitCycles);
         if (!ok) break;
         tc::fence_after_sync();
-        const uint64_t d_k = tc::desc_sw128(kb, 16384, 1024), d_v = tc::desc_sw128(vb, 16384, 1024);
+        const uint64_t d_k = tc::desc_sw128(base + L::K0 + st * L::KT, 16384, 1024);
+        const uint64_t d_v = tc::desc_sw128(base + L::V0 + st * L::TILE, 16384, 1024);
 #pragma unroll 1
         for (int k = 0; k < kC / 16; ++k)
           tc::mma_bf16(tmem, d_k + static_cast<uint64_t>(k) * 128, d_v + static_cast<uint64_t>(k) * 128,
                        ID_KV, (c > 0 || k > 0) ? 1u : 0u);
-        tc::mma_commit(bar_empty + 8 * s);
+        tc::mma_commit(bar_free + 8 * st);
       }
       // the last accumulation
       const int last = nchunks - 1;
-      if (ok) ok = tc::mbar_wait(bar_empty + 8 * (last & 1), (last >> 1) & 1, kWaitCycles);
+      if (ok && last >= 0) ok = tc::mbar_wait(bar_free + 8 * (last % S), (last / S) & 1, kWaitCycles);
       if (!ok) atomicExch(s_abort, 1);
       *reinterpret_cast<volatile int*>(smem + L::MISC + 8) = 1;  // accumulation complete
+    } else if (warp == kProd / 32 + 1 && lane == 0) {
+      // ======================================================= TMA: raw k and v tiles of each chunk
+      int ok = 1;
+      for (int c = 0; c < nchunks; ++c) {
+        const int st = c % S;
+        // the stage's previous chunk (c - S) has been consumed by its product
+        if (c >= S) ok = tc::mbar_wait(bar_free + 8 * st, ((c / S) + 1) & 1, kWaitCycles);
+        if (!ok || *reinterpret_cast<volatile int*>(s_abort)) break;
+        const int row = static_cast<int>(row0 + seg_start + c * kC);
+        tc::mbar_arrive_expect_tx(bar_kfull + 8 * st, L::TILE);
+        tc::mbar_arrive_expect_tx(bar_vfull + 8 * st, L::TILE);
+#pragma unroll
+        for (int jb = 0; jb < D / 64; ++jb) {
+          tc::tma_load_3d(base + L::K0 + st * L::KT + jb * 16384, &tmap_k, 64 * jb, h, row, bar_kfull + 8 * st);
+          tc::tma_load_3d(base + L::V0 + st * L::TILE + jb * 16384, &tmap_v, 64 * jb, h, row, bar_vfull + 8 * st);
+        }
+      }
+      if (!ok) atomicExch(s_abort, 1);
     }
     __syncwarp();
     // the issuer warpgroup copies the increment out of TMEM (one lane quarter per warp)
@@ -959,6 +980,23 @@ __global__ void __launch_bounds__(kThreadsA, 1)
   if (warp == 0) tc::tmem_dealloc(tmem, 128);
 }
 
+// The documents in order of decreasing length (ties by index): order[rank] = doc, one CTA; the
+// lengths of a malformed cu_seqlens are clamped (the prefill kernel reports such documents).
+__global__ void __launch_bounds__(1024) doc_order_kernel(const int32_t* cu, int N, int total, int* order) {
+  extern __shared__ int lens[];
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    const int l = cu[i + 1] - cu[i];
+    lens[i] = l < 0 ? 0 : (l > total ? total : l);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    const int li = lens[i];
+    int rank = 0;
+    for (int j = 0; j < N; ++j) rank += (lens[j] > li || (lens[j] == li && j < i)) ? 1 : 0;
+    order[rank] = i;
+  }
+}
+
 template <typename K>
 cudaError_t set_smem(K kernel, uint32_t bytes, unsigned long long& configured) {
   int dev = 0;
@@ -971,13 +1009,14 @@ cudaError_t set_smem(K kernel, uint32_t bytes, unsigned long long& configured) {
 }
 
 template <int D>
-cudaError_t launch_state_d(const TcArgs& ta, const CUtensorMap& tmap_v, cudaStream_t stream) {
+cudaError_t launch_state_d(const TcArgs& ta, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                           cudaStream_t stream) {
   static unsigned long long cfg_a = 0;
   cudaError_t e = set_smem(segment_state_kernel<D>, LayA<D>::BYTES, cfg_a);
   if (e != cudaSuccess) return e;
   const long grid = static_cast<long>(ta.p.n_docs) * ta.p.H * ta.nblk_max;
   if (grid == 0) return cudaSuccess;
-  segment_state_kernel<D><<<static_cast<unsigned>(grid), kThreadsA, LayA<D>::BYTES, stream>>>(ta, tmap_v);
+  segment_state_kernel<D><<<static_cast<unsigned>(grid), kThreadsA, LayA<D>::BYTES, stream>>>(ta, tmap_k, tmap_v);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -1002,7 +1041,9 @@ cudaError_t launch_tc_d(const TcArgs& ta, cudaStream_t stream) {
   }
   const bool with_a = ta.nblk_max > 0;
   if (with_a) {
-    e = launch_state_d<D>(ta, tmap_v, stream);
+    CUtensorMap tmap_k;
+    e = make_rows_map(&tmap_k, ta.p.k, ta.p.total_rows, ta.p.H, D);
+    if (e == cudaSuccess) e = launch_state_d<D>(ta, tmap_k, tmap_v, stream);
     if (e != cudaSuccess) return e;
   }
   // kernel B as a programmatic dependent of kernel A (only then: it must not overlap anything else)
@@ -1026,16 +1067,28 @@ cudaError_t launch_tc_d(const TcArgs& ta, cudaStream_t stream) {
 
 bool tc_supported(DType dt, int d) { return dt == DType::BF16 && (d == 64 || d == 128); }
 
-TcPlan tc_plan(int n_docs, int H, int max_seqlen, long total_tokens, int d) {
+TcPlan tc_plan(int n_docs, int H, int max_seqlen, long total_tokens, int d, bool varlen) {
   // Estimated time in units of one kernel-B chunk. Kernel B runs one CTA per SM (waves of 152
   // CTAs, each costing its chunks plus about one chunk of state set-up); a kernel-A chunk (k
   // features and one GEMM) costs about half a kernel-B chunk, also one CTA per SM. Documents are
   // assumed to share the tokens evenly, except that the longest one bounds the segment count.
   // More segments or blocks cost workspace, so a longer plan must be clearly (5 %) faster to win.
-  TcPlan best{1, kC, 1, 0};
+  TcPlan best{1, kC, 1, 0, false, 0};
   const int chunks_max = max_seqlen > 0 ? (max_seqlen + kC - 1) / kC : 1;
   const double avg_chunks = n_docs > 0 ? static_cast<double>(total_tokens) / n_docs / kC : 0.0;
   double best_cost = 1e300;
+  // One segment per document, with the longest units dispatched first: bounded by the longest
+  // unit or by the total work spread over the SMs (plus a chunk of set-up). Documents of unequal
+  // lengths (varlen) make the wave estimate of the split plans below optimistic, so this plan wins
+  // whenever it is within reach.
+  {
+    const double total_chunks = static_cast<double>(H) * (static_cast<double>(total_tokens) / kC + 0.5 * n_docs);
+    const double cost1 = (chunks_max > total_chunks / 152 ? chunks_max : total_chunks / 152) + 1.0;
+    if (varlen && cost1 <= 1.15 * (total_chunks / 152 + 1.0)) {
+      best = TcPlan{1, chunks_max * kC, 1, 0, n_docs <= 1024, 0};
+      best_cost = 0.0;  // taken: no split plan below can beat the spread of the work
+    }
+  }
   for (int seg_chunks = chunks_max; seg_chunks >= 1; --seg_chunks) {
     const int nseg = (chunks_max + seg_chunks - 1) / seg_chunks;
     if (nseg > 64) break;
@@ -1067,15 +1120,20 @@ TcPlan tc_plan(int n_docs, int H, int max_seqlen, long total_tokens, int d) {
   best.ws_bytes = best.nseg_max > 1 ? static_cast<size_t>(units) * (best.nseg_max - 1) *
                                           best.blk_per_seg * rec * sizeof(float)
                                     : 0;
+  if (best.sort_docs) {
+    best.order_off = (best.ws_bytes + 255) / 256 * 256;
+    best.ws_bytes = best.order_off + static_cast<size_t>(n_docs) * sizeof(int);
+  }
   return best;
 }
 
 cudaError_t launch_state_tc(int d, const TcArgs& ta, cudaStream_t stream) {
   if (static_cast<long>(ta.p.n_docs) * ta.p.H * ta.nblk_max == 0 || ta.p.total_rows == 0) return cudaSuccess;
-  CUtensorMap tmap_v;
-  const cudaError_t e = make_rows_map(&tmap_v, ta.p.v, ta.p.total_rows, ta.p.H, d);
+  CUtensorMap tmap_k, tmap_v;
+  cudaError_t e = make_rows_map(&tmap_k, ta.p.k, ta.p.total_rows, ta.p.H, d);
+  if (e == cudaSuccess) e = make_rows_map(&tmap_v, ta.p.v, ta.p.total_rows, ta.p.H, d);
   if (e != cudaSuccess) return e;
-  return d == 128 ? launch_state_d<128>(ta, tmap_v, stream) : launch_state_d<64>(ta, tmap_v, stream);
+  return d == 128 ? launch_state_d<128>(ta, tmap_k, tmap_v, stream) : launch_state_d<64>(ta, tmap_k, tmap_v, stream);
 }
 
 cudaError_t launch_prefill_tc(int d, const PrefillArgs& a, const TcPlan& plan, float* ws,
@@ -1088,6 +1146,16 @@ cudaError_t launch_prefill_tc(int d, const PrefillArgs& a, const TcPlan& plan, f
   ta.blk_per_seg = plan.blk_per_seg;
   ta.blk_len = plan.seg_len / plan.blk_per_seg;
   ta.nblk_max = (plan.nseg_max - 1) * plan.blk_per_seg;
+  ta.order = nullptr;
+  if (plan.sort_docs && a.cu_seqlens != nullptr && a.n_docs > 0) {
+    int* order = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ws) + plan.order_off);
+    doc_order_kernel<<<1, 1024, static_cast<size_t>(a.n_docs) * sizeof(int), stream>>>(
+        a.cu_seqlens, a.n_docs, a.total_rows, order);
+    note_launches(1);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ta.order = order;
+  }
   return d == 128 ? launch_tc_d<128>(ta, stream) : launch_tc_d<64>(ta, stream);
 }
 

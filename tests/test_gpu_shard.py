@@ -110,15 +110,20 @@ def test_empty_shard_adds_nothing(cuda_device, lib):
 
 
 def test_sharded_helper_without_process_group_is_the_whole_prefill(cuda_device, lib):
+    """One rank: the helper's state call, exchange and prefill give the whole sequence."""
     B, L, H, d = 2, 500, 2, 128
-    q, k, v = (to_dev(x, "bf16") for x in draw(720, (B, L, H, d), "bf16"))
-    gq, gk = (torch.from_numpy(x).to(cuda_device) for x in gammas(721, H, d, True))
+    qn, kn, vn = draw(720, (B, L, H, d), "bf16")
+    gqn, gkn = gammas(721, H, d, True)
+    q, k, v = (to_dev(x, "bf16") for x in (qn, kn, vn))
+    gq, gk = (torch.from_numpy(x).to(cuda_device) for x in (gqn, gkn))
     out, Sf, zf = R.rapt_prefill_fwd_sharded(q, k, v, gq, gk, final_state=True)
-    ref, Sref, zref = R.rapt_prefill_fwd(q, k, v, gq, gk, final_state=True)
     torch.cuda.synchronize()
-    assert O.relative_error(to_host(out), to_host(ref))[0] <= TOL["bf16"]
-    assert O.relative_error(to_host(Sf), to_host(Sref))[1] <= 1e-5
-    assert O.relative_error(to_host(zf), to_host(zref))[1] <= 1e-5
+    ref, Sref, zref = O.rla2_prefill(widen(qn, "bf16"), widen(kn, "bf16"), widen(vn, "bf16"), gqn, gkn)
+    assert O.relative_error(to_host(out), ref)[0] <= TOL["bf16"]
+    for b in range(B):
+        for h in range(H):
+            assert O.relative_error(to_host(Sf[b, h]), Sref[b, h])[1] <= TOL["bf16"]
+            assert O.relative_error(to_host(zf[b, h]), zref[b, h])[1] <= TOL["bf16"]
 
 
 L2_CASES = [
