@@ -454,8 +454,9 @@ def run_gpu(args, rank, world, local):
               "roofline": {"bound": "hbm", "achieved": v_bytes / (v_mean * 1e-3) / 1e9,
                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": v_bytes / (v_mean * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                           "traffic": read_traffic("varlen", "segment_state_kernel", "prefill_tc_kernel"),
-                           "kernels": "segment_state_kernel<64> + prefill_tc_kernel<64> (one call)"}}
+                           "traffic": read_traffic("varlen", "doc_order_kernel", "prefill_tc_kernel"),
+                           "kernels": "doc_order_kernel + prefill_tc_kernel<64> (one call: one segment "
+                                      "per document, longest first)"}}
     del vq, vk, vv, vo, wv
 
     # ---------------- original RLA, L2 denominator (B=2, L=16384, H=16, d=128)
