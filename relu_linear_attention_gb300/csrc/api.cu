@@ -529,14 +529,21 @@ rapt_status l2_causal_common(const void* q, const void* k, const void* v, rapt_d
   if (workspace_bytes < need || (need > 0 && (workspace == nullptr || !aligned16(workspace))))
     return RAPT_ERR_WORKSPACE;
   if (total_rows == 0) return RAPT_OK;
-  if (cu_seqlens == nullptr && rapt::l2c_tc_supported(to_dt(dtype), d, false)) {
-    const rapt::L2cPlan plan = rapt::l2c_tc_plan(n_docs, doc_len, H);
-    rapt::L2Args a{};
+  if (rapt::l2c_tc_supported(to_dt(dtype), d)) {
+    rapt::L2cTcArgs a{};
     a.q = q; a.k = k; a.v = v; a.out = out;
-    a.ws = static_cast<float*>(workspace);
-    a.B = n_docs; a.L = doc_len; a.H = H; a.eps = eps;
-    return from_cuda(rapt::launch_l2_causal_tc(a, plan.nseg, plan.seg_len,
-                                               reinterpret_cast<cudaStream_t>(stream)));
+    a.cu_seqlens = cu_seqlens; a.dev_status = dev_status;
+    a.n_docs = n_docs; a.doc_len = doc_len; a.total_rows = static_cast<int>(total_rows);
+    a.max_seqlen = max_seqlen; a.H = H; a.eps = eps;
+    if (cu_seqlens == nullptr) {
+      const rapt::L2cPlan plan = rapt::l2c_tc_plan(n_docs, doc_len, H, d);
+      a.nseg = plan.nseg;
+      a.seg_len = plan.seg_len;
+    } else {
+      a.nseg = 1;
+      a.seg_len = max_seqlen > 0 ? (max_seqlen + 127) / 128 * 128 : 128;
+    }
+    return from_cuda(rapt::launch_l2_causal_tc(d, a, workspace, reinterpret_cast<cudaStream_t>(stream)));
   }
   const rapt::L2cPlan plan = rapt::l2c_plan(n_docs, H, max_seqlen, d);
   rapt::L2cArgs b{};
@@ -557,7 +564,7 @@ rapt_status l2_causal_common(const void* q, const void* k, const void* v, rapt_d
 
 size_t rla_l2_causal_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype) {
   if (!known_dtype(dtype) || !supported_d(d) || B < 1 || H < 1 || L < 1) return 0;
-  if (rapt::l2c_tc_supported(to_dt(dtype), d, false)) return rapt::l2c_tc_plan(B, L, H).ws_bytes;
+  if (rapt::l2c_tc_supported(to_dt(dtype), d)) return rapt::l2c_tc_plan(B, L, H, d).ws_bytes;
   return rapt::l2c_plan(B, H, L, d).ws_bytes;
 }
 
@@ -576,6 +583,7 @@ size_t rla_l2_causal_varlen_workspace_size(int32_t T, int32_t N, int32_t H, int3
                                            int32_t max_seqlen, rapt_dtype dtype) {
   if (!known_dtype(dtype) || !supported_d(d) || N < 1 || H < 1 || max_seqlen < 0 || T < 1)
     return 0;
+  if (rapt::l2c_tc_supported(to_dt(dtype), d)) return rapt::l2c_tc_varlen_ws_bytes(N);
   return rapt::l2c_plan(N, H, max_seqlen, d).ws_bytes;
 }
 

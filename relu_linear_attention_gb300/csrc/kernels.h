@@ -215,12 +215,40 @@ struct L2Args {
 size_t l2_workspace_bytes(int B, int L, int H, int d);
 // The moments [K'^T V | K'^T K'] of every (batch row, head, split of split_len tokens) into a.ws as
 // fp32 partials (bf16, d = 128; float4 (i, 4c .. 4c+3) of a split at index c * d + i, 2d columns).
-cudaError_t launch_l2_moments_tc(const L2Args& a, int nsplit, int split_len, cudaStream_t stream);
-// Causal L2 on the tensor cores (dense bf16, d = 128): segments of seg_len tokens start from the
-// moments of the splits before them (ws, written by launch_l2_moments_tc with split_len = seg_len).
-bool l2c_tc_supported(DType dt, int d, bool varlen);
-L2cPlan l2c_tc_plan(int B, int L, int H);
-cudaError_t launch_l2_causal_tc(const L2Args& a, int nseg, int seg_len, cudaStream_t stream);
+// (d in {64, 128}; the moments kernel reads k and v of a.B rows of a.L tokens.)
+cudaError_t launch_l2_moments_tc(int d, const L2Args& a, int nsplit, int split_len, cudaStream_t stream);
+// Causal L2 on the tensor cores (bf16, d in {64, 128}), dense batch rows (doc_len tokens each,
+// cu_seqlens null) or packed documents (cu_seqlens[n_docs + 1] on the device). Dense rows are cut
+// into nseg segments of seg_len tokens that start from the moments of the splits before them
+// (written by launch_l2_moments_tc into the workspace: l2c_tc_plan().ws_bytes); packed documents
+// run one segment each (nseg = 1, seg_len >= max_seqlen), the longest first (their document order,
+// l2c_tc_varlen_ws_bytes(n_docs) bytes, is the workspace).
+struct L2cTcArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  const float* ws;
+  const int32_t* cu_seqlens;
+  const int* order;
+  uint32_t* dev_status;
+  int n_docs;
+  int doc_len;
+  int total_rows;
+  int max_seqlen;
+  int H;
+  float eps;
+  int nseg;
+  int seg_len;
+};
+bool l2c_tc_supported(DType dt, int d);
+L2cPlan l2c_tc_plan(int B, int L, int H, int d);
+size_t l2c_tc_varlen_ws_bytes(int n_docs);
+cudaError_t launch_l2_causal_tc(int d, L2cTcArgs a, void* ws, cudaStream_t stream);
+// The documents of cu_seqlens in order of decreasing length (ties by index) into order[n_docs]
+// (n_docs <= 1024), one small launch.
+cudaError_t launch_doc_order(const int32_t* cu_seqlens, int n_docs, int total_rows, int* order,
+                             cudaStream_t stream);
 cudaError_t launch_rla_l2(DType dt, int d, const L2Args& a, cudaStream_t stream);
 
 // Split count launch_rla_l2 would choose, and the launch with an explicit split count

@@ -589,13 +589,14 @@ size_t l2_tc_workspace_bytes(int B, int L, int H, int d) {
   return static_cast<size_t>(n_bh * l2_tc_splits(B, L, H) * mat * 4 + n_bh * mat * 2);
 }
 
-cudaError_t launch_l2_moments_tc(const L2Args& a, int nsplit, int split_len, cudaStream_t stream) {
-  constexpr int D = 128;
+namespace {
+template <int D>
+cudaError_t launch_moments_split_d(const L2Args& a, int nsplit, int split_len, cudaStream_t stream) {
   static unsigned long long cfg1 = 0;
   cudaError_t e = set_smem(l2_tc_moments<D>, P1<D>::BYTES, cfg1);
   if (e != cudaSuccess) return e;
   const long n_bh = static_cast<long>(a.B) * a.H;
-  if (n_bh == 0 || a.L == 0) return cudaSuccess;
+  if (n_bh == 0 || a.L == 0 || nsplit == 0) return cudaSuccess;
   CUtensorMap tk, tv;
   e = make_bshd_map(&tk, a.k, a.B, a.L, a.H, D);
   if (e == cudaSuccess) e = make_bshd_map(&tv, a.v, a.B, a.L, a.H, D);
@@ -604,6 +605,12 @@ cudaError_t launch_l2_moments_tc(const L2Args& a, int nsplit, int split_len, cud
       a, nsplit, split_len, tk, tv);
   note_launches(1);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_l2_moments_tc(int d, const L2Args& a, int nsplit, int split_len, cudaStream_t stream) {
+  return d == 128 ? launch_moments_split_d<128>(a, nsplit, split_len, stream)
+                  : launch_moments_split_d<64>(a, nsplit, split_len, stream);
 }
 
 cudaError_t launch_rla_l2_tc(int d, const L2Args& a, cudaStream_t stream) {

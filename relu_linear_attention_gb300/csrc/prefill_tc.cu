@@ -1136,6 +1136,15 @@ cudaError_t launch_state_tc(int d, const TcArgs& ta, cudaStream_t stream) {
   return d == 128 ? launch_state_d<128>(ta, tmap_k, tmap_v, stream) : launch_state_d<64>(ta, tmap_k, tmap_v, stream);
 }
 
+cudaError_t launch_doc_order(const int32_t* cu_seqlens, int n_docs, int total_rows, int* order,
+                             cudaStream_t stream) {
+  if (n_docs <= 0) return cudaSuccess;
+  doc_order_kernel<<<1, 1024, static_cast<size_t>(n_docs) * sizeof(int), stream>>>(cu_seqlens, n_docs,
+                                                                               total_rows, order);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prefill_tc(int d, const PrefillArgs& a, const TcPlan& plan, float* ws,
                               cudaStream_t stream) {
   TcArgs ta{};
@@ -1149,10 +1158,7 @@ cudaError_t launch_prefill_tc(int d, const PrefillArgs& a, const TcPlan& plan, f
   ta.order = nullptr;
   if (plan.sort_docs && a.cu_seqlens != nullptr && a.n_docs > 0) {
     int* order = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ws) + plan.order_off);
-    doc_order_kernel<<<1, 1024, static_cast<size_t>(a.n_docs) * sizeof(int), stream>>>(
-        a.cu_seqlens, a.n_docs, a.total_rows, order);
-    note_launches(1);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_doc_order(a.cu_seqlens, a.n_docs, a.total_rows, order, stream);
     if (e != cudaSuccess) return e;
     ta.order = order;
   }
