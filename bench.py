@@ -303,6 +303,14 @@ def profile_case(args):
         gq, gk = (torch.from_numpy(x).to(device) for x in (w.gamma_q, w.gamma_k))
         tg = torch.empty_like(q).normal_(generator=torch.Generator(device=device).manual_seed(5))
         call = lambda: R.rapt_prefill_bwd(q, k, v, tg, gq, gk)
+    elif args.only == "varlen_backward":
+        wv = syn.varlen_bf16(seed=2)
+        q, k, v = (_bf(x, device) for x in (wv.q, wv.k, wv.v))
+        cu = torch.from_numpy(wv.cu_seqlens).to(device)
+        g = torch.ones(64, dtype=torch.float32, device=device)
+        tg = torch.empty_like(q).normal_(generator=torch.Generator(device=device).manual_seed(6))
+        msl = int(wv.lengths.max())
+        call = lambda: R.rapt_varlen_bwd(q, k, v, tg, cu, g, g, max_seqlen=msl)
     elif args.only == "linear":
         gen = torch.Generator(device=device).manual_seed(6)
         x = torch.empty((16384, 2048), dtype=torch.bfloat16, device=device).normal_(generator=gen)
@@ -457,7 +465,32 @@ def run_gpu(args, rank, world, local):
                            "traffic": read_traffic("varlen", "doc_order_kernel", "prefill_tc_kernel"),
                            "kernels": "doc_order_kernel + prefill_tc_kernel<64> (one call: one segment "
                                       "per document, longest first)"}}
-    del vq, vk, vv, vo, wv
+    # its backward (dq, dk, dv, dgamma; the tensor-core passes on 128-column tiles, 64 of them zero)
+    vg = torch.empty_like(vq).normal_(generator=torch.Generator(device=device).manual_seed(6))
+    vws = torch.empty(lib.rapt_varlen_bwd_workspace_size(wv.T, len(wv.lengths), 32, 64, msl, 1),
+                      dtype=torch.uint8, device=device)
+    vgr = [torch.empty_like(vq) for _ in range(3)] + [torch.empty_like(g64), torch.empty_like(g64)]
+    vb_ms = time_steps(
+        lambda: R.rapt_varlen_bwd(vq, vk, vv, vg, cu, g64, g64, max_seqlen=msl, dq=vgr[0], dk=vgr[1],
+                                  dv=vgr[2], dgamma_q=vgr[3], dgamma_k=vgr[4], workspace=vws),
+        max(3, args.steps // 4), args.warmup, flush)
+    vb_mean = max_over_ranks(statistics.fmean(vb_ms), device)
+    vb_bytes = 7 * wv.T * 32 * 64 * 2  # q, k, v, dout read; dq, dk, dv written (bf16)
+    varlen_backward = {
+        "value": world * wv.T / (vb_mean * 1e-3), "unit": "tokens/s", "ms_per_step": vb_mean,
+        "workload": "varlen backward T=65536 H=32 d=64 bf16, %d documents U[128,8192] (dq, dk, dv, "
+                    "dgamma_q, dgamma_k)" % len(wv.lengths),
+        "roofline": {"bound": "hbm", "achieved": vb_bytes / (vb_mean * 1e-3) / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": vb_bytes / (vb_mean * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     "algorithmic_bytes_per_call": vb_bytes,
+                     "traffic": read_traffic("varlen_backward", "bwd_tc_featmap", "bwd_tc_forward",
+                                             "bwd_tc_reverse", "bwd_tc_features", "bwd_gain_kernel",
+                                             "bwd_gain_final"),
+                     "kernels": "bwd_tc_featmap<64> + bwd_tc_forward + bwd_tc_reverse + "
+                                "bwd_tc_features<64> + bwd_gain_kernel + bwd_gain_final (one call: "
+                                "one segment per document, tiles padded to 128 columns)"}}
+    del vq, vk, vv, vo, wv, vg, vws, vgr
 
     # ---------------- original RLA, L2 denominator (B=2, L=16384, H=16, d=128)
     wl = syn.l2_bf16(seed=rank_seed(4, rank))
@@ -524,7 +557,7 @@ def run_gpu(args, rank, world, local):
                           "kernels": "segment_state_kernel + bidir_readout (one call; the second is a programmatic dependent of the first)"}}
     del bws
 
-    # ---------------- backward of the headline prefill (dq, dk, dv, dgamma; CUDA cores, fp32 math)
+    # ---------------- backward of the headline prefill (dq, dk, dv, dgamma; tensor cores, fp32 states)
     tg = torch.empty_like(q).normal_(generator=torch.Generator(device=device).manual_seed(5))
     gws = torch.empty(lib.rapt_prefill_bwd_workspace_size(B, L, H, d, 1), dtype=torch.uint8,
                       device=device)
@@ -624,7 +657,7 @@ def run_gpu(args, rank, world, local):
         "clocks": clk,
         "cpu_baseline": cpu,
         "rla_l2": rla_l2, "bidir": bidir, "backward": backward, "l2_causal": l2_causal,
-        "layer": layer, "varlen": varlen, "decode": decode,
+        "layer": layer, "varlen": varlen, "varlen_backward": varlen_backward, "decode": decode,
         # the headline numbers once more, compactly, at the end of the line
         "summary": {"prefill_tokens_per_s": value, "prefill_hbm_frac": achieved / peaks["hbm_gbs"],
                     "decode_tokens_per_s": decode["value"],
@@ -671,7 +704,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--oracle-seconds", type=float, default=15.0)
-    ap.add_argument("--only", choices=["prefill", "varlen", "l2", "bidir", "backward", "linear", "l2_causal"], default=None,
+    ap.add_argument("--only", choices=["prefill", "varlen", "varlen_backward", "l2", "bidir", "backward",
+                             "linear", "l2_causal"], default=None,
                     help="run one workload's calls without timing (for an ncu capture)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

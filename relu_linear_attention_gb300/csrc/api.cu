@@ -458,6 +458,7 @@ rapt_status backward_common(const void* q, const void* k, const void* v, const v
   b.dqf = w + plan.off_dqf;
   b.dkf = w + plan.off_dkf;
   b.chunks_max = plan.chunks_max;
+  b.d = d;
   if (tc) return from_cuda(rapt::launch_backward_tc(b, s));
   return from_cuda(rapt::launch_backward_simt(to_dt(dtype), d, b, s));
 }

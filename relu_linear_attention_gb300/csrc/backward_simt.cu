@@ -29,7 +29,8 @@
 //      and the segment's increment of the suffix state (Q'^T Gnum, sum scale q');
 //   3. bwd_reverse_kernel, one CTA per (document, head, segment), chunks in reverse: the suffix
 //      state from the later segments' increments, dk', dv, dk and the gain partials of k;
-//   4. bwd_gain_kernel: the gain partials summed in a fixed order.
+//   4. bwd_gain_kernel (+ bwd_gain_final where the partials are many): the gain partials summed in a
+//      fixed order.
 // No float atomics anywhere: every sum has a fixed order, so results are bitwise repeatable.
 #include "feature_bwd.cuh"
 #include "kernels.h"
@@ -541,7 +542,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_reverse_kernel(const BwdArgs 
 // segment) (and head, when shared). One CTA of 8 warps per 32 outputs (lane = output): warp w
 // sums the items w, w + 8, ... of the (document, [head,] segment) list in order, then the eight
 // warp sums are added in warp order, so the result is bitwise repeatable. blockIdx.y: 0 = q, 1 = k.
-__global__ void __launch_bounds__(256) bwd_gain_kernel(const BwdArgs b, int D) {
+// Sums the gain partials (item = (document * nh + head offset) * nseg + segment, D values each) of
+// items [it0, it1), it0 = blockIdx.z * per_split, for 32 output elements per CTA (blockIdx.y: 0 = q,
+// 1 = k), warp w taking items it0 + w, it0 + w + 8, ... and the warps added in order. With a
+// scratch buffer the CTA's sum is the first of two stages and goes to
+// scratch[(y * gridDim.z + z) * n_out + e]; without one it is the gain's gradient.
+__global__ void __launch_bounds__(256)
+    bwd_gain_kernel(const BwdArgs b, int D, int per_split, float* scratch) {
   const PrefillArgs& a = b.p;
   const bool per_head = a.fa.gamma_stride != 0;
   const int n_out = per_head ? a.H * D : D;
@@ -556,12 +563,13 @@ __global__ void __launch_bounds__(256) bwd_gain_kernel(const BwdArgs b, int D) {
     const int c = e % D;
     const int nh = per_head ? 1 : a.H;        // heads per output
     const int h0 = per_head ? e / D : 0;
-    // item it = (doc * nh + (h - h0)) * nseg + seg; walked with counters (no divisions in the loop)
     const int items = a.n_docs * nh * b.nseg;
-    int seg = warp % b.nseg, dh = warp / b.nseg;
+    const int it0 = blockIdx.z * per_split, it1 = min(items, it0 + per_split);
+    // walked with counters (one division at the start, none in the loop)
+    int seg = (it0 + warp) % b.nseg, dh = (it0 + warp) / b.nseg;
     const int dseg = 8 % b.nseg, ddh = 8 / b.nseg;
 #pragma unroll 4
-    for (int it = warp; it < items; it += 8) {  // (unrolled: the loads are issued ahead of the adds)
+    for (int it = it0 + warp; it < it1; it += 8) {  // (unrolled: the loads are issued ahead of the adds)
       const int doc = dh / nh, h = h0 + dh % nh;
       s += __ldg(part + ((static_cast<long>(doc) * a.H + h) * b.nseg + seg) * D + c);
       seg += dseg;
@@ -578,8 +586,21 @@ __global__ void __launch_bounds__(256) bwd_gain_kernel(const BwdArgs b, int D) {
     float t = 0.f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) t += ws[w][lane];
-    out[e] = t;
+    if (scratch != nullptr) scratch[(static_cast<long>(blockIdx.y) * gridDim.z + blockIdx.z) * n_out + e] = t;
+    else out[e] = t;
   }
+}
+
+// Second stage: the splits' sums of every output element added in split order.
+__global__ void __launch_bounds__(256) bwd_gain_final(const BwdArgs b, int n_out, int splits,
+                                                      const float* scratch) {
+  const int e = blockIdx.x * 256 + threadIdx.x;
+  float* out = blockIdx.y == 0 ? b.dgamma_q : b.dgamma_k;
+  if (out == nullptr || e >= n_out) return;
+  const float* p = scratch + static_cast<long>(blockIdx.y) * splits * n_out + e;
+  float t = 0.f;
+  for (int g = 0; g < splits; ++g) t += p[static_cast<long>(g) * n_out];
+  out[e] = t;
 }
 
 template <typename K>
@@ -676,7 +697,8 @@ BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d, bool
   }
   p.nblk_max = (p.nseg - 1) * p.blk_per_seg;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  const size_t rec = static_cast<size_t>(d) * (d + 1) * sizeof(float);
+  const int dr = tc ? 128 : d;  // the tensor-core records keep the 128 x 128 layout at d = 64
+  const size_t rec = static_cast<size_t>(dr) * (dr + 1) * sizeof(float);
   const size_t recs_f = up(static_cast<size_t>(units) * (tc ? p.nblk_max : p.nseg) * rec);
   const size_t recs_r = up(static_cast<size_t>(units) * p.nseg * p.rblk_per_seg * rec);
   const size_t rows = up(static_cast<size_t>(total_rows) * H * sizeof(float));
@@ -700,8 +722,29 @@ BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d, bool
 
 cudaError_t launch_bwd_gain(const BwdArgs& b, int d, cudaStream_t stream) {
   if (b.dgamma_q == nullptr && b.dgamma_k == nullptr) return cudaSuccess;
-  const int n_out = b.p.fa.gamma_stride != 0 ? b.p.H * d : d;
-  bwd_gain_kernel<<<dim3(static_cast<unsigned>((n_out + 31) / 32), 2), 256, 0, stream>>>(b, d);
+  const bool per_head = b.p.fa.gamma_stride != 0;
+  const int n_out = per_head ? b.p.H * d : d;
+  const long items = static_cast<long>(b.p.n_docs) * (per_head ? 1 : b.p.H) * b.nseg;
+  const unsigned gx = static_cast<unsigned>((n_out + 31) / 32);
+  // Many items per output element (gains shared by the heads of many documents and chunks): the
+  // items are cut into splits summed by separate CTAs, then the splits are added in order. The
+  // splits' sums go to the per-row den region of the workspace, which the passes no longer need.
+  const long room = static_cast<long>(b.p.total_rows) * b.p.H / (2L * n_out);
+  long splits = items > 512 ? (items + 255) / 256 : 1;
+  splits = splits > 128 ? 128 : splits;
+  splits = splits > room ? room : splits;
+  if (splits <= 1) {
+    bwd_gain_kernel<<<dim3(gx, 2, 1), 256, 0, stream>>>(b, d, static_cast<int>(items), nullptr);
+    note_launches(1);
+    return cudaGetLastError();
+  }
+  const int per_split = static_cast<int>((items + splits - 1) / splits);
+  bwd_gain_kernel<<<dim3(gx, 2, static_cast<unsigned>(splits)), 256, 0, stream>>>(b, d, per_split, b.den);
+  note_launches(1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_gain_final<<<dim3(static_cast<unsigned>((n_out + 255) / 256), 2), 256, 0, stream>>>(
+      b, n_out, static_cast<int>(splits), b.den);
   note_launches(1);
   return cudaGetLastError();
 }

@@ -1,5 +1,8 @@
 // Backward of causal RLA-2 on the 5th-generation tensor cores (tcgen05 + TMEM), sm_103a; bf16
-// tensors, d = 128, fp32 accumulation and fp32 states.
+// tensors, d = 64 or 128, fp32 accumulation and fp32 states. The passes work on 128-column tiles:
+// at d = 64 the TMA fills columns 64..127 of every loaded tile with zeros, so the products, the
+// states and their records carry zero columns (the records keep the 128 x 128 layout), and only
+// the first d columns of a row are written out.
 //
 // The gradients of sum dout . out (08-rapt-algorithm.md §4.2 "backward": the main and z scans,
 // gnum = g / den and scale = -(g . num) / den^2, two suffix scans, then ReLU, RoPE and RMSNorm
@@ -149,43 +152,6 @@ __device__ __forceinline__ void feature_sums(uint32_t tile, int n, int t0, const
     }
   }
 }
-
-// Several raw tiles at once (all loads in flight before any is stored): tile i gets rows of src[i];
-// with dv[i] set, its rows are divided by their den (gnum = g / den) and rounded to bf16.
-template <int NT>
-__device__ __forceinline__ void raw_tiles_tc(const __nv_bfloat16* const (&src)[NT],
-                                             const uint32_t (&tile)[NT], const bool (&dv)[NT],
-                                             long row0, int n, int t0, int H, int h, const float* den) {
-  constexpr int kPer = kC * 16 / kThreads;
-  uint4 v[NT][kPer];
-  float dn[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int idx = threadIdx.x + kThreads * i, r = idx >> 4, m = idx & 15;
-    const bool valid = t0 + r < n;
-#pragma unroll
-    for (int x = 0; x < NT; ++x)
-      v[x][i] = valid ? ldg16(src[x] + ((row0 + t0 + r) * H + h) * kD + 8 * m) : make_uint4(0, 0, 0, 0);
-    dn[i] = (den != nullptr && valid) ? den[(row0 + t0 + r) * H + h] : 1.f;
-  }
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int idx = threadIdx.x + kThreads * i, r = idx >> 4, m = idx & 15;
-#pragma unroll
-    for (int x = 0; x < NT; ++x) {
-      if (dv[x]) {
-        float f[8];
-        unpack8(v[x][i], f);
-        const float inv = 1.0f / dn[i];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] *= inv;
-        v[x][i] = feat::pack8(f);
-      }
-      sts16(tile[x] + tile_off(r, m), v[x][i]);
-    }
-  }
-}
-
 
 // ------------------------------------------------------------------------------------------------
 // Pass A: chunks in order.
@@ -405,8 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 32; ++j) u[j] = fmaf(u[j], inv, scale * zs[32 * gw + j]);
       if (t0 + kC <= n) {  // a whole chunk: staged in AS (its last reader, phase 4, is done)
         store_row32<false>(base + Lay::AS, t, gw, u);
-      } else if (valid) {  // the ragged last chunk row by row (a tile store would reach past it)
-        __nv_bfloat16* dst = dqf_out + ((row0 + t0 + t) * a.H + h) * kD + 32 * gw;
+      } else if (valid && gw < b.d / 32) {  // the ragged last chunk row by row
+        __nv_bfloat16* dst = dqf_out + ((row0 + t0 + t) * a.H + h) * b.d + 32 * gw;
 #pragma unroll
         for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(u + 8 * m);
       }
@@ -419,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (tid == 0 && t0 + kC <= n) {
 #pragma unroll
-      for (int jb = 0; jb < 2; ++jb)
+      for (int jb = 0; jb < b.d / 64; ++jb)
         tc::tma_store_3d(&tmdq, base + Lay::AS + jb * 16384, 64 * jb, h, static_cast<int>(row0 + t0));
       tc::bulk_commit();
     }
@@ -438,8 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) tc::bulk_wait0();  // the dq' tile stores are complete before the NaN fill or exit
   __syncthreads();
   if (bad) {  // a wait gave up: NaN dq' over the segment, so the failure cannot pass for a result
-    for (long r = s0 + tid / 16; r < s1; r += kThreads / 16)
-      *reinterpret_cast<uint4*>(dqf_out + ((row0 + r) * a.H + h) * kD + 8 * (tid % 16)) =
+    const int cpr = b.d / 8;  // 16-byte chunks per row
+    for (long r = s0 + tid / cpr; r < s1; r += kThreads / cpr)
+      *reinterpret_cast<uint4*>(dqf_out + ((row0 + r) * a.H + h) * b.d + 8 * (tid % cpr)) =
           make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
     if (tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, 2u);
   }
@@ -713,8 +680,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tmem + tl + kTDV + 32 * gw, o);
       if (whole) {  // into XS: R~'s last readers (the first two groups) are done
         store_row32<false>(base + Lay::XS, t, gw, o);
-      } else if (t0 + t < n) {
-        __nv_bfloat16* dst = dv + ((row0 + t0 + t) * a.H + h) * kD + 32 * gw;
+      } else if (t0 + t < n && gw < b.d / 32) {
+        __nv_bfloat16* dst = dv + ((row0 + t0 + t) * a.H + h) * b.d + 32 * gw;
 #pragma unroll
         for (int m = 0; m < 4; ++m)
           *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(o + 8 * m);
@@ -725,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
       if (tid == 0) {
 #pragma unroll
-        for (int jb = 0; jb < 2; ++jb)
+        for (int jb = 0; jb < b.d / 64; ++jb)
           tc::tma_store_3d(&tmdv, base + Lay::XS + jb * 16384, 64 * jb, h, static_cast<int>(row0 + t0));
         tc::bulk_commit();
       }
@@ -745,8 +712,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 32; ++j) o[j] += ws[32 * gw + j];
       if (whole) {  // into AS: A's last reader (the third group) is done
         store_row32<false>(base + Lay::AS, t, gw, o);
-      } else if (t0 + t < n) {  // dk' (bf16) to the workspace
-        __nv_bfloat16* dst = dkf_out + ((row0 + t0 + t) * a.H + h) * kD + 32 * gw;
+      } else if (t0 + t < n && gw < b.d / 32) {  // dk' (bf16) to the workspace
+        __nv_bfloat16* dst = dkf_out + ((row0 + t0 + t) * a.H + h) * b.d + 32 * gw;
 #pragma unroll
         for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(o + 8 * m);
       }
@@ -756,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();  // w is read
       if (whole && tid == 0) {
 #pragma unroll
-        for (int jb = 0; jb < 2; ++jb)
+        for (int jb = 0; jb < b.d / 64; ++jb)
           tc::tma_store_3d(&tmdk, base + Lay::AS + jb * 16384, 64 * jb, h, static_cast<int>(row0 + t0));
         tc::bulk_commit();
       }
@@ -777,8 +744,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) tc::bulk_wait0();  // the tile stores are complete before the NaN fill or exit
   __syncthreads();
   if (bad) {  // a wait gave up: NaN dk' and dv over the segment
-    for (long r = s0 + tid / 16; r < s1; r += kThreads / 16) {
-      const long o = ((row0 + r) * a.H + h) * kD + 8 * (tid % 16);
+    const int cpr = b.d / 8;  // 16-byte chunks per row
+    for (long r = s0 + tid / cpr; r < s1; r += kThreads / cpr) {
+      const long o = ((row0 + r) * a.H + h) * b.d + 8 * (tid % cpr);
       const uint4 nan = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
       *reinterpret_cast<uint4*>(dkf_out + o) = nan;
       *reinterpret_cast<uint4*>(dv + o) = nan;
@@ -982,10 +950,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // rotation in shared memory.
 constexpr int kMThreads = 256;
 
+template <int D>
 __global__ void __launch_bounds__(kMThreads)
     bwd_tc_featmap(const BwdArgs b, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k) {
-  constexpr int TPR = kD / 8, RPP = kMThreads / TPR, NPASS = kC / RPP;
+  constexpr int TPR = D / 8, RPP = kMThreads / TPR, NPASS = kC / RPP;
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x;
   const int which = blockIdx.x & 1;  // 0: q, 1: k
@@ -996,7 +965,7 @@ __global__ void __launch_bounds__(kMThreads)
   doc_bounds(a, doc, row0, n);
   const int t0 = chunk * kC;
   if (t0 >= n) return;  // uniform
-  __shared__ __align__(16) float tabmem[4 * kD];
+  __shared__ __align__(16) float tabmem[4 * D];
   __shared__ __align__(8) uint64_t bar_storage;
   extern __shared__ __align__(1024) uint8_t fsmem[];
   const uint32_t tile = (tc::smem_u32(fsmem) + 1023u) & ~1023u;  // the chunk's raw rows (TMA)
@@ -1011,15 +980,15 @@ __global__ void __launch_bounds__(kMThreads)
     const uint32_t tl[1] = {tile};
     tma_chunk<1>(maps, tl, h, static_cast<int>(row0 + t0), bar);
   }
-  const feat::FeatTab tab = feat::feat_tab<kD>(reinterpret_cast<uint8_t*>(tabmem));
-  feat::fill_tab<kD>(tab, a, h, RPP, tid, kMThreads);
+  const feat::FeatTab tab = feat::feat_tab<D>(reinterpret_cast<uint8_t*>(tabmem));
+  feat::fill_tab<D>(tab, a, h, RPP, tid, kMThreads);
   __syncthreads();
   const int prow = tid / TPR, part = tid % TPR, e0 = 8 * part;
-  const long rstride = static_cast<long>(a.H) * kD;
-  const long off0 = (row0 + t0 + prow) * rstride + static_cast<long>(h) * kD + e0;
+  const long rstride = static_cast<long>(a.H) * D;
+  const long off0 = (row0 + t0 + prow) * rstride + static_cast<long>(h) * D + e0;
   __nv_bfloat16* xf = static_cast<__nv_bfloat16*>(which ? b.kf : b.qf) + off0;
   float2 g0[2], g1[2];
-  feat::split_load<kD>(which ? tab.gk : tab.gq, part, g0, g1);
+  feat::split_load<D>(which ? tab.gk : tab.gq, part, g0, g1);
   feat::Rot step, rot;
   feat::tab_step(tab, e0 / 2, step);
   feat::tab_rot_at(tab, a.pos_offset + t0 + prow, e0 / 2, rot);
@@ -1038,7 +1007,7 @@ __global__ void __launch_bounds__(kMThreads)
     feat::Pairs f = feat::unpack_pairs(feat::lds16(tile + tile_off(r, part)));
     const float ss = feat::row_sum<TPR>(feat::sumsq(f));
     float2 ga[2] = {g0[0], g0[1]}, gb[2] = {g1[0], g1[1]};
-    feat::scale_gains(ga, gb, rsqrtf(ss * (1.0f / kD) + a.fa.eps_norm));
+    feat::scale_gains(ga, gb, rsqrtf(ss * (1.0f / D) + a.fa.eps_norm));
     feat::rope_relu(f, ga, gb, rot);
     if (t0 + r < n) *reinterpret_cast<uint4*>(xf + p * RPP * rstride) = feat::pack_pairs(f);
   }
@@ -1055,11 +1024,12 @@ __global__ void __launch_bounds__(kMThreads)
 // tiles per CTA, three CTAs per SM), so that each SM has ~200 KB of loads in flight.
 constexpr uint32_t kFeatSmem = 2 * kTile + 1024;  // two tiles (+ alignment slack)
 
+template <int D>
 __global__ void __launch_bounds__(kMThreads, 3)
     bwd_tc_features(const BwdArgs b, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_dq,
                     const __grid_constant__ CUtensorMap tm_dk) {
-  constexpr int TPR = kD / 8, RPP = kMThreads / TPR, NPASS = kC / RPP;
+  constexpr int TPR = D / 8, RPP = kMThreads / TPR, NPASS = kC / RPP;
   constexpr int WARPS = kMThreads / 32;
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1070,8 +1040,8 @@ __global__ void __launch_bounds__(kMThreads, 3)
   int n;
   doc_bounds(a, doc, row0, n);
   const int t0 = chunk * kC;
-  __shared__ __align__(16) float tabmem[4 * kD];
-  __shared__ __align__(16) float scratch[WARPS * kD];
+  __shared__ __align__(16) float tabmem[4 * D];
+  __shared__ __align__(16) float scratch[WARPS * D];
   __shared__ __align__(8) uint64_t bar_storage;
   extern __shared__ __align__(1024) uint8_t fsmem[];
   const uint32_t tiles_base = (tc::smem_u32(fsmem) + 1023u) & ~1023u;  // 1024-byte aligned
@@ -1091,14 +1061,14 @@ __global__ void __launch_bounds__(kMThreads, 3)
       const uint32_t tl[2] = {tiles_base, tiles_base + kTile};
       tma_chunk<2>(maps, tl, h, static_cast<int>(row0 + t0), bar);
     }
-    const feat::FeatTab tab = feat::feat_tab<kD>(reinterpret_cast<uint8_t*>(tabmem));
-    feat::fill_tab<kD>(tab, a, h, RPP, tid, kMThreads);
+    const feat::FeatTab tab = feat::feat_tab<D>(reinterpret_cast<uint8_t*>(tabmem));
+    feat::fill_tab<D>(tab, a, h, RPP, tid, kMThreads);
     __syncthreads();
-    const long rstride = static_cast<long>(a.H) * kD;
-    const long off0 = (row0 + t0 + prow) * rstride + static_cast<long>(h) * kD + e0;
+    const long rstride = static_cast<long>(a.H) * D;
+    const long off0 = (row0 + t0 + prow) * rstride + static_cast<long>(h) * D + e0;
     __nv_bfloat16* dx = static_cast<__nv_bfloat16*>(which ? b.dk : b.dq) + off0;
     float2 g0[2], g1[2];
-    feat::split_load<kD>(which ? tab.gk : tab.gq, part, g0, g1);
+    feat::split_load<D>(which ? tab.gk : tab.gq, part, g0, g1);
     feat::Rot step, rot;
     feat::tab_step(tab, e0 / 2, step);
     feat::tab_rot_at(tab, a.pos_offset + t0 + prow, e0 / 2, rot);
@@ -1119,7 +1089,7 @@ __global__ void __launch_bounds__(kMThreads, 3)
         if (p > 0) feat::rot_step(rot, step);
         const bool valid = t0 + p * RPP + prow < n;
         const feat::Pairs f = feat::unpack_pairs(rx[i]), d = feat::unpack_pairs(rd[i]);
-        const float r = rsqrtf(feat::row_sum<TPR>(feat::sumsq(f)) * (1.0f / kD) + a.fa.eps_norm);
+        const float r = rsqrtf(feat::row_sum<TPR>(feat::sumsq(f)) * (1.0f / D) + a.fa.eps_norm);
         const float2 r2 = make_float2(r, r);
         float2 dotv = make_float2(0.f, 0.f);
         float2 u0[2], u1[2];
@@ -1142,7 +1112,7 @@ __global__ void __launch_bounds__(kMThreads, 3)
           dotv = __ffma2_rn(u1[g], f.x1[g], dotv);
         }
         const float dot = feat::row_sum<TPR>(dotv.x + dotv.y);
-        const float c3 = r * r * r * dot * (1.0f / kD);
+        const float c3 = r * r * r * dot * (1.0f / D);
         const float2 c32 = make_float2(-c3, -c3);
         feat::Pairs o;
 #pragma unroll
@@ -1160,13 +1130,13 @@ __global__ void __launch_bounds__(kMThreads, 3)
   feat::warp_colsum<TPR>(dg);
   if (lane < TPR) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) scratch[warp * kD + e0 + e] = dg[e];
+    for (int e = 0; e < 8; ++e) scratch[warp * D + e0 + e] = dg[e];
   }
   __syncthreads();
-  if (tid < kD) {
+  if (tid < D) {
     float sum = 0.f;
-    for (int w = 0; w < WARPS; ++w) sum += scratch[w * kD + tid];
-    (which ? b.dgp_k : b.dgp_q)[(static_cast<long>(unit) * b.chunks_max + chunk) * kD + tid] =
+    for (int w = 0; w < WARPS; ++w) sum += scratch[w * D + tid];
+    (which ? b.dgp_k : b.dgp_q)[(static_cast<long>(unit) * b.chunks_max + chunk) * D + tid] =
         failed ? __int_as_float(0x7fc00000) : sum;  // a wait that gave up cannot pass for a result
   }
   if (failed && tid == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, 2u);
@@ -1174,7 +1144,7 @@ __global__ void __launch_bounds__(kMThreads, 3)
 
 }  // namespace
 
-bool bwd_tc_supported(DType dt, int d) { return dt == DType::BF16 && d == kD; }
+bool bwd_tc_supported(DType dt, int d) { return dt == DType::BF16 && (d == 64 || d == 128); }
 
 cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   int dev = 0;
@@ -1190,27 +1160,32 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
                                static_cast<int>(Lay::BYTES));
       if (e != cudaSuccess) return e;
     }
-    e = cudaFuncSetAttribute(bwd_tc_features, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kFeatSmem));
-    if (e != cudaSuccess) return e;
+    for (const void* f : {reinterpret_cast<const void*>(bwd_tc_features<64>),
+                          reinterpret_cast<const void*>(bwd_tc_features<128>)}) {
+      e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kFeatSmem));
+      if (e != cudaSuccess) return e;
+    }
     configured |= 1ull << dev;
   }
   const long grid = static_cast<long>(b.p.n_docs) * b.p.H * b.nseg;
   if (grid == 0) return cudaSuccess;
   const long fgrid = static_cast<long>(b.p.n_docs) * b.p.H * b.chunks_max * 2;
+  const int d = b.d;  // the tensors' head size; the tiles are 128 columns wide
   CUtensorMap tmq, tmk;
-  if ((e = make_rows_map(&tmq, b.p.q, b.p.total_rows, b.p.H, kD)) != cudaSuccess) return e;
-  if ((e = make_rows_map(&tmk, b.p.k, b.p.total_rows, b.p.H, kD)) != cudaSuccess) return e;
-  bwd_tc_featmap<<<static_cast<unsigned>(fgrid), kMThreads, kTile + 1024, stream>>>(b, tmq, tmk);  // q', k'
+  if ((e = make_rows_map(&tmq, b.p.q, b.p.total_rows, b.p.H, d)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmk, b.p.k, b.p.total_rows, b.p.H, d)) != cudaSuccess) return e;
+  if (d == 128) bwd_tc_featmap<128><<<static_cast<unsigned>(fgrid), kMThreads, kTile + 1024, stream>>>(b, tmq, tmk);
+  else bwd_tc_featmap<64><<<static_cast<unsigned>(fgrid), kMThreads, kTile + 1024, stream>>>(b, tmq, tmk);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // TMA maps of the row-major [rows, H, D] tensors the kernels stream
   CUtensorMap tmv, tmg, tmqf, tmkf;
   const long rows = b.p.total_rows;
-  if ((e = make_rows_map(&tmv, b.p.v, rows, b.p.H, kD)) != cudaSuccess) return e;
-  if ((e = make_rows_map(&tmg, b.dout, rows, b.p.H, kD)) != cudaSuccess) return e;
-  if ((e = make_rows_map(&tmqf, b.qf, rows, b.p.H, kD)) != cudaSuccess) return e;
-  if ((e = make_rows_map(&tmkf, b.kf, rows, b.p.H, kD)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmv, b.p.v, rows, b.p.H, d)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmg, b.dout, rows, b.p.H, d)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmqf, b.qf, rows, b.p.H, d)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmkf, b.kf, rows, b.p.H, d)) != cudaSuccess) return e;
   if (b.nseg > 1) {  // the prefix-state increments of the blocks before each document's last segment
     bwd_tc_blockstate<true><<<static_cast<unsigned>(static_cast<long>(b.p.n_docs) * b.p.H * b.nblk_max),
                               kThreads, Lay::BYTES, stream>>>(b, tmkf, tmv);
@@ -1219,9 +1194,9 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   }
   // dq', dk' (written by the passes, read by the feature kernel) and dv
   CUtensorMap tmdq, tmdk, tmdv;
-  if ((e = make_rows_map(&tmdq, b.dqf, rows, b.p.H, kD)) != cudaSuccess) return e;
-  if ((e = make_rows_map(&tmdk, b.dkf, rows, b.p.H, kD)) != cudaSuccess) return e;
-  if ((e = make_rows_map(&tmdv, b.dv, rows, b.p.H, kD)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmdq, b.dqf, rows, b.p.H, d)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmdk, b.dkf, rows, b.p.H, d)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmdv, b.dv, rows, b.p.H, d)) != cudaSuccess) return e;
   bwd_tc_forward<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b, tmqf, tmkf, tmv,
                                                                                  tmg, tmdq);
   note_launches(1);
@@ -1236,13 +1211,15 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
                                                                                  tmg, tmdv, tmdk);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_tc_features<<<static_cast<unsigned>(fgrid), kMThreads, kFeatSmem, stream>>>(b, tmq, tmk, tmdq,
-                                                                                  tmdk);
+  if (d == 128)
+    bwd_tc_features<128><<<static_cast<unsigned>(fgrid), kMThreads, kFeatSmem, stream>>>(b, tmq, tmk, tmdq, tmdk);
+  else
+    bwd_tc_features<64><<<static_cast<unsigned>(fgrid), kMThreads, kFeatSmem, stream>>>(b, tmq, tmk, tmdq, tmdk);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   BwdArgs g = b;  // the gain partials are per (document, head, chunk)
   g.nseg = b.chunks_max;
-  return launch_bwd_gain(g, kD, stream);
+  return launch_bwd_gain(g, d, stream);
 }
 
 }  // namespace rapt

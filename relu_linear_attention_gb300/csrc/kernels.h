@@ -84,6 +84,7 @@ struct BwdArgs {
   void* dqf;
   void* dkf;
   int chunks_max;
+  int d;  // head size of q, k, v and the gradients (the tensor-core passes pad it to 128 inside)
 };
 struct BwdPlan {
   int nseg;

@@ -16,32 +16,32 @@
 // q'.z is formed while the features are computed, and the row sums of the masked fp32 scores
 // while P is converted to the bf16 operand of the intra-chunk product.
 //
-// Kernel B is warp-specialised (768 threads, six warpgroups):
-//   warps 0-15  (producers): features of chunk c+1 into one of two q' buffers while the tensor
-//                            core works on chunk c; k' (one buffer) is held in registers until the
-//                            tensor core has released the previous k'; z and q'.z. Features are
-//                            the bulk of the CUDA-core work, so they get most of the warps;
-//   warps 16-19 (consumers): one TMEM lane quarter (32 tile rows) each: S -> S~, P -> P~ and its
-//                            row sums, then the output epilogue from one of two O accumulators;
-//   warp 20     (issuer):    one thread issues the MMAs (an issue blocks while the tensor core is
-//                            busy, so it gets a warp of its own);
-//   warp 21     (store):     one thread writes each staged output tile with TMA stores and, once the
-//                            store has read the buffer, loads the v tile of two chunks later into it;
-//   warps 22-23 (helpers):   z_c = z_{c-1} + the producer warps' column sums of k'_c, so that the
-//                            producers never wait for one another, and half of the score conversion
-//                            of TMEM lane quarters 2 and 3 (the rows whose masked scores span the
-//                            most columns).
-// v tiles need no transformation: the tensor-memory accelerator (TMA) copies them from HBM straight
-// into the swizzled operand layout, one chunk ahead. q and k go through registers (a short load
-// ring) because the features are computed on the way.
-// Hand-offs go through mbarriers: full[2] (producers -> issuer, consumers, helpers), vfull[2] (TMA ->
-// issuer), zr (helpers -> producers: z updated), staged[2] (consumers -> store thread),
-// empty[2] (chunk c's MMAs done -> its q' buffer free), s_done / a_done / b_done (tensor core -> consumers),
-// conv_done (consumers -> issuer: S~ and P~ written, S and P read). The recurrence step of chunk c
-// (O = Q'S~, then S += K'^T V) is issued first and committed on its own (s_done), so turning S
-// into the next chunk's operand, the one serial dependency between chunks, starts early.
-// Every wait is bounded; a wait that gives up sets RAPT_DEV_INTERNAL in the caller's status word
-// and the CTA winds down.
+// Kernel B is warp-specialised (896 threads, one CTA per SM):
+//   warps 0-15  (producers):  RMSNorm, RoPE and ReLU of chunk c+1 while the tensor core works on
+//                             chunk c. Raw q arrives by TMA in one of two q' buffers and q' is
+//                             written back in place; k comes through registers two passes ahead
+//                             and k' is held there until the single k' buffer is free. Features
+//                             are the bulk of the CUDA-core work, so they get most of the warps;
+//   warps 16-23 (converters): two per TMEM lane quarter (32 tile rows), half of the columns each:
+//                             q'.z_{c-1} from the q' tile, P -> masked bf16 P~ written back into
+//                             TMEM (the A operand of P~V) with the row sums of the masked scores,
+//                             S -> S~ in shared memory, then the epilogue O / den from one of two
+//                             O accumulators, staged in the chunk's v buffer;
+//   warp 24     (issuer):     one thread issues the MMAs (P, then QS, KV, PV) and commits them to
+//                             mbarriers;
+//   warp 25     (TMA):        one thread loads raw q two chunks ahead (once both products and the
+//                             converters have read the buffer), writes each staged output tile with
+//                             TMA stores and loads the v tile of two chunks later into the freed
+//                             buffer;
+//   warps 26-27 (z helpers):  z_c = z_{c-1} + the column sums of the bf16 k' tile, into a ring of
+//                             three slots that the converters read.
+// Hand-offs are mbarriers: qfull[2] (TMA -> producers), full[2] (producers -> issuer, converters,
+// helpers), vfull[2] (TMA -> issuer), empty[2] (both products and the converters' q'.z done with a
+// q' buffer), p_done, kv_done, b_done (tensor core -> converters), kfree (k' read by the MMAs and
+// the helpers), pconv / sconv (converters -> issuer: P~ and S~ written), staged[2] / ofree[2]
+// (converters -> TMA thread / issuer), zfull[3] / zempty[3] (the z ring). Every ring has as many
+// phases in flight as its depth, so no waiter can be lapped. Every wait is bounded; a wait that
+// gives up sets RAPT_DEV_INTERNAL in the caller's status word and the CTA winds down.
 //
 // Sequence parallelism: a document is cut into segments of seg_len tokens. Kernel A computes the
 // state increments (K'^T V and sum k') of the parts of the document that precede its last

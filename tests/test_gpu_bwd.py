@@ -127,6 +127,34 @@ def test_varlen_bwd_matches_oracle(cuda_device, lib, dtype, d):
     assert _vec_err(to_host(dgk), rgk) <= TOL[dtype]
 
 
+def test_varlen_bwd_shared_gains_many_documents(cuda_device, lib):
+    """Gains shared by the heads of 64 documents: the gain partials (one per document, head and
+    128-token chunk) are many, so their sum runs in two stages (splits, then the splits in order);
+    checked against the oracle, with every document's dq, dk, dv."""
+    lens = [int(x) for x in np.random.default_rng(380).integers(1, 600, size=64)]
+    lens[5] = 0
+    cu = syn.cu_seqlens_from_lengths(lens)
+    T, H, d = int(cu[-1]), 4, 64
+    q, k, v = draw(381, (T, H, d), "bf16")
+    (g,) = draw(382, (T, H, d), "bf16")[:1]
+    gq, gk = gammas(383, H, d, False)
+    dev = lambda x: torch.from_numpy(x).to(cuda_device)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    dq, dk, dv, dgq, dgk = R.rapt_varlen_bwd(to_dev(q, "bf16"), to_dev(k, "bf16"), to_dev(v, "bf16"),
+                                             to_dev(g, "bf16"), dev(cu), dev(gq), dev(gk),
+                                             max_seqlen=max(lens), dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    wq, wk, wv, wg = (widen(x, "bf16") for x in (q, k, v, g))
+    rq, rk, rv, rgq, rgk = O.rla2_varlen_bwd(wq, wk, wv, wg, cu, gq, gk, EPS_N, BASE, EPS_D)
+    pos = np.concatenate([np.arange(n) for n in lens])
+    assert _row_err(to_host(dq), rq, _keep(wq, gq, pos)) <= TOL["bf16"]
+    assert _row_err(to_host(dk), rk, _keep(wk, gk, pos)) <= TOL["bf16"]
+    assert O.relative_error(to_host(dv), rv)[0] <= TOL["bf16"]
+    assert _vec_err(to_host(dgq), rgq) <= TOL["bf16"]
+    assert _vec_err(to_host(dgk), rgk) <= TOL["bf16"]
+
+
 def test_prefill_bwd_full_size_sampled(cuda_device, lib):
     """The dense prefill workload (B=4, L=4096, H=16, d=128, bf16, per-head gains) in the bench's
     launch configuration; the oracle checks two whole (batch row, head) pairs. The gains' gradients
@@ -220,10 +248,12 @@ def test_varlen_bwd_reports_malformed_cu_seqlens(cuda_device, lib, d, dtype):
     assert _row_err(to_host(dk)[:200], rk, keep_k) <= TOL[dtype]
 
 
-def test_prefill_bwd_tensor_cores_shared_gains_many_segments(cuda_device, lib):
-    """bf16 d = 128 (the tensor-core path) with gains shared by the heads, a RoPE offset and two
-    (batch row, head) pairs only, so that every document is cut into many segments."""
-    B, L, H, d, off = 2, 900, 1, 128, 9
+@pytest.mark.parametrize("d", [64, 128])
+def test_prefill_bwd_tensor_cores_shared_gains_many_segments(cuda_device, lib, d):
+    """bf16 d = 64 or 128 (the tensor-core path; at 64 the tiles carry 64 zero columns) with gains
+    shared by the heads, a RoPE offset and two (batch row, head) pairs only, so that every document
+    is cut into many segments."""
+    B, L, H, off = 2, 900, 1, 9
     q, k, v = draw(360, (B, L, H, d), "bf16")
     (g,) = draw(361, (B, L, H, d), "bf16")[:1]
     gq, gk = gammas(362, H, d, False)
@@ -244,7 +274,8 @@ def test_prefill_bwd_tensor_cores_shared_gains_many_segments(cuda_device, lib):
     assert _vec_err(to_host(dgk), rgk) <= TOL["bf16"]
 
 
-def test_varlen_bwd_multi_block_segments_sampled(cuda_device, lib):
+@pytest.mark.parametrize("d", [64, 128])
+def test_varlen_bwd_multi_block_segments_sampled(cuda_device, lib, d):
     """Tensor-core backward over 4 documents x 16 heads (64 (document, head) pairs, so the plan
     cuts documents into two segments of several blocks each): a full-length document, one whose
     second segment ends inside its first suffix block, one whose second segment ends inside its
@@ -252,7 +283,7 @@ def test_varlen_bwd_multi_block_segments_sampled(cuda_device, lib):
     checks whole (document, head) pairs; positions restart at every document."""
     lens = [4096, 3000, 4005, 1500]
     cu = syn.cu_seqlens_from_lengths(lens)
-    T, H, d = int(cu[-1]), 16, 128
+    T, H = int(cu[-1]), 16
     q, k, v = draw(370, (T, H, d), "bf16")
     (g,) = draw(371, (T, H, d), "bf16")[:1]
     gq, gk = gammas(372, H, d, True)
