@@ -25,10 +25,10 @@
 // Between the passes, the suffix state at each segment's end is the sum of per-block increments
 // R = sum q' gnum^T, w = sum scale q' of the later blocks (bwd_tc_blockstate<false>).
 // Pass B (chunks in reverse; suffix state R = sum q' gnum^T in TMEM, bf16 copy R~, w = sum scale q'):
-//   P = Q'K'^T,  Gv = Gnum V^T                                              (first group)
-//   then, while P~ and A are formed:  dv = K' R~,  R += Q'^T Gnum
-//   P~ = P masked to tau <= t;  A[t][tau] = A'/den, with c = den Gv
-//   dv += P~^T Gnum,  dk' = V R~^T                                           (second group)
+//   P = Q'K'^T,  Cv = G V^T (raw bf16 g and v: c exact)                    (first group)
+//   then, while gnum = g / den, P~ and A are formed:  dv = K' R~
+//   P~ = P masked to tau <= t;  A[t][tau] = A'/den
+//   dv += P~^T Gnum,  R += Q'^T Gnum,  dk' = V R~^T                          (second group)
 //   dk' += A^T Q' (+ w)                                                      (third group)
 //   dk' (bf16) to the workspace, dv out.
 // The passes stage a whole chunk's dq' (pass A) and dk', dv (pass B) in shared memory that the
@@ -530,8 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   row_scalars(s0 + (nch - 1) * kC, rs_next);
   for (int c = nch - 1; c >= 0 && !bad; --c, ++it) {
     const int t0 = s0 + c * kC;
-    // ---- phase 1: q', k' (stored by pass A), v and g by TMA; the row scalars of pass A; gnum =
-    // g / den in place; rows past the document cleared
+    // ---- phase 1: q', k' (stored by pass A), v and g by TMA; the row scalars of pass A; rows
+    // past the document cleared
     if (tid < kC) {
       den_s[tid] = rs_next[0];
       scl_s[tid] = rs_next[1];
@@ -543,33 +543,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       atomicExch(s_abort, 1);
     if (tid == 0) tc::bulk_wait_read0();  // the previous chunk's dk' store has read AS
     __syncthreads();  // den_s
-    for (int idx = tid; idx < kC * 16; idx += kThreads) {
+    for (int idx = tid + (n - t0) * 16; idx < kC * 16; idx += kThreads) {  // (n > t0)
       const int r = idx >> 4, m = idx & 15;
-      const uint32_t ga = base + Lay::GS + tile_off(r, m);
-      if (t0 + r < n) {
-        float f[8];
-        unpack8(lds16(ga), f);
-        const float inv = 1.0f / den_s[r];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] *= inv;
-        sts16(ga, feat::pack8(f));
-      } else {
-        sts16(ga, make_uint4(0, 0, 0, 0));
-        sts16(base + Lay::QF + tile_off(r, m), make_uint4(0, 0, 0, 0));
-        sts16(base + Lay::KF + tile_off(r, m), make_uint4(0, 0, 0, 0));
-        sts16(base + Lay::VS + tile_off(r, m), make_uint4(0, 0, 0, 0));
-      }
+      sts16(base + Lay::GS + tile_off(r, m), make_uint4(0, 0, 0, 0));
+      sts16(base + Lay::QF + tile_off(r, m), make_uint4(0, 0, 0, 0));
+      sts16(base + Lay::KF + tile_off(r, m), make_uint4(0, 0, 0, 0));
+      sts16(base + Lay::VS + tile_off(r, m), make_uint4(0, 0, 0, 0));
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
-    // ---- phase 2: P = Q'K'^T, Gv = Gnum V^T; then, while phase 3 runs on the CUDA cores, the
-    // products that need no P~ or A: dv = K' R~ and R += Q'^T Gnum (R~ in XS is not touched)
+    // ---- phase 2: P = Q'K'^T, Cv = G V^T (from the raw bf16 g and v, so that c = g . v is exact
+    // to fp32 accumulation: A below is a difference of nearly equal terms for keys that few
+    // queries see, the last ones of a document); then, while phase 3 runs on the CUDA cores, the
+    // product that needs no P~, A or gnum: dv = K' R~
     if (tid == 0) {
       constexpr uint32_t ID = tc::idesc_bf16(128, 128, false, false);
-      constexpr uint32_t ID_MM = tc::idesc_bf16(128, 128, true, true);
       constexpr uint32_t ID_KM = tc::idesc_bf16(128, 128, false, true);
 #pragma unroll 1
       for (int kk = 0; kk < kD / 16; ++kk) {
@@ -581,10 +572,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kk = 0; kk < kD / 16; ++kk)
         tc::mma_bf16(tmem + kTDV, kmaj(base + Lay::KF, kk), mnmaj(base + Lay::XS, kk, kD * 128),
                      ID_KM, kk > 0);
-#pragma unroll 1
-      for (int kk = 0; kk < kC / 16; ++kk)
-        tc::mma_bf16(tmem + kTR, mnmaj(base + Lay::QF, kk, 16384), mnmaj(base + Lay::GS, kk, 16384),
-                     ID_MM, 1u);
     }
     {  // meanwhile the partial increment of w = sum_t scale_t q'_t: column i, rows 32 (tid / 128) ..
        // + 31, into the third section of RED (added to w once this chunk's dk' has used it)
@@ -604,16 +591,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       red[(8 + (tid >> 7)) * kC + i] = dw;
     }
     if (!wait_mma(bar1, it & 1)) atomicExch(s_abort, 1);
-    // ---- phase 3: P~ (masked) into AS; A kept in registers
+    // ---- phase 3: gnum = g / den in place (the products that read g are done); P~ (masked) into
+    // AS; A kept in registers
+    for (int idx = tid; idx < kC * 16; idx += kThreads) {
+      const int r = idx >> 4, m = idx & 15;
+      if (t0 + r < n) {
+        const uint32_t ga = base + Lay::GS + tile_off(r, m);
+        float f[8];
+        unpack8(lds16(ga), f);
+        const float inv = 1.0f / den_s[r];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] *= inv;
+        sts16(ga, feat::pack8(f));
+      }
+    }
     const float den = den_s[t], sst = sst_s[t], nst = nst_s[t];
     float pv[32], av[32];
     tmem_ld32(tmem + tl + kTP + 32 * gw, pv);
-    tmem_ld32(tmem + tl + kTG + 32 * gw, av);  // Gnum . v, times den below = g . v
+    tmem_ld32(tmem + tl + kTG + 32 * gw, av);  // c = g . v
     float ps = 0.f, pc = 0.f;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const bool vis = 32 * gw + j <= t;
-      av[j] *= den;
       pv[j] = vis ? pv[j] : 0.f;
       ps += pv[j];
       pc += pv[j] * av[j];
@@ -637,13 +636,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         av[j] = (32 * gw + j <= t) ? num * inv2 : 0.f;
       }
     }
-    // ---- phase 4: dv += P~^T Gnum; dk' = V R~^T (over P, which phase 3 has read)
+    // ---- phase 4: dv += P~^T Gnum; R += Q'^T Gnum (R~ in XS is not touched); dk' = V R~^T (over
+    // P, which phase 3 has read)
     if (tid == 0) {
       constexpr uint32_t ID_MM = tc::idesc_bf16(128, 128, true, true);
       constexpr uint32_t ID_KK = tc::idesc_bf16(128, 128, false, false);
 #pragma unroll 1
       for (int kk = 0; kk < kC / 16; ++kk)
         tc::mma_bf16(tmem + kTDV, mnmaj(base + Lay::AS, kk, 16384), mnmaj(base + Lay::GS, kk, 16384),
+                     ID_MM, 1u);
+#pragma unroll 1
+      for (int kk = 0; kk < kC / 16; ++kk)
+        tc::mma_bf16(tmem + kTR, mnmaj(base + Lay::QF, kk, 16384), mnmaj(base + Lay::GS, kk, 16384),
                      ID_MM, 1u);
 #pragma unroll 1
       for (int kk = 0; kk < kD / 16; ++kk)

@@ -138,7 +138,8 @@ cudaError_t launch_linear_tc(const void* x, const void* w, void* const* outs, in
 // hold them.
 // With sort_docs (varlen, one segment per document), the workspace ends with an int32 order of
 // the documents by decreasing length at order_off, so that the longest (document, head) units
-// are dispatched first.
+// are dispatched first. With pair (d = 64, even H), the prefill kernel takes the heads two at a
+// time, as the 128-column tiles of the [rows, H / 2, 128] view.
 struct TcPlan {
   int nseg_max;
   int seg_len;
@@ -146,6 +147,7 @@ struct TcPlan {
   size_t ws_bytes;
   bool sort_docs;
   size_t order_off;
+  bool pair;
 };
 bool tc_supported(DType dt, int d);
 TcPlan tc_plan(int n_docs, int H, int max_seqlen, long total_tokens, int d, bool varlen);

@@ -108,8 +108,9 @@ struct Prod {
   static constexpr uint32_t TILE = (D / 64) * 16384;  // one 128-row bf16 tile of d columns
 };
 
-// Kernel B shared memory (byte offsets from a 1024-byte aligned base).
-template <int D>
+// Kernel B shared memory (byte offsets from a 1024-byte aligned base). With PAIR (D = 128), the
+// tiles hold two heads of 64 (columns 0-63 and 64-127).
+template <int D, bool PAIR = false>
 struct LayB {
   static constexpr uint32_t TILE = Prod<D>::TILE;
   static constexpr uint32_t Q0 = 0, Q1 = TILE;                 // raw q (TMA), turned into q' in place
@@ -128,9 +129,13 @@ struct LayB {
   static constexpr uint32_t MISC = BAR + NBAR * 8;             // TMEM base, abort flag
   static constexpr uint32_t BYTES = MISC + 16;
   // TMEM columns: P (fp32 scores; the bf16 P~ is written over columns [0, 32) and [64, 96)), two
-  // O accumulators, S
-  static constexpr uint32_t TP = 0, TO0 = 128, TO1 = 128 + D, TS = 128 + 2 * D;
+  // O accumulators, S. PAIR: the two heads' scores (P~ over the first 64 columns of each), one
+  // O accumulator for both heads, S.
+  static constexpr uint32_t TP = 0, TP1 = 128;
+  static constexpr uint32_t TO0 = PAIR ? 256 : 128, TO1 = PAIR ? 256 : 128 + D;
+  static constexpr uint32_t TS = PAIR ? 384 : 128 + 2 * D;
   static_assert(TS + D <= 512, "TMEM budget");
+  static_assert(!PAIR || D == 128, "head pairs fill 128-column tiles");
   static_assert(BYTES <= 232448, "shared memory budget");
 };
 
@@ -153,33 +158,41 @@ struct LayA {
 
 // Initial state of a segment for columns [c0, c0 + D/2) of the calling thread's TMEM lane er:
 // S0 (if any) + the increments of the first nblk blocks, in block order, into the fp32 state in
-// TMEM (tmem_s: lane and column base of S) and its bf16 copy S~ in shared memory (ss); TMEM rows
-// >= D are zeroed. Eight columns at a time, with two blocks' loads in flight.
-template <int D>
-__device__ __forceinline__ void init_state(const PrefillArgs& a, const float* wsb, int nblk, long bh,
-                                           int er, uint32_t tmem_s, uint32_t ss, int c0) {
+// TMEM (tmem_s: lane and column base of S) and its bf16 copy S~ in shared memory (ss). Heads of DH
+// (= D, or 64 for a pair of heads in a 128-wide tile): lane er is row er % DH of head er / DH (bh +
+// er / DH, whose records start rec_head floats after the first head's), and the state is block
+// diagonal: columns of the other head, and TMEM rows >= D of a single head, are zero. Eight
+// columns at a time, with two blocks' loads in flight.
+template <int D, int DH = D>
+__device__ __forceinline__ void init_state(const PrefillArgs& a, const float* wsb, long rec_head,
+                                           int nblk, long bh, int er, uint32_t tmem_s, uint32_t ss,
+                                           int c0) {
+  const int hh = DH == D ? 0 : er / DH, r = DH == D ? er : er % DH;
+  const bool live = DH == D ? er < D : c0 / DH == hh;
+  const float* wh = wsb + hh * rec_head;
 #pragma unroll 1
   for (int j0 = c0; j0 < c0 + D / 2; j0 += 8) {
+    const int jh = j0 - hh * DH;  // column within the head
     float v[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) v[e] = 0.f;
-    if (er < D) {
+    if (live) {
       if (a.S0 != nullptr) {
-        const float4* src = reinterpret_cast<const float4*>(a.S0 + (bh * D + er) * D + j0);
+        const float4* src = reinterpret_cast<const float4*>(a.S0 + ((bh + hh) * DH + r) * DH + jh);
         const float4 x0 = src[0], x1 = src[1];
         v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
         v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
       }
-      const float4* inc = reinterpret_cast<const float4*>(wsb) + (j0 / 4) * D + er;
-      constexpr long R4 = Rec<D>::FLOATS / 4;
+      const float4* inc = reinterpret_cast<const float4*>(wh) + (jh / 4) * DH + r;
+      constexpr long R4 = Rec<DH>::FLOATS / 4;
 #pragma unroll 1
       for (int g = 0; g < nblk; g += 2) {
         const bool two = g + 1 < nblk;
-        const float4 x0 = __ldcg(inc + g * R4), x1 = __ldcg(inc + g * R4 + D);
+        const float4 x0 = __ldcg(inc + g * R4), x1 = __ldcg(inc + g * R4 + DH);
         float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
         if (two) {
           y0 = __ldcg(inc + (g + 1) * R4);
-          y1 = __ldcg(inc + (g + 1) * R4 + D);
+          y1 = __ldcg(inc + (g + 1) * R4 + DH);
         }
         v[0] += x0.x; v[1] += x0.y; v[2] += x0.z; v[3] += x0.w;
         v[4] += x1.x; v[5] += x1.y; v[6] += x1.z; v[7] += x1.w;
@@ -249,21 +262,28 @@ __device__ __forceinline__ float qz_half(const uint8_t* qb, const float* z, int 
 }
 
 // ------------------------------------------------------------------------------------------------
-// Kernel B: one CTA per (document, head, segment).
-template <int D>
+// Kernel B: one CTA per (document, head, segment). With PAIR (d = 64 heads, D = 128), one CTA per
+// (document, pair of heads 2h and 2h + 1, segment): the q, k, v and output tiles of the pair are
+// the 128-column tiles of the [rows, H / 2, 128] view of the tensors; each head has its own
+// RMSNorm, gains, scores, denominators and state (the state and S~ are block diagonal, so one
+// product Q'S~ serves both heads), and the two P~V products write the two halves of O.
+template <int D, bool PAIR>
 __global__ void __launch_bounds__(kThreadsB, 1)
     prefill_tc_kernel(const TcArgs ta, const __grid_constant__ CUtensorMap tmap_q,
                       const __grid_constant__ CUtensorMap tmap_v,
                       const __grid_constant__ CUtensorMap tmap_o) {
-  using L = LayB<D>;
+  using L = LayB<D, PAIR>;
   using PM = Prod<D>;
   constexpr int TPR = PM::TPR, RPP = PM::RPP, NPASS = PM::NPASS;
+  constexpr int DH = PAIR ? D / 2 : D;  // head size
+  constexpr int NH = PAIR ? 2 : 1;      // heads per CTA
   const PrefillArgs& a = ta.p;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int HV = a.H / NH;  // heads of the tile view
   const int seg = blockIdx.x % ta.nseg_max;
-  const int h = (blockIdx.x / ta.nseg_max) % a.H;
-  const int slot = blockIdx.x / (ta.nseg_max * a.H);
+  const int h = (blockIdx.x / ta.nseg_max) % HV;  // view head: heads NH h .. NH h + NH - 1
+  const int slot = blockIdx.x / (ta.nseg_max * HV);
   const int doc = ta.order != nullptr ? ta.order[slot] : slot;
 
   long row0;
@@ -276,7 +296,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const int seg_n = min(ta.seg_len, n - seg_start);  // 0 only for an empty document
   const int nchunks = (seg_n + kC - 1) / kC;
   const bool last_seg = seg == nseg_doc - 1;
-  const long bh = static_cast<long>(doc) * a.H + h;
+  const long bh = static_cast<long>(doc) * a.H + NH * h;  // (document, head) index of the first head
 
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t base = tc::smem_u32(smem);
@@ -325,12 +345,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     for (int i = tid; i < 16384 / 16; i += kThreadsB) sts16(base + L::KS + 16384 + i * 16, make_uint4(0, 0, 0, 0));
   }
   const FeatTab tab = feat_tab<D>(smem + L::TAB);
-  fill_tab<D>(tab, a, h, RPP, tid, kThreadsB);
+  fill_tab<D, DH>(tab, a, NH * h, RPP, tid, kThreadsB);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *s_tmem;
-  const float* wsb = ta.ws + bh * ta.nblk_max * Rec<D>::FLOATS;
+  const long rec_head = ta.nblk_max * Rec<DH>::FLOATS;  // records of one (document, head)
+  const float* wsb = ta.ws + bh * rec_head;
   const int nblk = seg * ta.blk_per_seg;  // increment blocks before this segment
 
   if (warp < kProd / 32) {
@@ -346,7 +367,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     static_assert(NPASS % RK == 0, "k load ring");
     const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(a.k);
     const int pos_base = a.pos_offset + seg_start;
-    const long rstride = static_cast<long>(a.H) * D;  // elements from one token row to the next
+    const long rstride = static_cast<long>(HV) * D;  // elements from one token row to the next
     const __nv_bfloat16* krow = kg + (row0 + seg_start + prow) * rstride + static_cast<long>(h) * D + e0;
     auto load = [&](int c, int p, uint4& xk) {
       if (c * kC + p * RPP + prow < seg_n) xk = ldg16(krow + static_cast<long>(c * kC + p * RPP) * rstride);
@@ -401,9 +422,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         }
         Pairs fq = unpack_pairs(xq), fk = unpack_pairs(xk);
         const float rq2 = sumsq(fq), rk2 = sumsq(fk);
-        const float sq = row_sum<TPR>(rq2), sk = row_sum<TPR>(rk2);
-        const float rinvq = valid ? rsqrtf(sq * (1.0f / D) + a.fa.eps_norm) : 0.f;
-        const float rinvk = valid ? rsqrtf(sk * (1.0f / D) + a.fa.eps_norm) : 0.f;
+        // (the 16-byte chunks of one head of a row are TPR / NH consecutive lanes)
+        const float sq = row_sum<TPR / NH>(rq2), sk = row_sum<TPR / NH>(rk2);
+        const float rinvq = valid ? rsqrtf(sq * (1.0f / DH) + a.fa.eps_norm) : 0.f;
+        const float rinvk = valid ? rsqrtf(sk * (1.0f / DH) + a.fa.eps_norm) : 0.f;
         {
           float2 g0[2], g1[2];
           split_load<D>(tab.gq, part, g0, g1);
@@ -436,7 +458,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const int j_lo = hf * (D / 2), j_hi = j_lo + D / 2;
     // initial state of this half of the columns: S (TMEM) and S~ (completion 0 of sconv)
     if (nblk > 0) tc::grid_dep_wait();
-    init_state<D>(a, wsb, nblk, bh, er, tmem + tl + L::TS, base + L::SS, j_lo);
+    init_state<D, DH>(a, wsb, rec_head, nblk, bh, er, tmem + tl + L::TS, base + L::SS, j_lo);
     tc::tmem_wait_st();
     tc::fence_async_smem();
     tc::fence_before_sync();
@@ -462,18 +484,23 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       float rs = 0.f;
       if (!bad) {
         // Key groups of 32: left of this warp's rows (col < 32 q4) fully visible, col == 32 q4 the
-        // diagonal, the rest above it (all zero). This half's keys [64 hf, 64 hf + 64) become the
-        // bf16 pairs in TMEM columns [64 hf, 64 hf + 32).
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          const int col = 64 * hf + 32 * g;
+        // diagonal, the rest above it (all zero). One head: this half's keys [64 hf, 64 hf + 64)
+        // become the bf16 pairs in TMEM columns [64 hf, 64 hf + 32). A pair of heads: all 128 keys
+        // of head hf's scores become the bf16 pairs in the first 64 of its columns (group g is
+        // written over columns that group g - 1 or g itself has already read).
+        constexpr int NG = PAIR ? 4 : 2;
+        const uint32_t tp = tmem + tl + (PAIR ? (hf ? L::TP1 : L::TP) : L::TP);
+#pragma unroll(PAIR ? 1 : NG)
+        for (int g = 0; g < NG; ++g) {
+          const int col = PAIR ? 32 * g : 64 * hf + 32 * g;
+          const int dst = PAIR ? 16 * g : 64 * hf + 16 * g;
           if (col > 32 * q4) {  // warp-uniform: strictly above the diagonal
             uint32_t zero[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) zero[e] = 0u;
-            tc::tmem_st16(tmem + tl + L::TP + 64 * hf + 16 * g, zero);
+            tc::tmem_st16(tp + dst, zero);
           } else {
-            convert_p_group(tmem + tl + L::TP, col, 64 * hf + 16 * g, er, col == 32 * q4, rs);
+            convert_p_group(tp, col, dst, er, col == 32 * q4, rs);
           }
         }
         tc::tmem_wait_st();
@@ -485,7 +512,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       ok = tc::mbar_wait(bar_kv, c & 1, kWaitCycles);
       if (__any_sync(0xffffffffu, !ok)) bad = 1;
       tc::fence_after_sync();
-      if (!bad && 32 * q4 < D) {
+      if (!bad && (PAIR ? (q4 >> 1) == hf : 32 * q4 < D)) {
 #pragma unroll 1
         for (int j0 = j_lo; j0 < j_hi; j0 += 32) {
           uint32_t u[2][16];
@@ -510,7 +537,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       // ---- out = O / (q'.z_{c-1} + rowsum(P) + eps), this half's columns
       ok = tc::mbar_wait(bar_b, c & 1, kWaitCycles);
       if (__any_sync(0xffffffffu, !ok)) bad = 1;
-      tc::named_sync(kBarQuarter + q4, 64);  // the other half's q'.z and row sums are written
+      // one head: the other half's q'.z and row sums are written (a pair: each half is one head)
+      if (!PAIR) tc::named_sync(kBarQuarter + q4, 64);
       // A whole chunk is staged in its v buffer (free: v was read by the finished MMAs) in the box
       // layout of the output tensor map and written by TMA in full 128-byte lines; the ragged last
       // chunk of a document is written row by row (its tile would reach past it).
@@ -518,12 +546,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       const uint32_t ob = base + (s ? L::V1 : L::V0);
       if (!bad) {
         tc::fence_after_sync();
-        const float den = di[(2 * s) * kC + er] + di[(2 * s + 1) * kC + er] +
-                          rsm[(2 * s) * kC + er] + rsm[(2 * s + 1) * kC + er] + a.eps_den;
+        const float den = PAIR ? di[(2 * s + hf) * kC + er] + rsm[(2 * s + hf) * kC + er] + a.eps_den
+                               : di[(2 * s) * kC + er] + di[(2 * s + 1) * kC + er] +
+                                     rsm[(2 * s) * kC + er] + rsm[(2 * s + 1) * kC + er] + a.eps_den;
         const uint32_t to = tmem + tl + (s ? L::TO1 : L::TO0);
         const float inv = 1.0f / den;
         const int lt = c * kC + er;
-        __nv_bfloat16* orow = og + ((row0 + seg_start + lt) * a.H + h) * D;
+        __nv_bfloat16* orow = og + ((row0 + seg_start + lt) * HV + h) * D;
 #pragma unroll 1
         for (int j0 = j_lo; j0 < j_hi; j0 += 32) {
           uint32_t u[2][16];
@@ -551,18 +580,19 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       }
       tc::fence_before_sync();
       tc::mbar_arrive(bar_staged + 8 * s);  // the store thread takes it from here
-      tc::mbar_arrive(bar_ofree + 8 * s);   // the O accumulator may take chunk c + 2
+      tc::mbar_arrive(bar_ofree + (PAIR ? 0 : 8 * s));  // the O accumulator may take chunk c + 2 (a pair: c + 1)
       if (bad) atomicExch(s_abort, 1);
       if (group_sync_or(kBarConv, kConv, *s_abort)) break;
     }
     if (bad) atomicExch(s_abort, 1);
-    if (last_seg && a.S_final != nullptr && !*s_abort && 32 * q4 < D) {
+    if (last_seg && a.S_final != nullptr && !*s_abort && (PAIR ? (q4 >> 1) == hf : 32 * q4 < D)) {
       tc::fence_after_sync();
+      const int hh = PAIR ? hf : 0, r = PAIR ? er % DH : er;  // the diagonal block of head hh
       for (int j0 = j_lo; j0 < j_hi; j0 += 16) {
         uint32_t u[16];
         tc::tmem_ld16(tmem + tl + L::TS + j0, u);
         tc::tmem_wait_ld();
-        float4* dst = reinterpret_cast<float4*>(a.S_final + (bh * D + er) * D + j0);
+        float4* dst = reinterpret_cast<float4*>(a.S_final + ((bh + hh) * DH + r) * DH + j0 - hh * DH);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           dst[e] = make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
@@ -577,7 +607,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       constexpr uint32_t ID_P = tc::idesc_bf16(128, 128, false, false);
       constexpr uint32_t ID_QS = tc::idesc_bf16(128, D, false, true);
       constexpr uint32_t ID_KV = tc::idesc_bf16(128, D, true, true);
-      constexpr uint32_t ID_PV = tc::idesc_bf16(128, D, false, true);
+      constexpr uint32_t ID_PV = tc::idesc_bf16(128, DH, false, true);
       int ok = 1;
       // descriptors: k-major operands advance 32 bytes per K=16 step inside a 64-column block and
       // 16 KB per block; MN-major operands advance 2 KB (16 rows) per step
@@ -594,16 +624,19 @@ __global__ void __launch_bounds__(kThreadsB, 1)
              tc::mbar_wait(bar_vfull + 8 * s, ph, kWaitCycles);
         if (!ok) break;
         tc::fence_after_sync();
-        // P = Q' K'^T (the converters turn it into P~ while the next two products run)
+        // P = Q' K'^T (the converters turn it into P~ while the next two products run); a pair of
+        // heads: Q'_h K'_h^T over each head's 64 feature columns, into the head's own columns
 #pragma unroll 1
         for (int k = 0; k < D / 16; ++k) {
           const uint64_t kofs = static_cast<uint64_t>((k / 4) * 1024 + (k % 4) * 2);
-          tc::mma_bf16(tmem + L::TP, d_q + kofs, d_ks_k + kofs, ID_P, k > 0);
+          const uint32_t tp = tmem + (PAIR && k >= 4 ? L::TP1 : L::TP);
+          tc::mma_bf16(tp, d_q + kofs, d_ks_k + kofs, ID_P, PAIR ? (k % 4) > 0 : k > 0);
         }
         tc::mma_commit(bar_p);
         // O = Q' S~_{c-1}, once S~ holds the state before this chunk and the O buffer is free
         ok = tc::mbar_wait(bar_sconv, c & 1, kWaitCycles) &&
-             (c < 2 || tc::mbar_wait(bar_ofree + 8 * s, ((c >> 1) + 1) & 1, kWaitCycles));
+             (PAIR ? (c < 1 || tc::mbar_wait(bar_ofree, (c - 1) & 1, kWaitCycles))
+                   : (c < 2 || tc::mbar_wait(bar_ofree + 8 * s, ((c >> 1) + 1) & 1, kWaitCycles)));
         if (!ok) break;
         tc::fence_after_sync();
 #pragma unroll 1
@@ -620,14 +653,21 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         }
         tc::mma_commit(bar_kv);
         tc::mma_commit(bar_kfree);
-        // O += P~ V, with P~ read from TMEM (keys 16 k .. 16 k + 15 in columns 64 (k / 4) + 8 (k % 4))
+        // O += P~ V, with P~ read from TMEM (keys 16 k .. 16 k + 15 in columns 64 (k / 4) + 8 (k % 4);
+        // a pair of heads: in columns 8 k of the head's scores, and each head's product takes its
+        // own 64 columns of v and writes its own half of O)
         ok = tc::mbar_wait(bar_pconv, c & 1, kWaitCycles);
         if (!ok) break;
         tc::fence_after_sync();
 #pragma unroll 1
-        for (int k = 0; k < kC / 16; ++k) {
-          tc::mma_bf16_ta(to, tmem + L::TP + 64 * (k / 4) + 8 * (k % 4),
-                          d_v + static_cast<uint64_t>(k) * 128, ID_PV, 1u);
+        for (int hh = 0; hh < NH; ++hh) {
+#pragma unroll 1
+          for (int k = 0; k < kC / 16; ++k) {
+            const uint32_t pa = PAIR ? tmem + (hh ? L::TP1 : L::TP) + 8 * k
+                                     : tmem + L::TP + 64 * (k / 4) + 8 * (k % 4);
+            tc::mma_bf16_ta(to + 64 * hh, pa, d_v + static_cast<uint64_t>(hh) * 1024 + static_cast<uint64_t>(k) * 128,
+                            ID_PV, 1u);
+          }
         }
         tc::mma_commit(bar_b);
       }
@@ -694,13 +734,15 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     float z0 = 0.f, z1 = 0.f;
     if (own) {
       if (nblk > 0) tc::grid_dep_wait();
+      const int hh = (2 * ht) / DH, cz = (2 * ht) % DH;  // head and its column
       if (a.z0 != nullptr) {
-        z0 = a.z0[bh * D + 2 * ht];
-        z1 = a.z0[bh * D + 2 * ht + 1];
+        z0 = a.z0[(bh + hh) * DH + cz];
+        z1 = a.z0[(bh + hh) * DH + cz + 1];
       }
+      const float* wz = wsb + hh * rec_head + Rec<DH>::Z + cz;
       for (int g = 0; g < nblk; ++g) {
-        z0 += __ldcg(wsb + g * Rec<D>::FLOATS + Rec<D>::Z + 2 * ht);
-        z1 += __ldcg(wsb + g * Rec<D>::FLOATS + Rec<D>::Z + 2 * ht + 1);
+        z0 += __ldcg(wz + g * Rec<DH>::FLOATS);
+        z1 += __ldcg(wz + g * Rec<DH>::FLOATS + 1);
       }
       zs[2 * ht] = z0;  // slot 0: z before the segment, read by chunk 0
       zs[2 * ht + 1] = z1;
@@ -750,8 +792,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     if (bad) atomicExch(s_abort, 1);
     tc::named_sync(kBarHelp, kHelp);
     if (last_seg && a.z_final != nullptr && !*s_abort && own) {
-      a.z_final[bh * D + 2 * ht] = z0;
-      a.z_final[bh * D + 2 * ht + 1] = z1;
+      const int hh = (2 * ht) / DH, cz = (2 * ht) % DH;
+      a.z_final[(bh + hh) * DH + cz] = z0;
+      a.z_final[(bh + hh) * DH + cz + 1] = z1;
     }
   }
   }
@@ -1021,18 +1064,24 @@ cudaError_t launch_state_d(const TcArgs& ta, const CUtensorMap& tmap_k, const CU
   return cudaGetLastError();
 }
 
-template <int D>
+// Kernel B with head size D (PAIR: two heads of 64 per CTA, tiles of the [rows, H / 2, 128] view),
+// after kernel A (single heads of the tensors' own size) where segments need their start states.
+template <int D, bool PAIR>
 cudaError_t launch_tc_d(const TcArgs& ta, cudaStream_t stream) {
+  constexpr int DT = PAIR ? 2 * D : D;  // tile width
+  constexpr int NH = PAIR ? 2 : 1;
   static unsigned long long cfg_b = 0;
-  cudaError_t e = set_smem(prefill_tc_kernel<D>, LayB<D>::BYTES, cfg_b);
+  cudaError_t e = set_smem(prefill_tc_kernel<DT, PAIR>, LayB<DT, PAIR>::BYTES, cfg_b);
   if (e != cudaSuccess) return e;
-  const long units = static_cast<long>(ta.p.n_docs) * ta.p.H;
+  const long units = static_cast<long>(ta.p.n_docs) * (ta.p.H / NH);
   if (units == 0) return cudaSuccess;
   CUtensorMap tmap_q, tmap_v, tmap_o;
-  if (ta.p.v != nullptr && ta.p.total_rows > 0) {
-    e = make_rows_map(&tmap_q, ta.p.q, ta.p.total_rows, ta.p.H, D);
-    if (e == cudaSuccess) e = make_rows_map(&tmap_v, ta.p.v, ta.p.total_rows, ta.p.H, D);
-    if (e == cudaSuccess) e = make_rows_map(&tmap_o, ta.p.out, ta.p.total_rows, ta.p.H, D);
+  const bool rows = ta.p.v != nullptr && ta.p.total_rows > 0;
+  if (rows) {
+    const int hv = ta.p.H / NH;
+    e = make_rows_map(&tmap_q, ta.p.q, ta.p.total_rows, hv, DT);
+    if (e == cudaSuccess) e = make_rows_map(&tmap_v, ta.p.v, ta.p.total_rows, hv, DT);
+    if (e == cudaSuccess) e = make_rows_map(&tmap_o, ta.p.out, ta.p.total_rows, hv, DT);
     if (e != cudaSuccess) return e;
   } else {
     memset(&tmap_q, 0, sizeof(tmap_q));  // no rows: the kernels issue no copy
@@ -1041,23 +1090,24 @@ cudaError_t launch_tc_d(const TcArgs& ta, cudaStream_t stream) {
   }
   const bool with_a = ta.nblk_max > 0;
   if (with_a) {
-    CUtensorMap tmap_k;
+    CUtensorMap tmap_k, tmap_va;
     e = make_rows_map(&tmap_k, ta.p.k, ta.p.total_rows, ta.p.H, D);
-    if (e == cudaSuccess) e = launch_state_d<D>(ta, tmap_k, tmap_v, stream);
+    if (e == cudaSuccess) e = make_rows_map(&tmap_va, ta.p.v, ta.p.total_rows, ta.p.H, D);
+    if (e == cudaSuccess) e = launch_state_d<D>(ta, tmap_k, tmap_va, stream);
     if (e != cudaSuccess) return e;
   }
   // kernel B as a programmatic dependent of kernel A (only then: it must not overlap anything else)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(units * ta.nseg_max));
   cfg.blockDim = dim3(kThreadsB);
-  cfg.dynamicSmemBytes = LayB<D>::BYTES;
+  cfg.dynamicSmemBytes = LayB<DT, PAIR>::BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = with_a ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D>, ta, tmap_q, tmap_v, tmap_o);
+  e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<DT, PAIR>, ta, tmap_q, tmap_v, tmap_o);
   note_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -1067,13 +1117,17 @@ cudaError_t launch_tc_d(const TcArgs& ta, cudaStream_t stream) {
 
 bool tc_supported(DType dt, int d) { return dt == DType::BF16 && (d == 64 || d == 128); }
 
-TcPlan tc_plan(int n_docs, int H, int max_seqlen, long total_tokens, int d, bool varlen) {
+TcPlan tc_plan(int n_docs, int H_heads, int max_seqlen, long total_tokens, int d, bool varlen) {
+  // d = 64 with an even head count: kernel B takes the heads in pairs (one 128-wide tile), so it
+  // has half the units, each costing about one d = 128 chunk per chunk; kernel A stays per head.
+  const bool pair = d == 64 && H_heads % 2 == 0;
+  const int H = pair ? H_heads / 2 : H_heads;  // kernel B units per document
   // Estimated time in units of one kernel-B chunk. Kernel B runs one CTA per SM (waves of 152
   // CTAs, each costing its chunks plus about one chunk of state set-up); a kernel-A chunk (k
   // features and one GEMM) costs about half a kernel-B chunk, also one CTA per SM. Documents are
   // assumed to share the tokens evenly, except that the longest one bounds the segment count.
   // More segments or blocks cost workspace, so a longer plan must be clearly (5 %) faster to win.
-  TcPlan best{1, kC, 1, 0, false, 0};
+  TcPlan best{1, kC, 1, 0, false, 0, pair};
   const int chunks_max = max_seqlen > 0 ? (max_seqlen + kC - 1) / kC : 1;
   const double avg_chunks = n_docs > 0 ? static_cast<double>(total_tokens) / n_docs / kC : 0.0;
   double best_cost = 1e300;
@@ -1084,8 +1138,8 @@ TcPlan tc_plan(int n_docs, int H, int max_seqlen, long total_tokens, int d, bool
   {
     const double total_chunks = static_cast<double>(H) * (static_cast<double>(total_tokens) / kC + 0.5 * n_docs);
     const double cost1 = (chunks_max > total_chunks / 152 ? chunks_max : total_chunks / 152) + 1.0;
-    if (varlen && cost1 <= 1.15 * (total_chunks / 152 + 1.0)) {
-      best = TcPlan{1, chunks_max * kC, 1, 0, n_docs <= 1024, 0};
+    if (varlen && cost1 <= (pair ? 1.2 : 1.15) * (total_chunks / 152 + 1.0)) {
+      best = TcPlan{1, chunks_max * kC, 1, 0, n_docs <= 1024, 0, pair};
       best_cost = 0.0;  // taken: no split plan below can beat the spread of the work
     }
   }
@@ -1099,23 +1153,23 @@ TcPlan tc_plan(int n_docs, int H, int max_seqlen, long total_tokens, int d, bool
     const double waves_b = static_cast<double>(static_cast<long>((items_b + 151) / 152));
     for (int f = 1; f <= 8 && nseg > 1; f *= 2) {
       if (seg_chunks % f != 0) break;
-      const double items_a = (items_b - static_cast<double>(H) * n_docs) * f;
+      const double items_a = (items_b - static_cast<double>(H) * n_docs) * f * (pair ? 2 : 1);
       const double waves_a = items_a > 0 ? static_cast<double>(static_cast<long>((items_a + 151) / 152)) : 0.0;
       const double cost = waves_b * (seg_chunks + 1.0) + waves_a * (0.5 * seg_chunks / f + 0.5);
       if (cost < 0.95 * best_cost) {
         best_cost = cost;
-        best = TcPlan{nseg, seg_chunks * kC, f, 0};
+        best = TcPlan{nseg, seg_chunks * kC, f, 0, false, 0, pair};
       }
     }
     if (nseg == 1) {
       const double cost = waves_b * (seg_chunks + 1.0);
       if (cost < 0.95 * best_cost) {
         best_cost = cost;
-        best = TcPlan{1, seg_chunks * kC, 1, 0};
+        best = TcPlan{1, seg_chunks * kC, 1, 0, false, 0, pair};
       }
     }
   }
-  const long units = static_cast<long>(n_docs) * H;
+  const long units = static_cast<long>(n_docs) * H_heads;  // kernel A's records are per head
   const long rec = static_cast<long>(d) * (d + 1);
   best.ws_bytes = best.nseg_max > 1 ? static_cast<size_t>(units) * (best.nseg_max - 1) *
                                           best.blk_per_seg * rec * sizeof(float)
@@ -1162,7 +1216,8 @@ cudaError_t launch_prefill_tc(int d, const PrefillArgs& a, const TcPlan& plan, f
     if (e != cudaSuccess) return e;
     ta.order = order;
   }
-  return d == 128 ? launch_tc_d<128>(ta, stream) : launch_tc_d<64>(ta, stream);
+  if (d == 128) return launch_tc_d<128, false>(ta, stream);
+  return plan.pair ? launch_tc_d<64, true>(ta, stream) : launch_tc_d<64, false>(ta, stream);
 }
 
 }  // namespace rapt

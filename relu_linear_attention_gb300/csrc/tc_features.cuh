@@ -217,18 +217,22 @@ template <int D>
 __device__ __forceinline__ int split_idx(int i) {
   return (i & 4) * (D / 8) + (i >> 3) * 4 + (((i & 1) << 1) | ((i >> 1) & 1));
 }
-template <int D>
+// A row of D elements holds D / DH heads of DH elements (heads h, h + 1, ...: two heads of 64 in a
+// 128-wide tile, or one head), each with its own gains and the same RoPE frequencies.
+template <int D, int DH = D>
 __device__ __forceinline__ void fill_tab(const FeatTab& t, const PrefillArgs& a, int h, int rpp,
                                          int tid, int nthreads) {
   for (int i = tid; i < D; i += nthreads) {
-    t.gq[split_idx<D>(i)] = a.gamma_q[h * a.fa.gamma_stride + i];
-    t.gk[split_idx<D>(i)] = a.gamma_k[h * a.fa.gamma_stride + i];
+    const long gi = static_cast<long>(h + i / DH) * a.fa.gamma_stride + i % DH;
+    t.gq[split_idx<D>(i)] = a.gamma_q[gi];
+    t.gk[split_idx<D>(i)] = a.gamma_k[gi];
   }
   for (int j = tid; j < D / 2; j += nthreads) {
-    t.fhi[j] = a.fa.rope_hi[j];
-    t.flo[j] = a.fa.rope_lo[j];
+    const int jh = j % (DH / 2);
+    t.fhi[j] = a.fa.rope_hi[jh];
+    t.flo[j] = a.fa.rope_lo[jh];
     float sn, cs;
-    rope_sincos(rpp, a.fa.rope_hi[j], a.fa.rope_lo[j], sn, cs);
+    rope_sincos(rpp, a.fa.rope_hi[jh], a.fa.rope_lo[jh], sn, cs);
     t.stc[j] = cs;
     t.sts[j] = sn;
   }

@@ -28,6 +28,9 @@ PREFILL_CASES = [
     (1, 130, 3, 128, "bf16", True, 17, True),
     (3, 384, 2, 128, "bf16", True, 0, False),
     (1, 2, 1, 32, "bf16", False, 0, False),
+    (2, 3000, 4, 64, "bf16", True, 5, True),   # heads in pairs, several segments per row
+    (3, 200, 6, 64, "bf16", False, 9, False),  # heads in pairs, gains shared by the heads
+    (1, 300, 3, 64, "bf16", False, 0, True),   # odd head count: one head per CTA
 ]
 
 
