@@ -178,6 +178,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 
 // TMA: copies one box of a 3-D tensor map (coordinates x innermost) into shared memory; the bytes
 // are reported to the mbarrier. x * element size must be a multiple of 16 bytes.
+// Starts fetching a 3-D box into L2 (no shared memory, no completion): a later load of the same box
+// finds it there.
+__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z,
                                             uint32_t bar) {
   asm volatile(
