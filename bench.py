@@ -463,8 +463,9 @@ def run_gpu(args, rank, world, local):
                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": v_bytes / (v_mean * 1e-3) / 1e9 / peaks["hbm_gbs"],
                            "traffic": read_traffic("varlen", "doc_order_kernel", "prefill_tc_kernel"),
-                           "kernels": "doc_order_kernel + prefill_tc_kernel<64> (one call: one segment "
-                                      "per document, longest first)"}}
+                           "kernels": "doc_order_kernel + prefill_tc_kernel<128, true> (one call: the "
+                                      "d = 64 heads two per CTA, one segment per document, longest "
+                                      "first)"}}
     # its backward (dq, dk, dv, dgamma; the tensor-core passes on 128-column tiles, 64 of them zero)
     vg = torch.empty_like(vq).normal_(generator=torch.Generator(device=device).manual_seed(6))
     vws = torch.empty(lib.rapt_varlen_bwd_workspace_size(wv.T, len(wv.lengths), 32, 64, msl, 1),
@@ -523,7 +524,6 @@ def run_gpu(args, rank, world, local):
                                 counter=lib.rapt_launch_counter)
     c_mean = max_over_ranks(statistics.fmean(c_ms), device)
     c_flops = 2 * 16384 * 16 * (8 * 128 * 128 + 2 * 128)  # q'S, q'A q', S and A updates
-    fp32_peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
     c_bytes = prefill_bytes(2, 16384, 16, 128)
     l2_causal = {"value": world * 2 * 16384 / (c_mean * 1e-3), "unit": "tokens/s",
                  "ms_per_step": c_mean,
@@ -534,8 +534,7 @@ def run_gpu(args, rank, world, local):
                               "frac": c_bytes / (c_mean * 1e-3) / 1e9 / peaks["hbm_gbs"],
                               "algorithmic_bytes_per_call": c_bytes,
                               "algorithmic_flops_per_call": c_flops,
-                              "fp32_alu_frac": c_flops / (c_mean * 1e-3) / 1e12 / fp32_peak,
-                              "fp32_alu_peak_source": "152 SMs x 128 lanes x 2 flop x max SM clock",
+                              "tensor_tflops_algorithmic": c_flops / (c_mean * 1e-3) / 1e12,
                               "traffic": read_traffic("l2_causal", "l2_tc_moments", "l2c_tc_kernel"),
                               "kernels": "l2_tc_moments + l2c_tc_kernel (one call; tensor cores)"}}
     del lq, lk, lv, lo, ws, wl
