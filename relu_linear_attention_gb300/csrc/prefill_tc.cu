@@ -374,6 +374,11 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       else xk = make_uint4(0, 0, 0, 0);
     };
     Rot rot;  // RoPE cos / sin of this thread's current row
+    // rotation by RPP positions (one pass further down the chunk): held in registers for one head
+    // per CTA; re-read from the table each pass for a pair of heads (its producers have no
+    // registers to spare)
+    Rot step_held;
+    if constexpr (!PAIR) tab_step(tab, e0 / 2, step_held);
     uint4 rk[RK];
     if (nchunks > 0) {
 #pragma unroll
@@ -401,10 +406,12 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       // incremental rotation from the previous chunk's last pass (RPP positions further down)
       if ((c & 7) == 0) {
         tab_rot_at(tab, pos_base + c * kC + prow, e0 / 2, rot);
+      } else if constexpr (PAIR) {
+        Rot st;
+        tab_step(tab, e0 / 2, st);
+        rot_step(rot, st);
       } else {
-        Rot step;
-        tab_step(tab, e0 / 2, step);
-        rot_step(rot, step);
+        rot_step(rot, step_held);
       }
       uint4 xq_next = ld_shared16(smem, qb - base + cblk + tc::sw128(prow, cidx));
 #pragma unroll
@@ -416,9 +423,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         const int r = p * RPP + prow;
         const bool valid = c * kC + r < seg_n;
         if (p > 0) {
-          Rot step;  // rotation by RPP positions (one pass further down the chunk)
-          tab_step(tab, e0 / 2, step);
-          rot_step(rot, step);
+          if constexpr (PAIR) {
+            Rot st;
+            tab_step(tab, e0 / 2, st);
+            rot_step(rot, st);
+          } else {
+            rot_step(rot, step_held);
+          }
         }
         Pairs fq = unpack_pairs(xq), fk = unpack_pairs(xk);
         const float rq2 = sumsq(fq), rk2 = sumsq(fk);
