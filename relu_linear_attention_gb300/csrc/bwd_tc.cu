@@ -109,6 +109,16 @@ __device__ __forceinline__ void tma_chunk(const CUtensorMap* const (&maps)[NT],
     for (int jb = 0; jb < 2; ++jb) tc::tma_load_3d(tiles[i] + jb * 16384, maps[i], 64 * jb, h, row, bar);
 }
 
+// The same rows fetched into L2 only (no shared memory, no completion), a chunk before their load:
+// the load, which must wait until the chunk before has read its tiles, then finds them there.
+template <int NT>
+__device__ __forceinline__ void prefetch_chunk(const CUtensorMap* const (&maps)[NT], int h, int row) {
+#pragma unroll
+  for (int i = 0; i < NT; ++i)
+#pragma unroll
+    for (int jb = 0; jb < 2; ++jb) tc::tma_prefetch_3d(maps[i], 64 * jb, h, row);
+}
+
 // Rows nvalid .. 127 of a tile set to zero (all threads).
 __device__ __forceinline__ void clear_rows(uint32_t tile, int nvalid) {
   for (int idx = threadIdx.x + nvalid * 16; idx < kC * 16; idx += kThreads)
@@ -246,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- phase 1: the chunk's tiles (TMA; q' and k' from the feature kernel); q'.z of every
     // row and the column sums of k'; rows past the document cleared
     if (!tc::mbar_wait(bar_ld, c & 1, kWait)) atomicExch(s_abort, 1);
+    if (tid == 0 && c + 1 < nch) prefetch_chunk<4>(maps, h, static_cast<int>(row0 + t0 + kC));
     if (t0 + kC > n) {  // uniform over the CTA
       clear_rows(base + Lay::QF, n - t0);
       clear_rows(base + Lay::KF, n - t0);
@@ -541,6 +552,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (c > 0) row_scalars(t0 - kC, rs_next);  // the earlier chunk's, one chunk ahead
     if (!tc::mbar_wait(bar_ld, it & 1, kWait) || !tc::mbar_wait(bar_ldq, it & 1, kWait))
       atomicExch(s_abort, 1);
+    if (tid == 0 && c > 0) {  // the earlier chunk's tiles into L2 while this one runs
+      prefetch_chunk<3>(maps3, h, static_cast<int>(row0 + t0 - kC));
+      prefetch_chunk<1>(maps1, h, static_cast<int>(row0 + t0 - kC));
+    }
     if (tid == 0) tc::bulk_wait_read0();  // the previous chunk's dk' store has read AS
     __syncthreads();  // den_s
     for (int idx = tid + (n - t0) * 16; idx < kC * 16; idx += kThreads) {  // (n > t0)
