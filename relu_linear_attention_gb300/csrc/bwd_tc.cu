@@ -61,8 +61,10 @@ using feat::sts16;
 using namespace tct;
 
 constexpr int kC = 128;
-constexpr int kThreads = 512;
+constexpr int kThreads = 512;               // the lockstep worker threads (16 warps)
 constexpr int kWarps = kThreads / 32;
+constexpr int kThreadsA = kThreads + 32;     // pass A: + one warp that issues the MMAs and loads
+constexpr uint32_t kBarWork = 1;             // named barrier of pass A's worker warps
 constexpr uint32_t kTile = 32768;          // 128 rows x 128 bf16 columns (two 64-column blocks)
 
 // Shared memory (bytes from a 1024-byte aligned base). Both passes use the same map: six bf16
@@ -75,8 +77,8 @@ struct Lay {
   static constexpr uint32_t ZP = ZS + kD * 4;                 // per-warp k' column sums [16][D]
   static constexpr uint32_t ROW = ZP + kWarps * kD * 4;       // den, scale, sst, nst [4][128]
   static constexpr uint32_t RED = ROW + 4 * kC * 4;           // partial row sums [3][4][128]
-  static constexpr uint32_t BAR = RED + 3 * 4 * kC * 4;       // five mbarriers
-  static constexpr uint32_t MISC = BAR + 5 * 8;               // TMEM base, abort flag
+  static constexpr uint32_t BAR = RED + 3 * 4 * kC * 4;       // eight mbarriers
+  static constexpr uint32_t MISC = BAR + 8 * 8;               // TMEM base, abort flag
   static constexpr uint32_t BYTES = MISC + 16;
   static_assert(BYTES <= 232448, "shared memory budget");
 };
@@ -165,7 +167,7 @@ __device__ __forceinline__ void feature_sums(uint32_t tile, int n, int t0, const
 
 // ------------------------------------------------------------------------------------------------
 // Pass A: chunks in order.
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsA, 1)
     bwd_tc_forward(const BwdArgs b, const __grid_constant__ CUtensorMap tmqf,
                    const __grid_constant__ CUtensorMap tmkf, const __grid_constant__ CUtensorMap tmv,
                    const __grid_constant__ CUtensorMap tmg, const __grid_constant__ CUtensorMap tmdq) {
@@ -189,6 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sst_s = scl_s + kC;
   float* red = reinterpret_cast<float*>(smem + Lay::RED);
   const uint32_t bar1 = base + Lay::BAR, bar2 = bar1 + 8, bar1b = bar1 + 16, bar_ld = bar1 + 24;
+  // worker warps -> issuer: the chunk's tiles cleared (ready), A' written (a_ready), S~ written and
+  // S read (s_ready; completion 0 is the segment's initial state)
+  const uint32_t bar_ready = bar1 + 32, bar_aready = bar1 + 40, bar_sready = bar1 + 48;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + Lay::MISC);
   int* s_abort = reinterpret_cast<int*>(smem + Lay::MISC + 4);
   const bool misaligned = (base & 1023u) != 0;
@@ -202,6 +207,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(bar2, 1);
     tc::mbar_init(bar1b, 1);
     tc::mbar_init(bar_ld, 1);
+    tc::mbar_init(bar_ready, kWarps);
+    tc::mbar_init(bar_aready, kWarps);
+    tc::mbar_init(bar_sready, kWarps);
     tc::mbar_fence_init();
     *s_abort = misaligned ? 1 : 0;
   }
@@ -215,13 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the first chunk's tiles are requested before the state is summed (they do not overlap it)
   const CUtensorMap* const maps[4] = {&tmqf, &tmkf, &tmv, &tmg};
   const uint32_t ld_tiles[4] = {base + Lay::QF, base + Lay::KF, base + Lay::VS, base + Lay::GS};
-  int tma_issued = 0;  // chunks whose tiles have been requested (thread 0)
-  if (tid == 0 && nch > 0 && !*s_abort) {
-    tma_chunk<4>(maps, ld_tiles, h, static_cast<int>(row0 + s0), bar_ld);
-    tma_issued = 1;
-  }
+  if (tid == 0 && nch > 0 && !*s_abort) tma_chunk<4>(maps, ld_tiles, h, static_cast<int>(row0 + s0), bar_ld);
   // the prefix state at the segment's start: the increments of the blocks before it, in order
-  if (nch > 0) {
+  // (the worker warps: lane quarter q4, column group gw < 4; the issuing warp takes no part)
+  if (nch > 0 && warp < kWarps) {
     const int nb = seg * b.blk_per_seg;
     constexpr long R4 = static_cast<long>(kD) * (kD + 1) / 4;
     const float4* rec = reinterpret_cast<const float4*>(b.rec_fwd) + static_cast<long>(unit) * b.nblk_max * R4;
@@ -251,6 +256,65 @@ __global__ void __launch_bounds__(kThreads, 1)
   __nv_bfloat16* dqf_out = static_cast<__nv_bfloat16*>(b.dqf);
   bool bad = *s_abort != 0;
 
+  if (warp == kWarps) {
+    // ============================================ MMA issue and tile loads (one thread)
+    if (lane == 0) {
+      constexpr uint32_t ID_KK = tc::idesc_bf16(128, 128, false, false);
+      constexpr uint32_t ID_MM = tc::idesc_bf16(128, 128, true, true);
+      constexpr uint32_t ID = tc::idesc_bf16(128, 128, false, true);
+      bool ok = !bad;  // false only once a wait has given up
+      int loads = 0;
+      for (int c = 0; c < nch && ok; ++c) {
+        const int t0 = s0 + c * kC;
+        // P = Q'K'^T, Cv = G V^T once the workers have cleared the rows past the document
+        ok = tc::mbar_wait(bar_ready, c & 1, kWait);
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll 1
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          tc::mma_bf16(tmem + kTP, kmaj(base + Lay::QF, kk), kmaj(base + Lay::KF, kk), ID_KK, kk > 0);
+          tc::mma_bf16(tmem + kTG, kmaj(base + Lay::GS, kk), kmaj(base + Lay::VS, kk), ID_KK, kk > 0);
+        }
+        tc::mma_commit(bar1);  // P and Cv: the row sums can start
+        // U = G S~^T and S += K'^T V once the previous chunk has read U and S and written S~
+        ok = tc::mbar_wait(bar_sready, c & 1, kWait);
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll 1
+        for (int kk = 0; kk < kD / 16; ++kk)
+          tc::mma_bf16(tmem + kTU, kmaj(base + Lay::GS, kk), kmaj_d(base + Lay::XS, kk), ID_KK, kk > 0);
+        tc::mma_commit(bar1b);
+#pragma unroll 1
+        for (int kk = 0; kk < kC / 16; ++kk)
+          tc::mma_bf16(tmem + kTS, mnmaj(base + Lay::KF, kk, 16384), mnmaj(base + Lay::VS, kk, 16384),
+                       ID_MM, 1u);
+        // U += A'~ K' once A' is written
+        ok = tc::mbar_wait(bar_aready, c & 1, kWait);
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll 1
+        for (int kk = 0; kk < kC / 16; ++kk)
+          tc::mma_bf16(tmem + kTU, kmaj(base + Lay::AS, kk), mnmaj(base + Lay::KF, kk, 16384), ID, 1u);
+        tc::mma_commit(bar2);
+        // every MMA and every worker (A' was their last read of q') is done with the tiles: the
+        // next chunk's may arrive while this one finishes
+        if (c + 1 < nch) {
+          ok = tc::mbar_wait(bar2, c & 1, kWait);
+          if (!ok || *reinterpret_cast<volatile int*>(s_abort)) break;
+          tma_chunk<4>(maps, ld_tiles, h, static_cast<int>(row0 + t0 + kC), bar_ld);
+          ++loads;
+        }
+      }
+      if (!ok) atomicExch(s_abort, 1);
+      // a copy requested but not waited for (an early exit) must land before the CTA leaves: this
+      // thread's load k (from 1; chunk 0's was the worker's) completes bar_ld's phase k
+      if (loads > 0) tc::mbar_wait(bar_ld, loads & 1, kWait);
+    }
+  } else {
+  if (!bad && nch > 0) {  // the initial S~ is written (completion 0 of s_ready)
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(bar_sready);
+  }
   for (int c = 0; c < nch && !bad; ++c) {
     const int t0 = s0 + c * kC;
     // ---- phase 1: the chunk's tiles (TMA; q' and k' from the feature kernel); q'.z of every
@@ -262,8 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       clear_rows(base + Lay::KF, n - t0);
       clear_rows(base + Lay::VS, n - t0);
       clear_rows(base + Lay::GS, n - t0);
-      __syncthreads();
+      tc::fence_async_smem();
+      tc::named_sync(kBarWork, kThreads);
     }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(bar_ready);  // the first products may start
     float zc[4] = {0.f, 0.f, 0.f, 0.f}, dummy[4] = {0.f, 0.f, 0.f, 0.f};
     feature_sums(base + Lay::QF, n, t0, zs, sst_s, dummy);
     feature_sums(base + Lay::KF, n, t0, nullptr, nullptr, zc);
@@ -272,29 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) tc::bulk_wait_read0();  // the previous chunk's dq' store has read AS
     tc::fence_async_smem();
     tc::fence_before_sync();
-    __syncthreads();
+    tc::named_sync(kBarWork, kThreads);
     tc::fence_after_sync();
-    if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
-    // ---- phase 2: P = Q'K'^T, Cv = G V^T, U = G S~^T, S += K'^T V
-    if (tid == 0) {
-      constexpr uint32_t ID_KK = tc::idesc_bf16(128, 128, false, false);
-      constexpr uint32_t ID_MM = tc::idesc_bf16(128, 128, true, true);
-#pragma unroll 1
-      for (int kk = 0; kk < kD / 16; ++kk) {
-        tc::mma_bf16(tmem + kTP, kmaj(base + Lay::QF, kk), kmaj(base + Lay::KF, kk), ID_KK, kk > 0);
-        tc::mma_bf16(tmem + kTG, kmaj(base + Lay::GS, kk), kmaj(base + Lay::VS, kk), ID_KK, kk > 0);
-      }
-      tc::mma_commit(bar1);  // P and Cv: the row sums can start
-#pragma unroll 1
-      for (int kk = 0; kk < kD / 16; ++kk)
-        tc::mma_bf16(tmem + kTU, kmaj(base + Lay::GS, kk), kmaj_d(base + Lay::XS, kk), ID_KK, kk > 0);
-      tc::mma_commit(bar1b);
-      // the state update is waited for only through bar2 (phase 4 commits after it)
-#pragma unroll 1
-      for (int kk = 0; kk < kC / 16; ++kk)
-        tc::mma_bf16(tmem + kTS, mnmaj(base + Lay::KF, kk, 16384), mnmaj(base + Lay::VS, kk, 16384),
-                     ID_MM, 1u);
-    }
+    // ---- phase 2 (the issuing warp): P = Q'K'^T, Cv = G V^T, U = G S~^T, S += K'^T V
     if (!wait_mma(bar1, c & 1)) atomicExch(s_abort, 1);
     // ---- phase 3: row sums, den, scale, A'
     const bool valid = t0 + t < n;
@@ -325,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     red[(1 * 4 + gw) * kC + t] = pc;
     red[(2 * 4 + gw) * kC + t] = nst;
     tc::fence_before_sync();
-    __syncthreads();
+    tc::named_sync(kBarWork, kThreads);
     ps = red[t] + red[kC + t] + red[2 * kC + t] + red[3 * kC + t];
     pc = red[4 * kC + t] + red[5 * kC + t] + red[6 * kC + t] + red[7 * kC + t];
     nst = red[8 * kC + t] + red[9 * kC + t] + red[10 * kC + t] + red[11 * kC + t];
@@ -356,23 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
-    // ---- phase 4: U += A'~ K'
-    if (tid == 0) {
-      constexpr uint32_t ID = tc::idesc_bf16(128, 128, false, true);
-#pragma unroll 1
-      for (int kk = 0; kk < kC / 16; ++kk)
-        tc::mma_bf16(tmem + kTU, kmaj(base + Lay::AS, kk), mnmaj(base + Lay::KF, kk, 16384), ID, 1u);
-      tc::mma_commit(bar2);
-    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(bar_aready);  // every read of q' is done, A' is written
+    // ---- phase 4 (the issuing warp): U += A'~ K'; then the next chunk's tiles
     if (!wait_mma(bar2, c & 1)) atomicExch(s_abort, 1);
-    // every MMA has read the tiles: the next chunk's raw tiles may arrive while this one finishes
-    if (tid == 0 && c + 1 < nch && !*reinterpret_cast<volatile int*>(s_abort)) {
-      tma_chunk<4>(maps, ld_tiles, h, static_cast<int>(row0 + t0 + kC), bar_ld);
-      ++tma_issued;
-    }
     // ---- phase 5: dq' = U / den + scale z (bf16, to the workspace); S -> S~
     {
       float u[32];
@@ -393,27 +427,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
-    __syncthreads();
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(bar_sready);  // U and S read, S~ written: the next products
+    tc::named_sync(kBarWork, kThreads);
     if (tid == 0 && t0 + kC <= n) {
 #pragma unroll
       for (int jb = 0; jb < b.d / 64; ++jb)
         tc::tma_store_3d(&tmdq, base + Lay::AS + jb * 16384, 64 * jb, h, static_cast<int>(row0 + t0));
       tc::bulk_commit();
     }
-    if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
     // ---- phase 6: z += column sums of k'
     if (tid < kD) {
       float zz = zs[tid];
       for (int w = 0; w < kWarps; ++w) zz += zp[w * kD + tid];
       zs[tid] = zz;
     }
-    __syncthreads();  // zs is read before the next chunk uses it
+    // zs is read before the next chunk uses it; the workers leave together
+    if (feat::group_sync_or(kBarWork, kThreads, *reinterpret_cast<volatile int*>(s_abort))) {
+      bad = true;
+      break;
+    }
   }
-  bad = bad || *reinterpret_cast<volatile int*>(s_abort) != 0;
-  // a copy requested but not waited for (an early exit) must land before the CTA leaves
-  if (tid == 0 && tma_issued > 0) tc::mbar_wait(bar_ld, (tma_issued - 1) & 1, kWait);
   if (tid == 0) tc::bulk_wait0();  // the dq' tile stores are complete before the NaN fill or exit
+  }
   __syncthreads();
+  bad = *reinterpret_cast<volatile int*>(s_abort) != 0;
   if (bad) {  // a wait gave up: NaN dq' over the segment, so the failure cannot pass for a result
     const int cpr = b.d / 8;  // 16-byte chunks per row
     for (long r = s0 + tid / cpr; r < s1; r += kThreads / cpr)
@@ -1216,7 +1254,7 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   if ((e = make_rows_map(&tmdq, b.dqf, rows, b.p.H, d)) != cudaSuccess) return e;
   if ((e = make_rows_map(&tmdk, b.dkf, rows, b.p.H, d)) != cudaSuccess) return e;
   if ((e = make_rows_map(&tmdv, b.dv, rows, b.p.H, d)) != cudaSuccess) return e;
-  bwd_tc_forward<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b, tmqf, tmkf, tmv,
+  bwd_tc_forward<<<static_cast<unsigned>(grid), kThreadsA, Lay::BYTES, stream>>>(b, tmqf, tmkf, tmv,
                                                                                  tmg, tmdq);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
