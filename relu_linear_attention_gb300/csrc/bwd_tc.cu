@@ -346,8 +346,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     // ---- phase 3: row sums, den, scale, A'
     const bool valid = t0 + t < n;
     float pv[32], cv[32];
-    tmem_ld32(tmem + tl + kTP + 32 * gw, pv);
-    tmem_ld32(tmem + tl + kTG + 32 * gw, cv);
+    tmem_ld32x2(tmem + tl + kTP + 32 * gw, pv, tmem + tl + kTG + 32 * gw, cv);
     float ps = 0.f, pc = 0.f;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
@@ -409,8 +408,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     if (!wait_mma(bar2, c & 1)) atomicExch(s_abort, 1);
     // ---- phase 5: dq' = U / den + scale z (bf16, to the workspace); S -> S~
     {
-      float u[32];
-      tmem_ld32(tmem + tl + kTU + 32 * gw, u);
+      float u[32], sv[32];
+      tmem_ld32x2(tmem + tl + kTU + 32 * gw, u, tmem + tl + kTS + 32 * gw, sv);
       const float inv = 1.0f / den;
 #pragma unroll
       for (int j = 0; j < 32; ++j) u[j] = fmaf(u[j], inv, scale * zs[32 * gw + j]);
@@ -421,8 +420,6 @@ __global__ void __launch_bounds__(kThreadsA, 1)
 #pragma unroll
         for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(u + 8 * m);
       }
-      float sv[32];
-      tmem_ld32(tmem + tl + kTS + 32 * gw, sv);
       store_row32<true>(base + Lay::XS, t, gw, sv);
     }
     tc::fence_async_smem();
@@ -660,8 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const float den = den_s[t], sst = sst_s[t], nst = nst_s[t];
     float pv[32], av[32];
-    tmem_ld32(tmem + tl + kTP + 32 * gw, pv);
-    tmem_ld32(tmem + tl + kTG + 32 * gw, av);  // c = g . v
+    tmem_ld32x2(tmem + tl + kTP + 32 * gw, pv, tmem + tl + kTG + 32 * gw, av);  // av: c = g . v
     float ps = 0.f, pc = 0.f;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {

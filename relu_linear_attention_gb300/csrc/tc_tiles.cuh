@@ -59,6 +59,23 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   }
 }
 
+// Two such reads with both in flight before the one wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, float (&va)[32], uint32_t tb, float (&vb)[32]) {
+  uint32_t u[4][16];
+  tc::tmem_ld16(ta, u[0]);
+  tc::tmem_ld16(ta + 16, u[1]);
+  tc::tmem_ld16(tb, u[2]);
+  tc::tmem_ld16(tb + 16, u[3]);
+  tc::tmem_wait_ld();
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    va[e] = __uint_as_float(u[0][e]);
+    va[16 + e] = __uint_as_float(u[1][e]);
+    vb[e] = __uint_as_float(u[2][e]);
+    vb[16 + e] = __uint_as_float(u[3][e]);
+  }
+}
+
 // 32 fp32 values as bf16 into row r, columns 32 g .. 32 g + 31 of a tile (tile_off or dtile_off).
 template <bool DROWS>
 __device__ __forceinline__ void store_row32(uint32_t tile, int r, int g, const float (&v)[32]) {
