@@ -37,11 +37,13 @@
 // Then, fully parallel over (document, head, chunk), dq and dk through the feature map (ReLU mask,
 // inverse RoPE rotation, RMSNorm backward) from dq', dk' and the raw q, k, with gain partials
 // (bwd_tc_features), and the gains summed in a fixed order.
-// The passes run one CTA per (document, head, segment), 512 threads in lockstep phases: all threads
-// read TMEM rows (thread = TMEM lane = tile row, four warps per lane quarter splitting the columns)
-// and do the per-row arithmetic; one thread issues the MMAs and the TMA copies of the next chunk's
-// tiles and commits them to mbarriers. Every wait is bounded (~1 s); a CTA whose wait gives up sets
-// RAPT_DEV_INTERNAL in the status word and writes NaN results, so a failure cannot pass for one.
+// The passes run one CTA per (document, head, segment) with 512 worker threads in lockstep phases:
+// they read TMEM rows (thread = TMEM lane = tile row, four warps per lane quarter splitting the
+// columns) and do the per-row arithmetic. In pass B one of them issues the MMAs and the TMA copies
+// of the next chunk's tiles and commits them to mbarriers; pass A has a 17th warp for that, which
+// waits on mbarriers the workers arrive at (rows cleared, A' written, S~ written), so the first
+// products overlap the workers' row sums. Every wait is bounded (~1 s); a CTA whose wait gives up
+// sets RAPT_DEV_INTERNAL in the status word and writes NaN results, so a failure cannot pass for one.
 #include <cuda.h>
 
 #include "feature_bwd.cuh"
