@@ -341,8 +341,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     tc::mbar_fence_init();
     *s_abort = 0;
   }
-  if (D == 64) {  // zero block that pads k'^T to M = 128 rows
+  if (D == 64) {  // zero block that pads k'^T to M = 128 rows (read by the tensor core)
     for (int i = tid; i < 16384 / 16; i += kThreadsB) sts16(base + L::KS + 16384 + i * 16, make_uint4(0, 0, 0, 0));
+    tc::fence_async_smem();
   }
   const FeatTab tab = feat_tab<D>(smem + L::TAB);
   fill_tab<D, DH>(tab, a, NH * h, RPP, tid, kThreadsB);
@@ -890,6 +891,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
       const int st = i / (16384 / 16), j = i % (16384 / 16);
       sts16(base + L::K0 + st * L::KT + 16384 + j * 16, make_uint4(0, 0, 0, 0));
     }
+    tc::fence_async_smem();  // (read by the tensor core)
   }
   const FeatTab tab = feat_tab<D>(smem + L::TAB);
   fill_tab<D>(tab, a, h, RPP, tid, kThreadsA);
