@@ -103,24 +103,35 @@ constexpr int kRB = kRPW / 2;  // rows of a warp loaded together (two batches pe
 // each, in the swizzled operand layout), completing on one mbarrier; one thread calls it. Rows
 // past the tensor read as zero; rows past the document but inside the tensor are other tokens,
 // which the caller clears after the wait.
-template <int NT>
+template <int NT, int D>
 __device__ __forceinline__ void tma_chunk(const CUtensorMap* const (&maps)[NT],
                                           const uint32_t (&tiles)[NT], int h, int row, uint32_t bar) {
-  tc::mbar_arrive_expect_tx(bar, NT * kTile);
+  tc::mbar_arrive_expect_tx(bar, NT * kC * D * 2);
 #pragma unroll
   for (int i = 0; i < NT; ++i)
 #pragma unroll
-    for (int jb = 0; jb < 2; ++jb) tc::tma_load_3d(tiles[i] + jb * 16384, maps[i], 64 * jb, h, row, bar);
+    for (int jb = 0; jb < D / 64; ++jb) tc::tma_load_3d(tiles[i] + jb * 16384, maps[i], 64 * jb, h, row, bar);
 }
 
 // The same rows fetched into L2 only (no shared memory, no completion), a chunk before their load:
 // the load, which must wait until the chunk before has read its tiles, then finds them there.
-template <int NT>
+template <int NT, int D>
 __device__ __forceinline__ void prefetch_chunk(const CUtensorMap* const (&maps)[NT], int h, int row) {
 #pragma unroll
   for (int i = 0; i < NT; ++i)
 #pragma unroll
-    for (int jb = 0; jb < 2; ++jb) tc::tma_prefetch_3d(maps[i], 64 * jb, h, row);
+    for (int jb = 0; jb < D / 64; ++jb) tc::tma_prefetch_3d(maps[i], 64 * jb, h, row);
+}
+
+// At d = 64 the second 64-column block of the streamed tiles (QF, KF, VS, GS: the first four) is
+// never loaded: it is cleared once, so that the products whose M runs over the 128 feature rows
+// (K'^T V, Q'^T Gnum) see zeros there. The worker threads call it.
+template <int D>
+__device__ __forceinline__ void clear_upper_blocks(uint32_t base) {
+  if (D == 64) {
+    for (int idx = threadIdx.x; idx < 4 * 1024; idx += kThreads)
+      feat::sts16(base + (idx >> 10) * kTile + 16384 + 16 * (idx & 1023), make_uint4(0, 0, 0, 0));
+  }
 }
 
 // Rows nvalid .. 127 of a tile set to zero (all threads).
@@ -130,27 +141,34 @@ __device__ __forceinline__ void clear_rows(uint32_t tile, int nvalid) {
 }
 
 // Sums over the features of a chunk (bf16 in the tile, by TMA from the workspace; warp w takes rows
-// w, w + 16, ..., lane r elements 4r .. 4r+3): with z given, q'.z of every row into sst[] (zero past
+// w, w + 16, ...): with z given, q'.z of every row into sst[] (zero past
 // the document); the column sums of the rows inside the document are added to zc.
+template <int D>
 __device__ __forceinline__ void feature_sums(uint32_t tile, int n, int t0, const float* z, float* sst,
                                              float (&zc)[4]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // d = 128: a row per warp load, lane r on elements 4r .. 4r+3; d = 64: two rows per load, one
+  // per half warp
+  constexpr int RPL = D == 64 ? 2 : 1;
+  const int sub = D == 64 ? lane >> 4 : 0, cl = D == 64 ? lane & 15 : lane;
   float zl[4] = {0.f, 0.f, 0.f, 0.f};
   if (z != nullptr) {
-    const float4 zz = *reinterpret_cast<const float4*>(z + 4 * lane);
+    const float4 zz = *reinterpret_cast<const float4*>(z + 4 * cl);
     zl[0] = zz.x; zl[1] = zz.y; zl[2] = zz.z; zl[3] = zz.w;
   }
+  constexpr int NL = kRPW / RPL;  // loads per warp
 #pragma unroll 1
-  for (int i0 = 0; i0 < kRPW; i0 += kRB) {
+  for (int i0 = 0; i0 < NL; i0 += kRB) {
     uint32_t lo[kRB], hi[kRB];
 #pragma unroll
     for (int i = 0; i < kRB; ++i) {
-      const uint32_t addr = tile + tile_off(warp + kWarps * (i0 + i), lane >> 1) + (lane & 1) * 8;
+      const int rr = warp + kWarps * (RPL * (i0 + i) + sub);
+      const uint32_t addr = tile + tile_off(rr, cl >> 1) + (cl & 1) * 8;
       asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(lo[i]), "=r"(hi[i]) : "r"(addr) : "memory");
     }
 #pragma unroll
     for (int i = 0; i < kRB; ++i) {
-      const int rr = warp + kWarps * (i0 + i);
+      const int rr = warp + kWarps * (RPL * (i0 + i) + sub);
       const bool valid = t0 + rr < n;
       const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&lo[i]));
       const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi[i]));
@@ -158,17 +176,22 @@ __device__ __forceinline__ void feature_sums(uint32_t tile, int n, int t0, const
       if (z != nullptr) {
         float sdot = f[0] * zl[0] + f[1] * zl[1] + f[2] * zl[2] + f[3] * zl[3];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sdot += __shfl_xor_sync(0xffffffffu, sdot, off);
-        if (lane == 0) sst[rr] = sdot;
+        for (int off = D == 64 ? 8 : 16; off > 0; off >>= 1) sdot += __shfl_xor_sync(0xffffffffu, sdot, off);
+        if (cl == 0) sst[rr] = sdot;
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) zc[e] += f[e];
     }
   }
+  if (D == 64) {  // both halves' rows of the same columns
+#pragma unroll
+    for (int e = 0; e < 4; ++e) zc[e] += __shfl_xor_sync(0xffffffffu, zc[e], 16);
+  }
 }
 
 // ------------------------------------------------------------------------------------------------
 // Pass A: chunks in order.
+template <int D>
 __global__ void __launch_bounds__(kThreadsA, 1)
     bwd_tc_forward(const BwdArgs b, const __grid_constant__ CUtensorMap tmqf,
                    const __grid_constant__ CUtensorMap tmkf, const __grid_constant__ CUtensorMap tmv,
@@ -225,10 +248,12 @@ __global__ void __launch_bounds__(kThreadsA, 1)
   // the first chunk's tiles are requested before the state is summed (they do not overlap it)
   const CUtensorMap* const maps[4] = {&tmqf, &tmkf, &tmv, &tmg};
   const uint32_t ld_tiles[4] = {base + Lay::QF, base + Lay::KF, base + Lay::VS, base + Lay::GS};
-  if (tid == 0 && nch > 0 && !*s_abort) tma_chunk<4>(maps, ld_tiles, h, static_cast<int>(row0 + s0), bar_ld);
+  if (tid == 0 && nch > 0 && !*s_abort) tma_chunk<4, D>(maps, ld_tiles, h, static_cast<int>(row0 + s0), bar_ld);
   // the prefix state at the segment's start: the increments of the blocks before it, in order
   // (the worker warps: lane quarter q4, column group gw < 4; the issuing warp takes no part)
+  constexpr int GD = D / 32;  // column groups of 32 that hold one of the d feature columns
   if (nch > 0 && warp < kWarps) {
+    clear_upper_blocks<D>(base);
     const int nb = seg * b.blk_per_seg;
     constexpr long R4 = static_cast<long>(kD) * (kD + 1) / 4;
     const float4* rec = reinterpret_cast<const float4*>(b.rec_fwd) + static_cast<long>(unit) * b.nblk_max * R4;
@@ -236,7 +261,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
 #pragma unroll
     for (int e = 0; e < 32; ++e) sv[e] = 0.f;
 #pragma unroll 2  // two records' loads in flight together
-    for (int blk = 0; blk < nb; ++blk) {
+    for (int blk = 0; blk < (D == 128 || gw < GD ? nb : 0); ++blk) {
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
         const float4 x = __ldcg(rec + blk * R4 + (8 * gw + jj) * kD + t);
@@ -261,9 +286,11 @@ __global__ void __launch_bounds__(kThreadsA, 1)
   if (warp == kWarps) {
     // ============================================ MMA issue and tile loads (one thread)
     if (lane == 0) {
+      // the products with d output columns have N = d
       constexpr uint32_t ID_KK = tc::idesc_bf16(128, 128, false, false);
-      constexpr uint32_t ID_MM = tc::idesc_bf16(128, 128, true, true);
-      constexpr uint32_t ID = tc::idesc_bf16(128, 128, false, true);
+      constexpr uint32_t ID_U = tc::idesc_bf16(128, D, false, false);
+      constexpr uint32_t ID_MM = tc::idesc_bf16(128, D, true, true);
+      constexpr uint32_t ID = tc::idesc_bf16(128, D, false, true);
       bool ok = !bad;  // false only once a wait has given up
       int loads = 0;
       for (int c = 0; c < nch && ok; ++c) {
@@ -273,7 +300,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         if (!ok) break;
         tc::fence_after_sync();
 #pragma unroll 1
-        for (int kk = 0; kk < kD / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           tc::mma_bf16(tmem + kTP, kmaj(base + Lay::QF, kk), kmaj(base + Lay::KF, kk), ID_KK, kk > 0);
           tc::mma_bf16(tmem + kTG, kmaj(base + Lay::GS, kk), kmaj(base + Lay::VS, kk), ID_KK, kk > 0);
         }
@@ -283,8 +310,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         if (!ok) break;
         tc::fence_after_sync();
 #pragma unroll 1
-        for (int kk = 0; kk < kD / 16; ++kk)
-          tc::mma_bf16(tmem + kTU, kmaj(base + Lay::GS, kk), kmaj_d(base + Lay::XS, kk), ID_KK, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc::mma_bf16(tmem + kTU, kmaj(base + Lay::GS, kk), kmaj_d(base + Lay::XS, kk), ID_U, kk > 0);
         tc::mma_commit(bar1b);
 #pragma unroll 1
         for (int kk = 0; kk < kC / 16; ++kk)
@@ -303,7 +330,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         if (c + 1 < nch) {
           ok = tc::mbar_wait(bar2, c & 1, kWait);
           if (!ok || *reinterpret_cast<volatile int*>(s_abort)) break;
-          tma_chunk<4>(maps, ld_tiles, h, static_cast<int>(row0 + t0 + kC), bar_ld);
+          tma_chunk<4, D>(maps, ld_tiles, h, static_cast<int>(row0 + t0 + kC), bar_ld);
           ++loads;
         }
       }
@@ -322,7 +349,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     // ---- phase 1: the chunk's tiles (TMA; q' and k' from the feature kernel); q'.z of every
     // row and the column sums of k'; rows past the document cleared
     if (!tc::mbar_wait(bar_ld, c & 1, kWait)) atomicExch(s_abort, 1);
-    if (tid == 0 && c + 1 < nch) prefetch_chunk<4>(maps, h, static_cast<int>(row0 + t0 + kC));
+    if (tid == 0 && c + 1 < nch) prefetch_chunk<4, D>(maps, h, static_cast<int>(row0 + t0 + kC));
     if (t0 + kC > n) {  // uniform over the CTA
       clear_rows(base + Lay::QF, n - t0);
       clear_rows(base + Lay::KF, n - t0);
@@ -334,10 +361,12 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(bar_ready);  // the first products may start
     float zc[4] = {0.f, 0.f, 0.f, 0.f}, dummy[4] = {0.f, 0.f, 0.f, 0.f};
-    feature_sums(base + Lay::QF, n, t0, zs, sst_s, dummy);
-    feature_sums(base + Lay::KF, n, t0, nullptr, nullptr, zc);
+    feature_sums<D>(base + Lay::QF, n, t0, zs, sst_s, dummy);
+    feature_sums<D>(base + Lay::KF, n, t0, nullptr, nullptr, zc);
+    if (4 * lane < D) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) zp[warp * kD + 4 * lane + e] = zc[e];
+      for (int e = 0; e < 4; ++e) zp[warp * kD + 4 * lane + e] = zc[e];
+    }
     if (tid == 0) tc::bulk_wait_read0();  // the previous chunk's dq' store has read AS
     tc::fence_async_smem();
     tc::fence_before_sync();
@@ -358,7 +387,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     }
     float nst = 0.f;
     if (!wait_mma(bar1b, c & 1)) atomicExch(s_abort, 1);
-    {
+    if (D == 128 || gw < GD) {  // U has d columns
       float u[32];
       tmem_ld32(tmem + tl + kTU + 32 * gw, u);
 #pragma unroll
@@ -408,8 +437,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     if (lane == 0) tc::mbar_arrive(bar_aready);  // every read of q' is done, A' is written
     // ---- phase 4 (the issuing warp): U += A'~ K'; then the next chunk's tiles
     if (!wait_mma(bar2, c & 1)) atomicExch(s_abort, 1);
-    // ---- phase 5: dq' = U / den + scale z (bf16, to the workspace); S -> S~
-    {
+    // ---- phase 5: dq' = U / den + scale z (bf16, to the workspace); S -> S~ (d columns)
+    if (D == 128 || gw < GD) {
       float u[32], sv[32];
       tmem_ld32x2(tmem + tl + kTU + 32 * gw, u, tmem + tl + kTS + 32 * gw, sv);
       const float inv = 1.0f / den;
@@ -422,7 +451,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
 #pragma unroll
         for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(u + 8 * m);
       }
-      store_row32<true>(base + Lay::XS, t, gw, sv);
+      if (D == 128 || t < D) store_row32<true>(base + Lay::XS, t, gw, sv);
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
@@ -431,12 +460,12 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     tc::named_sync(kBarWork, kThreads);
     if (tid == 0 && t0 + kC <= n) {
 #pragma unroll
-      for (int jb = 0; jb < b.d / 64; ++jb)
+      for (int jb = 0; jb < D / 64; ++jb)
         tc::tma_store_3d(&tmdq, base + Lay::AS + jb * 16384, 64 * jb, h, static_cast<int>(row0 + t0));
       tc::bulk_commit();
     }
     // ---- phase 6: z += column sums of k'
-    if (tid < kD) {
+    if (tid < D) {
       float zz = zs[tid];
       for (int w = 0; w < kWarps; ++w) zz += zp[w * kD + tid];
       zs[tid] = zz;
@@ -466,6 +495,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
 
 // ------------------------------------------------------------------------------------------------
 // Pass B: chunks in reverse.
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_reverse(const BwdArgs b, const __grid_constant__ CUtensorMap tmqf,
                    const __grid_constant__ CUtensorMap tmkf, const __grid_constant__ CUtensorMap tmv,
@@ -525,10 +555,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_ldq = bar4;
   int tma_issued = 0, tmaq_issued = 0;  // chunks whose tiles have been requested (thread 0)
   if (tid == 0 && nch > 0 && !*s_abort) {
-    tma_chunk<3>(maps3, ld_tiles3, h, static_cast<int>(row0 + s0 + (nch - 1) * kC), bar_ld);
-    tma_chunk<1>(maps1, ld_tiles1, h, static_cast<int>(row0 + s0 + (nch - 1) * kC), bar_ldq);
+    tma_chunk<3, D>(maps3, ld_tiles3, h, static_cast<int>(row0 + s0 + (nch - 1) * kC), bar_ld);
+    tma_chunk<1, D>(maps1, ld_tiles1, h, static_cast<int>(row0 + s0 + (nch - 1) * kC), bar_ldq);
     tma_issued = tmaq_issued = 1;
   }
+  constexpr int GD = D / 32;  // column groups of 32 that hold one of the d feature columns
+  clear_upper_blocks<D>(base);
   // the suffix state at the segment's end: the later segments' increments, in segment order
   if (nch > 0) {
     constexpr long REC = static_cast<long>(kD) * kD + kD;
@@ -540,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int e = 0; e < 32; ++e) rv[e] = 0.f;
 #pragma unroll 2  // two records' loads in flight together
-    for (int kb = k0; kb < k1; ++kb) {
+    for (int kb = k0; kb < (D == 128 || gw < GD ? k1 : k0); ++kb) {
       const float4* src = reinterpret_cast<const float4*>(rr + kb * REC + t * kD + 32 * gw);
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
@@ -590,8 +622,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!tc::mbar_wait(bar_ld, it & 1, kWait) || !tc::mbar_wait(bar_ldq, it & 1, kWait))
       atomicExch(s_abort, 1);
     if (tid == 0 && c > 0) {  // the earlier chunk's tiles into L2 while this one runs
-      prefetch_chunk<3>(maps3, h, static_cast<int>(row0 + t0 - kC));
-      prefetch_chunk<1>(maps1, h, static_cast<int>(row0 + t0 - kC));
+      prefetch_chunk<3, D>(maps3, h, static_cast<int>(row0 + t0 - kC));
+      prefetch_chunk<1, D>(maps1, h, static_cast<int>(row0 + t0 - kC));
     }
     if (tid == 0) tc::bulk_wait_read0();  // the previous chunk's dk' store has read AS
     __syncthreads();  // den_s
@@ -613,25 +645,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     // product that needs no P~, A or gnum: dv = K' R~
     if (tid == 0) {
       constexpr uint32_t ID = tc::idesc_bf16(128, 128, false, false);
-      constexpr uint32_t ID_KM = tc::idesc_bf16(128, 128, false, true);
+      constexpr uint32_t ID_KM = tc::idesc_bf16(128, D, false, true);
 #pragma unroll 1
-      for (int kk = 0; kk < kD / 16; ++kk) {
+      for (int kk = 0; kk < D / 16; ++kk) {
         tc::mma_bf16(tmem + kTP, kmaj(base + Lay::QF, kk), kmaj(base + Lay::KF, kk), ID, kk > 0);
         tc::mma_bf16(tmem + kTG, kmaj(base + Lay::GS, kk), kmaj(base + Lay::VS, kk), ID, kk > 0);
       }
       tc::mma_commit(bar1);
 #pragma unroll 1
-      for (int kk = 0; kk < kD / 16; ++kk)
+      for (int kk = 0; kk < D / 16; ++kk)
         tc::mma_bf16(tmem + kTDV, kmaj(base + Lay::KF, kk), mnmaj(base + Lay::XS, kk, kD * 128),
                      ID_KM, kk > 0);
     }
-    {  // meanwhile the partial increment of w = sum_t scale_t q'_t: column i, rows 32 (tid / 128) ..
-       // + 31, into the third section of RED (added to w once this chunk's dk' has used it)
-      const int i = tid & (kD - 1), r0 = 32 * (tid >> 7);
+    {  // meanwhile the partial increment of w = sum_t scale_t q'_t: column i, rows RP (tid / D) ..
+       // + RP - 1, into the third section of RED (added to w once this chunk's dk' has used it)
+      constexpr int RP = kC * D / kThreads;
+      const int i = tid & (D - 1), r0 = RP * (tid / D);
       const int m = i >> 3, e = i & 7;
       float dw = 0.f;
 #pragma unroll 4
-      for (int r = r0; r < r0 + 32; ++r) {
+      for (int r = r0; r < r0 + RP; ++r) {
         uint32_t word;
         asm volatile("ld.shared.b32 %0, [%1];"
                      : "=r"(word)
@@ -640,13 +673,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&word));
         dw = fmaf(scl_s[r], (e & 1) ? p.y : p.x, dw);
       }
-      red[(8 + (tid >> 7)) * kC + i] = dw;
+      red[8 * kC + tid] = dw;  // partial tid / D of column i
     }
     if (!wait_mma(bar1, it & 1)) atomicExch(s_abort, 1);
     // ---- phase 3: gnum = g / den in place (the products that read g are done); P~ (masked) into
     // AS; A kept in registers
-    for (int idx = tid; idx < kC * 16; idx += kThreads) {
-      const int r = idx >> 4, m = idx & 15;
+    for (int idx = tid; idx < kC * D / 8; idx += kThreads) {
+      const int r = idx / (D / 8), m = idx % (D / 8);
       if (t0 + r < n) {
         const uint32_t ga = base + Lay::GS + tile_off(r, m);
         float f[8];
@@ -690,8 +723,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- phase 4: dv += P~^T Gnum; R += Q'^T Gnum (R~ in XS is not touched); dk' = V R~^T (over
     // P, which phase 3 has read)
     if (tid == 0) {
-      constexpr uint32_t ID_MM = tc::idesc_bf16(128, 128, true, true);
-      constexpr uint32_t ID_KK = tc::idesc_bf16(128, 128, false, false);
+      constexpr uint32_t ID_MM = tc::idesc_bf16(128, D, true, true);
+      constexpr uint32_t ID_KK = tc::idesc_bf16(128, D, false, false);
 #pragma unroll 1
       for (int kk = 0; kk < kC / 16; ++kk)
         tc::mma_bf16(tmem + kTDV, mnmaj(base + Lay::AS, kk, 16384), mnmaj(base + Lay::GS, kk, 16384),
@@ -701,14 +734,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mma_bf16(tmem + kTR, mnmaj(base + Lay::QF, kk, 16384), mnmaj(base + Lay::GS, kk, 16384),
                      ID_MM, 1u);
 #pragma unroll 1
-      for (int kk = 0; kk < kD / 16; ++kk)
+      for (int kk = 0; kk < D / 16; ++kk)
         tc::mma_bf16(tmem + kTDK, kmaj(base + Lay::VS, kk), kmaj_d(base + Lay::XS, kk), ID_KK, kk > 0);
       tc::mma_commit(bar2);
     }
     if (!wait_mma(bar2, it & 1)) atomicExch(s_abort, 1);
     // k', v and gnum are read by every MMA that needs them: the earlier chunk's may arrive
     if (tid == 0 && c > 0 && !*reinterpret_cast<volatile int*>(s_abort)) {
-      tma_chunk<3>(maps3, ld_tiles3, h, static_cast<int>(row0 + t0 - kC), bar_ld);
+      tma_chunk<3, D>(maps3, ld_tiles3, h, static_cast<int>(row0 + t0 - kC), bar_ld);
       ++tma_issued;
     }
     // ---- phase 5: A over P~ (the dv MMAs have read it)
@@ -720,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (*reinterpret_cast<volatile int*>(s_abort)) { bad = true; break; }
     // ---- phase 6: dk' += A^T Q'; dv (complete) out meanwhile
     if (tid == 0) {
-      constexpr uint32_t ID_MM = tc::idesc_bf16(128, 128, true, true);
+      constexpr uint32_t ID_MM = tc::idesc_bf16(128, D, true, true);
 #pragma unroll 1
       for (int kk = 0; kk < kC / 16; ++kk)
         tc::mma_bf16(tmem + kTDK, mnmaj(base + Lay::AS, kk, 16384), mnmaj(base + Lay::QF, kk, 16384),
@@ -730,13 +763,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // a whole chunk's dv and dk' are staged in shared memory and written by TMA (full lines); the
     // ragged last chunk of a document is written row by row (a tile store would reach past it)
     const bool whole = t0 + kC <= n;
-    {
+    if (D == 128 || gw < GD) {
       float o[32];
       tmem_ld32(tmem + tl + kTDV + 32 * gw, o);
       if (whole) {  // into XS: R~'s last readers (the first two groups) are done
         store_row32<false>(base + Lay::XS, t, gw, o);
-      } else if (t0 + t < n && gw < b.d / 32) {
-        __nv_bfloat16* dst = dv + ((row0 + t0 + t) * a.H + h) * b.d + 32 * gw;
+      } else if (t0 + t < n) {
+        __nv_bfloat16* dst = dv + ((row0 + t0 + t) * a.H + h) * D + 32 * gw;
 #pragma unroll
         for (int m = 0; m < 4; ++m)
           *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(o + 8 * m);
@@ -747,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
       if (tid == 0) {
 #pragma unroll
-        for (int jb = 0; jb < b.d / 64; ++jb)
+        for (int jb = 0; jb < D / 64; ++jb)
           tc::tma_store_3d(&tmdv, base + Lay::XS + jb * 16384, 64 * jb, h, static_cast<int>(row0 + t0));
         tc::bulk_commit();
       }
@@ -756,21 +789,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // every MMA of the chunk has completed and no CUDA-core read of q' is left: the earlier
     // chunk's q' may arrive while this one finishes
     if (tid == 0 && c > 0 && !*reinterpret_cast<volatile int*>(s_abort)) {
-      tma_chunk<1>(maps1, ld_tiles1, h, static_cast<int>(row0 + t0 - kC), bar_ldq);
+      tma_chunk<1, D>(maps1, ld_tiles1, h, static_cast<int>(row0 + t0 - kC), bar_ldq);
       ++tmaq_issued;
     }
     // ---- phase 7: dk' + w into the staging, w += sum_t scale_t q'_t, R -> R~
     {
-      float o[32];
-      tmem_ld32(tmem + tl + kTDK + 32 * gw, o);
+      if (D == 128 || gw < GD) {
+        float o[32];
+        tmem_ld32(tmem + tl + kTDK + 32 * gw, o);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] += ws[32 * gw + j];
-      if (whole) {  // into AS: A's last reader (the third group) is done
-        store_row32<false>(base + Lay::AS, t, gw, o);
-      } else if (t0 + t < n && gw < b.d / 32) {  // dk' (bf16) to the workspace
-        __nv_bfloat16* dst = dkf_out + ((row0 + t0 + t) * a.H + h) * b.d + 32 * gw;
+        for (int j = 0; j < 32; ++j) o[j] += ws[32 * gw + j];
+        if (whole) {  // into AS: A's last reader (the third group) is done
+          store_row32<false>(base + Lay::AS, t, gw, o);
+        } else if (t0 + t < n) {  // dk' (bf16) to the workspace
+          __nv_bfloat16* dst = dkf_out + ((row0 + t0 + t) * a.H + h) * D + 32 * gw;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(o + 8 * m);
+          for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(o + 8 * m);
+        }
       }
       tc::fence_async_smem();
       if (tid == 0) tc::bulk_wait_read0();  // the dv store has read XS (R~ is rewritten below)
@@ -778,15 +813,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();  // w is read
       if (whole && tid == 0) {
 #pragma unroll
-        for (int jb = 0; jb < b.d / 64; ++jb)
+        for (int jb = 0; jb < D / 64; ++jb)
           tc::tma_store_3d(&tmdk, base + Lay::AS + jb * 16384, 64 * jb, h, static_cast<int>(row0 + t0));
         tc::bulk_commit();
       }
-      if (tid < kD)
-        ws[tid] += red[8 * kC + tid] + red[9 * kC + tid] + red[10 * kC + tid] + red[11 * kC + tid];
-      float rv[32];
-      tmem_ld32(tmem + tl + kTR + 32 * gw, rv);
-      store_row32<true>(base + Lay::XS, t, gw, rv);
+      if (tid < D) {
+        float dw = 0.f;
+#pragma unroll
+        for (int p = 0; p < kThreads / D; ++p) dw += red[8 * kC + p * D + tid];
+        ws[tid] += dw;
+      }
+      if (D == 128 || (gw < GD && t < D)) {
+        float rv[32];
+        tmem_ld32(tmem + tl + kTR + 32 * gw, rv);
+        store_row32<true>(base + Lay::XS, t, gw, rv);
+      }
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
@@ -824,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   otherwise (between the passes): the suffix-state increments of the blocks of the segments
 //     after a document's first (rblk_per_seg per segment), R = sum q' gnum^T and w = sum scale q'
 //     (gnum = g / den), as records [R row-major | w].
-template <bool kFwd>
+template <bool kFwd, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_blockstate(const BwdArgs b, const __grid_constant__ CUtensorMap tma_a,
                       const __grid_constant__ CUtensorMap tma_b) {
@@ -869,6 +910,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     *s_abort = misaligned ? 1 : 0;
   }
   if (tid < kD) ws[tid] = 0.f;
+  clear_upper_blocks<D>(base);
+  tc::fence_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -884,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < 2 && c < nch; ++c) {
       uint32_t t[2];
       tiles(c, t);
-      tma_chunk<2>(maps, t, h, static_cast<int>(row0 + s0 + c * kC), bar_ld0 + 8 * c);
+      tma_chunk<2, D>(maps, t, h, static_cast<int>(row0 + s0 + c * kC), bar_ld0 + 8 * c);
     }
     issued0 = 1;
     issued1 = nch > 1 ? 1 : 0;
@@ -912,8 +955,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();  // scl_s
     // rows past the document cleared; reverse: b = g / den in place
     if (!kFwd || t0 + kC > n) {
-      for (int idx = tid; idx < kC * 16; idx += kThreads) {
-        const int r = idx >> 4, m = idx & 15;
+      for (int idx = tid; idx < kC * D / 8; idx += kThreads) {
+        const int r = idx / (D / 8), m = idx % (D / 8);
         const uint32_t ga = t[1] + tile_off(r, m);
         if (t0 + r >= n) {
           sts16(ga, make_uint4(0, 0, 0, 0));
@@ -932,19 +975,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     if (tid == 0) {
-      constexpr uint32_t ID_MM = tc::idesc_bf16(128, 128, true, true);
+      constexpr uint32_t ID_MM = tc::idesc_bf16(128, D, true, true);
 #pragma unroll 1
       for (int kk = 0; kk < kC / 16; ++kk)
         tc::mma_bf16(tmem, mnmaj(t[0], kk, 16384), mnmaj(t[1], kk, 16384), ID_MM,
                      (c > 0 || kk > 0) ? 1u : 0u);
       tc::mma_commit(bar1);
     }
-    {  // partial increment of x: column i of a, rows 32 (tid / 128) .. + 31
-      const int i = tid & (kD - 1), r0 = 32 * (tid >> 7);
+    {  // partial increment of x: column i of a, rows RP (tid / D) .. + RP - 1
+      constexpr int RP = kC * D / kThreads;
+      const int i = tid & (D - 1), r0 = RP * (tid / D);
       const int m = i >> 3, e = i & 7;
       float dw = 0.f;
 #pragma unroll 4
-      for (int r = r0; r < r0 + 32; ++r) {
+      for (int r = r0; r < r0 + RP; ++r) {
         uint32_t word;
         asm volatile("ld.shared.b32 %0, [%1];"
                      : "=r"(word)
@@ -953,16 +997,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&word));
         dw = fmaf(scl_s[r], (e & 1) ? p.y : p.x, dw);
       }
-      red[(tid >> 7) * kC + i] = dw;
+      red[tid] = dw;  // partial tid / D of column i
     }
     if (!wait_mma(bar1, c & 1)) atomicExch(s_abort, 1);
     __syncthreads();  // the MMA and every thread are done with this set's tiles
     if (tid == 0 && c + 2 < nch && !*reinterpret_cast<volatile int*>(s_abort)) {
-      tma_chunk<2>(maps, t, h, static_cast<int>(row0 + t0 + 2 * kC), bar_ld0 + 8 * set);
+      tma_chunk<2, D>(maps, t, h, static_cast<int>(row0 + t0 + 2 * kC), bar_ld0 + 8 * set);
       if (set) ++issued1;
       else ++issued0;
     }
-    if (tid < kD) ws[tid] += red[tid] + red[kC + tid] + red[2 * kC + tid] + red[3 * kC + tid];
+    if (tid < D) {
+      float dw = 0.f;
+#pragma unroll
+      for (int p = 0; p < kThreads / D; ++p) dw += red[p * D + tid];
+      ws[tid] += dw;
+    }
     bad = *reinterpret_cast<volatile int*>(s_abort) != 0;
     __syncthreads();
   }
@@ -976,7 +1025,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q4 = warp & 3, gw = warp >> 2;
   const int tr = 32 * q4 + lane;
   float rv[32];
-  if (!bad) {
+  if (D == 64 && gw >= D / 32) {  // columns past d: the product has N = d
+#pragma unroll
+    for (int e = 0; e < 32; ++e) rv[e] = 0.f;
+  } else if (!bad) {
     tmem_ld32(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 32 * gw, rv);
   } else {
 #pragma unroll
@@ -1033,7 +1085,7 @@ __global__ void __launch_bounds__(kMThreads)
   if (tid == 0) {
     const CUtensorMap* const maps[1] = {which ? &tm_k : &tm_q};
     const uint32_t tl[1] = {tile};
-    tma_chunk<1>(maps, tl, h, static_cast<int>(row0 + t0), bar);
+    tma_chunk<1, D>(maps, tl, h, static_cast<int>(row0 + t0), bar);
   }
   const feat::FeatTab tab = feat::feat_tab<D>(reinterpret_cast<uint8_t*>(tabmem));
   feat::fill_tab<D>(tab, a, h, RPP, tid, kMThreads);
@@ -1114,7 +1166,7 @@ __global__ void __launch_bounds__(kMThreads, 3)
     if (tid == 0) {
       const CUtensorMap* const maps[2] = {which ? &tm_k : &tm_q, which ? &tm_dk : &tm_dq};
       const uint32_t tl[2] = {tiles_base, tiles_base + kTile};
-      tma_chunk<2>(maps, tl, h, static_cast<int>(row0 + t0), bar);
+      tma_chunk<2, D>(maps, tl, h, static_cast<int>(row0 + t0), bar);
     }
     const feat::FeatTab tab = feat::feat_tab<D>(reinterpret_cast<uint8_t*>(tabmem));
     feat::fill_tab<D>(tab, a, h, RPP, tid, kMThreads);
@@ -1207,10 +1259,14 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   static unsigned long long configured = 0;  // bit per device (idempotent; races are benign)
   if (dev < 64 && !((configured >> dev) & 1ull)) {
-    for (const void* f : {reinterpret_cast<const void*>(bwd_tc_forward),
-                          reinterpret_cast<const void*>(bwd_tc_reverse),
-                          reinterpret_cast<const void*>(bwd_tc_blockstate<true>),
-                          reinterpret_cast<const void*>(bwd_tc_blockstate<false>)}) {
+    for (const void* f : {reinterpret_cast<const void*>(bwd_tc_forward<64>),
+                          reinterpret_cast<const void*>(bwd_tc_forward<128>),
+                          reinterpret_cast<const void*>(bwd_tc_reverse<64>),
+                          reinterpret_cast<const void*>(bwd_tc_reverse<128>),
+                          reinterpret_cast<const void*>(bwd_tc_blockstate<true, 64>),
+                          reinterpret_cast<const void*>(bwd_tc_blockstate<true, 128>),
+                          reinterpret_cast<const void*>(bwd_tc_blockstate<false, 64>),
+                          reinterpret_cast<const void*>(bwd_tc_blockstate<false, 128>)}) {
       e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(Lay::BYTES));
       if (e != cudaSuccess) return e;
@@ -1242,8 +1298,9 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   if ((e = make_rows_map(&tmqf, b.qf, rows, b.p.H, d)) != cudaSuccess) return e;
   if ((e = make_rows_map(&tmkf, b.kf, rows, b.p.H, d)) != cudaSuccess) return e;
   if (b.nseg > 1) {  // the prefix-state increments of the blocks before each document's last segment
-    bwd_tc_blockstate<true><<<static_cast<unsigned>(static_cast<long>(b.p.n_docs) * b.p.H * b.nblk_max),
-                              kThreads, Lay::BYTES, stream>>>(b, tmkf, tmv);
+    const unsigned g = static_cast<unsigned>(static_cast<long>(b.p.n_docs) * b.p.H * b.nblk_max);
+    if (d == 128) bwd_tc_blockstate<true, 128><<<g, kThreads, Lay::BYTES, stream>>>(b, tmkf, tmv);
+    else bwd_tc_blockstate<true, 64><<<g, kThreads, Lay::BYTES, stream>>>(b, tmkf, tmv);
     note_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -1252,18 +1309,23 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   if ((e = make_rows_map(&tmdq, b.dqf, rows, b.p.H, d)) != cudaSuccess) return e;
   if ((e = make_rows_map(&tmdk, b.dkf, rows, b.p.H, d)) != cudaSuccess) return e;
   if ((e = make_rows_map(&tmdv, b.dv, rows, b.p.H, d)) != cudaSuccess) return e;
-  bwd_tc_forward<<<static_cast<unsigned>(grid), kThreadsA, Lay::BYTES, stream>>>(b, tmqf, tmkf, tmv,
-                                                                                 tmg, tmdq);
+  if (d == 128)
+    bwd_tc_forward<128><<<static_cast<unsigned>(grid), kThreadsA, Lay::BYTES, stream>>>(b, tmqf, tmkf, tmv, tmg, tmdq);
+  else
+    bwd_tc_forward<64><<<static_cast<unsigned>(grid), kThreadsA, Lay::BYTES, stream>>>(b, tmqf, tmkf, tmv, tmg, tmdq);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (b.nseg > 1) {
-    bwd_tc_blockstate<false><<<static_cast<unsigned>(grid * b.rblk_per_seg), kThreads, Lay::BYTES,
-                               stream>>>(b, tmqf, tmg);
+    const unsigned g = static_cast<unsigned>(grid * b.rblk_per_seg);
+    if (d == 128) bwd_tc_blockstate<false, 128><<<g, kThreads, Lay::BYTES, stream>>>(b, tmqf, tmg);
+    else bwd_tc_blockstate<false, 64><<<g, kThreads, Lay::BYTES, stream>>>(b, tmqf, tmg);
     note_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  bwd_tc_reverse<<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b, tmqf, tmkf, tmv,
-                                                                                 tmg, tmdv, tmdk);
+  if (d == 128)
+    bwd_tc_reverse<128><<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b, tmqf, tmkf, tmv, tmg, tmdv, tmdk);
+  else
+    bwd_tc_reverse<64><<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b, tmqf, tmkf, tmv, tmg, tmdv, tmdk);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (d == 128)
