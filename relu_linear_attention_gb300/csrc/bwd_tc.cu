@@ -134,6 +134,46 @@ __device__ __forceinline__ void clear_upper_blocks(uint32_t base) {
   }
 }
 
+// The per-row phases on the d feature columns give each of the four column groups W = d / 4 of
+// them: W consecutive fp32 TMEM columns of this thread's lane (two such reads in flight together
+// in the x2 form), and W values as bf16 into row r, columns W g .. W g + W - 1 of a tile.
+template <int W>
+__device__ __forceinline__ void tmem_ldn(uint32_t taddr, float (&v)[W]) {
+  if constexpr (W == 32) {
+    tmem_ld32(taddr, v);
+  } else {
+    uint32_t u[16];
+    tc::tmem_ld16(taddr, u);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(u[e]);
+  }
+}
+template <int W>
+__device__ __forceinline__ void tmem_ldnx2(uint32_t ta, float (&va)[W], uint32_t tb, float (&vb)[W]) {
+  if constexpr (W == 32) {
+    tmem_ld32x2(ta, va, tb, vb);
+  } else {
+    uint32_t u[2][16];
+    tc::tmem_ld16(ta, u[0]);
+    tc::tmem_ld16(tb, u[1]);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      va[e] = __uint_as_float(u[0][e]);
+      vb[e] = __uint_as_float(u[1][e]);
+    }
+  }
+}
+template <bool DROWS, int W>
+__device__ __forceinline__ void store_rown(uint32_t tile, int r, int g, const float (&v)[W]) {
+#pragma unroll
+  for (int m = 0; m < W / 8; ++m) {
+    const int ch = (W / 8) * g + m;
+    feat::sts16(tile + (DROWS ? dtile_off(r, ch) : tile_off(r, ch)), feat::pack8(v + 8 * m));
+  }
+}
+
 // Rows nvalid .. 127 of a tile set to zero (all threads).
 __device__ __forceinline__ void clear_rows(uint32_t tile, int nvalid) {
   for (int idx = threadIdx.x + nvalid * 16; idx < kC * 16; idx += kThreads)
@@ -252,6 +292,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
   // the prefix state at the segment's start: the increments of the blocks before it, in order
   // (the worker warps: lane quarter q4, column group gw < 4; the issuing warp takes no part)
   constexpr int GD = D / 32;  // column groups of 32 that hold one of the d feature columns
+  constexpr int W = D / 4;    // d columns per column group in the per-row phases
   if (nch > 0 && warp < kWarps) {
     clear_upper_blocks<D>(base);
     const int nb = seg * b.blk_per_seg;
@@ -387,13 +428,13 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     }
     float nst = 0.f;
     if (!wait_mma(bar1b, c & 1)) atomicExch(s_abort, 1);
-    if (D == 128 || gw < GD) {  // U has d columns
-      float u[32];
-      tmem_ld32(tmem + tl + kTU + 32 * gw, u);
+    {  // U has d columns
+      float u[W];
+      tmem_ldn<W>(tmem + tl + kTU + W * gw, u);
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
+      for (int m = 0; m < W / 8; ++m) {
         float f[8];
-        unpack8(lds16(base + Lay::QF + tile_off(t, 4 * gw + m)), f);
+        unpack8(lds16(base + Lay::QF + tile_off(t, (W / 8) * gw + m)), f);
 #pragma unroll
         for (int e = 0; e < 8; ++e) nst += f[e] * u[8 * m + e];
       }
@@ -438,20 +479,20 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     // ---- phase 4 (the issuing warp): U += A'~ K'; then the next chunk's tiles
     if (!wait_mma(bar2, c & 1)) atomicExch(s_abort, 1);
     // ---- phase 5: dq' = U / den + scale z (bf16, to the workspace); S -> S~ (d columns)
-    if (D == 128 || gw < GD) {
-      float u[32], sv[32];
-      tmem_ld32x2(tmem + tl + kTU + 32 * gw, u, tmem + tl + kTS + 32 * gw, sv);
+    {
+      float u[W], sv[W];
+      tmem_ldnx2<W>(tmem + tl + kTU + W * gw, u, tmem + tl + kTS + W * gw, sv);
       const float inv = 1.0f / den;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) u[j] = fmaf(u[j], inv, scale * zs[32 * gw + j]);
+      for (int j = 0; j < W; ++j) u[j] = fmaf(u[j], inv, scale * zs[W * gw + j]);
       if (t0 + kC <= n) {  // a whole chunk: staged in AS (its last reader, phase 4, is done)
-        store_row32<false>(base + Lay::AS, t, gw, u);
-      } else if (valid && gw < b.d / 32) {  // the ragged last chunk row by row
-        __nv_bfloat16* dst = dqf_out + ((row0 + t0 + t) * a.H + h) * b.d + 32 * gw;
+        store_rown<false, W>(base + Lay::AS, t, gw, u);
+      } else if (valid && (D == 64 || gw < b.d / 32)) {  // the ragged last chunk row by row
+        __nv_bfloat16* dst = dqf_out + ((row0 + t0 + t) * a.H + h) * b.d + W * gw;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(u + 8 * m);
+        for (int m = 0; m < W / 8; ++m) *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(u + 8 * m);
       }
-      if (D == 128 || t < D) store_row32<true>(base + Lay::XS, t, gw, sv);
+      if (D == 128 || t < D) store_rown<true, W>(base + Lay::XS, t, gw, sv);
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
@@ -560,6 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_issued = tmaq_issued = 1;
   }
   constexpr int GD = D / 32;  // column groups of 32 that hold one of the d feature columns
+  constexpr int W = D / 4;    // d columns per column group in the per-row phases
   clear_upper_blocks<D>(base);
   // the suffix state at the segment's end: the later segments' increments, in segment order
   if (nch > 0) {
@@ -763,15 +805,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // a whole chunk's dv and dk' are staged in shared memory and written by TMA (full lines); the
     // ragged last chunk of a document is written row by row (a tile store would reach past it)
     const bool whole = t0 + kC <= n;
-    if (D == 128 || gw < GD) {
-      float o[32];
-      tmem_ld32(tmem + tl + kTDV + 32 * gw, o);
+    {
+      float o[W];
+      tmem_ldn<W>(tmem + tl + kTDV + W * gw, o);
       if (whole) {  // into XS: R~'s last readers (the first two groups) are done
-        store_row32<false>(base + Lay::XS, t, gw, o);
+        store_rown<false, W>(base + Lay::XS, t, gw, o);
       } else if (t0 + t < n) {
-        __nv_bfloat16* dst = dv + ((row0 + t0 + t) * a.H + h) * D + 32 * gw;
+        __nv_bfloat16* dst = dv + ((row0 + t0 + t) * a.H + h) * D + W * gw;
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
+        for (int m = 0; m < W / 8; ++m)
           *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(o + 8 * m);
       }
     }
@@ -794,17 +836,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- phase 7: dk' + w into the staging, w += sum_t scale_t q'_t, R -> R~
     {
-      if (D == 128 || gw < GD) {
-        float o[32];
-        tmem_ld32(tmem + tl + kTDK + 32 * gw, o);
+      {
+        float o[W];
+        tmem_ldn<W>(tmem + tl + kTDK + W * gw, o);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] += ws[32 * gw + j];
+        for (int j = 0; j < W; ++j) o[j] += ws[W * gw + j];
         if (whole) {  // into AS: A's last reader (the third group) is done
-          store_row32<false>(base + Lay::AS, t, gw, o);
+          store_rown<false, W>(base + Lay::AS, t, gw, o);
         } else if (t0 + t < n) {  // dk' (bf16) to the workspace
-          __nv_bfloat16* dst = dkf_out + ((row0 + t0 + t) * a.H + h) * D + 32 * gw;
+          __nv_bfloat16* dst = dkf_out + ((row0 + t0 + t) * a.H + h) * D + W * gw;
 #pragma unroll
-          for (int m = 0; m < 4; ++m) *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(o + 8 * m);
+          for (int m = 0; m < W / 8; ++m) *reinterpret_cast<uint4*>(dst + 8 * m) = feat::pack8(o + 8 * m);
         }
       }
       tc::fence_async_smem();
@@ -823,10 +865,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int p = 0; p < kThreads / D; ++p) dw += red[8 * kC + p * D + tid];
         ws[tid] += dw;
       }
-      if (D == 128 || (gw < GD && t < D)) {
-        float rv[32];
-        tmem_ld32(tmem + tl + kTR + 32 * gw, rv);
-        store_row32<true>(base + Lay::XS, t, gw, rv);
+      if (D == 128 || t < D) {
+        float rv[W];
+        tmem_ldn<W>(tmem + tl + kTR + W * gw, rv);
+        store_rown<true, W>(base + Lay::XS, t, gw, rv);
       }
     }
     tc::fence_async_smem();
