@@ -1170,20 +1170,21 @@ __global__ void __launch_bounds__(kMThreads)
 //   h = R^T (da, db) (the inverse rotation), u = gamma h,
 //   dx = r u - x r^3 (u . x) / d,   dgamma += h x r.
 // The chunk's rows of x and of its feature gradient are staged in shared memory by TMA (two 32 KB
-// tiles per CTA, three CTAs per SM), so that each SM has ~200 KB of loads in flight.
+// tiles per CTA, three CTAs per SM), so that each SM has ~200 KB of loads in flight. One launch
+// takes one of q (which = 0) and k (which = 1): dq needs only pass A's dq', so it runs while the
+// reverse pass does.
 constexpr uint32_t kFeatSmem = 2 * kTile + 1024;  // two tiles (+ alignment slack)
 
 template <int D>
 __global__ void __launch_bounds__(kMThreads, 3)
     bwd_tc_features(const BwdArgs b, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_dq,
-                    const __grid_constant__ CUtensorMap tm_dk) {
+                    const __grid_constant__ CUtensorMap tm_dk, const int which) {
   constexpr int TPR = D / 8, RPP = kMThreads / TPR, NPASS = kC / RPP;
   constexpr int WARPS = kMThreads / 32;
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int which = blockIdx.x & 1;  // 0: q, 1: k
-  const int chunk = (blockIdx.x >> 1) % b.chunks_max, unit = (blockIdx.x >> 1) / b.chunks_max;
+  const int chunk = blockIdx.x % b.chunks_max, unit = blockIdx.x / b.chunks_max;
   const int h = unit % a.H, doc = unit / a.H;
   long row0;
   int n;
@@ -1295,6 +1296,39 @@ __global__ void __launch_bounds__(kMThreads, 3)
 
 bool bwd_tc_supported(DType dt, int d) { return dt == DType::BF16 && (d == 64 || d == 128); }
 
+namespace {
+// Per thread and device: a stream of the greatest priority that carries the backward's critical
+// path (feature map, block states, both passes, dk), forked from the caller's stream and joined back
+// to it, and the three events of the fork, the hand-over after pass A and the join. The feature
+// backward of q runs on the caller's stream meanwhile; with the priorities the passes' CTAs are
+// dispatched first and it fills the SMs they leave idle.
+struct Side {
+  cudaStream_t hi = nullptr;
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+};
+cudaError_t side_stream(int dev, Side*& out) {
+  thread_local Side side[64];
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  Side& sd = side[dev];
+  if (sd.hi == nullptr) {
+    int least = 0, greatest = 0;
+    Side n;
+    cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&n.hi, cudaStreamNonBlocking, greatest);
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&n.ev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      for (cudaEvent_t ev : n.ev)
+        if (ev != nullptr) cudaEventDestroy(ev);
+      if (n.hi != nullptr) cudaStreamDestroy(n.hi);
+      return e;
+    }
+    sd = n;
+  }
+  out = &sd;
+  return cudaSuccess;
+}
+}  // namespace
+
 cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1323,62 +1357,83 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   }
   const long grid = static_cast<long>(b.p.n_docs) * b.p.H * b.nseg;
   if (grid == 0) return cudaSuccess;
-  const long fgrid = static_cast<long>(b.p.n_docs) * b.p.H * b.chunks_max * 2;
-  const int d = b.d;  // the tensors' head size; the tiles are 128 columns wide
+  const long fgrid = static_cast<long>(b.p.n_docs) * b.p.H * b.chunks_max;  // per tensor
+  const int d = b.d;  // the tensors' head size
+  Side* side = nullptr;
+  if ((e = side_stream(dev, side)) != cudaSuccess) return e;
+  const cudaStream_t user = stream;
+  if ((e = cudaEventRecord(side->ev[0], user)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(side->hi, side->ev[0], 0)) != cudaSuccess) return e;
+  stream = side->hi;
+  // from here on every exit joins the side stream back to the caller's stream first
+  const auto join = [&](cudaError_t err) {
+    cudaError_t j = cudaEventRecord(side->ev[2], side->hi);
+    if (j == cudaSuccess) j = cudaStreamWaitEvent(user, side->ev[2], 0);
+    return err != cudaSuccess ? err : j;
+  };
   CUtensorMap tmq, tmk;
-  if ((e = make_rows_map(&tmq, b.p.q, b.p.total_rows, b.p.H, d)) != cudaSuccess) return e;
-  if ((e = make_rows_map(&tmk, b.p.k, b.p.total_rows, b.p.H, d)) != cudaSuccess) return e;
-  if (d == 128) bwd_tc_featmap<128><<<static_cast<unsigned>(fgrid), kMThreads, kTile + 1024, stream>>>(b, tmq, tmk);
-  else bwd_tc_featmap<64><<<static_cast<unsigned>(fgrid), kMThreads, kTile + 1024, stream>>>(b, tmq, tmk);
+  if ((e = make_rows_map(&tmq, b.p.q, b.p.total_rows, b.p.H, d)) != cudaSuccess) return join(e);
+  if ((e = make_rows_map(&tmk, b.p.k, b.p.total_rows, b.p.H, d)) != cudaSuccess) return join(e);
+  if (d == 128) bwd_tc_featmap<128><<<static_cast<unsigned>(2 * fgrid), kMThreads, kTile + 1024, stream>>>(b, tmq, tmk);
+  else bwd_tc_featmap<64><<<static_cast<unsigned>(2 * fgrid), kMThreads, kTile + 1024, stream>>>(b, tmq, tmk);
   note_launches(1);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = cudaGetLastError()) != cudaSuccess) return join(e);
   // TMA maps of the row-major [rows, H, D] tensors the kernels stream
   CUtensorMap tmv, tmg, tmqf, tmkf;
   const long rows = b.p.total_rows;
-  if ((e = make_rows_map(&tmv, b.p.v, rows, b.p.H, d)) != cudaSuccess) return e;
-  if ((e = make_rows_map(&tmg, b.dout, rows, b.p.H, d)) != cudaSuccess) return e;
-  if ((e = make_rows_map(&tmqf, b.qf, rows, b.p.H, d)) != cudaSuccess) return e;
-  if ((e = make_rows_map(&tmkf, b.kf, rows, b.p.H, d)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmv, b.p.v, rows, b.p.H, d)) != cudaSuccess) return join(e);
+  if ((e = make_rows_map(&tmg, b.dout, rows, b.p.H, d)) != cudaSuccess) return join(e);
+  if ((e = make_rows_map(&tmqf, b.qf, rows, b.p.H, d)) != cudaSuccess) return join(e);
+  if ((e = make_rows_map(&tmkf, b.kf, rows, b.p.H, d)) != cudaSuccess) return join(e);
   if (b.nseg > 1) {  // the prefix-state increments of the blocks before each document's last segment
     const unsigned g = static_cast<unsigned>(static_cast<long>(b.p.n_docs) * b.p.H * b.nblk_max);
     if (d == 128) bwd_tc_blockstate<true, 128><<<g, kThreads, Lay::BYTES, stream>>>(b, tmkf, tmv);
     else bwd_tc_blockstate<true, 64><<<g, kThreads, Lay::BYTES, stream>>>(b, tmkf, tmv);
     note_launches(1);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = cudaGetLastError()) != cudaSuccess) return join(e);
   }
   // dq', dk' (written by the passes, read by the feature kernel) and dv
   CUtensorMap tmdq, tmdk, tmdv;
-  if ((e = make_rows_map(&tmdq, b.dqf, rows, b.p.H, d)) != cudaSuccess) return e;
-  if ((e = make_rows_map(&tmdk, b.dkf, rows, b.p.H, d)) != cudaSuccess) return e;
-  if ((e = make_rows_map(&tmdv, b.dv, rows, b.p.H, d)) != cudaSuccess) return e;
+  if ((e = make_rows_map(&tmdq, b.dqf, rows, b.p.H, d)) != cudaSuccess) return join(e);
+  if ((e = make_rows_map(&tmdk, b.dkf, rows, b.p.H, d)) != cudaSuccess) return join(e);
+  if ((e = make_rows_map(&tmdv, b.dv, rows, b.p.H, d)) != cudaSuccess) return join(e);
   if (d == 128)
     bwd_tc_forward<128><<<static_cast<unsigned>(grid), kThreadsA, Lay::BYTES, stream>>>(b, tmqf, tmkf, tmv, tmg, tmdq);
   else
     bwd_tc_forward<64><<<static_cast<unsigned>(grid), kThreadsA, Lay::BYTES, stream>>>(b, tmqf, tmkf, tmv, tmg, tmdq);
   note_launches(1);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = cudaGetLastError()) != cudaSuccess) return join(e);
+  // dq through the feature map needs only pass A: on the caller's stream, beside the reverse pass
+  if ((e = cudaEventRecord(side->ev[1], stream)) != cudaSuccess) return join(e);
+  if ((e = cudaStreamWaitEvent(user, side->ev[1], 0)) != cudaSuccess) return join(e);
+  if (d == 128)
+    bwd_tc_features<128><<<static_cast<unsigned>(fgrid), kMThreads, kFeatSmem, user>>>(b, tmq, tmk, tmdq, tmdk, 0);
+  else
+    bwd_tc_features<64><<<static_cast<unsigned>(fgrid), kMThreads, kFeatSmem, user>>>(b, tmq, tmk, tmdq, tmdk, 0);
+  note_launches(1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return join(e);
   if (b.nseg > 1) {
     const unsigned g = static_cast<unsigned>(grid * b.rblk_per_seg);
     if (d == 128) bwd_tc_blockstate<false, 128><<<g, kThreads, Lay::BYTES, stream>>>(b, tmqf, tmg);
     else bwd_tc_blockstate<false, 64><<<g, kThreads, Lay::BYTES, stream>>>(b, tmqf, tmg);
     note_launches(1);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = cudaGetLastError()) != cudaSuccess) return join(e);
   }
   if (d == 128)
     bwd_tc_reverse<128><<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b, tmqf, tmkf, tmv, tmg, tmdv, tmdk);
   else
     bwd_tc_reverse<64><<<static_cast<unsigned>(grid), kThreads, Lay::BYTES, stream>>>(b, tmqf, tmkf, tmv, tmg, tmdv, tmdk);
   note_launches(1);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = cudaGetLastError()) != cudaSuccess) return join(e);
   if (d == 128)
-    bwd_tc_features<128><<<static_cast<unsigned>(fgrid), kMThreads, kFeatSmem, stream>>>(b, tmq, tmk, tmdq, tmdk);
+    bwd_tc_features<128><<<static_cast<unsigned>(fgrid), kMThreads, kFeatSmem, stream>>>(b, tmq, tmk, tmdq, tmdk, 1);
   else
-    bwd_tc_features<64><<<static_cast<unsigned>(fgrid), kMThreads, kFeatSmem, stream>>>(b, tmq, tmk, tmdq, tmdk);
+    bwd_tc_features<64><<<static_cast<unsigned>(fgrid), kMThreads, kFeatSmem, stream>>>(b, tmq, tmk, tmdq, tmdk, 1);
   note_launches(1);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = join(cudaGetLastError())) != cudaSuccess) return e;
   BwdArgs g = b;  // the gain partials are per (document, head, chunk)
   g.nseg = b.chunks_max;
-  return launch_bwd_gain(g, d, stream);
+  return launch_bwd_gain(g, d, user);
 }
 
 }  // namespace rapt
