@@ -459,6 +459,7 @@ rapt_status backward_common(const void* q, const void* k, const void* v, const v
   b.dkf = w + plan.off_dkf;
   b.chunks_max = plan.chunks_max;
   b.d = d;
+  b.order = (tc && cu_seqlens != nullptr && n_docs > 1) ? reinterpret_cast<int*>(w + plan.off_order) : nullptr;
   if (tc) return from_cuda(rapt::launch_backward_tc(b, s));
   return from_cuda(rapt::launch_backward_simt(to_dt(dtype), d, b, s));
 }

@@ -716,7 +716,8 @@ BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d, bool
   p.off_dkf = p.off_dqf + feats;
   p.off_dgq = p.off_dkf + feats;
   p.off_dgk = p.off_dgq + gp;
-  p.ws_bytes = p.off_dgk + gp;
+  p.off_order = p.off_dgk + gp;
+  p.ws_bytes = p.off_order + (tc ? up(static_cast<size_t>(n_docs) * sizeof(int)) : 0);
   return p;
 }
 

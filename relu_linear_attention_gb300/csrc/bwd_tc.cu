@@ -238,8 +238,9 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                    const __grid_constant__ CUtensorMap tmg, const __grid_constant__ CUtensorMap tmdq) {
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int seg = blockIdx.x % b.nseg, unit = blockIdx.x / b.nseg;
-  const int h = unit % a.H, doc = unit / a.H;
+  const int seg = blockIdx.x % b.nseg, slot = blockIdx.x / b.nseg;  // packed: longest first
+  const int h = slot % a.H, doc = b.order != nullptr ? b.order[slot / a.H] : slot / a.H;
+  const int unit = doc * a.H + h;
   long row0;
   int n;
   if (!doc_bounds(a, doc, row0, n) && h == 0 && seg == 0 && tid == 0 && a.dev_status != nullptr)
@@ -544,8 +545,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmdk) {
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int seg = blockIdx.x % b.nseg, unit = blockIdx.x / b.nseg;
-  const int h = unit % a.H, doc = unit / a.H;
+  const int seg = blockIdx.x % b.nseg, slot = blockIdx.x / b.nseg;  // packed: longest first
+  const int h = slot % a.H, doc = b.order != nullptr ? b.order[slot / a.H] : slot / a.H;
+  const int unit = doc * a.H + h;
   long row0;
   int n;
   doc_bounds(a, doc, row0, n);
@@ -1378,6 +1380,10 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   else bwd_tc_featmap<64><<<static_cast<unsigned>(2 * fgrid), kMThreads, kTile + 1024, stream>>>(b, tmq, tmk);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return join(e);
+  if (b.order != nullptr) {  // packed documents: the passes take the longest first
+    if ((e = launch_doc_order(b.p.cu_seqlens, b.p.n_docs, b.p.total_rows, b.order, stream)) != cudaSuccess)
+      return join(e);
+  }
   // TMA maps of the row-major [rows, H, D] tensors the kernels stream
   CUtensorMap tmv, tmg, tmqf, tmkf;
   const long rows = b.p.total_rows;

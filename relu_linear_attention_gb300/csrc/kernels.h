@@ -84,7 +84,10 @@ struct BwdArgs {
   void* dqf;
   void* dkf;
   int chunks_max;
-  int d;  // head size of q, k, v and the gradients (the tensor-core passes pad it to 128 inside)
+  int d;  // head size of q, k, v and the gradients
+  // tensor-core path, packed documents: the passes' CTA slots take the documents in order of
+  // decreasing length (order[rank] = document, written by the doc-order kernel); nullable
+  int* order;
 };
 struct BwdPlan {
   int nseg;
@@ -94,7 +97,7 @@ struct BwdPlan {
   int nblk_max;      // tensor-core path
   int chunks_max;   // tensor-core path: 128-token chunks of the longest document
   size_t off_rev, off_den, off_scl, off_sst, off_nst, off_dgq, off_dgk, off_qf, off_kf, off_dqf,
-      off_dkf;
+      off_dkf, off_order;
   size_t ws_bytes;
 };
 // tc: the tensor-core path (one CTA per (document, head), no segment increments).
