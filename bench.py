@@ -466,7 +466,7 @@ def run_gpu(args, rank, world, local):
                            "kernels": "doc_order_kernel + prefill_tc_kernel<128, true> (one call: the "
                                       "d = 64 heads two per CTA, one segment per document, longest "
                                       "first)"}}
-    # its backward (dq, dk, dv, dgamma; the tensor-core passes on 128-column tiles, 64 of them zero)
+    # its backward (dq, dk, dv, dgamma; the tensor-core passes with d = 64 products)
     vg = torch.empty_like(vq).normal_(generator=torch.Generator(device=device).manual_seed(6))
     vws = torch.empty(lib.rapt_varlen_bwd_workspace_size(wv.T, len(wv.lengths), 32, 64, msl, 1),
                       dtype=torch.uint8, device=device)
@@ -485,12 +485,13 @@ def run_gpu(args, rank, world, local):
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": vb_bytes / (vb_mean * 1e-3) / 1e9 / peaks["hbm_gbs"],
                      "algorithmic_bytes_per_call": vb_bytes,
-                     "traffic": read_traffic("varlen_backward", "bwd_tc_featmap", "bwd_tc_forward",
-                                             "bwd_tc_reverse", "bwd_tc_features", "bwd_gain_kernel",
-                                             "bwd_gain_final"),
-                     "kernels": "bwd_tc_featmap<64> + bwd_tc_forward + bwd_tc_reverse + "
-                                "bwd_tc_features<64> + bwd_gain_kernel + bwd_gain_final (one call: "
-                                "one segment per document, tiles padded to 128 columns)"}}
+                     "traffic": read_traffic("varlen_backward", "bwd_tc_featmap", "doc_order_kernel",
+                                             "bwd_tc_forward", "bwd_tc_reverse", "bwd_tc_features*2",
+                                             "bwd_gain_kernel", "bwd_gain_final"),
+                     "kernels": "bwd_tc_featmap<64> + doc_order_kernel + bwd_tc_forward<64> + "
+                                "bwd_tc_reverse<64> + 2 x bwd_tc_features<64> + bwd_gain_kernel + "
+                                "bwd_gain_final (one call: one segment per document, longest first; "
+                                "the features of q beside the reverse pass)"}}
     del vq, vk, vv, vo, wv, vg, vws, vgr
 
     # ---------------- original RLA, L2 denominator (B=2, L=16384, H=16, d=128)
@@ -581,10 +582,11 @@ def run_gpu(args, rank, world, local):
                              "traffic": read_traffic("backward", "bwd_tc_featmap",
                                                      "bwd_tc_blockstate<true>", "bwd_tc_forward",
                                                      "bwd_tc_blockstate<false>", "bwd_tc_reverse",
-                                                     "bwd_tc_features", "bwd_gain_kernel"),
+                                                     "bwd_tc_features*2", "bwd_gain_kernel"),
                              "kernels": "bwd_tc_featmap + bwd_tc_blockstate<true> + bwd_tc_forward + "
                                         "bwd_tc_blockstate<false> + bwd_tc_reverse + "
-                                        "bwd_tc_features + bwd_gain_kernel (one call; tensor cores)"}}
+                                        "2 x bwd_tc_features (q beside the reverse pass, then k) + "
+                                        "bwd_gain_kernel (one call; tensor cores)"}}
     del tg, gws, grads
 
     # ---------------- one RAPT layer around the headline attention (d_model = H d = 2048), and its
@@ -675,9 +677,16 @@ def run_gpu(args, rank, world, local):
 
 def read_traffic(case: str, *kernels: str):
     """DRAM bytes per call of workload ``case`` (a ``--only`` name), summed over ``kernels`` (the
-    launches of one call), from the committed ncu summary; None unless every kernel has a row for
-    that case taken on its source as it is now (each row records a hash of the source file)."""
+    launches of one call; ``name*n``: n launches of that kernel per call), from the committed ncu
+    summary; None unless every kernel has a row for that case taken on its source as it is now (each
+    row records a hash of the source file)."""
     import hashlib
+
+    count = {}
+    for k in kernels:
+        name, _, n = k.partition("*")
+        count[name] = int(n) if n else 1
+    kernels = tuple(count)
 
     table = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(table):
@@ -692,7 +701,7 @@ def read_traffic(case: str, *kernels: str):
             h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
             if h != parts[3]:
                 return None
-            found[parts[1]] = float(parts[4])
+            found[parts[1]] = float(parts[4]) * count[parts[1]]
     return sum(found.values()) if len(found) == len(kernels) else None
 
 
