@@ -1,8 +1,8 @@
 // Backward of causal RLA-2 on the 5th-generation tensor cores (tcgen05 + TMEM), sm_103a; bf16
-// tensors, d = 64 or 128, fp32 accumulation and fp32 states. The passes work on 128-column tiles:
-// at d = 64 the TMA fills columns 64..127 of every loaded tile with zeros, so the products, the
-// states and their records carry zero columns (the records keep the 128 x 128 layout), and only
-// the first d columns of a row are written out.
+// tensors, d = 64 or 128, fp32 accumulation and fp32 states. The passes keep 128-column tiles in
+// shared memory; at d = 64 only the first 64-column block of a streamed tile is loaded (the second
+// is cleared once), the products whose output has d columns run with N = d and those that contract
+// over the features with K = d, and the state records keep the 128 x 128 layout.
 //
 // The gradients of sum dout . out (08-rapt-algorithm.md §4.2 "backward": the main and z scans,
 // gnum = g / den and scale = -(g . num) / den^2, two suffix scans, then ReLU, RoPE and RMSNorm
@@ -36,7 +36,9 @@
 // is written row by row.
 // Then, fully parallel over (document, head, chunk), dq and dk through the feature map (ReLU mask,
 // inverse RoPE rotation, RMSNorm backward) from dq', dk' and the raw q, k, with gain partials
-// (bwd_tc_features), and the gains summed in a fixed order.
+// (bwd_tc_features, one launch per tensor: dq's runs beside pass B on the caller's stream while the
+// rest runs on a stream of higher priority), and the gains summed in a fixed order. With packed
+// documents the passes take the documents longest first.
 // The passes run one CTA per (document, head, segment) with 512 worker threads in lockstep phases:
 // they read TMEM rows (thread = TMEM lane = tile row, four warps per lane quarter splitting the
 // columns) and do the per-row arithmetic. In pass B one of them issues the MMAs and the TMA copies

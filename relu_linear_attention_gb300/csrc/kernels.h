@@ -100,12 +100,14 @@ struct BwdPlan {
       off_dkf, off_order;
   size_t ws_bytes;
 };
-// tc: the tensor-core path (one CTA per (document, head), no segment increments).
+// tc: the tensor-core path (128-token chunks; the workspace also holds its block-state records,
+// q', k', dq', dk' and the document order).
 BwdPlan bwd_plan(int n_docs, int H, int max_seqlen, long total_rows, int d, bool tc);
 cudaError_t launch_backward_simt(DType dt, int d, const BwdArgs& b, cudaStream_t stream);
 // The gain gradients from the per-(document, head, segment) partials (launched by both paths).
 cudaError_t launch_bwd_gain(const BwdArgs& b, int d, cudaStream_t stream);
-// Tensor-core backward (bf16, d = 128): two passes, then the gains.
+// Tensor-core backward (bf16, d = 64 or 128): the feature map, two passes, the feature backward,
+// then the gains.
 bool bwd_tc_supported(DType dt, int d);
 cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream);
 
