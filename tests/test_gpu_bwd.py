@@ -208,6 +208,38 @@ def test_prefill_bwd_repeats_bitwise(cuda_device, lib):
             assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_prefill_bwd_side_stream_and_graph(cuda_device, lib, d):
+    """The tensor-core backward forks its critical path onto a stream of its own and joins it back:
+    the same bits on the default stream, on another stream, and replayed from a CUDA graph."""
+    q, k, v = draw(335, (2, 700, 3, d), "bf16")
+    (g,) = draw(336, (2, 700, 3, d), "bf16")[:1]
+    gq, gk = gammas(337, 3, d, True)
+    dev = lambda x: torch.from_numpy(x).to(cuda_device)
+    args = [to_dev(x, "bf16") for x in (q, k, v, g)] + [dev(gq), dev(gk)]
+    first = [t.clone() for t in R.rapt_prefill_bwd(*args)]
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream(device=cuda_device)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        again = R.rapt_prefill_bwd(*args)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for a, b in zip(first, again):
+        assert torch.equal(a, b)
+    outs = [torch.full_like(t, float("nan")) for t in first]
+    ws = torch.empty(lib.rapt_prefill_bwd_workspace_size(2, 700, 3, d, 1), dtype=torch.uint8,
+                     device=cuda_device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        R.rapt_prefill_bwd(*args, dq=outs[0], dk=outs[1], dv=outs[2], dgamma_q=outs[3],
+                           dgamma_k=outs[4], workspace=ws)
+    graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(first, outs):
+        assert torch.equal(a, b)
+
+
 def test_prefill_bwd_without_gains_and_empty(cuda_device, lib):
     q, k, v = draw(340, (1, 40, 2, 32), "f32")
     (g,) = draw(341, (1, 40, 2, 32), "f32")[:1]
