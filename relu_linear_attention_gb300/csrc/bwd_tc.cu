@@ -1174,18 +1174,25 @@ __global__ void __launch_bounds__(kMThreads)
 //   h = R^T (da, db) (the inverse rotation), u = gamma h,
 //   dx = r u - x r^3 (u . x) / d,   dgamma += h x r.
 // The chunk's rows of x and of its feature gradient are staged in shared memory by TMA (two 32 KB
-// tiles per CTA, three CTAs per SM), so that each SM has ~200 KB of loads in flight. One launch
+// tiles per CTA, three CTAs per SM; at d = 64 two 16 KB tiles, 128 threads and six CTAs per SM),
+// so that each SM has ~200 KB of loads in flight. One launch
 // takes one of q (which = 0) and k (which = 1): dq needs only pass A's dq', so it runs while the
 // reverse pass does.
-constexpr uint32_t kFeatSmem = 2 * kTile + 1024;  // two tiles (+ alignment slack)
+template <int D>
+struct FeatCfg {
+  static constexpr int THREADS = D == 64 ? 128 : 256, MIN_CTAS = D == 64 ? 6 : 3;
+  static constexpr uint32_t TILE = kC * D * 2;            // one chunk's rows (D / 64 blocks)
+  static constexpr uint32_t SMEM = 2 * TILE + 1024;       // two tiles (+ alignment slack)
+};
 
 template <int D>
-__global__ void __launch_bounds__(kMThreads, 3)
+__global__ void __launch_bounds__(FeatCfg<D>::THREADS, FeatCfg<D>::MIN_CTAS)
     bwd_tc_features(const BwdArgs b, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_dq,
                     const __grid_constant__ CUtensorMap tm_dk, const int which) {
-  constexpr int TPR = D / 8, RPP = kMThreads / TPR, NPASS = kC / RPP;
-  constexpr int WARPS = kMThreads / 32;
+  constexpr int NT = FeatCfg<D>::THREADS;
+  constexpr int TPR = D / 8, RPP = NT / TPR, NPASS = kC / RPP;
+  constexpr int WARPS = NT / 32;
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int chunk = blockIdx.x % b.chunks_max, unit = blockIdx.x / b.chunks_max;
@@ -1212,11 +1219,11 @@ __global__ void __launch_bounds__(kMThreads, 3)
     __syncthreads();
     if (tid == 0) {
       const CUtensorMap* const maps[2] = {which ? &tm_k : &tm_q, which ? &tm_dk : &tm_dq};
-      const uint32_t tl[2] = {tiles_base, tiles_base + kTile};
+      const uint32_t tl[2] = {tiles_base, tiles_base + FeatCfg<D>::TILE};
       tma_chunk<2, D>(maps, tl, h, static_cast<int>(row0 + t0), bar);
     }
     const feat::FeatTab tab = feat::feat_tab<D>(reinterpret_cast<uint8_t*>(tabmem));
-    feat::fill_tab<D>(tab, a, h, RPP, tid, kMThreads);
+    feat::fill_tab<D>(tab, a, h, RPP, tid, NT);
     __syncthreads();
     const long rstride = static_cast<long>(a.H) * D;
     const long off0 = (row0 + t0 + prow) * rstride + static_cast<long>(h) * D + e0;
@@ -1235,7 +1242,7 @@ __global__ void __launch_bounds__(kMThreads, 3)
         const int r = (p0 + i) * RPP + prow;
         const bool valid = t0 + r < n;
         rx[i] = valid ? feat::lds16(tiles_base + tile_off(r, part)) : make_uint4(0, 0, 0, 0);
-        rd[i] = valid ? feat::lds16(tiles_base + kTile + tile_off(r, part)) : make_uint4(0, 0, 0, 0);
+        rd[i] = valid ? feat::lds16(tiles_base + FeatCfg<D>::TILE + tile_off(r, part)) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
@@ -1351,12 +1358,12 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
                                static_cast<int>(Lay::BYTES));
       if (e != cudaSuccess) return e;
     }
-    for (const void* f : {reinterpret_cast<const void*>(bwd_tc_features<64>),
-                          reinterpret_cast<const void*>(bwd_tc_features<128>)}) {
-      e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kFeatSmem));
-      if (e != cudaSuccess) return e;
-    }
+    e = cudaFuncSetAttribute(bwd_tc_features<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(FeatCfg<64>::SMEM));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(bwd_tc_features<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(FeatCfg<128>::SMEM));
+    if (e != cudaSuccess) return e;
     configured |= 1ull << dev;
   }
   const long grid = static_cast<long>(b.p.n_docs) * b.p.H * b.nseg;
@@ -1415,9 +1422,11 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   if ((e = cudaEventRecord(side->ev[1], stream)) != cudaSuccess) return join(e);
   if ((e = cudaStreamWaitEvent(user, side->ev[1], 0)) != cudaSuccess) return join(e);
   if (d == 128)
-    bwd_tc_features<128><<<static_cast<unsigned>(fgrid), kMThreads, kFeatSmem, user>>>(b, tmq, tmk, tmdq, tmdk, 0);
+    bwd_tc_features<128><<<static_cast<unsigned>(fgrid), FeatCfg<128>::THREADS, FeatCfg<128>::SMEM, user>>>(
+        b, tmq, tmk, tmdq, tmdk, 0);
   else
-    bwd_tc_features<64><<<static_cast<unsigned>(fgrid), kMThreads, kFeatSmem, user>>>(b, tmq, tmk, tmdq, tmdk, 0);
+    bwd_tc_features<64><<<static_cast<unsigned>(fgrid), FeatCfg<64>::THREADS, FeatCfg<64>::SMEM, user>>>(
+        b, tmq, tmk, tmdq, tmdk, 0);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return join(e);
   if (b.nseg > 1) {
@@ -1434,9 +1443,11 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return join(e);
   if (d == 128)
-    bwd_tc_features<128><<<static_cast<unsigned>(fgrid), kMThreads, kFeatSmem, stream>>>(b, tmq, tmk, tmdq, tmdk, 1);
+    bwd_tc_features<128><<<static_cast<unsigned>(fgrid), FeatCfg<128>::THREADS, FeatCfg<128>::SMEM, stream>>>(
+        b, tmq, tmk, tmdq, tmdk, 1);
   else
-    bwd_tc_features<64><<<static_cast<unsigned>(fgrid), kMThreads, kFeatSmem, stream>>>(b, tmq, tmk, tmdq, tmdk, 1);
+    bwd_tc_features<64><<<static_cast<unsigned>(fgrid), FeatCfg<64>::THREADS, FeatCfg<64>::SMEM, stream>>>(
+        b, tmq, tmk, tmdq, tmdk, 1);
   note_launches(1);
   if ((e = join(cudaGetLastError())) != cudaSuccess) return e;
   BwdArgs g = b;  // the gain partials are per (document, head, chunk)
