@@ -1097,17 +1097,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------------------------------------
 // Before the passes, fully parallel: q' = ReLU(RoPE(RMSNorm(q))) and k' likewise (bf16) of every
 // row into the workspace, where the forward and reverse passes take their q', k' tiles from. One
-// CTA of 256 threads per (document, head, chunk, q or k): the chunk's raw rows arrive in shared
-// memory by TMA; a thread owns 8 consecutive elements of a row (16 threads per row, 16 rows per
-// pass) and works on packed fp32 pairs, with the gains and the RoPE frequencies and per-pass
-// rotation in shared memory.
-constexpr int kMThreads = 256;
+// CTA per (document, head, chunk, q or k), 256 threads (128 at d = 64, so that twice the CTAs,
+// each with half the bytes, keep as many loads in flight per SM): the chunk's raw rows arrive in
+// shared memory by TMA; a thread owns 8 consecutive elements of a row (d / 8 threads per row) and
+// works on packed fp32 pairs, with the gains and the RoPE frequencies and per-pass rotation in
+// shared memory.
+template <int D>
+struct MapCfg {
+  static constexpr int THREADS = D == 64 ? 128 : 256;
+  static constexpr uint32_t SMEM = kC * D * 2 + 1024;  // one tile (+ alignment slack)
+};
 
 template <int D>
-__global__ void __launch_bounds__(kMThreads)
+__global__ void __launch_bounds__(MapCfg<D>::THREADS)
     bwd_tc_featmap(const BwdArgs b, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k) {
-  constexpr int TPR = D / 8, RPP = kMThreads / TPR, NPASS = kC / RPP;
+  constexpr int NT = MapCfg<D>::THREADS;
+  constexpr int TPR = D / 8, RPP = NT / TPR, NPASS = kC / RPP;
   const PrefillArgs& a = b.p;
   const int tid = threadIdx.x;
   const int which = blockIdx.x & 1;  // 0: q, 1: k
@@ -1134,7 +1140,7 @@ __global__ void __launch_bounds__(kMThreads)
     tma_chunk<1, D>(maps, tl, h, static_cast<int>(row0 + t0), bar);
   }
   const feat::FeatTab tab = feat::feat_tab<D>(reinterpret_cast<uint8_t*>(tabmem));
-  feat::fill_tab<D>(tab, a, h, RPP, tid, kMThreads);
+  feat::fill_tab<D>(tab, a, h, RPP, tid, NT);
   __syncthreads();
   const int prow = tid / TPR, part = tid % TPR, e0 = 8 * part;
   const long rstride = static_cast<long>(a.H) * D;
@@ -1385,8 +1391,10 @@ cudaError_t launch_backward_tc(const BwdArgs& b, cudaStream_t stream) {
   CUtensorMap tmq, tmk;
   if ((e = make_rows_map(&tmq, b.p.q, b.p.total_rows, b.p.H, d)) != cudaSuccess) return join(e);
   if ((e = make_rows_map(&tmk, b.p.k, b.p.total_rows, b.p.H, d)) != cudaSuccess) return join(e);
-  if (d == 128) bwd_tc_featmap<128><<<static_cast<unsigned>(2 * fgrid), kMThreads, kTile + 1024, stream>>>(b, tmq, tmk);
-  else bwd_tc_featmap<64><<<static_cast<unsigned>(2 * fgrid), kMThreads, kTile + 1024, stream>>>(b, tmq, tmk);
+  if (d == 128)
+    bwd_tc_featmap<128><<<static_cast<unsigned>(2 * fgrid), MapCfg<128>::THREADS, MapCfg<128>::SMEM, stream>>>(b, tmq, tmk);
+  else
+    bwd_tc_featmap<64><<<static_cast<unsigned>(2 * fgrid), MapCfg<64>::THREADS, MapCfg<64>::SMEM, stream>>>(b, tmq, tmk);
   note_launches(1);
   if ((e = cudaGetLastError()) != cudaSuccess) return join(e);
   if (b.order != nullptr) {  // packed documents: the passes take the longest first
