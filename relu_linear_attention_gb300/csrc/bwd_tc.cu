@@ -47,6 +47,7 @@
 // products overlap the workers' row sums. Every wait is bounded (~1 s); a CTA whose wait gives up
 // sets RAPT_DEV_INTERNAL in the status word and writes NaN results, so a failure cannot pass for one.
 #include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "feature_bwd.cuh"
 #include "kernels.h"
@@ -1320,14 +1321,38 @@ namespace {
 // backward of q runs on the caller's stream meanwhile; with the priorities the passes' CTAs are
 // dispatched first and it fills the SMs they leave idle.
 struct Side {
+  unsigned long long ctx = 0;  // the context the handles belong to (its unique id)
   cudaStream_t hi = nullptr;
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
 };
+// The unique id of the calling thread's current context (0 if it cannot be read): handles made in
+// a context that has since been destroyed (a device reset) are never reused.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  if (get_current == nullptr || get_id == nullptr) {
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 4000, cudaEnableDefault, &q1) != cudaSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || f1 == nullptr || f2 == nullptr)
+      return 0;
+    get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f2);
+    get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f1);
+  }
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&c) != CUDA_SUCCESS || c == nullptr || get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 cudaError_t side_stream(int dev, Side*& out) {
   thread_local Side side[64];
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   Side& sd = side[dev];
-  if (sd.hi == nullptr) {
+  const unsigned long long ctx = current_context_id();
+  if (ctx == 0) return cudaErrorDeviceUninitialized;
+  if (sd.hi == nullptr || sd.ctx != ctx) {  // the handles of a destroyed context are left alone
     int least = 0, greatest = 0;
     Side n;
     cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
@@ -1339,6 +1364,7 @@ cudaError_t side_stream(int dev, Side*& out) {
       if (n.hi != nullptr) cudaStreamDestroy(n.hi);
       return e;
     }
+    n.ctx = ctx;
     sd = n;
   }
   out = &sd;
