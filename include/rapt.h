@@ -33,8 +33,12 @@
  *   - Inputs must be finite. Tiles are read whole, so a non-finite value anywhere in q, k or v
  *     may make any output of the same call non-finite.
  *   - d must be one of 16, 32, 64, 128 (d_v = d_k = d).
- *   - Every call is asynchronous on `stream` (NULL = the legacy default stream), launches only on
- *     that stream, allocates no device memory and never synchronises.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default stream), allocates no
+ *     device memory and never synchronises. Every call but the tensor-core backward launches only
+ *     on `stream`; the backward (bf16, d = 64 or 128) forks part of its work onto a stream of
+ *     greater priority that it makes once per thread and device (with three events; remade after a
+ *     device reset) and joins it back to `stream` before it returns, so work queued on `stream`
+ *     after the call waits for all of it.
  *   - Host-checkable errors are returned before anything is launched and nothing is written:
  *     RAPT_ERR_INVALID_ARG (null required pointer, size <= 0 where > 0 is required, eps not
  *     finite or <= 0, misalignment, `out` aliasing an input), RAPT_ERR_UNSUPPORTED (d or dtype not
@@ -201,9 +205,11 @@ rapt_status rapt_varlen_fwd(const void* q, const void* k, const void* v, rapt_dt
  *   dev_status     (varlen) as for rapt_varlen_fwd: malformed documents are skipped and their
  *                  gradients are not written.
  * The forward has no carried-in state here (S0 = z0 = 0: documents start fresh). The computation
- * is recomputed from q, k, v (no activations of the forward are kept). All arithmetic is fp32 on
- * CUDA cores for every dtype and d; bf16 outputs are rounded to nearest even. Every sum has a
- * fixed order: repeated calls give bitwise-identical results.
+ * is recomputed from q, k, v (no activations of the forward are kept). bf16 at d = 64 or 128 runs
+ * the chunk products on the tensor cores (bf16 operands: q', k', dout, dout / den, the masked
+ * scores and their gradient, the states' bf16 copies; fp32 accumulation, states, denominators and
+ * feature backward); everything else is fp32 on the CUDA cores. bf16 outputs are rounded to
+ * nearest even. Every sum has a fixed order: repeated calls give bitwise-identical results.
  */
 size_t rapt_prefill_bwd_workspace_size(int32_t B, int32_t L, int32_t H, int32_t d, rapt_dtype dtype);
 rapt_status rapt_prefill_bwd(const void* q, const void* k, const void* v, const void* dout,
