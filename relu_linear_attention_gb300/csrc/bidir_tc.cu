@@ -10,13 +10,14 @@
 //      column sums of k' of every block of blk_len tokens (features on 16 producer warps, one GEMM
 //      per 128-token chunk into TMEM), fp32 records in the workspace;
 //   2. readout, one CTA per (document, head, run of 128-token tiles), a programmatic dependent of
-//      launch 1: q tiles arrive by TMA from the start; once launch 1 is complete, twelve warps sum
-//      the document's block records in block order (deterministic) straight into the bf16 B
-//      operand of S in shared memory (the layout the tensor core reads) and z in fp32; eight
-//      feature warps turn each q tile into q' in place, several rows at a time, and form the fp32
-//      q'.z of every row; one thread issues O = Q' S into one of two TMEM accumulators; four
-//      epilogue warps scale O by 1 / (q'.z + eps) and stage whole tiles for a TMA store (the
-//      ragged last tile of a document is written row by row, so no store reaches past it).
+//      launch 1: q tiles arrive by TMA from the start; once launch 1 is complete, the twenty
+//      epilogue and feature warps sum the document's block records in block order (deterministic)
+//      straight into the bf16 B operand of S in shared memory (the layout the tensor core reads)
+//      and z in fp32; sixteen feature warps turn each q tile into q' in place, several rows at a
+//      time, and form the fp32 q'.z of every row; one thread issues O = Q' S into one of two TMEM
+//      accumulators; four epilogue warps scale O by 1 / (q'.z + eps) and stage whole tiles for a
+//      TMA store (the ragged last tile of a document is written row by row, so no store reaches
+//      past it).
 // Every wait is bounded; a readout CTA whose wait gives up writes NaN over its rows and sets
 // RAPT_DEV_INTERNAL.
 #include <cuda.h>
