@@ -240,6 +240,45 @@ def test_prefill_bwd_side_stream_and_graph(cuda_device, lib, d):
         assert torch.equal(a, b)
 
 
+def test_prefill_bwd_from_two_threads(cuda_device, lib):
+    """Two host threads, each on a stream of its own, run the tensor-core backward at once (each
+    thread forks onto a side stream of its own): both give the bits of a call made alone."""
+    import threading
+
+    q, k, v = draw(338, (1, 900, 2, 128), "bf16")
+    (g,) = draw(339, (1, 900, 2, 128), "bf16")[:1]
+    gq, gk = gammas(340, 2, 128, False)
+    dev = lambda x: torch.from_numpy(x).to(cuda_device)
+    args = [to_dev(x, "bf16") for x in (q, k, v, g)] + [dev(gq), dev(gk)]
+    ref = [t.clone() for t in R.rapt_prefill_bwd(*args)]
+    torch.cuda.synchronize()
+    results, errors = [None, None], []
+
+    def work(slot):
+        try:
+            torch.cuda.set_device(cuda_device)
+            stream = torch.cuda.Stream(device=cuda_device)
+            with torch.cuda.stream(stream):
+                outs = None
+                for _ in range(3):
+                    outs = R.rapt_prefill_bwd(*args)
+                stream.synchronize()
+            results[slot] = outs
+        except Exception as e:  # reported on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join(timeout=120)
+    assert not errors, errors
+    for outs in results:
+        assert outs is not None
+        for a, b in zip(ref, outs):
+            assert torch.equal(a, b)
+
+
 def test_prefill_bwd_without_gains_and_empty(cuda_device, lib):
     q, k, v = draw(340, (1, 40, 2, 32), "f32")
     (g,) = draw(341, (1, 40, 2, 32), "f32")[:1]
